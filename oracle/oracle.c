@@ -1,0 +1,515 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU statement of fused PPO
+ * experience collection (actor -> categorical sample -> critic -> portfolio,
+ * triple-barrier, diversity and curiosity reward -> reset on done, then a
+ * backward GAE scan per episode).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header, table or constant with the CUDA
+ * path: it reads the same packed float32 weights and the same seeded inputs
+ * and computes everything again from the definitions below, accumulating in
+ * double.
+ *
+ * Sources (page titles; sections named):
+ *  [P1] "PPO CUDA Pipeline Design -- Zero-Roundtrip Experience Collection":
+ *       "Kernel Phases" (Phase A steps 1-12, Phase B GAE), "Weight Layout",
+ *       "Output Buffers".
+ *  [P2] "GPU Pipeline Phase 2b: Zero-Roundtrip CUDA Experience Collection":
+ *       "Kernel Components" 2 (action category for curiosity / diversity),
+ *       4 (barrier labels -1/0/+1), 5 (Shannon entropy over 3 categories,
+ *       log2, penalty when H < 1.0), 6 (reward = pnl*(1+barrier_scale) +
+ *       diversity + curiosity - risk; barrier_scale +0.5 profit, -0.5 stop),
+ *       8 (LCG s = s*1664525 + 1013904223), and the dense-layer convention
+ *       out[j] = b[j] + sum_i in[i] * W[j*in + i].
+ * The workload specification fixes what the pages leave open: exposure
+ * {-1,-.5,0,.5,1}[a/9], cost (1+(a%9)/3+a%3)*1e-4, barriers +-theta on PnL or
+ * K bars, diversity window 20 and penalty -0.01, curiosity (54+45 one-hot)->
+ * 64->54 with bonus 0.01*MSE, risk 1e-3*|exposure|, uniform (s>>8)*2^-24,
+ * bootstrap V_boot = critic(final pre-reset next state).
+ *
+ * Readings where the pages are silent (each is listed with its reason in the
+ * design notes): state = [F[b,0..50], V, e, spread] with V the portfolio value
+ * since the last reset (reset capital 1), e the exposure held entering the
+ * step and spread the constant tx_base; the price ratio P[b+1]/P[b] is
+ * exp(F[b+1,0]); V' = V*(1-|e'-e|*rate)*(1+e'*(g-1)); the barrier tests
+ * V'-1 against +-theta (price barrier wins over time for the label); the
+ * diversity window covers the actions since the last reset (at most 20,
+ * including the current one); the curiosity target is the full pre-reset next
+ * state; log p is the log-softmax (l_a - m) - ln(sum exp(l - m)); the CDF is
+ * summed in index order and a = min{i : u < cdf_i}, else the last action.
+ *
+ * "Mode Q" (quant = 1 bf16 round-to-nearest-even, quant = 2 tf32
+ * round-to-nearest-ties-away) states what a reduced-precision tensor-core path
+ * computes: every weight matrix element and every layer input is rounded to
+ * the operand format once, products and sums are exact (here: double), biases
+ * and activations stay at full precision.  quant = 0 rounds nothing.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_MAX_W 1024   /* widest layer supported */
+#define ORACLE_MAX_WIN 256  /* longest diversity window supported */
+
+typedef struct {
+    int n_market;        /* market features per bar (51) */
+    int n_actions;       /* actions (45) */
+    int actor_h1;        /* 128 */
+    int actor_h2;        /* 64 */
+    int critic_nh;       /* hidden layers of the critic (5) */
+    int critic_h[8];     /* their widths */
+    int cur_h;           /* curiosity hidden width (64) */
+    int quant;           /* 0 none, 1 bf16 RNE, 2 tf32 RNA */
+    double barrier;      /* theta */
+    int max_hold;        /* K */
+    double pt_scale;     /* barrier_scale on a profit-take hit */
+    double sl_scale;     /* barrier_scale on a stop-loss hit */
+    int div_window;      /* 20 */
+    double div_thresh;   /* 1.0 */
+    double div_penalty;  /* -0.01 */
+    double cur_coef;     /* 0.01 */
+    double risk_coef;    /* 1e-3 */
+    double tx_base;      /* 1e-4 */
+    double spread;       /* portfolio feature 3 (constant) */
+} oracle_cfg;
+
+typedef struct {
+    long action_replays;     /* GPU action adopted: oracle differed inside the band */
+    long done_replays;       /* GPU done adopted: oracle differed inside the band */
+    long action_mismatches;  /* differed outside the band */
+    long done_mismatches;
+    double max_action_gap;   /* largest |u - cdf boundary| among action differences */
+    double max_done_gap;     /* largest |V'-1 -+ theta| among done differences */
+} oracle_stats;
+
+/* ------------------------------------------------------------------ */
+/* LCG ([P2] "Epsilon-Greedy RNG"; uniform from the top 24 state bits)  */
+/* ------------------------------------------------------------------ */
+
+uint32_t oracle_lcg_step(uint32_t s)
+{
+    return (uint32_t)((uint64_t)s * 1664525u + 1013904223u); /* mod 2^32 */
+}
+
+/* advances *s once and returns u = (s >> 8) * 2^-24 in [0, 1) */
+double oracle_lcg_uniform(uint32_t *s)
+{
+    *s = oracle_lcg_step(*s);
+    return (double)(*s >> 8) / 16777216.0;
+}
+
+/* n consecutive uniforms from state seed */
+void oracle_lcg_fill(uint32_t seed, long n, double *out)
+{
+    uint32_t s = seed;
+    for (long i = 0; i < n; ++i) out[i] = oracle_lcg_uniform(&s);
+}
+
+/* ------------------------------------------------------------------ */
+/* operand rounding for mode Q                                          */
+/* ------------------------------------------------------------------ */
+
+static uint32_t f2u(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static float u2f(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+/* IEEE round-to-nearest-even of a float to 8 significant bits (bfloat16). */
+float oracle_round_bf16(float x)
+{
+    uint32_t u = f2u(x);
+    if ((u & 0x7f800000u) == 0x7f800000u) return x;          /* inf / nan */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return u2f(u & 0xffff0000u);
+}
+
+/* round-to-nearest, ties away from zero, to 11 significant bits (tf32). */
+float oracle_round_tf32(float x)
+{
+    uint32_t u = f2u(x);
+    if ((u & 0x7f800000u) == 0x7f800000u) return x;
+    u += 0x1000u;                 /* half an ulp of the 10-bit mantissa */
+    return u2f(u & 0xffffe000u);
+}
+
+static double q_operand(double v, int quant)
+{
+    if (quant == 0) return v;
+    float f = (float)v;
+    return (double)(quant == 1 ? oracle_round_bf16(f) : oracle_round_tf32(f));
+}
+
+/* ------------------------------------------------------------------ */
+/* dense layers ([P2] "Kernel Components" 1, weight layout [out, in])   */
+/* ------------------------------------------------------------------ */
+
+/* out[j] = b[j] + sum_i W[j*n_in + i] * in[i], optional ReLU.
+ * Under mode Q the weights are rounded here and the caller passes an input
+ * vector that has already been rounded. */
+void oracle_dense(const float *W, const float *b, int n_out, int n_in,
+                  const double *in, double *out, int relu, int quant)
+{
+    for (int j = 0; j < n_out; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < n_in; ++i)
+            acc += q_operand((double)W[(long)j * n_in + i], quant) * in[i];
+        acc += (double)b[j];
+        out[j] = (relu && acc < 0.0) ? 0.0 : acc;
+    }
+}
+
+static void q_vector(const double *in, double *out, int n, int quant)
+{
+    for (int i = 0; i < n; ++i) out[i] = q_operand(in[i], quant);
+}
+
+/* offsets into the packed weight buffer ([P1] "Weight Layout" order:
+ * actor, critic, curiosity; each matrix followed by its bias) */
+typedef struct {
+    long a_w[3], a_b[3];
+    long c_w[9], c_b[9];
+    long q_w[2], q_b[2];
+    int a_in[3], a_out[3];
+    int c_in[9], c_out[9];
+    int q_in[2], q_out[2];
+    int n_critic;          /* layers including the scalar head */
+} layout;
+
+static void make_layout(const oracle_cfg *c, layout *lo)
+{
+    long off = 0;
+    int sd = c->n_market + 3;
+    int ain[3] = {sd, c->actor_h1, c->actor_h2};
+    int aout[3] = {c->actor_h1, c->actor_h2, c->n_actions};
+    for (int l = 0; l < 3; ++l) {
+        lo->a_in[l] = ain[l]; lo->a_out[l] = aout[l];
+        lo->a_w[l] = off; off += (long)ain[l] * aout[l];
+        lo->a_b[l] = off; off += aout[l];
+    }
+    int prev = sd;
+    lo->n_critic = c->critic_nh + 1;
+    for (int l = 0; l < lo->n_critic; ++l) {
+        int o = (l < c->critic_nh) ? c->critic_h[l] : 1;
+        lo->c_in[l] = prev; lo->c_out[l] = o;
+        lo->c_w[l] = off; off += (long)prev * o;
+        lo->c_b[l] = off; off += o;
+        prev = o;
+    }
+    int qin[2] = {sd + c->n_actions, c->cur_h};
+    int qout[2] = {c->cur_h, sd};
+    for (int l = 0; l < 2; ++l) {
+        lo->q_in[l] = qin[l]; lo->q_out[l] = qout[l];
+        lo->q_w[l] = off; off += (long)qin[l] * qout[l];
+        lo->q_b[l] = off; off += qout[l];
+    }
+}
+
+long oracle_weight_count(const oracle_cfg *c)
+{
+    layout lo;
+    make_layout(c, &lo);
+    return lo.q_b[1] + lo.q_out[1];
+}
+
+/* [P1] Phase A step 3: state[54] -> h1[128] ReLU -> h2[64] ReLU -> logits[45] */
+void oracle_actor(const float *w, const oracle_cfg *c, const double *x, double *logits)
+{
+    layout lo;
+    double in[ORACLE_MAX_W], out[ORACLE_MAX_W];
+    make_layout(c, &lo);
+    q_vector(x, in, lo.a_in[0], c->quant);
+    for (int l = 0; l < 3; ++l) {
+        int last = (l == 2);
+        oracle_dense(w + lo.a_w[l], w + lo.a_b[l], lo.a_out[l], lo.a_in[l], in,
+                     last ? logits : out, !last, c->quant);
+        if (!last) q_vector(out, in, lo.a_out[l], c->quant);
+    }
+}
+
+/* [P1] Phase A step 5: state[54] -> 512 -> 384 -> 256 -> 128 -> 64 (ReLU) -> 1 */
+double oracle_critic(const float *w, const oracle_cfg *c, const double *x)
+{
+    layout lo;
+    double in[ORACLE_MAX_W], out[ORACLE_MAX_W];
+    make_layout(c, &lo);
+    q_vector(x, in, lo.c_in[0], c->quant);
+    for (int l = 0; l < lo.n_critic; ++l) {
+        int last = (l == lo.n_critic - 1);
+        oracle_dense(w + lo.c_w[l], w + lo.c_b[l], lo.c_out[l], lo.c_in[l], in, out,
+                     !last, c->quant);
+        if (last) return out[0];
+        q_vector(out, in, lo.c_out[l], c->quant);
+    }
+    return 0.0;
+}
+
+/* [P1] Phase A step 9 / [P2] "Curiosity Forward Model": forward-dynamics
+ * prediction from [state ; one-hot(action)] -> cur_h ReLU -> next state. */
+void oracle_curiosity(const float *w, const oracle_cfg *c, const double *x, int a, double *pred)
+{
+    layout lo;
+    double in[ORACLE_MAX_W], hid[ORACLE_MAX_W];
+    make_layout(c, &lo);
+    int sd = c->n_market + 3;
+    q_vector(x, in, sd, c->quant);
+    for (int i = 0; i < c->n_actions; ++i) in[sd + i] = (i == a) ? 1.0 : 0.0;
+    oracle_dense(w + lo.q_w[0], w + lo.q_b[0], lo.q_out[0], lo.q_in[0], in, hid, 1, c->quant);
+    q_vector(hid, in, lo.q_out[0], c->quant);
+    oracle_dense(w + lo.q_w[1], w + lo.q_b[1], lo.q_out[1], lo.q_in[1], in, pred, 0, c->quant);
+}
+
+/* [P1] Phase A step 4: stable softmax, CDF summed in index order, inverse-CDF
+ * draw with uniform u.  Returns the action; writes log p[action] and the CDF. */
+int oracle_sample(const double *logits, int n, double u, double *logp, double *cdf)
+{
+    double m = logits[0];
+    for (int i = 1; i < n; ++i) if (logits[i] > m) m = logits[i];
+    double q[ORACLE_MAX_W], s = 0.0;
+    for (int i = 0; i < n; ++i) { q[i] = exp(logits[i] - m); s += q[i]; }
+    double run = 0.0;
+    int a = -1;
+    for (int i = 0; i < n; ++i) {
+        run += q[i] / s;
+        cdf[i] = run;
+        if (a < 0 && u < run) a = i;
+    }
+    if (a < 0) a = n - 1;
+    *logp = (logits[a] - m) - log(s);
+    return a;
+}
+
+/* log p[a] for a given action (used when the GPU's action is adopted). */
+static double log_prob(const double *logits, int n, int a)
+{
+    double m = logits[0];
+    for (int i = 1; i < n; ++i) if (logits[i] > m) m = logits[i];
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += exp(logits[i] - m);
+    return (logits[a] - m) - log(s);
+}
+
+/* ------------------------------------------------------------------ */
+/* environment ([P1] steps 6-10, [P2] components 3-6)                   */
+/* ------------------------------------------------------------------ */
+
+double oracle_exposure(int a) { return 0.5 * (double)(a / 9 - 2); } /* {-1,-.5,0,.5,1} */
+
+double oracle_tx_rate(int a, double base) { return (double)(1 + (a % 9) / 3 + a % 3) * base; }
+
+/* [P2] component 2: Short (exposure index 0,1) / Flat (2) / Long (3,4) */
+int oracle_category(int a)
+{
+    int x = a / 9;
+    return (x <= 1) ? 0 : (x == 2) ? 1 : 2;
+}
+
+/* [P2] component 5: Shannon entropy (bits) of the category histogram */
+double oracle_window_entropy(const int *cats, int n)
+{
+    if (n <= 0) return 0.0;
+    int cnt[3] = {0, 0, 0};
+    for (int i = 0; i < n; ++i) cnt[cats[i]]++;
+    double h = 0.0;
+    for (int k = 0; k < 3; ++k) {
+        if (cnt[k] == 0) continue;
+        double p = (double)cnt[k] / (double)n;
+        h -= p * log2(p);
+    }
+    return h;
+}
+
+/* [P1] Phase B: backward GAE over one episode.  v_boot is V(next) of the last
+ * step; (1 - d) masks the bootstrap and the recursion at episode ends. */
+void oracle_gae(const double *r, const double *v, const int32_t *d, int L, double v_boot,
+                double gamma, double lambda, double *adv, double *ret)
+{
+    double next_adv = 0.0;
+    for (int t = L - 1; t >= 0; --t) {
+        double v_next = (t == L - 1) ? v_boot : v[t + 1];
+        double nd = d[t] ? 0.0 : 1.0;
+        double delta = r[t] + gamma * v_next * nd - v[t];
+        adv[t] = delta + gamma * lambda * nd * next_adv;
+        next_adv = adv[t];
+        ret[t] = adv[t] + v[t];
+    }
+}
+
+/* float entry point for the GAE pins */
+void oracle_gae_f32(const float *r, const float *v, const int32_t *d, int L, double v_boot,
+                    double gamma, double lambda, double *adv, double *ret)
+{
+    double *rr = malloc(sizeof(double) * (size_t)L), *vv = malloc(sizeof(double) * (size_t)L);
+    for (int t = 0; t < L; ++t) { rr[t] = r[t]; vv[t] = v[t]; }
+    oracle_gae(rr, vv, d, L, v_boot, gamma, lambda, adv, ret);
+    free(rr); free(vv);
+}
+
+/* ------------------------------------------------------------------ */
+/* one episode                                                          */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Runs episode n from bar `start` with LCG state `seed` for L steps.
+ * features: [n_bars, n_market] float32 row-major.
+ * gpu_a / gpu_d (length L, may be NULL): decisions of the path under test.
+ *   Where the oracle's own action (done) differs from it and the uniform lies
+ *   within act_band of the CDF boundary that separates them (|V'-1 -+ theta|
+ *   < done_band), the oracle adopts it and counts a replay.  A difference
+ *   outside the band is counted as a mismatch and also adopted, so that the
+ *   rest of the episode can still be compared.
+ * Outputs (each of length L, or L*state_dim for states) may be NULL.
+ * Returns 0, or -1 on an invalid argument.
+ */
+int oracle_episode(const float *w, const oracle_cfg *c, const float *features, long n_bars,
+                   int start, uint32_t seed, int L, double gamma, double lambda,
+                   const int32_t *gpu_a, const int32_t *gpu_d, double act_band, double done_band,
+                   float *o_states, int32_t *o_a, float *o_logp, float *o_v, float *o_r,
+                   int32_t *o_d, float *o_adv, float *o_ret, double *o_vboot, oracle_stats *st)
+{
+    const int nm = c->n_market, sd = nm + 3, na = c->n_actions;
+    if (L <= 0 || start < 0 || (long)start + L > n_bars - 1 || na > ORACLE_MAX_W ||
+        c->div_window > ORACLE_MAX_WIN || c->div_window <= 0)
+        return -1;
+
+    double *r = malloc(sizeof(double) * (size_t)L), *v = malloc(sizeof(double) * (size_t)L);
+    int32_t *d = malloc(sizeof(int32_t) * (size_t)L);
+    double x[ORACLE_MAX_W], xn[ORACLE_MAX_W], logits[ORACLE_MAX_W], cdf[ORACLE_MAX_W];
+    double pred[ORACLE_MAX_W];
+    int win[ORACLE_MAX_WIN];
+    int nwin = 0, k = 0;
+    double V = 1.0, e = 0.0;
+    uint32_t s = seed;
+
+    for (int t = 0; t < L; ++t) {
+        long b = (long)start + t;
+        /* steps 1-2: market features and portfolio features */
+        for (int j = 0; j < nm; ++j) x[j] = (double)features[b * nm + j];
+        x[nm] = V; x[nm + 1] = e; x[nm + 2] = c->spread;
+
+        /* steps 3-4: actor, softmax, CDF draw */
+        oracle_actor(w, c, x, logits);
+        double u = oracle_lcg_uniform(&s);
+        double logp;
+        int a = oracle_sample(logits, na, u, &logp, cdf);
+        if (gpu_a && gpu_a[t] != a) {
+            int g = gpu_a[t];
+            double gap;
+            if (g < 0 || g >= na) gap = INFINITY;
+            else if (g < a) gap = u - cdf[g];          /* GPU saw u below cdf[g] */
+            else gap = cdf[g - 1] - u;                 /* GPU saw u at/above cdf[g-1] */
+            if (gap < act_band) st->action_replays++;
+            else {
+                st->action_mismatches++;
+                if (gap > st->max_action_gap) st->max_action_gap = gap;
+            }
+            if (g >= 0 && g < na) { a = g; logp = log_prob(logits, na, a); }
+        }
+
+        /* step 5: critic */
+        double val = oracle_critic(w, c, x);
+
+        /* step 6: portfolio */
+        double e2 = oracle_exposure(a);
+        double rate = oracle_tx_rate(a, c->tx_base);
+        double g = exp((double)features[(b + 1) * nm + 0]);
+        double V2 = V * (1.0 - fabs(e2 - e) * rate) * (1.0 + e2 * (g - 1.0));
+        double pnl = V2 / V - 1.0;
+
+        /* step 7: triple barrier */
+        k += 1;
+        double cpl = V2 - 1.0;
+        int label = (cpl >= c->barrier) ? 1 : (cpl <= -c->barrier) ? -1 : 0;
+        int done = (label != 0) || (k >= c->max_hold);
+        if (gpu_d && (gpu_d[t] != 0) != done) {
+            double gap = fmin(fabs(cpl - c->barrier), fabs(cpl + c->barrier));
+            if (gap < done_band) st->done_replays++;
+            else {
+                st->done_mismatches++;
+                if (gap > st->max_done_gap) st->max_done_gap = gap;
+            }
+            done = gpu_d[t] != 0;
+            if (!done) label = 0;
+            else if (k < c->max_hold || label == 0)
+                label = (fabs(cpl - c->barrier) <= fabs(cpl + c->barrier)) ? 1 : -1;
+        }
+
+        /* step 8: diversity over the actions since reset (window of div_window) */
+        if (nwin == c->div_window) {
+            memmove(win, win + 1, sizeof(int) * (size_t)(nwin - 1));
+            nwin--;
+        }
+        win[nwin++] = oracle_category(a);
+        double H = oracle_window_entropy(win, nwin);
+        double div = (H < c->div_thresh) ? c->div_penalty : 0.0;
+
+        /* step 9: curiosity against the pre-reset next state */
+        for (int j = 0; j < nm; ++j) xn[j] = (double)features[(b + 1) * nm + j];
+        xn[nm] = V2; xn[nm + 1] = e2; xn[nm + 2] = c->spread;
+        oracle_curiosity(w, c, x, a, pred);
+        double mse = 0.0;
+        for (int j = 0; j < sd; ++j) mse += (pred[j] - xn[j]) * (pred[j] - xn[j]);
+        mse /= (double)sd;
+        double cur = c->cur_coef * mse;
+
+        /* step 10: reward */
+        double risk = c->risk_coef * fabs(e2);
+        double beta = (label > 0) ? c->pt_scale : (label < 0) ? c->sl_scale : 0.0;
+        double rew = pnl * (1.0 + beta) + div + cur - risk;
+
+        /* step 11: store */
+        if (o_states) for (int j = 0; j < sd; ++j) o_states[(long)t * sd + j] = (float)x[j];
+        if (o_a) o_a[t] = a;
+        if (o_logp) o_logp[t] = (float)logp;
+        if (o_v) o_v[t] = (float)val;
+        if (o_r) o_r[t] = (float)rew;
+        if (o_d) o_d[t] = done;
+        r[t] = rew; v[t] = val; d[t] = done;
+
+        /* step 12: reset on done (LCG is not reseeded, the bar keeps advancing) */
+        if (done) { V = 1.0; e = 0.0; k = 0; nwin = 0; }
+        else { V = V2; e = e2; }
+    }
+
+    /* bootstrap: critic of the final pre-reset next state */
+    double vboot = oracle_critic(w, c, xn);
+    if (o_vboot) *o_vboot = vboot;
+
+    double *adv = malloc(sizeof(double) * (size_t)L), *ret = malloc(sizeof(double) * (size_t)L);
+    oracle_gae(r, v, d, L, vboot, gamma, lambda, adv, ret);
+    for (int t = 0; t < L; ++t) {
+        if (o_adv) o_adv[t] = (float)adv[t];
+        if (o_ret) o_ret[t] = (float)ret[t];
+    }
+    free(adv); free(ret); free(r); free(v); free(d);
+    return 0;
+}
+
+/*
+ * Runs episodes idx[0..n_sel-1] of a batch.  Per-episode outputs are written
+ * at row i of the [n_sel, L(, state_dim)] output arrays.  gpu_a / gpu_d, when
+ * given, are the path-under-test's full [N, L] arrays.
+ */
+int oracle_rollout(const float *w, const oracle_cfg *c, const float *features, long n_bars,
+                   const int32_t *starts, const uint32_t *seeds, const int32_t *idx, int n_sel,
+                   int L, double gamma, double lambda,
+                   const int32_t *gpu_a, const int32_t *gpu_d, double act_band, double done_band,
+                   float *o_states, int32_t *o_a, float *o_logp, float *o_v, float *o_r,
+                   int32_t *o_d, float *o_adv, float *o_ret, double *o_vboot, oracle_stats *st)
+{
+    const int sd = c->n_market + 3;
+    for (int i = 0; i < n_sel; ++i) {
+        long n = idx[i];
+        long row = (long)i * L;
+        int rc = oracle_episode(w, c, features, n_bars, starts[n], seeds[n], L, gamma, lambda,
+                                gpu_a ? gpu_a + n * L : NULL, gpu_d ? gpu_d + n * L : NULL,
+                                act_band, done_band,
+                                o_states ? o_states + row * sd : NULL,
+                                o_a ? o_a + row : NULL, o_logp ? o_logp + row : NULL,
+                                o_v ? o_v + row : NULL, o_r ? o_r + row : NULL,
+                                o_d ? o_d + row : NULL, o_adv ? o_adv + row : NULL,
+                                o_ret ? o_ret + row : NULL, o_vboot ? o_vboot + i : NULL, st);
+        if (rc) return rc;
+    }
+    return 0;
+}

@@ -1,0 +1,171 @@
+"""Seeded synthetic workloads for fused PPO experience collection.
+
+This module only *generates inputs*: market-feature matrices, episode start
+bars, per-episode LCG seeds and initial network weights.  It holds none of the
+method's arithmetic (no network, sampler, environment or GAE step), so both the
+CUDA path and the CPU oracle can consume the same bytes without sharing code.
+
+Sources for the shapes and distributions ("PPO CUDA Pipeline Design —
+Zero-Roundtrip Experience Collection", sections "Kernel Phases" and "Weight
+Layout"; the DQN phase-2b page, section "Memory Budget" for the 51 market
+features per bar):
+
+* market features ``F[B, 51]`` float32, i.i.d. N(0, 1); column 0 is replaced by
+  the bar's log-return ~ N(0, sigma) so that the close price is
+  ``P[b] = 100 * exp(cumsum(F[:, 0]))[b]`` and ``P[b+1] / P[b] = exp(F[b+1, 0])``;
+* episode starts uniform in ``[0, B - L)`` (overlaps allowed);
+* LCG seeds ``seeds[n] = low32(splitmix64(seed * 2**32 + n))`` (SplitMix64 of
+  Steele, Lea & Flood 2014 used as the named ``hash(seed, episode)``);
+* every weight matrix ``[out, in]`` row-major, He/Kaiming-uniform
+  ``U(-sqrt(6/fan_in), +sqrt(6/fan_in))``, every bias zero.
+
+Draw order from ``numpy.random.default_rng(seed)``: features, then column 0,
+then starts, then the weights in packing order (actor, critic, curiosity).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, List, Tuple
+
+import numpy as np
+
+N_MARKET = 51          # market features per bar
+STATE_DIM = 54         # 51 market + 3 portfolio features
+N_ACTIONS = 45         # 5 exposures x 3 order types x 3 urgencies
+ACTOR_H = (128, 64)
+CRITIC_STD = (512, 384, 256, 128, 64)
+CRITIC_WIDE = (1024, 768, 512, 256, 128)
+CUR_H = 64             # curiosity forward model: (54 + 45 one-hot) -> 64 -> 54
+
+DTYPES = ("fp32", "tf32", "bf16")
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One experience-collection problem: sizes, precision, env constants."""
+    name: str
+    n_episodes: int            # N
+    horizon: int               # L (timesteps per episode)
+    n_bars: int                # B (rows of the feature matrix)
+    dtype: str                 # "fp32" | "tf32" | "bf16"
+    seed: int
+    sigma: float               # std of the log-return column
+    barrier: float             # +-theta on portfolio PnL since reset
+    max_hold: int              # K: time barrier in bars
+    gamma: float
+    lam: float
+    critic_h: Tuple[int, ...] = CRITIC_STD
+    # reward / env constants (identical for every workload)
+    pt_scale: float = 0.5      # barrier_scale on a profit-take hit
+    sl_scale: float = -0.5     # barrier_scale on a stop-loss hit
+    div_window: int = 20
+    div_thresh: float = 1.0
+    div_penalty: float = -0.01
+    cur_coef: float = 0.01
+    risk_coef: float = 1e-3
+    tx_base: float = 1e-4
+    spread: float = 1e-4
+
+    @property
+    def tuples(self) -> int:
+        return self.n_episodes * self.horizon
+
+
+WORKLOADS: Dict[str, Workload] = {
+    # 32 x 200, fp32, 20000 bars, seed 0.
+    "tiny_fp32": Workload("tiny_fp32", 32, 200, 20000, "fp32", 0, 1e-3, 0.02, 50, 0.99, 0.95),
+    # the pages' default launch: 128 episodes x 500 steps = 64,000 tuples.
+    "default_fp32": Workload("default_fp32", 128, 500, 50000, "fp32", 0, 1e-3, 0.02, 50, 0.99, 0.95),
+    # 4096 x 500, tf32 tensor-core MLPs, 100000 bars, seed 1.
+    "scaleout_tf32": Workload("scaleout_tf32", 4096, 500, 100000, "tf32", 1, 1e-3, 0.02, 50, 0.99, 0.95),
+    # 16384 x 1000, bf16, tight barriers (+-0.2 %, 10 bars), sigma 5e-3, seed 2.
+    "reset_heavy_bf16": Workload("reset_heavy_bf16", 16384, 1000, 200000, "bf16", 2, 5e-3, 0.002, 10, 0.99, 0.95),
+    # 65536 x 256, bf16, widened critic, gamma .995 lambda .97, seed 3.
+    "ceiling_bf16": Workload("ceiling_bf16", 65536, 256, 200000, "bf16", 3, 1e-3, 0.02, 50, 0.995, 0.97,
+                             critic_h=CRITIC_WIDE),
+}
+WORKLOAD_ORDER = ["tiny_fp32", "default_fp32", "scaleout_tf32", "reset_heavy_bf16", "ceiling_bf16"]
+
+
+def layer_shapes(critic_h: Tuple[int, ...] = CRITIC_STD) -> List[Tuple[str, Tuple[int, int]]]:
+    """Weight matrices ``(name, (out, in))`` in packing order.
+
+    Packing order is actor W1,b1,W2,b2,W3,b3; critic V1,c1 ... V6,c6; curiosity
+    C1,d1,C2,d2.  Each matrix is followed by its bias of length ``out``.
+    """
+    shapes = [("actor0", (ACTOR_H[0], STATE_DIM)), ("actor1", (ACTOR_H[1], ACTOR_H[0])),
+              ("actor2", (N_ACTIONS, ACTOR_H[1]))]
+    prev = STATE_DIM
+    for i, h in enumerate(critic_h):
+        shapes.append((f"critic{i}", (h, prev)))
+        prev = h
+    shapes.append((f"critic{len(critic_h)}", (1, prev)))
+    shapes.append(("cur0", (CUR_H, STATE_DIM + N_ACTIONS)))
+    shapes.append(("cur1", (STATE_DIM, CUR_H)))
+    return shapes
+
+
+def n_params(critic_h: Tuple[int, ...] = CRITIC_STD) -> int:
+    return sum(o * i + o for _, (o, i) in layer_shapes(critic_h))
+
+
+def splitmix64(x: int) -> int:
+    """SplitMix64 output for state ``x`` (Steele, Lea & Flood, OOPSLA 2014)."""
+    m = (1 << 64) - 1
+    z = (x + 0x9E3779B97F4A7C15) & m
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & m
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & m
+    return z ^ (z >> 31)
+
+
+def episode_seeds(seed: int, n: int) -> np.ndarray:
+    """``seeds[i] = low32(splitmix64(seed * 2**32 + i))`` as uint32."""
+    base = (seed & 0xFFFFFFFF) << 32
+    return np.array([splitmix64(base + i) & 0xFFFFFFFF for i in range(n)], dtype=np.uint32)
+
+
+def init_weights(rng: np.random.Generator, critic_h: Tuple[int, ...]) -> np.ndarray:
+    """Packed float32 buffer of every layer in packing order (He-uniform, zero bias)."""
+    parts = []
+    for _, (o, i) in layer_shapes(critic_h):
+        bound = math.sqrt(6.0 / i)
+        parts.append(rng.uniform(-bound, bound, size=(o, i)).astype(np.float32).ravel())
+        parts.append(np.zeros(o, dtype=np.float32))
+    return np.concatenate(parts)
+
+
+@dataclasses.dataclass
+class Inputs:
+    features: np.ndarray       # [B, 51] float32
+    starts: np.ndarray         # [N] int32
+    seeds: np.ndarray          # [N] uint32
+    weights: np.ndarray        # packed float32
+
+
+def generate(w: Workload, n_episodes: int | None = None, horizon: int | None = None) -> Inputs:
+    """Seeded synthetic inputs for workload ``w``.
+
+    ``n_episodes``/``horizon`` override N and L (starts are then drawn for the
+    overridden sizes); everything else follows the workload's recipe.
+    """
+    n = w.n_episodes if n_episodes is None else n_episodes
+    L = w.horizon if horizon is None else horizon
+    rng = np.random.default_rng(w.seed)
+    feats = rng.standard_normal((w.n_bars, N_MARKET)).astype(np.float32)
+    feats[:, 0] = rng.normal(0.0, w.sigma, size=w.n_bars).astype(np.float32)
+    starts = rng.integers(0, w.n_bars - L, size=n).astype(np.int32)
+    weights = init_weights(rng, w.critic_h)
+    return Inputs(np.ascontiguousarray(feats), starts, episode_seeds(w.seed, n), weights)
+
+
+def weight_views(weights: np.ndarray, critic_h: Tuple[int, ...] = CRITIC_STD) -> Dict[str, np.ndarray]:
+    """Named ``[out, in]`` matrix and bias views into a packed buffer."""
+    out, off = {}, 0
+    for name, (o, i) in layer_shapes(critic_h):
+        out[name + ".w"] = weights[off:off + o * i].reshape(o, i)
+        off += o * i
+        out[name + ".b"] = weights[off:off + o]
+        off += o
+    assert off == weights.size, (off, weights.size)
+    return out
