@@ -1,0 +1,304 @@
+"""Benchmark: fused PPO experience collection on GB300.
+
+Default workload: 16384 episodes x 1000 steps, bf16 tensor-core MLPs, 200000
+bars x 51 features (the reset-heavy configuration: barriers +-0.2 % / 10 bars,
+log-return sigma 5e-3, seed 2).  One step = one rollout_run: rollout
+(actor + sample + environment), value (critic + curiosity) and GAE over the
+whole batch.  Inputs are resident in HBM; L2 is flushed between timed steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rl_experience_collection_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "experience tuples/sec incl. GAE at 1 GB300; tensor-pipe % of peak"
+DEFAULT_WORKLOAD = "reset_heavy_bf16"
+ACTOR_FLOP = 2 * (54 * 128 + 128 * 64 + 64 * 45)
+CUR_FLOP = 2 * (54 * 64 + 64 * 54)
+
+
+def critic_flop(h):
+    dims = (54,) + tuple(h) + (1,)
+    return 2 * sum(a * b for a, b in zip(dims[:-1], dims[1:]))
+
+
+def path_flops(w: wl.Workload, N: int, L: int):
+    """Algorithmic FLOPs of one step (multiply-add = 2): whole path and the value kernel."""
+    c = critic_flop(w.critic_h)
+    value = N * L * (c + CUR_FLOP) + N * c          # + one bootstrap critic pass per episode
+    return N * L * ACTOR_FLOP + value, value
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16": d["bf16_tflops"], "bf16_sustained": d.get("bf16_tflops_sustained"),
+                "hbm": d["hbm_gbs"], "src": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "src": "fallback"}
+
+
+def tensor_peak(dtype: str, pk):
+    # tf32 dense rate is half of bf16's (nominal ratio); fp32 runs on CUDA cores
+    if dtype == "bf16":
+        return pk["bf16"], "bf16"
+    if dtype == "tf32":
+        return pk["bf16"] / 2.0, "tf32 (= measured bf16 x nominal 1/2)"
+    return None, "fp32 CUDA cores"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.count(",") >= 7]
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[0]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[4 + i]})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[2]) for r in rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+    dist.init_process_group("nccl")
+    return dist.get_rank(), ws, dist
+
+
+def max_over_ranks(x: float, dist, device):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_oracle_sample(w: wl.Workload, inputs, n_eps: int, first: int = 0):
+    from oracle import oracle as orc
+    idx = list(range(first, first + n_eps))
+    t0 = time.perf_counter()
+    orc.rollout(w, inputs, idx, quant=w.dtype, threads=1)
+    return time.perf_counter() - t0, n_eps * w.horizon
+
+
+def reference_arm(args, w: wl.Workload, rank: int):
+    if rank != 0:
+        return
+    inputs = wl.generate(w)
+    n_eps = max(1, int(args.ref_episodes))
+    for i in range(args.warmup):
+        run_oracle_sample(w, inputs, n_eps, first=i * n_eps % w.n_episodes)
+    times, tuples = [], 0
+    for i in range(args.steps):
+        dt, n = run_oracle_sample(w, inputs, n_eps, first=(args.warmup + i) * n_eps % w.n_episodes)
+        times.append(dt)
+        tuples += n
+    v = tuples / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tuples/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sum(times) / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "episodes": w.n_episodes, "horizon": w.horizon, "n_bars": w.n_bars,
+                       "mlp_dtype": w.dtype, "sample_episodes_per_step": n_eps},
+            "cpu_baseline": {"value": v, "unit": "tuples/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n_eps} episodes x {w.horizon} steps per step"},
+            "e2e": {"value": v, "unit": "tuples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS))
+    ap.add_argument("--ref-episodes", type=int, default=2, help="oracle episodes per reference step")
+    ap.add_argument("--cpu-episodes", type=int, default=12, help="oracle episodes for cpu_baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = wl.WORKLOADS[args.workload]
+
+    rank, world, dist = dist_setup()
+    if args.impl == "reference":
+        reference_arm(args, w, rank)
+        if dist is not None:
+            dist.barrier()
+        return
+
+    import torch
+    from rl_experience_collection_gb300 import binding, build
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    N, L = w.n_episodes, w.horizon
+    inputs = wl.generate(w)
+    h = binding.Rollout.for_workload(w, inputs.weights)
+    feats = torch.from_numpy(inputs.features).to(dev)
+    starts = torch.from_numpy(inputs.starts).to(dev)
+    seeds = torch.from_numpy(inputs.seeds.view(np.int32)).to(dev)
+    out = binding.make_outputs(N, L, dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 512 MB > L2
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        h.run(feats, starts, seeds, N, L, w.gamma, w.lam, out, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = h.status()
+    if st != binding.ROLLOUT_OK:
+        raise SystemExit(f"device status {st} after warm-up")
+
+    # ---------------- device-resident timing (per step, L2 flushed between steps)
+    h.set_timing(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    phase = []
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+            phase.append(h.phase_ms())
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    h.set_timing(False)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
+    st = h.status()
+    if st != binding.ROLLOUT_OK:
+        raise SystemExit(f"device status {st} after the timed steps")
+    ms = total_ms / args.steps
+    tuples = N * L * world
+    value = tuples * args.steps / (total_ms / 1000.0)
+
+    pk = peaks()
+    flop_step, flop_value = path_flops(w, N, L)
+    tpk, tpk_name = tensor_peak(w.dtype, pk)
+    value_ms = statistics.mean(p[1] for p in phase)
+    rollout_ms = statistics.mean(p[0] for p in phase)
+    gae_ms = statistics.mean(p[2] for p in phase)
+    achieved = flop_value / (value_ms / 1000.0) / 1e12
+    roofline = {"kernel": "value (critic + curiosity, tcgen05)", "bound": "tensor", "achieved": achieved,
+                "peak": tpk, "unit": "TFLOP/s", "frac": (achieved / tpk) if tpk else None, "traffic": None,
+                "peak_kind": f"{tpk_name}, burst, {pk['src']}",
+                "algorithmic_flop_per_launch": flop_value}
+    line = {"metric": METRIC, "value": value, "unit": "tuples/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "episodes": N, "horizon": L, "n_bars": w.n_bars,
+                       "critic": list(w.critic_h), "l2": "flushed between steps (512 MB write)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "tensor_pipe_frac_step": (flop_step / (ms / 1000.0) / 1e12 / tpk) if tpk else None,
+            "phase_ms": {"rollout": rollout_ms, "value": value_ms, "gae": gae_ms},
+            "roofline": roofline, "clocks": clk.summary(), "gpu_launches": 3 * args.steps}
+
+    # ---------------- end to end through the C ABI with host buffers
+    if not args.no_e2e:
+        hf = torch.from_numpy(inputs.features).pin_memory()
+        hs = torch.from_numpy(inputs.starts).pin_memory()
+        hd = torch.from_numpy(inputs.seeds.view(np.int32)).pin_memory()
+        keep = ("states", "actions", "logp", "adv", "ret", "dones", "rewards")
+        hout = {k: torch.empty(out[k].shape, dtype=out[k].dtype, pin_memory=True) for k in keep}
+        h2d = hf.numel() * 4 + hs.numel() * 4 + hd.numel() * 4
+        d2h = sum(t.numel() * 4 for t in hout.values())
+        e2e_ms = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(float(i))
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            feats.copy_(hf, non_blocking=True)
+            starts.copy_(hs, non_blocking=True)
+            seeds.copy_(hd, non_blocking=True)
+            step()
+            for k in keep:
+                hout[k].copy_(out[k], non_blocking=True)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(1000 * (time.perf_counter() - t0))
+        e2e_total = max_over_ranks(sum(e2e_ms), dist, dev)
+        line["e2e"] = {"value": tuples * args.steps / (e2e_total / 1000.0), "unit": "tuples/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---------------- CPU oracle baseline (rank 0, N=1 only)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        dt, n = run_oracle_sample(w, inputs, args.cpu_episodes)
+        line["cpu_baseline"] = {"value": n / dt, "unit": "tuples/s", "cores": 1, "kind": "oracle",
+                                "sample": f"first {args.cpu_episodes} episodes x {L} steps of {w.name}, "
+                                          f"{w.dtype} operand rounding, single thread, {dt:.1f} s"}
+    h.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

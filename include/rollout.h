@@ -1,0 +1,179 @@
+/*
+ * rollout.h -- C ABI of the GB300 (sm_103a) fused PPO experience collector.
+ *
+ * One call of rollout_run() collects N x L experience tuples with no host
+ * round trip: N independent episodes each step through L bars.  Per step an
+ * episode reads the 51 market features of its bar, appends 3 portfolio
+ * features, runs the actor MLP 54->128->64->45 (ReLU), samples an action from
+ * the softmax with a per-episode LCG uniform, runs the critic MLP
+ * 54->512->384->256->128->64->1 (ReLU), and takes the portfolio,
+ * triple-barrier, diversity-entropy and curiosity reward step, resetting the
+ * episode on done.  A backward GAE scan per episode then produces advantages
+ * and returns.
+ *
+ * Defining passages (page "PPO CUDA Pipeline Design -- Zero-Roundtrip
+ * Experience Collection"): section "Kernel Phases", Phase A steps 1-12 (the
+ * per-step body) and Phase B (GAE); section "Weight Layout" (tensor shapes and
+ * the [out, in] row-major convention); section "Output Buffers" (outputs).
+ * The environment functions it reuses are those of page "GPU Pipeline Phase
+ * 2b: Zero-Roundtrip CUDA Experience Collection", section "Kernel Components".
+ *
+ * All entry points are thread-compatible, not thread-safe: calls that use the
+ * same handle must not run concurrently (one stream, or external ordering).
+ */
+#ifndef ROLLOUT_H
+#define ROLLOUT_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ROLLOUT_API __attribute__((visibility("default")))
+#else
+#define ROLLOUT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes (every entry point returns one of these, 0 = success) */
+#define ROLLOUT_OK               0
+#define ROLLOUT_ERR_INVALID     -1  /* null pointer, bad size, gamma/lambda outside [0,1] */
+#define ROLLOUT_ERR_RANGE       -2  /* an episode start outside [0, n_bars - L - 1] (device-detected) */
+#define ROLLOUT_ERR_CUDA        -3  /* a CUDA runtime call failed; see rollout_last_error() */
+#define ROLLOUT_ERR_TIMEOUT     -4  /* a bounded device-side wait expired (device-detected) */
+#define ROLLOUT_ERR_UNSUPPORTED -5  /* network shape / dtype / constant this build does not handle */
+#define ROLLOUT_ERR_NOMEM       -6  /* device allocation failed */
+
+/* arithmetic of the MLPs (the environment, sampler and GAE are float32 throughout) */
+#define ROLLOUT_FP32 0   /* float32 CUDA-core FMA */
+#define ROLLOUT_TF32 1   /* tcgen05 kind::tf32 tensor cores, operands rounded to tf32 (ties away), f32 accumulate */
+#define ROLLOUT_BF16 2   /* tcgen05 kind::f16 tensor cores, operands rounded to bf16 (nearest even), f32 accumulate */
+
+/*
+ * Network shapes, precision and environment constants, fixed at create time.
+ * Supported shapes: n_market 51, n_actions 45, actor 128/64, curiosity 64,
+ * critic hidden widths {512,384,256,128,64} or {1024,768,512,256,128}
+ * (critic_nh = 5).  div_window in [1, 31].
+ */
+typedef struct {
+    int   n_market;      /* market features per bar (51); state width is n_market + 3 */
+    int   n_actions;     /* 45 = 5 exposures x 3 order types x 3 urgencies */
+    int   actor_h1;      /* 128 */
+    int   actor_h2;      /* 64 */
+    int   critic_nh;     /* number of hidden critic layers (5) */
+    int   critic_h[8];   /* their widths; the head is width 1 */
+    int   cur_h;         /* curiosity hidden width (64) */
+    int   dtype;         /* ROLLOUT_FP32 / ROLLOUT_TF32 / ROLLOUT_BF16 */
+    int   n_bars;        /* rows of every features buffer passed to rollout_run */
+    float barrier;       /* theta: done when portfolio PnL since reset >= +theta or <= -theta */
+    int   max_hold;      /* K: done after K steps since reset */
+    float pt_scale;      /* reward barrier_scale on a profit-take hit (0.5) */
+    float sl_scale;      /* reward barrier_scale on a stop-loss hit (-0.5) */
+    int   div_window;    /* diversity window length (20) */
+    float div_thresh;    /* entropy threshold in bits (1.0) */
+    float div_penalty;   /* added to the reward when entropy < threshold (-0.01) */
+    float cur_coef;      /* curiosity bonus = cur_coef * MSE (0.01) */
+    float risk_coef;     /* risk penalty = risk_coef * |exposure| (1e-3) */
+    float tx_base;       /* cost rate = (1 + order + urgency) * tx_base (1e-4) */
+    float spread;        /* third portfolio feature, a constant (1e-4) */
+} rollout_dims;
+
+typedef struct rollout_handle rollout_handle;
+
+/*
+ * rollout_create -- validate dims, convert and upload the weights.
+ *
+ * weights: HOST pointer to one packed float32 buffer, in this order, each
+ *   matrix [out, in] row-major followed by its bias [out]:
+ *     actor     W1[h1, n_market+3], b1, W2[h2, h1], b2, W3[n_actions, h2], b3
+ *     critic    V1[c1, n_market+3], c1 ... V_nh[c_nh, c_nh-1], V_head[1, c_nh], head bias
+ *     curiosity C1[cur_h, n_market+3+n_actions], d1, C2[n_market+3, cur_h], d2
+ *   The library copies it (rounding to the dtype's operand format and
+ *   re-tiling for the tensor cores); the caller keeps ownership and may free
+ *   it on return.
+ * out: receives the handle on success (unchanged on failure).
+ * Allocates device memory on the current device; all later calls must use
+ * that device.  Synchronous.  Returns ROLLOUT_OK, _INVALID, _UNSUPPORTED,
+ * _NOMEM or _CUDA.
+ */
+ROLLOUT_API int rollout_create(const float *weights, const rollout_dims *dims, rollout_handle **out);
+
+/*
+ * rollout_set_weights -- replace the weights of an existing handle (same
+ * packed layout as rollout_create; host pointer).  Synchronous with respect
+ * to the host; runs already enqueued on a stream are ordered before it only
+ * if the caller synchronises that stream first.
+ */
+ROLLOUT_API int rollout_set_weights(rollout_handle *h, const float *weights);
+
+/*
+ * rollout_run -- collect N x L experience tuples, including GAE.
+ *
+ * All array pointers are DEVICE pointers owned by the caller, 16-byte
+ * aligned, on the handle's device:
+ *   features        [n_bars, n_market] f32 row-major; column 0 is the bar's
+ *                   log-return, so P[b+1]/P[b] = exp(features[b+1, 0])
+ *   episode_starts  [N] i32, each in [0, n_bars - L - 1] (step t of episode n
+ *                   uses bar start+t and reads bar start+t+1 for its return)
+ *   seeds           [N] u32 initial LCG states; step t draws
+ *                   s = s*1664525 + 1013904223 (mod 2^32), u = (s >> 8) * 2^-24
+ *   out_states      [N, L, n_market+3] f32: [features of the bar, portfolio
+ *                   value since reset, held exposure, spread]
+ *   out_actions     [N, L] i32 in [0, n_actions)
+ *   out_logp        [N, L] f32 log pi(action | state)
+ *   out_values      [N, L] f32 critic value of the state
+ *   out_rewards     [N, L] f32
+ *   out_dones       [N, L] i32 (1 = the episode ended at this step and reset)
+ *   out_adv         [N, L] f32 GAE advantages
+ *   out_ret         [N, L] f32 returns = advantage + value
+ * gamma, lambda: in [0, 1].  The bootstrap value after the last step is the
+ *   critic of the last step's pre-reset next state.
+ * stream: a cudaStream_t (NULL = legacy default stream).
+ *
+ * Stream-ordered and asynchronous: returns after enqueuing; every output is
+ * fully overwritten by the time the stream reaches the end of the call (their
+ * contents in between are unspecified -- some serve as intermediate storage).
+ * Host-checkable arguments are validated before anything is enqueued
+ * (ROLLOUT_ERR_INVALID); device-detected problems (an out-of-range start,
+ * an expired bounded wait) are recorded in the handle's status word, read by
+ * rollout_status().  An episode with an out-of-range start is not simulated
+ * and its outputs are zero.  Returns ROLLOUT_OK, _INVALID or _CUDA.
+ */
+ROLLOUT_API int rollout_run(rollout_handle *h, const float *features, const int32_t *episode_starts,
+                const uint32_t *seeds, int N, int L, float gamma, float lambda,
+                float *out_states, int32_t *out_actions, float *out_logp, float *out_values,
+                float *out_rewards, int32_t *out_dones, float *out_adv, float *out_ret,
+                void *stream);
+
+/*
+ * rollout_status -- synchronise the stream of the last rollout_run on this
+ * handle and return its device status: ROLLOUT_OK, ROLLOUT_ERR_RANGE or
+ * ROLLOUT_ERR_TIMEOUT (or ROLLOUT_ERR_CUDA if the synchronisation failed).
+ */
+ROLLOUT_API int rollout_status(rollout_handle *h);
+
+/*
+ * rollout_set_timing -- when on != 0, every later rollout_run also records
+ * CUDA events on its stream before and after each of its kernels (rollout,
+ * value, GAE); off by default.  rollout_phase_ms synchronises the last run's
+ * final event and writes the three kernels' device times in milliseconds to
+ * ms[0..2].  Returns ROLLOUT_OK, _INVALID (timing was off or no run yet) or
+ * _CUDA.
+ */
+ROLLOUT_API int rollout_set_timing(rollout_handle *h, int on);
+ROLLOUT_API int rollout_phase_ms(rollout_handle *h, float *ms);
+
+/* rollout_destroy -- free the handle and its device memory (NULL is a no-op).
+ * Synchronises the device first. */
+ROLLOUT_API void rollout_destroy(rollout_handle *h);
+
+/* rollout_last_error -- message of the last failed call on this host thread
+ * ("" if none).  The pointer stays valid until the next call on the thread. */
+ROLLOUT_API const char *rollout_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROLLOUT_H */

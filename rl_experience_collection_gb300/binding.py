@@ -1,0 +1,206 @@
+"""Thin Python binding of the C ABI in ``include/rollout.h`` (ctypes).
+
+Argument marshalling only: every step of the computation runs in
+``librollout.so``.  There is no fallback -- if the library is missing or fails
+to load, :func:`lib` raises.  PyTorch supplies device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Dict, Optional
+
+from . import workloads as wl
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "librollout.so")
+
+ROLLOUT_OK = 0
+ROLLOUT_ERR_INVALID = -1
+ROLLOUT_ERR_RANGE = -2
+ROLLOUT_ERR_CUDA = -3
+ROLLOUT_ERR_TIMEOUT = -4
+ROLLOUT_ERR_UNSUPPORTED = -5
+ROLLOUT_ERR_NOMEM = -6
+DTYPE = {"fp32": 0, "tf32": 1, "bf16": 2}
+
+EXPORTS = ["rollout_create", "rollout_set_weights", "rollout_run", "rollout_status", "rollout_destroy",
+           "rollout_last_error", "rollout_set_timing", "rollout_phase_ms"]
+
+
+class RolloutDims(C.Structure):
+    _fields_ = [
+        ("n_market", C.c_int), ("n_actions", C.c_int), ("actor_h1", C.c_int), ("actor_h2", C.c_int),
+        ("critic_nh", C.c_int), ("critic_h", C.c_int * 8), ("cur_h", C.c_int), ("dtype", C.c_int),
+        ("n_bars", C.c_int), ("barrier", C.c_float), ("max_hold", C.c_int), ("pt_scale", C.c_float),
+        ("sl_scale", C.c_float), ("div_window", C.c_int), ("div_thresh", C.c_float),
+        ("div_penalty", C.c_float), ("cur_coef", C.c_float), ("risk_coef", C.c_float),
+        ("tx_base", C.c_float), ("spread", C.c_float),
+    ]
+
+
+class RolloutError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"rollout error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib(path: Optional[str] = None):
+    """Loads librollout.so (raises if it is missing: there is no fallback path)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with rl_experience_collection_gb300.build.build() "
+                           "(there is no CPU fallback)")
+    L = C.CDLL(p)
+    vp = C.c_void_p
+    L.rollout_create.restype = C.c_int
+    L.rollout_create.argtypes = [vp, C.POINTER(RolloutDims), C.POINTER(vp)]
+    L.rollout_set_weights.restype = C.c_int
+    L.rollout_set_weights.argtypes = [vp, vp]
+    L.rollout_run.restype = C.c_int
+    L.rollout_run.argtypes = [vp, vp, vp, vp, C.c_int, C.c_int, C.c_float, C.c_float,
+                              vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.rollout_status.restype = C.c_int
+    L.rollout_status.argtypes = [vp]
+    L.rollout_destroy.restype = None
+    L.rollout_destroy.argtypes = [vp]
+    L.rollout_set_timing.restype = C.c_int
+    L.rollout_set_timing.argtypes = [vp, C.c_int]
+    L.rollout_phase_ms.restype = C.c_int
+    L.rollout_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
+    L.rollout_last_error.restype = C.c_char_p
+    L.rollout_last_error.argtypes = []
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return lib().rollout_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != ROLLOUT_OK:
+        raise RolloutError(rc, last_error())
+
+
+def make_dims(w: wl.Workload, n_bars: Optional[int] = None, dtype: Optional[str] = None) -> RolloutDims:
+    d = RolloutDims()
+    d.n_market, d.n_actions = wl.N_MARKET, wl.N_ACTIONS
+    d.actor_h1, d.actor_h2 = wl.ACTOR_H
+    d.critic_nh = len(w.critic_h)
+    for i, h in enumerate(w.critic_h):
+        d.critic_h[i] = h
+    d.cur_h = wl.CUR_H
+    d.dtype = DTYPE[dtype or w.dtype]
+    d.n_bars = w.n_bars if n_bars is None else n_bars
+    d.barrier, d.max_hold = w.barrier, w.max_hold
+    d.pt_scale, d.sl_scale = w.pt_scale, w.sl_scale
+    d.div_window, d.div_thresh, d.div_penalty = w.div_window, w.div_thresh, w.div_penalty
+    d.cur_coef, d.risk_coef, d.tx_base, d.spread = w.cur_coef, w.risk_coef, w.tx_base, w.spread
+    return d
+
+
+OUTPUTS = ("states", "actions", "logp", "values", "rewards", "dones", "adv", "ret")
+
+
+def make_outputs(N: int, L: int, device="cuda") -> Dict[str, "torch.Tensor"]:
+    import torch
+    f32, i32 = torch.float32, torch.int32
+    return {
+        "states": torch.empty((N, L, wl.STATE_DIM), dtype=f32, device=device),
+        "actions": torch.empty((N, L), dtype=i32, device=device),
+        "logp": torch.empty((N, L), dtype=f32, device=device),
+        "values": torch.empty((N, L), dtype=f32, device=device),
+        "rewards": torch.empty((N, L), dtype=f32, device=device),
+        "dones": torch.empty((N, L), dtype=i32, device=device),
+        "adv": torch.empty((N, L), dtype=f32, device=device),
+        "ret": torch.empty((N, L), dtype=f32, device=device),
+    }
+
+
+class Rollout:
+    """Owns a ``rollout_handle``: ``rollout_create`` on construction, ``rollout_destroy`` on close."""
+
+    def __init__(self, weights, dims: RolloutDims):
+        import numpy as np
+        self._w = np.ascontiguousarray(weights, dtype=np.float32)
+        self.dims = dims
+        h = C.c_void_p()
+        _check(lib().rollout_create(self._w.ctypes.data_as(C.c_void_p), C.byref(dims), C.byref(h)))
+        self._h = h
+
+    @classmethod
+    def for_workload(cls, w: wl.Workload, weights, n_bars: Optional[int] = None, dtype: Optional[str] = None):
+        return cls(weights, make_dims(w, n_bars, dtype))
+
+    def set_weights(self, weights):
+        import numpy as np
+        self._w = np.ascontiguousarray(weights, dtype=np.float32)
+        _check(lib().rollout_set_weights(self._h, self._w.ctypes.data_as(C.c_void_p)))
+
+    def run(self, features, starts, seeds, N: int, L: int, gamma: float, lam: float,
+            out: Dict[str, "torch.Tensor"], stream=None) -> None:
+        """Enqueues one collection on ``stream`` (a torch.cuda.Stream, a raw handle, or None = current)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        p = lambda t: C.c_void_p(t.data_ptr())
+        _check(lib().rollout_run(self._h, p(features), p(starts), p(seeds), int(N), int(L), float(gamma),
+                                 float(lam), p(out["states"]), p(out["actions"]), p(out["logp"]),
+                                 p(out["values"]), p(out["rewards"]), p(out["dones"]), p(out["adv"]),
+                                 p(out["ret"]), C.c_void_p(sh)))
+
+    def run_raw(self, ptrs, N: int, L: int, gamma: float, lam: float, stream_handle: int = 0) -> int:
+        """Raw-pointer form (integers), returns the status code instead of raising."""
+        return lib().rollout_run(self._h, *[C.c_void_p(x) for x in ptrs[:3]], int(N), int(L), float(gamma),
+                                 float(lam), *[C.c_void_p(x) for x in ptrs[3:]], C.c_void_p(stream_handle))
+
+    def set_timing(self, on: bool = True) -> None:
+        _check(lib().rollout_set_timing(self._h, int(on)))
+
+    def phase_ms(self):
+        """Device milliseconds of the last run's rollout, value and GAE kernels."""
+        ms = (C.c_float * 3)()
+        _check(lib().rollout_phase_ms(self._h, ms))
+        return [float(x) for x in ms]
+
+    def status(self) -> int:
+        return lib().rollout_status(self._h)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().rollout_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def collect(w: wl.Workload, inputs: "wl.Inputs", N: Optional[int] = None, L: Optional[int] = None,
+            device="cuda", handle: Optional[Rollout] = None) -> Dict[str, "torch.Tensor"]:
+    """One-call convenience: uploads inputs, runs one collection, returns device outputs."""
+    import torch
+    N = w.n_episodes if N is None else N
+    L = w.horizon if L is None else L
+    h = handle or Rollout.for_workload(w, inputs.weights, n_bars=inputs.features.shape[0])
+    feats = torch.from_numpy(inputs.features).to(device)
+    starts = torch.from_numpy(inputs.starts[:N]).to(device)
+    seeds = torch.from_numpy(inputs.seeds[:N].view("int32")).to(device)
+    out = make_outputs(N, L, device)
+    h.run(feats, starts, seeds, N, L, w.gamma, w.lam, out)
+    st = h.status()
+    if st != ROLLOUT_OK:
+        raise RolloutError(st, "device-side status")
+    if handle is None:
+        h.close()
+    return out

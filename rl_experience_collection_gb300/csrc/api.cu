@@ -1,0 +1,381 @@
+// api.cu -- the C ABI (include/rollout.h): argument checks, weight
+// conversion, and the stream-ordered launch of the three phases.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "internal.cuh"
+#include "umma_path.cuh"
+
+using namespace rl;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(e == cudaErrorMemoryAllocation ? ROLLOUT_ERR_NOMEM : ROLLOUT_ERR_CUDA, "%s: %s", what,
+                cudaGetErrorString(e));
+}
+
+}  // namespace
+
+
+
+struct rollout_handle {
+    rollout_dims dims;
+    int device = 0;
+    int critic_w[kCriticLayers + 1] = {};
+    size_t n_weights = 0;
+    // float32 path
+    float *d_actor_packed = nullptr;   // phase-1 actor (SIMT layout)
+    float *d_simt = nullptr;           // transposed critic/curiosity + biases
+    SimtWeights simt{};
+    // tensor-core path
+    UmmaWeights umma{};
+    void *d_umma = nullptr;
+    // environment
+    uint32_t *d_div_low = nullptr;
+    int *d_status = nullptr;
+    cudaStream_t last_stream = nullptr;
+    // optional per-kernel timing
+    bool timing = false, timed_run = false;
+    cudaEvent_t ev[4] = {};
+};
+
+namespace {
+
+constexpr int kA1 = 0, kB1 = kA1 + kState * kActorH1, kA2 = kB1 + kActorH1, kB2 = kA2 + kActorH1 * kActorH2,
+              kA3 = kB2 + kActorH2, kB3 = kA3 + kActorH2 * 48, kActorPacked = kB3 + 48;
+
+int check_dims(const rollout_dims *d)
+{
+    if (d->n_market != kMarket || d->n_actions != kActions || d->actor_h1 != kActorH1 ||
+        d->actor_h2 != kActorH2 || d->cur_h != kCurH)
+        return fail(ROLLOUT_ERR_UNSUPPORTED, "unsupported network shape (need 51 market features, 45 actions, "
+                    "actor 128/64, curiosity 64)");
+    if (d->critic_nh != 5) return fail(ROLLOUT_ERR_UNSUPPORTED, "critic_nh must be 5");
+    static const int std_h[5] = {512, 384, 256, 128, 64}, wide_h[5] = {1024, 768, 512, 256, 128};
+    bool is_std = true, is_wide = true;
+    for (int i = 0; i < 5; ++i) {
+        is_std &= d->critic_h[i] == std_h[i];
+        is_wide &= d->critic_h[i] == wide_h[i];
+    }
+    if (!is_std && !is_wide)
+        return fail(ROLLOUT_ERR_UNSUPPORTED, "critic widths must be 512,384,256,128,64 or 1024,768,512,256,128");
+    if (d->dtype != ROLLOUT_FP32 && d->dtype != ROLLOUT_TF32 && d->dtype != ROLLOUT_BF16)
+        return fail(ROLLOUT_ERR_UNSUPPORTED, "unknown dtype %d", d->dtype);
+    if (d->n_bars < 2) return fail(ROLLOUT_ERR_INVALID, "n_bars must be >= 2");
+    if (d->div_window < 1 || d->div_window > 31)
+        return fail(ROLLOUT_ERR_UNSUPPORTED, "div_window must be in [1, 31]");
+    if (d->max_hold < 1) return fail(ROLLOUT_ERR_INVALID, "max_hold must be >= 1");
+    const float fs[] = {d->barrier, d->pt_scale, d->sl_scale, d->div_thresh, d->div_penalty, d->cur_coef,
+                        d->risk_coef, d->tx_base, d->spread};
+    for (float f : fs)
+        if (!isfinite(f)) return fail(ROLLOUT_ERR_INVALID, "environment constants must be finite");
+    return ROLLOUT_OK;
+}
+
+// offsets of the packed host buffer (rollout.h: actor, critic, curiosity)
+struct HostLayout {
+    size_t a_w[3], a_b[3], c_w[kCriticLayers], c_b[kCriticLayers], q_w[2], q_b[2], total;
+    int a_in[3], a_out[3], c_in[kCriticLayers], c_out[kCriticLayers], q_in[2], q_out[2];
+};
+
+HostLayout host_layout(const rollout_dims &d)
+{
+    HostLayout lo{};
+    size_t off = 0;
+    const int ain[3] = {kState, kActorH1, kActorH2}, aout[3] = {kActorH1, kActorH2, kActions};
+    for (int l = 0; l < 3; ++l) {
+        lo.a_in[l] = ain[l]; lo.a_out[l] = aout[l];
+        lo.a_w[l] = off; off += (size_t)ain[l] * aout[l];
+        lo.a_b[l] = off; off += aout[l];
+    }
+    int prev = kState;
+    for (int l = 0; l < kCriticLayers; ++l) {
+        const int o = l < 5 ? d.critic_h[l] : 1;
+        lo.c_in[l] = prev; lo.c_out[l] = o;
+        lo.c_w[l] = off; off += (size_t)prev * o;
+        lo.c_b[l] = off; off += o;
+        prev = o;
+    }
+    const int qin[2] = {kState + kActions, kCurH}, qout[2] = {kCurH, kState};
+    for (int l = 0; l < 2; ++l) {
+        lo.q_in[l] = qin[l]; lo.q_out[l] = qout[l];
+        lo.q_w[l] = off; off += (size_t)qin[l] * qout[l];
+        lo.q_b[l] = off; off += qout[l];
+    }
+    lo.total = off;
+    return lo;
+}
+
+void transpose_into(std::vector<float> &dst, size_t at, const float *W, int out, int in, int out_pad)
+{
+    for (int i = 0; i < in; ++i)
+        for (int j = 0; j < out_pad; ++j) dst[at + (size_t)i * out_pad + j] = j < out ? W[(size_t)j * in + i] : 0.f;
+}
+
+// float32 path: actor packed for phase 1, critic/curiosity transposed for phase 2
+int upload_simt(rollout_handle *h, const float *w)
+{
+    const HostLayout lo = host_layout(h->dims);
+    std::vector<float> ap(kActorPacked, 0.f);
+    transpose_into(ap, kA1, w + lo.a_w[0], kActorH1, kState, kActorH1);
+    memcpy(&ap[kB1], w + lo.a_b[0], sizeof(float) * kActorH1);
+    transpose_into(ap, kA2, w + lo.a_w[1], kActorH2, kActorH1, kActorH2);
+    memcpy(&ap[kB2], w + lo.a_b[1], sizeof(float) * kActorH2);
+    transpose_into(ap, kA3, w + lo.a_w[2], kActions, kActorH2, 48);
+    memcpy(&ap[kB3], w + lo.a_b[2], sizeof(float) * kActions);
+
+    std::vector<float> sp;
+    size_t offs_T[kCriticLayers], offs_b[kCriticLayers];
+    for (int l = 0; l < kCriticLayers; ++l) {
+        offs_T[l] = sp.size();
+        sp.resize(sp.size() + (size_t)lo.c_in[l] * lo.c_out[l]);
+        transpose_into(sp, offs_T[l], w + lo.c_w[l], lo.c_out[l], lo.c_in[l], lo.c_out[l]);
+        offs_b[l] = sp.size();
+        sp.insert(sp.end(), w + lo.c_b[l], w + lo.c_b[l] + lo.c_out[l]);
+    }
+    size_t q_T[2], q_b[2];
+    for (int l = 0; l < 2; ++l) {
+        q_T[l] = sp.size();
+        sp.resize(sp.size() + (size_t)lo.q_in[l] * lo.q_out[l]);
+        transpose_into(sp, q_T[l], w + lo.q_w[l], lo.q_out[l], lo.q_in[l], lo.q_out[l]);
+        q_b[l] = sp.size();
+        sp.insert(sp.end(), w + lo.q_b[l], w + lo.q_b[l] + lo.q_out[l]);
+    }
+    cudaError_t e;
+    if (!h->d_actor_packed) {
+        if ((e = cudaMalloc(&h->d_actor_packed, sizeof(float) * ap.size())) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(actor)");
+        if ((e = cudaMalloc(&h->d_simt, sizeof(float) * sp.size())) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(critic)");
+    }
+    if ((e = cudaMemcpy(h->d_actor_packed, ap.data(), sizeof(float) * ap.size(), cudaMemcpyHostToDevice)) !=
+        cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(actor)");
+    if ((e = cudaMemcpy(h->d_simt, sp.data(), sizeof(float) * sp.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(critic)");
+    for (int l = 0; l < kCriticLayers; ++l) {
+        h->simt.critic_T[l] = h->d_simt + offs_T[l];
+        h->simt.critic_b[l] = h->d_simt + offs_b[l];
+        h->simt.critic_w[l] = lo.c_in[l];
+    }
+    h->simt.critic_w[kCriticLayers] = 1;
+    h->simt.cur0_T = h->d_simt + q_T[0];
+    h->simt.cur0_b = h->d_simt + q_b[0];
+    h->simt.cur1_T = h->d_simt + q_T[1];
+    h->simt.cur1_b = h->d_simt + q_b[1];
+    h->simt.actor = h->d_actor_packed;
+    return ROLLOUT_OK;
+}
+
+// exact diversity decision per histogram (c0, c1, c2), c_k < 32
+int upload_div_table(rollout_handle *h)
+{
+    std::vector<uint32_t> bits(1024, 0u);
+    for (int c0 = 0; c0 < 32; ++c0)
+        for (int c1 = 0; c1 < 32; ++c1)
+            for (int c2 = 0; c2 < 32; ++c2) {
+                const int n = c0 + c1 + c2;
+                if (n == 0 || n > h->dims.div_window) continue;
+                double H = 0.0;
+                const int c[3] = {c0, c1, c2};
+                for (int k = 0; k < 3; ++k)
+                    if (c[k] > 0) {
+                        const double p = (double)c[k] / (double)n;
+                        H -= p * log2(p);
+                    }
+                if (H < (double)h->dims.div_thresh) {
+                    const int bit = c0 * 1024 + c1 * 32 + c2;
+                    bits[bit >> 5] |= 1u << (bit & 31);
+                }
+            }
+    cudaError_t e;
+    if (!h->d_div_low && (e = cudaMalloc(&h->d_div_low, bits.size() * 4)) != cudaSuccess)
+        return cuda_fail(e, "cudaMalloc(div table)");
+    if ((e = cudaMemcpy(h->d_div_low, bits.data(), bits.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(div table)");
+    return ROLLOUT_OK;
+}
+
+int upload_weights(rollout_handle *h, const float *w)
+{
+    const HostLayout lo = host_layout(h->dims);
+    for (size_t i = 0; i < lo.total; ++i)
+        if (!isfinite(w[i])) return fail(ROLLOUT_ERR_INVALID, "weight %zu is not finite", i);
+    if (h->dims.dtype == ROLLOUT_FP32) return upload_simt(h, w);
+    UmmaHostLayout ul{};
+    ul.n_critic = kCriticLayers;
+    for (int l = 0; l < 3; ++l) { ul.a_w[l] = lo.a_w[l]; ul.a_b[l] = lo.a_b[l]; }
+    for (int l = 0; l < kCriticLayers; ++l) {
+        ul.c_w[l] = lo.c_w[l]; ul.c_b[l] = lo.c_b[l]; ul.c_in[l] = lo.c_in[l]; ul.c_out[l] = lo.c_out[l];
+    }
+    for (int l = 0; l < 2; ++l) { ul.q_w[l] = lo.q_w[l]; ul.q_b[l] = lo.q_b[l]; }
+    return umma_upload(&h->umma, &h->d_umma, h->dims.dtype == ROLLOUT_BF16, w, ul, g_err, sizeof(g_err));
+}
+
+void free_handle(rollout_handle *h)
+{
+    if (!h) return;
+    cudaFree(h->d_actor_packed);
+    cudaFree(h->d_simt);
+    cudaFree(h->d_umma);
+    cudaFree(h->d_div_low);
+    cudaFree(h->d_status);
+    for (cudaEvent_t e : h->ev)
+        if (e) cudaEventDestroy(e);
+    delete h;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *rollout_last_error(void) { return g_err; }
+
+int rollout_create(const float *weights, const rollout_dims *dims, rollout_handle **out)
+{
+    g_err[0] = 0;
+    if (!weights || !dims || !out) return fail(ROLLOUT_ERR_INVALID, "null argument");
+    int rc = check_dims(dims);
+    if (rc) return rc;
+    rollout_handle *h = new (std::nothrow) rollout_handle();
+    if (!h) return fail(ROLLOUT_ERR_NOMEM, "host allocation failed");
+    h->dims = *dims;
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaGetDevice"); }
+    if ((e = cudaMalloc(&h->d_status, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMalloc(status)"); }
+    if ((e = cudaMemset(h->d_status, 0, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMemset"); }
+    if ((rc = upload_div_table(h)) || (rc = upload_weights(h, weights))) {
+        free_handle(h);
+        return rc;
+    }
+    *out = h;
+    return ROLLOUT_OK;
+}
+
+int rollout_set_weights(rollout_handle *h, const float *weights)
+{
+    g_err[0] = 0;
+    if (!h || !weights) return fail(ROLLOUT_ERR_INVALID, "null argument");
+    return upload_weights(h, weights);
+}
+
+int rollout_run(rollout_handle *h, const float *features, const int32_t *episode_starts, const uint32_t *seeds,
+                int N, int L, float gamma, float lambda, float *out_states, int32_t *out_actions,
+                float *out_logp, float *out_values, float *out_rewards, int32_t *out_dones, float *out_adv,
+                float *out_ret, void *stream)
+{
+    g_err[0] = 0;
+    if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
+    const void *ptrs[] = {features, episode_starts, seeds, out_states, out_actions, out_logp,
+                          out_values, out_rewards, out_dones, out_adv, out_ret};
+    for (const void *p : ptrs) {
+        if (!p) return fail(ROLLOUT_ERR_INVALID, "null array argument");
+        if (((uintptr_t)p & 15u) != 0) return fail(ROLLOUT_ERR_INVALID, "array arguments must be 16-byte aligned");
+    }
+    if (N <= 0 || L <= 0) return fail(ROLLOUT_ERR_INVALID, "N and L must be positive (N=%d, L=%d)", N, L);
+    if ((long long)L > (long long)h->dims.n_bars - 1)
+        return fail(ROLLOUT_ERR_INVALID, "L=%d needs at least L+1 bars (n_bars=%d)", L, h->dims.n_bars);
+    if ((long long)N * L * kState >= (1LL << 40))
+        return fail(ROLLOUT_ERR_INVALID, "N*L too large");
+    if (!(gamma >= 0.f && gamma <= 1.f) || !(lambda >= 0.f && lambda <= 1.f))
+        return fail(ROLLOUT_ERR_INVALID, "gamma and lambda must lie in [0, 1]");
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != h->device) return fail(ROLLOUT_ERR_INVALID, "current device %d is not the handle's device %d", dev, h->device);
+    h->last_stream = s;
+    if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+
+    const rollout_dims &d = h->dims;
+    EnvConst env{d.barrier, d.max_hold, d.pt_scale, d.sl_scale, d.div_window, d.div_thresh, d.div_penalty,
+                 d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div_low};
+    Phase1Args p1{features, episode_starts, seeds, N, L, d.n_bars, out_actions, out_logp, out_dones,
+                  out_rewards, out_values, out_adv, h->d_status, env};
+    ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_states, out_values,
+                 out_adv, out_rewards, out_ret, h->d_status, env};
+    GaeArgs ga{out_rewards, out_values, out_dones, out_adv, out_ret, N, L, gamma, lambda};
+
+    auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
+    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (d.dtype == ROLLOUT_FP32) {
+        if ((e = launch_phase1_simt(p1, h->d_actor_packed, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
+        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = launch_value_simt(va, h->simt, s)) != cudaSuccess) return cuda_fail(e, "value launch");
+    } else {
+        if ((e = launch_phase1_umma(p1, h->umma, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
+        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = launch_value_umma(va, h->umma, s)) != cudaSuccess) return cuda_fail(e, "value launch");
+    }
+    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
+    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    h->timed_run = h->timing;
+    return ROLLOUT_OK;
+}
+
+int rollout_status(rollout_handle *h)
+{
+    if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
+    cudaError_t e = cudaStreamSynchronize(h->last_stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int st = 0;
+    if ((e = cudaMemcpy(&st, h->d_status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(status)");
+    return st;
+}
+
+int rollout_set_timing(rollout_handle *h, int on)
+{
+    g_err[0] = 0;
+    if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
+    if (on && !h->ev[0]) {
+        for (cudaEvent_t &ev : h->ev) {
+            cudaError_t e = cudaEventCreate(&ev);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    h->timing = on != 0;
+    h->timed_run = false;
+    return ROLLOUT_OK;
+}
+
+int rollout_phase_ms(rollout_handle *h, float *ms)
+{
+    g_err[0] = 0;
+    if (!h || !ms) return fail(ROLLOUT_ERR_INVALID, "null argument");
+    if (!h->timed_run) return fail(ROLLOUT_ERR_INVALID, "no timed run (call rollout_set_timing first)");
+    cudaError_t e = cudaEventSynchronize(h->ev[3]);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    for (int i = 0; i < 3; ++i)
+        if ((e = cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1])) != cudaSuccess)
+            return cuda_fail(e, "cudaEventElapsedTime");
+    return ROLLOUT_OK;
+}
+
+void rollout_destroy(rollout_handle *h)
+{
+    if (!h) return;
+    cudaDeviceSynchronize();
+    free_handle(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// internal.cuh -- declarations shared by the translation units of librollout.
+//
+// The collector runs as three stream-ordered phases, with no host round trip:
+//   phase 1 (rollout): per episode, per step: actor MLP, softmax/CDF/LCG
+//     sample, portfolio, triple-barrier and diversity step, reset on done.
+//     The critic and the curiosity model do not feed the state trajectory,
+//     so they are not on this serial chain.
+//   phase 2 (value): every tuple independently (plus one bootstrap row per
+//     episode): rebuilds the state row, runs the critic MLP and the curiosity
+//     model, adds the curiosity bonus to the reward, writes the state row.
+//   phase 3 (gae): per episode, a warp-parallel segmented backward scan.
+// Between the phases the outputs double as intermediate storage:
+//   out_values[n,t] holds the portfolio value V entering step t (phase 1 ->
+//   phase 2, which overwrites it with the critic value), out_adv[n,t] holds
+//   the post-trade value V' (phase 1 -> phase 2, overwritten by phase 3),
+//   out_ret[n,L-1] holds the bootstrap value (phase 2 -> phase 3).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rollout.h"
+
+namespace rl {
+
+// environment constants, passed by value to the kernels
+struct EnvConst {
+    float barrier;
+    int max_hold;
+    float pt_scale, sl_scale;
+    int div_window;
+    float div_thresh, div_penalty;
+    float cur_coef, risk_coef, tx_base, spread;
+    // bit (c0*1024 + c1*32 + c2): 1 when the Shannon entropy (bits) of the
+    // category histogram (c0, c1, c2) is below div_thresh; 32768 bits
+    const uint32_t *div_low;
+};
+
+constexpr int kMarket = 51;
+constexpr int kState = 54;
+constexpr int kActions = 45;
+constexpr int kActorH1 = 128;
+constexpr int kActorH2 = 64;
+constexpr int kCurH = 64;
+constexpr int kCriticLayers = 6;   // 5 hidden + scalar head
+
+// device status word values (first error wins)
+constexpr int kStatusOk = 0;
+
+struct Phase1Args {
+    const float *F;            // [n_bars, 51]
+    const int32_t *starts;     // [N]
+    const uint32_t *seeds;     // [N]
+    int N, L, n_bars;
+    int32_t *actions;          // [N, L]
+    float *logp;               // [N, L]
+    int32_t *dones;            // [N, L]
+    float *rewards;            // [N, L]: reward without the curiosity bonus
+    float *v_in;               // [N, L]: V entering the step (out_values)
+    float *v_post;             // [N, L]: V' after the trade (out_adv)
+    int *status;
+    EnvConst env;
+};
+
+struct ValueArgs {
+    const float *F;
+    const int32_t *starts;
+    int N, L, n_bars;
+    const int32_t *actions;
+    const int32_t *dones;
+    float *states;             // [N, L, 54] written
+    float *values;             // in: V entering the step; out: critic value
+    const float *v_post;       // V' after the trade
+    float *rewards;            // in: base reward; out: + curiosity bonus
+    float *boot;               // out_ret: [n*L + L-1] receives the bootstrap value
+    int *status;
+    EnvConst env;
+};
+
+struct GaeArgs {
+    const float *rewards, *values;
+    const int32_t *dones;
+    float *adv, *ret;          // ret[n*L + L-1] holds the bootstrap value on entry
+    int N, L;
+    float gamma, lambda;
+};
+
+// --- float32 CUDA-core path (simt.cu) ---
+struct SimtWeights {
+    const float *actor;        // per layer: W^T [in][out_pad4] then b[out]; see api.cu
+    const float *critic_T[kCriticLayers];   // W^T [in][out]
+    const float *critic_b[kCriticLayers];
+    int critic_w[kCriticLayers + 1];         // widths: in, h1..h5, 1
+    const float *cur0_T, *cur0_b;           // [99][64], [64]
+    const float *cur1_T, *cur1_b;           // [64][54], [54]
+};
+cudaError_t launch_phase1_simt(const Phase1Args &a, const float *actor_packed, cudaStream_t s);
+cudaError_t launch_value_simt(const ValueArgs &a, const SimtWeights &w, cudaStream_t s);
+
+// --- GAE (gae.cu) ---
+cudaError_t launch_gae(const GaeArgs &a, cudaStream_t s);
+
+}  // namespace rl

@@ -1,0 +1,181 @@
+// umma_pack.cu -- host-side conversion of the packed float32 weights into the
+// tensor-core images: operands rounded once to the MMA format (bf16
+// round-to-nearest-even, or tf32 round-to-nearest ties away from zero, the
+// rounding of cvt.rna.tf32.f32), laid out as K-major 128-byte-swizzled tiles
+// (see umma.cuh), zero-padded in K and N.
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "umma_path.cuh"
+
+namespace rl {
+
+namespace {
+
+uint32_t f2u(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+float u2f(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+// bf16 bit pattern, round to nearest even (finite inputs)
+uint16_t bf16_bits(float x)
+{
+    const uint32_t u = f2u(x);
+    return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
+// tf32 value in a 32-bit container, round to nearest, ties away from zero
+uint32_t tf32_bits(float x) { return (f2u(x) + 0x1000u) & 0xFFFFE000u; }
+
+float rounded(float x, bool bf16) { return bf16 ? u2f((uint32_t)bf16_bits(x) << 16) : u2f(tf32_bits(x)); }
+
+struct Packer {
+    bool bf16;
+    int kc;   // elements per 128-byte K-chunk
+    explicit Packer(bool b) : bf16(b), kc(b ? 64 : 32) {}
+
+    // one swizzled tile: rows [row0, row0+nrows) of W[n_out][ld] (columns
+    // [0, k_valid) used, K-chunk `chunk`), appended to `out`
+    void tile(std::vector<uint8_t> &out, const float *W, int n_out, int ld, int k_valid, int row0, int nrows,
+              int chunk) const
+    {
+        const size_t base = out.size();
+        out.resize(base + (size_t)nrows * 128, 0);
+        for (int r = 0; r < nrows; ++r) {
+            const int n = row0 + r;
+            for (int c = 0; c < kc; ++c) {
+                const int k = chunk * kc + c;
+                const float v = (n < n_out && k < k_valid) ? W[(size_t)n * ld + k] : 0.f;
+                const int byte = c * (bf16 ? 2 : 4);
+                const int unit = byte >> 4, within = byte & 15;
+                const size_t off = base + (size_t)(r >> 3) * 1024 + (r & 7) * 128 + ((unit ^ (r & 7)) << 4) + within;
+                if (bf16) {
+                    const uint16_t b = bf16_bits(v);
+                    memcpy(&out[off], &b, 2);
+                } else {
+                    const uint32_t b = tf32_bits(v);
+                    memcpy(&out[off], &b, 4);
+                }
+            }
+        }
+    }
+};
+
+void set_layer(UmmaLayer &L, int n_out, int k_in, int kc, std::initializer_list<int> blocks)
+{
+    L.n_out = n_out;
+    L.k_chunks = (k_in + kc - 1) / kc;
+    L.n_blocks = 0;
+    for (int b : blocks) L.nb_rows[L.n_blocks++] = b;
+}
+
+}  // namespace
+
+int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const UmmaHostLayout &lo, char *err,
+                size_t err_len)
+{
+    const Packer P(bf16);
+    const int kc = P.kc;
+    const bool wide = lo.c_out[0] == 1024;
+    // ---------------- phase-1 actor image
+    std::vector<uint8_t> img;
+    const int k1 = (kState + kc - 1) / kc, k2 = kActorH1 / kc, k3 = kActorH2 / kc;
+    w->actor_off[0] = 0;
+    for (int c = 0; c < k1; ++c) P.tile(img, hw + lo.a_w[0], kActorH1, kState, kState, 0, kActorH1, c);
+    w->actor_off[1] = (uint32_t)img.size();
+    for (int c = 0; c < k2; ++c) P.tile(img, hw + lo.a_w[1], kActorH2, kActorH1, kActorH1, 0, kActorH2, c);
+    w->actor_off[2] = (uint32_t)img.size();
+    for (int c = 0; c < k3; ++c) P.tile(img, hw + lo.a_w[2], kActions, kActorH2, kActorH2, 0, 48, c);
+    w->actor_img_bytes = (uint32_t)img.size();
+
+    std::vector<float> abias(kActorH1 + kActorH2 + 48, 0.f);
+    memcpy(&abias[0], hw + lo.a_b[0], sizeof(float) * kActorH1);
+    memcpy(&abias[kActorH1], hw + lo.a_b[1], sizeof(float) * kActorH2);
+    memcpy(&abias[kActorH1 + kActorH2], hw + lo.a_b[2], sizeof(float) * kActions);
+
+    // ---------------- phase-2 unit stream
+    UmmaLayer *J = w->job;
+    if (!wide) {
+        set_layer(J[kJobCrit1], 512, kState, kc, {256, 256});
+        set_layer(J[kJobCrit2], 384, 512, kc, {256, 128});
+        set_layer(J[kJobCrit3], 256, 384, kc, {256});
+        set_layer(J[kJobCrit4], 128, 256, kc, {128});
+        set_layer(J[kJobCrit5], 64, 128, kc, {64});
+    } else {
+        set_layer(J[kJobCrit1], 1024, kState, kc, {256, 256, 256, 256});
+        set_layer(J[kJobCrit2], 768, 1024, kc, {256, 256, 256});
+        set_layer(J[kJobCrit3], 512, 768, kc, {256, 256});
+        set_layer(J[kJobCrit4], 256, 512, kc, {256});
+        set_layer(J[kJobCrit5], 128, 256, kc, {128});
+    }
+    set_layer(J[kJobCur1], kCurH, kState, kc, {64});
+    set_layer(J[kJobCur2], kState, kCurH, kc, {64});
+
+    std::vector<uint8_t> stream;
+    std::vector<float> vec;
+    auto emit = [&](int j, const float *W, int ld, int k_valid, const float *bias) {
+        UmmaLayer &L = J[j];
+        L.w_off = (long long)stream.size();
+        for (int c = 0; c < L.k_chunks; ++c) {
+            int row0 = 0;
+            for (int nb = 0; nb < L.n_blocks; ++nb) {
+                P.tile(stream, W, L.n_out, ld, k_valid, row0, L.nb_rows[nb], c);
+                row0 += L.nb_rows[nb];
+            }
+        }
+        L.bias_off = (int)vec.size();
+        int npad = 0;
+        for (int nb = 0; nb < L.n_blocks; ++nb) npad += L.nb_rows[nb];
+        for (int n = 0; n < npad; ++n) vec.push_back(n < L.n_out ? bias[n] : 0.f);
+    };
+    for (int l = 0; l < 5; ++l)
+        emit(kJobCrit1 + l, hw + lo.c_w[l], lo.c_in[l], lo.c_in[l], hw + lo.c_b[l]);
+    // curiosity layer 1: the state columns go through the MMA, the one-hot
+    // columns are gathered in the epilogue
+    emit(kJobCur1, hw + lo.q_w[0], kState + kActions, kState, hw + lo.q_b[0]);
+    emit(kJobCur2, hw + lo.q_w[1], kCurH, kCurH, hw + lo.q_b[1]);
+    w->head_w_off = (int)vec.size();
+    const int h5 = lo.c_in[5];
+    for (int k = 0; k < h5; ++k) vec.push_back(rounded(hw[lo.c_w[5] + k], bf16));
+    w->head_b_off = (int)vec.size();
+    vec.push_back(hw[lo.c_b[5]]);
+    while (vec.size() % 4) vec.push_back(0.f);
+    w->onehot_off = (int)vec.size();
+    for (int a = 0; a < kActions; ++a)
+        for (int j = 0; j < kCurH; ++j)
+            vec.push_back(rounded(hw[lo.q_w[0] + (size_t)j * (kState + kActions) + kState + a], bf16));
+
+    // ---------------- one device allocation: image | actor bias | stream | vec
+    auto align = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
+    const size_t o_img = 0, o_ab = align(img.size()), o_st = align(o_ab + abias.size() * 4),
+                 o_vec = align(o_st + stream.size()), total = align(o_vec + vec.size() * 4);
+    std::vector<uint8_t> host(total, 0);
+    memcpy(&host[o_img], img.data(), img.size());
+    memcpy(&host[o_ab], abias.data(), abias.size() * 4);
+    memcpy(&host[o_st], stream.data(), stream.size());
+    memcpy(&host[o_vec], vec.data(), vec.size() * 4);
+    cudaError_t e;
+    if (*d_buf) {
+        cudaFree(*d_buf);
+        *d_buf = nullptr;
+    }
+    if ((e = cudaMalloc(d_buf, total)) != cudaSuccess) {
+        snprintf(err, err_len, "cudaMalloc(tensor-core weights): %s", cudaGetErrorString(e));
+        return e == cudaErrorMemoryAllocation ? ROLLOUT_ERR_NOMEM : ROLLOUT_ERR_CUDA;
+    }
+    if ((e = cudaMemcpy(*d_buf, host.data(), total, cudaMemcpyHostToDevice)) != cudaSuccess) {
+        snprintf(err, err_len, "cudaMemcpy(tensor-core weights): %s", cudaGetErrorString(e));
+        return ROLLOUT_ERR_CUDA;
+    }
+    uint8_t *base = (uint8_t *)*d_buf;
+    w->bf16 = bf16;
+    w->wide = wide;
+    w->actor_img = base + o_img;
+    w->actor_bias = (const float *)(base + o_ab);
+    w->stream = base + o_st;
+    w->stream_bytes = (long long)stream.size();
+    w->vec = (const float *)(base + o_vec);
+    return ROLLOUT_OK;
+}
+
+}  // namespace rl

@@ -1,0 +1,59 @@
+// umma_path.cuh -- tensor-core (tcgen05) path for dtypes ROLLOUT_BF16 and
+// ROLLOUT_TF32: weight images and the phase-1 / phase-2 launchers.
+#pragma once
+
+#include <stddef.h>
+
+#include "internal.cuh"
+
+namespace rl {
+
+// One dense layer as the value kernel streams it.  Its weights are a sequence
+// of "units": for every 128-byte K-chunk k (in order) and every N-block nb (in
+// order), a swizzled K-major tile of nb_rows[nb] rows x 128 bytes.
+struct UmmaLayer {
+    int n_out;          // valid outputs
+    int k_chunks;       // 128-byte K-chunks of the (zero-padded) input
+    int n_blocks;       // MMA N-blocks
+    int nb_rows[4];     // rows of each N-block (multiple of 16, <= 256)
+    long long w_off;    // byte offset of the layer's first unit in the stream
+    int bias_off;       // float offset of the bias in `vec`
+};
+
+enum { kJobCrit1 = 0, kJobCrit2, kJobCrit3, kJobCrit4, kJobCrit5, kJobCur1, kJobCur2, kNumJobs };
+
+struct UmmaWeights {
+    bool bf16 = true;
+    bool wide = false;          // critic 1024/768/512/256/128
+    // phase 1: actor image [W1 chunks | W2 chunks | W3 chunks], copied whole into shared memory
+    const uint8_t *actor_img = nullptr;
+    uint32_t actor_img_bytes = 0;
+    uint32_t actor_off[3] = {};  // byte offsets of W1, W2, W3 in the image
+    const float *actor_bias = nullptr;   // b1[128] | b2[64] | b3[48] (b3 zero-padded)
+    // phase 2: weight-unit stream and per-layer table
+    const uint8_t *stream = nullptr;
+    long long stream_bytes = 0;
+    UmmaLayer job[kNumJobs];
+    const float *vec = nullptr;  // biases, head weights, curiosity one-hot columns (f32)
+    int head_w_off = 0;          // critic head weights [h5] (rounded to the operand format)
+    int head_b_off = 0;          // critic head bias [1]
+    int onehot_off = 0;          // curiosity layer-1 one-hot columns [45][64] (rounded)
+};
+
+// what the host packer needs from the packed f32 weight buffer (float offsets)
+struct UmmaHostLayout {
+    size_t a_w[3], a_b[3];
+    size_t c_w[kCriticLayers], c_b[kCriticLayers];
+    int c_in[kCriticLayers], c_out[kCriticLayers];
+    size_t q_w[2], q_b[2];
+    int n_critic;
+};
+
+// converts/uploads; *d_buf receives (or reuses) the device allocation
+int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *host_w, const UmmaHostLayout &lo,
+                char *err, size_t err_len);
+
+cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, cudaStream_t s);
+cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s);
+
+}  // namespace rl

@@ -1,0 +1,57 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/rollout.h declares.  CPU only: no compute calls."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "rollout.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rollout_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from rl_experience_collection_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("rollout_create", "rollout_run", "rollout_destroy", "rollout_status", "rollout_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    from rl_experience_collection_gb300 import binding
+    assert set(binding.EXPORTS) == set(_declared())
+
+
+def test_binding_struct_matches_header_field_order():
+    from rl_experience_collection_gb300 import binding
+    src = open(os.path.join(ROOT, "include", "rollout.h")).read()
+    body = src[src.index("typedef struct {"):src.index("} rollout_dims;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip().replace("typedef struct {", "").strip()
+        if not decl:
+            continue
+        typ, rest = decl.split(None, 1)
+        for name in rest.split(","):
+            fields.append(name.strip().split("[")[0])
+    assert fields == [f for f, _ in binding.RolloutDims._fields_]
+
+
+def test_last_error_callable_without_gpu(libpath):
+    from rl_experience_collection_gb300 import binding
+    binding.lib()
+    assert isinstance(binding.last_error(), str)
