@@ -104,7 +104,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [float(r[0]) for r in rows]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[4 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip() == "Active"})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]), "reasons": reasons,
                 "samples": len(rows), "power_w_max": max(float(r[2]) for r in rows)}
 

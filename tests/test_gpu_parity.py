@@ -62,10 +62,13 @@ def test_workload_matches_oracle(name, k):
     e_lp, e_v = parity.teacher_forced(w, inp, gpu, pairs, w.dtype)
     assert e_lp <= parity.RTOL[w.dtype] and e_v <= parity.RTOL[w.dtype], (e_lp, e_v)
     if w.dtype != "fp32":
-        # accuracy of the reduced-precision path against the unrounded definition
+        # accuracy of the reduced-precision path against the unrounded
+        # definition (fp32 weights, exact arithmetic): reported, and bounded
+        # by the bf16 operand error budget (2^-8 relative per operand over
+        # five layers), not by the parity tolerance
         e_lp, e_v = parity.teacher_forced(w, inp, gpu, pairs, "fp32")
         print(name, "vs unrounded oracle: logp", e_lp, "value", e_v)
-        assert e_lp <= 2e-2 and e_v <= 2e-2, (e_lp, e_v)
+        assert e_lp <= 5e-2 and e_v <= 5e-2, (e_lp, e_v)
 
 
 # ------------------------------------------------------------------ sampler through the kernel
