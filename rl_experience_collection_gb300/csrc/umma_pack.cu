@@ -113,27 +113,71 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const 
 
     std::vector<uint8_t> stream;
     std::vector<float> vec;
-    auto emit = [&](int j, const float *W, int ld, int k_valid, const float *bias) {
+    auto add_bias = [&](int j, const float *bias) {
         UmmaLayer &L = J[j];
-        L.w_off = (long long)stream.size();
-        for (int c = 0; c < L.k_chunks; ++c) {
-            int row0 = 0;
-            for (int nb = 0; nb < L.n_blocks; ++nb) {
-                P.tile(stream, W, L.n_out, ld, k_valid, row0, L.nb_rows[nb], c);
-                row0 += L.nb_rows[nb];
-            }
-        }
         L.bias_off = (int)vec.size();
         int npad = 0;
         for (int nb = 0; nb < L.n_blocks; ++nb) npad += L.nb_rows[nb];
         for (int n = 0; n < npad; ++n) vec.push_back(n < L.n_out ? bias[n] : 0.f);
     };
-    for (int l = 0; l < 5; ++l)
-        emit(kJobCrit1 + l, hw + lo.c_w[l], lo.c_in[l], lo.c_in[l], hw + lo.c_b[l]);
-    // curiosity layer 1: the state columns go through the MMA, the one-hot
-    // columns are gathered in the epilogue
-    emit(kJobCur1, hw + lo.q_w[0], kState + kActions, kState, hw + lo.q_b[0]);
-    emit(kJobCur2, hw + lo.q_w[1], kCurH, kCurH, hw + lo.q_b[1]);
+    for (int l = 0; l < 5; ++l) add_bias(kJobCrit1 + l, hw + lo.c_b[l]);
+    add_bias(kJobCur1, hw + lo.q_b[0]);
+    add_bias(kJobCur2, hw + lo.q_b[1]);
+    w->n_units = 0;
+    auto begin_unit = [&]() { w->unit_off[w->n_units] = (long long)stream.size(); };
+    auto end_unit = [&]() {
+        w->unit_bytes[w->n_units] = (uint32_t)((long long)stream.size() - w->unit_off[w->n_units]);
+        w->n_units++;
+    };
+    const float *V[5];
+    int vin[5];
+    for (int l = 0; l < 5; ++l) { V[l] = hw + lo.c_w[l]; vin[l] = lo.c_in[l]; }
+    const float *C1 = hw + lo.q_w[0], *C2 = hw + lo.q_w[1];
+    if (bf16 && !wide) {
+        // value-kernel consumption order (see value_umma.cu)
+        begin_unit();
+        P.tile(stream, C1, kCurH, kState + kActions, kState, 0, 64, 0);          // curiosity 1 (state part)
+        P.tile(stream, V[0], 512, vin[0], vin[0], 0, 64, 0);                      // layer-1 chunk 0
+        P.tile(stream, V[0], 512, vin[0], vin[0], 64, 64, 0);                     // layer-1 chunk 1
+        P.tile(stream, C2, kState, kCurH, kCurH, 0, 64, 0);                      // curiosity 2
+        end_unit();
+        for (int i = 0; i < 8; ++i) {
+            begin_unit();
+            P.tile(stream, V[1], 384, vin[1], vin[1], 0, 256, i);                // layer 2, K-chunk i
+            P.tile(stream, V[1], 384, vin[1], vin[1], 256, 128, i);
+            if (i + 2 < 8) P.tile(stream, V[0], 512, vin[0], vin[0], 64 * (i + 2), 64, 0);
+            end_unit();
+        }
+        const int order3[6] = {4, 5, 0, 1, 2, 3};
+        for (int kk = 0; kk < 6; ++kk) {
+            begin_unit();
+            P.tile(stream, V[2], 256, vin[2], vin[2], 0, 256, order3[kk]);       // layer 3
+            end_unit();
+        }
+        begin_unit();
+        for (int k = 0; k < 3; ++k) P.tile(stream, V[3], 128, vin[3], vin[3], 0, 128, k);   // layer 4
+        end_unit();
+        begin_unit();
+        P.tile(stream, V[3], 128, vin[3], vin[3], 0, 128, 3);
+        for (int k = 0; k < 2; ++k) P.tile(stream, V[4], 64, vin[4], vin[4], 0, 64, k);     // layer 5
+        end_unit();
+    } else {
+        // generic layer-by-layer order: for every layer, K-chunk-major units
+        auto emit = [&](int j, const float *W, int ld, int k_valid) {
+            UmmaLayer &L = J[j];
+            L.w_off = (long long)stream.size();
+            for (int c = 0; c < L.k_chunks; ++c) {
+                int row0 = 0;
+                for (int nb = 0; nb < L.n_blocks; ++nb) {
+                    P.tile(stream, W, L.n_out, ld, k_valid, row0, L.nb_rows[nb], c);
+                    row0 += L.nb_rows[nb];
+                }
+            }
+        };
+        for (int l = 0; l < 5; ++l) emit(kJobCrit1 + l, V[l], vin[l], vin[l]);
+        emit(kJobCur1, C1, kState + kActions, kState);
+        emit(kJobCur2, C2, kCurH, kCurH);
+    }
     w->head_w_off = (int)vec.size();
     const int h5 = lo.c_in[5];
     for (int k = 0; k < h5; ++k) vec.push_back(rounded(hw[lo.c_w[5] + k], bf16));

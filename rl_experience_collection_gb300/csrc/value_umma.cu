@@ -1,26 +1,44 @@
-// value_umma.cu -- tensor-core value phase (phase 2) for ROLLOUT_BF16.
+// value_umma.cu -- tensor-core value phase (phase 2), bf16 operands, critic
+// 54->512->384->256->128->64->1 and curiosity (54+45)->64->54.
 //
 // Page "PPO CUDA Pipeline Design -- Zero-Roundtrip Experience Collection",
-// section "Kernel Phases", Phase A step 5 (critic 54->512->384->256->128->64->1),
-// step 9 (curiosity forward model, bonus = cur_coef * MSE against the
-// pre-reset next state) and step 11 (state rows); section "Weight Layout".
+// section "Kernel Phases", Phase A step 5 (critic), step 9 (curiosity
+// forward model; bonus = cur_coef * MSE against the pre-reset next state) and
+// step 11 (state rows); section "Weight Layout".
 //
-// The critic and the curiosity model do not feed the state trajectory, so
-// they run here over every tuple at once instead of inside the serial step
-// loop: a persistent CTA takes tiles of 128 consecutive tuples (plus one
-// bootstrap row per episode: the pre-reset next state after the last step)
-// and runs each layer as M=128 tcgen05 MMAs with f32 accumulators in tensor
-// memory.  Warp roles:
-//   warps 0-3  rows: build the state rows (A operand + out_states), drain
-//              TMEM after every layer (bias, ReLU, bf16 rounding) into the
-//              next layer's swizzled A operand, head dot product, curiosity
-//              MSE, final stores
-//   warp 4     producer: streams the weight units (K-chunk x N-block tiles,
-//              pre-swizzled on the host) from L2 with 1-D bulk TMA into a
-//              two-stage ring
-//   warp 5     allocates TMEM; one lane issues the MMAs and the commits
-// Activations stay resident in shared memory (slots of 128 rows x 128 B);
-// each layer's output overwrites its input after the layer's MMAs complete.
+// The critic and the curiosity model do not feed the state trajectory, so they
+// run here over every tuple at once instead of inside the serial step loop.
+// A persistent CTA takes tiles of 128 consecutive rows (tuples, then one
+// bootstrap row per episode: the pre-reset next state after the last step) and
+// runs every layer as M=128 tcgen05 MMAs with f32 accumulators in TMEM.
+//
+// Warp roles (18 warps):
+//   0-15  row warps: warp w serves TMEM lanes / rows 32*(w%4)..+31 and the
+//         column quarter w/4 of every 64-column chunk.  They build the state
+//         rows (A operand + out_states), drain TMEM chunk by chunk (bias, ReLU,
+//         bf16 rounding) into the next layer's swizzled A operand, and finish
+//         with the head dot product, the curiosity MSE and the stores.  The
+//         next tile's row data is prefetched into registers one tile ahead.
+//   16    producer: streams the weights (pre-swizzled on the host, grouped
+//         into units of <= 56 KB because a bulk copy costs a fixed ~0.27 us)
+//         from L2 with 1-D bulk TMA into a two-stage ring
+//   17    allocates TMEM; one lane issues the MMAs and commits
+//
+// Per tile the MMA lane runs (TMEM columns in brackets):
+//   CUR1 [0,64) = X C1^T ; D1_0 [384,448), D1_1 [448,512) = X W1[chunk]^T
+//   CUR2 [64,128) = Z C2^T                         (after the rows wrote Z)
+//   for i < 8:  D2 [0,384) += h1_i W2[:, chunk i]^T  (after rows wrote h1_i)
+//               D1_{i+2} = X W1[chunk i+2]^T         (into the buffer h1_i left)
+//   D3 [256,512) += h2_k W3^T, k = 4,5,0,1,2,3       (as the rows write h2_k)
+//   D4 [0,128)   += h3_k W4^T, k = 0..3
+//   D5 [128,192) += h4_k W5^T, k = 0..1
+// so layer 1 never exists whole (its 64-column chunks are produced while the
+// tensor pipe accumulates layer 2) and every later layer starts on its first
+// K-chunk while the rows still drain the rest of the previous one.
+// Shared-memory operand slots (128 rows x 128 B each): X -> 4, Z -> 5,
+// h1 chunks -> 0/1 (alternating), h2 -> 0..5, h3 -> 0..3, h4 -> 0..1.
+// Every handoff has its own mbarrier (one phase per tile) so that no barrier
+// can complete twice before its waiter has seen the first completion.
 #include "env.cuh"
 #include "umma.cuh"
 #include "umma_path.cuh"
@@ -31,37 +49,30 @@ namespace {
 
 using namespace umma;
 
-constexpr int kVThreads = 192;
-constexpr int kSlot = 128 * 128;          // one activation K-chunk (128 rows x 128 B)
-constexpr int kStage = 256 * 128;         // one weight unit (<= 256 rows x 128 B)
+constexpr int kRowWarps = 16;
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kThreads = kRowThreads + 64;
+constexpr int kSlot = 128 * 128;
+constexpr int kNumSlots = 6;
+constexpr int kStage = 56 * 1024;
 constexpr int kStages = 2;
-constexpr int kXSlot = 8;                 // state operand
-constexpr int kZSlot = 2;                 // curiosity hidden operand
-constexpr int kNumSlots = 9;
-constexpr int kValueSmem = kNumSlots * kSlot + kStages * kStage + 1024;
+constexpr int kXSlot = 4, kZSlot = 5;
+constexpr int kBiasFloats = 1600;
+constexpr int kSmem = kNumSlots * kSlot + kStages * kStage + kBiasFloats * 4 + 2 * 4 * 128 * 4 + 1024;
+static_assert(kSmem <= 232448, "value kernel shared memory");
 
-// the producer and the MMA issuer both walk the jobs in enum order:
-// critic 1..5, then curiosity 1..2
-__host__ __device__ constexpr int a_slot_of(int j) { return (j == kJobCrit1 || j == kJobCur1) ? kXSlot : (j == kJobCur2 ? kZSlot : 0); }
-__host__ __device__ constexpr int d_col_of(int j) { return j == kJobCur1 ? 64 : (j == kJobCur2 ? 128 : 0); }
-__host__ __device__ constexpr bool waits_act(int j) { return j != kJobCur1; }
-__host__ __device__ constexpr int acc_bar_of(int j) { return (j == kJobCur1 || j == kJobCur2) ? 1 : 0; }
+// bias block layout in shared memory (floats)
+constexpr int kB1 = 0, kB2 = 512, kB3 = 896, kB4 = 1152, kB5 = 1280, kHW = 1344, kHB = 1408, kC1B = 1412,
+              kC2B = 1476;
 
-// 32 f32 values -> 4 bf16 units (64 bytes) of row r at column c0 of the activation slots
-__device__ __forceinline__ void put32_bf16(uint8_t *slots, int r, int c0, const float (&v)[32])
-{
-    uint8_t *tile = slots + (c0 >> 6) * kSlot;
-    const int u0 = (c0 & 63) >> 3;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 p;
-        p.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-        p.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-        p.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-        p.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-        *reinterpret_cast<uint4 *>(tile + sw128_offset(r, u0 + q)) = p;
-    }
-}
+// TMEM columns
+constexpr uint32_t kColCur1 = 0, kColCur2 = 64, kColD1 = 384, kColD2 = 0, kColD3 = 256, kColD4 = 0, kColD5 = 128;
+
+struct Bars {
+    uint64_t full[kStages], empty[kStages];
+    uint64_t act_x, act_z, act_h1[2], act_h2[6], act_h3[4], act_h4[2];
+    uint64_t acc_cur, acc_d1[2], acc_main, final_;
+};
 
 __device__ __forceinline__ float bf16_round(float x) { return __uint_as_float(pack_bf16x2(0.f, x) & 0xFFFF0000u); }
 
@@ -81,7 +92,7 @@ __device__ __forceinline__ RowInfo decode_row(const ValueArgs &a, long long r)
     const int L = a.L;
     if (r < NL) {
         const int n = (int)(r / L), t = (int)(r % L);
-        const int start = a.starts[n];
+        const int start = __ldg(a.starts + n);
         ri.row = r;
         if (start_ok(start, L, a.n_bars)) {
             ri.kind = 0;
@@ -96,7 +107,7 @@ __device__ __forceinline__ RowInfo decode_row(const ValueArgs &a, long long r)
         }
     } else if (r < NL + a.N) {
         const int n = (int)(r - NL);
-        const int start = a.starts[n];
+        const int start = __ldg(a.starts + n);
         const long long last = (long long)n * L + L - 1;
         ri.row = last;
         if (start_ok(start, L, a.n_bars)) {
@@ -112,13 +123,122 @@ __device__ __forceinline__ RowInfo decode_row(const ValueArgs &a, long long r)
     return ri;
 }
 
-__global__ void __launch_bounds__(kVThreads, 1) value_umma_bf16_kernel(ValueArgs a, UmmaWeights w)
+// the 16 state columns [16q, 16q+16) of a row, and its curiosity-target columns
+__device__ __forceinline__ void load_row_cols(const ValueArgs &a, const RowInfo &ri, int q, float (&xv)[16],
+                                              float (&tv)[16])
+{
+    const bool has = ri.kind == 0 || ri.kind == 1;
+    const float *fr = a.F + (has ? ri.bar : 0) * kMarket;
+    const float *fn = a.F + (ri.kind == 0 ? ri.bar + 1 : 0) * kMarket;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int c = 16 * q + j;
+        float x = 0.f, t = 0.f;
+        if (c < kMarket) {
+            x = has ? __ldg(fr + c) : 0.f;
+            t = ri.kind == 0 ? __ldg(fn + c) : 0.f;
+        } else if (c == kMarket) {
+            x = has ? ri.vin : 0.f;
+            t = ri.vpost;
+        } else if (c == kMarket + 1) {
+            x = has ? ri.ein : 0.f;
+            t = ri.epost;
+        } else if (c == kMarket + 2) {
+            x = has ? a.env.spread : 0.f;
+            t = a.env.spread;
+        }
+        xv[j] = x;
+        tv[j] = t;
+    }
+}
+
+// 16 f32 values -> 2 bf16 units of row r, columns [16q, 16q+16) of operand tile `tile`
+__device__ __forceinline__ void put16(uint8_t *tile, int r, int q, const float (&v)[16])
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint4 p;
+        p.x = pack_bf16x2(v[8 * h + 0], v[8 * h + 1]);
+        p.y = pack_bf16x2(v[8 * h + 2], v[8 * h + 3]);
+        p.z = pack_bf16x2(v[8 * h + 4], v[8 * h + 5]);
+        p.w = pack_bf16x2(v[8 * h + 6], v[8 * h + 7]);
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 2 * q + h)) = p;
+    }
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t x[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
+          "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15])
+        : "r"(taddr)
+        : "memory");
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(x[i]);
+}
+
+// relu(D[cols] + bias) rounded to bf16 into row r / quarter q of operand tile `tile`
+__device__ __forceinline__ void drain16(uint32_t taddr, const float *bias, uint8_t *tile, int r, int q)
+{
+    float v[16];
+    tmem_ld16(taddr, v);
+    const float4 *b4 = reinterpret_cast<const float4 *>(bias);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 b = b4[k];
+        v[4 * k + 0] = fmaxf(v[4 * k + 0] + b.x, 0.f);
+        v[4 * k + 1] = fmaxf(v[4 * k + 1] + b.y, 0.f);
+        v[4 * k + 2] = fmaxf(v[4 * k + 2] + b.z, 0.f);
+        v[4 * k + 3] = fmaxf(v[4 * k + 3] + b.w, 0.f);
+    }
+    put16(tile, r, q, v);
+}
+
+__device__ __forceinline__ void row_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory"); }
+
+// arrive after this thread's generic-proxy smem writes and TMEM reads
+__device__ __forceinline__ void publish(uint64_t *bar)
+{
+    fence_async_smem();
+    tc_fence_before();
+    mbar_arrive(bar);
+}
+
+struct MmaCtx {
+    uint32_t tmem, s_slots;
+    volatile int *abort;
+    bool ok;
+    __device__ __forceinline__ uint32_t slot(int s) const { return s_slots + s * kSlot; }
+    // D[col] (+)= A[a] * B[b]^T over one 128-byte K-chunk, N = n
+    __device__ __forceinline__ void mma_chunk(uint32_t col, uint32_t a, uint32_t b, int n, bool accumulate) const
+    {
+        const uint32_t id = idesc(true, 128, n);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            mma<true>(tmem + col, desc_sw128(a + 32 * k), desc_sw128(b + 32 * k), id,
+                      (accumulate || k > 0) ? 1u : 0u);
+    }
+    __device__ __forceinline__ void wait(uint64_t *bar, uint32_t &phase)
+    {
+        ok = ok && mbar_wait(bar, phase, abort);
+        phase ^= 1u;
+        tc_fence_after();
+    }
+};
+
+__global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs a, UmmaWeights w)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *slots = sm;
     uint8_t *ring = sm + kNumSlots * kSlot;
-    __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages], bar_acc[2], bar_act, bar_final;
+    float *bias = reinterpret_cast<float *>(ring + kStages * kStage);
+    float *part = bias + kBiasFloats;                    // [2][4][128] partial sums
+    __shared__ __align__(8) Bars B;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
 
@@ -126,16 +246,40 @@ __global__ void __launch_bounds__(kVThreads, 1) value_umma_bf16_kernel(ValueArgs
     if (tid == 0) {
         abort_sh = 0;
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 1);
+            mbar_init(&B.full[s], 1);
+            mbar_init(&B.empty[s], 1);
         }
-        mbar_init(&bar_acc[0], 1);
-        mbar_init(&bar_acc[1], 1);
-        mbar_init(&bar_act, 128);
-        mbar_init(&bar_final, 1);
+        mbar_init(&B.act_x, kRowThreads);
+        mbar_init(&B.act_z, kRowThreads);
+        for (int i = 0; i < 2; ++i) mbar_init(&B.act_h1[i], kRowThreads);
+        for (int i = 0; i < 6; ++i) mbar_init(&B.act_h2[i], kRowThreads);
+        for (int i = 0; i < 4; ++i) mbar_init(&B.act_h3[i], kRowThreads);
+        for (int i = 0; i < 2; ++i) mbar_init(&B.act_h4[i], kRowThreads);
+        mbar_init(&B.acc_cur, 1);
+        mbar_init(&B.acc_d1[0], 1);
+        mbar_init(&B.acc_d1[1], 1);
+        mbar_init(&B.acc_main, 1);
+        mbar_init(&B.final_, 1);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    // biases and head weights (f32; the head weights are already bf16-rounded)
+    {
+        const float *vec = w.vec;
+        for (int i = tid; i < kBiasFloats; i += kThreads) {
+            float v = 0.f;
+            if (i < kB2) v = vec[w.job[kJobCrit1].bias_off + i];
+            else if (i < kB3) v = vec[w.job[kJobCrit2].bias_off + i - kB2];
+            else if (i < kB4) v = vec[w.job[kJobCrit3].bias_off + i - kB3];
+            else if (i < kB5) v = vec[w.job[kJobCrit4].bias_off + i - kB4];
+            else if (i < kHW) v = vec[w.job[kJobCrit5].bias_off + i - kB5];
+            else if (i < kHB) v = vec[w.head_w_off + i - kHW];
+            else if (i == kHB) v = vec[w.head_b_off];
+            else if (i >= kC1B && i < kC2B) v = vec[w.job[kJobCur1].bias_off + i - kC1B];
+            else if (i >= kC2B && i < kC2B + 64) v = vec[w.job[kJobCur2].bias_off + i - kC2B];
+            bias[i] = v;
+        }
+    }
+    if (warp == kRowWarps + 1) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
@@ -148,234 +292,263 @@ __global__ void __launch_bounds__(kVThreads, 1) value_umma_bf16_kernel(ValueArgs
     const long long total = (long long)a.N * a.L + a.N;
     const long long n_tiles = (total + 127) / 128;
 
-    if (warp == 4) {
+    if (warp == kRowWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                for (int jj = 0; jj < kNumJobs && ok; ++jj) {
-                    const UmmaLayer &Ly = w.job[jj];
-                    const uint8_t *src = w.stream + Ly.w_off;
-                    for (int c = 0; c < Ly.k_chunks && ok; ++c) {
-                        for (int nb = 0; nb < Ly.n_blocks && ok; ++nb) {
-                            const uint32_t bytes = (uint32_t)Ly.nb_rows[nb] * 128u;
-                            ok = mbar_wait(&bar_empty[stage], phase ^ 1u, abort);
-                            if (!ok) break;
-                            mbar_arrive_expect_tx(&bar_full[stage], bytes);
-                            bulk_g2s(ring + stage * kStage, src, bytes, &bar_full[stage]);
-                            src += bytes;
-                            if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                        }
-                    }
+                for (int u = 0; u < w.n_units && ok; ++u) {
+                    const uint32_t bytes = w.unit_bytes[u];
+                    ok = mbar_wait(&B.empty[stage], phase ^ 1u, abort);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&B.full[stage], bytes);
+                    bulk_g2s(ring + stage * kStage, w.stream + w.unit_off[u], bytes, &B.full[stage]);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
             }
-            // wait until every issued copy has landed before the CTA may exit
+            // every issued copy has landed once the MMA lane has released its stage
             for (int s = 0; s < kStages && ok; ++s) {
-                ok = mbar_wait(&bar_empty[stage], phase ^ 1u, abort);
+                ok = mbar_wait(&B.empty[stage], phase ^ 1u, abort);
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
             if (!ok) {   // aborted: give copies already issued time to land (bounded)
-                const uint64_t t0 = global_ns();
-                while (global_ns() - t0 < 2000000ull) { }
+                const long long c0 = clock64();
+                while (clock64() - c0 < 4000000) { }
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kRowWarps + 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            MmaCtx m{tmem, smem_u32(slots), abort, true};
+            const uint32_t s_ring = smem_u32(ring);
             int stage = 0;
-            uint32_t phase = 0, act_phase = 0;
-            bool ok = true;
-            const uint32_t s_slots = smem_u32(slots), s_ring = smem_u32(ring);
-            for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                for (int jj = 0; jj < kNumJobs && ok; ++jj) {
-                    const int j = jj;
-                    const UmmaLayer &Ly = w.job[j];
-                    if (waits_act(j)) {
-                        ok = mbar_wait(&bar_act, act_phase, abort);
-                        act_phase ^= 1u;
-                        tc_fence_after();
+            uint32_t ring_ph = 0;
+            uint32_t ph_x = 0, ph_z = 0, ph_h1[2] = {0, 0}, ph_h2[6] = {}, ph_h3[4] = {}, ph_h4[2] = {};
+            auto take = [&]() -> uint32_t {      // wait for the next weight unit
+                uint32_t p = ring_ph;
+                m.wait(&B.full[stage], p);
+                return s_ring + stage * kStage;
+            };
+            auto release = [&]() {               // stage reusable once these MMAs complete
+                mma_commit(&B.empty[stage]);
+                if (++stage == kStages) { stage = 0; ring_ph ^= 1u; }
+            };
+            for (long long tile = blockIdx.x; tile < n_tiles && m.ok; tile += gridDim.x) {
+                // ---- unit 0: CUR1, D1_0, D1_1, CUR2
+                m.wait(&B.act_x, ph_x);
+                uint32_t u = take();
+                m.mma_chunk(kColCur1, m.slot(kXSlot), u, 64, false);
+                mma_commit(&B.acc_cur);
+                m.mma_chunk(kColD1, m.slot(kXSlot), u + 8192, 64, false);
+                mma_commit(&B.acc_d1[0]);
+                m.mma_chunk(kColD1 + 64, m.slot(kXSlot), u + 16384, 64, false);
+                mma_commit(&B.acc_d1[1]);
+                m.wait(&B.act_z, ph_z);
+                m.mma_chunk(kColCur2, m.slot(kZSlot), u + 24576, 64, false);
+                mma_commit(&B.acc_cur);
+                release();
+                // ---- layer 2 over the h1 chunks, layer-1 chunks two ahead
+                for (int i = 0; i < 8; ++i) {
+                    u = take();
+                    m.wait(&B.act_h1[i & 1], ph_h1[i & 1]);
+                    m.mma_chunk(kColD2, m.slot(i & 1), u, 256, i > 0);
+                    m.mma_chunk(kColD2 + 256, m.slot(i & 1), u + 32768, 128, i > 0);
+                    if (i + 2 < 8) {
+                        m.mma_chunk(kColD1 + 64 * (i & 1), m.slot(kXSlot), u + 49152, 64, false);
+                        mma_commit(&B.acc_d1[i & 1]);
                     }
-                    const uint32_t a_base = s_slots + a_slot_of(j) * kSlot;
-                    for (int c = 0; c < Ly.k_chunks && ok; ++c) {
-                        int col = d_col_of(j);
-                        for (int nb = 0; nb < Ly.n_blocks && ok; ++nb) {
-                            const int rows = Ly.nb_rows[nb];
-                            ok = mbar_wait(&bar_full[stage], phase, abort);
-                            if (!ok) break;
-                            tc_fence_after();
-                            const uint32_t b_base = s_ring + stage * kStage;
-                            const uint32_t id = idesc(true, 128, rows);
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                mma<true>(tmem + col, desc_sw128(a_base + c * kSlot + 32 * k),
-                                          desc_sw128(b_base + 32 * k), id, (c | k) != 0);
-                            mma_commit(&bar_empty[stage]);
-                            col += rows;
-                            if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                        }
-                    }
-                    mma_commit(&bar_acc[acc_bar_of(j)]);
+                    release();
                 }
+                mma_commit(&B.acc_main);
+                // ---- layer 3, K-chunks in the order the rows release them
+                for (int kk = 0; kk < 6; ++kk) {
+                    const int k = kk < 2 ? 4 + kk : kk - 2;
+                    u = take();
+                    m.wait(&B.act_h2[k], ph_h2[k]);
+                    m.mma_chunk(kColD3, m.slot(k), u, 256, kk > 0);
+                    release();
+                }
+                mma_commit(&B.acc_main);
+                // ---- layer 4 (unit: K0..K2; next unit: K3 + layer 5)
+                u = take();
+                for (int k = 0; k < 3; ++k) {
+                    m.wait(&B.act_h3[k], ph_h3[k]);
+                    m.mma_chunk(kColD4, m.slot(k), u + 16384 * k, 128, k > 0);
+                }
+                release();
+                u = take();
+                m.wait(&B.act_h3[3], ph_h3[3]);
+                m.mma_chunk(kColD4, m.slot(3), u, 128, true);
+                mma_commit(&B.acc_main);
+                // ---- layer 5
+                for (int k = 0; k < 2; ++k) {
+                    m.wait(&B.act_h4[k], ph_h4[k]);
+                    m.mma_chunk(kColD5, m.slot(k), u + 16384 + 8192 * k, 64, k > 0);
+                }
+                mma_commit(&B.acc_main);
+                release();
             }
             // every MMA issued must complete before TMEM is released (bounded wait)
-            mma_commit(&bar_final);
+            mma_commit(&B.final_);
             int never = 0;
-            mbar_wait(&bar_final, 0, &never, 100000000ull);
+            mbar_wait(&B.final_, 0, &never, 100000000ull);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ row warps
-        const int r = tid;                                  // TMEM lane / operand row
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-        uint32_t acc_phase[2] = {0, 0};
+        const int r = 32 * (warp & 3) + lane;                 // operand row / TMEM lane
+        const int q = warp >> 2;                               // column quarter of every 64-col chunk
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * q;
+        uint32_t ph_cur = 0, ph_d1[2] = {0, 0}, ph_main = 0;
         bool ok = true;
-        const float *vec = w.vec;
-        for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-            const RowInfo ri = decode_row(a, tile * 128 + r);
-            // ---- state row: A operand (bf16) and out_states (f32)
+        auto wait_acc = [&](uint64_t *bar, uint32_t &phase) {
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(bar, phase, abort));
+            phase ^= 1u;
+            tc_fence_after();
+        };
+        float *part_v = part, *part_s = part + 4 * 128;
+        auto build_x = [&](const RowInfo &ri, const float (&xv)[16]) {
+            put16(slots + kXSlot * kSlot, r, q, xv);
+            if ((ri.kind == 0 || ri.kind == 2) && 16 * q < kState) {
+                float2 *dst = reinterpret_cast<float2 *>(a.states + ri.row * kState + 16 * q);
+                const int n2 = (16 * q + 16 <= kState) ? 8 : (kState - 16 * q) / 2;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < n2) dst[j] = make_float2(xv[2 * j], xv[2 * j + 1]);
+            }
+            publish(&B.act_x);
+        };
+
+        long long tile = blockIdx.x;
+        RowInfo nri = decode_row(a, tile * 128 + r);
+        float nx[16], nt[16];
+        load_row_cols(a, nri, q, nx, nt);
+        build_x(nri, nx);
+
+        for (; tile < n_tiles && ok; tile += gridDim.x) {
+            const RowInfo ri = nri;
+            float tv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) tv[j] = nt[j];
+            const long long next = tile + gridDim.x;
+            const bool has_next = next < n_tiles;
+            if (has_next) {                                // prefetch one tile ahead
+                nri = decode_row(a, next * 128 + r);
+                load_row_cols(a, nri, q, nx, nt);
+            }
+            // ---- curiosity layer 1: state part from TMEM, one-hot column gathered
+            wait_acc(&B.acc_cur, ph_cur);
             {
-                float x[64];
-                const bool has = ri.kind == 0 || ri.kind == 1;
-                const float *fr = a.F + (has ? ri.bar : 0) * kMarket;
+                float v[16];
+                tmem_ld16(lane_addr + kColCur1, v);
+                const int act = (ri.act >= 0 && ri.act < kActions) ? ri.act : 0;
+                const float4 *oh = reinterpret_cast<const float4 *>(w.vec + w.onehot_off + act * kCurH + 16 * q);
+                const float4 *b4 = reinterpret_cast<const float4 *>(bias + kC1B + 16 * q);
 #pragma unroll
-                for (int j = 0; j < kMarket; ++j) x[j] = has ? __ldg(fr + j) : 0.f;
-                x[kMarket] = has ? ri.vin : 0.f;
-                x[kMarket + 1] = has ? ri.ein : 0.f;
-                x[kMarket + 2] = has ? a.env.spread : 0.f;
-#pragma unroll
-                for (int j = kState; j < 64; ++j) x[j] = 0.f;
-                float lo[32], hi[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) { lo[j] = x[j]; hi[j] = x[32 + j]; }
-                put32_bf16(slots + kXSlot * kSlot, r, 0, lo);
-                put32_bf16(slots + kXSlot * kSlot, r, 32, hi);
-                if (ri.kind == 0 || ri.kind == 2) {
-                    float2 *dst = reinterpret_cast<float2 *>(a.states + ri.row * kState);
-#pragma unroll
-                    for (int j = 0; j < kState / 2; ++j) dst[j] = make_float2(x[2 * j], x[2 * j + 1]);
+                for (int k = 0; k < 4; ++k) {
+                    const float4 o = __ldg(oh + k), b = b4[k];
+                    v[4 * k + 0] = fmaxf((v[4 * k + 0] + o.x) + b.x, 0.f);
+                    v[4 * k + 1] = fmaxf((v[4 * k + 1] + o.y) + b.y, 0.f);
+                    v[4 * k + 2] = fmaxf((v[4 * k + 2] + o.z) + b.z, 0.f);
+                    v[4 * k + 3] = fmaxf((v[4 * k + 3] + o.w) + b.w, 0.f);
                 }
+                put16(slots + kZSlot * kSlot, r, q, v);
+                publish(&B.act_z);
             }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar_act);
-            // ---- critic hidden layers 1-4
-            for (int l = 0; l < 4 && ok; ++l) {
-                const UmmaLayer &Ly = w.job[kJobCrit1 + l];
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc[0], acc_phase[0], abort));
-                acc_phase[0] ^= 1u;
-                tc_fence_after();
-                const float *bias = vec + Ly.bias_off;
-                for (int g = 0; g < Ly.n_out / 32; ++g) {
-                    float v[32];
-                    tmem_ld32(lane_addr + 32 * g, v);
-                    tmem_ld_wait();
+            // ---- curiosity layer 2: squared error against the pre-reset next state
+            wait_acc(&B.acc_cur, ph_cur);
+            {
+                float v[16];
+                tmem_ld16(lane_addr + kColCur2, v);
+                float se = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i] + __ldg(bias + 32 * g + i), 0.f);
-                    put32_bf16(slots, r, 32 * g, v);
-                }
-                fence_async_smem();
-                tc_fence_before();
-                mbar_arrive(&bar_act);
-            }
-            // ---- critic layer 5 + scalar head
-            float value = 0.f;
-            if (ok) {
-                const UmmaLayer &Ly = w.job[kJobCrit5];
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc[0], acc_phase[0], abort));
-                acc_phase[0] ^= 1u;
-                tc_fence_after();
-                const float *bias = vec + Ly.bias_off, *hw = vec + w.head_w_off;
-                for (int g = 0; g < Ly.n_out / 32; ++g) {
-                    float v[32];
-                    tmem_ld32(lane_addr + 32 * g, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        value = fmaf(bf16_round(fmaxf(v[i] + __ldg(bias + 32 * g + i), 0.f)), __ldg(hw + 32 * g + i), value);
-                }
-                value += __ldg(vec + w.head_b_off);
-            }
-            // ---- curiosity layer 1: state part from TMEM + one-hot column gather
-            if (ok) {
-                const UmmaLayer &Ly = w.job[kJobCur1];
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc[1], acc_phase[1], abort));
-                acc_phase[1] ^= 1u;
-                tc_fence_after();
-                const float *bias = vec + Ly.bias_off;
-                const float *oh = vec + w.onehot_off + (ri.act >= 0 && ri.act < kActions ? ri.act : 0) * kCurH;
-#pragma unroll
-                for (int g = 0; g < kCurH / 32; ++g) {
-                    float v[32];
-                    tmem_ld32(lane_addr + d_col_of(kJobCur1) + 32 * g, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = fmaxf((v[i] + __ldg(oh + 32 * g + i)) + __ldg(bias + 32 * g + i), 0.f);
-                    put32_bf16(slots + kZSlot * kSlot, r, 32 * g, v);
-                }
-                fence_async_smem();
-                tc_fence_before();
-                mbar_arrive(&bar_act);
-            }
-            // ---- curiosity layer 2 + MSE against the pre-reset next state
-            float se = 0.f;
-            if (ok) {
-                const UmmaLayer &Ly = w.job[kJobCur2];
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc[1], acc_phase[1], abort));
-                acc_phase[1] ^= 1u;
-                tc_fence_after();
-                const float *bias = vec + Ly.bias_off;
-                const float *fn = a.F + (ri.kind == 0 ? ri.bar + 1 : 0) * kMarket;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    float v[32];
-                    tmem_ld32(lane_addr + d_col_of(kJobCur2) + 32 * g, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int j = 32 * g + i;
-                        if (j < kState) {
-                            const float tgt = j < kMarket ? __ldg(fn + j)
-                                              : (j == kMarket ? ri.vpost : (j == kMarket + 1 ? ri.epost : a.env.spread));
-                            const float d = (v[i] + __ldg(bias + j)) - tgt;
-                            se = fmaf(d, d, se);
-                        }
+                for (int j = 0; j < 16; ++j) {
+                    if (16 * q + j < kState) {
+                        const float d = (v[j] + bias[kC2B + 16 * q + j]) - tv[j];
+                        se = fmaf(d, d, se);
                     }
                 }
-                tc_fence_before();
+                part_s[q * 128 + r] = se;
             }
-            // ---- outputs
-            if (ri.kind == 0) {
-                a.values[ri.row] = value;
-                a.rewards[ri.row] += a.env.cur_coef * (se / (float)kState);
-            } else if (ri.kind == 2) {
-                a.values[ri.row] = 0.f;
-            } else if (ri.kind == 1) {
-                a.boot[ri.row] = value;
-            } else if (ri.kind == 3) {
-                a.boot[ri.row] = 0.f;
+            // ---- layer-1 chunks (the tensor pipe accumulates layer 2 meanwhile)
+            for (int c = 0; c < 8; ++c) {
+                wait_acc(&B.acc_d1[c & 1], ph_d1[c & 1]);
+                drain16(lane_addr + kColD1 + 64 * (c & 1), bias + kB1 + 64 * c + 16 * q, slots + (c & 1) * kSlot, r, q);
+                publish(&B.act_h1[c & 1]);
             }
+            // ---- layer 2 -> h2, chunks 4,5 first (their TMEM columns become layer 3's)
+            wait_acc(&B.acc_main, ph_main);
+            for (int kk = 0; kk < 6; ++kk) {
+                const int k = kk < 2 ? 4 + kk : kk - 2;
+                drain16(lane_addr + kColD2 + 64 * k, bias + kB2 + 64 * k + 16 * q, slots + k * kSlot, r, q);
+                publish(&B.act_h2[k]);
+            }
+            // ---- layer 3 -> h3
+            wait_acc(&B.acc_main, ph_main);
+            for (int k = 0; k < 4; ++k) {
+                drain16(lane_addr + kColD3 + 64 * k, bias + kB3 + 64 * k + 16 * q, slots + k * kSlot, r, q);
+                publish(&B.act_h3[k]);
+            }
+            // ---- layer 4 -> h4
+            wait_acc(&B.acc_main, ph_main);
+            for (int k = 0; k < 2; ++k) {
+                drain16(lane_addr + kColD4 + 64 * k, bias + kB4 + 64 * k + 16 * q, slots + k * kSlot, r, q);
+                publish(&B.act_h4[k]);
+            }
+            // ---- next tile's state row (slot 4 and TMEM [0,128) are free now)
+            if (has_next) build_x(nri, nx);
+            // ---- layer 5 + scalar head
+            wait_acc(&B.acc_main, ph_main);
+            {
+                float v[16];
+                tmem_ld16(lane_addr + kColD5, v);
+                float dot = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float h = bf16_round(fmaxf(v[j] + bias[kB5 + 16 * q + j], 0.f));
+                    dot = fmaf(h, bias[kHW + 16 * q + j], dot);
+                }
+                part_v[q * 128 + r] = dot;
+            }
+            tc_fence_before();
+            row_sync();
+            if (q == 0) {
+                const float value = ((part_v[r] + part_v[128 + r]) + (part_v[256 + r] + part_v[384 + r])) + bias[kHB];
+                const float se = (part_s[r] + part_s[128 + r]) + (part_s[256 + r] + part_s[384 + r]);
+                if (ri.kind == 0) {
+                    a.values[ri.row] = value;
+                    a.rewards[ri.row] += a.env.cur_coef * (se / (float)kState);
+                } else if (ri.kind == 2) {
+                    a.values[ri.row] = 0.f;
+                } else if (ri.kind == 1) {
+                    a.boot[ri.row] = value;
+                } else if (ri.kind == 3) {
+                    a.boot[ri.row] = 0.f;
+                }
+            }
+            row_sync();
         }
     }
     if (abort_sh && tid == 0) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, 512);
+    if (warp == kRowWarps + 1) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
 
 cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s)
 {
-    if (!w.bf16 || w.wide) return cudaErrorNotSupported;
+    if (!w.bf16 || w.wide || w.n_units != 17) return cudaErrorNotSupported;
+    for (int u = 0; u < w.n_units; ++u)
+        if (w.unit_bytes[u] > (uint32_t)kStage || (w.unit_bytes[u] & 15u) || (w.unit_off[u] & 15)) return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(value_umma_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kValueSmem);
+        cudaError_t e = cudaFuncSetAttribute(value_umma_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -385,7 +558,7 @@ cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStre
     const long long total = (long long)a.N * a.L + a.N;
     const long long tiles = (total + 127) / 128;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    value_umma_bf16_kernel<<<grid, kVThreads, kValueSmem, s>>>(a, w);
+    value_umma_bf16_kernel<<<grid, kThreads, kSmem, s>>>(a, w);
     return cudaGetLastError();
 }
 
