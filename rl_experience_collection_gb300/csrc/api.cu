@@ -48,6 +48,10 @@ struct rollout_handle {
     // tensor-core path
     UmmaWeights umma{};
     void *d_umma = nullptr;
+    // per-CTA activation scratch of the generic value kernel (tf32 / widened critic)
+    uint8_t *d_scratch = nullptr;
+    long long scratch_per_cta = 0;
+    int scratch_ctas = 0;
     // environment
     uint32_t *d_div_low = nullptr;
     int *d_status = nullptr;
@@ -227,7 +231,18 @@ int upload_weights(rollout_handle *h, const float *w)
         ul.c_w[l] = lo.c_w[l]; ul.c_b[l] = lo.c_b[l]; ul.c_in[l] = lo.c_in[l]; ul.c_out[l] = lo.c_out[l];
     }
     for (int l = 0; l < 2; ++l) { ul.q_w[l] = lo.q_w[l]; ul.q_b[l] = lo.q_b[l]; }
-    return umma_upload(&h->umma, &h->d_umma, h->dims.dtype == ROLLOUT_BF16, w, ul, g_err, sizeof(g_err));
+    int rc = umma_upload(&h->umma, &h->d_umma, h->dims.dtype == ROLLOUT_BF16, w, ul, g_err, sizeof(g_err));
+    if (rc) return rc;
+    if (value_needs_scratch(h->umma) && !h->d_scratch) {
+        int sms = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        h->scratch_per_cta = value_generic_scratch_per_cta(h->umma);
+        h->scratch_ctas = sms;
+        if ((e = cudaMalloc(&h->d_scratch, (size_t)h->scratch_per_cta * sms)) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(value scratch)");
+    }
+    return ROLLOUT_OK;
 }
 
 void free_handle(rollout_handle *h)
@@ -236,6 +251,7 @@ void free_handle(rollout_handle *h)
     cudaFree(h->d_actor_packed);
     cudaFree(h->d_simt);
     cudaFree(h->d_umma);
+    cudaFree(h->d_scratch);
     cudaFree(h->d_div_low);
     cudaFree(h->d_status);
     for (cudaEvent_t e : h->ev)
@@ -323,7 +339,14 @@ int rollout_run(rollout_handle *h, const float *features, const int32_t *episode
     } else {
         if ((e = launch_phase1_umma(p1, h->umma, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if ((e = launch_value_umma(va, h->umma, s)) != cudaSuccess) return cuda_fail(e, "value launch");
+        if (value_needs_scratch(h->umma)) {
+            const long long tiles = ((long long)N * L + N + 127) / 128;
+            const int grid = (int)(tiles < h->scratch_ctas ? tiles : h->scratch_ctas);
+            e = launch_value_generic(va, h->umma, h->d_scratch, h->scratch_per_cta, grid, s);
+        } else {
+            e = launch_value_umma(va, h->umma, s);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "value launch");
     }
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");

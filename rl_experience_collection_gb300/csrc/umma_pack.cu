@@ -162,16 +162,15 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const 
         for (int k = 0; k < 2; ++k) P.tile(stream, V[4], 64, vin[4], vin[4], 0, 64, k);     // layer 5
         end_unit();
     } else {
-        // generic layer-by-layer order: for every layer, K-chunk-major units
+        // generic kernel order: per layer, N-block-major; the K-chunk tiles of
+        // one N-block are contiguous
         auto emit = [&](int j, const float *W, int ld, int k_valid) {
             UmmaLayer &L = J[j];
             L.w_off = (long long)stream.size();
-            for (int c = 0; c < L.k_chunks; ++c) {
-                int row0 = 0;
-                for (int nb = 0; nb < L.n_blocks; ++nb) {
-                    P.tile(stream, W, L.n_out, ld, k_valid, row0, L.nb_rows[nb], c);
-                    row0 += L.nb_rows[nb];
-                }
+            int row0 = 0;
+            for (int nb = 0; nb < L.n_blocks; ++nb) {
+                for (int c = 0; c < L.k_chunks; ++c) P.tile(stream, W, L.n_out, ld, k_valid, row0, L.nb_rows[nb], c);
+                row0 += L.nb_rows[nb];
             }
         };
         for (int l = 0; l < 5; ++l) emit(kJobCrit1 + l, V[l], vin[l], vin[l]);

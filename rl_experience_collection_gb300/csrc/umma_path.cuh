@@ -58,6 +58,12 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *host_w, co
                 char *err, size_t err_len);
 
 cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, cudaStream_t s);
+// bf16 operands with the 512/384/256/128/64 critic: activations resident in shared memory
 cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s);
+// every other shape: activations in per-CTA global scratch (see value_generic.cu)
+long long value_generic_scratch_per_cta(const UmmaWeights &w);
+cudaError_t launch_value_generic(const ValueArgs &a, const UmmaWeights &w, uint8_t *scratch, long long per_cta,
+                                 int grid, cudaStream_t s);
+inline bool value_needs_scratch(const UmmaWeights &w) { return !w.bf16 || w.wide; }
 
 }  // namespace rl

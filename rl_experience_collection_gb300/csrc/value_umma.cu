@@ -84,71 +84,106 @@ struct RowInfo {
     float vin, ein, vpost, epost;
 };
 
-__device__ __forceinline__ RowInfo decode_row(const ValueArgs &a, long long r)
+// Row data is fetched in two non-blocking stages so that no thread stalls on
+// a global load while the tensor pipe waits for it:
+//   stage 1 (issue_meta): every load whose address depends only on the row
+//            index, issued unconditionally from clamped addresses;
+//   stage 2 (issue_cols): once those values have arrived (mid-tile), the
+//            row's kind/bar and the feature-row loads that depend on them.
+struct RowFetch {
+    long long r, row;          // flat row, tuple index / bootstrap slot
+    int n, t, is_boot;         // episode, step, bootstrap row?
+    int start, act, aprev, dprev;
+    float vin, vpost;
+};
+
+__device__ __forceinline__ void issue_meta(const ValueArgs &a, long long r, RowFetch &f)
 {
-    RowInfo ri{};
-    ri.kind = -1;
     const long long NL = (long long)a.N * a.L;
     const int L = a.L;
-    if (r < NL) {
-        const int n = (int)(r / L), t = (int)(r % L);
-        const int start = __ldg(a.starts + n);
-        ri.row = r;
-        if (start_ok(start, L, a.n_bars)) {
-            ri.kind = 0;
-            ri.bar = (long long)start + t;
-            ri.act = a.actions[r];
-            ri.vin = a.values[r];
-            ri.vpost = a.v_post[r];
-            ri.epost = exposure_of(ri.act);
-            ri.ein = (t == 0 || a.dones[r - 1]) ? 0.f : exposure_of(a.actions[r - 1]);
-        } else {
-            ri.kind = 2;
-        }
-    } else if (r < NL + a.N) {
-        const int n = (int)(r - NL);
-        const int start = __ldg(a.starts + n);
-        const long long last = (long long)n * L + L - 1;
-        ri.row = last;
-        if (start_ok(start, L, a.n_bars)) {
-            ri.kind = 1;
-            ri.bar = (long long)start + L;
-            ri.act = a.actions[last];
-            ri.vin = a.v_post[last];
-            ri.ein = exposure_of(ri.act);
-        } else {
-            ri.kind = 3;
-        }
+    f.r = r;
+    f.is_boot = r >= NL;
+    const long long rc = r < NL + a.N ? r : NL + a.N - 1;      // rows past the end read row `total-1`
+    f.n = f.is_boot ? (int)(rc - NL) : (int)(rc / L);
+    f.t = f.is_boot ? L - 1 : (int)(rc % L);
+    f.row = (long long)f.n * L + f.t;
+    const long long prev = f.t > 0 ? f.row - 1 : f.row;
+    f.start = __ldg(a.starts + f.n);
+    f.act = a.actions[f.row];
+    f.vin = f.is_boot ? a.v_post[f.row] : a.values[f.row];
+    f.vpost = a.v_post[f.row];
+    f.aprev = a.actions[prev];
+    f.dprev = a.dones[prev];
+}
+
+__device__ __forceinline__ RowInfo resolve(const ValueArgs &a, const RowFetch &f)
+{
+    RowInfo ri{};
+    const long long NL = (long long)a.N * a.L;
+    const bool ok = start_ok(f.start, a.L, a.n_bars);
+    ri.row = f.row;
+    ri.act = f.act;
+    if (f.r >= NL + a.N) {
+        ri.kind = -1;
+    } else if (!f.is_boot) {
+        ri.kind = ok ? 0 : 2;
+        ri.bar = (long long)f.start + f.t;
+        ri.vin = f.vin;
+        ri.vpost = f.vpost;
+        ri.epost = exposure_of(f.act);
+        ri.ein = (f.t == 0 || f.dprev) ? 0.f : exposure_of(f.aprev);
+    } else {
+        ri.kind = ok ? 1 : 3;
+        ri.bar = (long long)f.start + a.L;
+        ri.vin = f.vin;
+        ri.ein = exposure_of(f.act);
     }
+    if (ri.kind != 0 && ri.kind != 1) ri.bar = 0;
     return ri;
 }
 
-// the 16 state columns [16q, 16q+16) of a row, and its curiosity-target columns
-__device__ __forceinline__ void load_row_cols(const ValueArgs &a, const RowInfo &ri, int q, float (&xv)[16],
-                                              float (&tv)[16])
+// issues the loads of the 16 market columns [16q, 16q+16) of the row's bar and
+// of the next bar (curiosity target); rows without a bar read bar 0 and are
+// masked by finish_cols, so that nothing here waits on a loaded value
+__device__ __forceinline__ void issue_cols(const ValueArgs &a, const RowInfo &ri, int q, float (&xv)[16],
+                                           float (&tv)[16])
 {
-    const bool has = ri.kind == 0 || ri.kind == 1;
-    const float *fr = a.F + (has ? ri.bar : 0) * kMarket;
+    const float *fr = a.F + ri.bar * kMarket;
     const float *fn = a.F + (ri.kind == 0 ? ri.bar + 1 : 0) * kMarket;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int c = 16 * q + j;
-        float x = 0.f, t = 0.f;
         if (c < kMarket) {
-            x = has ? __ldg(fr + c) : 0.f;
-            t = ri.kind == 0 ? __ldg(fn + c) : 0.f;
-        } else if (c == kMarket) {
-            x = has ? ri.vin : 0.f;
-            t = ri.vpost;
-        } else if (c == kMarket + 1) {
-            x = has ? ri.ein : 0.f;
-            t = ri.epost;
-        } else if (c == kMarket + 2) {
-            x = has ? a.env.spread : 0.f;
-            t = a.env.spread;
+            xv[j] = __ldg(fr + c);
+            tv[j] = __ldg(fn + c);
         }
-        xv[j] = x;
-        tv[j] = t;
+    }
+}
+
+// completes the state columns and target columns once the loads are consumed
+__device__ __forceinline__ void finish_cols(const ValueArgs &a, const RowInfo &ri, int q, float (&xv)[16],
+                                            float (&tv)[16])
+{
+    const bool has = ri.kind == 0 || ri.kind == 1;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int c = 16 * q + j;
+        if (c < kMarket) {
+            if (!has) xv[j] = 0.f;
+            if (ri.kind != 0) tv[j] = 0.f;
+        } else if (c == kMarket) {
+            xv[j] = has ? ri.vin : 0.f;
+            tv[j] = ri.vpost;
+        } else if (c == kMarket + 1) {
+            xv[j] = has ? ri.ein : 0.f;
+            tv[j] = ri.epost;
+        } else if (c == kMarket + 2) {
+            xv[j] = has ? a.env.spread : 0.f;
+            tv[j] = a.env.spread;
+        } else {
+            xv[j] = 0.f;
+            tv[j] = 0.f;
+        }
     }
 }
 
@@ -423,9 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         };
 
         long long tile = blockIdx.x;
-        RowInfo nri = decode_row(a, tile * 128 + r);
+        RowFetch nf;
+        issue_meta(a, tile * 128 + r, nf);
+        RowInfo nri = resolve(a, nf);
         float nx[16], nt[16];
-        load_row_cols(a, nri, q, nx, nt);
+        issue_cols(a, nri, q, nx, nt);
+        finish_cols(a, nri, q, nx, nt);
         build_x(nri, nx);
 
         for (; tile < n_tiles && ok; tile += gridDim.x) {
@@ -435,10 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             for (int j = 0; j < 16; ++j) tv[j] = nt[j];
             const long long next = tile + gridDim.x;
             const bool has_next = next < n_tiles;
-            if (has_next) {                                // prefetch one tile ahead
-                nri = decode_row(a, next * 128 + r);
-                load_row_cols(a, nri, q, nx, nt);
-            }
+            if (has_next) issue_meta(a, next * 128 + r, nf);   // stage 1 of the next tile's rows
             // ---- curiosity layer 1: state part from TMEM, one-hot column gathered
             wait_acc(&B.acc_cur, ph_cur);
             {
@@ -479,6 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 drain16(lane_addr + kColD1 + 64 * (c & 1), bias + kB1 + 64 * c + 16 * q, slots + (c & 1) * kSlot, r, q);
                 publish(&B.act_h1[c & 1]);
             }
+            // stage 2 of the next tile's rows: its metadata has arrived by now
+            if (has_next) {
+                nri = resolve(a, nf);
+                issue_cols(a, nri, q, nx, nt);
+            }
             // ---- layer 2 -> h2, chunks 4,5 first (their TMEM columns become layer 3's)
             wait_acc(&B.acc_main, ph_main);
             for (int kk = 0; kk < 6; ++kk) {
@@ -499,7 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 publish(&B.act_h4[k]);
             }
             // ---- next tile's state row (slot 4 and TMEM [0,128) are free now)
-            if (has_next) build_x(nri, nx);
+            if (has_next) {
+                finish_cols(a, nri, q, nx, nt);
+                build_x(nri, nx);
+            }
             // ---- layer 5 + scalar head
             wait_acc(&B.acc_main, ph_main);
             {

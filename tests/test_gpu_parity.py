@@ -35,7 +35,7 @@ def _sample(N, k, seed=0):
 
 # ------------------------------------------------------------------ small, several tiles, ragged tails
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "reset_heavy_bf16"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "scaleout_tf32", "reset_heavy_bf16", "ceiling_bf16"])
 @pytest.mark.parametrize("N,L", [(130, 37), (1, 1), (1, 2), (129, 3), (33, 130)])
 def test_small_shapes_match_oracle(name, N, L):
     w = wl.WORKLOADS[name]
@@ -47,7 +47,8 @@ def test_small_shapes_match_oracle(name, N, L):
 
 # ------------------------------------------------------------------ full workload sizes, sampled episodes
 
-@pytest.mark.parametrize("name,k", [("tiny_fp32", 32), ("default_fp32", 16), ("reset_heavy_bf16", 12)])
+@pytest.mark.parametrize("name,k", [("tiny_fp32", 32), ("default_fp32", 16), ("scaleout_tf32", 12),
+                                    ("reset_heavy_bf16", 12), ("ceiling_bf16", 8)])
 def test_workload_matches_oracle(name, k):
     w = wl.WORKLOADS[name]
     inp = wl.generate(w)
