@@ -179,7 +179,6 @@ template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a, UmmaWeights w, uint8_t *scratch,
                                                                     long long scratch_per_cta)
 {
-    constexpr int KC = Geo<BF16>::KC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *ring = sm;
