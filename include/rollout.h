@@ -164,6 +164,43 @@ ROLLOUT_API int rollout_status(rollout_handle *h);
 ROLLOUT_API int rollout_set_timing(rollout_handle *h, int on);
 ROLLOUT_API int rollout_phase_ms(rollout_handle *h, float *ms);
 
+/*
+ * rollout_run_static -- rollout_run for callers that cannot allocate device
+ * memory.  (An addition of this library; the paper has no counterpart.)
+ *
+ * Who needs it: code that must not call cudaMalloc -- a path that runs while
+ * a CUDA graph is being captured, a latency-critical loop that must never
+ * block on the device allocator, or a host that hands the library a fixed
+ * device-memory budget at start-up and forbids later allocations.  The tf32
+ * and widened-critic configurations run their value phase with per-CTA
+ * activation scratch; rollout_run takes it from memory rollout_create
+ * allocated, this entry point takes it from a fixed array compiled into the
+ * library (ROLLOUT_STATIC_SCRATCH_BYTES, 16 MiB), and it allocates nothing
+ * itself.  Every GPU that loads the library holds that array until the
+ * process exits.  Other configurations use no scratch and run exactly as
+ * rollout_run.
+ *
+ * Same arguments, results, stream ordering and return codes as
+ * rollout_run, plus ROLLOUT_ERR_UNSUPPORTED when the handle's layer shapes
+ * need more scratch per CTA than the array holds.  The value phase then runs
+ * on at most ROLLOUT_STATIC_SCRATCH_BYTES / (scratch per CTA) CTAs, so it is
+ * slower than rollout_run for large batches.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture on that device.  All calls share the one array, which keeps
+ * the last call's contents (nothing in it has to start at zero: every tile
+ * writes its activations before reading them): calls that overlap on the
+ * GPU -- on different streams, handles or host threads -- race on it and
+ * must be serialised by the caller.
+ */
+#define ROLLOUT_STATIC_SCRATCH_BYTES (16u << 20)
+ROLLOUT_API int rollout_run_static(rollout_handle *h, const float *features, const int32_t *episode_starts,
+                                   const uint32_t *seeds, int N, int L, float gamma, float lambda,
+                                   float *out_states, int32_t *out_actions, float *out_logp, float *out_values,
+                                   float *out_rewards, int32_t *out_dones, float *out_adv, float *out_ret,
+                                   void *stream);
+
 /* rollout_destroy -- free the handle and its device memory (NULL is a no-op).
  * Synchronises the device first. */
 ROLLOUT_API void rollout_destroy(rollout_handle *h);

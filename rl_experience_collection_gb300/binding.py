@@ -25,7 +25,7 @@ ROLLOUT_ERR_NOMEM = -6
 DTYPE = {"fp32": 0, "tf32": 1, "bf16": 2}
 
 EXPORTS = ["rollout_create", "rollout_set_weights", "rollout_run", "rollout_status", "rollout_destroy",
-           "rollout_last_error", "rollout_set_timing", "rollout_phase_ms"]
+           "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static"]
 
 
 class RolloutDims(C.Structure):
@@ -66,6 +66,8 @@ def lib(path: Optional[str] = None):
     L.rollout_run.restype = C.c_int
     L.rollout_run.argtypes = [vp, vp, vp, vp, C.c_int, C.c_int, C.c_float, C.c_float,
                               vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.rollout_run_static.restype = C.c_int
+    L.rollout_run_static.argtypes = list(L.rollout_run.argtypes)
     L.rollout_status.restype = C.c_int
     L.rollout_status.argtypes = [vp]
     L.rollout_destroy.restype = None
@@ -156,6 +158,20 @@ class Rollout:
                                  float(lam), p(out["states"]), p(out["actions"]), p(out["logp"]),
                                  p(out["values"]), p(out["rewards"]), p(out["dones"]), p(out["adv"]),
                                  p(out["ret"]), C.c_void_p(sh)))
+
+    def run_static(self, features, starts, seeds, N: int, L: int, gamma: float, lam: float,
+                   out: Dict[str, "torch.Tensor"], stream=None) -> None:
+        """rollout_run_static: same as run(), with the value phase's scratch taken
+        from the library's fixed device array instead of handle-owned memory."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        p = lambda t: C.c_void_p(t.data_ptr())
+        _check(lib().rollout_run_static(self._h, p(features), p(starts), p(seeds), int(N), int(L), float(gamma),
+                                        float(lam), p(out["states"]), p(out["actions"]), p(out["logp"]),
+                                        p(out["values"]), p(out["rewards"]), p(out["dones"]), p(out["adv"]),
+                                        p(out["ret"]), C.c_void_p(sh)))
 
     def run_raw(self, ptrs, N: int, L: int, gamma: float, lam: float, stream_handle: int = 0) -> int:
         """Raw-pointer form (integers), returns the status code instead of raising."""

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -346,6 +347,109 @@ int rollout_run(rollout_handle *h, const float *features, const int32_t *episode
         } else {
             e = launch_value_umma(va, h->umma, s);
         }
+        if (e != cudaSuccess) return cuda_fail(e, "value launch");
+    }
+    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
+    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    h->timed_run = h->timing;
+    return ROLLOUT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant (rollout_run_static): the generic value kernel's
+// per-CTA activation scratch comes from this fixed device array instead of
+// memory allocated by rollout_create.  Its device address is looked up once
+// per device, with that device current, and cached.
+static __device__ __align__(256) uint8_t g_static_scratch[ROLLOUT_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+uint8_t *g_static_ptr[kMaxDevices] = {};
+
+int static_scratch(int dev, uint8_t **out)
+{
+    if (dev < 0 || dev >= kMaxDevices) return fail(ROLLOUT_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_static_ptr[dev] = (uint8_t *)p;
+    }
+    *out = g_static_ptr[dev];
+    return ROLLOUT_OK;
+}
+
+}  // namespace
+
+int rollout_run_static(rollout_handle *h, const float *features, const int32_t *episode_starts, const uint32_t *seeds,
+                       int N, int L, float gamma, float lambda, float *out_states, int32_t *out_actions,
+                       float *out_logp, float *out_values, float *out_rewards, int32_t *out_dones, float *out_adv,
+                       float *out_ret, void *stream)
+{
+    g_err[0] = 0;
+    if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
+    const void *ptrs[] = {features, episode_starts, seeds, out_states, out_actions, out_logp,
+                          out_values, out_rewards, out_dones, out_adv, out_ret};
+    for (const void *p : ptrs) {
+        if (!p) return fail(ROLLOUT_ERR_INVALID, "null array argument");
+        if (((uintptr_t)p & 15u) != 0) return fail(ROLLOUT_ERR_INVALID, "array arguments must be 16-byte aligned");
+    }
+    if (N <= 0 || L <= 0) return fail(ROLLOUT_ERR_INVALID, "N and L must be positive (N=%d, L=%d)", N, L);
+    if ((long long)L > (long long)h->dims.n_bars - 1)
+        return fail(ROLLOUT_ERR_INVALID, "L=%d needs at least L+1 bars (n_bars=%d)", L, h->dims.n_bars);
+    if ((long long)N * L * kState >= (1LL << 40))
+        return fail(ROLLOUT_ERR_INVALID, "N*L too large");
+    if (!(gamma >= 0.f && gamma <= 1.f) || !(lambda >= 0.f && lambda <= 1.f))
+        return fail(ROLLOUT_ERR_INVALID, "gamma and lambda must lie in [0, 1]");
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != h->device) return fail(ROLLOUT_ERR_INVALID, "current device %d is not the handle's device %d", dev, h->device);
+
+    const rollout_dims &d = h->dims;
+    const bool scratch = d.dtype != ROLLOUT_FP32 && value_needs_scratch(h->umma);
+    uint8_t *sp = nullptr;
+    int grid = 0;
+    long long per_cta = 0;
+    if (scratch) {
+        per_cta = value_generic_scratch_per_cta(h->umma);
+        if (per_cta > (long long)ROLLOUT_STATIC_SCRATCH_BYTES)
+            return fail(ROLLOUT_ERR_UNSUPPORTED, "these layer shapes need %lld bytes of scratch per CTA, more than "
+                        "the %u-byte static array", per_cta, (unsigned)ROLLOUT_STATIC_SCRATCH_BYTES);
+        int rc = static_scratch(dev, &sp);
+        if (rc) return rc;
+        int sms = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        const long long fit = (long long)ROLLOUT_STATIC_SCRATCH_BYTES / per_cta;
+        const long long tiles = ((long long)N * L + N + 127) / 128;
+        long long g = tiles < sms ? tiles : sms;
+        grid = (int)(g < fit ? g : fit);
+    }
+    h->last_stream = s;
+    if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    EnvConst env{d.barrier, d.max_hold, d.pt_scale, d.sl_scale, d.div_window, d.div_thresh, d.div_penalty,
+                 d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div_low};
+    Phase1Args p1{features, episode_starts, seeds, N, L, d.n_bars, out_actions, out_logp, out_dones,
+                  out_rewards, out_values, out_adv, h->d_status, env};
+    ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_states, out_values,
+                 out_adv, out_rewards, out_ret, h->d_status, env};
+    GaeArgs ga{out_rewards, out_values, out_dones, out_adv, out_ret, N, L, gamma, lambda};
+    auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
+    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (d.dtype == ROLLOUT_FP32) {
+        if ((e = launch_phase1_simt(p1, h->d_actor_packed, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
+        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = launch_value_simt(va, h->simt, s)) != cudaSuccess) return cuda_fail(e, "value launch");
+    } else {
+        if ((e = launch_phase1_umma(p1, h->umma, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
+        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        e = scratch ? launch_value_generic(va, h->umma, sp, per_cta, grid, s) : launch_value_umma(va, h->umma, s);
         if (e != cudaSuccess) return cuda_fail(e, "value launch");
     }
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
