@@ -241,9 +241,10 @@ def main():
     pk = peaks()
     flop_step, flop_value = path_flops(w, N, L)
     tpk, tpk_name = tensor_peak(w.dtype, pk)
-    value_ms = statistics.mean(p[1] for p in phase)
     rollout_ms = statistics.mean(p[0] for p in phase)
-    gae_ms = statistics.mean(p[2] for p in phase)
+    states_ms = statistics.mean(p[1] for p in phase)
+    value_ms = statistics.mean(p[2] for p in phase)
+    gae_ms = statistics.mean(p[3] for p in phase)
     achieved = flop_value / (value_ms / 1000.0) / 1e12
     roofline = {"kernel": "value (critic + curiosity, tcgen05)", "bound": "tensor", "achieved": achieved,
                 "peak": tpk, "unit": "TFLOP/s", "frac": (achieved / tpk) if tpk else None, "traffic": None,
@@ -256,8 +257,8 @@ def main():
                        "critic": list(w.critic_h), "l2": "flushed between steps (512 MB write)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "tensor_pipe_frac_step": (flop_step / (ms / 1000.0) / 1e12 / tpk) if tpk else None,
-            "phase_ms": {"rollout": rollout_ms, "value": value_ms, "gae": gae_ms},
-            "roofline": roofline, "clocks": clk.summary(), "gpu_launches": 3 * args.steps}
+            "phase_ms": {"rollout": rollout_ms, "states": states_ms, "value": value_ms, "gae": gae_ms},
+            "roofline": roofline, "clocks": clk.summary(), "gpu_launches": 4 * args.steps}
 
     # ---------------- end to end through the C ABI with host buffers
     if not args.no_e2e:

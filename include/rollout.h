@@ -156,10 +156,10 @@ ROLLOUT_API int rollout_status(rollout_handle *h);
 /*
  * rollout_set_timing -- when on != 0, every later rollout_run also records
  * CUDA events on its stream before and after each of its kernels (rollout,
- * value, GAE); off by default.  rollout_phase_ms synchronises the last run's
- * final event and writes the three kernels' device times in milliseconds to
- * ms[0..2].  Returns ROLLOUT_OK, _INVALID (timing was off or no run yet) or
- * _CUDA.
+ * state rows, value, GAE); off by default.  rollout_phase_ms synchronises the
+ * last run's final event and writes the four kernels' device times in
+ * milliseconds to ms[0..3].  Returns ROLLOUT_OK, _INVALID (timing was off or
+ * no run yet) or _CUDA.
  */
 ROLLOUT_API int rollout_set_timing(rollout_handle *h, int on);
 ROLLOUT_API int rollout_phase_ms(rollout_handle *h, float *ms);

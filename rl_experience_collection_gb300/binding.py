@@ -182,8 +182,8 @@ class Rollout:
         _check(lib().rollout_set_timing(self._h, int(on)))
 
     def phase_ms(self):
-        """Device milliseconds of the last run's rollout, value and GAE kernels."""
-        ms = (C.c_float * 3)()
+        """Device milliseconds of the last run's rollout, state-row, value and GAE kernels."""
+        ms = (C.c_float * 4)()
         _check(lib().rollout_phase_ms(self._h, ms))
         return [float(x) for x in ms]
 

@@ -33,9 +33,10 @@ int cuda_fail(cudaError_t e, const char *what)
                 cudaGetErrorString(e));
 }
 
+// kernels of one run, timed when rollout_set_timing is on: rollout, state rows, value, GAE
+constexpr int kTimedKernels = 4;
+
 }  // namespace
-
-
 
 struct rollout_handle {
     rollout_dims dims;
@@ -59,7 +60,7 @@ struct rollout_handle {
     cudaStream_t last_stream = nullptr;
     // optional per-kernel timing
     bool timing = false, timed_run = false;
-    cudaEvent_t ev[4] = {};
+    cudaEvent_t ev[kTimedKernels + 1] = {};
 };
 
 namespace {
@@ -327,7 +328,8 @@ int rollout_run(rollout_handle *h, const float *features, const int32_t *episode
                  d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div_low};
     Phase1Args p1{features, episode_starts, seeds, N, L, d.n_bars, out_actions, out_logp, out_dones,
                   out_rewards, out_values, out_adv, h->d_status, env};
-    ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_states, out_values,
+    StatesArgs sa{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values, d.spread, out_states};
+    ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values,
                  out_adv, out_rewards, out_ret, h->d_status, env};
     GaeArgs ga{out_rewards, out_values, out_dones, out_adv, out_ret, N, L, gamma, lambda};
 
@@ -336,10 +338,14 @@ int rollout_run(rollout_handle *h, const float *features, const int32_t *episode
     if (d.dtype == ROLLOUT_FP32) {
         if ((e = launch_phase1_simt(p1, h->d_actor_packed, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
+        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         if ((e = launch_value_simt(va, h->simt, s)) != cudaSuccess) return cuda_fail(e, "value launch");
     } else {
         if ((e = launch_phase1_umma(p1, h->umma, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
+        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         if (value_needs_scratch(h->umma)) {
             const long long tiles = ((long long)N * L + N + 127) / 128;
             const int grid = (int)(tiles < h->scratch_ctas ? tiles : h->scratch_ctas);
@@ -349,9 +355,9 @@ int rollout_run(rollout_handle *h, const float *features, const int32_t *episode
         }
         if (e != cudaSuccess) return cuda_fail(e, "value launch");
     }
-    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
+    if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     h->timed_run = h->timing;
     return ROLLOUT_OK;
 }
@@ -437,7 +443,8 @@ int rollout_run_static(rollout_handle *h, const float *features, const int32_t *
                  d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div_low};
     Phase1Args p1{features, episode_starts, seeds, N, L, d.n_bars, out_actions, out_logp, out_dones,
                   out_rewards, out_values, out_adv, h->d_status, env};
-    ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_states, out_values,
+    StatesArgs sa{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values, d.spread, out_states};
+    ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values,
                  out_adv, out_rewards, out_ret, h->d_status, env};
     GaeArgs ga{out_rewards, out_values, out_dones, out_adv, out_ret, N, L, gamma, lambda};
     auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
@@ -445,16 +452,20 @@ int rollout_run_static(rollout_handle *h, const float *features, const int32_t *
     if (d.dtype == ROLLOUT_FP32) {
         if ((e = launch_phase1_simt(p1, h->d_actor_packed, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
+        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         if ((e = launch_value_simt(va, h->simt, s)) != cudaSuccess) return cuda_fail(e, "value launch");
     } else {
         if ((e = launch_phase1_umma(p1, h->umma, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
+        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         e = scratch ? launch_value_generic(va, h->umma, sp, per_cta, grid, s) : launch_value_umma(va, h->umma, s);
         if (e != cudaSuccess) return cuda_fail(e, "value launch");
     }
-    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
+    if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     h->timed_run = h->timing;
     return ROLLOUT_OK;
 }
@@ -490,9 +501,9 @@ int rollout_phase_ms(rollout_handle *h, float *ms)
     g_err[0] = 0;
     if (!h || !ms) return fail(ROLLOUT_ERR_INVALID, "null argument");
     if (!h->timed_run) return fail(ROLLOUT_ERR_INVALID, "no timed run (call rollout_set_timing first)");
-    cudaError_t e = cudaEventSynchronize(h->ev[3]);
+    cudaError_t e = cudaEventSynchronize(h->ev[kTimedKernels]);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < kTimedKernels; ++i)
         if ((e = cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1])) != cudaSuccess)
             return cuda_fail(e, "cudaEventElapsedTime");
     return ROLLOUT_OK;

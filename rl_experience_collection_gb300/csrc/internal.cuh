@@ -68,13 +68,24 @@ struct ValueArgs {
     int N, L, n_bars;
     const int32_t *actions;
     const int32_t *dones;
-    float *states;             // [N, L, 54] written
     float *values;             // in: V entering the step; out: critic value
     const float *v_post;       // V' after the trade
     float *rewards;            // in: base reward; out: + curiosity bonus
     float *boot;               // out_ret: [n*L + L-1] receives the bootstrap value
     int *status;
     EnvConst env;
+};
+
+// the stored state rows (states.cu), written between the rollout and the value phase
+struct StatesArgs {
+    const float *F;
+    const int32_t *starts;
+    int N, L, n_bars;
+    const int32_t *actions;
+    const int32_t *dones;
+    const float *v_in;         // V entering each step (out_values before the value phase)
+    float spread;
+    float *states;             // [N, L, 54] written
 };
 
 struct GaeArgs {
@@ -96,6 +107,9 @@ struct SimtWeights {
 };
 cudaError_t launch_phase1_simt(const Phase1Args &a, const float *actor_packed, cudaStream_t s);
 cudaError_t launch_value_simt(const ValueArgs &a, const SimtWeights &w, cudaStream_t s);
+
+// --- state rows (states.cu) ---
+cudaError_t launch_states(const StatesArgs &a, cudaStream_t s);
 
 // --- GAE (gae.cu) ---
 cudaError_t launch_gae(const GaeArgs &a, cudaStream_t s);

@@ -9,8 +9,8 @@
 //
 // Phase 2 (value): tiles of rows (tuples) run the critic MLP
 // 54->512->384->256->128->64->1 (Phase A step 5), the curiosity model
-// (step 9, bonus = cur_coef * MSE against the pre-reset next state) and write
-// the state rows (step 11).  Every dense layer is out[j] = b[j] + sum_k in[k] *
+// (step 9, bonus = cur_coef * MSE against the pre-reset next state); the
+// stored state rows come from states.cu.  Every dense layer is out[j] = b[j] + sum_k in[k] *
 // W[j][k] with f32 accumulation in k order (page "GPU Pipeline Phase 2b",
 // "Kernel Components" 1).
 #include "env.cuh"
@@ -259,7 +259,6 @@ __global__ void __launch_bounds__(kVThreads) value_simt_kernel(ValueArgs a, Simt
             }
             A[rr * LD + j] = x;
             T[rr * 56 + j] = tg;
-            if ((kind == 0 || kind == -2) && s_row[rr] >= 0) a.states[s_row[rr] * kState + j] = x;
         }
         __syncthreads();
         // curiosity: [x ; onehot(a)] -> 64 ReLU -> 54

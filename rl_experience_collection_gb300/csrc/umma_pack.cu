@@ -134,7 +134,7 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const 
     for (int l = 0; l < 5; ++l) { V[l] = hw + lo.c_w[l]; vin[l] = lo.c_in[l]; }
     const float *C1 = hw + lo.q_w[0], *C2 = hw + lo.q_w[1];
     if (bf16 && !wide) {
-        // value-kernel consumption order (see value_umma.cu)
+        // value-kernel consumption order (see value_umma.cu): 26 units of <= 32 KB
         begin_unit();
         P.tile(stream, C1, kCurH, kState + kActions, kState, 0, 64, 0);          // curiosity 1 (state part)
         P.tile(stream, V[0], 512, vin[0], vin[0], 0, 64, 0);                      // layer-1 chunk 0
@@ -143,8 +143,10 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const 
         end_unit();
         for (int i = 0; i < 8; ++i) {
             begin_unit();
-            P.tile(stream, V[1], 384, vin[1], vin[1], 0, 256, i);                // layer 2, K-chunk i
-            P.tile(stream, V[1], 384, vin[1], vin[1], 256, 128, i);
+            P.tile(stream, V[1], 384, vin[1], vin[1], 0, 256, i);                // layer 2, K-chunk i, rows 0-255
+            end_unit();
+            begin_unit();
+            P.tile(stream, V[1], 384, vin[1], vin[1], 256, 128, i);              // rows 256-383
             if (i + 2 < 8) P.tile(stream, V[0], 512, vin[0], vin[0], 64 * (i + 2), 64, 0);
             end_unit();
         }
@@ -154,11 +156,12 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const 
             P.tile(stream, V[2], 256, vin[2], vin[2], 0, 256, order3[kk]);       // layer 3
             end_unit();
         }
+        for (int h = 0; h < 2; ++h) {
+            begin_unit();
+            for (int k = 2 * h; k < 2 * h + 2; ++k) P.tile(stream, V[3], 128, vin[3], vin[3], 0, 128, k);  // layer 4
+            end_unit();
+        }
         begin_unit();
-        for (int k = 0; k < 3; ++k) P.tile(stream, V[3], 128, vin[3], vin[3], 0, 128, k);   // layer 4
-        end_unit();
-        begin_unit();
-        P.tile(stream, V[3], 128, vin[3], vin[3], 0, 128, 3);
         for (int k = 0; k < 2; ++k) P.tile(stream, V[4], 64, vin[4], vin[4], 0, 64, k);     // layer 5
         end_unit();
     } else {

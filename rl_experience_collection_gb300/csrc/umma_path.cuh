@@ -36,8 +36,8 @@ struct UmmaWeights {
     UmmaLayer job[kNumJobs];
     // bulk-copy units of the stream, in consumption order (one tile's worth)
     int n_units = 0;
-    long long unit_off[24] = {};
-    uint32_t unit_bytes[24] = {};
+    long long unit_off[32] = {};
+    uint32_t unit_bytes[32] = {};
     const float *vec = nullptr;  // biases, head weights, curiosity one-hot columns (f32)
     int head_w_off = 0;          // critic head weights [h5] (rounded to the operand format)
     int head_b_off = 0;          // critic head bias [1]

@@ -3,8 +3,8 @@
 // the widened critic 54->1024->768->512->256->128->1.
 //
 // Page "PPO CUDA Pipeline Design -- Zero-Roundtrip Experience Collection",
-// section "Kernel Phases", Phase A steps 5 (critic), 9 (curiosity, bonus =
-// cur_coef * MSE against the pre-reset next state) and 11 (state rows).
+// section "Kernel Phases", Phase A steps 5 (critic) and 9 (curiosity, bonus =
+// cur_coef * MSE against the pre-reset next state).
 //
 // Same roles as the bf16 kernel (16 row warps, a producer warp, an MMA warp;
 // M = 128 rows per tile, f32 accumulators in TMEM), but every activation --
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
         for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
             const RowInfoG ri = decode_g(a, tile * 128 + r);
             const bool has = ri.kind == 0 || ri.kind == 1;
-            // ---- state row: X buffer (operand) and out_states (f32)
+            // ---- state row: X buffer (operand)
             {
                 float xv[16];
 #pragma unroll
@@ -335,12 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                     xv[j] = x;
                 }
                 put16g<BF16>(bufs[kBufX], r, 16 * q, xv);
-                if ((ri.kind == 0 || ri.kind == 2) && 16 * q < kState) {
-                    float *dst = a.states + ri.row * kState + 16 * q;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (16 * q + j < kState) dst[j] = xv[j];
-                }
             }
             fence_async_global();
             mbar_arrive(&B.act);

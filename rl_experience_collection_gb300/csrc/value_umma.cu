@@ -2,9 +2,9 @@
 // 54->512->384->256->128->64->1 and curiosity (54+45)->64->54.
 //
 // Page "PPO CUDA Pipeline Design -- Zero-Roundtrip Experience Collection",
-// section "Kernel Phases", Phase A step 5 (critic), step 9 (curiosity
-// forward model; bonus = cur_coef * MSE against the pre-reset next state) and
-// step 11 (state rows); section "Weight Layout".
+// section "Kernel Phases", Phase A step 5 (critic) and step 9 (curiosity
+// forward model; bonus = cur_coef * MSE against the pre-reset next state);
+// section "Weight Layout".
 //
 // The critic and the curiosity model do not feed the state trajectory, so they
 // run here over every tuple at once instead of inside the serial step loop.
@@ -12,17 +12,19 @@
 // bootstrap row per episode: the pre-reset next state after the last step) and
 // runs every layer as M=128 tcgen05 MMAs with f32 accumulators in TMEM.
 //
-// Warp roles (18 warps):
+// Warp roles (20 warps):
 //   0-15  row warps: warp w serves TMEM lanes / rows 32*(w%4)..+31 and the
 //         column quarter w/4 of every 64-column chunk.  They build the state
-//         rows (A operand + out_states), drain TMEM chunk by chunk (bias, ReLU,
-//         bf16 rounding) into the next layer's swizzled A operand, and finish
-//         with the head dot product, the curiosity MSE and the stores.  The
-//         next tile's row data is prefetched into registers one tile ahead.
-//   16    producer: streams the weights (pre-swizzled on the host, grouped
-//         into units of <= 56 KB because a bulk copy costs a fixed ~0.27 us)
-//         from L2 with 1-D bulk TMA into a two-stage ring
-//   17    allocates TMEM; one lane issues the MMAs and commits
+//         rows (A operand), drain TMEM chunk by chunk (bias, ReLU, bf16
+//         rounding) into the next layer's swizzled A operand, and finish with
+//         the head dot product, the curiosity MSE and the stores.  The next
+//         tile's row metadata is loaded one tile ahead.
+//   16-18 producers: stream the weights (pre-swizzled on the host, grouped
+//         into 26 units of <= 32 KB per tile) from L2 with 1-D bulk TMA into a
+//         three-stage ring.  Producer s owns stage s and so waits on its empty
+//         barrier strictly in order; the bulk copies of one warp complete one
+//         after another, those of different warps overlap.
+//   19    allocates TMEM; one lane issues the MMAs and commits
 //
 // Per tile the MMA lane runs (TMEM columns in brackets):
 //   CUR1 [0,64) = X C1^T ; D1_0 [384,448), D1_1 [448,512) = X W1[chunk]^T
@@ -35,8 +37,13 @@
 // so layer 1 never exists whole (its 64-column chunks are produced while the
 // tensor pipe accumulates layer 2) and every later layer starts on its first
 // K-chunk while the rows still drain the rest of the previous one.
-// Shared-memory operand slots (128 rows x 128 B each): X -> 4, Z -> 5,
-// h1 chunks -> 0/1 (alternating), h2 -> 0..5, h3 -> 0..3, h4 -> 0..1.
+// Shared-memory operand slots (128 rows x 128 B each): X -> 2, Z -> 3,
+// h1 chunks -> 0/1 (alternating), h2 -> 0..5, h3 -> 0..3, h4 -> 0..1.  From
+// the end of layer 3 of the previous tile until the curiosity epilogue, slots
+// 4-5 hold the tile's market-feature rows: one bulk copy per episode the tile
+// touches (at most four), each a run of consecutive bars of the feature
+// matrix, so that X and the curiosity targets are built from shared memory
+// instead of gathering 204-byte rows thread by thread.
 // Every handoff has its own mbarrier (one phase per tile) so that no barrier
 // can complete twice before its waiter has seen the first completion.
 #include "env.cuh"
@@ -51,14 +58,20 @@ using namespace umma;
 
 constexpr int kRowWarps = 16;
 constexpr int kRowThreads = kRowWarps * 32;
-constexpr int kThreads = kRowThreads + 64;
+constexpr int kProducers = 3;            // one per ring stage
+constexpr int kProdWarp0 = kRowWarps, kMmaWarp = kRowWarps + kProducers;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kSlot = 128 * 128;
 constexpr int kNumSlots = 6;
-constexpr int kStage = 56 * 1024;
-constexpr int kStages = 2;
-constexpr int kXSlot = 4, kZSlot = 5;
+constexpr int kStage = 32 * 1024;
+constexpr int kStages = kProducers;
+constexpr int kUnits = 26;
+constexpr int kXSlot = 2, kZSlot = 3, kFeatSlot = 4;
+constexpr int kFeatFloats = 2 * kSlot / 4;      // feature staging area (slots 4-5): 8192 floats
+constexpr int kMaxSeg = 4;                      // episodes of one tile staged at most
 constexpr int kBiasFloats = 1600;
-constexpr int kSmem = kNumSlots * kSlot + kStages * kStage + kBiasFloats * 4 + 2 * 4 * 128 * 4 + 1024;
+constexpr int kOneHotFloats = kActions * kCurH;
+constexpr int kSmem = kNumSlots * kSlot + kStages * kStage + (kBiasFloats + kOneHotFloats) * 4 + 2 * 4 * 128 * 4 + 1024;
 static_assert(kSmem <= 232448, "value kernel shared memory");
 
 // bias block layout in shared memory (floats)
@@ -72,24 +85,113 @@ struct Bars {
     uint64_t full[kStages], empty[kStages];
     uint64_t act_x, act_z, act_h1[2], act_h2[6], act_h3[4], act_h4[2];
     uint64_t acc_cur, acc_d1[2], acc_main, final_;
+    uint64_t feat_full;        // the staged feature rows of the next tile have landed
+};
+
+// Where the feature rows of a tile's episodes sit in the staging area.
+// Segment j covers episode n0 + j: bars [lo, hi) of the feature matrix at
+// float offset soff; lo < 0 when the episode is not staged.
+struct SegTable {
+    long long n0;
+    int count;
+    int lo[kMaxSeg], hi[kMaxSeg], soff[kMaxSeg];
+};
+
+// the starts of the (up to kMaxSeg) episodes of the tile at r0, loaded early
+struct SegPre {
+    long long r0, n0;
+    int count;
+    int st[kMaxSeg];
 };
 
 __device__ __forceinline__ float bf16_round(float x) { return __uint_as_float(pack_bf16x2(0.f, x) & 0xFFFF0000u); }
 
+__device__ __forceinline__ void seg_prefetch(const ValueArgs &a, long long r0, SegPre &p)
+{
+    const long long NL = (long long)a.N * a.L;
+    p.r0 = r0;
+    p.n0 = 0;
+    p.count = 0;
+    if (r0 < NL) {
+        p.n0 = r0 / a.L;
+        const long long r_end = r0 + 128 < NL ? r0 + 128 : NL;
+        const long long n_last = (r_end - 1) / a.L;
+        p.count = (int)(n_last - p.n0 + 1 < kMaxSeg ? n_last - p.n0 + 1 : kMaxSeg);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxSeg; ++j) {
+        const long long n = p.n0 + j < a.N ? p.n0 + j : a.N - 1;
+        p.st[j] = __ldg(a.starts + n);
+    }
+}
+
+// One thread: lays the segments out, publishes the table and issues the
+// copies, completing `bar` with their bytes.  A segment starts on a bar that
+// is a multiple of 4 and spans a multiple of 4 bars (4 x 204 bytes = 816, a
+// multiple of 16, as a bulk copy requires); it covers the bars of the tile's
+// steps plus the next bar (the curiosity target) and never reaches past the
+// feature matrix.  Rows outside every segment are read from global memory.
+__device__ __forceinline__ void seg_issue(const ValueArgs &a, const SegPre &p, SegTable &T, float *area,
+                                          uint64_t *bar)
+{
+    const long long NL = (long long)a.N * a.L;
+    const long long r_end = p.r0 + 128 < NL ? p.r0 + 128 : NL;
+    int soff = 0;
+    uint32_t total = 0;
+    T.n0 = p.n0;
+    T.count = p.count;
+#pragma unroll
+    for (int j = 0; j < kMaxSeg; ++j) {
+        T.lo[j] = -1;
+        T.hi[j] = -1;
+        T.soff[j] = 0;
+        if (j >= p.count) continue;
+        const long long n = p.n0 + j, e0 = n * a.L;
+        const int ta = (int)((p.r0 > e0 ? p.r0 : e0) - e0);
+        const int tb = (int)((r_end < e0 + a.L ? r_end : e0 + a.L) - 1 - e0);
+        const int st = p.st[j];
+        if (!start_ok(st, a.L, a.n_bars)) continue;
+        const long long lo = ((long long)st + ta) & ~3LL;
+        long long hi = ((long long)st + tb + 2 + 3) & ~3LL;
+        if (hi > a.n_bars) hi = lo + (((long long)a.n_bars - lo) & ~3LL);
+        const int nb = (int)(hi - lo);
+        if (nb <= 0 || soff + nb * kMarket > kFeatFloats) continue;
+        T.lo[j] = (int)lo;
+        T.hi[j] = (int)hi;
+        T.soff[j] = soff;
+        soff += nb * kMarket;
+        total += (uint32_t)nb * kMarket * 4u;
+    }
+    mbar_arrive_expect_tx(bar, total);
+#pragma unroll
+    for (int j = 0; j < kMaxSeg; ++j)
+        if (T.lo[j] >= 0)
+            bulk_g2s(area + T.soff[j], a.F + (long long)T.lo[j] * kMarket,
+                     (uint32_t)(T.hi[j] - T.lo[j]) * kMarket * 4u, bar);
+}
+
+// float offset of bar `b` of episode n in the staging area, or -1
+__device__ __forceinline__ int staged_off(const SegTable &T, long long n, long long b)
+{
+    const long long j = n - T.n0;
+    if (j < 0 || j >= T.count) return -1;
+    const int lo = T.lo[j];
+    if (lo < 0 || b < lo || b >= T.hi[j]) return -1;
+    return T.soff[j] + (int)(b - lo) * kMarket;
+}
+
 struct RowInfo {
     int kind;            // 0 tuple, 1 bootstrap row, 2 tuple of an invalid episode, 3 bootstrap of one, -1 none
+    long long n;         // episode
     long long row;       // flat tuple index (kind 0/2) or the slot receiving the bootstrap value (kind 1/3)
     long long bar;       // bar of the state row
     int act;
     float vin, ein, vpost, epost;
 };
 
-// Row data is fetched in two non-blocking stages so that no thread stalls on
-// a global load while the tensor pipe waits for it:
-//   stage 1 (issue_meta): every load whose address depends only on the row
-//            index, issued unconditionally from clamped addresses;
-//   stage 2 (issue_cols): once those values have arrived (mid-tile), the
-//            row's kind/bar and the feature-row loads that depend on them.
+// Per-row metadata, loaded one tile ahead: every load's address depends only
+// on the row index (issued at the start of the previous tile, consumed in its
+// middle), so no thread stalls on them.
 struct RowFetch {
     long long r, row;          // flat row, tuple index / bootstrap slot
     int n, t, is_boot;         // episode, step, bootstrap row?
@@ -121,6 +223,7 @@ __device__ __forceinline__ RowInfo resolve(const ValueArgs &a, const RowFetch &f
     RowInfo ri{};
     const long long NL = (long long)a.N * a.L;
     const bool ok = start_ok(f.start, a.L, a.n_bars);
+    ri.n = f.n;
     ri.row = f.row;
     ri.act = f.act;
     if (f.r >= NL + a.N) {
@@ -142,48 +245,43 @@ __device__ __forceinline__ RowInfo resolve(const ValueArgs &a, const RowFetch &f
     return ri;
 }
 
-// issues the loads of the 16 market columns [16q, 16q+16) of the row's bar and
-// of the next bar (curiosity target); rows without a bar read bar 0 and are
-// masked by finish_cols, so that nothing here waits on a loaded value
-__device__ __forceinline__ void issue_cols(const ValueArgs &a, const RowInfo &ri, int q, float (&xv)[16],
-                                           float (&tv)[16])
+// state columns [16q, 16q+16) of the row: [F[bar], V, e, spread, 0...]
+__device__ __forceinline__ void state_cols(const ValueArgs &a, const RowInfo &ri, const SegTable &T,
+                                           const float *area, int q, float (&xv)[16])
 {
-    const float *fr = a.F + ri.bar * kMarket;
-    const float *fn = a.F + (ri.kind == 0 ? ri.bar + 1 : 0) * kMarket;
+    const bool has = ri.kind == 0 || ri.kind == 1;
+    const int off = ri.kind == 0 ? staged_off(T, ri.n, ri.bar) : -1;
+    const float *src = off >= 0 ? area + off : a.F + ri.bar * kMarket;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int c = 16 * q + j;
-        if (c < kMarket) {
-            xv[j] = __ldg(fr + c);
-            tv[j] = __ldg(fn + c);
+        float x = 0.f;
+        if (has) {
+            if (c < kMarket) x = src[c];
+            else if (c == kMarket) x = ri.vin;
+            else if (c == kMarket + 1) x = ri.ein;
+            else if (c == kMarket + 2) x = a.env.spread;
         }
+        xv[j] = x;
     }
 }
 
-// completes the state columns and target columns once the loads are consumed
-__device__ __forceinline__ void finish_cols(const ValueArgs &a, const RowInfo &ri, int q, float (&xv)[16],
-                                            float (&tv)[16])
+// curiosity target columns [16q, 16q+16): the pre-reset next state
+// [F[bar+1], V', e', spread] (used for tuples only)
+__device__ __forceinline__ void target_cols(const ValueArgs &a, const RowInfo &ri, const SegTable &T,
+                                            const float *area, int q, float (&tv)[16])
 {
-    const bool has = ri.kind == 0 || ri.kind == 1;
+    const int off = ri.kind == 0 ? staged_off(T, ri.n, ri.bar + 1) : -1;
+    const float *src = off >= 0 ? area + off : a.F + (ri.kind == 0 ? ri.bar + 1 : 0) * kMarket;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int c = 16 * q + j;
-        if (c < kMarket) {
-            if (!has) xv[j] = 0.f;
-            if (ri.kind != 0) tv[j] = 0.f;
-        } else if (c == kMarket) {
-            xv[j] = has ? ri.vin : 0.f;
-            tv[j] = ri.vpost;
-        } else if (c == kMarket + 1) {
-            xv[j] = has ? ri.ein : 0.f;
-            tv[j] = ri.epost;
-        } else if (c == kMarket + 2) {
-            xv[j] = has ? a.env.spread : 0.f;
-            tv[j] = a.env.spread;
-        } else {
-            xv[j] = 0.f;
-            tv[j] = 0.f;
-        }
+        float x = 0.f;
+        if (c < kMarket) x = ri.kind == 0 ? src[c] : 0.f;
+        else if (c == kMarket) x = ri.vpost;
+        else if (c == kMarket + 1) x = ri.epost;
+        else if (c == kMarket + 2) x = a.env.spread;
+        tv[j] = x;
     }
 }
 
@@ -235,7 +333,7 @@ __device__ __forceinline__ void drain16(uint32_t taddr, const float *bias, uint8
 
 __device__ __forceinline__ void row_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory"); }
 
-// arrive after this thread's generic-proxy smem writes and TMEM reads
+// arrive after this thread's generic-proxy smem accesses and TMEM reads
 __device__ __forceinline__ void publish(uint64_t *bar)
 {
     fence_async_smem();
@@ -272,8 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
     uint8_t *slots = sm;
     uint8_t *ring = sm + kNumSlots * kSlot;
     float *bias = reinterpret_cast<float *>(ring + kStages * kStage);
-    float *part = bias + kBiasFloats;                    // [2][4][128] partial sums
+    float *onehot = bias + kBiasFloats;                  // curiosity layer-1 one-hot columns [45][64]
+    float *part = onehot + kOneHotFloats;                // [2][4][128] partial sums
+    float *feat = reinterpret_cast<float *>(slots + kFeatSlot * kSlot);
     __shared__ __align__(8) Bars B;
+    __shared__ SegTable seg;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
 
@@ -295,9 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         mbar_init(&B.acc_d1[1], 1);
         mbar_init(&B.acc_main, 1);
         mbar_init(&B.final_, 1);
+        mbar_init(&B.feat_full, 1);
         fence_mbar_init();
     }
-    // biases and head weights (f32; the head weights are already bf16-rounded)
+    // biases, head weights and one-hot columns (f32; the latter two already bf16-rounded)
     {
         const float *vec = w.vec;
         for (int i = tid; i < kBiasFloats; i += kThreads) {
@@ -313,8 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             else if (i >= kC2B && i < kC2B + 64) v = vec[w.job[kJobCur2].bias_off + i - kC2B];
             bias[i] = v;
         }
+        for (int i = tid; i < kOneHotFloats; i += kThreads) onehot[i] = vec[w.onehot_off + i];
     }
-    if (warp == kRowWarps + 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
@@ -327,34 +430,33 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
     const long long total = (long long)a.N * a.L + a.N;
     const long long n_tiles = (total + 127) / 128;
 
-    if (warp == kRowWarps) {
-        // ------------------------------------------------------------ producer
+    if (warp >= kProdWarp0 && warp < kMmaWarp) {
+        // ------------------------------------------------------------ producers
+        const int ps = warp - kProdWarp0;             // the ring stage this warp fills
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            uint32_t k = 0;                            // uses of stage ps so far
+            long long g = 0;                           // unit counter over all tiles: unit g goes to stage g % kStages
             bool ok = true;
             for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                for (int u = 0; u < w.n_units && ok; ++u) {
+                for (int u = 0; u < kUnits && ok; ++u, ++g) {
+                    if (g % kStages != ps) continue;
                     const uint32_t bytes = w.unit_bytes[u];
-                    ok = mbar_wait(&B.empty[stage], phase ^ 1u, abort);
+                    ok = mbar_wait(&B.empty[ps], (k & 1u) ^ 1u, abort);   // release of the previous use
                     if (!ok) break;
-                    mbar_arrive_expect_tx(&B.full[stage], bytes);
-                    bulk_g2s(ring + stage * kStage, w.stream + w.unit_off[u], bytes, &B.full[stage]);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    mbar_arrive_expect_tx(&B.full[ps], bytes);
+                    bulk_g2s(ring + ps * kStage, w.stream + w.unit_off[u], bytes, &B.full[ps]);
+                    ++k;
                 }
             }
-            // every issued copy has landed once the MMA lane has released its stage
-            for (int s = 0; s < kStages && ok; ++s) {
-                ok = mbar_wait(&B.empty[stage], phase ^ 1u, abort);
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
-            }
+            // the last copy into this stage has landed once the MMA lane has released it
+            if (ok && k > 0) ok = mbar_wait(&B.empty[ps], (k - 1) & 1u, abort);
             if (!ok) {   // aborted: give copies already issued time to land (bounded)
                 const long long c0 = clock64();
                 while (clock64() - c0 < 4000000) { }
             }
         }
         __syncwarp();
-    } else if (warp == kRowWarps + 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             MmaCtx m{tmem, smem_u32(slots), abort, true};
@@ -385,14 +487,16 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 m.mma_chunk(kColCur2, m.slot(kZSlot), u + 24576, 64, false);
                 mma_commit(&B.acc_cur);
                 release();
-                // ---- layer 2 over the h1 chunks, layer-1 chunks two ahead
+                // ---- layer 2 over the h1 chunks (two units per K-chunk), layer-1 chunks two ahead
                 for (int i = 0; i < 8; ++i) {
                     u = take();
                     m.wait(&B.act_h1[i & 1], ph_h1[i & 1]);
                     m.mma_chunk(kColD2, m.slot(i & 1), u, 256, i > 0);
-                    m.mma_chunk(kColD2 + 256, m.slot(i & 1), u + 32768, 128, i > 0);
+                    release();
+                    u = take();
+                    m.mma_chunk(kColD2 + 256, m.slot(i & 1), u, 128, i > 0);
                     if (i + 2 < 8) {
-                        m.mma_chunk(kColD1 + 64 * (i & 1), m.slot(kXSlot), u + 49152, 64, false);
+                        m.mma_chunk(kColD1 + 64 * (i & 1), m.slot(kXSlot), u + 16384, 64, false);
                         mma_commit(&B.acc_d1[i & 1]);
                     }
                     release();
@@ -407,21 +511,21 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                     release();
                 }
                 mma_commit(&B.acc_main);
-                // ---- layer 4 (unit: K0..K2; next unit: K3 + layer 5)
-                u = take();
-                for (int k = 0; k < 3; ++k) {
-                    m.wait(&B.act_h3[k], ph_h3[k]);
-                    m.mma_chunk(kColD4, m.slot(k), u + 16384 * k, 128, k > 0);
+                // ---- layer 4 (two units of two K-chunks)
+                for (int h = 0; h < 2; ++h) {
+                    u = take();
+                    for (int k = 2 * h; k < 2 * h + 2; ++k) {
+                        m.wait(&B.act_h3[k], ph_h3[k]);
+                        m.mma_chunk(kColD4, m.slot(k), u + 16384 * (k - 2 * h), 128, k > 0);
+                    }
+                    if (h == 1) mma_commit(&B.acc_main);
+                    release();
                 }
-                release();
-                u = take();
-                m.wait(&B.act_h3[3], ph_h3[3]);
-                m.mma_chunk(kColD4, m.slot(3), u, 128, true);
-                mma_commit(&B.acc_main);
                 // ---- layer 5
+                u = take();
                 for (int k = 0; k < 2; ++k) {
                     m.wait(&B.act_h4[k], ph_h4[k]);
-                    m.mma_chunk(kColD5, m.slot(k), u + 16384 + 8192 * k, 64, k > 0);
+                    m.mma_chunk(kColD5, m.slot(k), u + 8192 * k, 64, k > 0);
                 }
                 mma_commit(&B.acc_main);
                 release();
@@ -437,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         const int r = 32 * (warp & 3) + lane;                 // operand row / TMEM lane
         const int q = warp >> 2;                               // column quarter of every 64-col chunk
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * q;
-        uint32_t ph_cur = 0, ph_d1[2] = {0, 0}, ph_main = 0;
+        uint32_t ph_cur = 0, ph_d1[2] = {0, 0}, ph_main = 0, ph_feat = 0;
         bool ok = true;
         auto wait_acc = [&](uint64_t *bar, uint32_t &phase) {
             ok = __all_sync(0xffffffffu, ok && mbar_wait(bar, phase, abort));
@@ -445,46 +549,45 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             tc_fence_after();
         };
         float *part_v = part, *part_s = part + 4 * 128;
-        auto build_x = [&](const RowInfo &ri, const float (&xv)[16]) {
+        SegPre pre;                                            // thread 0 only
+        auto build_x = [&](const RowInfo &ri) {
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(&B.feat_full, ph_feat, abort));
+            ph_feat ^= 1u;
+            float xv[16];
+            state_cols(a, ri, seg, feat, q, xv);
             put16(slots + kXSlot * kSlot, r, q, xv);
-            if ((ri.kind == 0 || ri.kind == 2) && 16 * q < kState) {
-                float2 *dst = reinterpret_cast<float2 *>(a.states + ri.row * kState + 16 * q);
-                const int n2 = (16 * q + 16 <= kState) ? 8 : (kState - 16 * q) / 2;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (j < n2) dst[j] = make_float2(xv[2 * j], xv[2 * j + 1]);
-            }
             publish(&B.act_x);
         };
 
         long long tile = blockIdx.x;
         RowFetch nf;
         issue_meta(a, tile * 128 + r, nf);
+        if (tid == 0) {
+            seg_prefetch(a, tile * 128, pre);
+            seg_issue(a, pre, seg, feat, &B.feat_full);
+        }
         RowInfo nri = resolve(a, nf);
-        float nx[16], nt[16];
-        issue_cols(a, nri, q, nx, nt);
-        finish_cols(a, nri, q, nx, nt);
-        build_x(nri, nx);
+        build_x(nri);
 
         for (; tile < n_tiles && ok; tile += gridDim.x) {
             const RowInfo ri = nri;
-            float tv[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) tv[j] = nt[j];
             const long long next = tile + gridDim.x;
             const bool has_next = next < n_tiles;
-            if (has_next) issue_meta(a, next * 128 + r, nf);   // stage 1 of the next tile's rows
+            if (has_next) {                                    // consumed in the middle / at the end of this tile
+                issue_meta(a, next * 128 + r, nf);
+                if (tid == 0) seg_prefetch(a, next * 128, pre);
+            }
             // ---- curiosity layer 1: state part from TMEM, one-hot column gathered
             wait_acc(&B.acc_cur, ph_cur);
             {
                 float v[16];
                 tmem_ld16(lane_addr + kColCur1, v);
                 const int act = (ri.act >= 0 && ri.act < kActions) ? ri.act : 0;
-                const float4 *oh = reinterpret_cast<const float4 *>(w.vec + w.onehot_off + act * kCurH + 16 * q);
+                const float4 *oh = reinterpret_cast<const float4 *>(onehot + act * kCurH + 16 * q);
                 const float4 *b4 = reinterpret_cast<const float4 *>(bias + kC1B + 16 * q);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float4 o = __ldg(oh + k), b = b4[k];
+                    const float4 o = oh[k], b = b4[k];
                     v[4 * k + 0] = fmaxf((v[4 * k + 0] + o.x) + b.x, 0.f);
                     v[4 * k + 1] = fmaxf((v[4 * k + 1] + o.y) + b.y, 0.f);
                     v[4 * k + 2] = fmaxf((v[4 * k + 2] + o.z) + b.z, 0.f);
@@ -496,6 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             // ---- curiosity layer 2: squared error against the pre-reset next state
             wait_acc(&B.acc_cur, ph_cur);
             {
+                float tv[16];
+                target_cols(a, ri, seg, feat, q, tv);
                 float v[16];
                 tmem_ld16(lane_addr + kColCur2, v);
                 float se = 0.f;
@@ -514,11 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 drain16(lane_addr + kColD1 + 64 * (c & 1), bias + kB1 + 64 * c + 16 * q, slots + (c & 1) * kSlot, r, q);
                 publish(&B.act_h1[c & 1]);
             }
-            // stage 2 of the next tile's rows: its metadata has arrived by now
-            if (has_next) {
-                nri = resolve(a, nf);
-                issue_cols(a, nri, q, nx, nt);
-            }
+            if (has_next) nri = resolve(a, nf);                // the next tile's metadata has arrived
             // ---- layer 2 -> h2, chunks 4,5 first (their TMEM columns become layer 3's)
             wait_acc(&B.acc_main, ph_main);
             for (int kk = 0; kk < 6; ++kk) {
@@ -526,8 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 drain16(lane_addr + kColD2 + 64 * k, bias + kB2 + 64 * k + 16 * q, slots + k * kSlot, r, q);
                 publish(&B.act_h2[k]);
             }
-            // ---- layer 3 -> h3
+            // ---- layer 3 -> h3 (layer 3 has read slots 4-5: stage the next tile's features there)
             wait_acc(&B.acc_main, ph_main);
+            if (has_next && tid == 0) seg_issue(a, pre, seg, feat, &B.feat_full);
             for (int k = 0; k < 4; ++k) {
                 drain16(lane_addr + kColD3 + 64 * k, bias + kB3 + 64 * k + 16 * q, slots + k * kSlot, r, q);
                 publish(&B.act_h3[k]);
@@ -538,11 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 drain16(lane_addr + kColD4 + 64 * k, bias + kB4 + 64 * k + 16 * q, slots + k * kSlot, r, q);
                 publish(&B.act_h4[k]);
             }
-            // ---- next tile's state row (slot 4 and TMEM [0,128) are free now)
-            if (has_next) {
-                finish_cols(a, nri, q, nx, nt);
-                build_x(nri, nx);
-            }
+            // ---- next tile's state row (slot 2 and TMEM [0,128) are free now)
+            if (has_next) build_x(nri);
             // ---- layer 5 + scalar head
             wait_acc(&B.acc_main, ph_main);
             {
@@ -574,19 +673,25 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             }
             row_sync();
         }
+        // an abort can leave a feature copy in flight: give it time to land (bounded)
+        if (!ok && tid == 0) {
+            const long long c0 = clock64();
+            while (clock64() - c0 < 4000000) { }
+        }
     }
     if (abort_sh && tid == 0) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kRowWarps + 1) tmem_dealloc(tmem, 512);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
 
 cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s)
 {
-    if (!w.bf16 || w.wide || w.n_units != 17) return cudaErrorNotSupported;
+    if (!w.bf16 || w.wide || w.n_units != kUnits) return cudaErrorNotSupported;
+    if ((reinterpret_cast<uintptr_t>(a.F) & 15u) != 0) return cudaErrorInvalidValue;   // feature copies
     for (int u = 0; u < w.n_units; ++u)
         if (w.unit_bytes[u] > (uint32_t)kStage || (w.unit_bytes[u] & 15u) || (w.unit_off[u] & 15)) return cudaErrorInvalidValue;
     static bool attr = false;
