@@ -14,6 +14,7 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -169,11 +170,16 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS))
     ap.add_argument("--ref-episodes", type=int, default=2, help="oracle episodes per reference step")
     ap.add_argument("--cpu-episodes", type=int, default=12, help="oracle episodes for cpu_baseline")
+    ap.add_argument("--episodes", type=int, default=None,
+                    help="override the workload's episode count (a smaller case for profiling)")
+    ap.add_argument("--horizon", type=int, default=None, help="override the workload's horizon")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = wl.WORKLOADS[args.workload]
+    if args.episodes or args.horizon:
+        w = dataclasses.replace(w, n_episodes=args.episodes or w.n_episodes, horizon=args.horizon or w.horizon)
 
     rank, world, dist = dist_setup()
     if args.impl == "reference":

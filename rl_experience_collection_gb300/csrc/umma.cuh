@@ -227,6 +227,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// max(x, 0) of both values rounded to bf16 and packed (the rounding commutes
+// with the clamp, so this equals rounding relu(x))
+__device__ __forceinline__ uint32_t pack_bf16x2_relu(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // byte offset of 16-byte unit u of row r inside a swizzled K-chunk tile
 __device__ __forceinline__ uint32_t sw128_offset(int r, int u)
 {

@@ -175,6 +175,15 @@ __device__ __forceinline__ RowInfoG decode_g(const ValueArgs &a, long long r)
     return ri;
 }
 
+// one arrival per warp once every lane has passed its fences (the barriers
+// count warps: per-thread arrivals on one barrier serialise in the
+// shared-memory atomic unit)
+__device__ __forceinline__ void warp_arrive(uint64_t *bar)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a, UmmaWeights w, uint8_t *scratch,
                                                                     long long scratch_per_cta)
@@ -199,10 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
             mbar_init(&B.full[s], 1);
             mbar_init(&B.empty[s], 1);
         }
-        mbar_init(&B.act, kRowThreads);
+        mbar_init(&B.act, kRowWarps);
         for (int h = 0; h < 2; ++h) {
             mbar_init(&B.acc[h], 1);
-            mbar_init(&B.tfree[h], kRowThreads);
+            mbar_init(&B.tfree[h], kRowWarps);
         }
         mbar_init(&B.final_, 1);
         fence_mbar_init();
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                 put16g<BF16>(bufs[kBufX], r, 16 * q, xv);
             }
             fence_async_global();
-            mbar_arrive(&B.act);
+            warp_arrive(&B.act);
             float se = 0.f, dot = 0.f;
             for (int jj = 0; jj < 7; ++jj) {
                 const Job J = kJobs[jj];
@@ -391,9 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                     // TMEM half drained (and, for the last pass of a layer, its output written)
                     fence_async_global();
                     tc_fence_before();
-                    mbar_arrive(&B.tfree[h]);
+                    warp_arrive(&B.tfree[h]);
                 }
-                if (J.out_buf >= 0) mbar_arrive(&B.act);     // this layer's output is complete
+                if (J.out_buf >= 0) warp_arrive(&B.act);     // this layer's output is complete
             }
             part_v[q * 128 + r] = dot;
             part_s[q * 128 + r] = se;

@@ -28,15 +28,19 @@
 //
 // Per tile the MMA lane runs (TMEM columns in brackets):
 //   CUR1 [0,64) = X C1^T ; D1_0 [384,448), D1_1 [448,512) = X W1[chunk]^T
-//   CUR2 [64,128) = Z C2^T                         (after the rows wrote Z)
-//   for i < 8:  D2 [0,384) += h1_i W2[:, chunk i]^T  (after rows wrote h1_i)
+//   CUR2 [256,320) = Z C2^T                        (after the rows wrote Z)
+//   for i < 8:  D2 [0,384) += h1_i W2[:, chunk i]^T  (after rows wrote h1_i;
+//                 for i = 0 the columns [256,384) also wait for CUR2's drain)
 //               D1_{i+2} = X W1[chunk i+2]^T         (into the buffer h1_i left)
 //   D3 [256,512) += h2_k W3^T, k = 4,5,0,1,2,3       (as the rows write h2_k)
 //   D4 [0,128)   += h3_k W4^T, k = 0..3
 //   D5 [128,192) += h4_k W5^T, k = 0..1
 // so layer 1 never exists whole (its 64-column chunks are produced while the
 // tensor pipe accumulates layer 2) and every later layer starts on its first
-// K-chunk while the rows still drain the rest of the previous one.
+// K-chunk while the rows still drain the rest of the previous one.  The rows
+// build X and Z of the next tile at the end of the current one, and at the
+// start of a tile drain h1_0 before the curiosity error, so that layer 2
+// starts without waiting for the curiosity epilogues.
 // Shared-memory operand slots (128 rows x 128 B each): X -> 2, Z -> 3,
 // h1 chunks -> 0/1 (alternating), h2 -> 0..5, h3 -> 0..3, h4 -> 0..1.  From
 // the end of layer 3 of the previous tile until the curiosity epilogue, slots
@@ -70,7 +74,8 @@ constexpr int kXSlot = 2, kZSlot = 3, kFeatSlot = 4;
 constexpr int kFeatFloats = 2 * kSlot / 4;      // feature staging area (slots 4-5): 8192 floats
 constexpr int kMaxSeg = 4;                      // episodes of one tile staged at most
 constexpr int kBiasFloats = 1600;
-constexpr int kOneHotFloats = kActions * kCurH;
+constexpr int kOneHotLd = kCurH + 4;             // padded row: the rows of different actions start on different banks
+constexpr int kOneHotFloats = kActions * kOneHotLd;
 constexpr int kSmem = kNumSlots * kSlot + kStages * kStage + (kBiasFloats + kOneHotFloats) * 4 + 2 * 4 * 128 * 4 + 1024;
 static_assert(kSmem <= 232448, "value kernel shared memory");
 
@@ -79,11 +84,11 @@ constexpr int kB1 = 0, kB2 = 512, kB3 = 896, kB4 = 1152, kB5 = 1280, kHW = 1344,
               kC2B = 1476;
 
 // TMEM columns
-constexpr uint32_t kColCur1 = 0, kColCur2 = 64, kColD1 = 384, kColD2 = 0, kColD3 = 256, kColD4 = 0, kColD5 = 128;
+constexpr uint32_t kColCur1 = 0, kColCur2 = 256, kColD1 = 384, kColD2 = 0, kColD3 = 256, kColD4 = 0, kColD5 = 128;
 
 struct Bars {
     uint64_t full[kStages], empty[kStages];
-    uint64_t act_x, act_z, act_h1[2], act_h2[6], act_h3[4], act_h4[2];
+    uint64_t act_x, act_z, act_cz, act_h1[2], act_h2[6], act_h3[4], act_h4[2];   // act_cz: CUR2 columns drained
     uint64_t acc_cur, acc_d1[2], acc_main, final_;
     uint64_t feat_full;        // the staged feature rows of the next tile have landed
 };
@@ -106,6 +111,13 @@ struct SegPre {
 
 __device__ __forceinline__ float bf16_round(float x) { return __uint_as_float(pack_bf16x2(0.f, x) & 0xFFFF0000u); }
 
+// x / L for x >= 0, in 32 bits when x fits (the 64-bit division is a long
+// instruction sequence)
+__device__ __forceinline__ long long div_L(long long x, int L)
+{
+    return x <= 0x7fffffffLL ? (long long)((uint32_t)x / (uint32_t)L) : x / L;
+}
+
 __device__ __forceinline__ void seg_prefetch(const ValueArgs &a, long long r0, SegPre &p)
 {
     const long long NL = (long long)a.N * a.L;
@@ -113,9 +125,9 @@ __device__ __forceinline__ void seg_prefetch(const ValueArgs &a, long long r0, S
     p.n0 = 0;
     p.count = 0;
     if (r0 < NL) {
-        p.n0 = r0 / a.L;
+        p.n0 = div_L(r0, a.L);
         const long long r_end = r0 + 128 < NL ? r0 + 128 : NL;
-        const long long n_last = (r_end - 1) / a.L;
+        const long long n_last = div_L(r_end - 1, a.L);
         p.count = (int)(n_last - p.n0 + 1 < kMaxSeg ? n_last - p.n0 + 1 : kMaxSeg);
     }
 #pragma unroll
@@ -206,8 +218,13 @@ __device__ __forceinline__ void issue_meta(const ValueArgs &a, long long r, RowF
     f.r = r;
     f.is_boot = r >= NL;
     const long long rc = r < NL + a.N ? r : NL + a.N - 1;      // rows past the end read row `total-1`
-    f.n = f.is_boot ? (int)(rc - NL) : (int)(rc / L);
-    f.t = f.is_boot ? L - 1 : (int)(rc % L);
+    if (f.is_boot) {
+        f.n = (int)(rc - NL);
+        f.t = L - 1;
+    } else {
+        f.n = (int)div_L(rc, L);
+        f.t = (int)(rc - (long long)f.n * L);
+    }
     f.row = (long long)f.n * L + f.t;
     const long long prev = f.t > 0 ? f.row - 1 : f.row;
     f.start = __ldg(a.starts + f.n);
@@ -314,6 +331,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(x[i]);
 }
 
+// 16 f32 values -> relu -> 2 bf16 units, as put16
+__device__ __forceinline__ void put16_relu(uint8_t *tile, int r, int q, const float (&v)[16])
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint4 p;
+        p.x = pack_bf16x2_relu(v[8 * h + 0], v[8 * h + 1]);
+        p.y = pack_bf16x2_relu(v[8 * h + 2], v[8 * h + 3]);
+        p.z = pack_bf16x2_relu(v[8 * h + 4], v[8 * h + 5]);
+        p.w = pack_bf16x2_relu(v[8 * h + 6], v[8 * h + 7]);
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 2 * q + h)) = p;
+    }
+}
+
 // relu(D[cols] + bias) rounded to bf16 into row r / quarter q of operand tile `tile`
 __device__ __forceinline__ void drain16(uint32_t taddr, const float *bias, uint8_t *tile, int r, int q)
 {
@@ -323,22 +354,26 @@ __device__ __forceinline__ void drain16(uint32_t taddr, const float *bias, uint8
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const float4 b = b4[k];
-        v[4 * k + 0] = fmaxf(v[4 * k + 0] + b.x, 0.f);
-        v[4 * k + 1] = fmaxf(v[4 * k + 1] + b.y, 0.f);
-        v[4 * k + 2] = fmaxf(v[4 * k + 2] + b.z, 0.f);
-        v[4 * k + 3] = fmaxf(v[4 * k + 3] + b.w, 0.f);
+        v[4 * k + 0] += b.x;
+        v[4 * k + 1] += b.y;
+        v[4 * k + 2] += b.z;
+        v[4 * k + 3] += b.w;
     }
-    put16(tile, r, q, v);
+    put16_relu(tile, r, q, v);
 }
 
 __device__ __forceinline__ void row_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory"); }
 
-// arrive after this thread's generic-proxy smem accesses and TMEM reads
+// one arrival per warp, after every lane's generic-proxy smem accesses and
+// TMEM reads: each lane fences its own accesses, the warp synchronises, lane
+// 0 arrives (512 per-thread arrivals on one barrier would serialise in the
+// shared-memory atomic unit)
 __device__ __forceinline__ void publish(uint64_t *bar)
 {
     fence_async_smem();
     tc_fence_before();
-    mbar_arrive(bar);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 struct MmaCtx {
@@ -370,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
     uint8_t *slots = sm;
     uint8_t *ring = sm + kNumSlots * kSlot;
     float *bias = reinterpret_cast<float *>(ring + kStages * kStage);
-    float *onehot = bias + kBiasFloats;                  // curiosity layer-1 one-hot columns [45][64]
+    float *onehot = bias + kBiasFloats;                  // curiosity layer-1 one-hot columns [45][kOneHotLd]
     float *part = onehot + kOneHotFloats;                // [2][4][128] partial sums
     float *feat = reinterpret_cast<float *>(slots + kFeatSlot * kSlot);
     __shared__ __align__(8) Bars B;
@@ -385,12 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             mbar_init(&B.full[s], 1);
             mbar_init(&B.empty[s], 1);
         }
-        mbar_init(&B.act_x, kRowThreads);
-        mbar_init(&B.act_z, kRowThreads);
-        for (int i = 0; i < 2; ++i) mbar_init(&B.act_h1[i], kRowThreads);
-        for (int i = 0; i < 6; ++i) mbar_init(&B.act_h2[i], kRowThreads);
-        for (int i = 0; i < 4; ++i) mbar_init(&B.act_h3[i], kRowThreads);
-        for (int i = 0; i < 2; ++i) mbar_init(&B.act_h4[i], kRowThreads);
+        mbar_init(&B.act_x, kRowWarps);
+        mbar_init(&B.act_z, kRowWarps);
+        mbar_init(&B.act_cz, kRowWarps);
+        for (int i = 0; i < 2; ++i) mbar_init(&B.act_h1[i], kRowWarps);
+        for (int i = 0; i < 6; ++i) mbar_init(&B.act_h2[i], kRowWarps);
+        for (int i = 0; i < 4; ++i) mbar_init(&B.act_h3[i], kRowWarps);
+        for (int i = 0; i < 2; ++i) mbar_init(&B.act_h4[i], kRowWarps);
         mbar_init(&B.acc_cur, 1);
         mbar_init(&B.acc_d1[0], 1);
         mbar_init(&B.acc_d1[1], 1);
@@ -415,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             else if (i >= kC2B && i < kC2B + 64) v = vec[w.job[kJobCur2].bias_off + i - kC2B];
             bias[i] = v;
         }
-        for (int i = tid; i < kOneHotFloats; i += kThreads) onehot[i] = vec[w.onehot_off + i];
+        for (int i = tid; i < kActions * kCurH; i += kThreads)
+            onehot[(i / kCurH) * kOneHotLd + i % kCurH] = vec[w.onehot_off + i];
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&tmem_base_sh, 512);
@@ -463,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             const uint32_t s_ring = smem_u32(ring);
             int stage = 0;
             uint32_t ring_ph = 0;
-            uint32_t ph_x = 0, ph_z = 0, ph_h1[2] = {0, 0}, ph_h2[6] = {}, ph_h3[4] = {}, ph_h4[2] = {};
+            uint32_t ph_x = 0, ph_z = 0, ph_cz = 0, ph_h1[2] = {0, 0}, ph_h2[6] = {}, ph_h3[4] = {}, ph_h4[2] = {};
             auto take = [&]() -> uint32_t {      // wait for the next weight unit
                 uint32_t p = ring_ph;
                 m.wait(&B.full[stage], p);
@@ -494,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                     m.mma_chunk(kColD2, m.slot(i & 1), u, 256, i > 0);
                     release();
                     u = take();
+                    if (i == 0) m.wait(&B.act_cz, ph_cz);   // D2 columns [256,384) begin where CUR2 was
                     m.mma_chunk(kColD2 + 256, m.slot(i & 1), u, 128, i > 0);
                     if (i + 2 < 8) {
                         m.mma_chunk(kColD1 + 64 * (i & 1), m.slot(kXSlot), u + 16384, 64, false);
@@ -559,6 +597,26 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             publish(&B.act_x);
         };
 
+        // curiosity layer 1 of a tile: state part from TMEM, one-hot column gathered -> Z
+        auto cur1_epilogue = [&](const RowInfo &ri) {
+            wait_acc(&B.acc_cur, ph_cur);
+            float v[16];
+            tmem_ld16(lane_addr + kColCur1, v);
+            const int act = (ri.act >= 0 && ri.act < kActions) ? ri.act : 0;
+            const float4 *oh = reinterpret_cast<const float4 *>(onehot + act * kOneHotLd + 16 * q);
+            const float4 *b4 = reinterpret_cast<const float4 *>(bias + kC1B + 16 * q);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 o = oh[k], b = b4[k];
+                v[4 * k + 0] = (v[4 * k + 0] + o.x) + b.x;
+                v[4 * k + 1] = (v[4 * k + 1] + o.y) + b.y;
+                v[4 * k + 2] = (v[4 * k + 2] + o.z) + b.z;
+                v[4 * k + 3] = (v[4 * k + 3] + o.w) + b.w;
+            }
+            put16_relu(slots + kZSlot * kSlot, r, q, v);
+            publish(&B.act_z);
+        };
+
         long long tile = blockIdx.x;
         RowFetch nf;
         issue_meta(a, tile * 128 + r, nf);
@@ -568,33 +626,19 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         }
         RowInfo nri = resolve(a, nf);
         build_x(nri);
+        cur1_epilogue(nri);
 
         for (; tile < n_tiles && ok; tile += gridDim.x) {
             const RowInfo ri = nri;
             const long long next = tile + gridDim.x;
             const bool has_next = next < n_tiles;
+            // ---- layer-1 chunk 0 first: the tensor pipe waits for it
+            wait_acc(&B.acc_d1[0], ph_d1[0]);
+            drain16(lane_addr + kColD1, bias + kB1 + 16 * q, slots, r, q);
+            publish(&B.act_h1[0]);
             if (has_next) {                                    // consumed in the middle / at the end of this tile
                 issue_meta(a, next * 128 + r, nf);
                 if (tid == 0) seg_prefetch(a, next * 128, pre);
-            }
-            // ---- curiosity layer 1: state part from TMEM, one-hot column gathered
-            wait_acc(&B.acc_cur, ph_cur);
-            {
-                float v[16];
-                tmem_ld16(lane_addr + kColCur1, v);
-                const int act = (ri.act >= 0 && ri.act < kActions) ? ri.act : 0;
-                const float4 *oh = reinterpret_cast<const float4 *>(onehot + act * kCurH + 16 * q);
-                const float4 *b4 = reinterpret_cast<const float4 *>(bias + kC1B + 16 * q);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 o = oh[k], b = b4[k];
-                    v[4 * k + 0] = fmaxf((v[4 * k + 0] + o.x) + b.x, 0.f);
-                    v[4 * k + 1] = fmaxf((v[4 * k + 1] + o.y) + b.y, 0.f);
-                    v[4 * k + 2] = fmaxf((v[4 * k + 2] + o.z) + b.z, 0.f);
-                    v[4 * k + 3] = fmaxf((v[4 * k + 3] + o.w) + b.w, 0.f);
-                }
-                put16(slots + kZSlot * kSlot, r, q, v);
-                publish(&B.act_z);
             }
             // ---- curiosity layer 2: squared error against the pre-reset next state
             wait_acc(&B.acc_cur, ph_cur);
@@ -612,9 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                     }
                 }
                 part_s[q * 128 + r] = se;
+                publish(&B.act_cz);                            // its TMEM columns are layer 2's next
             }
-            // ---- layer-1 chunks (the tensor pipe accumulates layer 2 meanwhile)
-            for (int c = 0; c < 8; ++c) {
+            // ---- layer-1 chunks 1..7 (the tensor pipe accumulates layer 2 meanwhile)
+            for (int c = 1; c < 8; ++c) {
                 wait_acc(&B.acc_d1[c & 1], ph_d1[c & 1]);
                 drain16(lane_addr + kColD1 + 64 * (c & 1), bias + kB1 + 64 * c + 16 * q, slots + (c & 1) * kSlot, r, q);
                 publish(&B.act_h1[c & 1]);
@@ -640,8 +685,13 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 drain16(lane_addr + kColD4 + 64 * k, bias + kB4 + 64 * k + 16 * q, slots + k * kSlot, r, q);
                 publish(&B.act_h4[k]);
             }
-            // ---- next tile's state row (slot 2 and TMEM [0,128) are free now)
-            if (has_next) build_x(nri);
+            // ---- next tile's state row (slot 2 and TMEM [0,128) are free now) and its
+            // curiosity layer 1 (slot 3 is free too), ahead of this tile's head so that
+            // the next tile's curiosity layer 2 does not wait for the head and the stores
+            if (has_next) {
+                build_x(nri);
+                cur1_epilogue(nri);
+            }
             // ---- layer 5 + scalar head
             wait_acc(&B.acc_main, ph_main);
             {
