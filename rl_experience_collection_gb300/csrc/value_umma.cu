@@ -24,6 +24,7 @@
 //         three-stage ring.  Producer s owns stage s and so waits on its empty
 //         barrier strictly in order; the bulk copies of one warp complete one
 //         after another, those of different warps overlap.
+//         (lane 1 of warp 16 stages each tile's market-feature rows)
 //   19    allocates TMEM; one lane issues the MMAs and commits
 //
 // Per tile the MMA lane runs (TMEM columns in brackets):
@@ -91,6 +92,7 @@ struct Bars {
     uint64_t act_x, act_z, act_cz, act_h1[2], act_h2[6], act_h3[4], act_h4[2];   // act_cz: CUR2 columns drained
     uint64_t acc_cur, acc_d1[2], acc_main, final_;
     uint64_t feat_full;        // the staged feature rows of the next tile have landed
+    uint64_t feat_free;        // layer 3 has read slots 4-5: the next tile's rows may be staged there
 };
 
 // Where the feature rows of a tile's episodes sit in the staging area.
@@ -194,11 +196,11 @@ __device__ __forceinline__ int staged_off(const SegTable &T, long long n, long l
 
 struct RowInfo {
     int kind;            // 0 tuple, 1 bootstrap row, 2 tuple of an invalid episode, 3 bootstrap of one, -1 none
-    long long n;         // episode
+    int n;               // episode
     long long row;       // flat tuple index (kind 0/2) or the slot receiving the bootstrap value (kind 1/3)
-    long long bar;       // bar of the state row
+    int bar;             // bar of the state row (< n_bars)
     int act;
-    float vin, ein, vpost, epost;
+    float vin, ein, vpost, rew;
 };
 
 // Per-row metadata, loaded one tile ahead: every load's address depends only
@@ -208,7 +210,7 @@ struct RowFetch {
     long long r, row;          // flat row, tuple index / bootstrap slot
     int n, t, is_boot;         // episode, step, bootstrap row?
     int start, act, aprev, dprev;
-    float vin, vpost;
+    float vin, vpost, rew;
 };
 
 __device__ __forceinline__ void issue_meta(const ValueArgs &a, long long r, RowFetch &f)
@@ -231,6 +233,7 @@ __device__ __forceinline__ void issue_meta(const ValueArgs &a, long long r, RowF
     f.act = a.actions[f.row];
     f.vin = f.is_boot ? a.v_post[f.row] : a.values[f.row];
     f.vpost = a.v_post[f.row];
+    f.rew = a.rewards[f.row];                  // base reward: the curiosity bonus is added to it
     f.aprev = a.actions[prev];
     f.dprev = a.dones[prev];
 }
@@ -243,18 +246,18 @@ __device__ __forceinline__ RowInfo resolve(const ValueArgs &a, const RowFetch &f
     ri.n = f.n;
     ri.row = f.row;
     ri.act = f.act;
+    ri.rew = f.rew;
     if (f.r >= NL + a.N) {
         ri.kind = -1;
     } else if (!f.is_boot) {
         ri.kind = ok ? 0 : 2;
-        ri.bar = (long long)f.start + f.t;
+        ri.bar = f.start + f.t;
         ri.vin = f.vin;
         ri.vpost = f.vpost;
-        ri.epost = exposure_of(f.act);
         ri.ein = (f.t == 0 || f.dprev) ? 0.f : exposure_of(f.aprev);
     } else {
         ri.kind = ok ? 1 : 3;
-        ri.bar = (long long)f.start + a.L;
+        ri.bar = f.start + a.L;
         ri.vin = f.vin;
         ri.ein = exposure_of(f.act);
     }
@@ -268,7 +271,7 @@ __device__ __forceinline__ void state_cols(const ValueArgs &a, const RowInfo &ri
 {
     const bool has = ri.kind == 0 || ri.kind == 1;
     const int off = ri.kind == 0 ? staged_off(T, ri.n, ri.bar) : -1;
-    const float *src = off >= 0 ? area + off : a.F + ri.bar * kMarket;
+    const float *src = off >= 0 ? area + off : a.F + (long long)ri.bar * kMarket;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int c = 16 * q + j;
@@ -289,14 +292,14 @@ __device__ __forceinline__ void target_cols(const ValueArgs &a, const RowInfo &r
                                             const float *area, int q, float (&tv)[16])
 {
     const int off = ri.kind == 0 ? staged_off(T, ri.n, ri.bar + 1) : -1;
-    const float *src = off >= 0 ? area + off : a.F + (ri.kind == 0 ? ri.bar + 1 : 0) * kMarket;
+    const float *src = off >= 0 ? area + off : a.F + (ri.kind == 0 ? (long long)ri.bar + 1 : 0LL) * kMarket;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int c = 16 * q + j;
         float x = 0.f;
         if (c < kMarket) x = ri.kind == 0 ? src[c] : 0.f;
         else if (c == kMarket) x = ri.vpost;
-        else if (c == kMarket + 1) x = ri.epost;
+        else if (c == kMarket + 1) x = exposure_of(ri.act);
         else if (c == kMarket + 2) x = a.env.spread;
         tv[j] = x;
     }
@@ -363,6 +366,22 @@ __device__ __forceinline__ void drain16(uint32_t taddr, const float *bias, uint8
 }
 
 __device__ __forceinline__ void row_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory"); }
+
+// row_sync that also returns the AND of `pred` over every row thread, so that
+// all row warps leave the tile loop on the same tile
+__device__ __forceinline__ bool row_sync_and(bool pred)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)pred), "n"(kRowThreads)
+        : "memory");
+    return out != 0;
+}
 
 // one arrival per warp, after every lane's generic-proxy smem accesses and
 // TMEM reads: each lane fences its own accesses, the warp synchronises, lane
@@ -433,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         mbar_init(&B.acc_main, 1);
         mbar_init(&B.final_, 1);
         mbar_init(&B.feat_full, 1);
+        mbar_init(&B.feat_free, 1);
         fence_mbar_init();
     }
     // biases, head weights and one-hot columns (f32; the latter two already bf16-rounded)
@@ -491,6 +511,29 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 const long long c0 = clock64();
                 while (clock64() - c0 < 4000000) { }
             }
+        } else if (ps == 0 && lane == 1) {
+            // ---- feature stager (lane 1 of the first producer warp): stages each
+            // tile's market-feature rows into slots 4-5, for the first tile at once,
+            // for every later one once the rows report that layer 3 of the previous
+            // tile has read those slots; loading the episode starts here keeps
+            // their latency off the row warps
+            bool ok = true;
+            uint32_t ph = 0, issued = 0;
+            for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                SegPre pre;
+                seg_prefetch(a, tile * 128, pre);
+                if (tile != blockIdx.x) {
+                    ok = mbar_wait(&B.feat_free, ph, abort);
+                    ph ^= 1u;
+                    if (!ok) break;
+                }
+                seg_issue(a, pre, seg, feat, &B.feat_full);
+                ++issued;
+            }
+            // the last copies have landed before the CTA may exit, also after an
+            // abort (bounded wait independent of the abort flag)
+            int never = 0;
+            if (issued > 0) mbar_wait(&B.feat_full, (issued - 1) & 1u, &never, 100000000ull);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -587,7 +630,6 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             tc_fence_after();
         };
         float *part_v = part, *part_s = part + 4 * 128;
-        SegPre pre;                                            // thread 0 only
         auto build_x = [&](const RowInfo &ri) {
             ok = __all_sync(0xffffffffu, ok && mbar_wait(&B.feat_full, ph_feat, abort));
             ph_feat ^= 1u;
@@ -620,10 +662,6 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         long long tile = blockIdx.x;
         RowFetch nf;
         issue_meta(a, tile * 128 + r, nf);
-        if (tid == 0) {
-            seg_prefetch(a, tile * 128, pre);
-            seg_issue(a, pre, seg, feat, &B.feat_full);
-        }
         RowInfo nri = resolve(a, nf);
         build_x(nri);
         cur1_epilogue(nri);
@@ -636,10 +674,6 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             wait_acc(&B.acc_d1[0], ph_d1[0]);
             drain16(lane_addr + kColD1, bias + kB1 + 16 * q, slots, r, q);
             publish(&B.act_h1[0]);
-            if (has_next) {                                    // consumed in the middle / at the end of this tile
-                issue_meta(a, next * 128 + r, nf);
-                if (tid == 0) seg_prefetch(a, next * 128, pre);
-            }
             // ---- curiosity layer 2: squared error against the pre-reset next state
             wait_acc(&B.acc_cur, ph_cur);
             {
@@ -664,7 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 drain16(lane_addr + kColD1 + 64 * (c & 1), bias + kB1 + 64 * c + 16 * q, slots + (c & 1) * kSlot, r, q);
                 publish(&B.act_h1[c & 1]);
             }
-            if (has_next) nri = resolve(a, nf);                // the next tile's metadata has arrived
+            // the next tile's row metadata: loads issued where the rows wait for
+            // layer 2 anyway, consumed after layer 3
+            if (has_next) issue_meta(a, next * 128 + r, nf);
             // ---- layer 2 -> h2, chunks 4,5 first (their TMEM columns become layer 3's)
             wait_acc(&B.acc_main, ph_main);
             for (int kk = 0; kk < 6; ++kk) {
@@ -674,11 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             }
             // ---- layer 3 -> h3 (layer 3 has read slots 4-5: stage the next tile's features there)
             wait_acc(&B.acc_main, ph_main);
-            if (has_next && tid == 0) seg_issue(a, pre, seg, feat, &B.feat_full);
+            if (has_next && tid == 0) mbar_arrive(&B.feat_free);
             for (int k = 0; k < 4; ++k) {
                 drain16(lane_addr + kColD3 + 64 * k, bias + kB3 + 64 * k + 16 * q, slots + k * kSlot, r, q);
                 publish(&B.act_h3[k]);
             }
+            if (has_next) nri = resolve(a, nf);                // the next tile's metadata has arrived
             // ---- layer 4 -> h4
             wait_acc(&B.acc_main, ph_main);
             for (int k = 0; k < 2; ++k) {
@@ -712,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 const float se = (part_s[r] + part_s[128 + r]) + (part_s[256 + r] + part_s[384 + r]);
                 if (ri.kind == 0) {
                     a.values[ri.row] = value;
-                    a.rewards[ri.row] += a.env.cur_coef * (se / (float)kState);
+                    a.rewards[ri.row] = ri.rew + a.env.cur_coef * (se / (float)kState);
                 } else if (ri.kind == 2) {
                     a.values[ri.row] = 0.f;
                 } else if (ri.kind == 1) {
@@ -721,12 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                     a.boot[ri.row] = 0.f;
                 }
             }
-            row_sync();
-        }
-        // an abort can leave a feature copy in flight: give it time to land (bounded)
-        if (!ok && tid == 0) {
-            const long long c0 = clock64();
-            while (clock64() - c0 < 4000000) { }
+            ok = row_sync_and(ok);                             // every row warp leaves on the same tile
         }
     }
     if (abort_sh && tid == 0) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
