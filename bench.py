@@ -47,6 +47,33 @@ def path_flops(w: wl.Workload, N: int, L: int):
     return N * L * ACTOR_FLOP + value, value
 
 
+# DRAM bytes (read + write) of one value-kernel launch, from a two-counter ncu
+# capture at the bench's full size (profiles/ncu_dram_value_umma_reset_heavy_bf16.md).
+# A figure only holds for the source it was measured on: the sha256 below covers
+# the kernel and the files it is built from; any change makes the traffic null.
+VALUE_DRAM_CAPTURE = {"workload": "reset_heavy_bf16", "episodes": 16384, "horizon": 1000,
+                      "bytes": 542.49e6,
+                      "sources_sha256": "51270865894a84a248843b86358f4b05ca63860cc8b1b86b121239d5d14f5529"}
+VALUE_KERNEL_SOURCES = ["value_umma.cu", "umma.cuh", "umma_path.cuh", "env.cuh", "internal.cuh", "umma_pack.cu"]
+
+
+def value_sources_sha256():
+    import hashlib
+    hsh = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "rl_experience_collection_gb300", "csrc")
+    for f in VALUE_KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            hsh.update(fh.read())
+    return hsh.hexdigest()
+
+
+def value_dram_traffic(w, N, L):
+    c = VALUE_DRAM_CAPTURE
+    if c["bytes"] is None or (w.name, N, L) != (c["workload"], c["episodes"], c["horizon"]):
+        return None
+    return c["bytes"] if value_sources_sha256() == c["sources_sha256"] else None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -253,7 +280,8 @@ def main():
     gae_ms = statistics.mean(p[3] for p in phase)
     achieved = flop_value / (value_ms / 1000.0) / 1e12
     roofline = {"kernel": "value (critic + curiosity, tcgen05)", "bound": "tensor", "achieved": achieved,
-                "peak": tpk, "unit": "TFLOP/s", "frac": (achieved / tpk) if tpk else None, "traffic": None,
+                "peak": tpk, "unit": "TFLOP/s", "frac": (achieved / tpk) if tpk else None,
+                "traffic": value_dram_traffic(w, N, L),
                 "peak_kind": f"{tpk_name}, burst, {pk['src']}",
                 "algorithmic_flop_per_launch": flop_value}
     line = {"metric": METRIC, "value": value, "unit": "tuples/s", "n_gpus": world, "steps": args.steps,
