@@ -111,7 +111,7 @@ __device__ __forceinline__ float env_step(EpState &s, int a, float f0_next, cons
     s.nwin += 1;
     // H < threshold, decided exactly (in double, on the host, per histogram)
     const uint32_t bit = (uint32_t)(s.cnt[0] * 1024 + s.cnt[1] * 32 + s.cnt[2]);
-    const bool low = (__ldg(c.div_low + (bit >> 5)) >> (bit & 31u)) & 1u;
+    const bool low = (c.div_low[bit >> 5] >> (bit & 31u)) & 1u;   // global or a shared-memory copy
     const float div = low ? c.div_penalty : 0.0f;
     const float beta = (label > 0) ? c.pt_scale : ((label < 0) ? c.sl_scale : 0.0f);
     const float reward = pnl * (1.0f + beta) + div - c.risk_coef * fabsf(e2);

@@ -33,9 +33,11 @@ struct EnvConst {
     float cur_coef, risk_coef, tx_base, spread;
     // bit (c0*1024 + c1*32 + c2): 1 when the Shannon entropy (bits) of the
     // category histogram (c0, c1, c2) is below div_thresh; 32768 bits
+    // (kDivWords words); kernels may point this at a shared-memory copy
     const uint32_t *div_low;
 };
 
+constexpr int kDivWords = 1024;
 constexpr int kMarket = 51;
 constexpr int kState = 54;
 constexpr int kActions = 45;

@@ -36,7 +36,8 @@ struct P1Geo {
     static constexpr int H1_OFF = X_OFF + XC * SLOT;
     static constexpr int H2_OFF = H1_OFF + H1C * SLOT;
     static constexpr int BIAS_OFF = H2_OFF + H2C * SLOT;
-    static constexpr int SMEM = BIAS_OFF + (kActorH1 + kActorH2 + 48) * 4 + 1024;   // + alignment slack
+    static constexpr int DIV_OFF = BIAS_OFF + 1024;          // diversity table (kDivWords words)
+    static constexpr int SMEM = DIV_OFF + kDivWords * 4 + 1024;   // + alignment slack
 };
 
 // write values v[0..n) (n multiple of 8 for bf16, 4 for tf32) as row `r` of a
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
     uint8_t *H1 = sm + G::H1_OFF;
     uint8_t *H2 = sm + G::H2_OFF;
     float *bias = reinterpret_cast<float *>(sm + G::BIAS_OFF);
+    uint32_t *sdiv = reinterpret_cast<uint32_t *>(sm + G::DIV_OFF);
     __shared__ __align__(8) uint64_t bar_img, bar_mma, bar_final;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -126,6 +128,9 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
         fence_mbar_init();
     }
     for (int i = tid; i < kActorH1 + kActorH2 + 48; i += kP1Threads) bias[i] = w.actor_bias[i];
+    for (int i = tid; i < kDivWords; i += kP1Threads) sdiv[i] = a.env.div_low[i];
+    EnvConst env = a.env;
+    env.div_low = sdiv;                        // the environment step reads its table from shared memory
     if (warp == 0) {
         tmem_alloc(&tmem_base_sh, 256);
         tmem_relinquish();
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
         const float v_in = st.V;
         float v_post;
         int done;
-        const float rew = env_step(st, act, nxt[0], a.env, v_post, done);
+        const float rew = env_step(st, act, nxt[0], env, v_post, done);
         if (valid && ok) {
             a.actions[row0 + t] = act;
             a.logp[row0 + t] = logp;
