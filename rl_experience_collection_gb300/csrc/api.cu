@@ -1,5 +1,5 @@
 // api.cu -- the C ABI (include/rollout.h): argument checks, weight
-// conversion, and the stream-ordered launch of the three phases.
+// conversion, and the stream-ordered launch of the phases.
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -54,6 +54,9 @@ struct rollout_handle {
     uint8_t *d_scratch = nullptr;
     long long scratch_per_cta = 0;
     int scratch_ctas = 0;
+    // bf16 rollout: feature rows padded to kFPad floats and a tensor map over them
+    float *d_fpad = nullptr;
+    alignas(64) CUtensorMap fmap{};
     // environment
     uint32_t *d_div_low = nullptr;
     int *d_status = nullptr;
@@ -247,9 +250,38 @@ int upload_weights(rollout_handle *h, const float *w)
     return ROLLOUT_OK;
 }
 
+// the padded copy of the feature matrix and the 2-D tensor map the bf16
+// rollout kernel gathers its rows with ([n_bars][kFPad] f32, box kFPad x 1)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int make_feature_map(rollout_handle *h)
+{
+    const size_t bytes = (size_t)h->dims.n_bars * kFPad * sizeof(float);
+    cudaError_t e;
+    if ((e = cudaMalloc(&h->d_fpad, bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(padded features)");
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(ROLLOUT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {(cuuint64_t)kFPad, (cuuint64_t)h->dims.n_bars};
+    const cuuint64_t strides[1] = {(cuuint64_t)kFPad * sizeof(float)};
+    const cuuint32_t box[2] = {(cuuint32_t)kFPad, 1};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = reinterpret_cast<EncodeTiledFn>(fn)(
+        &h->fmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, h->d_fpad, dims, strides, box, elem,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ROLLOUT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return ROLLOUT_OK;
+}
+
 void free_handle(rollout_handle *h)
 {
     if (!h) return;
+    cudaFree(h->d_fpad);
     cudaFree(h->d_actor_packed);
     cudaFree(h->d_simt);
     cudaFree(h->d_umma);
@@ -280,7 +312,8 @@ int rollout_create(const float *weights, const rollout_dims *dims, rollout_handl
     if (e != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaGetDevice"); }
     if ((e = cudaMalloc(&h->d_status, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMalloc(status)"); }
     if ((e = cudaMemset(h->d_status, 0, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMemset"); }
-    if ((rc = upload_div_table(h)) || (rc = upload_weights(h, weights))) {
+    if ((rc = upload_div_table(h)) || (rc = upload_weights(h, weights)) ||
+        (dims->dtype == ROLLOUT_BF16 && (rc = make_feature_map(h)))) {
         free_handle(h);
         return rc;
     }
@@ -342,7 +375,9 @@ int rollout_run(rollout_handle *h, const float *features, const int32_t *episode
         if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         if ((e = launch_value_simt(va, h->simt, s)) != cudaSuccess) return cuda_fail(e, "value launch");
     } else {
-        if ((e = launch_phase1_umma(p1, h->umma, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
+        if (d.dtype == ROLLOUT_BF16 && (e = launch_pad_features(features, h->d_fpad, d.n_bars, s)) != cudaSuccess)
+            return cuda_fail(e, "feature padding launch");
+        if ((e = launch_phase1_umma(p1, h->umma, h->fmap, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
         if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
@@ -456,7 +491,9 @@ int rollout_run_static(rollout_handle *h, const float *features, const int32_t *
         if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         if ((e = launch_value_simt(va, h->simt, s)) != cudaSuccess) return cuda_fail(e, "value launch");
     } else {
-        if ((e = launch_phase1_umma(p1, h->umma, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
+        if (d.dtype == ROLLOUT_BF16 && (e = launch_pad_features(features, h->d_fpad, d.n_bars, s)) != cudaSuccess)
+            return cuda_fail(e, "feature padding launch");
+        if ((e = launch_phase1_umma(p1, h->umma, h->fmap, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
         if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");

@@ -1,13 +1,14 @@
 // internal.cuh -- declarations shared by the translation units of librollout.
 //
-// The collector runs as three stream-ordered phases, with no host round trip:
+// The collector runs as stream-ordered phases, with no host round trip:
 //   phase 1 (rollout): per episode, per step: actor MLP, softmax/CDF/LCG
 //     sample, portfolio, triple-barrier and diversity step, reset on done.
 //     The critic and the curiosity model do not feed the state trajectory,
 //     so they are not on this serial chain.
+//   state rows: every tuple's stored state row (states.cu).
 //   phase 2 (value): every tuple independently (plus one bootstrap row per
 //     episode): rebuilds the state row, runs the critic MLP and the curiosity
-//     model, adds the curiosity bonus to the reward, writes the state row.
+//     model, adds the curiosity bonus to the reward.
 //   phase 3 (gae): per episode, a warp-parallel segmented backward scan.
 // Between the phases the outputs double as intermediate storage:
 //   out_values[n,t] holds the portfolio value V entering step t (phase 1 ->
@@ -16,6 +17,7 @@
 //   out_ret[n,L-1] holds the bootstrap value (phase 2 -> phase 3).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,6 +41,7 @@ struct EnvConst {
 
 constexpr int kDivWords = 1024;
 constexpr int kMarket = 51;
+constexpr int kFPad = 52;          // padded feature row (208 bytes, a multiple of 16) for tensor maps
 constexpr int kState = 54;
 constexpr int kActions = 45;
 constexpr int kActorH1 = 128;

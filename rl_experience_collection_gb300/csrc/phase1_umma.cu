@@ -37,8 +37,24 @@ struct P1Geo {
     static constexpr int H2_OFF = H1_OFF + H1C * SLOT;
     static constexpr int BIAS_OFF = H2_OFF + H2C * SLOT;
     static constexpr int DIV_OFF = BIAS_OFF + 1024;          // diversity table (kDivWords words)
-    static constexpr int SMEM = DIV_OFF + kDivWords * 4 + 1024;   // + alignment slack
+    // bf16: ring of the market-feature rows of three consecutive steps, one
+    // padded row (kFPad floats) per episode, filled by tensor gathers; tf32
+    // has no room for it and loads each row thread by thread
+    // Layout of a slot: per warp 8 groups of 4 rows, a group (one gather of
+    // 4 x 208 B) starting every 896 bytes -- a tensor copy's shared-memory
+    // destination must be 128-byte aligned
+    static constexpr bool STAGE_F = BF16;
+    static constexpr int FR_OFF = DIV_OFF + kDivWords * 4;   // 1024-aligned
+    static constexpr int FR_GROUP = 896;
+    static constexpr int FR_WARP = 8 * FR_GROUP;
+    static constexpr int FR_SLOT = 4 * FR_WARP;
+    static constexpr int FR_BYTES = STAGE_F ? 3 * FR_SLOT : 0;
+    static constexpr int SMEM = FR_OFF + FR_BYTES + 1024;   // + alignment slack
 };
+
+static_assert(P1Geo<true>::FR_OFF % 1024 == 0 && P1Geo<true>::FR_GROUP % 128 == 0 &&
+                  P1Geo<true>::FR_GROUP >= 4 * kFPad * 4 && P1Geo<true>::SMEM <= 232448,
+              "row ring: 128-byte aligned gather destinations, fits in shared memory");
 
 // write values v[0..n) (n multiple of 8 for bf16, 4 for tf32) as row `r` of a
 // K-major swizzled operand starting at column c0 (c0 a multiple of 8 / 4)
@@ -104,7 +120,8 @@ __device__ __forceinline__ void epi_hidden(uint32_t taddr, const float *bias, ui
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a, UmmaWeights w)
+__global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a, UmmaWeights w,
+                                                                    const __grid_constant__ CUtensorMap fmap)
 {
     using G = P1Geo<BF16>;
     extern __shared__ uint8_t smem_raw[];
@@ -115,7 +132,9 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
     uint8_t *H2 = sm + G::H2_OFF;
     float *bias = reinterpret_cast<float *>(sm + G::BIAS_OFF);
     uint32_t *sdiv = reinterpret_cast<uint32_t *>(sm + G::DIV_OFF);
-    __shared__ __align__(8) uint64_t bar_img, bar_mma, bar_final;
+    uint8_t *fring = sm + G::FR_OFF;                             // [3][128][kFPad] f32
+    __shared__ __align__(8) uint64_t bar_img, bar_mma, bar_final, bar_rows[3];
+    __shared__ int s_row0[kP1Threads];                           // bar of step 0 (0 for an episode without rows)
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
 
@@ -125,6 +144,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
         mbar_init(&bar_img, 1);
         mbar_init(&bar_mma, 1);
         mbar_init(&bar_final, 1);
+        for (int k = 0; k < 3; ++k) mbar_init(&bar_rows[k], kP1Threads / 32);   // one arrival per warp
         fence_mbar_init();
     }
     for (int i = tid; i < kActorH1 + kActorH2 + 48; i += kP1Threads) bias[i] = w.actor_bias[i];
@@ -161,22 +181,75 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
     ep_reset(st);
     st.rng = live ? a.seeds[n] : 0u;
     const float *F = a.F;
+    const int lane = tid & 31;
+    s_row0[tid] = valid ? start : 0;
+    __syncwarp();
+    // bf16: lane 0 of each warp gathers the feature rows of step s (bar
+    // start + s; row 0 for an episode without rows) of the warp's 32 episodes
+    // into ring slot s % 3 -- eight tensor gathers of four padded rows --
+    // two steps ahead of their use; the slot's barrier counts one arrival per warp
+    int issued = -1;                                             // last step whose rows were issued
+    auto issue_rows = [&](int s) {
+        if constexpr (G::STAGE_F) {
+            if (s > L) return;
+            if (lane == 0) {
+                uint64_t *bar = &bar_rows[s % 3];
+                uint8_t *dst = fring + (s % 3) * G::FR_SLOT + warp * G::FR_WARP;
+                fence_async_smem();                              // the slot's previous rows were read before
+                mbar_arrive_expect_tx(bar, 32 * kFPad * 4);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const int *r0 = s_row0 + warp * 32 + 4 * g;
+                    tma_gather4(dst + g * G::FR_GROUP, &fmap, 0, r0[0] + s, r0[1] + s, r0[2] + s, r0[3] + s, bar);
+                }
+            }
+            issued = s;
+        }
+    };
+    // all threads: the rows of step s have landed
+    auto wait_rows = [&](int s, volatile int *ab, uint64_t limit) -> bool {
+        return mbar_wait(&bar_rows[s % 3], (uint32_t)((s / 3) & 1), ab, limit);
+    };
 
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
     const uint32_t sX = smem_u32(X), sH1 = smem_u32(H1), sH2 = smem_u32(H2), sImg = smem_u32(img);
     uint32_t ph = 0;
-    float cur[kMarket];
+    float cur[G::STAGE_F ? 1 : kMarket];
+    if constexpr (G::STAGE_F) {
+        issue_rows(0);
+        issue_rows(1);
+    } else {
 #pragma unroll
-    for (int j = 0; j < kMarket; ++j) cur[j] = valid ? __ldg(F + (long long)start * kMarket + j) : 0.f;
+        for (int j = 0; j < kMarket; ++j) cur[j] = valid ? __ldg(F + (long long)start * kMarket + j) : 0.f;
+    }
+    int waited = -1;                                             // last step whose rows were waited for
 
     ok = __syncthreads_and(ok);
     for (int t = 0; t < L; ++t) {
-        const long long b = (long long)start + t;
+        // this thread's row in a slot: group lane/4 of its warp, row lane%4 (16-byte aligned)
+        const int row_off = warp * G::FR_WARP + (lane >> 2) * G::FR_GROUP + (lane & 3) * kFPad * 4;
+        const float4 *row_t = reinterpret_cast<const float4 *>(fring + (t % 3) * G::FR_SLOT + row_off);
+        const float *row_n = reinterpret_cast<const float *>(fring + ((t + 1) % 3) * G::FR_SLOT + row_off);
+        if constexpr (G::STAGE_F) {
+            ok = ok && wait_rows(t, abort, 2000000000ull) && wait_rows(t + 1, abort, 2000000000ull);
+            waited = t + 1;
+        }
         // state row -> operand X
         {
             float x[G::XC * G::KC];
+            if constexpr (G::STAGE_F) {
 #pragma unroll
-            for (int j = 0; j < kMarket; ++j) x[j] = cur[j];
+                for (int k = 0; k < kFPad / 4; ++k) {
+                    const float4 v = row_t[k];
+                    x[4 * k + 0] = valid ? v.x : 0.f;
+                    x[4 * k + 1] = valid ? v.y : 0.f;
+                    x[4 * k + 2] = valid ? v.z : 0.f;
+                    if (4 * k + 3 < kMarket) x[4 * k + 3] = valid ? v.w : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kMarket; ++j) x[j] = cur[j];
+            }
             x[kMarket] = st.V;
             x[kMarket + 1] = st.e;
             x[kMarket + 2] = a.env.spread;
@@ -185,9 +258,14 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
             put_row<BF16, G::XC * G::KC>(X, tid, 0, x);
         }
         // next bar's features: its log-return drives this step, its row is the next state
-        float nxt[kMarket];
+        float nxt[G::STAGE_F ? 1 : kMarket];
+        if constexpr (G::STAGE_F) {
+            nxt[0] = valid ? row_n[0] : 0.f;
+        } else {
+            const long long b = (long long)start + t;
 #pragma unroll
-        for (int j = 0; j < kMarket; ++j) nxt[j] = valid ? __ldg(F + (b + 1) * kMarket + j) : 0.f;
+            for (int j = 0; j < kMarket; ++j) nxt[j] = valid ? __ldg(F + (b + 1) * kMarket + j) : 0.f;
+        }
 
         fence_async_smem();
         tc_fence_before();
@@ -197,6 +275,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
             issue_layer<BF16>(tmem + 0, sX, sImg + w.actor_off[0], G::XC, kActorH1);
             mma_commit(&bar_mma);
         }
+        issue_rows(t + 2);          // slot (t+2)%3 held step t-1's rows, all read before the barrier above
         ok = ok && mbar_wait(&bar_mma, ph, abort);
         ph ^= 1;
         tc_fence_after();
@@ -260,8 +339,16 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
             a.v_in[row0 + t] = 0.f;
             a.v_post[row0 + t] = 0.f;
         }
+        if constexpr (!G::STAGE_F) {
 #pragma unroll
-        for (int j = 0; j < kMarket; ++j) cur[j] = nxt[j];
+            for (int j = 0; j < kMarket; ++j) cur[j] = nxt[j];
+        }
+    }
+    if constexpr (G::STAGE_F) {
+        // rows still in flight after an early exit land before the CTA ends
+        // (bounded waits that do not give up on the abort flag)
+        int never = 0;
+        for (int s = waited + 1; s <= issued; ++s) wait_rows(s, &never, 100000000ull);
     }
     if (tid == 0) {
         if (!ok) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
@@ -277,7 +364,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
 }
 
 template <bool BF16>
-cudaError_t launch_p1(const Phase1Args &a, const UmmaWeights &w, cudaStream_t s)
+cudaError_t launch_p1(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
 {
     using G = P1Geo<BF16>;
     static bool attr = false;
@@ -288,15 +375,49 @@ cudaError_t launch_p1(const Phase1Args &a, const UmmaWeights &w, cudaStream_t s)
         attr = true;
     }
     const int blocks = (a.N + kP1Threads - 1) / kP1Threads;
-    phase1_umma_kernel<BF16><<<blocks, kP1Threads, G::SMEM, s>>>(a, w);
+    phase1_umma_kernel<BF16><<<blocks, kP1Threads, G::SMEM, s>>>(a, w, fmap);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, cudaStream_t s)
+cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
 {
-    return w.bf16 ? launch_p1<true>(a, w, s) : launch_p1<false>(a, w, s);
+    return w.bf16 ? launch_p1<true>(a, w, fmap, s) : launch_p1<false>(a, w, fmap, s);
+}
+
+namespace {
+
+// the feature matrix with rows padded to kFPad floats (the extra column is
+// zero): a tensor map's row pitch must be a multiple of 16 bytes, 51 floats
+// (204 bytes) is not
+__global__ void pad_features_kernel(const float *F, float4 *P, long long n_bars)
+{
+    constexpr int W = kFPad / 4;                 // 16-byte words per padded row
+    const long long total = n_bars * W;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long b = i / W;
+        const int c0 = 4 * (int)(i - b * W);
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = c0 + j < kMarket ? __ldg(F + b * kMarket + c0 + j) : 0.f;
+        P[i] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pad_features(const float *F, float *fpad, int n_bars, cudaStream_t s)
+{
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long words = (long long)n_bars * (kFPad / 4);
+    const long long blocks = (words + 255) / 256;
+    const int grid = (int)(blocks < (long long)sms * 8 ? blocks : (long long)sms * 8);
+    pad_features_kernel<<<grid, 256, 0, s>>>(F, reinterpret_cast<float4 *>(fpad), n_bars);
+    return cudaGetLastError();
 }
 
 }  // namespace rl

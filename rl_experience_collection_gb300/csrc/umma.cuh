@@ -102,6 +102,19 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src)
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// 2-D tensor gather of four rows (row indices y0..y3, columns from x, the
+// map's box being one row high) into dst, completing bytes on `bar`; the map
+// lives in kernel-parameter or global memory
+__device__ __forceinline__ void tma_gather4(void *dst, const void *map, int x, int y0, int y1, int y2, int y3,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_async_smem()

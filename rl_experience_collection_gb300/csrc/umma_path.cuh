@@ -57,7 +57,10 @@ struct UmmaHostLayout {
 int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *host_w, const UmmaHostLayout &lo,
                 char *err, size_t err_len);
 
-cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, cudaStream_t s);
+// fmap: 2-D tensor map over the padded feature copy [n_bars][kFPad] (f32,
+// box 52 x 1), used by the bf16 kernel; fpad is filled by launch_pad_features
+cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s);
+cudaError_t launch_pad_features(const float *F, float *fpad, int n_bars, cudaStream_t s);
 // bf16 operands with the 512/384/256/128/64 critic: activations resident in shared memory
 cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s);
 // every other shape: activations in per-CTA global scratch (see value_generic.cu)
