@@ -26,7 +26,7 @@ namespace rl {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kBatchRows = 8;
+constexpr int kBatchRows = 16;
 
 __global__ void __launch_bounds__(kWarps * 32) states_kernel(StatesArgs a)
 {

@@ -722,13 +722,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 drain16(lane_addr + kColD4 + 64 * k, bias + kB4 + 64 * k + 16 * q, slots + k * kSlot, r, q);
                 publish(&B.act_h4[k]);
             }
-            // ---- next tile's state row (slot 2 and TMEM [0,128) are free now) and its
-            // curiosity layer 1 (slot 3 is free too), ahead of this tile's head so that
-            // the next tile's curiosity layer 2 does not wait for the head and the stores
-            if (has_next) {
-                build_x(nri);
-                cur1_epilogue(nri);
-            }
+            // ---- next tile's state row (slot 2 and TMEM [0,128) are free now): the
+            // tensor pipe runs its curiosity layer 1 while the rows finish this tile's head
+            if (has_next) build_x(nri);
             // ---- layer 5 + scalar head
             wait_acc(&B.acc_main, ph_main);
             {
@@ -758,6 +754,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                     a.boot[ri.row] = 0.f;
                 }
             }
+            // ---- the next tile's curiosity layer 1 -> Z (slot 3 is free)
+            if (has_next) cur1_epilogue(nri);
             ok = row_sync_and(ok);                             // every row warp leaves on the same tile
         }
     }
