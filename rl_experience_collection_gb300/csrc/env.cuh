@@ -32,7 +32,7 @@ struct EpState {
     int k;            // steps since the last reset
     int nwin;         // actions in the diversity window
     uint64_t win;     // 2-bit categories, newest in bits [0,2)
-    int cnt[3];       // histogram of the window
+    uint32_t hist;    // histogram of the window: n_short * 1024 + n_flat * 32 + n_long (each <= 31)
     uint32_t rng;     // LCG state
 };
 
@@ -43,8 +43,11 @@ __device__ __forceinline__ void ep_reset(EpState &s)
     s.k = 0;
     s.nwin = 0;
     s.win = 0;
-    s.cnt[0] = s.cnt[1] = s.cnt[2] = 0;
+    s.hist = 0;
 }
+
+// the histogram word's unit for category c (Short 0 / Flat 1 / Long 2)
+__device__ __forceinline__ uint32_t hist_unit(int c) { return 1u << (5 * (2 - c)); }
 
 __device__ __forceinline__ float lcg_uniform(uint32_t &s)
 {
@@ -80,50 +83,78 @@ __device__ __forceinline__ int sample_action(const float (&l)[N], float u, float
     return a;
 }
 
+// The portfolio part of a step for action a, given em1 = expm1(F[b+1, 0]) (the
+// bar's simple return): trade cost, P&L, V', the triple-barrier label and
+// done.  Updates V, e and the holding time k (reset to 1, 0, 0 on done); the
+// diversity window is left to env_window_reward.
+__device__ __forceinline__ void env_trade(EpState &s, int a, float em1, const EnvConst &c, float &pnl,
+                                          float &v_post, int &label, int &done)
+{
+    const int xi = a / 9;
+    const float e2 = 0.5f * (float)(xi - 2);
+    const float rate = (float)(1 + (a % 9) / 3 + a % 3) * c.tx_base;
+    const float cost = fabsf(e2 - s.e) * rate;
+    const float move = e2 * em1;                          // e' * (P[b+1]/P[b] - 1)
+    pnl = (move - cost) - cost * move;                    // (1 - cost)(1 + move) - 1
+    const float V2 = s.V + s.V * pnl;
+    s.k += 1;
+    const float cpl = V2 - 1.0f;
+    label = (cpl >= c.barrier) ? 1 : ((cpl <= -c.barrier) ? -1 : 0);
+    done = (label != 0) || (s.k >= c.max_hold);
+    v_post = V2;
+    if (done) {
+        s.V = 1.0f;
+        s.e = 0.0f;
+        s.k = 0;
+    } else {
+        s.V = V2;
+        s.e = e2;
+    }
+}
+
+// The rest of the step: the diversity window of categories takes action a's
+// category, and the reward combines the trade's pnl and label with the window's
+// penalty and the risk term.  Resets the window on done.
+__device__ __forceinline__ float env_window_reward(EpState &s, int a, float pnl, int label, int done,
+                                                   const EnvConst &c)
+{
+    const int xi = a / 9;
+    const float e2 = 0.5f * (float)(xi - 2);
+    // diversity window of categories (Short 0 / Flat 1 / Long 2)
+    const int cat = (xi <= 1) ? 0 : ((xi == 2) ? 1 : 2);
+    const int W = c.div_window;
+    if (s.nwin == W) {
+        const int old = (int)((s.win >> (2 * (W - 1))) & 3u);
+        s.hist -= hist_unit(old);
+        s.nwin -= 1;
+    }
+    s.win = ((s.win << 2) | (uint64_t)cat) & ((W >= 32) ? ~0ull : ((1ull << (2 * W)) - 1ull));
+    s.hist += hist_unit(cat);
+    s.nwin += 1;
+    // H < threshold, decided exactly (in double, on the host, per histogram)
+    const uint32_t bit = s.hist;
+    const bool low = (c.div_low[bit >> 5] >> (bit & 31u)) & 1u;   // global or a shared-memory copy
+    const float div = low ? c.div_penalty : 0.0f;
+    const float beta = (label > 0) ? c.pt_scale : ((label < 0) ? c.sl_scale : 0.0f);
+    const float reward = pnl * (1.0f + beta) + div - c.risk_coef * fabsf(e2);
+    if (done) {
+        s.nwin = 0;
+        s.win = 0;
+        s.hist = 0;
+    }
+    return reward;
+}
+
 // One environment step for action a; f0_next = F[b+1, 0].  Returns the reward
 // without the curiosity bonus; sets v_post = V' and done.  Updates s (including
 // the reset on done).
 __device__ __forceinline__ float env_step(EpState &s, int a, float f0_next, const EnvConst &c,
                                           float &v_post, int &done)
 {
-    const int xi = a / 9;
-    const float e2 = 0.5f * (float)(xi - 2);
-    const float rate = (float)(1 + (a % 9) / 3 + a % 3) * c.tx_base;
-    const float cost = fabsf(e2 - s.e) * rate;
-    const float move = e2 * expm1f(f0_next);              // e' * (P[b+1]/P[b] - 1)
-    const float pnl = (move - cost) - cost * move;        // (1 - cost)(1 + move) - 1
-    const float V2 = s.V + s.V * pnl;
-    s.k += 1;
-    const float cpl = V2 - 1.0f;
-    const int label = (cpl >= c.barrier) ? 1 : ((cpl <= -c.barrier) ? -1 : 0);
-    done = (label != 0) || (s.k >= c.max_hold);
-
-    // diversity window of categories (Short 0 / Flat 1 / Long 2)
-    const int cat = (xi <= 1) ? 0 : ((xi == 2) ? 1 : 2);
-    const int W = c.div_window;
-    if (s.nwin == W) {
-        const int old = (int)((s.win >> (2 * (W - 1))) & 3u);
-        s.cnt[old] -= 1;
-        s.nwin -= 1;
-    }
-    s.win = ((s.win << 2) | (uint64_t)cat) & ((W >= 32) ? ~0ull : ((1ull << (2 * W)) - 1ull));
-    s.cnt[cat] += 1;
-    s.nwin += 1;
-    // H < threshold, decided exactly (in double, on the host, per histogram)
-    const uint32_t bit = (uint32_t)(s.cnt[0] * 1024 + s.cnt[1] * 32 + s.cnt[2]);
-    const bool low = (c.div_low[bit >> 5] >> (bit & 31u)) & 1u;   // global or a shared-memory copy
-    const float div = low ? c.div_penalty : 0.0f;
-    const float beta = (label > 0) ? c.pt_scale : ((label < 0) ? c.sl_scale : 0.0f);
-    const float reward = pnl * (1.0f + beta) + div - c.risk_coef * fabsf(e2);
-
-    v_post = V2;
-    if (done) {
-        ep_reset(s);
-    } else {
-        s.V = V2;
-        s.e = e2;
-    }
-    return reward;
+    float pnl;
+    int label;
+    env_trade(s, a, expm1f(f0_next), c, pnl, v_post, label, done);
+    return env_window_reward(s, a, pnl, label, done, c);
 }
 
 // exposure held entering step t, recovered from the previous step's action/done

@@ -10,7 +10,11 @@
 // Each layer's epilogue (bias, ReLU, rounding to the operand format) is done
 // by the owning thread straight from TMEM into the next layer's swizzled
 // operand tile; the logits never leave registers: softmax, CDF, LCG draw and
-// the environment step follow in the same thread.
+// the environment step follow in the same thread.  The bf16 kernel gives each
+// episode four threads instead and takes layer 1's action-independent inputs
+// off the serial chain (see phase1_bf16_kernel).
+#include <cuda_bf16.h>
+
 #include "env.cuh"
 #include "umma.cuh"
 #include "umma_path.cuh"
@@ -363,6 +367,448 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// ---------------------------------------------------------------------------
+// bf16 rollout with four threads per episode.  Warp w serves TMEM lanes and
+// episodes 32*(w%4)..+31 (its "quarter") and part p = w/4 of each row: the
+// state columns [16p, +16), layer 1's [32p, +32), layer 2's [16p, +16) and
+// the logits [12p, +12).
+//
+// Layer 1 is split by what each input depends on.  The 51 market features,
+// the spread and the bias (three bf16 pieces b = hi + mid + lo against three
+// constant-one columns 54..56 of the state tile) do not depend on the action
+// drawn in the step before, so their MMA for step t+1 runs on the tensor pipe
+// while step t samples its action.  The two portfolio inputs V and e (columns
+// 51, 52, zero in the MMA operand) enter in the epilogue as
+// bf16(V)*W1[:,51] + e*W1[:,52], exact products of bf16 values summed in f32.
+// Every part runs the short trade step (V', label, done, the V/e/k update)
+// itself from the shared draw, so no exchange closes the step; the diversity
+// window and the reward, which nothing else in the step needs, run one step
+// late on part 3 while the next step's layer 2 is on the tensor pipe.
+//
+// The softmax is split over the four parts: each takes its block's maximum
+// and sum, the blocks are merged (sum_p s_p * exp(m_p - m)), and each part
+// scans its block of the index-order CDF from the sum of the blocks before
+// it; the lowest part with a crossing gives the action, part 3 taking action
+// 44 when round-off leaves u*S above every running sum.
+// A 17th warp issues every MMA and row gather, so that no worker warp stalls
+// behind the tensor pipe's instruction queue.  Barrier 0 (the CTA) orders the
+// operand tiles before each MMA; barriers 1-4 order the exchanges inside each
+// quarter.
+constexpr int kWorkerWarps = 16;
+constexpr int kQThreads = 32 * (kWorkerWarps + 1);
+constexpr int kNone = 99;                      // no crossing in a part's block
+constexpr int kLogitsPerPart = 12;
+
+__device__ __forceinline__ void qsync(int quarter)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + quarter), "n"(kP1Threads) : "memory");
+}
+
+template <int NX>
+__device__ __forceinline__ void tmem_ld_x(uint32_t taddr, float *v);
+
+template <>
+__device__ __forceinline__ void tmem_ld_x<16>(uint32_t taddr, float *v)
+{
+    uint32_t x[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
+          "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(x[i]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld_x<4>(uint32_t taddr, float *v)
+{
+    uint32_t x[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(x[i]);
+}
+
+// relu(v[0..N)) as bf16, row r, columns c0.. of a K-major swizzled operand (c0 % 8 == 0, N % 8 == 0)
+template <int N>
+__device__ __forceinline__ void put_row_relu(uint8_t *op, int r, int c0, const float (&v)[N])
+{
+    constexpr int KC = P1Geo<true>::KC;
+#pragma unroll
+    for (int q = 0; q < N / 8; ++q) {
+        const int c = c0 + 8 * q;
+        uint4 p;
+        p.x = pack_bf16x2_relu(v[8 * q + 0], v[8 * q + 1]);
+        p.y = pack_bf16x2_relu(v[8 * q + 2], v[8 * q + 3]);
+        p.z = pack_bf16x2_relu(v[8 * q + 4], v[8 * q + 5]);
+        p.w = pack_bf16x2_relu(v[8 * q + 6], v[8 * q + 7]);
+        uint8_t *tile = op + (c / KC) * (128 * 128);
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(r, (c % KC) / 8)) = p;
+    }
+}
+
+// byte offset of element (row n, column k) in a bf16 K-major swizzled tile
+__device__ __forceinline__ uint32_t bf16_elem_offset(int n, int k)
+{
+    return sw128_offset(n, k >> 3) + 2 * (k & 7);
+}
+
+__device__ __forceinline__ float bf16_round(float x)
+{
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a, UmmaWeights w,
+                                                                  const __grid_constant__ CUtensorMap fmap)
+{
+    using G = P1Geo<true>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *img = sm;
+    uint8_t *X = sm + G::X_OFF;
+    uint8_t *H1 = sm + G::H1_OFF;
+    uint8_t *H2 = sm + G::H2_OFF;
+    float *bias = reinterpret_cast<float *>(sm + G::BIAS_OFF);   // b2[64] | b3[48]
+    uint32_t *sdiv = reinterpret_cast<uint32_t *>(sm + G::DIV_OFF);
+    uint8_t *fring = sm + G::FR_OFF;                             // [3] slots, see P1Geo
+    __shared__ __align__(8) uint64_t bar_img, bar_l1, bar_mma, bar_final, bar_rows[3];
+    __shared__ int s_row0[kP1Threads];                           // start bar (0 for an episode without rows)
+    __shared__ __align__(16) float s_wv[kActorH1];               // W1[:, 51] (bf16 values), read as float4
+    __shared__ __align__(16) float s_we[kActorH1];               // W1[:, 52]
+    __shared__ float2 s_ms[4][kP1Threads];                       // per part: block maximum, block sum
+    __shared__ int s_cand[4][kP1Threads];                        // per part: first crossing or kNone
+    __shared__ float s_la[4][kP1Threads];                        // its logit
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool issuer = warp == kWorkerWarps;                    // the MMA / gather warp
+    const bool leader = issuer && lane == 0;                     // the thread that issues
+    const int quarter = warp & 3, part = warp >> 2;
+    const int ei = 32 * quarter + lane;                          // episode within the CTA = TMEM lane = MMA row
+    if (tid == 0) {
+        abort_sh = 0;
+        mbar_init(&bar_img, 1);
+        mbar_init(&bar_l1, 1);
+        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_final, 1);
+        for (int k = 0; k < 3; ++k) mbar_init(&bar_rows[k], kWorkerWarps);   // one arrival per worker warp
+        fence_mbar_init();
+    }
+    for (int i = tid; i < kActorH2 + 48; i += kQThreads) bias[i] = w.actor_bias[kActorH1 + i];
+    for (int i = tid; i < kDivWords; i += kQThreads) sdiv[i] = a.env.div_low[i];
+    EnvConst env = a.env;
+    env.div_low = sdiv;
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_sh, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    volatile int *abort = &abort_sh;
+
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar_img, w.actor_img_bytes);
+        for (uint32_t off = 0; off < w.actor_img_bytes; off += 16384) {
+            const uint32_t nb = min(16384u, w.actor_img_bytes - off);
+            bulk_g2s(img + off, w.actor_img + off, nb, &bar_img);
+        }
+    }
+    bool ok = mbar_wait(&bar_img, 0, abort);
+    if (tid < kActorH1) {
+        // W1 row j: take out the portfolio weights, put the bias pieces at columns 54..56
+        uint8_t *w1 = img + w.actor_off[0];
+        const int j = tid;
+        s_wv[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(w1 + bf16_elem_offset(j, kMarket)));
+        s_we[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(w1 + bf16_elem_offset(j, kMarket + 1)));
+        const float b = w.actor_bias[j];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(b);
+        const float r1 = b - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+        *reinterpret_cast<__nv_bfloat16 *>(w1 + bf16_elem_offset(j, kState + 0)) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(w1 + bf16_elem_offset(j, kState + 1)) = mid;
+        *reinterpret_cast<__nv_bfloat16 *>(w1 + bf16_elem_offset(j, kState + 2)) = lo;
+    }
+
+    const int n = blockIdx.x * kP1Threads + ei;
+    const bool live = !issuer && n < a.N;
+    const int L = a.L;
+    const long long row0 = (long long)n * L;
+    const int start = live ? a.starts[n] : 0;
+    const bool valid = live && start_ok(start, L, a.n_bars);
+    if (part == 0 && live && !valid) set_status(a.status, ROLLOUT_ERR_RANGE);
+    EpState st;
+    ep_reset(st);
+    st.rng = live ? a.seeds[n] : 0u;
+    if (part == 0) s_row0[ei] = valid ? start : 0;
+    __syncthreads();
+    // lane 0 of each worker warp gathers two of its quarter's eight groups of
+    // four rows (tensor copies issued by one warp run one after another)
+    int issued = -1;
+    auto issue_rows = [&](int s) {
+        if (s > L) return;
+        if (!issuer && lane == 0) {
+            uint64_t *bar = &bar_rows[s % 3];
+            uint8_t *dst = fring + (s % 3) * G::FR_SLOT + quarter * G::FR_WARP;
+            fence_async_smem();
+            mbar_arrive_expect_tx(bar, 2 * 4 * kFPad * 4);
+#pragma unroll
+            for (int g = 2 * part; g < 2 * part + 2; ++g) {
+                const int *r0 = s_row0 + 32 * quarter + 4 * g;
+                tma_gather4(dst + g * G::FR_GROUP, &fmap, 0, r0[0] + s, r0[1] + s, r0[2] + s, r0[3] + s, bar);
+            }
+        }
+        issued = s;
+    };
+    int waited = -1;
+    auto wait_rows = [&](int s) -> bool {
+        if (!mbar_wait(&bar_rows[s % 3], (uint32_t)((s / 3) & 1), abort)) return false;
+        waited = s;
+        return true;
+    };
+    const int row_off = quarter * G::FR_WARP + (lane >> 2) * G::FR_GROUP + (lane & 3) * kFPad * 4;
+    auto ring_row = [&](int s) { return reinterpret_cast<const float4 *>(fring + (s % 3) * G::FR_SLOT + row_off); };
+    // state columns [16p, +16) of step s from its feature row; the portfolio
+    // columns are zero here, the three bias columns one
+    auto build_x = [&](int s) {
+        const float4 *row = ring_row(s);
+        float x[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 v = row[4 * part + k];
+            x[4 * k + 0] = v.x;
+            x[4 * k + 1] = v.y;
+            x[4 * k + 2] = v.z;
+            x[4 * k + 3] = v.w;
+        }
+        if (part == 3) {                                         // columns 48..63
+            x[3] = 0.f;                                          // V
+            x[4] = 0.f;                                          // e
+            x[5] = a.env.spread;
+            x[6] = x[7] = x[8] = 1.f;                            // bias pieces
+#pragma unroll
+            for (int j = 9; j < 16; ++j) x[j] = 0.f;
+        }
+        if (!valid) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = 0.f;
+        }
+        put_row<true, 16>(X, ei, 16 * part, x);
+    };
+
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    const uint32_t sX = smem_u32(X), sH1 = smem_u32(H1), sH2 = smem_u32(H2), sImg = smem_u32(img);
+    issue_rows(0);
+    issue_rows(1);
+    issue_rows(2);
+    int t = 0;
+    if (issuer) {
+        // the same CTA barriers as the workers, each followed by its MMAs
+        ok = __syncthreads_and(ok);
+        tc_fence_after();
+        if (ok && leader && L > 0) {
+            issue_layer<true>(tmem + 0, sX, sImg + w.actor_off[0], G::XC, kActorH1);
+            mma_commit(&bar_l1);
+        }
+        for (; t < L; ++t) {
+            if (!__syncthreads_and(ok)) break;                  // barrier A: H1 of step t
+            tc_fence_after();
+            if (leader) {
+                issue_layer<true>(tmem + 128, sH1, sImg + w.actor_off[1], G::H1C, kActorH2);
+                mma_commit(&bar_mma);
+            }
+            __syncthreads();                                     // barrier B: H2 of step t, X of step t+1
+            tc_fence_after();
+            if (leader) {
+                issue_layer<true>(tmem + 192, sH2, sImg + w.actor_off[2], G::H2C, 48);
+                mma_commit(&bar_mma);
+                if (t + 1 < L) {
+                    issue_layer<true>(tmem + 0, sX, sImg + w.actor_off[0], G::XC, kActorH1);
+                    mma_commit(&bar_l1);
+                }
+            }
+        }
+    } else {
+        uint32_t ph = 0, ph1 = 0;
+        ok = ok && wait_rows(0);
+        build_x(0);
+        fence_async_smem();                                          // X and the edited W1 tile, for the MMA
+        tc_fence_before();
+        ok = __syncthreads_and(ok);
+        tc_fence_after();
+
+        // the step before's window/reward, pending on part 3
+        int p_act = 0, p_label = 0, p_done = 0;
+        float p_pnl = 0.f;
+        bool p_store = false;
+        auto window_reward = [&](int t) {
+            const float rew = env_window_reward(st, p_act, p_pnl, p_label, p_done, env);
+            if (live) a.rewards[row0 + t] = p_store ? rew : 0.f;
+        };
+
+        for (; t < L; ++t) {                       // leaves only at the CTA-uniform test below
+            ok = ok && mbar_wait(&bar_l1, ph1, abort) && wait_rows(t + 1);
+            ph1 ^= 1;
+            tc_fence_after();
+            // ---- layer 1 epilogue, columns [32p, +32): + bf16(V) W1[:,51] + e W1[:,52]
+            {
+                float v[32];
+                tmem_ld32(lane_addr + 32 * part, v);
+                tmem_ld_wait();
+                const float bv = bf16_round(st.V), be = st.e;
+                const float4 *wv = reinterpret_cast<const float4 *>(s_wv + 32 * part);
+                const float4 *we = reinterpret_cast<const float4 *>(s_we + 32 * part);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float4 a4 = wv[k], b4 = we[k];
+                    v[4 * k + 0] = fmaf(bv, a4.x, fmaf(be, b4.x, v[4 * k + 0]));
+                    v[4 * k + 1] = fmaf(bv, a4.y, fmaf(be, b4.y, v[4 * k + 1]));
+                    v[4 * k + 2] = fmaf(bv, a4.z, fmaf(be, b4.z, v[4 * k + 2]));
+                    v[4 * k + 3] = fmaf(bv, a4.w, fmaf(be, b4.w, v[4 * k + 3]));
+                }
+                put_row_relu<32>(H1, ei, 32 * part, v);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            if (!__syncthreads_and(ok)) break;      // CTA-uniform exit after a failed wait
+            tc_fence_after();
+            // ---- while layer 2 runs: the next state tile, the bar's return, the step before's reward
+            if (t + 1 < L) build_x(t + 1);
+            const float em1 = valid ? ring_row(t + 1)[12].w : 0.f;   // expm1(F[b+1, 0]) of this step's bar b
+            if (part == 3 && t > 0) window_reward(t - 1);
+            ok = ok && mbar_wait(&bar_mma, ph, abort);
+            ph ^= 1;
+            tc_fence_after();
+            // ---- layer 2 epilogue, columns [16p, +16)
+            {
+                float v[16];
+                tmem_ld_x<16>(lane_addr + 128 + 16 * part, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += bias[16 * part + j];
+                put_row_relu<16>(H2, ei, 16 * part, v);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            // while layer 3 runs: slot (t+3)%3 held step t's rows, last read in step t-1
+            issue_rows(t + 3);
+            ok = ok && mbar_wait(&bar_mma, ph, abort);
+            ph ^= 1;
+            tc_fence_after();
+            // ---- logits [12p, +12) (45 valid), block maximum and sum
+            const int nv = part < 3 ? kLogitsPerPart : kActions - 3 * kLogitsPerPart;
+            float lg[kLogitsPerPart], q[kLogitsPerPart];
+#pragma unroll
+            for (int i = 0; i < kLogitsPerPart / 4; ++i)
+                tmem_ld_x<4>(lane_addr + 192 + kLogitsPerPart * part + 4 * i, lg + 4 * i);
+            tmem_ld_wait();
+            const float u = lcg_uniform(st.rng);                     // every part's LCG copy advances alike
+            float mp = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kLogitsPerPart; ++j) {
+                lg[j] += bias[kActorH2 + kLogitsPerPart * part + j];
+                if (j < nv) mp = fmaxf(mp, lg[j]);
+            }
+            float sp = 0.f;
+#pragma unroll
+            for (int j = 0; j < kLogitsPerPart; ++j) {
+                q[j] = j < nv ? __expf(lg[j] - mp) : 0.f;
+                sp += q[j];
+            }
+            s_ms[part][ei] = make_float2(mp, sp);
+            qsync(quarter);
+            float2 ms[4];
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) ms[pp] = s_ms[pp][ei];
+            const float m = fmaxf(fmaxf(ms[0].x, ms[1].x), fmaxf(ms[2].x, ms[3].x));
+            float S = 0.f, base = 0.f, scale = 1.f;
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const float sc = __expf(ms[pp].x - m);
+                if (pp == part) {
+                    base = S;
+                    scale = sc;
+                }
+                S = fmaf(ms[pp].y, sc, S);
+            }
+            const float thr = u * S;
+            float run = base;
+            int cand = kNone;
+            float lcand = 0.f;
+#pragma unroll
+            for (int j = 0; j < kLogitsPerPart; ++j) {
+                if (j < nv) {
+                    run = fmaf(q[j], scale, run);
+                    if (cand == kNone && thr < run) {
+                        cand = kLogitsPerPart * part + j;
+                        lcand = lg[j];
+                    }
+                }
+            }
+            if (part == 3 && cand == kNone) {                        // u*S above every running sum: action 44
+                cand = kActions - 1;
+                lcand = lg[kActions - 1 - 3 * kLogitsPerPart];
+            }
+            s_cand[part][ei] = cand;
+            s_la[part][ei] = lcand;
+            qsync(quarter);
+            int act = kActions - 1, pa = 3;
+#pragma unroll
+            for (int pp = 3; pp >= 0; --pp)
+                if (s_cand[pp][ei] != kNone) {
+                    act = s_cand[pp][ei];
+                    pa = pp;
+                }
+            // ---- the trade step, in every part
+            const float v_in = st.V;
+            float pnl, v_post;
+            int label, done;
+            env_trade(st, act, em1, env, pnl, v_post, label, done);
+            const bool store = valid && ok;
+            if (part == 0 && live) {
+                const float logp = (s_la[pa][ei] - m) - logf(S);
+                a.actions[row0 + t] = store ? act : 0;
+                a.logp[row0 + t] = store ? logp : 0.f;
+                a.dones[row0 + t] = store ? done : 0;
+                a.v_in[row0 + t] = store ? v_in : 0.f;
+                a.v_post[row0 + t] = store ? v_post : 0.f;
+            }
+            p_act = act;
+            p_pnl = pnl;
+            p_label = label;
+            p_done = done;
+            p_store = store;
+        }
+        if (part == 3 && t == L && L > 0) window_reward(L - 1);
+    }
+    if (!issuer) {
+        if (!ok) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
+        // rows still in flight after an early exit land before the CTA ends
+        int never = 0;
+        for (int s = waited + 1; s <= issued; ++s)
+            mbar_wait(&bar_rows[s % 3], (uint32_t)((s / 3) & 1), &never, 100000000ull);
+    }
+    if (leader) {
+        mma_commit(&bar_final);                                  // every MMA completes before TMEM is released
+        int never = 0;
+        mbar_wait(&bar_final, 0, &never, 100000000ull);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 template <bool BF16>
 cudaError_t launch_p1(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
 {
@@ -383,14 +829,25 @@ cudaError_t launch_p1(const Phase1Args &a, const UmmaWeights &w, const CUtensorM
 
 cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
 {
-    return w.bf16 ? launch_p1<true>(a, w, fmap, s) : launch_p1<false>(a, w, fmap, s);
+    if (!w.bf16) return launch_p1<false>(a, w, fmap, s);
+    using G = P1Geo<true>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(phase1_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int blocks = (a.N + kP1Threads - 1) / kP1Threads;
+    phase1_bf16_kernel<<<blocks, kQThreads, G::SMEM, s>>>(a, w, fmap);
+    return cudaGetLastError();
 }
 
 namespace {
 
-// the feature matrix with rows padded to kFPad floats (the extra column is
-// zero): a tensor map's row pitch must be a multiple of 16 bytes, 51 floats
-// (204 bytes) is not
+// the feature matrix with rows padded to kFPad floats (a tensor map's row
+// pitch must be a multiple of 16 bytes, 51 floats -- 204 bytes -- is not); the
+// extra column carries expm1(F[b, 0]), the bar's simple return, which the
+// environment step needs for the bar after its own
 __global__ void pad_features_kernel(const float *F, float4 *P, long long n_bars)
 {
     constexpr int W = kFPad / 4;                 // 16-byte words per padded row
@@ -402,6 +859,7 @@ __global__ void pad_features_kernel(const float *F, float4 *P, long long n_bars)
         float v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) v[j] = c0 + j < kMarket ? __ldg(F + b * kMarket + c0 + j) : 0.f;
+        if (c0 + 3 == kMarket) v[3] = expm1f(__ldg(F + b * kMarket));   // the bar's simple return
         P[i] = make_float4(v[0], v[1], v[2], v[3]);
     }
 }
