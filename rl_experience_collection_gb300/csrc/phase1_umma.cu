@@ -390,18 +390,39 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
 // scans its block of the index-order CDF from the sum of the blocks before
 // it; the lowest part with a crossing gives the action, part 3 taking action
 // 44 when round-off leaves u*S above every running sum.
-// A 17th warp issues every MMA and row gather, so that no worker warp stalls
-// behind the tensor pipe's instruction queue.  Barrier 0 (the CTA) orders the
-// operand tiles before each MMA; barriers 1-4 order the exchanges inside each
-// quarter.
+// A 17th warp issues every MMA, so that no worker warp stalls behind the
+// tensor pipe's instruction queue, and two more issue the row gathers (tensor
+// copies issued by one warp run one after another, at over a hundred cycles
+// each).  Barrier 0 (the whole CTA) orders H1 before layer 2 and frees the
+// ring slot the loaders refill; barrier 5 (workers and MMA warp) orders H2 and
+// the next state tile before layer 3 and layer 1; barriers 1-4 order the
+// exchanges inside each quarter.
 constexpr int kWorkerWarps = 16;
-constexpr int kQThreads = 32 * (kWorkerWarps + 1);
+constexpr int kLoaderWarps = 2;
+constexpr int kQThreads = 32 * (kWorkerWarps + 1 + kLoaderWarps);
+constexpr int kBarB = 5, kBarBThreads = 32 * (kWorkerWarps + 1);
 constexpr int kNone = 99;                      // no crossing in a part's block
+// tensor memory columns: layer 1 [0, 128), layer 2 [128, 192), layer 3 [192, 240)
+constexpr int kP1TmemCols = 256;
+constexpr int kD1 = 0, kD2 = 128, kD3 = 192;
 constexpr int kLogitsPerPart = 12;
 
 __device__ __forceinline__ void qsync(int quarter)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(1 + quarter), "n"(kP1Threads) : "memory");
+}
+
+__device__ __forceinline__ void barrier_b() { asm volatile("bar.sync %0, %1;" ::"n"(kBarB), "n"(kBarBThreads) : "memory"); }
+
+// d = a * b + c on two f32 lanes at once, each rounded as fmaf
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
+          "l"(*reinterpret_cast<uint64_t *>(&c)));
+    return *reinterpret_cast<float2 *>(&r);
 }
 
 template <int NX>
@@ -487,8 +508,10 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
     __shared__ int abort_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool issuer = warp == kWorkerWarps;                    // the MMA / gather warp
+    const bool issuer = warp == kWorkerWarps;                    // the MMA warp
     const bool leader = issuer && lane == 0;                     // the thread that issues
+    const bool loader = warp > kWorkerWarps;                     // the gather warps
+    const bool worker = warp < kWorkerWarps;
     const int quarter = warp & 3, part = warp >> 2;
     const int ei = 32 * quarter + lane;                          // episode within the CTA = TMEM lane = MMA row
     if (tid == 0) {
@@ -497,7 +520,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
         mbar_init(&bar_l1, 1);
         mbar_init(&bar_mma, 1);
         mbar_init(&bar_final, 1);
-        for (int k = 0; k < 3; ++k) mbar_init(&bar_rows[k], kWorkerWarps);   // one arrival per worker warp
+        for (int k = 0; k < 3; ++k) mbar_init(&bar_rows[k], kLoaderWarps);   // one arrival per loader warp
         fence_mbar_init();
     }
     for (int i = tid; i < kActorH2 + 48; i += kQThreads) bias[i] = w.actor_bias[kActorH1 + i];
@@ -505,7 +528,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
     EnvConst env = a.env;
     env.div_low = sdiv;
     if (warp == 0) {
-        tmem_alloc(&tmem_base_sh, 256);
+        tmem_alloc(&tmem_base_sh, kP1TmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -539,7 +562,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
     }
 
     const int n = blockIdx.x * kP1Threads + ei;
-    const bool live = !issuer && n < a.N;
+    const bool live = worker && n < a.N;
     const int L = a.L;
     const long long row0 = (long long)n * L;
     const int start = live ? a.starts[n] : 0;
@@ -550,20 +573,21 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
     st.rng = live ? a.seeds[n] : 0u;
     if (part == 0) s_row0[ei] = valid ? start : 0;
     __syncthreads();
-    // lane 0 of each worker warp gathers two of its quarter's eight groups of
-    // four rows (tensor copies issued by one warp run one after another)
+    // lane 0 of loader warp k gathers quarters 2k and 2k+1 (16 groups of four
+    // rows); every thread tracks `issued`
     int issued = -1;
     auto issue_rows = [&](int s) {
         if (s > L) return;
-        if (!issuer && lane == 0) {
+        if (loader && lane == 0) {
+            const int k = warp - kWorkerWarps - 1;
             uint64_t *bar = &bar_rows[s % 3];
-            uint8_t *dst = fring + (s % 3) * G::FR_SLOT + quarter * G::FR_WARP;
+            uint8_t *dst = fring + (s % 3) * G::FR_SLOT;
             fence_async_smem();
-            mbar_arrive_expect_tx(bar, 2 * 4 * kFPad * 4);
-#pragma unroll
-            for (int g = 2 * part; g < 2 * part + 2; ++g) {
-                const int *r0 = s_row0 + 32 * quarter + 4 * g;
-                tma_gather4(dst + g * G::FR_GROUP, &fmap, 0, r0[0] + s, r0[1] + s, r0[2] + s, r0[3] + s, bar);
+            mbar_arrive_expect_tx(bar, (kP1Threads / kLoaderWarps) * kFPad * 4);
+            for (int g = 16 * k; g < 16 * k + 16; ++g) {
+                const int *r0 = s_row0 + 4 * g;
+                tma_gather4(dst + (g >> 3) * G::FR_WARP + (g & 7) * G::FR_GROUP, &fmap, 0, r0[0] + s, r0[1] + s,
+                            r0[2] + s, r0[3] + s, bar);
             }
         }
         issued = s;
@@ -615,26 +639,32 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
         ok = __syncthreads_and(ok);
         tc_fence_after();
         if (ok && leader && L > 0) {
-            issue_layer<true>(tmem + 0, sX, sImg + w.actor_off[0], G::XC, kActorH1);
+            issue_layer<true>(tmem + kD1, sX, sImg + w.actor_off[0], G::XC, kActorH1);
             mma_commit(&bar_l1);
         }
         for (; t < L; ++t) {
             if (!__syncthreads_and(ok)) break;                  // barrier A: H1 of step t
             tc_fence_after();
             if (leader) {
-                issue_layer<true>(tmem + 128, sH1, sImg + w.actor_off[1], G::H1C, kActorH2);
+                issue_layer<true>(tmem + kD2, sH1, sImg + w.actor_off[1], G::H1C, kActorH2);
                 mma_commit(&bar_mma);
             }
-            __syncthreads();                                     // barrier B: H2 of step t, X of step t+1
+            barrier_b();                                         // H2 of step t, X of step t+1
             tc_fence_after();
             if (leader) {
-                issue_layer<true>(tmem + 192, sH2, sImg + w.actor_off[2], G::H2C, 48);
+                issue_layer<true>(tmem + kD3, sH2, sImg + w.actor_off[2], G::H2C, 48);
                 mma_commit(&bar_mma);
                 if (t + 1 < L) {
-                    issue_layer<true>(tmem + 0, sX, sImg + w.actor_off[0], G::XC, kActorH1);
+                    issue_layer<true>(tmem + kD1, sX, sImg + w.actor_off[0], G::XC, kActorH1);
                     mma_commit(&bar_l1);
                 }
             }
+        }
+    } else if (loader) {
+        ok = __syncthreads_and(ok);                              // the workers' first state tile
+        for (; t < L; ++t) {
+            if (!__syncthreads_and(ok)) break;                  // barrier A of step t
+            issue_rows(t + 3);                  // slot (t+3)%3 held step t's rows, last read in step t-1
         }
     } else {
         uint32_t ph = 0, ph1 = 0;
@@ -661,18 +691,21 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             // ---- layer 1 epilogue, columns [32p, +32): + bf16(V) W1[:,51] + e W1[:,52]
             {
                 float v[32];
-                tmem_ld32(lane_addr + 32 * part, v);
+                tmem_ld32(lane_addr + kD1 + 32 * part, v);
                 tmem_ld_wait();
-                const float bv = bf16_round(st.V), be = st.e;
+                const float2 bv = make_float2(bf16_round(st.V), bf16_round(st.V)), be = make_float2(st.e, st.e);
                 const float4 *wv = reinterpret_cast<const float4 *>(s_wv + 32 * part);
                 const float4 *we = reinterpret_cast<const float4 *>(s_we + 32 * part);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const float4 a4 = wv[k], b4 = we[k];
-                    v[4 * k + 0] = fmaf(bv, a4.x, fmaf(be, b4.x, v[4 * k + 0]));
-                    v[4 * k + 1] = fmaf(bv, a4.y, fmaf(be, b4.y, v[4 * k + 1]));
-                    v[4 * k + 2] = fmaf(bv, a4.z, fmaf(be, b4.z, v[4 * k + 2]));
-                    v[4 * k + 3] = fmaf(bv, a4.w, fmaf(be, b4.w, v[4 * k + 3]));
+                    float2 lo = make_float2(v[4 * k + 0], v[4 * k + 1]), hi = make_float2(v[4 * k + 2], v[4 * k + 3]);
+                    lo = fma2(bv, make_float2(a4.x, a4.y), fma2(be, make_float2(b4.x, b4.y), lo));
+                    hi = fma2(bv, make_float2(a4.z, a4.w), fma2(be, make_float2(b4.z, b4.w), hi));
+                    v[4 * k + 0] = lo.x;
+                    v[4 * k + 1] = lo.y;
+                    v[4 * k + 2] = hi.x;
+                    v[4 * k + 3] = hi.y;
                 }
                 put_row_relu<32>(H1, ei, 32 * part, v);
             }
@@ -680,6 +713,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             tc_fence_before();
             if (!__syncthreads_and(ok)) break;      // CTA-uniform exit after a failed wait
             tc_fence_after();
+            issue_rows(t + 3);                  // tracks the loaders' `issued`
             // ---- while layer 2 runs: the next state tile, the bar's return, the step before's reward
             if (t + 1 < L) build_x(t + 1);
             const float em1 = valid ? ring_row(t + 1)[12].w : 0.f;   // expm1(F[b+1, 0]) of this step's bar b
@@ -690,7 +724,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             // ---- layer 2 epilogue, columns [16p, +16)
             {
                 float v[16];
-                tmem_ld_x<16>(lane_addr + 128 + 16 * part, v);
+                tmem_ld_x<16>(lane_addr + kD2 + 16 * part, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] += bias[16 * part + j];
@@ -698,10 +732,8 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             }
             fence_async_smem();
             tc_fence_before();
-            __syncthreads();
+            barrier_b();
             tc_fence_after();
-            // while layer 3 runs: slot (t+3)%3 held step t's rows, last read in step t-1
-            issue_rows(t + 3);
             ok = ok && mbar_wait(&bar_mma, ph, abort);
             ph ^= 1;
             tc_fence_after();
@@ -710,7 +742,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             float lg[kLogitsPerPart], q[kLogitsPerPart];
 #pragma unroll
             for (int i = 0; i < kLogitsPerPart / 4; ++i)
-                tmem_ld_x<4>(lane_addr + 192 + kLogitsPerPart * part + 4 * i, lg + 4 * i);
+                tmem_ld_x<4>(lane_addr + kD3 + kLogitsPerPart * part + 4 * i, lg + 4 * i);
             tmem_ld_wait();
             const float u = lcg_uniform(st.rng);                     // every part's LCG copy advances alike
             float mp = -INFINITY;
@@ -775,13 +807,17 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             int label, done;
             env_trade(st, act, em1, env, pnl, v_post, label, done);
             const bool store = valid && ok;
-            if (part == 0 && live) {
-                const float logp = (s_la[pa][ei] - m) - logf(S);
-                a.actions[row0 + t] = store ? act : 0;
-                a.logp[row0 + t] = store ? logp : 0.f;
-                a.dones[row0 + t] = store ? done : 0;
-                a.v_in[row0 + t] = store ? v_in : 0.f;
-                a.v_post[row0 + t] = store ? v_post : 0.f;
+            if (live) {                                          // the step's outputs, spread over the parts
+                if (part == 0) {
+                    const float logp = (s_la[pa][ei] - m) - logf(S);
+                    a.actions[row0 + t] = store ? act : 0;
+                    a.logp[row0 + t] = store ? logp : 0.f;
+                } else if (part == 1) {
+                    a.dones[row0 + t] = store ? done : 0;
+                    a.v_in[row0 + t] = store ? v_in : 0.f;
+                } else if (part == 2) {
+                    a.v_post[row0 + t] = store ? v_post : 0.f;
+                }
             }
             p_act = act;
             p_pnl = pnl;
@@ -791,7 +827,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
         }
         if (part == 3 && t == L && L > 0) window_reward(L - 1);
     }
-    if (!issuer) {
+    if (worker) {
         if (!ok) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
         // rows still in flight after an early exit land before the CTA ends
         int never = 0;
@@ -806,7 +842,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, kP1TmemCols);
 }
 
 template <bool BF16>
