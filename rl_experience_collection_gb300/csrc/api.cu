@@ -362,6 +362,7 @@ int rollout_run(rollout_handle *h, const float *features, const int32_t *episode
     Phase1Args p1{features, episode_starts, seeds, N, L, d.n_bars, out_actions, out_logp, out_dones,
                   out_rewards, out_values, out_adv, h->d_status, env};
     StatesArgs sa{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values, d.spread, out_states};
+    if (d.dtype == ROLLOUT_BF16) sa.Fpad = h->d_fpad;   // refilled by launch_pad_features before the state rows
     ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values,
                  out_adv, out_rewards, out_ret, h->d_status, env};
     GaeArgs ga{out_rewards, out_values, out_dones, out_adv, out_ret, N, L, gamma, lambda};
@@ -479,6 +480,7 @@ int rollout_run_static(rollout_handle *h, const float *features, const int32_t *
     Phase1Args p1{features, episode_starts, seeds, N, L, d.n_bars, out_actions, out_logp, out_dones,
                   out_rewards, out_values, out_adv, h->d_status, env};
     StatesArgs sa{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values, d.spread, out_states};
+    if (d.dtype == ROLLOUT_BF16) sa.Fpad = h->d_fpad;   // refilled by launch_pad_features before the state rows
     ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values,
                  out_adv, out_rewards, out_ret, h->d_status, env};
     GaeArgs ga{out_rewards, out_values, out_dones, out_adv, out_ret, N, L, gamma, lambda};

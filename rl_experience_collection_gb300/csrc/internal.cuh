@@ -91,6 +91,7 @@ struct StatesArgs {
     const float *v_in;         // V entering each step (out_values before the value phase)
     float spread;
     float *states;             // [N, L, 54] written
+    const float *Fpad = nullptr;   // optional copy of F with rows padded to kFPad floats (16-byte aligned rows)
 };
 
 struct GaeArgs {

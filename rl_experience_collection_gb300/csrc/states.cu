@@ -12,13 +12,16 @@
 // and after a reset, else the exposure of a_{t-1}.  Every row of an episode
 // whose start bar is out of range is zero.
 //
-// Each warp owns chunks of 32 consecutive rows: its lanes resolve one row's
-// metadata each, then the warp writes the chunk row by row, lane l storing
-// columns l and 32 + l (l < 22), so that every store instruction covers a
-// contiguous run of the row.  Warps synchronise only with themselves, so
-// many chunks are in flight per SM, and the feature loads of 8 rows are
-// issued before their stores.  The market columns come from the feature
-// matrix, which is small enough to stay in L2.
+// Each warp owns chunks of 32 consecutive rows (6912 bytes, 54 whole 128-byte
+// lines of out_states): its lanes resolve one row's metadata each into shared
+// memory, then the warp writes the chunk as a flat run of 864 float pairs, lane
+// l storing pairs l, l + 32, ... -- a pair never straddles two rows (54 is
+// even), and every store instruction covers two whole lines.  Pairs 0..24 of a
+// row are market features, pair 25 is (F[.., 50], V), pair 26 is (e, spread).
+// The feature loads of nine pairs are issued before their stores.  The market
+// columns come from the feature matrix, which is small enough to stay in L2;
+// where the padded copy (rows of kFPad floats, 16-byte aligned) exists, each
+// pair is one 8-byte load, which halves the loads the L1 has in flight.
 #include "env.cuh"
 
 namespace rl {
@@ -26,18 +29,23 @@ namespace rl {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kBatchRows = 16;
+constexpr int kPairs = kState / 2;            // 27 float pairs per row
+constexpr int kBatch = 9;                     // pairs per lane with loads in flight
 
+template <bool PAD>
 __global__ void __launch_bounds__(kWarps * 32) states_kernel(StatesArgs a)
 {
+    constexpr int RS = PAD ? kFPad : kMarket;  // row stride of the feature source
+    const float *src = PAD ? a.Fpad : a.F;
+    __shared__ long long s_fb[kWarps][32];    // float offset of the row's bar in the source, or -1: zero row
+    __shared__ float2 s_ve[kWarps][32];       // V, e of the row
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
     const long long NL = (long long)a.N * a.L;
     const long long n_chunks = (NL + 31) / 32;
     const bool narrow = NL <= 0x7fffffffLL;
-    const int c1 = 32 + lane;                     // the lane's column in the row's second part
     for (long long ch = (long long)blockIdx.x * kWarps + wi; ch < n_chunks; ch += (long long)gridDim.x * kWarps) {
         const long long row0 = ch * 32, row = row0 + lane;
-        long long fb = -1;                        // float offset of the row's bar in F, or -1: zero row
+        long long fb = -1;
         float v = 0.f, e = 0.f;
         if (row < NL) {
             long long n;
@@ -49,39 +57,51 @@ __global__ void __launch_bounds__(kWarps * 32) states_kernel(StatesArgs a)
             const int dprev = t > 0 ? a.dones[row - 1] : 1;
             const int aprev = t > 0 ? a.actions[row - 1] : 0;
             if (start_ok(start, a.L, a.n_bars)) {
-                fb = ((long long)start + t) * kMarket;
+                fb = ((long long)start + t) * RS;
                 v = vin;
                 e = dprev ? 0.f : exposure_of(aprev);
             }
         }
+        __syncwarp();                         // the previous chunk's reads of the slots are done
+        s_fb[wi][lane] = fb;
+        s_ve[wi][lane] = make_float2(v, e);
+        __syncwarp();
         const int n_rows = NL - row0 < 32 ? (int)(NL - row0) : 32;
-        float *dst = a.states + row0 * kState;
+        const int n_pairs = n_rows * kPairs;
+        float2 *dst = reinterpret_cast<float2 *>(a.states + row0 * kState);
 #pragma unroll 1
-        for (int r0 = 0; r0 < 32; r0 += kBatchRows) {
-            float x0[kBatchRows], x1[kBatchRows];
+        for (int j0 = 0; j0 < 32 * kPairs; j0 += 32 * kBatch) {
+            float2 x[kBatch];
 #pragma unroll
-            for (int k = 0; k < kBatchRows; ++k) {
-                const long long f = __shfl_sync(0xffffffffu, fb, r0 + k);
-                const float vv = __shfl_sync(0xffffffffu, v, r0 + k);
-                const float ee = __shfl_sync(0xffffffffu, e, r0 + k);
-                float y0 = 0.f, y1 = 0.f;
-                if (f >= 0) {
-                    y0 = __ldg(a.F + f + lane);
-                    if (c1 < kMarket) y1 = __ldg(a.F + f + c1);
-                    else if (c1 == kMarket) y1 = vv;
-                    else if (c1 == kMarket + 1) y1 = ee;
-                    else if (c1 == kMarket + 2) y1 = a.spread;
+            for (int k = 0; k < kBatch; ++k) {
+                const int j = j0 + 32 * k + lane;
+                const int r = j / kPairs, cp = j - kPairs * r;
+                float2 y = make_float2(0.f, 0.f);
+                if (j < n_pairs) {
+                    const long long f = s_fb[wi][r];
+                    if (f >= 0) {
+                        if (cp < kPairs - 2) {
+                            if constexpr (PAD) {
+                                y = __ldg(reinterpret_cast<const float2 *>(src + f) + cp);
+                            } else {
+                                y.x = __ldg(src + f + 2 * cp);
+                                y.y = __ldg(src + f + 2 * cp + 1);
+                            }
+                        } else if (cp == kPairs - 2) {
+                            y.x = __ldg(src + f + kMarket - 1);
+                            y.y = s_ve[wi][r].x;
+                        } else {
+                            y.x = s_ve[wi][r].y;
+                            y.y = a.spread;
+                        }
+                    }
                 }
-                x0[k] = y0;
-                x1[k] = y1;
+                x[k] = y;
             }
 #pragma unroll
-            for (int k = 0; k < kBatchRows; ++k) {
-                const int rr = r0 + k;
-                if (rr < n_rows) {
-                    __stcs(dst + rr * kState + lane, x0[k]);
-                    if (c1 < kState) __stcs(dst + rr * kState + c1, x1[k]);
-                }
+            for (int k = 0; k < kBatch; ++k) {
+                const int j = j0 + 32 * k + lane;
+                if (j < n_pairs) __stcs(dst + j, x[k]);
             }
         }
     }
@@ -98,7 +118,8 @@ cudaError_t launch_states(const StatesArgs &a, cudaStream_t s)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long cap = (long long)sms * 16;
     const int grid = (int)(blocks < cap ? blocks : cap);
-    states_kernel<<<grid, kWarps * 32, 0, s>>>(a);
+    if (a.Fpad) states_kernel<true><<<grid, kWarps * 32, 0, s>>>(a);
+    else states_kernel<false><<<grid, kWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 
