@@ -18,7 +18,7 @@
 // l storing pairs l, l + 32, ... -- a pair never straddles two rows (54 is
 // even), and every store instruction covers two whole lines.  Pairs 0..24 of a
 // row are market features, pair 25 is (F[.., 50], V), pair 26 is (e, spread).
-// The feature loads of nine pairs are issued before their stores.  The market
+// The feature loads of three pairs are issued before their stores.  The market
 // columns come from the feature matrix, which is small enough to stay in L2;
 // where the padded copy (rows of kFPad floats, 16-byte aligned) exists, each
 // pair is one 8-byte load, which halves the loads the L1 has in flight.
@@ -28,9 +28,9 @@ namespace rl {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 32;
 constexpr int kPairs = kState / 2;            // 27 float pairs per row
-constexpr int kBatch = 9;                     // pairs per lane with loads in flight
+constexpr int kBatch = 3;                     // pairs per lane with loads in flight (more warps beat deeper batches)
 
 template <bool PAD>
 __global__ void __launch_bounds__(kWarps * 32) states_kernel(StatesArgs a)
