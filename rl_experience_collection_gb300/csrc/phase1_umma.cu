@@ -381,9 +381,10 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
 // 51, 52, zero in the MMA operand) enter in the epilogue as
 // bf16(V)*W1[:,51] + e*W1[:,52], exact products of bf16 values summed in f32.
 // Every part runs the short trade step (V', label, done, the V/e/k update)
-// itself from the shared draw, so no exchange closes the step; the diversity
-// window and the reward, which nothing else in the step needs, run one step
-// late on part 3 while the next step's layer 2 is on the tensor pipe.
+// itself from the shared draw, so no exchange closes the step; the step's
+// outputs, and on part 3 the diversity window and the reward, which nothing
+// else in the step needs, are written one step late while the next step's
+// layer 3 is on the tensor pipe.
 //
 // The softmax is split over the four parts: each takes its block's maximum
 // and sum, the blocks are merged (sum_p s_p * exp(m_p - m)), and each part
@@ -675,10 +676,22 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
         ok = __syncthreads_and(ok);
         tc_fence_after();
 
-        // the step before's window/reward, pending on part 3
         int p_act = 0, p_label = 0, p_done = 0;
-        float p_pnl = 0.f;
+        float p_pnl = 0.f, p_logp = 0.f, p_vin = 0.f, p_vpost = 0.f;
         bool p_store = false;
+        auto flush_out = [&](int t) {
+            if (live && part < 3) {
+                if (part == 0) {
+                    a.actions[row0 + t] = p_store ? p_act : 0;
+                    a.logp[row0 + t] = p_store ? p_logp : 0.f;
+                } else if (part == 1) {
+                    a.dones[row0 + t] = p_store ? p_done : 0;
+                    a.v_in[row0 + t] = p_store ? p_vin : 0.f;
+                } else {
+                    a.v_post[row0 + t] = p_store ? p_vpost : 0.f;
+                }
+            }
+        };
         auto window_reward = [&](int t) {
             const float rew = env_window_reward(st, p_act, p_pnl, p_label, p_done, env);
             if (live) a.rewards[row0 + t] = p_store ? rew : 0.f;
@@ -717,7 +730,6 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             // ---- while layer 2 runs: the next state tile, the bar's return, the step before's reward
             if (t + 1 < L) build_x(t + 1);
             const float em1 = valid ? ring_row(t + 1)[12].w : 0.f;   // expm1(F[b+1, 0]) of this step's bar b
-            if (part == 3 && t > 0) window_reward(t - 1);
             ok = ok && mbar_wait(&bar_mma, ph, abort);
             ph ^= 1;
             tc_fence_after();
@@ -734,6 +746,8 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             tc_fence_before();
             barrier_b();
             tc_fence_after();
+            if (t > 0) flush_out(t - 1);
+            if (part == 3 && t > 0) window_reward(t - 1);
             ok = ok && mbar_wait(&bar_mma, ph, abort);
             ph ^= 1;
             tc_fence_after();
@@ -807,18 +821,9 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             int label, done;
             env_trade(st, act, em1, env, pnl, v_post, label, done);
             const bool store = valid && ok;
-            if (live) {                                          // the step's outputs, spread over the parts
-                if (part == 0) {
-                    const float logp = (s_la[pa][ei] - m) - logf(S);
-                    a.actions[row0 + t] = store ? act : 0;
-                    a.logp[row0 + t] = store ? logp : 0.f;
-                } else if (part == 1) {
-                    a.dones[row0 + t] = store ? done : 0;
-                    a.v_in[row0 + t] = store ? v_in : 0.f;
-                } else if (part == 2) {
-                    a.v_post[row0 + t] = store ? v_post : 0.f;
-                }
-            }
+            if (part == 0) p_logp = (s_la[pa][ei] - m) - logf(S);
+            p_vin = v_in;
+            p_vpost = v_post;
             p_act = act;
             p_pnl = pnl;
             p_label = label;
@@ -826,6 +831,7 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
             p_store = store;
         }
         if (part == 3 && t == L && L > 0) window_reward(L - 1);
+        if (t == L && L > 0) flush_out(L - 1);
     }
     if (worker) {
         if (!ok) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
