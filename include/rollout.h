@@ -201,6 +201,44 @@ ROLLOUT_API int rollout_run_static(rollout_handle *h, const float *features, con
                                    float *out_rewards, int32_t *out_dones, float *out_adv, float *out_ret,
                                    void *stream);
 
+/*
+ * rollout_run_host -- rollout_run from and to HOST memory.  (An addition of
+ * this library: the pages' pipeline downloads six output buffers after its
+ * kernel -- page "PPO CUDA Pipeline Design -- Zero-Roundtrip Experience
+ * Collection", section "Output Buffers"; here every download starts as soon
+ * as the kernel that finishes that output is done.)
+ *
+ * features, episode_starts, seeds: HOST arrays with the layouts rollout_run
+ * gives (features is [n_bars, n_market], the handle's n_bars).  The out_*
+ * arrays are HOST arrays with rollout_run's layouts; any of them may be NULL,
+ * and that output is then not copied back.  No alignment is required.
+ *
+ * The inputs are copied to device memory that the handle owns and keeps for
+ * later calls: the first call, and any call with a larger N * L, allocates it
+ * (about 4 * N * L * (n_market + 10) + 4 * n_bars * n_market bytes) and
+ * waits for the device if it has to free a smaller one.  The kernels then
+ * run as in rollout_run, and each output is copied back on one of the
+ * handle's four copy streams right after its kernel: actions, log-probs and
+ * dones after the rollout, the state rows after the state-row kernel (while
+ * the value kernel runs), values and rewards after the value kernel,
+ * advantages and returns after GAE.  Outputs above 64 MiB are split over the
+ * four streams.  `stream` waits for every copy at the end, so the call is
+ * stream-ordered like rollout_run: once the stream has reached the end of the
+ * call, the host outputs hold the results.  Copies only overlap the kernels
+ * when the host arrays are page-locked (cudaHostAlloc / cudaHostRegister);
+ * with pageable memory the call returns only after those copies are done.
+ *
+ * Returns ROLLOUT_OK, _INVALID, _NOMEM or _CUDA; device-detected problems go
+ * to rollout_status() as for rollout_run.  Calls on one handle must be
+ * ordered (one stream, or external synchronisation): they share the device
+ * copies.
+ */
+ROLLOUT_API int rollout_run_host(rollout_handle *h, const float *features, const int32_t *episode_starts,
+                                 const uint32_t *seeds, int N, int L, float gamma, float lambda,
+                                 float *out_states, int32_t *out_actions, float *out_logp, float *out_values,
+                                 float *out_rewards, int32_t *out_dones, float *out_adv, float *out_ret,
+                                 void *stream);
+
 /* rollout_destroy -- free the handle and its device memory (NULL is a no-op).
  * Synchronises the device first. */
 ROLLOUT_API void rollout_destroy(rollout_handle *h);

@@ -25,7 +25,7 @@ ROLLOUT_ERR_NOMEM = -6
 DTYPE = {"fp32": 0, "tf32": 1, "bf16": 2}
 
 EXPORTS = ["rollout_create", "rollout_set_weights", "rollout_run", "rollout_status", "rollout_destroy",
-           "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static"]
+           "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static", "rollout_run_host"]
 
 
 class RolloutDims(C.Structure):
@@ -68,6 +68,8 @@ def lib(path: Optional[str] = None):
                               vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.rollout_run_static.restype = C.c_int
     L.rollout_run_static.argtypes = list(L.rollout_run.argtypes)
+    L.rollout_run_host.restype = C.c_int
+    L.rollout_run_host.argtypes = list(L.rollout_run.argtypes)
     L.rollout_status.restype = C.c_int
     L.rollout_status.argtypes = [vp]
     L.rollout_destroy.restype = None
@@ -172,6 +174,26 @@ class Rollout:
                                         float(lam), p(out["states"]), p(out["actions"]), p(out["logp"]),
                                         p(out["values"]), p(out["rewards"]), p(out["dones"]), p(out["adv"]),
                                         p(out["ret"]), C.c_void_p(sh)))
+
+    def run_host(self, features, starts, seeds, N: int, L: int, gamma: float, lam: float,
+                 out: Dict[str, object], stream=None) -> None:
+        """rollout_run_host: inputs and outputs in HOST memory (numpy arrays or CPU
+        tensors, page-locked for the copies to overlap the kernels).  `out` maps
+        output names (OUTPUTS) to host arrays; a missing name is not copied back.
+        Enqueues on `stream` (a torch.cuda.Stream, a raw handle, or None = current)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+        def p(x):
+            if x is None:
+                return C.c_void_p(None)
+            return C.c_void_p(x.data_ptr() if hasattr(x, "data_ptr") else x.ctypes.data)
+
+        o = [out.get(k) for k in ("states", "actions", "logp", "values", "rewards", "dones", "adv", "ret")]
+        _check(lib().rollout_run_host(self._h, p(features), p(starts), p(seeds), int(N), int(L), float(gamma),
+                                      float(lam), *[p(x) for x in o], C.c_void_p(sh)))
 
     def run_raw(self, ptrs, N: int, L: int, gamma: float, lam: float, stream_handle: int = 0) -> int:
         """Raw-pointer form (integers), returns the status code instead of raising."""

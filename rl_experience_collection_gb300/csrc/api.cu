@@ -36,6 +36,14 @@ int cuda_fail(cudaError_t e, const char *what)
 // kernels of one run, timed when rollout_set_timing is on: rollout, state rows, value, GAE
 constexpr int kTimedKernels = 4;
 
+// points of a run after which outputs are final: the rollout (actions, log-probs,
+// dones), the state rows, the value kernel (values, rewards), GAE (advantages, returns)
+enum RunPoint { kAfterRollout = 0, kAfterStates, kAfterValue, kAfterGae, kRunPoints };
+
+// streams rollout_run_host spreads its device-to-host copies over (the copy engines
+// work on several at once)
+constexpr int kCopyStreams = 4;
+
 }  // namespace
 
 struct rollout_handle {
@@ -64,6 +72,13 @@ struct rollout_handle {
     // optional per-kernel timing
     bool timing = false, timed_run = false;
     cudaEvent_t ev[kTimedKernels + 1] = {};
+    // rollout_run_host: device copies of the inputs and outputs (one allocation,
+    // grown on demand), the copy streams and their events
+    uint8_t *d_stage = nullptr;
+    size_t stage_bytes = 0;
+    cudaStream_t copy_stream[kCopyStreams] = {};
+    cudaEvent_t point_ev[kRunPoints] = {};
+    cudaEvent_t copy_done[kCopyStreams] = {};
 };
 
 namespace {
@@ -290,6 +305,13 @@ void free_handle(rollout_handle *h)
     cudaFree(h->d_status);
     for (cudaEvent_t e : h->ev)
         if (e) cudaEventDestroy(e);
+    cudaFree(h->d_stage);
+    for (cudaStream_t st : h->copy_stream)
+        if (st) cudaStreamDestroy(st);
+    for (cudaEvent_t e : h->point_ev)
+        if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : h->copy_done)
+        if (e) cudaEventDestroy(e);
     delete h;
 }
 
@@ -328,6 +350,117 @@ int rollout_set_weights(rollout_handle *h, const float *weights)
     return upload_weights(h, weights);
 }
 
+}  // extern "C"
+
+namespace {
+
+// the device arrays of one run
+struct RunBuffers {
+    const float *features;
+    const int32_t *starts;
+    const uint32_t *seeds;
+    float *states;
+    int32_t *actions;
+    float *logp;
+    float *values;
+    float *rewards;
+    int32_t *dones;
+    float *adv;
+    float *ret;
+};
+
+// where the generic value kernel takes its per-CTA activation scratch
+struct ValueScratch {
+    uint8_t *ptr = nullptr;
+    long long per_cta = 0;
+    int grid = 0;
+};
+
+int check_run_args(rollout_handle *h, int N, int L, float gamma, float lambda)
+{
+    if (N <= 0 || L <= 0) return fail(ROLLOUT_ERR_INVALID, "N and L must be positive (N=%d, L=%d)", N, L);
+    if ((long long)L > (long long)h->dims.n_bars - 1)
+        return fail(ROLLOUT_ERR_INVALID, "L=%d needs at least L+1 bars (n_bars=%d)", L, h->dims.n_bars);
+    if ((long long)N * L * kState >= (1LL << 40)) return fail(ROLLOUT_ERR_INVALID, "N*L too large");
+    if (!(gamma >= 0.f && gamma <= 1.f) || !(lambda >= 0.f && lambda <= 1.f))
+        return fail(ROLLOUT_ERR_INVALID, "gamma and lambda must lie in [0, 1]");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != h->device) return fail(ROLLOUT_ERR_INVALID, "current device %d is not the handle's device %d", dev, h->device);
+    return ROLLOUT_OK;
+}
+
+int check_device_buffers(const RunBuffers &b)
+{
+    const void *ptrs[] = {b.features, b.starts, b.seeds, b.states, b.actions, b.logp,
+                          b.values, b.rewards, b.dones, b.adv, b.ret};
+    for (const void *p : ptrs) {
+        if (!p) return fail(ROLLOUT_ERR_INVALID, "null array argument");
+        if (((uintptr_t)p & 15u) != 0) return fail(ROLLOUT_ERR_INVALID, "array arguments must be 16-byte aligned");
+    }
+    return ROLLOUT_OK;
+}
+
+// Enqueues the kernels of one run on s.  points (kRunPoints events, or null) are
+// recorded after the kernels that finish each group of outputs.
+int enqueue_run(rollout_handle *h, const RunBuffers &b, int N, int L, float gamma, float lambda,
+                const ValueScratch &vs, cudaStream_t s, cudaEvent_t *points)
+{
+    const rollout_dims &d = h->dims;
+    cudaError_t e;
+    h->last_stream = s;
+    if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    EnvConst env{d.barrier, d.max_hold, d.pt_scale, d.sl_scale, d.div_window, d.div_thresh, d.div_penalty,
+                 d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div_low};
+    Phase1Args p1{b.features, b.starts, b.seeds, N, L, d.n_bars, b.actions, b.logp, b.dones,
+                  b.rewards, b.values, b.adv, h->d_status, env};
+    StatesArgs sa{b.features, b.starts, N, L, d.n_bars, b.actions, b.dones, b.values, d.spread, b.states};
+    if (d.dtype == ROLLOUT_BF16) sa.Fpad = h->d_fpad;   // refilled by launch_pad_features before the state rows
+    ValueArgs va{b.features, b.starts, N, L, d.n_bars, b.actions, b.dones, b.values,
+                 b.adv, b.rewards, b.ret, h->d_status, env};
+    GaeArgs ga{b.rewards, b.values, b.dones, b.adv, b.ret, N, L, gamma, lambda};
+
+    auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
+    auto point = [&](int p) { return points ? cudaEventRecord(points[p], s) : cudaSuccess; };
+    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (d.dtype == ROLLOUT_FP32) {
+        if ((e = launch_phase1_simt(p1, h->d_actor_packed, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
+    } else {
+        if (d.dtype == ROLLOUT_BF16 && (e = launch_pad_features(b.features, h->d_fpad, d.n_bars, s)) != cudaSuccess)
+            return cuda_fail(e, "feature padding launch");
+        if ((e = launch_phase1_umma(p1, h->umma, h->fmap, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
+    }
+    if ((e = mark(1)) != cudaSuccess || (e = point(kAfterRollout)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
+    if ((e = mark(2)) != cudaSuccess || (e = point(kAfterStates)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (d.dtype == ROLLOUT_FP32) e = launch_value_simt(va, h->simt, s);
+    else if (value_needs_scratch(h->umma)) e = launch_value_generic(va, h->umma, vs.ptr, vs.per_cta, vs.grid, s);
+    else e = launch_value_umma(va, h->umma, s);
+    if (e != cudaSuccess) return cuda_fail(e, "value launch");
+    if ((e = mark(3)) != cudaSuccess || (e = point(kAfterValue)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
+    if ((e = mark(4)) != cudaSuccess || (e = point(kAfterGae)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    h->timed_run = h->timing;
+    return ROLLOUT_OK;
+}
+
+// the handle's own scratch (allocated by rollout_create) for rollout_run
+ValueScratch handle_scratch(rollout_handle *h, int N, int L)
+{
+    ValueScratch vs;
+    if (h->dims.dtype == ROLLOUT_FP32 || !value_needs_scratch(h->umma)) return vs;
+    const long long tiles = ((long long)N * L + N + 127) / 128;
+    vs.ptr = h->d_scratch;
+    vs.per_cta = h->scratch_per_cta;
+    vs.grid = (int)(tiles < h->scratch_ctas ? tiles : h->scratch_ctas);
+    return vs;
+}
+
+}  // namespace
+
+extern "C" {
+
 int rollout_run(rollout_handle *h, const float *features, const int32_t *episode_starts, const uint32_t *seeds,
                 int N, int L, float gamma, float lambda, float *out_states, int32_t *out_actions,
                 float *out_logp, float *out_values, float *out_rewards, int32_t *out_dones, float *out_adv,
@@ -335,68 +468,14 @@ int rollout_run(rollout_handle *h, const float *features, const int32_t *episode
 {
     g_err[0] = 0;
     if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
-    const void *ptrs[] = {features, episode_starts, seeds, out_states, out_actions, out_logp,
-                          out_values, out_rewards, out_dones, out_adv, out_ret};
-    for (const void *p : ptrs) {
-        if (!p) return fail(ROLLOUT_ERR_INVALID, "null array argument");
-        if (((uintptr_t)p & 15u) != 0) return fail(ROLLOUT_ERR_INVALID, "array arguments must be 16-byte aligned");
-    }
-    if (N <= 0 || L <= 0) return fail(ROLLOUT_ERR_INVALID, "N and L must be positive (N=%d, L=%d)", N, L);
-    if ((long long)L > (long long)h->dims.n_bars - 1)
-        return fail(ROLLOUT_ERR_INVALID, "L=%d needs at least L+1 bars (n_bars=%d)", L, h->dims.n_bars);
-    if ((long long)N * L * kState >= (1LL << 40))
-        return fail(ROLLOUT_ERR_INVALID, "N*L too large");
-    if (!(gamma >= 0.f && gamma <= 1.f) || !(lambda >= 0.f && lambda <= 1.f))
-        return fail(ROLLOUT_ERR_INVALID, "gamma and lambda must lie in [0, 1]");
-    cudaStream_t s = (cudaStream_t)stream;
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev != h->device) return fail(ROLLOUT_ERR_INVALID, "current device %d is not the handle's device %d", dev, h->device);
-    h->last_stream = s;
-    if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-
-    const rollout_dims &d = h->dims;
-    EnvConst env{d.barrier, d.max_hold, d.pt_scale, d.sl_scale, d.div_window, d.div_thresh, d.div_penalty,
-                 d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div_low};
-    Phase1Args p1{features, episode_starts, seeds, N, L, d.n_bars, out_actions, out_logp, out_dones,
-                  out_rewards, out_values, out_adv, h->d_status, env};
-    StatesArgs sa{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values, d.spread, out_states};
-    if (d.dtype == ROLLOUT_BF16) sa.Fpad = h->d_fpad;   // refilled by launch_pad_features before the state rows
-    ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values,
-                 out_adv, out_rewards, out_ret, h->d_status, env};
-    GaeArgs ga{out_rewards, out_values, out_dones, out_adv, out_ret, N, L, gamma, lambda};
-
-    auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
-    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (d.dtype == ROLLOUT_FP32) {
-        if ((e = launch_phase1_simt(p1, h->d_actor_packed, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
-        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
-        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if ((e = launch_value_simt(va, h->simt, s)) != cudaSuccess) return cuda_fail(e, "value launch");
-    } else {
-        if (d.dtype == ROLLOUT_BF16 && (e = launch_pad_features(features, h->d_fpad, d.n_bars, s)) != cudaSuccess)
-            return cuda_fail(e, "feature padding launch");
-        if ((e = launch_phase1_umma(p1, h->umma, h->fmap, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
-        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
-        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if (value_needs_scratch(h->umma)) {
-            const long long tiles = ((long long)N * L + N + 127) / 128;
-            const int grid = (int)(tiles < h->scratch_ctas ? tiles : h->scratch_ctas);
-            e = launch_value_generic(va, h->umma, h->d_scratch, h->scratch_per_cta, grid, s);
-        } else {
-            e = launch_value_umma(va, h->umma, s);
-        }
-        if (e != cudaSuccess) return cuda_fail(e, "value launch");
-    }
-    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
-    if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    h->timed_run = h->timing;
-    return ROLLOUT_OK;
+    const RunBuffers b{features, episode_starts, seeds, out_states, out_actions, out_logp,
+                       out_values, out_rewards, out_dones, out_adv, out_ret};
+    int rc = check_device_buffers(b);
+    if (rc || (rc = check_run_args(h, N, L, gamma, lambda))) return rc;
+    return enqueue_run(h, b, N, L, gamma, lambda, handle_scratch(h, N, L), (cudaStream_t)stream, nullptr);
 }
+
+}  // extern "C"
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant (rollout_run_static): the generic value kernel's
@@ -425,7 +504,67 @@ int static_scratch(int dev, uint8_t **out)
     return ROLLOUT_OK;
 }
 
+// ---------------------------------------------------------------------------
+// rollout_run_host: device staging and the download schedule
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Lays out the staging allocation for (N, L); grows it when it is too small.
+int stage_buffers(rollout_handle *h, int N, int L, RunBuffers *b)
+{
+    const size_t nl = (size_t)N * L;
+    const size_t sizes[11] = {(size_t)h->dims.n_bars * kMarket * 4, (size_t)N * 4, (size_t)N * 4,
+                              nl * kState * 4, nl * 4, nl * 4, nl * 4, nl * 4, nl * 4, nl * 4, nl * 4};
+    size_t total = 0;
+    for (size_t z : sizes) total += align256(z);
+    cudaError_t e;
+    if (total > h->stage_bytes) {
+        // the previous run's copies may still read the old allocation: cudaFree waits for the device
+        cudaFree(h->d_stage);
+        h->d_stage = nullptr;
+        h->stage_bytes = 0;
+        if ((e = cudaMalloc(&h->d_stage, total)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(staging)");
+        h->stage_bytes = total;
+    }
+    uint8_t *p[11];
+    size_t at = 0;
+    for (int i = 0; i < 11; ++i) {
+        p[i] = h->d_stage + at;
+        at += align256(sizes[i]);
+    }
+    *b = RunBuffers{(const float *)p[0], (const int32_t *)p[1], (const uint32_t *)p[2], (float *)p[3],
+                    (int32_t *)p[4], (float *)p[5], (float *)p[6], (float *)p[7], (int32_t *)p[8],
+                    (float *)p[9], (float *)p[10]};
+    return ROLLOUT_OK;
+}
+
+int make_copy_streams(rollout_handle *h)
+{
+    if (h->copy_stream[0]) return ROLLOUT_OK;
+    cudaError_t e;
+    for (int k = 0; k < kCopyStreams; ++k) {
+        if ((e = cudaStreamCreateWithFlags(&h->copy_stream[k], cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamCreateWithFlags");
+        if ((e = cudaEventCreateWithFlags(&h->copy_done[k], cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventCreateWithFlags");
+    }
+    for (cudaEvent_t &ev : h->point_ev)
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventCreateWithFlags");
+    return ROLLOUT_OK;
+}
+
+// one output's download: host destination, device source, bytes, the run point after which it is final
+struct Download {
+    void *host;
+    const void *dev;
+    size_t bytes;
+    int point;
+};
+
 }  // namespace
+
+extern "C" {
 
 int rollout_run_static(rollout_handle *h, const float *features, const int32_t *episode_starts, const uint32_t *seeds,
                        int N, int L, float gamma, float lambda, float *out_states, int32_t *out_actions,
@@ -434,78 +573,80 @@ int rollout_run_static(rollout_handle *h, const float *features, const int32_t *
 {
     g_err[0] = 0;
     if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
-    const void *ptrs[] = {features, episode_starts, seeds, out_states, out_actions, out_logp,
-                          out_values, out_rewards, out_dones, out_adv, out_ret};
-    for (const void *p : ptrs) {
-        if (!p) return fail(ROLLOUT_ERR_INVALID, "null array argument");
-        if (((uintptr_t)p & 15u) != 0) return fail(ROLLOUT_ERR_INVALID, "array arguments must be 16-byte aligned");
-    }
-    if (N <= 0 || L <= 0) return fail(ROLLOUT_ERR_INVALID, "N and L must be positive (N=%d, L=%d)", N, L);
-    if ((long long)L > (long long)h->dims.n_bars - 1)
-        return fail(ROLLOUT_ERR_INVALID, "L=%d needs at least L+1 bars (n_bars=%d)", L, h->dims.n_bars);
-    if ((long long)N * L * kState >= (1LL << 40))
-        return fail(ROLLOUT_ERR_INVALID, "N*L too large");
-    if (!(gamma >= 0.f && gamma <= 1.f) || !(lambda >= 0.f && lambda <= 1.f))
-        return fail(ROLLOUT_ERR_INVALID, "gamma and lambda must lie in [0, 1]");
-    cudaStream_t s = (cudaStream_t)stream;
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev != h->device) return fail(ROLLOUT_ERR_INVALID, "current device %d is not the handle's device %d", dev, h->device);
-
-    const rollout_dims &d = h->dims;
-    const bool scratch = d.dtype != ROLLOUT_FP32 && value_needs_scratch(h->umma);
-    uint8_t *sp = nullptr;
-    int grid = 0;
-    long long per_cta = 0;
-    if (scratch) {
-        per_cta = value_generic_scratch_per_cta(h->umma);
-        if (per_cta > (long long)ROLLOUT_STATIC_SCRATCH_BYTES)
+    const RunBuffers b{features, episode_starts, seeds, out_states, out_actions, out_logp,
+                       out_values, out_rewards, out_dones, out_adv, out_ret};
+    int rc = check_device_buffers(b);
+    if (rc || (rc = check_run_args(h, N, L, gamma, lambda))) return rc;
+    ValueScratch vs;
+    if (h->dims.dtype != ROLLOUT_FP32 && value_needs_scratch(h->umma)) {
+        vs.per_cta = value_generic_scratch_per_cta(h->umma);
+        if (vs.per_cta > (long long)ROLLOUT_STATIC_SCRATCH_BYTES)
             return fail(ROLLOUT_ERR_UNSUPPORTED, "these layer shapes need %lld bytes of scratch per CTA, more than "
-                        "the %u-byte static array", per_cta, (unsigned)ROLLOUT_STATIC_SCRATCH_BYTES);
-        int rc = static_scratch(dev, &sp);
-        if (rc) return rc;
+                        "the %u-byte static array", vs.per_cta, (unsigned)ROLLOUT_STATIC_SCRATCH_BYTES);
+        if ((rc = static_scratch(h->device, &vs.ptr))) return rc;
         int sms = 0;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return cuda_fail(e, "cudaDeviceGetAttribute");
-        const long long fit = (long long)ROLLOUT_STATIC_SCRATCH_BYTES / per_cta;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        const long long fit = (long long)ROLLOUT_STATIC_SCRATCH_BYTES / vs.per_cta;
         const long long tiles = ((long long)N * L + N + 127) / 128;
-        long long g = tiles < sms ? tiles : sms;
-        grid = (int)(g < fit ? g : fit);
+        const long long g = tiles < sms ? tiles : sms;
+        vs.grid = (int)(g < fit ? g : fit);
     }
-    h->last_stream = s;
-    if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-    EnvConst env{d.barrier, d.max_hold, d.pt_scale, d.sl_scale, d.div_window, d.div_thresh, d.div_penalty,
-                 d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div_low};
-    Phase1Args p1{features, episode_starts, seeds, N, L, d.n_bars, out_actions, out_logp, out_dones,
-                  out_rewards, out_values, out_adv, h->d_status, env};
-    StatesArgs sa{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values, d.spread, out_states};
-    if (d.dtype == ROLLOUT_BF16) sa.Fpad = h->d_fpad;   // refilled by launch_pad_features before the state rows
-    ValueArgs va{features, episode_starts, N, L, d.n_bars, out_actions, out_dones, out_values,
-                 out_adv, out_rewards, out_ret, h->d_status, env};
-    GaeArgs ga{out_rewards, out_values, out_dones, out_adv, out_ret, N, L, gamma, lambda};
-    auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
-    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (d.dtype == ROLLOUT_FP32) {
-        if ((e = launch_phase1_simt(p1, h->d_actor_packed, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
-        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
-        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if ((e = launch_value_simt(va, h->simt, s)) != cudaSuccess) return cuda_fail(e, "value launch");
-    } else {
-        if (d.dtype == ROLLOUT_BF16 && (e = launch_pad_features(features, h->d_fpad, d.n_bars, s)) != cudaSuccess)
-            return cuda_fail(e, "feature padding launch");
-        if ((e = launch_phase1_umma(p1, h->umma, h->fmap, s)) != cudaSuccess) return cuda_fail(e, "phase 1 launch");
-        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
-        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        e = scratch ? launch_value_generic(va, h->umma, sp, per_cta, grid, s) : launch_value_umma(va, h->umma, s);
-        if (e != cudaSuccess) return cuda_fail(e, "value launch");
+    return enqueue_run(h, b, N, L, gamma, lambda, vs, (cudaStream_t)stream, nullptr);
+}
+
+int rollout_run_host(rollout_handle *h, const float *features, const int32_t *episode_starts, const uint32_t *seeds,
+                     int N, int L, float gamma, float lambda, float *out_states, int32_t *out_actions,
+                     float *out_logp, float *out_values, float *out_rewards, int32_t *out_dones, float *out_adv,
+                     float *out_ret, void *stream)
+{
+    g_err[0] = 0;
+    if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
+    if (!features || !episode_starts || !seeds) return fail(ROLLOUT_ERR_INVALID, "null input array");
+    int rc = check_run_args(h, N, L, gamma, lambda);
+    RunBuffers b{};
+    if (rc || (rc = make_copy_streams(h)) || (rc = stage_buffers(h, N, L, &b))) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+    const size_t nl = (size_t)N * L;
+    if ((e = cudaMemcpyAsync((void *)b.features, features, (size_t)h->dims.n_bars * kMarket * 4,
+                             cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync((void *)b.starts, episode_starts, (size_t)N * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync((void *)b.seeds, seeds, (size_t)N * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(inputs)");
+    if ((rc = enqueue_run(h, b, N, L, gamma, lambda, handle_scratch(h, N, L), s, h->point_ev))) return rc;
+
+    // Each output is copied back as soon as the kernel that finishes it is done;
+    // the large ones are split over the copy streams.  The caller's stream then
+    // waits for every copy stream, so the call stays stream-ordered.
+    const Download downloads[] = {
+        {out_actions, b.actions, nl * 4, kAfterRollout}, {out_logp, b.logp, nl * 4, kAfterRollout},
+        {out_dones, b.dones, nl * 4, kAfterRollout},     {out_states, b.states, nl * kState * 4, kAfterStates},
+        {out_values, b.values, nl * 4, kAfterValue},     {out_rewards, b.rewards, nl * 4, kAfterValue},
+        {out_adv, b.adv, nl * 4, kAfterGae},             {out_ret, b.ret, nl * 4, kAfterGae}};
+    constexpr size_t kSplitBytes = 64u << 20;   // outputs larger than this go out in kCopyStreams pieces
+    int next = 0;
+    for (int p = 0; p < kRunPoints; ++p) {
+        for (int k = 0; k < kCopyStreams; ++k)
+            if ((e = cudaStreamWaitEvent(h->copy_stream[k], h->point_ev[p], 0)) != cudaSuccess)
+                return cuda_fail(e, "cudaStreamWaitEvent");
+        for (const Download &dl : downloads) {
+            if (dl.point != p || !dl.host) continue;
+            const int pieces = dl.bytes > kSplitBytes ? kCopyStreams : 1;
+            const size_t piece = ((dl.bytes / pieces) + 255) & ~(size_t)255;
+            for (size_t at = 0; at < dl.bytes; at += piece) {
+                const size_t n = dl.bytes - at < piece ? dl.bytes - at : piece;
+                if ((e = cudaMemcpyAsync((uint8_t *)dl.host + at, (const uint8_t *)dl.dev + at, n,
+                                         cudaMemcpyDeviceToHost, h->copy_stream[next])) != cudaSuccess)
+                    return cuda_fail(e, "cudaMemcpyAsync(outputs)");
+                next = (next + 1) % kCopyStreams;
+            }
+        }
     }
-    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
-    if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    h->timed_run = h->timing;
+    for (int k = 0; k < kCopyStreams; ++k)
+        if ((e = cudaEventRecord(h->copy_done[k], h->copy_stream[k])) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(s, h->copy_done[k], 0)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord / cudaStreamWaitEvent");
     return ROLLOUT_OK;
 }
 
