@@ -137,18 +137,26 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const 
         // value-kernel consumption order (see value_umma.cu): 26 units of <= 32 KB
         begin_unit();
         P.tile(stream, C1, kCurH, kState + kActions, kState, 0, 64, 0);          // curiosity 1 (state part)
-        P.tile(stream, V[0], 512, vin[0], vin[0], 0, 64, 0);                      // layer-1 chunk 0
-        P.tile(stream, V[0], 512, vin[0], vin[0], 64, 64, 0);                     // layer-1 chunk 1
+        P.tile(stream, V[0], 512, vin[0], vin[0], 0, 128, 0);                     // layer-1 chunk 0 (128 rows)
         P.tile(stream, C2, kState, kCurH, kCurH, 0, 64, 0);                      // curiosity 2
         end_unit();
         for (int i = 0; i < 8; ++i) {
+            // K-chunk 0: rows 0-255 of W2, then rows 256-383; later K-chunks the other
+            // way round, for odd i < 7 with the next 128 layer-1 rows in front
+            if (i == 0) {
+                begin_unit();
+                P.tile(stream, V[1], 384, vin[1], vin[1], 0, 256, i);
+                end_unit();
+            }
             begin_unit();
-            P.tile(stream, V[1], 384, vin[1], vin[1], 0, 256, i);                // layer 2, K-chunk i, rows 0-255
+            if ((i & 1) && i < 7) P.tile(stream, V[0], 512, vin[0], vin[0], 128 * ((i + 1) / 2), 128, 0);
+            P.tile(stream, V[1], 384, vin[1], vin[1], 256, 128, i);
             end_unit();
-            begin_unit();
-            P.tile(stream, V[1], 384, vin[1], vin[1], 256, 128, i);              // rows 256-383
-            if (i + 2 < 8) P.tile(stream, V[0], 512, vin[0], vin[0], 64 * (i + 2), 64, 0);
-            end_unit();
+            if (i > 0) {
+                begin_unit();
+                P.tile(stream, V[1], 384, vin[1], vin[1], 0, 256, i);
+                end_unit();
+            }
         }
         const int order3[6] = {4, 5, 0, 1, 2, 3};
         for (int kk = 0; kk < 6; ++kk) {

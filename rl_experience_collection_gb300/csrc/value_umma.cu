@@ -28,17 +28,22 @@
 //   19    allocates TMEM; one lane issues the MMAs and commits
 //
 // Per tile the MMA lane runs (TMEM columns in brackets):
-//   CUR1 [0,64) = X C1^T ; D1_0 [384,448), D1_1 [448,512) = X W1[chunk]^T
+//   CUR1 [0,64) = X C1^T ; D1_0 [384,512) = X W1[rows 0..127]^T
 //   CUR2 [256,320) = Z C2^T                        (after the rows wrote Z)
 //   for i < 8:  D2 [0,384) += h1_i W2[:, chunk i]^T  (after rows wrote h1_i;
 //                 for i = 0 the columns [256,384) also wait for CUR2's drain)
-//               D1_{i+2} = X W1[chunk i+2]^T         (into the buffer h1_i left)
+//     odd i < 7, first: D1_c = X W1[rows 128c..]^T, c = (i+1)/2, into the
+//                 buffer the rows just emptied (h1_{i-1}, h1_i came from it)
 //   D3 [256,512) += h2_k W3^T, k = 4,5,0,1,2,3       (as the rows write h2_k)
 //   D4 [0,128)   += h3_k W4^T, k = 0..3
 //   D5 [128,192) += h4_k W5^T, k = 0..1
-// so layer 1 never exists whole (its 64-column chunks are produced while the
-// tensor pipe accumulates layer 2) and every later layer starts on its first
-// K-chunk while the rows still drain the rest of the previous one.  The rows
+// so layer 1 never exists whole (its 128-column chunks are produced while the
+// tensor pipe accumulates layer 2: N=128 MMAs cost the tensor pipe about what
+// N=64 ones do, so four of them replace eight) and every later layer starts on
+// its first K-chunk while the rows still drain the rest of the previous one.
+// A layer-1 chunk is issued ahead of layer 2's MMAs on h1 slot 1, so the rows
+// drain its second half into slot 1 only after a commit (acc_h1free) shows
+// that those MMAs are done.  The rows
 // build X and Z of the next tile at the end of the current one, and at the
 // start of a tile drain h1_0 before the curiosity error, so that layer 2
 // starts without waiting for the curiosity epilogues.
@@ -90,7 +95,7 @@ constexpr uint32_t kColCur1 = 0, kColCur2 = 256, kColD1 = 384, kColD2 = 0, kColD
 struct Bars {
     uint64_t full[kStages], empty[kStages];
     uint64_t act_x, act_z, act_cz, act_h1[2], act_h2[6], act_h3[4], act_h4[2];   // act_cz: CUR2 columns drained
-    uint64_t acc_cur, acc_d1[2], acc_main, final_;
+    uint64_t acc_cur, acc_d1, acc_h1free, acc_main, final_;   // acc_h1free: h1 slot 1 read
     uint64_t feat_full;        // the staged feature rows of the next tile have landed
     uint64_t feat_free;        // layer 3 has read slots 4-5: the next tile's rows may be staged there
 };
@@ -447,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         for (int i = 0; i < 4; ++i) mbar_init(&B.act_h3[i], kRowWarps);
         for (int i = 0; i < 2; ++i) mbar_init(&B.act_h4[i], kRowWarps);
         mbar_init(&B.acc_cur, 1);
-        mbar_init(&B.acc_d1[0], 1);
-        mbar_init(&B.acc_d1[1], 1);
+        mbar_init(&B.acc_d1, 1);
+        mbar_init(&B.acc_h1free, 1);
         mbar_init(&B.acc_main, 1);
         mbar_init(&B.final_, 1);
         mbar_init(&B.feat_full, 1);
@@ -559,27 +564,36 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 uint32_t u = take();
                 m.mma_chunk(kColCur1, m.slot(kXSlot), u, 64, false);
                 mma_commit(&B.acc_cur);
-                m.mma_chunk(kColD1, m.slot(kXSlot), u + 8192, 64, false);
-                mma_commit(&B.acc_d1[0]);
-                m.mma_chunk(kColD1 + 64, m.slot(kXSlot), u + 16384, 64, false);
-                mma_commit(&B.acc_d1[1]);
+                m.mma_chunk(kColD1, m.slot(kXSlot), u + 8192, 128, false);
+                mma_commit(&B.acc_d1);
                 m.wait(&B.act_z, ph_z);
                 m.mma_chunk(kColCur2, m.slot(kZSlot), u + 24576, 64, false);
                 mma_commit(&B.acc_cur);
                 release();
-                // ---- layer 2 over the h1 chunks (two units per K-chunk), layer-1 chunks two ahead
-                for (int i = 0; i < 8; ++i) {
+                // ---- layer 2 over the h1 chunks (two units per K-chunk): K-chunk 0 takes
+                // rows 0-255 of W2 first (the rest waits for CUR2's drain); every later
+                // one takes rows 256-383 first, for odd i preceded by the next layer-1 chunk
+                u = take();
+                m.wait(&B.act_h1[0], ph_h1[0]);
+                m.mma_chunk(kColD2, m.slot(0), u, 256, false);
+                release();
+                u = take();
+                m.wait(&B.act_cz, ph_cz);                      // D2 columns [256,384) begin where CUR2 was
+                m.mma_chunk(kColD2 + 256, m.slot(0), u, 128, false);
+                release();
+                for (int i = 1; i < 8; ++i) {
+                    const bool d1 = (i & 1) && i < 7;
                     u = take();
                     m.wait(&B.act_h1[i & 1], ph_h1[i & 1]);
-                    m.mma_chunk(kColD2, m.slot(i & 1), u, 256, i > 0);
+                    if (d1) {                                   // the rows have emptied the layer-1 buffer
+                        m.mma_chunk(kColD1, m.slot(kXSlot), u, 128, false);
+                        mma_commit(&B.acc_d1);
+                    }
+                    m.mma_chunk(kColD2 + 256, m.slot(i & 1), u + (d1 ? 16384 : 0), 128, true);
                     release();
                     u = take();
-                    if (i == 0) m.wait(&B.act_cz, ph_cz);   // D2 columns [256,384) begin where CUR2 was
-                    m.mma_chunk(kColD2 + 256, m.slot(i & 1), u, 128, i > 0);
-                    if (i + 2 < 8) {
-                        m.mma_chunk(kColD1 + 64 * (i & 1), m.slot(kXSlot), u + 16384, 64, false);
-                        mma_commit(&B.acc_d1[i & 1]);
-                    }
+                    m.mma_chunk(kColD2, m.slot(i & 1), u, 256, true);
+                    if (d1) mma_commit(&B.acc_h1free);         // h1 slot 1 may take the next chunk
                     release();
                 }
                 mma_commit(&B.acc_main);
@@ -622,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         const int r = 32 * (warp & 3) + lane;                 // operand row / TMEM lane
         const int q = warp >> 2;                               // column quarter of every 64-col chunk
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * q;
-        uint32_t ph_cur = 0, ph_d1[2] = {0, 0}, ph_main = 0, ph_feat = 0;
+        uint32_t ph_cur = 0, ph_d1 = 0, ph_free = 0, ph_main = 0, ph_feat = 0;
         bool ok = true;
         auto wait_acc = [&](uint64_t *bar, uint32_t &phase) {
             ok = __all_sync(0xffffffffu, ok && mbar_wait(bar, phase, abort));
@@ -670,8 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             const RowInfo ri = nri;
             const long long next = tile + gridDim.x;
             const bool has_next = next < n_tiles;
-            // ---- layer-1 chunk 0 first: the tensor pipe waits for it
-            wait_acc(&B.acc_d1[0], ph_d1[0]);
+            // ---- h1 chunk 0 first: the tensor pipe waits for it
+            wait_acc(&B.acc_d1, ph_d1);
             drain16(lane_addr + kColD1, bias + kB1 + 16 * q, slots, r, q);
             publish(&B.act_h1[0]);
             // ---- curiosity layer 2: squared error against the pre-reset next state
@@ -692,11 +706,18 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 part_s[q * 128 + r] = se;
                 publish(&B.act_cz);                            // its TMEM columns are layer 2's next
             }
-            // ---- layer-1 chunks 1..7 (the tensor pipe accumulates layer 2 meanwhile)
-            for (int c = 1; c < 8; ++c) {
-                wait_acc(&B.acc_d1[c & 1], ph_d1[c & 1]);
-                drain16(lane_addr + kColD1 + 64 * (c & 1), bias + kB1 + 64 * c + 16 * q, slots + (c & 1) * kSlot, r, q);
-                publish(&B.act_h1[c & 1]);
+            // ---- h1 chunks 1..7 (the tensor pipe accumulates layer 2 meanwhile): the
+            // first half of each layer-1 chunk goes to slot 0, the second to slot 1
+            // once layer 2 has read the chunk before it there
+            drain16(lane_addr + kColD1 + 64, bias + kB1 + 64 + 16 * q, slots + kSlot, r, q);
+            publish(&B.act_h1[1]);
+            for (int c = 1; c < 4; ++c) {
+                wait_acc(&B.acc_d1, ph_d1);
+                drain16(lane_addr + kColD1, bias + kB1 + 128 * c + 16 * q, slots, r, q);
+                publish(&B.act_h1[0]);
+                wait_acc(&B.acc_h1free, ph_free);
+                drain16(lane_addr + kColD1 + 64, bias + kB1 + 128 * c + 64 + 16 * q, slots + kSlot, r, q);
+                publish(&B.act_h1[1]);
             }
             // the next tile's row metadata: loads issued where the rows wait for
             // layer 2 anyway, consumed after layer 3
