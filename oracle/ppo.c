@@ -128,6 +128,45 @@ static void backward(const double *p, const net *n, const double *x, double act[
 }
 
 /*
+ * The smallest relative distance of any hidden pre-activation of the actor and
+ * the critic from the ReLU kink on each row: margin[i] = min over hidden units
+ * of |pre| / (|b| + sum |w x|).  Where it is of the order of float32 rounding,
+ * a float32 evaluation may take the other side of the kink (a floating-point
+ * decision, like an action drawn within rounding of a CDF boundary), and that
+ * row's gradient through every earlier layer changes with it.
+ */
+void ppo_kink_margin(const double *p, const ppo_shape *s, const float *states, const int32_t *rows, int B,
+                     double *margin)
+{
+    net an, cn;
+    layout(s, &an, &cn);
+    const int sd = s->n_market + 3;
+    double in[PPO_MAX_W], out[PPO_MAX_W];
+    const net *nets[2] = {&an, &cn};
+    for (int r = 0; r < B; ++r) {
+        double best = INFINITY;
+        for (int k = 0; k < 2; ++k) {
+            const net *n = nets[k];
+            for (int i = 0; i < sd; ++i) in[i] = (double)states[(long)rows[r] * sd + i];
+            for (int l = 0; l < n->n_layers - 1; ++l) {
+                for (int j = 0; j < n->out[l]; ++j) {
+                    double acc = p[n->b[l] + j], mag = fabs(p[n->b[l] + j]);
+                    for (int i = 0; i < n->in[l]; ++i) {
+                        const double t = p[n->w[l] + (long)j * n->in[l] + i] * in[i];
+                        acc += t;
+                        mag += fabs(t);
+                    }
+                    if (mag > 0.0 && fabs(acc) / mag < best) best = fabs(acc) / mag;
+                    out[j] = acc <= 0.0 ? 0.0 : acc;
+                }
+                memcpy(in, out, sizeof(double) * n->out[l]);
+            }
+        }
+        margin[r] = best;
+    }
+}
+
+/*
  * Loss and gradient of one mini-batch.  rows[i] indexes the tuple arrays
  * (states [T, n_market+3], actions, logp_old, adv, ret).  g (length
  * ppo_trained_count) is overwritten.  stats (optional): [0] surrogate loss,

@@ -75,6 +75,8 @@ def lib():
         L.ppo_update.restype = C.c_int
         L.ppo_update.argtypes = [vp, C.POINTER(Shape), C.POINTER(HP), vp, vp, vp, vp, vp, vp, C.c_int, C.c_int,
                                  vp, vp, C.POINTER(C.c_long), vp]
+        L.ppo_kink_margin.restype = None
+        L.ppo_kink_margin.argtypes = [vp, C.POINTER(Shape), vp, vp, C.c_int, vp]
         _lib = L
     return _lib
 
@@ -125,6 +127,16 @@ def loss_grad(params: np.ndarray, shape: Shape, hp: Hyper, b: Batch, rows: np.nd
     lib().ppo_loss_grad(_p(p), C.byref(shape), C.byref(h), _p(b.states), _p(b.actions), _p(b.logp), _p(b.adv),
                         _p(b.ret), _p(rows), len(rows), _p(g), _p(st))
     return st, g
+
+
+def kink_margin(params: np.ndarray, shape: Shape, b: Batch, rows: np.ndarray) -> np.ndarray:
+    """Per row, the smallest relative distance |pre| / (|b| + sum |w x|) of any hidden
+    pre-activation from the ReLU kink, at double parameters."""
+    p = np.ascontiguousarray(params, dtype=np.float64)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    out = np.zeros(len(rows), dtype=np.float64)
+    lib().ppo_kink_margin(_p(p), C.byref(shape), _p(b.states), _p(rows), len(rows), _p(out))
+    return out
 
 
 def adam_step(params: np.ndarray, grad: np.ndarray, m: np.ndarray, v: np.ndarray, t: int, hp: Hyper) -> float:

@@ -39,6 +39,21 @@ class RolloutDims(C.Structure):
     ]
 
 
+PPO_EXPORTS = ["ppo_create", "ppo_update", "ppo_gradient", "ppo_get_weights", "ppo_reset_optimizer", "ppo_status",
+               "ppo_destroy"]
+
+
+class PpoHparams(C.Structure):
+    """include/ppo.h ppo_hparams; defaults are the readings stated in the design notes."""
+    _fields_ = [(k, C.c_float) for k in ("clip_eps", "value_coef", "lr", "beta1", "beta2", "adam_eps",
+                                           "max_grad_norm", "weight_decay")]
+
+    @classmethod
+    def make(cls, clip_eps=0.2, value_coef=1.0, lr=3e-4, beta1=0.9, beta2=0.999, adam_eps=1e-8, max_grad_norm=0.5,
+             weight_decay=0.0):
+        return cls(clip_eps, value_coef, lr, beta1, beta2, adam_eps, max_grad_norm, weight_decay)
+
+
 class RolloutError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"rollout error {code}: {msg}")
@@ -80,6 +95,21 @@ def lib(path: Optional[str] = None):
     L.rollout_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
     L.rollout_last_error.restype = C.c_char_p
     L.rollout_last_error.argtypes = []
+    L.ppo_create.restype = C.c_int
+    L.ppo_create.argtypes = [vp, C.POINTER(RolloutDims), C.POINTER(vp)]
+    L.ppo_update.restype = C.c_int
+    L.ppo_update.argtypes = [vp, vp, vp, vp, vp, vp, C.c_longlong, vp, C.c_int, C.c_int, C.POINTER(PpoHparams),
+                             vp, vp]
+    L.ppo_gradient.restype = C.c_int
+    L.ppo_gradient.argtypes = [vp, vp, vp, vp, vp, vp, C.c_longlong, vp, C.c_int, C.POINTER(PpoHparams), vp, vp, vp]
+    L.ppo_get_weights.restype = C.c_int
+    L.ppo_get_weights.argtypes = [vp, vp, vp]
+    L.ppo_reset_optimizer.restype = C.c_int
+    L.ppo_reset_optimizer.argtypes = [vp, vp]
+    L.ppo_status.restype = C.c_int
+    L.ppo_status.argtypes = [vp]
+    L.ppo_destroy.restype = None
+    L.ppo_destroy.argtypes = [vp]
     _lib = L
     return L
 
@@ -215,6 +245,76 @@ class Rollout:
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:
             lib().rollout_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class PpoTrainer:
+    """Owns a ``ppo_trainer`` (include/ppo.h): a float32 device copy of the packed
+    weights and its Adam state."""
+
+    def __init__(self, weights, dims: RolloutDims):
+        import numpy as np
+        self._w = np.ascontiguousarray(weights, dtype=np.float32)
+        h = C.c_void_p()
+        _check(lib().ppo_create(self._w.ctypes.data_as(C.c_void_p), C.byref(dims), C.byref(h)))
+        self._h = h
+        self.n_weights = self._w.size
+
+    @classmethod
+    def for_workload(cls, w: wl.Workload, weights):
+        return cls(weights, make_dims(w))
+
+    def update(self, states, actions, logp_old, adv, ret, indices, n_steps: int, batch: int,
+               hp: Optional[PpoHparams] = None, stats=None, stream=None) -> None:
+        """Enqueues n_steps Adam steps; all arrays are device tensors (tuples flattened
+        over episode and step; indices int32, n_steps*batch of them)."""
+        hp = hp or PpoHparams.make()
+        T = actions.numel()
+        p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else C.c_void_p(None)
+        _check(lib().ppo_update(self._h, p(states), p(actions), p(logp_old), p(adv), p(ret), int(T), p(indices),
+                                int(n_steps), int(batch), C.byref(hp), p(stats), C.c_void_p(_stream_handle(stream))))
+
+    def gradient(self, states, actions, logp_old, adv, ret, indices, batch: int, grad, stats=None,
+                 hp: Optional[PpoHparams] = None, stream=None) -> None:
+        """Enqueues the loss statistics and gradient of one mini-batch at the current
+        weights (grad: a device float32 tensor of the actor + critic parameter count)."""
+        hp = hp or PpoHparams.make()
+        T = actions.numel()
+        p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else C.c_void_p(None)
+        _check(lib().ppo_gradient(self._h, p(states), p(actions), p(logp_old), p(adv), p(ret), int(T), p(indices),
+                                  int(batch), C.byref(hp), p(grad), p(stats), C.c_void_p(_stream_handle(stream))))
+
+    def weights(self, stream=None):
+        """The packed float32 weights, as a host numpy array (synchronises the stream)."""
+        import numpy as np
+        import torch
+        out = np.empty(self.n_weights, dtype=np.float32)
+        _check(lib().ppo_get_weights(self._h, out.ctypes.data_as(C.c_void_p), C.c_void_p(_stream_handle(stream))))
+        torch.cuda.synchronize()
+        return out
+
+    def reset_optimizer(self, stream=None) -> None:
+        _check(lib().ppo_reset_optimizer(self._h, C.c_void_p(_stream_handle(stream))))
+
+    def status(self) -> int:
+        return lib().ppo_status(self._h)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().ppo_destroy(self._h)
             self._h = C.c_void_p()
 
     def __del__(self):

@@ -317,6 +317,24 @@ void free_handle(rollout_handle *h)
 
 }  // namespace
 
+// shared with the PPO trainer (ppo.cu): one error message per host thread, one shape check
+namespace rl {
+
+int set_error(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+void clear_error() { g_err[0] = 0; }
+
+int validate_dims(const rollout_dims *d) { return check_dims(d); }
+
+}  // namespace rl
+
 extern "C" {
 
 const char *rollout_last_error(void) { return g_err; }

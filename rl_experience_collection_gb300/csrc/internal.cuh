@@ -120,4 +120,9 @@ cudaError_t launch_states(const StatesArgs &a, cudaStream_t s);
 // --- GAE (gae.cu) ---
 cudaError_t launch_gae(const GaeArgs &a, cudaStream_t s);
 
+// --- shared host helpers (api.cu) ---
+int set_error(int code, const char *fmt, ...);   // records the message rollout_last_error returns; returns code
+void clear_error();
+int validate_dims(const rollout_dims *d);         // the shapes rollout_create accepts
+
 }  // namespace rl

@@ -35,6 +35,31 @@ def test_library_exports_every_declared_symbol(libpath):
     assert set(binding.EXPORTS) == set(_declared())
 
 
+def _declared_ppo():
+    src = open(os.path.join(ROOT, "include", "ppo.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ppo_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_ppo_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    names = _declared_ppo()
+    assert "ppo_update" in names and "ppo_create" in names
+    for name in names:
+        assert hasattr(lib, name), name
+    from rl_experience_collection_gb300 import binding
+    assert set(binding.PPO_EXPORTS) == set(names)
+
+
+def test_ppo_hparams_field_order_matches_header():
+    from rl_experience_collection_gb300 import binding
+    src = open(os.path.join(ROOT, "include", "ppo.h")).read()
+    body = src[src.index("typedef struct {"):src.index("} ppo_hparams;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b([a-z_0-9]+)\s*(?=[,;])", body.replace("typedef struct {", "").replace("float", ""))
+    assert fields == [f for f, _ in binding.PpoHparams._fields_]
+
+
 def test_binding_struct_matches_header_field_order():
     from rl_experience_collection_gb300 import binding
     src = open(os.path.join(ROOT, "include", "rollout.h")).read()

@@ -120,6 +120,25 @@ def test_loss_and_gradient_are_means_over_rows(setup):
     np.testing.assert_allclose(g2[18221:], 2.0 * g_all[18221:], rtol=1e-12, atol=1e-18)
 
 
+def test_kink_margin_finds_a_pre_activation_at_zero(setup):
+    """A bias chosen to cancel one unit's sum on one row puts that row at the kink;
+    the other rows stay away from it."""
+    w, inp = setup
+    shape = ppo.shape_of(w.critic_h)
+    n = ppo.trained_count(shape)
+    b, _ = _batch(w, inp, 6, seed=8)
+    p = inp.weights[:n].astype(np.float64)
+    rows = np.arange(6, dtype=np.int32)
+    base = ppo.kink_margin(p, shape, b, rows)
+    assert np.all(base > 0)
+    W1 = p[:54 * 128].reshape(128, 54)
+    x = b.states[3].astype(np.float64)
+    p[54 * 128 + 5] = -(W1[5] @ x)                     # actor b1[5]: unit 5 of row 3 at exactly 0
+    mg = ppo.kink_margin(p, shape, b, rows)
+    assert mg[3] < 1e-15
+    assert np.all(mg[[0, 1, 2, 4, 5]] > 1e-12)
+
+
 def test_adam_first_step_and_global_norm_clip_closed_forms():
     rng = np.random.default_rng(5)
     n = 1000
