@@ -67,6 +67,60 @@ def value_sources_sha256():
     return hsh.hexdigest()
 
 
+PPO_BATCH = 512
+
+
+def ppo_flop_per_row(critic_h):
+    """Multiply-adds of one row through the PPO update's dense products, times 2:
+    forward and weight gradient for every layer, input gradient for every layer
+    but each network's first."""
+    actor = [(54, 128), (128, 64), (64, 45)]
+    dims = [54] + list(critic_h) + [1]
+    critic = list(zip(dims[:-1], dims[1:]))
+    macs = 0
+    for net in (actor, critic):
+        fwd = sum(i * o for i, o in net)
+        macs += 2 * fwd + (fwd - net[0][0] * net[0][1])
+    return 2 * macs
+
+
+def fp32_peak_tflops(sm_mhz):
+    """Derived float32 FMA peak: SMs x 128 FP32 lanes x 2 FLOP x clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def measure_ppo(w, weights, out, N, L, n_steps, warmup, dev):
+    """Times ppo_update on the collected tuples: n_steps Adam steps on mini-batches of
+    512 from a seeded permutation, CUDA events on the launching stream."""
+    import torch
+    from rl_experience_collection_gb300 import binding
+    T = N * L
+    tr = binding.PpoTrainer.for_workload(w, weights)
+    states = out["states"].reshape(-1, 54)
+    actions, logp, adv, ret = (out[k].reshape(-1) for k in ("actions", "logp", "adv", "ret"))
+    rng = np.random.default_rng(5)
+    idx = torch.from_numpy(rng.choice(T, size=(warmup + n_steps) * PPO_BATCH, replace=False).astype(np.int32)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    timed = idx[warmup * PPO_BATCH:]
+    # the warm-up call uses the timed call's arrays, so that the step graph it
+    # captures is the one the timed call replays
+    tr.update(states, actions, logp, adv, ret, timed, warmup, PPO_BATCH, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    tr.update(states, actions, logp, adv, ret, timed, n_steps, PPO_BATCH, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n_steps
+    if tr.status() != binding.ROLLOUT_OK:
+        raise SystemExit("PPO update status")
+    tr.close()
+    flop = ppo_flop_per_row(w.critic_h) * PPO_BATCH
+    return ms, flop
+
+
 def launches_per_run(dtype):
     """Kernels one rollout_run launches: feature padding (bf16 only), rollout,
     state rows, value, GAE."""
@@ -208,6 +262,8 @@ def main():
     ap.add_argument("--horizon", type=int, default=None, help="override the workload's horizon")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-ppo", action="store_true", help="skip the PPO-update measurement")
+    ap.add_argument("--ppo-steps", type=int, default=200, help="timed PPO optimizer steps (mini-batches of 512)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = wl.WORKLOADS[args.workload]
@@ -299,6 +355,17 @@ def main():
             "tensor_pipe_frac_step": (flop_step / (ms / 1000.0) / 1e12 / tpk) if tpk else None,
             "phase_ms": {"rollout": rollout_ms, "states": states_ms, "value": value_ms, "gae": gae_ms},
             "roofline": roofline, "clocks": clk.summary(), "gpu_launches": launches_per_run(w.dtype) * args.steps}
+
+    # ---------------- the PPO update on the collected tuples (rank 0 alone, float32)
+    if not args.no_ppo and rank == 0:
+        ms, flop = measure_ppo(w, inputs.weights, out, N, L, args.ppo_steps, 10, dev)
+        peak = fp32_peak_tflops(line["clocks"].get("sm_max_mhz") or 2070.0)
+        achieved = flop / (ms / 1000.0) / 1e12
+        line["ppo_update"] = {"batch": PPO_BATCH, "steps": args.ppo_steps, "ms_per_step": ms,
+                              "tuples_per_s": PPO_BATCH / (ms / 1000.0), "flop_per_step": flop,
+                              "achieved_tflops": achieved, "peak_tflops": peak,
+                              "peak_kind": "fp32 FMA, derived: SMs x 128 lanes x 2 x max SM clock",
+                              "frac": achieved / peak, "bound": "alu"}
 
     # ---------------- end to end through the C ABI with host buffers (rollout_run_host:
     # inputs copied in, every output copied back as soon as its kernel is done)

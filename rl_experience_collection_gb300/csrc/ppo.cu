@@ -15,8 +15,14 @@
 // the gather, bias, ReLU, loss heads, bias gradients, the norm and Adam are the
 // kernels below.  Every reduction runs in a fixed order (per column, per
 // block, then over the blocks), so a step's result does not depend on timing.
+// One optimizer step is captured as a CUDA graph (about 55 launches) and
+// replayed for every step of a call: the step's mini-batch slice, statistics
+// slot and Adam step count are read from device counters that a last 1-thread
+// kernel advances, so that the same graph serves every step.
 #include <cublas_v2.h>
 #include <math.h>
+#include <string.h>
+
 #include <new>
 
 #include "../../include/ppo.h"
@@ -32,10 +38,27 @@ constexpr int kMaxWidth = 1024;
 constexpr int kNormBlocks = 304;   // fixed, so that the norm's summation order is fixed
 constexpr int kNormThreads = 256;
 
+constexpr int kGraphMinSteps = 4;              // calls with fewer steps launch directly
+constexpr size_t kBlasWorkspace = 32u << 20;   // cuBLAS workspace, fixed so that capture allocates nothing
+
 struct Net {
     int n = 0;
     size_t w[kMaxLayers] = {}, b[kMaxLayers] = {};
     int in[kMaxLayers] = {}, out[kMaxLayers] = {};
+};
+
+// what a captured step depends on besides the trainer's own buffers
+struct GraphKey {
+    const void *ptr[7] = {};           // states, actions, logp_old, adv, ret, indices, stats
+    long long T = 0;
+    int batch = 0;
+    ppo_hparams hp{};
+    bool operator==(const GraphKey &o) const
+    {
+        for (int i = 0; i < 7; ++i)
+            if (ptr[i] != o.ptr[i]) return false;
+        return T == o.T && batch == o.batch && memcmp(&hp, &o.hp, sizeof hp) == 0;
+    }
 };
 
 }  // namespace
@@ -56,8 +79,14 @@ struct ppo_trainer {
     float *d_rows = nullptr;           // per-row statistics [4][cap]
     double *d_part = nullptr;          // [kNormBlocks] partial sums of g^2
     int *d_status = nullptr;
+    int *d_k = nullptr;                // step index within the current call
+    long long *d_t = nullptr;          // Adam step count
     cublasHandle_t blas = nullptr;
+    void *d_ws = nullptr;              // cuBLAS workspace
     cudaStream_t last_stream = nullptr;
+    cudaStream_t cap_stream = nullptr; // where one step is captured
+    cudaGraphExec_t exec = nullptr;
+    GraphKey key;
 };
 
 namespace {
@@ -78,11 +107,11 @@ int blas_err(cublasStatus_t st, const char *what)
 
 // one block per mini-batch row: copy the tuple the index names
 __global__ void gather_kernel(const float *states, const int32_t *actions, const float *logp_old,
-                              const float *adv, const float *ret, long long T, const int32_t *idx, float *x,
-                              int32_t *a, float *lpo, float *A, float *R, int *status)
+                              const float *adv, const float *ret, long long T, const int32_t *idx_base,
+                              const int *step_k, float *x, int32_t *a, float *lpo, float *A, float *R, int *status)
 {
     const int r = blockIdx.x;
-    long long i = idx[r];
+    long long i = idx_base[(size_t)*step_k * gridDim.x + r];
     if (i < 0 || i >= T) {
         if (threadIdx.x == 0) atomicCAS(status, 0, ROLLOUT_ERR_RANGE);
         i = 0;
@@ -154,14 +183,25 @@ __global__ void critic_head_kernel(const float *v, const float *R, int B, float 
     dv[r] = 2.f * value_coef * d / (float)B;
 }
 
-// db[j] = sum over rows of dY[r, j], in row order (double)
-__global__ void bias_grad_kernel(const float *dY, int rows, int n, float *db)
+// db[j] = sum over rows of dY[r, j] (double): a block takes 32 columns; row
+// group y (of 8) sums rows y, y+8, ... in order, then the groups are added in
+// order, so the result does not depend on scheduling
+constexpr int kBgCols = 32, kBgGroups = 8;
+__global__ void __launch_bounds__(kBgCols * kBgGroups) bias_grad_kernel(const float *dY, int rows, int n, float *db)
 {
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= n) return;
+    __shared__ double part[kBgGroups][kBgCols];
+    const int c = threadIdx.x % kBgCols, y = threadIdx.x / kBgCols;
+    const int j = blockIdx.x * kBgCols + c;
     double s = 0.0;
-    for (int r = 0; r < rows; ++r) s += (double)dY[(size_t)r * n + j];
-    db[j] = (float)s;
+    if (j < n)
+        for (int r = y; r < rows; r += kBgGroups) s += (double)dY[(size_t)r * n + j];
+    part[y][c] = s;
+    __syncthreads();
+    if (y == 0 && j < n) {
+        double t = 0.0;
+        for (int k = 0; k < kBgGroups; ++k) t += part[k][c];
+        db[j] = (float)t;
+    }
 }
 
 // ReLU' of the layer whose output is H: dX = 0 where H = 0
@@ -198,11 +238,15 @@ __global__ void __launch_bounds__(kNormThreads) norm_partial_kernel(const float 
 // every block first sums the partials in the same order (so all see the same
 // norm), then updates its share of the parameters
 __global__ void __launch_bounds__(kNormThreads) adam_kernel(float *p, const float *g, float *m, float *v, size_t n,
-                                                             const double *part, ppo_hparams hp, float bc1, float bc2,
-                                                             float *norm_out)
+                                                             const double *part, ppo_hparams hp, const long long *step_t,
+                                                             const int *step_k, float *stats)
 {
-    __shared__ float sh_scale;
+    __shared__ float sh_scale, sh_bc1, sh_bc2;
     if (threadIdx.x == 0) {
+        const double t = (double)(*step_t + 1);
+        sh_bc1 = (float)(1.0 - pow((double)hp.beta1, t));
+        sh_bc2 = (float)(1.0 - pow((double)hp.beta2, t));
+        float *norm_out = stats ? stats + (size_t)*step_k * 5 + 4 : nullptr;
         double ss = 0.0;
         for (int b = 0; b < kNormBlocks; ++b) ss += part[b];
         const double norm = sqrt(ss);
@@ -212,7 +256,7 @@ __global__ void __launch_bounds__(kNormThreads) adam_kernel(float *p, const floa
         if (blockIdx.x == 0 && norm_out) *norm_out = (float)norm;
     }
     __syncthreads();
-    const float scale = sh_scale;
+    const float scale = sh_scale, bc1 = sh_bc1, bc2 = sh_bc2;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const float gi = g[i] * scale;
         const float mi = hp.beta1 * m[i] + (1.f - hp.beta1) * gi;
@@ -224,16 +268,24 @@ __global__ void __launch_bounds__(kNormThreads) adam_kernel(float *p, const floa
     }
 }
 
-// means of the four per-row statistics, in row order
-__global__ void stats_kernel(const float *rows, int B, float *out)
+// means of the four per-row statistics, in row order, into slot step_k of stats
+__global__ void stats_kernel(const float *rows, int B, float *stats, const int *step_k)
 {
     __shared__ double sh[256];
+    float *out = stats + (size_t)*step_k * 5;
     for (int k = 0; k < 4; ++k) {
         double s = 0.0;
         for (int r = threadIdx.x; r < B; r += blockDim.x) s += (double)rows[k * B + r];
         s = block_sum(s, sh);
         if (threadIdx.x == 0) out[k] = (float)(s / B);
     }
+}
+
+// the end of a step: the next step's slice and Adam count
+__global__ void advance_kernel(int *step_k, long long *step_t)
+{
+    *step_k += 1;
+    *step_t += 1;
 }
 
 // ------------------------------------------------------------------ host side
@@ -268,6 +320,10 @@ void free_batch(ppo_trainer *t)
 int ensure_batch(ppo_trainer *t, int B)
 {
     if (B <= t->cap) return ROLLOUT_OK;
+    if (t->exec) {   // the captured step names the old buffers
+        cudaGraphExecDestroy(t->exec);
+        t->exec = nullptr;
+    }
     free_batch(t);   // cudaFree waits for work that may still use the old buffers
     cudaError_t e;
 #define ALLOC(p, bytes) if ((e = cudaMalloc(&(p), (bytes))) != cudaSuccess) { free_batch(t); return cuda_err(e, "cudaMalloc(mini-batch)"); }
@@ -296,7 +352,12 @@ void free_trainer(ppo_trainer *t)
     cudaFree(t->d_v);
     cudaFree(t->d_part);
     cudaFree(t->d_status);
+    cudaFree(t->d_k);
+    cudaFree(t->d_t);
+    if (t->exec) cudaGraphExecDestroy(t->exec);
     if (t->blas) cublasDestroy(t->blas);
+    cudaFree(t->d_ws);
+    if (t->cap_stream) cudaStreamDestroy(t->cap_stream);
     delete t;
 }
 
@@ -345,7 +406,8 @@ int backward(ppo_trainer *t, int k, int B, cudaStream_t s)
         const float *in = l == 0 ? t->d_x : t->d_act[k][l - 1];
         cublasStatus_t st = gemm_dw(t->blas, in, dy, t->d_g + n.w[l], B, n.in[l], n.out[l]);
         if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "weight-gradient GEMM");
-        bias_grad_kernel<<<(n.out[l] + 127) / 128, 128, 0, s>>>(dy, B, n.out[l], t->d_g + n.b[l]);
+        bias_grad_kernel<<<(n.out[l] + kBgCols - 1) / kBgCols, kBgCols * kBgGroups, 0, s>>>(dy, B, n.out[l],
+                                                                                          t->d_g + n.b[l]);
         if (l == 0) break;
         st = gemm_dx(t->blas, t->d_w + n.w[l], dy, dx, B, n.in[l], n.out[l]);
         if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "input-gradient GEMM");
@@ -382,14 +444,14 @@ int check_update_args(ppo_trainer *t, const float *states, const int32_t *action
 }
 
 // the loss statistics (per row, in d_rows) and the gradient (d_g) of the
-// mini-batch rows[0..B) at the current weights
+// mini-batch rows[d_k * B .. d_k * B + B) at the current weights
 int loss_gradient(ppo_trainer *t, const float *states, const int32_t *actions, const float *logp_old,
                   const float *adv, const float *ret, long long T, const int32_t *rows, int B, const ppo_hparams *hp,
                   cudaStream_t s)
 {
     int rc;
-    gather_kernel<<<B, 64, 0, s>>>(states, actions, logp_old, adv, ret, T, rows, t->d_x, t->d_a, t->d_lpo, t->d_adv,
-                                   t->d_ret, t->d_status);
+    gather_kernel<<<B, 64, 0, s>>>(states, actions, logp_old, adv, ret, T, rows, t->d_k, t->d_x, t->d_a, t->d_lpo,
+                                   t->d_adv, t->d_ret, t->d_status);
     // actor: log-probs, surrogate, its gradient
     if ((rc = forward(t, 0, B, s))) return rc;
     actor_head_kernel<<<(B * 32 + 255) / 256, 256, 0, s>>>(t->d_act[0][2], t->d_a, t->d_lpo, t->d_adv, B,
@@ -400,6 +462,55 @@ int loss_gradient(ppo_trainer *t, const float *states, const int32_t *actions, c
     critic_head_kernel<<<(B + 255) / 256, 256, 0, s>>>(t->d_act[1][kCriticLayers - 1], t->d_ret, B, hp->value_coef,
                                                        t->d_da, t->d_rows);
     return backward(t, 1, B, s);
+}
+
+// one optimizer step (the counters pick the mini-batch, the statistics slot and t)
+int step(ppo_trainer *t, const float *states, const int32_t *actions, const float *logp_old, const float *adv,
+         const float *ret, long long T, const int32_t *indices, int B, const ppo_hparams *hp, float *stats,
+         cudaStream_t s)
+{
+    cublasStatus_t st = cublasSetStream(t->blas, s);
+    if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "cublasSetStream");
+    int rc = loss_gradient(t, states, actions, logp_old, adv, ret, T, indices, B, hp, s);
+    if (rc) return rc;
+    norm_partial_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_g, t->n_trained, t->d_part);
+    adam_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_w, t->d_g, t->d_m, t->d_v, t->n_trained, t->d_part, *hp,
+                                                     t->d_t, t->d_k, stats);
+    if (stats) stats_kernel<<<1, 256, 0, s>>>(t->d_rows, B, stats, t->d_k);
+    advance_kernel<<<1, 1, 0, s>>>(t->d_k, t->d_t);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ROLLOUT_OK : cuda_err(e, "PPO step launch");
+}
+
+// the graph of one step for these arguments (captured on the trainer's own
+// stream; reused while the arguments stay the same)
+int step_graph(ppo_trainer *t, const GraphKey &key, const float *states, const int32_t *actions,
+               const float *logp_old, const float *adv, const float *ret, long long T, const int32_t *indices, int B,
+               const ppo_hparams *hp, float *stats)
+{
+    if (t->exec && t->key == key) return ROLLOUT_OK;
+    if (t->exec) {
+        cudaGraphExecDestroy(t->exec);
+        t->exec = nullptr;
+    }
+    cudaError_t e = cudaStreamBeginCapture(t->cap_stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_err(e, "cudaStreamBeginCapture");
+    int rc = step(t, states, actions, logp_old, adv, ret, T, indices, B, hp, stats, t->cap_stream);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(t->cap_stream, &g);
+    if (rc) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+    }
+    if (e != cudaSuccess) return cuda_err(e, "cudaStreamEndCapture");
+    e = cudaGraphInstantiate(&t->exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+        t->exec = nullptr;
+        return cuda_err(e, "cudaGraphInstantiate");
+    }
+    t->key = key;
+    return ROLLOUT_OK;
 }
 
 }  // namespace
@@ -445,23 +556,33 @@ int ppo_create(const float *weights, const rollout_dims *dims, ppo_trainer **out
         (e = cudaMalloc(&t->d_m, t->n_trained * 4)) != cudaSuccess ||
         (e = cudaMalloc(&t->d_v, t->n_trained * 4)) != cudaSuccess ||
         (e = cudaMalloc(&t->d_part, kNormBlocks * sizeof(double))) != cudaSuccess ||
-        (e = cudaMalloc(&t->d_status, sizeof(int))) != cudaSuccess) {
+        (e = cudaMalloc(&t->d_status, sizeof(int))) != cudaSuccess ||
+        (e = cudaMalloc(&t->d_k, sizeof(int))) != cudaSuccess ||
+        (e = cudaMalloc(&t->d_t, sizeof(long long))) != cudaSuccess ||
+        (e = cudaMalloc(&t->d_ws, kBlasWorkspace)) != cudaSuccess) {
         free_trainer(t);
         return cuda_err(e, "cudaMalloc(trainer)");
+    }
+    if ((e = cudaStreamCreateWithFlags(&t->cap_stream, cudaStreamNonBlocking)) != cudaSuccess) {
+        free_trainer(t);
+        return cuda_err(e, "cudaStreamCreateWithFlags");
     }
     if ((e = cudaMemcpy(t->d_w, weights, t->n_weights * 4, cudaMemcpyHostToDevice)) != cudaSuccess ||
         (e = cudaMemset(t->d_m, 0, t->n_trained * 4)) != cudaSuccess ||
         (e = cudaMemset(t->d_v, 0, t->n_trained * 4)) != cudaSuccess ||
-        (e = cudaMemset(t->d_status, 0, sizeof(int))) != cudaSuccess) {
+        (e = cudaMemset(t->d_status, 0, sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(t->d_k, 0, sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(t->d_t, 0, sizeof(long long))) != cudaSuccess) {
         free_trainer(t);
         return cuda_err(e, "trainer upload");
     }
     cublasStatus_t st = cublasCreate(&t->blas);
     if (st != CUBLAS_STATUS_SUCCESS) { free_trainer(t); return blas_err(st, "cublasCreate"); }
     // float32 GEMMs: no TF32 or other reduced-precision math
-    if ((st = cublasSetMathMode(t->blas, CUBLAS_PEDANTIC_MATH)) != CUBLAS_STATUS_SUCCESS) {
+    if ((st = cublasSetMathMode(t->blas, CUBLAS_PEDANTIC_MATH)) != CUBLAS_STATUS_SUCCESS ||
+        (st = cublasSetWorkspace(t->blas, t->d_ws, kBlasWorkspace)) != CUBLAS_STATUS_SUCCESS) {
         free_trainer(t);
-        return blas_err(st, "cublasSetMathMode");
+        return blas_err(st, "cuBLAS setup");
     }
     *out = t;
     return ROLLOUT_OK;
@@ -475,25 +596,26 @@ int ppo_update(ppo_trainer *t, const float *states, const int32_t *actions, cons
     if (n_steps < 0) return set_error(ROLLOUT_ERR_INVALID, "n_steps must be >= 0");
     int rc = check_update_args(t, states, actions, logp_old, adv, ret, T, indices, batch, hp);
     if (rc) return rc;
-    cudaError_t e;
     cudaStream_t s = (cudaStream_t)stream;
     t->last_stream = s;
-    cublasStatus_t st = cublasSetStream(t->blas, s);
-    if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "cublasSetStream");
-    const int B = batch;
-    for (int k = 0; k < n_steps; ++k) {
-        rc = loss_gradient(t, states, actions, logp_old, adv, ret, T, indices + (size_t)k * B, B, hp, s);
-        if (rc) return rc;
-        // clip to the global norm, Adam
-        t->step += 1;
-        const float bc1 = (float)(1.0 - pow((double)hp->beta1, (double)t->step));
-        const float bc2 = (float)(1.0 - pow((double)hp->beta2, (double)t->step));
-        norm_partial_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_g, t->n_trained, t->d_part);
-        adam_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_w, t->d_g, t->d_m, t->d_v, t->n_trained, t->d_part,
-                                                         *hp, bc1, bc2, stats ? stats + (size_t)k * 5 + 4 : nullptr);
-        if (stats) stats_kernel<<<1, 256, 0, s>>>(t->d_rows, B, stats + (size_t)k * 5);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "PPO update launch");
+    if (n_steps == 0) return ROLLOUT_OK;
+    cudaError_t e = cudaMemsetAsync(t->d_k, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_err(e, "cudaMemsetAsync(step index)");
+    if (n_steps >= kGraphMinSteps) {
+        GraphKey key;
+        const void *ptrs[7] = {states, actions, logp_old, adv, ret, indices, stats};
+        memcpy(key.ptr, ptrs, sizeof ptrs);
+        key.T = T;
+        key.batch = batch;
+        key.hp = *hp;
+        if ((rc = step_graph(t, key, states, actions, logp_old, adv, ret, T, indices, batch, hp, stats))) return rc;
+        for (int k = 0; k < n_steps; ++k)
+            if ((e = cudaGraphLaunch(t->exec, s)) != cudaSuccess) return cuda_err(e, "cudaGraphLaunch");
+    } else {
+        for (int k = 0; k < n_steps; ++k)
+            if ((rc = step(t, states, actions, logp_old, adv, ret, T, indices, batch, hp, stats, s))) return rc;
     }
+    t->step += n_steps;
     return ROLLOUT_OK;
 }
 
@@ -509,9 +631,11 @@ int ppo_gradient(ppo_trainer *t, const float *states, const int32_t *actions, co
     t->last_stream = s;
     cublasStatus_t st = cublasSetStream(t->blas, s);
     if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "cublasSetStream");
+    cudaError_t e = cudaMemsetAsync(t->d_k, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_err(e, "cudaMemsetAsync(step index)");
     if ((rc = loss_gradient(t, states, actions, logp_old, adv, ret, T, indices, batch, hp, s))) return rc;
-    if (stats) stats_kernel<<<1, 256, 0, s>>>(t->d_rows, batch, stats);
-    cudaError_t e = cudaMemcpyAsync(grad, t->d_g, t->n_trained * 4, cudaMemcpyDefault, s);
+    if (stats) stats_kernel<<<1, 256, 0, s>>>(t->d_rows, batch, stats, t->d_k);
+    e = cudaMemcpyAsync(grad, t->d_g, t->n_trained * 4, cudaMemcpyDefault, s);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? ROLLOUT_OK : cuda_err(e, "PPO gradient");
 }
@@ -530,7 +654,8 @@ int ppo_reset_optimizer(ppo_trainer *t, void *stream)
     if (!t) return set_error(ROLLOUT_ERR_INVALID, "null trainer");
     cudaError_t e;
     if ((e = cudaMemsetAsync(t->d_m, 0, t->n_trained * 4, (cudaStream_t)stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(t->d_v, 0, t->n_trained * 4, (cudaStream_t)stream)) != cudaSuccess)
+        (e = cudaMemsetAsync(t->d_v, 0, t->n_trained * 4, (cudaStream_t)stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(t->d_t, 0, sizeof(long long), (cudaStream_t)stream)) != cudaSuccess)
         return cuda_err(e, "cudaMemsetAsync(moments)");
     t->step = 0;
     return ROLLOUT_OK;

@@ -136,28 +136,35 @@ def test_update_matches_oracle_batch_512_without_clip_with_decay(tuples):
                     dict(lr=1e-3, max_grad_norm=0.0, weight_decay=1e-4, clip_eps=0.1, value_coef=0.5))
 
 
-def test_multi_step_call_equals_single_steps(tuples):
-    """n_steps in one call runs the same steps as n calls of one step."""
+@pytest.mark.parametrize("n", [3, 6])
+def test_multi_step_call_equals_single_steps(tuples, n):
+    """n steps in one call (3: launched directly; 6: one captured step replayed)
+    equal n calls of one step; after reset_optimizer a trainer repeats its first step."""
     import torch
     from rl_experience_collection_gb300 import binding
     w, inp, g = tuples
     T = g["actions"].size
-    idx = np.random.default_rng(14).permutation(T)[:3 * 50].astype(np.int32)
+    idx = np.random.default_rng(14).permutation(T)[:n * 50].astype(np.int32)
     states, actions, logp, adv, ret = _device(g)
     a = binding.PpoTrainer.for_workload(w, inp.weights)
-    st_a = torch.zeros((3, 5), dtype=torch.float32, device="cuda")
-    a.update(states, actions, logp, adv, ret, torch.from_numpy(idx).cuda(), 3, 50, stats=st_a)
+    st_a = torch.zeros((n, 5), dtype=torch.float32, device="cuda")
+    a.update(states, actions, logp, adv, ret, torch.from_numpy(idx).cuda(), n, 50, stats=st_a)
     b = binding.PpoTrainer.for_workload(w, inp.weights)
-    st_b = torch.zeros((3, 5), dtype=torch.float32, device="cuda")
-    for k in range(3):
+    st_b = torch.zeros((n, 5), dtype=torch.float32, device="cuda")
+    for k in range(n):
         b.update(states, actions, logp, adv, ret, torch.from_numpy(idx[50 * k:50 * k + 50].copy()).cuda(), 1, 50,
                  stats=st_b[k:k + 1])
     np.testing.assert_array_equal(a.weights(), b.weights())
     np.testing.assert_array_equal(st_a.cpu().numpy(), st_b.cpu().numpy())
-    # the optimizer reset starts the bias correction again: the first step repeats
-    b.reset_optimizer()
-    a.close()
-    b.close()
+    # a fresh trainer's first step equals a reset trainer's first step from the same weights
+    c = binding.PpoTrainer(a.weights(), binding.make_dims(w))
+    a.reset_optimizer()
+    first = torch.from_numpy(idx[:50].copy()).cuda()
+    a.update(states, actions, logp, adv, ret, first, 1, 50)
+    c.update(states, actions, logp, adv, ret, first, 1, 50)
+    np.testing.assert_array_equal(a.weights(), c.weights())
+    for tr in (a, b, c):
+        tr.close()
 
 
 def test_update_is_deterministic_and_reports_out_of_range_indices(tuples):
