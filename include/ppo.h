@@ -99,6 +99,12 @@ ROLLOUT_API int ppo_gradient(ppo_trainer *t, const float *states, const int32_t 
  * destination, n_weights floats) after the work enqueued on `stream`. */
 ROLLOUT_API int ppo_get_weights(ppo_trainer *t, float *weights, void *stream);
 
+/* ppo_device_weights -- the trainer's own device array of the packed float32
+ * weights (n_weights floats), which ppo_update rewrites in place; valid until
+ * ppo_destroy.  Pass it to rollout_set_weights_device, on the stream of the
+ * updates, to refresh a rollout handle with no copy. */
+ROLLOUT_API int ppo_device_weights(ppo_trainer *t, const float **weights);
+
 /* ppo_reset_optimizer -- zero the Adam moments and the step count (on `stream`). */
 ROLLOUT_API int ppo_reset_optimizer(ppo_trainer *t, void *stream);
 

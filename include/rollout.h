@@ -108,6 +108,21 @@ ROLLOUT_API int rollout_create(const float *weights, const rollout_dims *dims, r
 ROLLOUT_API int rollout_set_weights(rollout_handle *h, const float *weights);
 
 /*
+ * rollout_set_weights_device -- rollout_set_weights from a DEVICE array of
+ * the packed float32 weights (the layout rollout_create takes; for example a
+ * PPO trainer's, see ppo.h), with no host round trip.  Enqueued on `stream`:
+ * it rewrites the handle's converted weights element by element, rounding as
+ * rollout_create does, so a later rollout_run on the same stream computes
+ * what it would after rollout_set_weights with the same values.  `weights`
+ * (caller-owned, 4-byte aligned) must stay valid until the work completes;
+ * its values are not checked for finiteness, unlike rollout_set_weights.
+ * Runs on the handle must be ordered after it (one stream, or an event).
+ * (An addition of this library: the pages copy the updated weights from the
+ * host.)  Returns ROLLOUT_OK, _INVALID or _CUDA.
+ */
+ROLLOUT_API int rollout_set_weights_device(rollout_handle *h, const float *weights, void *stream);
+
+/*
  * rollout_run -- collect N x L experience tuples, including GAE.
  *
  * All array pointers are DEVICE pointers owned by the caller, 16-byte

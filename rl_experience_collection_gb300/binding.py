@@ -25,7 +25,8 @@ ROLLOUT_ERR_NOMEM = -6
 DTYPE = {"fp32": 0, "tf32": 1, "bf16": 2}
 
 EXPORTS = ["rollout_create", "rollout_set_weights", "rollout_run", "rollout_status", "rollout_destroy",
-           "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static", "rollout_run_host"]
+           "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static", "rollout_run_host",
+           "rollout_set_weights_device"]
 
 
 class RolloutDims(C.Structure):
@@ -40,6 +41,7 @@ class RolloutDims(C.Structure):
 
 
 PPO_EXPORTS = ["ppo_create", "ppo_update", "ppo_gradient", "ppo_get_weights", "ppo_reset_optimizer", "ppo_status",
+               "ppo_device_weights",
                "ppo_destroy"]
 
 
@@ -78,6 +80,8 @@ def lib(path: Optional[str] = None):
     L.rollout_create.argtypes = [vp, C.POINTER(RolloutDims), C.POINTER(vp)]
     L.rollout_set_weights.restype = C.c_int
     L.rollout_set_weights.argtypes = [vp, vp]
+    L.rollout_set_weights_device.restype = C.c_int
+    L.rollout_set_weights_device.argtypes = [vp, vp, vp]
     L.rollout_run.restype = C.c_int
     L.rollout_run.argtypes = [vp, vp, vp, vp, C.c_int, C.c_int, C.c_float, C.c_float,
                               vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -95,6 +99,8 @@ def lib(path: Optional[str] = None):
     L.rollout_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
     L.rollout_last_error.restype = C.c_char_p
     L.rollout_last_error.argtypes = []
+    L.ppo_device_weights.restype = C.c_int
+    L.ppo_device_weights.argtypes = [vp, C.POINTER(vp)]
     L.ppo_create.restype = C.c_int
     L.ppo_create.argtypes = [vp, C.POINTER(RolloutDims), C.POINTER(vp)]
     L.ppo_update.restype = C.c_int
@@ -177,6 +183,18 @@ class Rollout:
         import numpy as np
         self._w = np.ascontiguousarray(weights, dtype=np.float32)
         _check(lib().rollout_set_weights(self._h, self._w.ctypes.data_as(C.c_void_p)))
+
+    def set_weights_device(self, weights, stream=None) -> None:
+        """rollout_set_weights_device: enqueues the refresh from a contiguous float32
+        CUDA tensor of the packed weights, or a device address of them (for example
+        PpoTrainer.device_weights())."""
+        if isinstance(weights, int):
+            ptr = weights
+        elif weights.is_cuda and weights.is_contiguous() and weights.dtype.itemsize == 4:
+            ptr = weights.data_ptr()
+        else:
+            raise ValueError("weights must be a contiguous float32 CUDA tensor or a device address")
+        _check(lib().rollout_set_weights_device(self._h, C.c_void_p(ptr), C.c_void_p(_stream_handle(stream))))
 
     def run(self, features, starts, seeds, N: int, L: int, gamma: float, lam: float,
             out: Dict[str, "torch.Tensor"], stream=None) -> None:
@@ -305,6 +323,20 @@ class PpoTrainer:
         _check(lib().ppo_get_weights(self._h, out.ctypes.data_as(C.c_void_p), C.c_void_p(_stream_handle(stream))))
         torch.cuda.synchronize()
         return out
+
+    def weights_into(self, out, stream=None) -> None:
+        """Enqueues a device-to-device copy of the packed float32 weights into `out`
+        (a contiguous float32 CUDA tensor of n_weights elements); no synchronisation."""
+        if not (out.is_cuda and out.is_contiguous()) or out.numel() != self.n_weights or out.dtype.itemsize != 4:
+            raise ValueError("out must be a contiguous float32 CUDA tensor of n_weights elements")
+        _check(lib().ppo_get_weights(self._h, C.c_void_p(out.data_ptr()), C.c_void_p(_stream_handle(stream))))
+
+    def device_weights(self) -> int:
+        """ppo_device_weights: the address of the trainer's own device weights (updated
+        in place by update()), for Rollout.set_weights_device."""
+        p = C.c_void_p()
+        _check(lib().ppo_device_weights(self._h, C.byref(p)))
+        return p.value
 
     def reset_optimizer(self, stream=None) -> None:
         _check(lib().ppo_reset_optimizer(self._h, C.c_void_p(_stream_handle(stream))))

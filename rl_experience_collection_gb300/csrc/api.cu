@@ -79,6 +79,16 @@ struct rollout_handle {
     cudaStream_t copy_stream[kCopyStreams] = {};
     cudaEvent_t point_ev[kRunPoints] = {};
     cudaEvent_t copy_done[kCopyStreams] = {};
+    // rollout_set_weights_device: per region of the converted device weights,
+    // the source of each element in the packed float32 vector
+    struct Region {
+        uint8_t *dev;
+        const int32_t *map;
+        long long n;
+        int elem;
+    } repack[4] = {};
+    int n_repack = 0;
+    int32_t *d_maps = nullptr;
 };
 
 namespace {
@@ -155,10 +165,18 @@ void transpose_into(std::vector<float> &dst, size_t at, const float *W, int out,
 }
 
 // float32 path: actor packed for phase 1, critic/curiosity transposed for phase 2
-int upload_simt(rollout_handle *h, const float *w)
+struct SimtHost {
+    std::vector<float> ap, sp;
+    size_t offs_T[kCriticLayers], offs_b[kCriticLayers], q_T[2], q_b[2];
+};
+
+void simt_pack_host(const rollout_dims &d, const float *w, SimtHost *out)
 {
-    const HostLayout lo = host_layout(h->dims);
-    std::vector<float> ap(kActorPacked, 0.f);
+    const HostLayout lo = host_layout(d);
+    std::vector<float> &ap = out->ap, &sp = out->sp;
+    size_t *offs_T = out->offs_T, *offs_b = out->offs_b, *q_T = out->q_T, *q_b = out->q_b;
+    ap.assign(kActorPacked, 0.f);
+    sp.clear();
     transpose_into(ap, kA1, w + lo.a_w[0], kActorH1, kState, kActorH1);
     memcpy(&ap[kB1], w + lo.a_b[0], sizeof(float) * kActorH1);
     transpose_into(ap, kA2, w + lo.a_w[1], kActorH2, kActorH1, kActorH2);
@@ -166,8 +184,6 @@ int upload_simt(rollout_handle *h, const float *w)
     transpose_into(ap, kA3, w + lo.a_w[2], kActions, kActorH2, 48);
     memcpy(&ap[kB3], w + lo.a_b[2], sizeof(float) * kActions);
 
-    std::vector<float> sp;
-    size_t offs_T[kCriticLayers], offs_b[kCriticLayers];
     for (int l = 0; l < kCriticLayers; ++l) {
         offs_T[l] = sp.size();
         sp.resize(sp.size() + (size_t)lo.c_in[l] * lo.c_out[l]);
@@ -175,7 +191,6 @@ int upload_simt(rollout_handle *h, const float *w)
         offs_b[l] = sp.size();
         sp.insert(sp.end(), w + lo.c_b[l], w + lo.c_b[l] + lo.c_out[l]);
     }
-    size_t q_T[2], q_b[2];
     for (int l = 0; l < 2; ++l) {
         q_T[l] = sp.size();
         sp.resize(sp.size() + (size_t)lo.q_in[l] * lo.q_out[l]);
@@ -183,6 +198,15 @@ int upload_simt(rollout_handle *h, const float *w)
         q_b[l] = sp.size();
         sp.insert(sp.end(), w + lo.q_b[l], w + lo.q_b[l] + lo.q_out[l]);
     }
+}
+
+int upload_simt(rollout_handle *h, const float *w)
+{
+    const HostLayout lo = host_layout(h->dims);
+    SimtHost sh;
+    simt_pack_host(h->dims, w, &sh);
+    const std::vector<float> &ap = sh.ap, &sp = sh.sp;
+    const size_t *offs_T = sh.offs_T, *offs_b = sh.offs_b, *q_T = sh.q_T, *q_b = sh.q_b;
     cudaError_t e;
     if (!h->d_actor_packed) {
         if ((e = cudaMalloc(&h->d_actor_packed, sizeof(float) * ap.size())) != cudaSuccess)
@@ -238,12 +262,8 @@ int upload_div_table(rollout_handle *h)
     return ROLLOUT_OK;
 }
 
-int upload_weights(rollout_handle *h, const float *w)
+UmmaHostLayout umma_layout(const HostLayout &lo)
 {
-    const HostLayout lo = host_layout(h->dims);
-    for (size_t i = 0; i < lo.total; ++i)
-        if (!isfinite(w[i])) return fail(ROLLOUT_ERR_INVALID, "weight %zu is not finite", i);
-    if (h->dims.dtype == ROLLOUT_FP32) return upload_simt(h, w);
     UmmaHostLayout ul{};
     ul.n_critic = kCriticLayers;
     for (int l = 0; l < 3; ++l) { ul.a_w[l] = lo.a_w[l]; ul.a_b[l] = lo.a_b[l]; }
@@ -251,7 +271,16 @@ int upload_weights(rollout_handle *h, const float *w)
         ul.c_w[l] = lo.c_w[l]; ul.c_b[l] = lo.c_b[l]; ul.c_in[l] = lo.c_in[l]; ul.c_out[l] = lo.c_out[l];
     }
     for (int l = 0; l < 2; ++l) { ul.q_w[l] = lo.q_w[l]; ul.q_b[l] = lo.q_b[l]; }
-    int rc = umma_upload(&h->umma, &h->d_umma, h->dims.dtype == ROLLOUT_BF16, w, ul, g_err, sizeof(g_err));
+    return ul;
+}
+
+int upload_weights(rollout_handle *h, const float *w)
+{
+    const HostLayout lo = host_layout(h->dims);
+    for (size_t i = 0; i < lo.total; ++i)
+        if (!isfinite(w[i])) return fail(ROLLOUT_ERR_INVALID, "weight %zu is not finite", i);
+    if (h->dims.dtype == ROLLOUT_FP32) return upload_simt(h, w);
+    int rc = umma_upload(&h->umma, &h->d_umma, h->dims.dtype == ROLLOUT_BF16, w, umma_layout(lo), g_err, sizeof(g_err));
     if (rc) return rc;
     if (value_needs_scratch(h->umma) && !h->d_scratch) {
         int sms = 0;
@@ -263,6 +292,125 @@ int upload_weights(rollout_handle *h, const float *w)
             return cuda_fail(e, "cudaMalloc(value scratch)");
     }
     return ROLLOUT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Device-side weight refresh.  The host packers only copy weights into place
+// or round them once (bf16 or tf32), so each converted element is a function
+// of one weight.  Once per handle, three probe vectors go through the same
+// packer as the real weights: two whose values are exact in bf16, tf32 and
+// float32 give each element the index of its source (13 bits each, as
+// mantissa and exponent), and a third (1 + 2^-20, exact in neither reduced
+// format) tells the rounded elements from the copied ones.  The resulting map
+// is a gather that rounds as the host packer does.
+
+// 13 bits as (1 + m/128) 2^(e-32), m < 128, e < 64
+float probe_value(uint32_t bits)
+{
+    return ldexpf(1.f + (float)(bits & 0x7Fu) / 128.f, (int)((bits >> 7) & 0x3Fu) - 32);
+}
+
+long long probe_bits(float v)
+{
+    int e = 0;
+    const float f = frexpf(v, &e);                 // v = f 2^e, f in [0.5, 1)
+    return ((long long)(e + 31) << 7) | (long long)lrintf((2.f * f - 1.f) * 128.f);
+}
+
+float element(const uint8_t *base, long long s, int elem)
+{
+    uint32_t u = 0;
+    if (elem == 2) {
+        uint16_t b;
+        memcpy(&b, base + (size_t)s * 2, 2);
+        u = (uint32_t)b << 16;
+    } else {
+        memcpy(&u, base + (size_t)s * 4, 4);
+    }
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+// one region of converted weights in a host image, and where it lives on the device
+struct ProbeRegion {
+    const uint8_t *host;
+    long long n;
+    int elem;
+    uint8_t *dev;
+};
+
+int build_repack(rollout_handle *h)
+{
+    const HostLayout lo = host_layout(h->dims);
+    const size_t nw = lo.total;
+    if (nw + 1 >= ((size_t)1 << 26)) return fail(ROLLOUT_ERR_UNSUPPORTED, "too many weights for the refresh map");
+    constexpr float kRoundProbe = 1.f + 0x1p-20f;
+    std::vector<float> probe(nw);
+    std::vector<ProbeRegion> reg[3];
+    SimtHost sh[3];
+    UmmaHostImage im[3];
+    for (int k = 0; k < 3; ++k) {
+        for (size_t i = 0; i < nw; ++i) {
+            const uint32_t j = (uint32_t)i + 1;    // 0 marks padding
+            probe[i] = k == 0 ? probe_value(j & 0x1FFFu) : k == 1 ? probe_value(j >> 13) : kRoundProbe;
+        }
+        if (h->dims.dtype == ROLLOUT_FP32) {
+            simt_pack_host(h->dims, probe.data(), &sh[k]);
+            reg[k].push_back({(const uint8_t *)sh[k].ap.data(), (long long)sh[k].ap.size(), 4, (uint8_t *)h->d_actor_packed});
+            reg[k].push_back({(const uint8_t *)sh[k].sp.data(), (long long)sh[k].sp.size(), 4, (uint8_t *)h->d_simt});
+        } else {
+            UmmaWeights tables = h->umma;
+            umma_pack_host(&tables, h->dims.dtype == ROLLOUT_BF16, probe.data(), umma_layout(lo), &im[k]);
+            for (const UmmaRegion &r : im[k].region)
+                reg[k].push_back({im[k].bytes.data() + r.off, (long long)(r.bytes / r.elem), r.elem,
+                                  (uint8_t *)h->d_umma + r.off});
+        }
+    }
+    std::vector<int32_t> maps;
+    std::vector<size_t> starts;
+    for (size_t r = 0; r < reg[0].size(); ++r) {
+        const ProbeRegion &a = reg[0][r], &b = reg[1][r], &c = reg[2][r];
+        starts.push_back(maps.size());
+        for (long long s = 0; s < a.n; ++s) {
+            const float va = element(a.host, s, a.elem);
+            if (va == 0.f) {
+                maps.push_back(0);
+                continue;
+            }
+            const long long j = probe_bits(va) | (probe_bits(element(b.host, s, b.elem)) << 13);
+            if (j < 1 || j > (long long)nw)
+                return fail(ROLLOUT_ERR_CUDA, "weight refresh map: element %lld of region %zu decodes to %lld", s, r, j);
+            const bool rounded = element(c.host, s, c.elem) != kRoundProbe;
+            maps.push_back((int32_t)j | (rounded ? (int32_t)1 << 30 : 0));
+        }
+    }
+    cudaError_t e;
+    if ((e = cudaMalloc(&h->d_maps, maps.size() * 4)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(weight map)");
+    if ((e = cudaMemcpy(h->d_maps, maps.data(), maps.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(weight map)");
+    h->n_repack = (int)reg[0].size();
+    for (int r = 0; r < h->n_repack; ++r)
+        h->repack[r] = {reg[0][r].dev, h->d_maps + starts[r], reg[0][r].n, reg[0][r].elem};
+    return ROLLOUT_OK;
+}
+
+// one region of the refresh: element s takes weight map[s]-1 (0: padding, a
+// zero), rounded where bit 30 says so, as the host packer rounds
+__global__ void repack_kernel(const float *__restrict__ w, const int32_t *__restrict__ map, long long n, int elem,
+                              int tf32, uint8_t *__restrict__ dst)
+{
+    for (long long s = blockIdx.x * (long long)blockDim.x + threadIdx.x; s < n; s += (long long)gridDim.x * blockDim.x) {
+        const int32_t code = map[s];
+        const uint32_t u = code ? __float_as_uint(w[(code & 0x3FFFFFFF) - 1]) : 0u;
+        const uint32_t bf = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;     // bf16, nearest even
+        if (elem == 2) {
+            reinterpret_cast<uint16_t *>(dst)[s] = (uint16_t)bf;
+        } else {
+            const uint32_t rnd = tf32 ? ((u + 0x1000u) & 0xFFFFE000u) : (bf << 16);   // tf32: nearest, ties away
+            reinterpret_cast<uint32_t *>(dst)[s] = (code & (1 << 30)) ? rnd : u;
+        }
+    }
 }
 
 // the padded copy of the feature matrix and the 2-D tensor map the bf16
@@ -312,6 +460,7 @@ void free_handle(rollout_handle *h)
         if (e) cudaEventDestroy(e);
     for (cudaEvent_t e : h->copy_done)
         if (e) cudaEventDestroy(e);
+    cudaFree(h->d_maps);
     delete h;
 }
 
@@ -352,7 +501,7 @@ int rollout_create(const float *weights, const rollout_dims *dims, rollout_handl
     if (e != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaGetDevice"); }
     if ((e = cudaMalloc(&h->d_status, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMalloc(status)"); }
     if ((e = cudaMemset(h->d_status, 0, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMemset"); }
-    if ((rc = upload_div_table(h)) || (rc = upload_weights(h, weights)) ||
+    if ((rc = upload_div_table(h)) || (rc = upload_weights(h, weights)) || (rc = build_repack(h)) ||
         (dims->dtype == ROLLOUT_BF16 && (rc = make_feature_map(h)))) {
         free_handle(h);
         return rc;
@@ -366,6 +515,24 @@ int rollout_set_weights(rollout_handle *h, const float *weights)
     g_err[0] = 0;
     if (!h || !weights) return fail(ROLLOUT_ERR_INVALID, "null argument");
     return upload_weights(h, weights);
+}
+
+int rollout_set_weights_device(rollout_handle *h, const float *weights, void *stream)
+{
+    g_err[0] = 0;
+    if (!h || !weights) return fail(ROLLOUT_ERR_INVALID, "null argument");
+    if (((uintptr_t)weights & 3u) != 0) return fail(ROLLOUT_ERR_INVALID, "weights must be 4-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    for (int r = 0; r < h->n_repack; ++r) {
+        const auto &g = h->repack[r];
+        const long long blocks = (g.n + 255) / 256;
+        repack_kernel<<<(int)(blocks < 1216 ? blocks : 1216), 256, 0, st>>>(weights, g.map, g.n, g.elem,
+                                                                           h->dims.dtype == ROLLOUT_TF32, g.dev);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "weight refresh launch");
+    h->last_stream = st;
+    return ROLLOUT_OK;
 }
 
 }  // extern "C"

@@ -648,6 +648,14 @@ int ppo_get_weights(ppo_trainer *t, float *weights, void *stream)
     return e == cudaSuccess ? ROLLOUT_OK : cuda_err(e, "cudaMemcpyAsync(weights)");
 }
 
+int ppo_device_weights(ppo_trainer *t, const float **weights)
+{
+    clear_error();
+    if (!t || !weights) return set_error(ROLLOUT_ERR_INVALID, "null argument");
+    *weights = t->d_w;
+    return ROLLOUT_OK;
+}
+
 int ppo_reset_optimizer(ppo_trainer *t, void *stream)
 {
     clear_error();

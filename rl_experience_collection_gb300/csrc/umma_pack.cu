@@ -71,8 +71,7 @@ void set_layer(UmmaLayer &L, int n_out, int k_in, int kc, std::initializer_list<
 
 }  // namespace
 
-int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const UmmaHostLayout &lo, char *err,
-                size_t err_len)
+void umma_pack_host(UmmaWeights *w, bool bf16, const float *hw, const UmmaHostLayout &lo, UmmaHostImage *out)
 {
     const Packer P(bf16);
     const int kc = P.kc;
@@ -199,36 +198,52 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const 
         for (int j = 0; j < kCurH; ++j)
             vec.push_back(rounded(hw[lo.q_w[0] + (size_t)j * (kState + kActions) + kState + a], bf16));
 
-    // ---------------- one device allocation: image | actor bias | stream | vec
+    // ---------------- one allocation: image | actor bias | stream | vec
     auto align = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
-    const size_t o_img = 0, o_ab = align(img.size()), o_st = align(o_ab + abias.size() * 4),
-                 o_vec = align(o_st + stream.size()), total = align(o_vec + vec.size() * 4);
-    std::vector<uint8_t> host(total, 0);
-    memcpy(&host[o_img], img.data(), img.size());
-    memcpy(&host[o_ab], abias.data(), abias.size() * 4);
-    memcpy(&host[o_st], stream.data(), stream.size());
-    memcpy(&host[o_vec], vec.data(), vec.size() * 4);
+    UmmaHostImage &im = *out;
+    im.region[0] = {0, img.size(), bf16 ? 2 : 4};                                   // actor image
+    im.region[1] = {align(img.size()), abias.size() * 4, 4};                         // actor bias (f32)
+    im.region[2] = {align(im.region[1].off + im.region[1].bytes), stream.size(), bf16 ? 2 : 4};   // unit stream
+    im.region[3] = {align(im.region[2].off + im.region[2].bytes), vec.size() * 4, 4};            // vec (f32)
+    im.bytes.assign(align(im.region[3].off + im.region[3].bytes), 0);
+    memcpy(&im.bytes[im.region[0].off], img.data(), img.size());
+    memcpy(&im.bytes[im.region[1].off], abias.data(), abias.size() * 4);
+    memcpy(&im.bytes[im.region[2].off], stream.data(), stream.size());
+    memcpy(&im.bytes[im.region[3].off], vec.data(), vec.size() * 4);
+    w->bf16 = bf16;
+    w->wide = wide;
+    w->stream_bytes = (long long)stream.size();
+}
+
+int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const UmmaHostLayout &lo, char *err,
+                size_t err_len)
+{
+    UmmaHostImage im;
+    umma_pack_host(w, bf16, hw, lo, &im);
+    const size_t total = im.bytes.size();
     cudaError_t e;
-    if (*d_buf) {
+    // later uploads of the same shapes reuse the allocation, so device pointers
+    // into it (the weight-refresh maps) stay valid
+    if (*d_buf && w->buf_bytes != total) {
         cudaFree(*d_buf);
         *d_buf = nullptr;
     }
-    if ((e = cudaMalloc(d_buf, total)) != cudaSuccess) {
-        snprintf(err, err_len, "cudaMalloc(tensor-core weights): %s", cudaGetErrorString(e));
-        return e == cudaErrorMemoryAllocation ? ROLLOUT_ERR_NOMEM : ROLLOUT_ERR_CUDA;
+    if (!*d_buf) {
+        if ((e = cudaMalloc(d_buf, total)) != cudaSuccess) {
+            snprintf(err, err_len, "cudaMalloc(tensor-core weights): %s", cudaGetErrorString(e));
+            return e == cudaErrorMemoryAllocation ? ROLLOUT_ERR_NOMEM : ROLLOUT_ERR_CUDA;
+        }
+        w->buf_bytes = total;
     }
-    if ((e = cudaMemcpy(*d_buf, host.data(), total, cudaMemcpyHostToDevice)) != cudaSuccess) {
+    if ((e = cudaMemcpy(*d_buf, im.bytes.data(), total, cudaMemcpyHostToDevice)) != cudaSuccess) {
         snprintf(err, err_len, "cudaMemcpy(tensor-core weights): %s", cudaGetErrorString(e));
         return ROLLOUT_ERR_CUDA;
     }
     uint8_t *base = (uint8_t *)*d_buf;
-    w->bf16 = bf16;
-    w->wide = wide;
-    w->actor_img = base + o_img;
-    w->actor_bias = (const float *)(base + o_ab);
-    w->stream = base + o_st;
-    w->stream_bytes = (long long)stream.size();
-    w->vec = (const float *)(base + o_vec);
+    w->actor_img = base + im.region[0].off;
+    w->actor_bias = (const float *)(base + im.region[1].off);
+    w->stream = base + im.region[2].off;
+    w->vec = (const float *)(base + im.region[3].off);
     return ROLLOUT_OK;
 }
 

@@ -4,6 +4,8 @@
 
 #include <stddef.h>
 
+#include <vector>
+
 #include "internal.cuh"
 
 namespace rl {
@@ -39,6 +41,7 @@ struct UmmaWeights {
     long long unit_off[32] = {};
     uint32_t unit_bytes[32] = {};
     const float *vec = nullptr;  // biases, head weights, curiosity one-hot columns (f32)
+    size_t buf_bytes = 0;        // size of the device allocation (reused by later uploads)
     int head_w_off = 0;          // critic head weights [h5] (rounded to the operand format)
     int head_b_off = 0;          // critic head bias [1]
     int onehot_off = 0;          // curiosity layer-1 one-hot columns [45][64] (rounded)
@@ -52,6 +55,19 @@ struct UmmaHostLayout {
     size_t q_w[2], q_b[2];
     int n_critic;
 };
+
+// the packed bytes of one upload and where its regions lie (element size 2 for
+// bf16 tiles, 4 for tf32 tiles and float32 vectors)
+struct UmmaRegion {
+    size_t off, bytes;
+    int elem;
+};
+struct UmmaHostImage {
+    std::vector<uint8_t> bytes;
+    UmmaRegion region[4];   // actor image, actor bias, unit stream, vec
+};
+// packs on the host (fills w's tables, not its device pointers)
+void umma_pack_host(UmmaWeights *w, bool bf16, const float *host_w, const UmmaHostLayout &lo, UmmaHostImage *out);
 
 // converts/uploads; *d_buf receives (or reuses) the device allocation
 int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *host_w, const UmmaHostLayout &lo,
