@@ -17,7 +17,8 @@
  *
  * Definitions (size = number of stored transitions, p the priorities of slots
  * 0 .. size-1, total = sum p, c_i = p_0 + ... + p_i):
- *   sample k draws u_k in [0, 1) (below), t_k = u_k total, and picks the slot
+ *   sample k draws u_k in [0, 1) (below), t_k = u_k total (moved just below
+ *     total if the product rounds up to it), and picks the slot
  *     i_k = min { i : c_i > t_k }  (a slot of zero priority is never picked);
  *   its weight is w_k = (size p_{i_k} / total)^(-beta) / max_j w_j (max over
  *     the batch);
@@ -26,8 +27,8 @@
  *     OOPSLA 2014): x = mix(seed + (offset + k + 1) 0x9E3779B97F4A7C15);
  *   an update sets p_i = fl32(|td|^alpha + eps) (computed in double, rounded
  *     once to float32) for each slot i it names; where a batch names a slot
- *     more than once the last entry wins; a NaN priority becomes eps and an
- *     infinite one the maximum priority held before the call;
+ *     more than once the last entry wins; a NaN td gives eps and a priority
+ *     past float32 (+inf) the maximum priority held before the call;
  *   the maximum priority starts at 1 and is the running maximum of every
  *     priority an update has written (it never decreases); inserted
  *     transitions take it.

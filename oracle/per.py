@@ -1,8 +1,8 @@
 """Oracle of the GPU-resident prioritised experience replay buffer (include/per.h).
 
 TEST INFRASTRUCTURE ONLY: the tests import this module; the product path never
-does.  Plain and sequential: numpy arrays, double-precision running sums in
-slot order, one Python loop per update batch.
+does.  Plain numpy: double-precision running sums in slot order, one search per
+sample, and updates applied as the batch-order writes they define.
 
 Follows page "GPU-Resident Prioritized Experience Replay":
 - "New struct: GpuReplayBuffer": the ring's arrays (states, next states,
@@ -20,8 +20,9 @@ Follows page "GPU-Resident Prioritized Experience Replay":
 Readings where the page leaves a step open (each stated in the design notes):
 the largest weight is taken over the sampled batch; the maximum priority
 starts at 1 and is the running maximum of every priority written; within one
-update the later entry for a slot wins; NaN becomes epsilon and +inf the
-maximum priority held before the update; the uniforms come from SplitMix64
+update the later entry for a slot wins; a NaN TD error gives epsilon and a
+priority past float32 (+inf) the maximum priority held before the update; a
+target u total that rounds up to the total is moved just below it; the uniforms come from SplitMix64
 (Steele, Lea & Flood, OOPSLA 2014), the (offset + k)-th output for sample k.
 """
 from __future__ import annotations
@@ -51,7 +52,8 @@ def uniform(seed: int, n: int) -> float:
 
 
 class Replay:
-    """The buffer, slot by slot."""
+    """The buffer.  state_dim 0 keeps no state rows (for checks of the
+    priorities and the sampling alone at large capacities)."""
 
     def __init__(self, capacity: int, state_dim: int):
         self.capacity = int(capacity)
@@ -72,14 +74,16 @@ class Replay:
         """Transition j to slot (cursor + j) mod capacity, in order; each takes the
         current maximum priority."""
         count = len(actions)
-        for j in range(count):
-            s = (self.cursor + j) % self.capacity
+        # inserted one at a time, only the last `capacity` items survive
+        j = np.arange(max(0, count - self.capacity), count)
+        s = (self.cursor + j) % self.capacity
+        if self.dim:
             self.states[s] = states[j]
             self.next_states[s] = next_states[j]
-            self.actions[s] = actions[j]
-            self.rewards[s] = rewards[j]
-            self.dones[s] = dones[j]
-            self.prio[s] = self.max_prio
+        self.actions[s] = actions[j]
+        self.rewards[s] = rewards[j]
+        self.dones[s] = dones[j]
+        self.prio[s] = self.max_prio
         self.cursor = (self.cursor + count) % self.capacity
         self.size = min(self.capacity, self.size + count)
 
@@ -107,6 +111,8 @@ class Replay:
         n_replayed = 0
         for k in range(batch):
             t = uniform(seed, offset + k) * total
+            if t >= total:                                     # the product can round up to the total
+                t = float(np.nextafter(total, 0.0))
             i = int(np.searchsorted(c, t, side="right"))     # first i with c_i > t
             lo = float(c[i - 1]) if i > 0 else 0.0
             margin[k] = min(t - lo, float(c[i]) - t) / total
@@ -120,6 +126,7 @@ class Replay:
                 i = j
             idx[k] = i
         p = self.prio[idx].astype(np.float64)
+        beta = float(np.float32(beta))                         # the ABI takes beta as float32
         w = np.array([(self.size * pk / total) ** (-beta) for pk in p])
         w = (w / w.max()).astype(np.float32)
         return idx, w, margin, n_replayed
@@ -134,17 +141,20 @@ class Replay:
         maximum priority is the running maximum of the values written."""
         snapshot = self.max_prio
         eps32 = float(np.float32(eps))
-        for k in range(len(indices)):
-            i = int(indices[k])
-            if not 0 <= i < self.size:
-                self.range_error = True
-                continue
-            d = abs(float(td[k]))
-            with np.errstate(over="ignore"):                   # past float32: +inf, clamped below
-                v = np.float32(d ** float(np.float32(alpha)) + eps32) if not math.isnan(d) else np.float32(math.nan)
-            if math.isnan(v):
-                v = np.float32(eps32)
-            elif math.isinf(v):
-                v = snapshot
-            self.prio[i] = v
-            self.max_prio = max(self.max_prio, v)
+        indices = np.asarray(indices, dtype=np.int64)
+        ok = (indices >= 0) & (indices < self.size)
+        if not ok.all():
+            self.range_error = True
+        idx = indices[ok]
+        d = np.abs(np.asarray(td, dtype=np.float32)[ok].astype(np.float64))
+        with np.errstate(over="ignore", invalid="ignore"):     # past float32: +inf, clamped below
+            v = (d ** float(np.float32(alpha)) + eps32).astype(np.float32)
+        v[np.isnan(d)] = np.float32(eps32)
+        v[np.isinf(v)] = snapshot
+        # in batch order the last write to a slot stays: keep each slot's last entry
+        rev = idx[::-1]
+        _, first_in_rev = np.unique(rev, return_index=True)
+        last = len(idx) - 1 - first_in_rev
+        self.prio[idx[last]] = v[last]
+        if len(v):
+            self.max_prio = max(self.max_prio, v.max())

@@ -56,6 +56,10 @@ class PpoHparams(C.Structure):
         return cls(clip_eps, value_coef, lr, beta1, beta2, adam_eps, max_grad_norm, weight_decay)
 
 
+PER_EXPORTS = ["per_create", "per_insert", "per_sample", "per_update_priorities", "per_size", "per_read",
+               "per_status", "per_destroy"]
+
+
 class RolloutError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"rollout error {code}: {msg}")
@@ -99,6 +103,22 @@ def lib(path: Optional[str] = None):
     L.rollout_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
     L.rollout_last_error.restype = C.c_char_p
     L.rollout_last_error.argtypes = []
+    L.per_create.restype = C.c_int
+    L.per_create.argtypes = [C.c_longlong, C.c_int, C.POINTER(vp)]
+    L.per_insert.restype = C.c_int
+    L.per_insert.argtypes = [vp, vp, vp, vp, vp, vp, C.c_longlong, vp]
+    L.per_sample.restype = C.c_int
+    L.per_sample.argtypes = [vp, C.c_int, C.c_float, C.c_uint64, C.c_uint64, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.per_update_priorities.restype = C.c_int
+    L.per_update_priorities.argtypes = [vp, vp, vp, C.c_int, C.c_float, C.c_float, vp]
+    L.per_size.restype = C.c_int
+    L.per_size.argtypes = [vp, C.POINTER(C.c_longlong), C.POINTER(C.c_longlong)]
+    L.per_read.restype = C.c_int
+    L.per_read.argtypes = [vp, vp, vp, vp]
+    L.per_status.restype = C.c_int
+    L.per_status.argtypes = [vp]
+    L.per_destroy.restype = None
+    L.per_destroy.argtypes = [vp]
     L.ppo_device_weights.restype = C.c_int
     L.ppo_device_weights.argtypes = [vp, C.POINTER(vp)]
     L.ppo_create.restype = C.c_int
@@ -374,3 +394,77 @@ def collect(w: wl.Workload, inputs: "wl.Inputs", N: Optional[int] = None, L: Opt
     if handle is None:
         h.close()
     return out
+
+
+class PerBuffer:
+    """Owns a ``per_buffer`` (include/per.h): the GPU-resident prioritised replay ring."""
+
+    def __init__(self, capacity: int, state_dim: int):
+        h = C.c_void_p()
+        _check(lib().per_create(int(capacity), int(state_dim), C.byref(h)))
+        self._h = h
+        self.capacity = int(capacity)
+        self.dim = int(state_dim)
+
+    @staticmethod
+    def _p(t):
+        return C.c_void_p(None) if t is None else C.c_void_p(t.data_ptr())
+
+    def insert(self, states, next_states, actions, rewards, dones, stream=None) -> None:
+        """Appends device tensors (states/next_states [n, dim] f32, actions i32,
+        rewards f32, dones u8)."""
+        p = self._p
+        _check(lib().per_insert(self._h, p(states), p(next_states), p(actions), p(rewards), p(dones),
+                                int(actions.numel()), C.c_void_p(_stream_handle(stream))))
+
+    def sample(self, batch: int, beta: float, seed: int, offset: int, out: Dict[str, "torch.Tensor"],
+               stream=None) -> None:
+        """Draws `batch` transitions into the device tensors of `out` (keys indices,
+        weights, states, next_states, actions, rewards, dones; the last five optional)."""
+        p = self._p
+        _check(lib().per_sample(self._h, int(batch), float(beta), C.c_uint64(seed), C.c_uint64(offset),
+                                p(out["indices"]), p(out["weights"]), p(out.get("states")),
+                                p(out.get("next_states")), p(out.get("actions")), p(out.get("rewards")),
+                                p(out.get("dones")), C.c_void_p(_stream_handle(stream))))
+
+    def make_batch(self, batch: int, device="cuda") -> Dict[str, "torch.Tensor"]:
+        import torch
+        return {"indices": torch.empty(batch, dtype=torch.int32, device=device),
+                "weights": torch.empty(batch, dtype=torch.float32, device=device),
+                "states": torch.empty((batch, self.dim), dtype=torch.float32, device=device),
+                "next_states": torch.empty((batch, self.dim), dtype=torch.float32, device=device),
+                "actions": torch.empty(batch, dtype=torch.int32, device=device),
+                "rewards": torch.empty(batch, dtype=torch.float32, device=device),
+                "dones": torch.empty(batch, dtype=torch.uint8, device=device)}
+
+    def update(self, indices, td_errors, alpha: float = 0.6, eps: float = 1e-6, stream=None) -> None:
+        _check(lib().per_update_priorities(self._h, self._p(indices), self._p(td_errors), int(indices.numel()),
+                                           float(alpha), float(eps), C.c_void_p(_stream_handle(stream))))
+
+    def size(self):
+        n, c = C.c_longlong(), C.c_longlong()
+        _check(lib().per_size(self._h, C.byref(n), C.byref(c)))
+        return n.value, c.value
+
+    def priorities(self, stream=None):
+        """(priorities [capacity] f32, maximum priority) as host values (synchronises)."""
+        import numpy as np
+        pr = np.empty(self.capacity, dtype=np.float32)
+        m = np.empty(1, dtype=np.float32)
+        _check(lib().per_read(self._h, pr.ctypes.data_as(C.c_void_p), m.ctypes.data_as(C.c_void_p),
+                              C.c_void_p(_stream_handle(stream))))
+        return pr, m[0]
+
+    def status(self) -> int:
+        return lib().per_status(self._h)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().per_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -169,3 +169,53 @@ def weight_views(weights: np.ndarray, critic_h: Tuple[int, ...] = CRITIC_STD) ->
         off += o
     assert off == weights.size, (off, weights.size)
     return out
+
+
+@dataclasses.dataclass(frozen=True)
+class ReplayWorkload:
+    """A prioritised replay buffer and its training-step traffic."""
+    name: str
+    capacity: int
+    state_dim: int
+    batch: int                 # transitions sampled (and priorities updated) per training step
+    alpha: float = 0.6
+    beta: float = 0.4
+    eps: float = 1e-6
+    seed: int = 7
+
+
+REPLAY_WORKLOADS: Dict[str, ReplayWorkload] = {
+    # the page's sizing example: 100K transitions
+    "replay_100k": ReplayWorkload("replay_100k", 100_000, STATE_DIM, 512),
+    # one whole reset-heavy collection (16384 episodes x 1000 steps) held for replay
+    "replay_16m": ReplayWorkload("replay_16m", 16_384_000, STATE_DIM, 512),
+}
+
+
+def replay_rows(j: np.ndarray, dim: int):
+    """Transition j of the synthetic replay stream, exact in float32 so that a row
+    can be recomputed from its index: state[c] = (j mod 65521) + c/64,
+    next[c] = (j mod 65519) - c/64, action j mod 45, reward (j mod 1021)/1024,
+    done when j mod 7 == 0."""
+    j = np.asarray(j, dtype=np.int64)
+    c = np.arange(dim, dtype=np.float64) / 64.0
+    states = ((j % 65521)[:, None] + c[None, :]).astype(np.float32)
+    nxt = ((j % 65519)[:, None] - c[None, :]).astype(np.float32)
+    return (states, nxt, (j % 45).astype(np.int32), ((j % 1021) / 1024.0).astype(np.float32),
+            (j % 7 == 0).astype(np.uint8))
+
+
+def replay_td(seed: int, step: int, n: int) -> np.ndarray:
+    """Seeded TD errors of one training step: N(0, 1) float32."""
+    return np.random.default_rng([seed, step]).standard_normal(n).astype(np.float32)
+
+
+def replay_rows_device(j0: int, n: int, dim: int, device="cuda"):
+    """replay_rows for j = j0 .. j0+n-1, made on the device (same values)."""
+    import torch
+    j = torch.arange(j0, j0 + n, dtype=torch.int64, device=device)
+    c = torch.arange(dim, dtype=torch.float64, device=device) / 64.0
+    states = ((j % 65521).to(torch.float64)[:, None] + c[None, :]).to(torch.float32)
+    nxt = ((j % 65519).to(torch.float64)[:, None] - c[None, :]).to(torch.float32)
+    return (states, nxt, (j % 45).to(torch.int32), ((j % 1021).to(torch.float64) / 1024.0).to(torch.float32),
+            (j % 7 == 0).to(torch.uint8))

@@ -80,3 +80,19 @@ def test_last_error_callable_without_gpu(libpath):
     from rl_experience_collection_gb300 import binding
     binding.lib()
     assert isinstance(binding.last_error(), str)
+
+
+def _declared_per():
+    src = open(os.path.join(ROOT, "include", "per.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(per_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_replay_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    names = _declared_per()
+    assert {"per_create", "per_insert", "per_sample", "per_update_priorities", "per_destroy"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+    from rl_experience_collection_gb300 import binding
+    assert set(binding.PER_EXPORTS) == set(names)

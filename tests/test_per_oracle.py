@@ -151,3 +151,37 @@ def test_zero_total_is_refused_and_replay_is_checked():
     idx2, _, _, n = r.sample(8, 0.4, 5, 0, replay=bad)                 # outside the band: ignored
     np.testing.assert_array_equal(idx2, idx)
     assert n == 0
+
+
+def test_update_equals_the_batch_order_loop():
+    """Brute force: the update applied entry by entry, in batch order."""
+    rng = np.random.default_rng(9)
+    for trial in range(40):
+        n = int(rng.integers(1, 30))
+        r = _filled(np.ones(n, dtype=np.float32))
+        B = int(rng.integers(1, 60))
+        idx = rng.integers(-2, n + 2, B)
+        td = rng.standard_normal(B).astype(np.float32) * 3
+        td[rng.random(B) < 0.1] = np.nan
+        td[rng.random(B) < 0.1] = np.inf
+        alpha, eps = float(rng.choice([0.0, 0.6, 1.0, 2.0])), float(rng.choice([0.0, 1e-6, 0.01]))
+        want = r.prio.copy()
+        m = r.max_prio
+        snap = m
+        for k in range(B):
+            i = int(idx[k])
+            if not 0 <= i < n:
+                continue
+            if math.isnan(float(td[k])):
+                v = np.float32(eps)
+            else:
+                with np.errstate(over="ignore"):
+                    v = np.float32(abs(float(td[k])) ** float(np.float32(alpha)) + float(np.float32(eps)))
+                if math.isinf(v):
+                    v = snap
+            want[i] = v
+            m = max(m, v)
+        r.update(idx, td, alpha, eps)
+        np.testing.assert_array_equal(r.prio, want)
+        assert r.max_prio == m
+        assert r.range_error == bool(((idx < 0) | (idx >= n)).any())
