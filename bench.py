@@ -16,6 +16,7 @@ from __future__ import annotations
 import argparse
 import dataclasses
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -52,8 +53,8 @@ def path_flops(w: wl.Workload, N: int, L: int):
 # A figure only holds for the source it was measured on: the sha256 below covers
 # the kernel and the files it is built from; any change makes the traffic null.
 VALUE_DRAM_CAPTURE = {"workload": "reset_heavy_bf16", "episodes": 16384, "horizon": 1000,
-                      "bytes": 542.61e6,
-                      "sources_sha256": "ed4c9f19773bf04188cb9445818873e8447f6ab8268ad8292a6a2ecf5001acd2"}
+                      "bytes": 546.98e6,
+                      "sources_sha256": "a819f0377067efaa4b6bc40424c9c647da571792f787a6099c0895b5a8842952"}
 VALUE_KERNEL_SOURCES = ["value_umma.cu", "umma.cuh", "umma_path.cuh", "env.cuh", "internal.cuh", "umma_pack.cu"]
 
 
@@ -119,6 +120,82 @@ def measure_ppo(w, weights, out, N, L, n_steps, warmup, dev):
     tr.close()
     flop = ppo_flop_per_row(w.critic_h) * PPO_BATCH
     return ms, flop
+
+
+REPLAY_BATCH = 512
+
+
+def measure_replay(out, N, L, dev, flush, iters):
+    """The prioritised replay buffer holding this collection (capacity N x L):
+    one insert of every tuple (next state = the episode's following row; the
+    last row repeats), priorities set from the advantages, then `iters` training
+    steps of one 512-sample draw and one 512-entry priority update, each call
+    timed with CUDA events after an L2 flush."""
+    import torch
+    from rl_experience_collection_gb300 import binding
+    T, D = N * L, wl.STATE_DIM
+    stream = torch.cuda.current_stream(dev)
+    states = out["states"].reshape(N, L, D)
+    nxt = torch.cat([states[:, 1:], states[:, -1:]], dim=1).reshape(T, D)
+    states = states.reshape(T, D)
+    actions, rewards = out["actions"].reshape(-1), out["rewards"].reshape(-1)
+    dones = out["dones"].reshape(-1).to(torch.uint8)
+    buf = binding.PerBuffer(T, D)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ins = []
+    for i in range(3):
+        flush.fill_(float(i))
+        e0.record(stream)
+        buf.insert(states, nxt, actions, rewards, dones, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ins.append(e0.elapsed_time(e1))
+    del nxt
+    adv = out["adv"].reshape(-1)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(T).astype(np.int32)).to(dev)
+    for k in range(0, T, 65536):
+        sl = perm[k:k + 65536]
+        buf.update(sl, adv[sl.long()], stream=stream)
+    batch = buf.make_batch(REPLAY_BATCH, dev)
+    td = torch.randn((iters + 3, REPLAY_BATCH), generator=torch.Generator(device=dev).manual_seed(9), device=dev)
+    samp, upd = [], []
+    for i in range(iters + 3):
+        flush.fill_(float(i))
+        e0.record(stream)
+        buf.sample(REPLAY_BATCH, 0.4, 17, i * REPLAY_BATCH, batch, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_s = e0.elapsed_time(e1)
+        flush.fill_(float(i))
+        e0.record(stream)
+        buf.update(batch["indices"], td[i], stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            samp.append(t_s)
+            upd.append(e0.elapsed_time(e1))
+    if buf.status() != binding.ROLLOUT_OK:
+        raise SystemExit("replay status")
+    buf.close()
+    return statistics.median(ins), statistics.median(samp), statistics.median(upd)
+
+
+def replay_insert_bytes(T, D):
+    """Algorithmic bytes of inserting T transitions: rows, action, reward, done
+    read and written, the priority written, the new priorities read once by the
+    sub-block sums."""
+    row = 2 * D * 4 + 4 + 4 + 1
+    return 2 * T * row + T * 4 + T * 4
+
+
+def replay_sample_bytes(B, D, n_blocks):
+    """Algorithmic bytes of one sampling call: per sample the 32-way search over
+    the block prefix (32 doubles a round), 16 sub-sums, 128 priorities, the
+    gathered transition read and written, the slot and weight written (and the
+    weight read and rewritten by the normalisation)."""
+    rounds = max(1, math.ceil(math.log(max(n_blocks, 2), 32)))
+    row = 2 * D * 4 + 4 + 4 + 1
+    return B * (rounds * 32 * 8 + 16 * 8 + 128 * 4 + 2 * row + 4 + 8 + 8 + 4)
 
 
 def launches_per_run(dtype):
@@ -264,6 +341,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-ppo", action="store_true", help="skip the PPO-update measurement")
     ap.add_argument("--ppo-steps", type=int, default=200, help="timed PPO optimizer steps (mini-batches of 512)")
+    ap.add_argument("--no-replay", action="store_true", help="skip the prioritised-replay measurement")
+    ap.add_argument("--replay-steps", type=int, default=200, help="timed replay sample + update calls")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = wl.WORKLOADS[args.workload]
@@ -366,6 +445,24 @@ def main():
                               "achieved_tflops": achieved, "peak_tflops": peak,
                               "peak_kind": "fp32 FMA, derived: SMs x 128 lanes x 2 x max SM clock",
                               "frac": achieved / peak, "bound": "alu"}
+
+    # ---------------- the prioritised replay buffer holding this collection (rank 0)
+    if not args.no_replay and rank == 0:
+        ins_ms, s_ms, u_ms = measure_replay(out, N, L, dev, flush, args.replay_steps)
+        T, D = N * L, wl.STATE_DIM
+        ib = replay_insert_bytes(T, D)
+        sb = replay_sample_bytes(REPLAY_BATCH, D, (T + 2047) // 2048)
+        line["replay"] = {
+            "workload": f"capacity {T} (this collection), state_dim {D}, batch {REPLAY_BATCH}, alpha 0.6, beta 0.4",
+            "insert_ms": ins_ms, "sample_us": 1000 * s_ms, "update_us": 1000 * u_ms,
+            "samples_per_s": REPLAY_BATCH / (s_ms / 1000.0),
+            "insert_roofline": {"bound": "hbm", "achieved": ib / (ins_ms / 1000.0) / 1e9, "peak": pk["hbm"],
+                                "unit": "GB/s", "frac": ib / (ins_ms / 1000.0) / 1e9 / pk["hbm"],
+                                "algorithmic_bytes": ib},
+            "sample_roofline": {"bound": "latency", "achieved": sb / (s_ms / 1000.0) / 1e9, "peak": pk["hbm"],
+                                "unit": "GB/s", "frac": sb / (s_ms / 1000.0) / 1e9 / pk["hbm"],
+                                "algorithmic_bytes": sb},
+            "gpu_launches_per_step": 7, "l2": "flushed before every timed call"}
 
     # ---------------- end to end through the C ABI with host buffers (rollout_run_host:
     # inputs copied in, every output copied back as soon as its kernel is done)
