@@ -21,7 +21,9 @@
  *     total if the product rounds up to it), and picks the slot
  *     i_k = min { i : c_i > t_k }  (a slot of zero priority is never picked);
  *   its weight is w_k = (size p_{i_k} / total)^(-beta) / max_j w_j (max over
- *     the batch);
+ *     the batch), formed in float32 (x = size p / total, 2^(-beta log2 x), the
+ *     division by the maximum): within about (5 + 1.5 beta |log2 x|) 2^-24
+ *     relative of the exact value;
  *   u_k = (x >> 11) 2^-53 with x the (offset + k)-th output (counting from 0)
  *     of the SplitMix64 generator seeded with `seed` (Steele, Lea & Flood,
  *     OOPSLA 2014): x = mix(seed + (offset + k + 1) 0x9E3779B97F4A7C15);
