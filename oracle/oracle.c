@@ -245,18 +245,26 @@ double oracle_critic(const float *w, const oracle_cfg *c, const double *x)
 }
 
 /* [P1] Phase A step 9 / [P2] "Curiosity Forward Model": forward-dynamics
- * prediction from [state ; one-hot(action)] -> cur_h ReLU -> next state. */
+ * prediction from [state ; one-hot(action)] -> cur_h ReLU -> next state.
+ * cw points at the curiosity block [C1 (cur_h x (sd + n_actions)), c1,
+ * C2 (sd x cur_h), c2]. */
+static void curiosity_block(const float *cw, const oracle_cfg *c, const double *x, int a, double *pred)
+{
+    double in[ORACLE_MAX_W], hid[ORACLE_MAX_W];
+    const int sd = c->n_market + 3, nin = sd + c->n_actions, h = c->cur_h;
+    const float *C1 = cw, *c1 = C1 + (long)h * nin, *C2 = c1 + h, *c2 = C2 + (long)sd * h;
+    q_vector(x, in, sd, c->quant);
+    for (int i = 0; i < c->n_actions; ++i) in[sd + i] = (i == a) ? 1.0 : 0.0;
+    oracle_dense(C1, c1, h, nin, in, hid, 1, c->quant);
+    q_vector(hid, in, h, c->quant);
+    oracle_dense(C2, c2, sd, h, in, pred, 0, c->quant);
+}
+
 void oracle_curiosity(const float *w, const oracle_cfg *c, const double *x, int a, double *pred)
 {
     layout lo;
-    double in[ORACLE_MAX_W], hid[ORACLE_MAX_W];
     make_layout(c, &lo);
-    int sd = c->n_market + 3;
-    q_vector(x, in, sd, c->quant);
-    for (int i = 0; i < c->n_actions; ++i) in[sd + i] = (i == a) ? 1.0 : 0.0;
-    oracle_dense(w + lo.q_w[0], w + lo.q_b[0], lo.q_out[0], lo.q_in[0], in, hid, 1, c->quant);
-    q_vector(hid, in, lo.q_out[0], c->quant);
-    oracle_dense(w + lo.q_w[1], w + lo.q_b[1], lo.q_out[1], lo.q_in[1], in, pred, 0, c->quant);
+    curiosity_block(w + lo.q_w[0], c, x, a, pred);
 }
 
 /* [P1] Phase A step 4: stable softmax, CDF summed in index order, inverse-CDF
@@ -346,6 +354,86 @@ void oracle_gae_f32(const float *r, const float *v, const int32_t *d, int L, dou
 }
 
 /* ------------------------------------------------------------------ */
+/* one environment step ([P1] steps 6-10)                               */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    double V, e;                 /* portfolio value since reset, exposure entering the step */
+    int k;                       /* steps since reset */
+    int nwin;                    /* actions in the diversity window */
+    int win[ORACLE_MAX_WIN];     /* their categories, oldest first */
+} env_state;
+
+static void env_reset(env_state *s) { s->V = 1.0; s->e = 0.0; s->k = 0; s->nwin = 0; }
+
+/* Portfolio, triple barrier, diversity, curiosity and reward for action a at
+ * bar b, from state x (= [F[b], V, e, spread]).  Fills xn with the pre-reset
+ * next state [F[b+1], V', e', spread].  gpu_done (or -1): the done decision of
+ * the path under test, adopted as in oracle_episode.  Sets *done; the state's
+ * V, e, k and window advance, and are reset when *done. */
+static double env_step(const float *cw, const oracle_cfg *c, const float *features, long b, const double *x,
+                       int a, int gpu_done, double done_band, env_state *es, oracle_stats *st, double *xn,
+                       int *done_out)
+{
+    const int nm = c->n_market, sd = nm + 3;
+    double pred[ORACLE_MAX_W];
+
+    /* step 6: portfolio */
+    double e2 = oracle_exposure(a);
+    double rate = oracle_tx_rate(a, c->tx_base);
+    double g = exp((double)features[(b + 1) * nm + 0]);
+    double V2 = es->V * (1.0 - fabs(e2 - es->e) * rate) * (1.0 + e2 * (g - 1.0));
+    double pnl = V2 / es->V - 1.0;
+
+    /* step 7: triple barrier */
+    es->k += 1;
+    double cpl = V2 - 1.0;
+    int label = (cpl >= c->barrier) ? 1 : (cpl <= -c->barrier) ? -1 : 0;
+    int done = (label != 0) || (es->k >= c->max_hold);
+    if (gpu_done >= 0 && (gpu_done != 0) != done) {
+        double gap = fmin(fabs(cpl - c->barrier), fabs(cpl + c->barrier));
+        if (gap < done_band) st->done_replays++;
+        else {
+            st->done_mismatches++;
+            if (gap > st->max_done_gap) st->max_done_gap = gap;
+        }
+        done = gpu_done != 0;
+        if (!done) label = 0;
+        else if (es->k < c->max_hold || label == 0)
+            label = (fabs(cpl - c->barrier) <= fabs(cpl + c->barrier)) ? 1 : -1;
+    }
+
+    /* step 8: diversity over the actions since reset (window of div_window) */
+    if (es->nwin == c->div_window) {
+        memmove(es->win, es->win + 1, sizeof(int) * (size_t)(es->nwin - 1));
+        es->nwin--;
+    }
+    es->win[es->nwin++] = oracle_category(a);
+    double H = oracle_window_entropy(es->win, es->nwin);
+    double div = (H < c->div_thresh) ? c->div_penalty : 0.0;
+
+    /* step 9: curiosity against the pre-reset next state */
+    for (int j = 0; j < nm; ++j) xn[j] = (double)features[(b + 1) * nm + j];
+    xn[nm] = V2; xn[nm + 1] = e2; xn[nm + 2] = c->spread;
+    curiosity_block(cw, c, x, a, pred);
+    double mse = 0.0;
+    for (int j = 0; j < sd; ++j) mse += (pred[j] - xn[j]) * (pred[j] - xn[j]);
+    mse /= (double)sd;
+    double cur = c->cur_coef * mse;
+
+    /* step 10: reward */
+    double risk = c->risk_coef * fabs(e2);
+    double beta = (label > 0) ? c->pt_scale : (label < 0) ? c->sl_scale : 0.0;
+    double rew = pnl * (1.0 + beta) + div + cur - risk;
+
+    /* step 12: reset on done (the caller's LCG is not reseeded, the bar keeps advancing) */
+    if (done) env_reset(es);
+    else { es->V = V2; es->e = e2; }
+    *done_out = done;
+    return rew;
+}
+
+/* ------------------------------------------------------------------ */
 /* one episode                                                          */
 /* ------------------------------------------------------------------ */
 
@@ -375,17 +463,17 @@ int oracle_episode(const float *w, const oracle_cfg *c, const float *features, l
     double *r = malloc(sizeof(double) * (size_t)L), *v = malloc(sizeof(double) * (size_t)L);
     int32_t *d = malloc(sizeof(int32_t) * (size_t)L);
     double x[ORACLE_MAX_W], xn[ORACLE_MAX_W], logits[ORACLE_MAX_W], cdf[ORACLE_MAX_W];
-    double pred[ORACLE_MAX_W];
-    int win[ORACLE_MAX_WIN];
-    int nwin = 0, k = 0;
-    double V = 1.0, e = 0.0;
+    env_state es;
+    env_reset(&es);
     uint32_t s = seed;
+    layout lo;
+    make_layout(c, &lo);
 
     for (int t = 0; t < L; ++t) {
         long b = (long)start + t;
         /* steps 1-2: market features and portfolio features */
         for (int j = 0; j < nm; ++j) x[j] = (double)features[b * nm + j];
-        x[nm] = V; x[nm + 1] = e; x[nm + 2] = c->spread;
+        x[nm] = es.V; x[nm + 1] = es.e; x[nm + 2] = c->spread;
 
         /* steps 3-4: actor, softmax, CDF draw */
         oracle_actor(w, c, x, logits);
@@ -409,53 +497,10 @@ int oracle_episode(const float *w, const oracle_cfg *c, const float *features, l
         /* step 5: critic */
         double val = oracle_critic(w, c, x);
 
-        /* step 6: portfolio */
-        double e2 = oracle_exposure(a);
-        double rate = oracle_tx_rate(a, c->tx_base);
-        double g = exp((double)features[(b + 1) * nm + 0]);
-        double V2 = V * (1.0 - fabs(e2 - e) * rate) * (1.0 + e2 * (g - 1.0));
-        double pnl = V2 / V - 1.0;
-
-        /* step 7: triple barrier */
-        k += 1;
-        double cpl = V2 - 1.0;
-        int label = (cpl >= c->barrier) ? 1 : (cpl <= -c->barrier) ? -1 : 0;
-        int done = (label != 0) || (k >= c->max_hold);
-        if (gpu_d && (gpu_d[t] != 0) != done) {
-            double gap = fmin(fabs(cpl - c->barrier), fabs(cpl + c->barrier));
-            if (gap < done_band) st->done_replays++;
-            else {
-                st->done_mismatches++;
-                if (gap > st->max_done_gap) st->max_done_gap = gap;
-            }
-            done = gpu_d[t] != 0;
-            if (!done) label = 0;
-            else if (k < c->max_hold || label == 0)
-                label = (fabs(cpl - c->barrier) <= fabs(cpl + c->barrier)) ? 1 : -1;
-        }
-
-        /* step 8: diversity over the actions since reset (window of div_window) */
-        if (nwin == c->div_window) {
-            memmove(win, win + 1, sizeof(int) * (size_t)(nwin - 1));
-            nwin--;
-        }
-        win[nwin++] = oracle_category(a);
-        double H = oracle_window_entropy(win, nwin);
-        double div = (H < c->div_thresh) ? c->div_penalty : 0.0;
-
-        /* step 9: curiosity against the pre-reset next state */
-        for (int j = 0; j < nm; ++j) xn[j] = (double)features[(b + 1) * nm + j];
-        xn[nm] = V2; xn[nm + 1] = e2; xn[nm + 2] = c->spread;
-        oracle_curiosity(w, c, x, a, pred);
-        double mse = 0.0;
-        for (int j = 0; j < sd; ++j) mse += (pred[j] - xn[j]) * (pred[j] - xn[j]);
-        mse /= (double)sd;
-        double cur = c->cur_coef * mse;
-
-        /* step 10: reward */
-        double risk = c->risk_coef * fabs(e2);
-        double beta = (label > 0) ? c->pt_scale : (label < 0) ? c->sl_scale : 0.0;
-        double rew = pnl * (1.0 + beta) + div + cur - risk;
+        /* steps 6-10 and 12 */
+        int done;
+        double rew = env_step(w + lo.q_w[0], c, features, b, x, a, gpu_d ? gpu_d[t] : -1, done_band, &es, st,
+                              xn, &done);
 
         /* step 11: store */
         if (o_states) for (int j = 0; j < sd; ++j) o_states[(long)t * sd + j] = (float)x[j];
@@ -465,10 +510,6 @@ int oracle_episode(const float *w, const oracle_cfg *c, const float *features, l
         if (o_r) o_r[t] = (float)rew;
         if (o_d) o_d[t] = done;
         r[t] = rew; v[t] = val; d[t] = done;
-
-        /* step 12: reset on done (LCG is not reseeded, the bar keeps advancing) */
-        if (done) { V = 1.0; e = 0.0; k = 0; nwin = 0; }
-        else { V = V2; e = e2; }
     }
 
     /* bootstrap: critic of the final pre-reset next state */

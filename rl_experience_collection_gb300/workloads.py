@@ -219,3 +219,49 @@ def replay_rows_device(j0: int, n: int, dim: int, device="cuda"):
     nxt = ((j % 65519).to(torch.float64)[:, None] - c[None, :]).to(torch.float32)
     return (states, nxt, (j % 45).to(torch.int32), ((j % 1021).to(torch.float64) / 1024.0).to(torch.float32),
             (j % 7 == 0).to(torch.uint8))
+
+
+# ---------------------------------------------------------------- DQN collector
+
+DQN_H, DQN_S = 256, 128     # dueling Q: 54 -> 256 -> 256, then value / advantage streams of 128
+DQN_EPSILON = 0.1           # exploration rate of the synthetic launches
+
+
+def dqn_layer_shapes() -> List[Tuple[str, Tuple[int, int]]]:
+    """One dueling Q net's matrices ``(name, (out, in))`` in packing order, each
+    followed by its bias: shared W1, W2; value stream Wv1, Wv2; advantage stream
+    Wa1, Wa2."""
+    return [("q1", (DQN_H, STATE_DIM)), ("q2", (DQN_H, DQN_H)), ("v1", (DQN_S, DQN_H)), ("v2", (1, DQN_S)),
+            ("a1", (DQN_S, DQN_H)), ("a2", (N_ACTIONS, DQN_S))]
+
+
+def dqn_net_params() -> int:
+    return sum(o * i + o for _, (o, i) in dqn_layer_shapes())
+
+
+def dqn_cur_params() -> int:
+    return CUR_H * (STATE_DIM + N_ACTIONS) + CUR_H + STATE_DIM * CUR_H + STATE_DIM
+
+
+# the DQN collector's workloads share the PPO workloads' environments and inputs
+DQN_WORKLOADS: Dict[str, Workload] = {
+    "dqn_tiny_bf16": dataclasses.replace(WORKLOADS["tiny_fp32"], name="dqn_tiny_bf16", dtype="bf16"),
+    "dqn_reset_heavy_bf16": dataclasses.replace(WORKLOADS["reset_heavy_bf16"], name="dqn_reset_heavy_bf16"),
+}
+
+
+def dqn_weights(seed: int, bias_scale: float = 0.0) -> np.ndarray:
+    """[online net | target net | curiosity block], float32: He-uniform matrices
+    (as init_weights), biases zero or U(-bias_scale, bias_scale).  The target net
+    is drawn independently of the online net (not a copy), so that a swap of the
+    two shows."""
+    rng = np.random.default_rng([seed, 0xD0])
+    parts = []
+    shapes = dqn_layer_shapes() + dqn_layer_shapes() + [("cur0", (CUR_H, STATE_DIM + N_ACTIONS)),
+                                                        ("cur1", (STATE_DIM, CUR_H))]
+    for _, (o, i) in shapes:
+        bound = math.sqrt(6.0 / i)
+        parts.append(rng.uniform(-bound, bound, size=(o, i)).astype(np.float32).ravel())
+        b = rng.uniform(-bias_scale, bias_scale, size=o) if bias_scale > 0 else np.zeros(o)
+        parts.append(b.astype(np.float32))
+    return np.concatenate(parts)
