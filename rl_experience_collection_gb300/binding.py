@@ -60,6 +60,11 @@ PER_EXPORTS = ["per_create", "per_insert", "per_sample", "per_update_priorities"
                "per_status", "per_destroy"]
 
 
+DQN_EXPORTS = ["dqn_weight_count", "dqn_create", "dqn_set_weights", "dqn_run", "dqn_status", "dqn_destroy",
+               "dqn_set_timing", "dqn_phase_ms"]
+DQN_OUTPUTS = ("states", "actions", "rewards", "dones", "q", "td", "next_states")
+
+
 class RolloutError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"rollout error {code}: {msg}")
@@ -103,6 +108,22 @@ def lib(path: Optional[str] = None):
     L.rollout_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
     L.rollout_last_error.restype = C.c_char_p
     L.rollout_last_error.argtypes = []
+    L.dqn_weight_count.restype = C.c_longlong
+    L.dqn_weight_count.argtypes = []
+    L.dqn_create.restype = C.c_int
+    L.dqn_create.argtypes = [vp, C.POINTER(RolloutDims), C.POINTER(vp)]
+    L.dqn_set_weights.restype = C.c_int
+    L.dqn_set_weights.argtypes = [vp, vp]
+    L.dqn_run.restype = C.c_int
+    L.dqn_run.argtypes = [vp, vp, vp, vp, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.dqn_status.restype = C.c_int
+    L.dqn_status.argtypes = [vp]
+    L.dqn_set_timing.restype = C.c_int
+    L.dqn_set_timing.argtypes = [vp, C.c_int]
+    L.dqn_phase_ms.restype = C.c_int
+    L.dqn_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
+    L.dqn_destroy.restype = None
+    L.dqn_destroy.argtypes = [vp]
     L.per_create.restype = C.c_int
     L.per_create.argtypes = [C.c_longlong, C.c_int, C.POINTER(vp)]
     L.per_insert.restype = C.c_int
@@ -461,6 +482,73 @@ class PerBuffer:
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:
             lib().per_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def make_dqn_outputs(N: int, L: int, device="cuda", next_states: bool = True) -> Dict[str, "torch.Tensor"]:
+    import torch
+    f32, i32 = torch.float32, torch.int32
+    out = {"states": torch.empty((N, L, wl.STATE_DIM), dtype=f32, device=device),
+           "actions": torch.empty((N, L), dtype=i32, device=device),
+           "rewards": torch.empty((N, L), dtype=f32, device=device),
+           "dones": torch.empty((N, L), dtype=i32, device=device),
+           "q": torch.empty((N, L), dtype=f32, device=device),
+           "td": torch.empty((N, L), dtype=f32, device=device)}
+    if next_states:
+        out["next_states"] = torch.empty((N, L, wl.STATE_DIM), dtype=f32, device=device)
+    return out
+
+
+class DqnCollector:
+    """Owns a ``dqn_handle`` (include/dqn.h): the DQN experience collector."""
+
+    def __init__(self, weights, dims: RolloutDims):
+        import numpy as np
+        self._w = np.ascontiguousarray(weights, dtype=np.float32)
+        if self._w.size != lib().dqn_weight_count():
+            raise ValueError(f"expected {lib().dqn_weight_count()} weights, got {self._w.size}")
+        h = C.c_void_p()
+        _check(lib().dqn_create(self._w.ctypes.data_as(C.c_void_p), C.byref(dims), C.byref(h)))
+        self._h = h
+
+    @classmethod
+    def for_workload(cls, w: wl.Workload, weights, n_bars: Optional[int] = None):
+        return cls(weights, make_dims(w, n_bars, "bf16"))
+
+    def set_weights(self, weights):
+        import numpy as np
+        self._w = np.ascontiguousarray(weights, dtype=np.float32)
+        _check(lib().dqn_set_weights(self._h, self._w.ctypes.data_as(C.c_void_p)))
+
+    def run(self, features, starts, seeds, N: int, L: int, gamma: float, epsilon: float,
+            out: Dict[str, "torch.Tensor"], stream=None) -> None:
+        """Enqueues one collection; `out` as make_dqn_outputs (next_states optional)."""
+        p = lambda t: C.c_void_p(None) if t is None else C.c_void_p(t.data_ptr())
+        _check(lib().dqn_run(self._h, p(features), p(starts), p(seeds), int(N), int(L), float(gamma), float(epsilon),
+                             p(out["states"]), p(out["actions"]), p(out["rewards"]), p(out["dones"]), p(out["q"]),
+                             p(out["td"]), p(out.get("next_states")), C.c_void_p(_stream_handle(stream))))
+
+    def set_timing(self, on: bool = True) -> None:
+        _check(lib().dqn_set_timing(self._h, int(on)))
+
+    def phase_ms(self):
+        """Device milliseconds of the last timed run's rollout, state-row and target kernels."""
+        ms = (C.c_float * 3)()
+        _check(lib().dqn_phase_ms(self._h, ms))
+        return [float(x) for x in ms]
+
+    def status(self) -> int:
+        return lib().dqn_status(self._h)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().dqn_destroy(self._h)
             self._h = C.c_void_p()
 
     def __del__(self):

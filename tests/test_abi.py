@@ -96,3 +96,21 @@ def test_library_exports_every_replay_symbol(libpath):
         assert hasattr(lib, name), name
     from rl_experience_collection_gb300 import binding
     assert set(binding.PER_EXPORTS) == set(names)
+
+
+def _declared_dqn():
+    src = open(os.path.join(ROOT, "include", "dqn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dqn_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_dqn_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    names = _declared_dqn()
+    assert {"dqn_create", "dqn_run", "dqn_destroy", "dqn_weight_count"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+    from rl_experience_collection_gb300 import binding
+    assert set(binding.DQN_EXPORTS) == set(names)
+    from rl_experience_collection_gb300 import workloads as wl
+    assert binding.lib().dqn_weight_count() == 2 * wl.dqn_net_params() + wl.dqn_cur_params()

@@ -1,0 +1,161 @@
+"""The DQN experience collector (include/dqn.h) against the oracle (oracle/dqn.c)
+on the same seeded inputs.
+
+Tolerances (the collector's bf16 tensor-core contract, as for the PPO path):
+  * actions, dones, the market and exposure columns of the states and next
+    states: exact.  Where the greedy action differs and the two actions' Q
+    values lie within Q_BAND * max(1, max |Q|) (a floating-point decision
+    between near-equal values) the oracle adopts the GPU's action and counts a
+    replay; dones as in the PPO parity (DONE_BAND);
+  * V (state column 51): float32 rounding, 2e-6 relative;
+  * rewards: abs 5e-2; q: |g - o| <= 2e-2 max(|o|, 1) (values);
+  * td = |r + gamma max Q_t - q|: its error is at most the reward's plus the two
+    values': 5e-2 + 2e-2 (2 |q| + |td| + 1).
+"""
+import numpy as np
+import pytest
+
+from rl_experience_collection_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+Q_BAND = 2e-3
+DONE_BAND = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rl_experience_collection_gb300 import build
+    build.build()
+    from oracle import dqn
+    dqn.build()
+
+
+def _run(w, inp, W, N, L, eps, next_states=True, starts=None):
+    import torch
+    from rl_experience_collection_gb300 import binding
+    h = binding.DqnCollector.for_workload(w, W, n_bars=inp.features.shape[0])
+    out = binding.make_dqn_outputs(N, L, next_states=next_states)
+    st = inp.starts[:N] if starts is None else starts
+    h.run(torch.from_numpy(inp.features).cuda(), torch.from_numpy(np.ascontiguousarray(st)).cuda(),
+          torch.from_numpy(inp.seeds[:N].view(np.int32)).cuda(), N, L, w.gamma, eps, out)
+    status = h.status()
+    h.close()
+    return status, {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def _compare(w, inp, W, g, idx, L, eps):
+    from oracle import dqn
+    sel = np.asarray(idx)
+    ref = dqn.rollout(w, inp, W, sel, eps, horizon=L, gpu_actions=g["actions"], gpu_dones=g["dones"],
+                      q_band=Q_BAND, done_band=DONE_BAND, threads=16)
+    st = ref["stats"]
+    assert st["action_mismatches"] == 0 and st["done_mismatches"] == 0, st
+    g = {k: v[sel] for k, v in g.items()}
+    np.testing.assert_array_equal(g["actions"], ref["actions"])
+    np.testing.assert_array_equal(g["dones"], ref["dones"])
+    for k in ("states", "next_states"):
+        if k not in g:
+            continue
+        np.testing.assert_array_equal(g[k][..., :51], ref[k][..., :51], err_msg=k)
+        np.testing.assert_array_equal(g[k][..., 52:], ref[k][..., 52:], err_msg=k)
+        np.testing.assert_allclose(g[k][..., 51], ref[k][..., 51], rtol=2e-6, atol=0, err_msg=k)
+    r64 = {k: ref[k].astype(np.float64) for k in ("rewards", "q", "td")}
+    assert np.abs(g["rewards"] - r64["rewards"]).max() <= 5e-2
+    assert (np.abs(g["q"] - r64["q"]) / np.maximum(np.abs(r64["q"]), 1.0)).max() <= 2e-2
+    tol = 5e-2 + 2e-2 * (2 * np.abs(r64["q"]) + np.abs(r64["td"]) + 1.0)
+    assert (np.abs(g["td"] - r64["td"]) <= tol).all()
+    assert (g["td"] >= 0).all()
+    return st
+
+
+@pytest.mark.parametrize("N,L,eps,next_states", [(300, 40, 0.1, True), (129, 25, 0.6, False), (1, 7, 0.0, True)])
+def test_dqn_matches_oracle(N, L, eps, next_states):
+    """Several CTAs with a ragged last one; exploration-heavy without the optional
+    next states; a single episode acting greedily."""
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
+    inp = wl.generate(w, n_episodes=N, horizon=L)
+    W = wl.dqn_weights(N, 0.05)
+    status, g = _run(w, inp, W, N, L, eps, next_states)
+    assert status == binding.ROLLOUT_OK
+    st = _compare(w, inp, W, g, np.arange(N), L, eps)
+    assert st["action_replays"] <= max(2, N * L // 2000)
+    if L > w.max_hold:                       # the time barrier alone ends every episode by then
+        assert g["dones"].sum() > 0
+
+
+def test_out_of_range_start_and_determinism():
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
+    N, L = 140, 20
+    inp = wl.generate(w, n_episodes=N, horizon=L)
+    W = wl.dqn_weights(7, 0.05)
+    starts = inp.starts[:N].copy()
+    starts[5] = inp.features.shape[0] - L          # start + L > n_bars - 1
+    s1, g1 = _run(w, inp, W, N, L, 0.2, starts=starts)
+    assert s1 == binding.ROLLOUT_ERR_RANGE
+    for k, v in g1.items():
+        assert not v[5].any(), k
+    keep = np.setdiff1d(np.arange(N), [5])
+    _compare(w, wl.Inputs(inp.features, starts, inp.seeds, inp.weights), W, g1, keep, L, 0.2)
+    s2, g2 = _run(w, inp, W, N, L, 0.2, starts=starts)
+    for k in g1:
+        np.testing.assert_array_equal(g1[k], g2[k], err_msg=k)
+
+
+def test_argument_validation():
+    import torch
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
+    inp = wl.generate(w, n_episodes=4, horizon=5)
+    W = wl.dqn_weights(1)
+    h = binding.DqnCollector.for_workload(w, W, n_bars=inp.features.shape[0])
+    out = binding.make_dqn_outputs(4, 5)
+    args = (torch.from_numpy(inp.features).cuda(), torch.from_numpy(inp.starts).cuda(),
+            torch.from_numpy(inp.seeds.view(np.int32)).cuda(), 4, 5, 0.99)
+    for eps in (-0.1, 1.5, float("nan")):
+        with pytest.raises(binding.RolloutError):
+            h.run(*args, eps, out)
+    bad = dict(out)
+    bad["td"] = None
+    with pytest.raises(binding.RolloutError):
+        h.run(*args, 0.1, bad)
+    with pytest.raises(ValueError):
+        binding.DqnCollector.for_workload(w, W[:-1], n_bars=inp.features.shape[0])
+    Wn = W.copy()
+    Wn[100] = np.inf
+    with pytest.raises(binding.RolloutError):
+        h.set_weights(Wn)
+    h.close()
+
+
+def test_full_size_sampled_episodes():
+    """The benchmark's launch (16384 episodes x 1000 steps): eight episodes spread
+    over the CTAs against the oracle, and properties of every transition."""
+    import torch
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_reset_heavy_bf16"]
+    N, L = w.n_episodes, w.horizon
+    inp = wl.generate(w)
+    W = wl.dqn_weights(w.seed, 0.05)
+    h = binding.DqnCollector.for_workload(w, W)
+    out = binding.make_dqn_outputs(N, L, next_states=False)
+    h.run(torch.from_numpy(inp.features).cuda(), torch.from_numpy(inp.starts).cuda(),
+          torch.from_numpy(inp.seeds.view(np.int32)).cuda(), N, L, w.gamma, wl.DQN_EPSILON, out)
+    assert h.status() == binding.ROLLOUT_OK
+    h.close()
+    a = out["actions"]
+    assert int(a.min()) >= 0 and int(a.max()) < wl.N_ACTIONS
+    assert bool((out["td"] >= 0).all()) and bool(torch.isfinite(out["q"]).all())
+    # V resets to 1 after every done
+    d = out["dones"][:, :-1].bool()
+    assert bool((out["states"][:, 1:, 51][d] == 1.0).all())
+    idx = np.array([0, 127, 128, 5000, 8191, 12345, 16255, 16383])
+    g = {k: v[idx].cpu().numpy() for k, v in out.items()}
+    sub = wl.Inputs(inp.features, inp.starts[idx], inp.seeds[idx], inp.weights)
+    st = _compare(w, sub, W, {k: v for k, v in g.items()}, np.arange(idx.size), L, wl.DQN_EPSILON)
+    assert st["action_replays"] <= 4
