@@ -198,6 +198,42 @@ def replay_sample_bytes(B, D, n_blocks):
     return B * (rounds * 32 * 8 + 16 * 8 + 128 * 4 + 2 * row + 4 + 8 + 8 + 4)
 
 
+DQN_NET_FLOP = 2 * (54 * 256 + 256 * 256 + 2 * 256 * 128 + 128 + 45 * 128)   # one dueling Q pass, valid dims
+DQN_CUR_FLOP = 2 * (54 * 64 + 64 * 54)                                    # curiosity (one-hot column adds not counted)
+
+
+def measure_dqn(dev, flush, steps, warmup):
+    """The DQN collector on the reset-heavy environment at full size (16384 x 1000,
+    bf16): CUDA events around each run (L2 flushed before it) and per-kernel times."""
+    import torch
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_reset_heavy_bf16"]
+    N, L = w.n_episodes, w.horizon
+    inp = wl.generate(w)
+    h = binding.DqnCollector.for_workload(w, wl.dqn_weights(w.seed, 0.05))
+    out = binding.make_dqn_outputs(N, L, dev, next_states=False)
+    stream = torch.cuda.current_stream(dev)
+    args = (torch.from_numpy(inp.features).to(dev), torch.from_numpy(inp.starts).to(dev),
+            torch.from_numpy(inp.seeds.view(np.int32)).to(dev), N, L, w.gamma, wl.DQN_EPSILON, out, stream)
+    for _ in range(warmup):
+        h.run(*args)
+    torch.cuda.synchronize()
+    h.set_timing(True)
+    ms, phase = [], []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(steps):
+        flush.fill_(float(i))
+        e0.record(stream)
+        h.run(*args)
+        e1.record(stream)
+        phase.append(h.phase_ms())
+        ms.append(e0.elapsed_time(e1))
+    if h.status() != binding.ROLLOUT_OK:
+        raise SystemExit("DQN status")
+    h.close()
+    return w, statistics.mean(ms), [statistics.mean(p[i] for p in phase) for i in range(3)]
+
+
 def launches_per_run(dtype):
     """Kernels one rollout_run launches: feature padding (bf16 only), rollout,
     state rows, value, GAE."""
@@ -343,6 +379,7 @@ def main():
     ap.add_argument("--ppo-steps", type=int, default=200, help="timed PPO optimizer steps (mini-batches of 512)")
     ap.add_argument("--no-replay", action="store_true", help="skip the prioritised-replay measurement")
     ap.add_argument("--replay-steps", type=int, default=200, help="timed replay sample + update calls")
+    ap.add_argument("--no-dqn", action="store_true", help="skip the DQN-collector measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = wl.WORKLOADS[args.workload]
@@ -463,6 +500,28 @@ def main():
                                 "unit": "GB/s", "frac": sb / (s_ms / 1000.0) / 1e9 / pk["hbm"],
                                 "algorithmic_bytes": sb},
             "gpu_launches_per_step": 7, "l2": "flushed before every timed call"}
+
+    # ---------------- the DQN collector on the same environment (rank 0)
+    if not args.no_dqn and rank == 0:
+        del out
+        out = None
+        torch.cuda.empty_cache()
+        dw, d_ms, (r_ms, s_ms, t_ms) = measure_dqn(dev, flush, args.steps, args.warmup)
+        T = dw.n_episodes * dw.horizon
+        r_fl, t_fl = T * DQN_NET_FLOP, T * (DQN_NET_FLOP + DQN_CUR_FLOP)
+        peak_b = pk["bf16"]
+        line["dqn"] = {
+            "workload": f"{dw.name}: {dw.n_episodes} x {dw.horizon}, epsilon {wl.DQN_EPSILON}, bf16",
+            "tuples_per_s": T / (d_ms / 1000.0), "ms_per_run": d_ms,
+            "phase_ms": {"rollout": r_ms, "states": s_ms, "target": t_ms},
+            "rollout_roofline": {"bound": "tensor", "achieved": r_fl / (r_ms / 1000.0) / 1e12, "peak": peak_b,
+                                 "unit": "TFLOP/s", "frac": r_fl / (r_ms / 1000.0) / 1e12 / peak_b,
+                                 "algorithmic_flop_per_launch": r_fl},
+            "target_roofline": {"bound": "tensor", "achieved": t_fl / (t_ms / 1000.0) / 1e12, "peak": peak_b,
+                                "unit": "TFLOP/s", "frac": t_fl / (t_ms / 1000.0) / 1e12 / peak_b,
+                                "algorithmic_flop_per_launch": t_fl},
+            "gpu_launches_per_run": 3, "l2": "flushed between runs"}
+        out = binding.make_outputs(N, L, dev)
 
     # ---------------- end to end through the C ABI with host buffers (rollout_run_host:
     # inputs copied in, every output copied back as soon as its kernel is done)
