@@ -25,9 +25,10 @@
 // array V' after the trade.
 //
 // Warp roles (both kernels): warps 0-7 are row warps (warp w serves TMEM lanes
-// and rows 32 (w % 4) .. + 31 and the column half w / 4 of each layer), warp 8
-// streams the weights (one elected lane), warp 9 allocates TMEM and one lane
-// issues the MMAs.  Every wait is bounded; a wait that gives up sets a flag
+// and rows 32 (w % 4) .. + 31 and the column half w / 4 of each layer), warps
+// 8-10 stream the weights, warp 8 + s filling ring stage s (the bulk copies of
+// one warp complete one after another, those of different warps overlap), and
+// warp 11 allocates TMEM and one lane issues the MMAs.  Every wait is bounded; a wait that gives up sets a flag
 // that ends every role's loop, and the status word records the timeout.
 #include <math.h>
 #include <string.h>
@@ -48,10 +49,10 @@ using namespace umma;
 
 constexpr int kH = 256, kHeadN = 48;
 constexpr int kRowWarps = 8;
-constexpr int kProdWarp = 8, kMmaWarp = 9, kThreads = 10 * 32;
+constexpr int kStages = 3;
+constexpr int kProdWarp0 = 8, kMmaWarp = kProdWarp0 + kStages, kThreads = (kMmaWarp + 1) * 32;
 constexpr int kChunk = 128 * 128;                   // one K-chunk (64 bf16 columns) of 128 rows
 constexpr int kStage = 32 * 1024;
-constexpr int kStages = 3;
 constexpr int kNetUnits = 10;                       // W1, W2 x4, W3 x4, head
 constexpr int kTargetUnits = 11;                    // curiosity C1|C2, then the target net's 10
 constexpr int kHeadTile = kHeadN * 128;             // one K-chunk of the head's 48 rows (6 KB)
@@ -343,21 +344,22 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_rollout_kernel(RolloutArgs a,
             }
             tc_fence_before();
         }
-    } else if (warp == kProdWarp) {
-        // ------------------------------------------------------------ weight stream
+    } else if (warp < kMmaWarp) {
+        // ------------------------------------------------------------ weight stream, stage st
+        const int st = warp - kProdWarp0;
         if (lane == 0) {
             const long long total = (long long)kNetUnits * L;
-            long long u = 0;
-            for (; u < total; ++u) {
-                const int st = (int)(u % kStages), i = (int)(u % kNetUnits);
+            long long last = -1;
+            for (long long u = st; u < total; u += kStages) {
+                const int i = (int)(u % kNetUnits);
                 if (u >= kStages && !mbar_wait(&bars->empty[st], (uint32_t)((u / kStages - 1) & 1), &abort_flag))
                     break;
                 mbar_arrive_expect_tx(&bars->full[st], w.unit_bytes[i]);
                 bulk_g2s(ring + st * kStage, w.base + w.unit_off[i], w.unit_bytes[i], &bars->full[st]);
+                last = u;
             }
-            // copies still in flight complete before the CTA may exit
-            for (long long v = (u > kStages ? u - kStages : 0); v < u; ++v)
-                mbar_wait_drain(&bars->full[v % kStages], (uint32_t)((v / kStages) & 1));
+            // its last copy completes before the CTA may exit
+            if (last >= 0) mbar_wait_drain(&bars->full[st], (uint32_t)((last / kStages) & 1));
         }
     } else {
         // ------------------------------------------------------------ MMA issue
@@ -606,20 +608,21 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, D
             }
             tc_fence_before();
         }
-    } else if (warp == kProdWarp) {
+    } else if (warp < kMmaWarp) {
+        const int st = warp - kProdWarp0;
         if (lane == 0) {
             const long long my_tiles = n_tiles > blockIdx.x ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
             const long long total = my_tiles * kTargetUnits;
-            long long u = 0;
-            for (; u < total; ++u) {
-                const int st = (int)(u % kStages), i = kNetUnits + (int)(u % kTargetUnits);
+            long long last = -1;
+            for (long long u = st; u < total; u += kStages) {
+                const int i = kNetUnits + (int)(u % kTargetUnits);
                 if (u >= kStages && !mbar_wait(&bars->empty[st], (uint32_t)((u / kStages - 1) & 1), &abort_flag))
                     break;
                 mbar_arrive_expect_tx(&bars->full[st], w.unit_bytes[i]);
                 bulk_g2s(ring + st * kStage, w.base + w.unit_off[i], w.unit_bytes[i], &bars->full[st]);
+                last = u;
             }
-            for (long long v = (u > kStages ? u - kStages : 0); v < u; ++v)
-                mbar_wait_drain(&bars->full[v % kStages], (uint32_t)((v / kStages) & 1));
+            if (last >= 0) mbar_wait_drain(&bars->full[st], (uint32_t)((last / kStages) & 1));
         }
     } else {
         if (lane == 0) {
