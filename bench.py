@@ -310,12 +310,14 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(float(r[2]) for r in rows)}
 
 
-def dist_setup():
+def dist_setup(backend: str = "nccl"):
+    """(rank, world size, torch.distributed or None) from the launcher's environment
+    (RANK, WORLD_SIZE, MASTER_ADDR, MASTER_PORT); one process per GPU."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws <= 1:
         return 0, 1, None
     import torch.distributed as dist
-    dist.init_process_group("nccl")
+    dist.init_process_group(backend)
     return dist.get_rank(), ws, dist
 
 
@@ -403,7 +405,7 @@ def main():
     if dist is not None:
         dist.barrier()
     N, L = w.n_episodes, w.horizon
-    inputs = wl.generate(w)
+    inputs = wl.generate(w, shard=rank)          # this rank's episodes (weak scaling: N per GPU)
     h = binding.Rollout.for_workload(w, inputs.weights)
     feats = torch.from_numpy(inputs.features).to(dev)
     starts = torch.from_numpy(inputs.starts).to(dev)

@@ -119,10 +119,11 @@ def splitmix64(x: int) -> int:
     return z ^ (z >> 31)
 
 
-def episode_seeds(seed: int, n: int) -> np.ndarray:
-    """``seeds[i] = low32(splitmix64(seed * 2**32 + i))`` as uint32."""
+def episode_seeds(seed: int, n: int, first: int = 0) -> np.ndarray:
+    """``seeds[i] = low32(splitmix64(seed * 2**32 + first + i))`` as uint32 (global
+    episode index first + i)."""
     base = (seed & 0xFFFFFFFF) << 32
-    return np.array([splitmix64(base + i) & 0xFFFFFFFF for i in range(n)], dtype=np.uint32)
+    return np.array([splitmix64(base + first + i) & 0xFFFFFFFF for i in range(n)], dtype=np.uint32)
 
 
 def init_weights(rng: np.random.Generator, critic_h: Tuple[int, ...]) -> np.ndarray:
@@ -143,11 +144,15 @@ class Inputs:
     weights: np.ndarray        # packed float32
 
 
-def generate(w: Workload, n_episodes: int | None = None, horizon: int | None = None) -> Inputs:
+def generate(w: Workload, n_episodes: int | None = None, horizon: int | None = None, shard: int = 0) -> Inputs:
     """Seeded synthetic inputs for workload ``w``.
 
     ``n_episodes``/``horizon`` override N and L (starts are then drawn for the
-    overridden sizes); everything else follows the workload's recipe.
+    overridden sizes); everything else follows the workload's recipe.  ``shard``
+    s > 0 gives the s-th block of N episodes of a larger batch (one block per
+    process of a multi-GPU run): the same features and weights, the episodes'
+    own LCG seeds (global episode indices s*N ..) and start bars (drawn from the
+    generator seeded with [seed, s]); shard 0 is the workload's own draw.
     """
     n = w.n_episodes if n_episodes is None else n_episodes
     L = w.horizon if horizon is None else horizon
@@ -156,7 +161,9 @@ def generate(w: Workload, n_episodes: int | None = None, horizon: int | None = N
     feats[:, 0] = rng.normal(0.0, w.sigma, size=w.n_bars).astype(np.float32)
     starts = rng.integers(0, w.n_bars - L, size=n).astype(np.int32)
     weights = init_weights(rng, w.critic_h)
-    return Inputs(np.ascontiguousarray(feats), starts, episode_seeds(w.seed, n), weights)
+    if shard:
+        starts = np.random.default_rng([w.seed, shard]).integers(0, w.n_bars - L, size=n).astype(np.int32)
+    return Inputs(np.ascontiguousarray(feats), starts, episode_seeds(w.seed, n, first=shard * n), weights)
 
 
 def weight_views(weights: np.ndarray, critic_h: Tuple[int, ...] = CRITIC_STD) -> Dict[str, np.ndarray]:
