@@ -377,7 +377,6 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_rollout_kernel(RolloutArgs a,
                         ++h_phase;
                         tc_fence_after();
                     }
-                    const int nk = layer == 0 ? 1 : 4;
                     const int n_units = (layer == 0 || layer == 3) ? 1 : 4;
                     for (int cu = 0; cu < n_units; ++cu, ++u) {
                         const int st = (int)(u % kStages);
@@ -393,7 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_rollout_kernel(RolloutArgs a,
                         mma_commit(&bars->empty[st]);
                     }
                     if (ok) mma_commit(&bars->acc);
-                    (void)nk;
                 }
             }
             // every MMA issued has completed before TMEM is freed
