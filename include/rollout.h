@@ -42,7 +42,7 @@ extern "C" {
 #define ROLLOUT_ERR_RANGE       -2  /* an episode start outside [0, n_bars - L - 1] (device-detected) */
 #define ROLLOUT_ERR_CUDA        -3  /* a CUDA runtime call failed; see rollout_last_error() */
 #define ROLLOUT_ERR_TIMEOUT     -4  /* a bounded device-side wait expired (device-detected) */
-#define ROLLOUT_ERR_UNSUPPORTED -5  /* network shape / dtype / constant this build does not handle */
+#define ROLLOUT_ERR_UNSUPPORTED -5  /* a network shape, dtype or constant the library does not handle */
 #define ROLLOUT_ERR_NOMEM       -6  /* device allocation failed */
 
 /* arithmetic of the MLPs (the environment, sampler and GAE are float32 throughout) */
