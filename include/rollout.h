@@ -180,6 +180,22 @@ ROLLOUT_API int rollout_set_timing(rollout_handle *h, int on);
 ROLLOUT_API int rollout_phase_ms(rollout_handle *h, float *ms);
 
 /*
+ * rollout_test_stall -- a test hook for the device-side timeout path, not for
+ * production use.  When on != 0, every later run of this handle on the
+ * tensor-core path (ROLLOUT_TF32, ROLLOUT_BF16) launches a test build of the
+ * value kernel in which CTA 0 never copies its first weight stage: that CTA's
+ * MMA issuer waits on a stage that never fills, its bounded wait expires
+ * after about two seconds, every warp of the CTA leaves, waits (bounded) for
+ * its copies in flight and releases its tensor memory, and the run records
+ * ROLLOUT_ERR_TIMEOUT (read with rollout_status).  The other CTAs finish
+ * normally; the values, rewards, advantages and returns of CTA 0's tiles are
+ * then undefined.  on == 0 restores the normal kernel.  Returns ROLLOUT_OK, or
+ * ROLLOUT_ERR_INVALID for a null handle or an ROLLOUT_FP32 handle (whose
+ * kernels have no waits).
+ */
+ROLLOUT_API int rollout_test_stall(rollout_handle *h, int on);
+
+/*
  * rollout_run_static -- rollout_run for callers that cannot allocate device
  * memory.  (An addition of this library; the paper has no counterpart.)
  *

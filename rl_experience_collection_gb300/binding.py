@@ -26,7 +26,7 @@ DTYPE = {"fp32": 0, "tf32": 1, "bf16": 2}
 
 EXPORTS = ["rollout_create", "rollout_set_weights", "rollout_run", "rollout_status", "rollout_destroy",
            "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static", "rollout_run_host",
-           "rollout_set_weights_device"]
+           "rollout_set_weights_device", "rollout_test_stall"]
 
 
 class RolloutDims(C.Structure):
@@ -106,6 +106,8 @@ def lib(path: Optional[str] = None):
     L.rollout_set_timing.argtypes = [vp, C.c_int]
     L.rollout_phase_ms.restype = C.c_int
     L.rollout_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
+    L.rollout_test_stall.restype = C.c_int
+    L.rollout_test_stall.argtypes = [vp, C.c_int]
     L.rollout_last_error.restype = C.c_char_p
     L.rollout_last_error.argtypes = []
     L.dqn_weight_count.restype = C.c_longlong
@@ -297,6 +299,10 @@ class Rollout:
         ms = (C.c_float * 4)()
         _check(lib().rollout_phase_ms(self._h, ms))
         return [float(x) for x in ms]
+
+    def test_stall(self, on: bool = True) -> None:
+        """Test hook: later runs launch the value kernel's stalling test build."""
+        _check(lib().rollout_test_stall(self._h, int(on)))
 
     def status(self) -> int:
         return lib().rollout_status(self._h)

@@ -64,13 +64,15 @@ struct rollout_handle {
     int scratch_ctas = 0;
     // bf16 rollout: feature rows padded to kFPad floats and a tensor map over them
     float *d_fpad = nullptr;
-    alignas(64) CUtensorMap fmap{};
+    CUtensorMap fmap{};   // the type carries its own alignment
     // environment
     uint32_t *d_div_low = nullptr;
     int *d_status = nullptr;
     cudaStream_t last_stream = nullptr;
     // optional per-kernel timing
     bool timing = false, timed_run = false;
+    // rollout_test_stall: runs launch the value kernel's stalling test build
+    bool test_stall = false;
     cudaEvent_t ev[kTimedKernels + 1] = {};
     // rollout_run_host: device copies of the inputs and outputs (one allocation,
     // grown on demand), the copy streams and their events
@@ -620,8 +622,9 @@ int enqueue_run(rollout_handle *h, const RunBuffers &b, int N, int L, float gamm
     if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
     if ((e = mark(2)) != cudaSuccess || (e = point(kAfterStates)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if (d.dtype == ROLLOUT_FP32) e = launch_value_simt(va, h->simt, s);
-    else if (value_needs_scratch(h->umma)) e = launch_value_generic(va, h->umma, vs.ptr, vs.per_cta, vs.grid, s);
-    else e = launch_value_umma(va, h->umma, s);
+    else if (value_needs_scratch(h->umma))
+        e = launch_value_generic(va, h->umma, vs.ptr, vs.per_cta, vs.grid, s, h->test_stall);
+    else e = launch_value_umma(va, h->umma, s, h->test_stall);
     if (e != cudaSuccess) return cuda_fail(e, "value launch");
     if ((e = mark(3)) != cudaSuccess || (e = point(kAfterValue)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if ((e = launch_gae(ga, s)) != cudaSuccess) return cuda_fail(e, "gae launch");
@@ -858,6 +861,15 @@ int rollout_set_timing(rollout_handle *h, int on)
     }
     h->timing = on != 0;
     h->timed_run = false;
+    return ROLLOUT_OK;
+}
+
+int rollout_test_stall(rollout_handle *h, int on)
+{
+    g_err[0] = 0;
+    if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
+    if (h->dims.dtype == ROLLOUT_FP32) return fail(ROLLOUT_ERR_INVALID, "the fp32 path has no bounded waits to stall");
+    h->test_stall = on != 0;
     return ROLLOUT_OK;
 }
 

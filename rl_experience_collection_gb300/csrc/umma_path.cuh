@@ -78,11 +78,13 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *host_w, co
 cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s);
 cudaError_t launch_pad_features(const float *F, float *fpad, int n_bars, cudaStream_t s);
 // bf16 operands with the 512/384/256/128/64 critic: activations resident in shared memory
-cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s);
+// stall: launch the test build whose first weight producer in CTA 0 issues
+// nothing (that CTA's bounded wait expires and the run reports a timeout)
+cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s, bool stall);
 // every other shape: activations in per-CTA global scratch (see value_generic.cu)
 long long value_generic_scratch_per_cta(const UmmaWeights &w);
 cudaError_t launch_value_generic(const ValueArgs &a, const UmmaWeights &w, uint8_t *scratch, long long per_cta,
-                                 int grid, cudaStream_t s);
+                                 int grid, cudaStream_t s, bool stall);
 inline bool value_needs_scratch(const UmmaWeights &w) { return !w.bf16 || w.wide; }
 
 }  // namespace rl

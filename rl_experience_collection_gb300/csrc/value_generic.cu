@@ -129,6 +129,23 @@ __device__ __forceinline__ void fence_async_global()
 
 __device__ __forceinline__ void row_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory"); }
 
+// row_sync that also returns the AND of `pred` over every row thread: a wait
+// that expired in one row warp may have succeeded in another, and all row
+// warps must leave the tile loop together (they share barrier 1)
+__device__ __forceinline__ bool row_sync_and(bool pred)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)pred), "n"(kRowThreads)
+        : "memory");
+    return out != 0;
+}
+
 struct RowInfoG {
     int kind;            // 0 tuple, 1 bootstrap row, 2 tuple of an invalid episode, 3 bootstrap of one, -1 none
     long long row, bar;
@@ -184,7 +201,10 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar)
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-template <bool BF16>
+// kStall: a test build in which the producer of CTA 0 issues no copy, so that
+// CTA's MMA issuer waits on a stage that never fills and the bounded-wait exit
+// runs (rollout_test_stall)
+template <bool BF16, bool kStall>
 __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a, UmmaWeights w, uint8_t *scratch,
                                                                     long long scratch_per_cta)
 {
@@ -234,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
             int stage = 0;
             uint32_t phase = 0, act_ph = 0;
             bool ok = true;
-            for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+            const bool silent = kStall && blockIdx.x == 0;
+            for (long long tile = blockIdx.x; tile < n_tiles && ok && !silent; tile += gridDim.x) {
                 for (int jj = 0; jj < 7 && ok; ++jj) {
                     const Job J = kJobs[jj];
                     const UmmaLayer &Ly = w.job[J.layer];
@@ -422,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                     a.boot[ri.row] = 0.f;
                 }
             }
-            row_sync();
+            ok = row_sync_and(ok);                             // every row warp leaves on the same tile
         }
     }
     if (abort_sh && tid == 0) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
@@ -434,16 +455,20 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
 
 template <bool BF16>
 cudaError_t launch_g(const ValueArgs &a, const UmmaWeights &w, uint8_t *scratch, long long per_cta, int grid,
-                     cudaStream_t s)
+                     cudaStream_t s, bool stall)
 {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(value_generic_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmem);
+        cudaError_t e = cudaFuncSetAttribute(value_generic_kernel<BF16, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(value_generic_kernel<BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    value_generic_kernel<BF16><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
+    if (stall) value_generic_kernel<BF16, true><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
+    else value_generic_kernel<BF16, false><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
     return cudaGetLastError();
 }
 
@@ -460,7 +485,7 @@ long long value_generic_scratch_per_cta(const UmmaWeights &w)
 }
 
 cudaError_t launch_value_generic(const ValueArgs &a, const UmmaWeights &w, uint8_t *scratch, long long per_cta,
-                                 int grid, cudaStream_t s)
+                                 int grid, cudaStream_t s, bool stall)
 {
     for (int j = 0; j < kNumJobs; ++j) {
         const UmmaLayer &L = w.job[j];
@@ -471,7 +496,8 @@ cudaError_t launch_value_generic(const ValueArgs &a, const UmmaWeights &w, uint8
         }
         if (L.k_chunks > 16) return cudaErrorInvalidValue;
     }
-    return w.bf16 ? launch_g<true>(a, w, scratch, per_cta, grid, s) : launch_g<false>(a, w, scratch, per_cta, grid, s);
+    return w.bf16 ? launch_g<true>(a, w, scratch, per_cta, grid, s, stall)
+                  : launch_g<false>(a, w, scratch, per_cta, grid, s, stall);
 }
 
 }  // namespace rl

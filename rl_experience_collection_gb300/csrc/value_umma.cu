@@ -422,6 +422,10 @@ struct MmaCtx {
     }
 };
 
+// kStall: a test build in which the first producer of CTA 0 issues no copy, so
+// that CTA's MMA issuer waits on a weight stage that never fills and the
+// bounded-wait exit runs (rollout_test_stall)
+template <bool kStall>
 __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs a, UmmaWeights w)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -499,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             uint32_t k = 0;                            // uses of stage ps so far
             long long g = 0;                           // unit counter over all tiles: unit g goes to stage g % kStages
             bool ok = true;
-            for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+            const bool silent = kStall && blockIdx.x == 0 && ps == 0;
+            for (long long tile = blockIdx.x; tile < n_tiles && ok && !silent; tile += gridDim.x) {
                 for (int u = 0; u < kUnits && ok; ++u, ++g) {
                     if (g % kStages != ps) continue;
                     const uint32_t bytes = w.unit_bytes[u];
@@ -679,6 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
         RowInfo nri = resolve(a, nf);
         build_x(nri);
         cur1_epilogue(nri);
+        // a wait that expired in one row warp may have succeeded in another (the
+        // barrier completing just after the limit): agree before the first
+        // row_sync, so that every row warp runs the same barriers
+        ok = row_sync_and(ok);
 
         for (; tile < n_tiles && ok; tile += gridDim.x) {
             const RowInfo ri = nri;
@@ -789,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
 
 }  // namespace
 
-cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s)
+cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStream_t s, bool stall)
 {
     if (!w.bf16 || w.wide || w.n_units != kUnits) return cudaErrorNotSupported;
     if ((reinterpret_cast<uintptr_t>(a.F) & 15u) != 0) return cudaErrorInvalidValue;   // feature copies
@@ -797,7 +806,10 @@ cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStre
         if (w.unit_bytes[u] > (uint32_t)kStage || (w.unit_bytes[u] & 15u) || (w.unit_off[u] & 15)) return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(value_umma_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        cudaError_t e = cudaFuncSetAttribute(value_umma_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(value_umma_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -807,7 +819,8 @@ cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStre
     const long long total = (long long)a.N * a.L + a.N;
     const long long tiles = (total + 127) / 128;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    value_umma_bf16_kernel<<<grid, kThreads, kSmem, s>>>(a, w);
+    if (stall) value_umma_bf16_kernel<true><<<grid, kThreads, kSmem, s>>>(a, w);
+    else value_umma_bf16_kernel<false><<<grid, kThreads, kSmem, s>>>(a, w);
     return cudaGetLastError();
 }
 

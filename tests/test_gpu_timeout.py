@@ -1,0 +1,85 @@
+"""The device-side timeout path (include/rollout.h, rollout_test_stall).
+
+A test build of the value kernel leaves CTA 0's first weight stage unfilled, so
+that CTA's MMA issuer waits on a barrier that nothing completes.  The bounded
+wait must expire (about two seconds), every warp of the CTA must leave and
+release its tensor memory, the run must report ROLLOUT_ERR_TIMEOUT, and the
+handle's next run must be bit-identical to a run before the stall.  Nothing
+faults, traps or hangs: the wait that runs out is the kernel's own bounded
+wait, and only the status word carries the failure to the host.
+
+Both value kernels are covered: the shared-memory-resident bf16 kernel
+(standard critic) and the scratch-staged one (tf32; bf16 with the wide
+critic)."""
+import time
+
+import numpy as np
+import pytest
+
+from rl_experience_collection_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rl_experience_collection_gb300 import build
+    build.build()
+
+
+def _run(h, dev, N, L, w):
+    from rl_experience_collection_gb300 import binding
+    out = binding.make_outputs(N, L)
+    t0 = time.perf_counter()
+    h.run(*dev, N, L, w.gamma, w.lam, out)
+    status = h.status()                       # synchronises
+    return status, time.perf_counter() - t0, {k: v.cpu().numpy() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("name,N,L", [("reset_heavy_bf16", 300, 20), ("scaleout_tf32", 130, 16),
+                                      ("ceiling_bf16", 129, 12)])
+def test_stalled_value_kernel_times_out_and_handle_recovers(name, N, L):
+    import torch
+    from rl_experience_collection_gb300 import binding
+    w = wl.WORKLOADS[name]
+    inp = wl.generate(w, n_episodes=N, horizon=L)
+    dev = (torch.from_numpy(inp.features).cuda(), torch.from_numpy(inp.starts[:N]).cuda(),
+           torch.from_numpy(inp.seeds[:N].view(np.int32)).cuda())
+    h = binding.Rollout.for_workload(w, inp.weights, n_bars=inp.features.shape[0])
+    s0, _, before = _run(h, dev, N, L, w)
+    assert s0 == binding.ROLLOUT_OK
+
+    h.test_stall(True)
+    s1, dt, stalled = _run(h, dev, N, L, w)
+    assert s1 == binding.ROLLOUT_ERR_TIMEOUT, binding.last_error()
+    assert 1.5 < dt < 60.0, dt                 # the wait ran to its limit, then the kernel left
+    assert h.status() == binding.ROLLOUT_ERR_TIMEOUT   # the last run's status until the next run
+    # the rollout kernel ran before the stalled one: its outputs are untouched
+    for k in ("actions", "logp", "dones", "states"):
+        np.testing.assert_array_equal(stalled[k], before[k], err_msg=k)
+    if name == "reset_heavy_bf16":
+        # one CTA per tile here (fewer tiles than SMs): only tile 0's rows
+        # (the first 128 of the N x L transitions) lack their values
+        tiles = (N * L + N + 127) // 128
+        assert tiles < torch.cuda.get_device_properties(0).multi_processor_count
+        np.testing.assert_array_equal(stalled["values"].reshape(-1)[128:], before["values"].reshape(-1)[128:])
+
+    h.test_stall(False)
+    s2, _, after = _run(h, dev, N, L, w)
+    assert s2 == binding.ROLLOUT_OK
+    for k in before:
+        np.testing.assert_array_equal(after[k], before[k], err_msg=k)
+    h.close()
+
+
+def test_stall_hook_rejects_the_fp32_path():
+    from rl_experience_collection_gb300 import binding
+    w = wl.WORKLOADS["tiny_fp32"]
+    inp = wl.generate(w, n_episodes=4, horizon=4)
+    h = binding.Rollout.for_workload(w, inp.weights, n_bars=inp.features.shape[0])
+    with pytest.raises(binding.RolloutError):
+        h.test_stall(True)
+    h.close()
