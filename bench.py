@@ -14,6 +14,7 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import atexit
 import dataclasses
 import json
 import math
@@ -267,48 +268,101 @@ def tensor_peak(dtype: str, pk):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms.
+
+    Started before the warm-up, so that nvidia-smi is already sampling when the
+    timed region begins; mark() brackets that region with the host's wall clock,
+    and summary() keeps the samples whose nvidia-smi timestamps fall inside it
+    (or, where a timestamp does not parse, the lines written after the region
+    began)."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
+    TS_FORMAT = "%Y/%m/%d %H:%M:%S.%f"
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, index: int, interval_ms: int = 50, exe: str = "nvidia-smi"):
+        self.index, self.interval_ms, self.exe = index, interval_ms, exe
         self.proc = None
         self.path = os.path.join(tempfile.gettempdir(), f"bench_clocks_{os.getpid()}.csv")   # transient
+        self.t0 = self.t1 = None
+        self.lines_at_t0 = 0
 
-    def __enter__(self):
+    def start(self, settle_s: float = 2.0):
+        """Starts sampling and waits (at most settle_s) for the first sample."""
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+            self.proc = subprocess.Popen([self.exe, f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return self
+        end = time.time() + settle_s
+        while time.time() < end and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+            time.sleep(0.01)
         return self
 
-    def __exit__(self, *a):
-        if self.proc:
+    def _lines(self):
+        try:
+            return open(self.path).read().strip().splitlines()
+        except OSError:
+            return []
+
+    def mark(self, begin: bool):
+        """Brackets the timed region (call with True just before it, False just after)."""
+        if begin:
+            self.t0 = time.time()
+            self.lines_at_t0 = len(self._lines())
+        else:
+            self.t1 = time.time()
+            time.sleep(2.5 * self.interval_ms / 1000.0)    # the sample taken at the region's end
+
+    def stop(self):
+        if not self.proc:
+            return
+        if self.proc.poll() is None:
             self.proc.terminate()
-            self.proc.wait()
+            try:
+                self.proc.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.proc.wait()
+        if not self.f.closed:
             self.f.close()
+
+    def _in_region(self, rows):
+        import datetime
+        slack = self.interval_ms / 1000.0
+        try:
+            ts = [datetime.datetime.strptime(r[0].strip(), self.TS_FORMAT).timestamp() for r in rows]
+        except ValueError:
+            return rows[self.lines_at_t0:], "lines written after the region began"
+        if self.t0 is None or self.t1 is None:
+            return rows, "whole run"
+        sel = [r for r, t in zip(rows, ts) if self.t0 - slack <= t <= self.t1 + slack]
+        return sel, "timed region"
 
     def summary(self):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.count(",") >= 7]
+        rows = [r.split(",") for r in self._lines() if r.count(",") >= 8]
         try:
             os.remove(self.path)
         except OSError:
             pass
+        rows, window = self._in_region(rows)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[0]) for r in rows]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip() == "Active"})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]), "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(float(r[2]) for r in rows)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "window": window}
+        try:
+            sm = [float(r[1]) for r in rows]
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+            return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                    "samples": len(rows), "window": window, "interval_ms": self.interval_ms,
+                    "power_w_median": statistics.median(float(r[3]) for r in rows),
+                    "power_w_max": max(float(r[3]) for r in rows)}
+        except (ValueError, IndexError):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed samples"], "window": window}
 
 
 def dist_setup(backend: str = "nccl"):
@@ -418,11 +472,14 @@ def main():
     def step():
         h.run(feats, starts, seeds, N, L, w.gamma, w.lam, out, stream)
 
+    clk = ClockSampler(torch.cuda.current_device()).start()
+    atexit.register(clk.stop)                    # no sampler outlives the run
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     st = h.status()
     if st != binding.ROLLOUT_OK:
+        clk.stop()
         raise SystemExit(f"device status {st} after warm-up")
 
     # ---------------- device-resident timing (per step, L2 flushed between steps)
@@ -432,7 +489,8 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
+    clk.mark(True)
+    try:
         for i in range(args.steps):
             flush.fill_(float(i))
             ev[i][0].record(stream)
@@ -440,6 +498,9 @@ def main():
             ev[i][1].record(stream)
             phase.append(h.phase_ms())
         torch.cuda.synchronize()
+        clk.mark(False)
+    finally:
+        clk.stop()
     if dist is not None:
         dist.barrier()
     h.set_timing(False)
