@@ -149,3 +149,41 @@ def test_td_error_closed_form():
                 want = abs(r + gamma * qt.max() * (1 - d) - q)
                 # the oracle forms td from unrounded r and q; the outputs are float32
                 assert abs(out["td"][n, t] - want) <= 1e-6 * max(1.0, abs(want)), (gamma, n, t)
+
+
+@pytest.mark.parametrize("quant", ["fp32", "bf16"])
+def test_biases_and_stream_heads_closed_form(quant):
+    """W1 = 0 and W2 = I with random biases (half of them negative, so that the
+    LeakyReLU slope shows in every layer), selector stream inputs, and random
+    stream heads Wv2 [1 x 128], Wa2 [45 x 128]: every bias enters its own layer,
+    and the heads are the stated [out, in] products (operands rounded once in
+    bf16 mode, biases not)."""
+    w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
+    cfg = orc.make_cfg(w, quant)
+    rng = np.random.default_rng(7)
+    f32 = lambda a: np.asarray(a, np.float32)
+    b1, b2 = f32(rng.standard_normal(H)), f32(rng.standard_normal(H))
+    bv1, ba1 = f32(rng.standard_normal(S)), f32(rng.standard_normal(S))
+    Wv2, bv2 = f32(rng.standard_normal((1, S)) * 0.1), f32([0.3])
+    Wa2, ba2 = f32(rng.standard_normal((NA, S)) * 0.1), f32(rng.standard_normal(NA) * 0.1)
+    Wv1 = np.zeros((S, H), np.float32)
+    Wv1[np.arange(S), np.arange(S)] = 1.0
+    Wa1 = np.zeros((S, H), np.float32)
+    Wa1[np.arange(S), S + np.arange(S)] = 1.0
+    parts = [np.zeros((H, SD)), b1, np.eye(H), b2, Wv1, bv1, Wv2, bv2, Wa1, ba1, Wa2, ba2]
+    net = np.concatenate([f32(p).ravel() for p in parts])
+    assert net.size == dqn.net_count(cfg)
+    rnd = _bf16 if quant == "bf16" else (lambda v: np.asarray(v, np.float64))
+    d = lambda a: np.asarray(a, np.float64)
+    h1 = _leaky(d(b1))                                   # W1 = 0: the state does not matter
+    h2 = _leaky(rnd(h1) + d(b2))
+    hv = _leaky(rnd(h2)[:S] + d(bv1))
+    ha = _leaky(rnd(h2)[S:] + d(ba1))
+    V0 = float(rnd(Wv2.ravel()) @ rnd(hv)) + float(bv2[0])
+    A0 = rnd(Wa2.ravel()).reshape(NA, S) @ rnd(ha) + d(ba2)
+    assert (b1 < 0).any() and (bv1 < 0).any() and (ba1 < 0).any()
+    for x in (np.zeros(SD), rng.standard_normal(SD)):
+        V, A = dqn.q_parts(net, cfg, x)
+        assert abs(V - V0) <= 1e-12 * max(1.0, abs(V0))
+        np.testing.assert_allclose(A, A0, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dqn.q_values(net, cfg, x), V0 + (A0 - A0.mean()), rtol=1e-12, atol=1e-12)
