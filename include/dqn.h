@@ -90,6 +90,20 @@ ROLLOUT_API int dqn_run(dqn_handle *h, const float *features, const int32_t *sta
 ROLLOUT_API int dqn_set_timing(dqn_handle *h, int on);
 ROLLOUT_API int dqn_phase_ms(dqn_handle *h, float *ms);
 
+/*
+ * dqn_test_stall -- a test hook for the device-side timeout path, not for
+ * production use.  When on != 0, every later dqn_run launches a test build of
+ * the target pass in which CTA 0 never copies its first weight stage: that
+ * CTA's MMA issuer waits on a stage that never fills, its bounded wait expires
+ * after about two seconds, every warp of the CTA leaves, waits (bounded) for
+ * its copies in flight and releases its tensor memory, and the run records
+ * ROLLOUT_ERR_TIMEOUT (read with dqn_status).  The rollout and state-row
+ * outputs (states, actions, dones, q) are complete; the rewards, td and
+ * next_states of CTA 0's rows are then undefined.  on == 0 restores the
+ * normal kernel.  Returns ROLLOUT_OK or ROLLOUT_ERR_INVALID (null handle).
+ */
+ROLLOUT_API int dqn_test_stall(dqn_handle *h, int on);
+
 /* dqn_status -- synchronise the last stream used; ROLLOUT_OK or the first
  * device-side error since the last call (the word is then cleared). */
 ROLLOUT_API int dqn_status(dqn_handle *h);

@@ -61,7 +61,7 @@ PER_EXPORTS = ["per_create", "per_insert", "per_sample", "per_update_priorities"
 
 
 DQN_EXPORTS = ["dqn_weight_count", "dqn_create", "dqn_set_weights", "dqn_run", "dqn_status", "dqn_destroy",
-               "dqn_set_timing", "dqn_phase_ms"]
+               "dqn_set_timing", "dqn_phase_ms", "dqn_test_stall"]
 DQN_OUTPUTS = ("states", "actions", "rewards", "dones", "q", "td", "next_states")
 
 
@@ -124,6 +124,8 @@ def lib(path: Optional[str] = None):
     L.dqn_set_timing.argtypes = [vp, C.c_int]
     L.dqn_phase_ms.restype = C.c_int
     L.dqn_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
+    L.dqn_test_stall.restype = C.c_int
+    L.dqn_test_stall.argtypes = [vp, C.c_int]
     L.dqn_destroy.restype = None
     L.dqn_destroy.argtypes = [vp]
     L.per_create.restype = C.c_int
@@ -548,6 +550,10 @@ class DqnCollector:
         ms = (C.c_float * 3)()
         _check(lib().dqn_phase_ms(self._h, ms))
         return [float(x) for x in ms]
+
+    def test_stall(self, on: bool = True) -> None:
+        """Test hook: later runs launch the target pass's stalling test build."""
+        _check(lib().dqn_test_stall(self._h, int(on)))
 
     def status(self) -> int:
         return lib().dqn_status(self._h)

@@ -426,6 +426,10 @@ constexpr int kTSmem = 1024 + 3 * kChunk + 4 * kChunk + kStages * kStage + (kBia
 static_assert(kTSmem <= 232448 - 2048, "target pass shared memory");
 constexpr uint32_t kTmemQ = 0, kTmemC1 = 256, kTmemC2 = 320;
 
+// kStall: a test build in which the first producer of CTA 0 issues no copy, so
+// that CTA's MMA issuer waits on a weight stage that never fills and the
+// bounded-wait exit runs (dqn_test_stall)
+template <bool kStall>
 __global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, DqnImage w)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -493,6 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, D
                 if (valid) {
                     b = (long long)start + t;
                     act = a.actions[i];
+                    // the one-hot row read below stays in bounds whatever the
+                    // rollout left here (its rows after a give-up are unwritten)
+                    if ((unsigned)act >= (unsigned)kActions) act = 0;
                     done = a.dones[i];
                     r0 = a.rewards[i];
                     qs = a.q[i];
@@ -610,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, D
         const int st = warp - kProdWarp0;
         if (lane == 0) {
             const long long my_tiles = n_tiles > blockIdx.x ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-            const long long total = my_tiles * kTargetUnits;
+            const long long total = (kStall && blockIdx.x == 0 && st == 0) ? 0 : my_tiles * kTargetUnits;
             long long last = -1;
             for (long long u = st; u < total; u += kStages) {
                 const int i = kNetUnits + (int)(u % kTargetUnits);
@@ -703,6 +710,7 @@ struct dqn_handle {
     cudaStream_t last_stream = nullptr;
     bool timing = false, timed_run = false;
     cudaEvent_t ev[4] = {};
+    bool test_stall = false;   // dqn_test_stall: launch the target pass's stalling test build
 };
 
 namespace rl {
@@ -941,7 +949,9 @@ int dqn_create(const float *weights, const rollout_dims *dims, dqn_handle **out)
         (e = cudaMemset(h->d_status, 0, sizeof(int))) != cudaSuccess ||
         (e = cudaFuncSetAttribute(dqn_rollout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem)) !=
             cudaSuccess ||
-        (e = cudaFuncSetAttribute(dqn_target_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem)) !=
+        (e = cudaFuncSetAttribute(dqn_target_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem)) !=
+            cudaSuccess ||
+        (e = cudaFuncSetAttribute(dqn_target_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem)) !=
             cudaSuccess) {
         free_handle(h);
         return cuda_fail(e, "DQN handle setup");
@@ -1004,7 +1014,8 @@ int dqn_run(dqn_handle *h, const float *features, const int32_t *starts, const u
                         next_states, h->d_status, env};
     const long long tiles = (long long)((NL + 127) / 128);
     const int grid = (int)(tiles < h->sms ? tiles : h->sms);
-    dqn_target_kernel<<<grid, kThreads, kTSmem, s>>>(ta, h->img);
+    if (h->test_stall) dqn_target_kernel<true><<<grid, kThreads, kTSmem, s>>>(ta, h->img);
+    else dqn_target_kernel<false><<<grid, kThreads, kTSmem, s>>>(ta, h->img);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "DQN target launch");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     h->timed_run = h->timing;
@@ -1021,6 +1032,14 @@ int dqn_set_timing(dqn_handle *h, int on)
             if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
         }
     h->timing = on != 0;
+    return ROLLOUT_OK;
+}
+
+int dqn_test_stall(dqn_handle *h, int on)
+{
+    clear_error();
+    if (!h) return set_error(ROLLOUT_ERR_INVALID, "null handle");
+    h->test_stall = on != 0;
     return ROLLOUT_OK;
 }
 
