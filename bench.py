@@ -365,6 +365,47 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed samples"], "window": window}
 
 
+def profile_run(kind: str, episodes: int, horizon: int) -> None:
+    """A fixed sequence of library calls for an ``ncu`` capture (no timing, no
+    JSON line): ``dqn`` creates the DQN collector for the reset-heavy workload
+    and runs it three times on ``episodes`` x ``horizon``; ``replay`` fills a
+    16,384,000-slot buffer of one-float states, gives every slot a priority in
+    250 updates of 65,536, then makes five draws of 512 each followed by its
+    priority update.  Ends with the handle's status check."""
+    import torch
+    from rl_experience_collection_gb300 import binding, build
+    build.build()
+    if kind == "dqn":
+        w = wl.DQN_WORKLOADS["dqn_reset_heavy_bf16"]
+        N, L = episodes or 2048, horizon or 200
+        inp = wl.generate(w, n_episodes=N, horizon=L)
+        h = binding.DqnCollector.for_workload(w, wl.dqn_weights(w.seed, 0.05))
+        out = binding.make_dqn_outputs(N, L, next_states=False)
+        args = (torch.from_numpy(inp.features).cuda(), torch.from_numpy(inp.starts).cuda(),
+                torch.from_numpy(inp.seeds.view(np.int32)).cuda(), N, L, w.gamma, wl.DQN_EPSILON, out)
+        for _ in range(3):
+            h.run(*args)
+        torch.cuda.synchronize()
+        st = h.status()
+    else:
+        C, D, U = 16_384_000, 1, 65_536
+        buf = binding.PerBuffer(C, D)
+        buf.insert(*wl.replay_rows_device(0, C, D))
+        g = torch.Generator(device="cuda").manual_seed(1)
+        perm = torch.randperm(C, device="cuda", generator=g).int()
+        for k in range(0, C, U):
+            buf.update(perm[k:k + U], torch.randn(U, device="cuda", generator=g))
+        batch = buf.make_batch(512)
+        for i in range(5):
+            buf.sample(512, 0.4, 17, i * 512, batch)
+            buf.update(batch["indices"], torch.randn(512, device="cuda", generator=g))
+        torch.cuda.synchronize()
+        st = buf.status()
+    if st != binding.ROLLOUT_OK:
+        raise SystemExit(f"device status {st}")
+    print("ok")
+
+
 def dist_setup(backend: str = "nccl"):
     """(rank, world size, torch.distributed or None) from the launcher's environment
     (RANK, WORLD_SIZE, MASTER_ADDR, MASTER_PORT); one process per GPU."""
@@ -437,7 +478,12 @@ def main():
     ap.add_argument("--no-replay", action="store_true", help="skip the prioritised-replay measurement")
     ap.add_argument("--replay-steps", type=int, default=200, help="timed replay sample + update calls")
     ap.add_argument("--no-dqn", action="store_true", help="skip the DQN-collector measurement")
+    ap.add_argument("--profile", choices=["dqn", "replay"],
+                    help="run a fixed call sequence for an ncu capture instead of the benchmark")
     args = ap.parse_args()
+    if args.profile:
+        profile_run(args.profile, args.episodes, args.horizon)
+        return
     args.warmup = max(args.warmup, 3)
     w = wl.WORKLOADS[args.workload]
     if args.episodes or args.horizon:
