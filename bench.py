@@ -489,7 +489,8 @@ def main():
     if args.episodes or args.horizon:
         w = dataclasses.replace(w, n_episodes=args.episodes or w.n_episodes, horizon=args.horizon or w.horizon)
 
-    rank, world, dist = dist_setup()
+    # the reference arm is host work on every rank: gloo, so that no rank touches a GPU
+    rank, world, dist = dist_setup("gloo" if args.impl == "reference" else "nccl")
     if args.impl == "reference":
         reference_arm(args, w, rank)
         if dist is not None:
