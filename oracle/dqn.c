@@ -6,7 +6,7 @@
  * network giving each transition its TD error.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
- * call this file; only the tests do.  It shares no code, header, table or
+ * call this file; only the tests and the smoke check do.  It shares no code, header, table or
  * constant with the CUDA path.
  *
  * Sources (page titles; sections named):

@@ -1,8 +1,8 @@
 """ctypes wrapper around the C oracle of DQN experience collection (``oracle/dqn.c``,
 which includes ``oracle/oracle.c`` for the shared environment).
 
-TEST INFRASTRUCTURE ONLY: the tests import this module; the product path never
-does.  Everything here is argument marshalling; the arithmetic is in the C files.
+TEST INFRASTRUCTURE ONLY: the tests and the smoke check import this module;
+the product path never does.  Everything here is argument marshalling; the arithmetic is in the C files.
 """
 from __future__ import annotations
 

@@ -1,7 +1,7 @@
 """Oracle of the GPU-resident prioritised experience replay buffer (include/per.h).
 
-TEST INFRASTRUCTURE ONLY: the tests import this module; the product path never
-does.  Plain numpy: double-precision running sums in slot order, one search per
+TEST INFRASTRUCTURE ONLY: the tests and the smoke check import this module;
+the product path never does.  Plain numpy: double-precision running sums in slot order, one search per
 sample, and updates applied as the batch-order writes they define.
 
 Follows page "GPU-Resident Prioritized Experience Replay":
