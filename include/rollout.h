@@ -199,6 +199,37 @@ ROLLOUT_API int rollout_phase_ms(rollout_handle *h, float *ms);
 ROLLOUT_API int rollout_test_stall(rollout_handle *h, int on);
 
 /*
+ * rollout_test_activations -- a test hook for checking the tensor-core paths
+ * layer by layer, not for production use.  (An addition of this library: the
+ * page "PPO CUDA Pipeline Design -- Zero-Roundtrip Experience Collection",
+ * section "Kernel Phases", Phase A steps 3, 5 and 9, defines the actor, critic
+ * and curiosity networks whose hidden layers it exposes.)
+ *
+ * When dump != NULL, every later run of this handle on the tensor-core path
+ * (ROLLOUT_TF32, ROLLOUT_BF16) launches test builds of the rollout and value
+ * kernels that also write, for episodes 0..n_episodes-1, every operand its
+ * layers consumed: the state input and each hidden activation (after bias,
+ * ReLU and rounding to the operand format: a bf16 or tf32 value, stored as
+ * float32).
+ * dump: DEVICE array, caller-owned, 16-byte aligned, of
+ *   n_episodes * (L + 1) rows of W floats, W = 64 + actor_h1 + actor_h2 +
+ *   (sum of the critic hidden widths) + cur_h (1664 for the standard critic,
+ *   3008 for the widened one).  Row n*(L+1) + t is step t of episode n:
+ *   [state input (64 columns, the first n_market + 3 written) | actor h1 |
+ *   actor h2 | critic hidden layers 1..critic_nh | curiosity hidden]; row
+ *   n*(L+1) + L is episode n's bootstrap critic (its state input and critic
+ *   columns only).  Columns a run does not produce are left as they were.
+ *   Episodes at or beyond the run's N are not written.  The array must stay
+ *   valid while runs that use it are in flight.
+ * dump == NULL restores the normal kernels (the timed kernels never write
+ * it).  The other outputs of a dumping run equal those of a normal run.
+ * Returns ROLLOUT_OK, or ROLLOUT_ERR_INVALID for a null handle, an
+ * ROLLOUT_FP32 handle (nothing is rounded), n_episodes <= 0 or a misaligned
+ * array.
+ */
+ROLLOUT_API int rollout_test_activations(rollout_handle *h, float *dump, int n_episodes);
+
+/*
  * rollout_run_static -- rollout_run for callers that cannot allocate device
  * memory.  (An addition of this library; the paper has no counterpart.)
  *

@@ -177,7 +177,8 @@ int dqn_episode(const float *w, const oracle_cfg *c, const float *features, long
 
         /* environment, curiosity, reward; xn = pre-reset next state */
         int done;
-        double rew = env_step(cw, c, features, b, x, a, gpu_d ? gpu_d[t] : -1, done_band, &es, st, xn, &done);
+        double rew = env_step(cw, c, features, b, x, a, gpu_d ? gpu_d[t] : -1, done_band, &es, st, xn, &done,
+                              NULL, NULL, NULL);
 
         /* target network on the next state, TD error */
         dqn_q(target, c, xn, qt);

@@ -44,6 +44,27 @@
  * computes: every weight matrix element and every layer input is rounded to
  * the operand format once, products and sums are exact (here: double), biases
  * and activations stay at full precision.  quant = 0 rounds nothing.
+ *
+ * Rounding replay (mode Q only).  A tensor-core path accumulates each hidden
+ * pre-activation z in float32 before rounding it to the operand format, so
+ * where the exact z lies within float32 accumulation error of a rounding
+ * boundary (the midpoint between two neighbouring bf16 / tf32 values, or 0
+ * for the ReLU) the path may round to the other neighbour.  That is a
+ * floating-point decision like an action drawn within rounding of a CDF
+ * boundary, and it is handled the same way: given the path's rounded hidden
+ * activations, the oracle adopts the path's value where it is the rounding
+ * of some point within the bound of the exact z (a replay), and counts any
+ * other difference as a mismatch (adopted as well, so that the rest can still
+ * be compared).  The bound for a K-term sum of products plus bias, whose
+ * magnitudes sum to S, is (K + 4) * 2^-23 * S: the standard error bound of
+ * recursive float32 summation (Higham, "Accuracy and Stability of Numerical
+ * Algorithms", section 4.2), charged a whole unit in the last place per
+ * operation so that accumulators that truncate are covered, with four
+ * operations to spare for bias and epilogue additions.  The state input is
+ * rounded the same way from the path's own float32 state, whose portfolio
+ * value may differ from the oracle's double one within the state tolerance
+ * (state_band, relative to max(|x|, 1)); its rounding is replayed within that
+ * band.
  */
 #include <math.h>
 #include <stdint.h>
@@ -82,6 +103,9 @@ typedef struct {
     long done_mismatches;
     double max_action_gap;   /* largest |u - cdf boundary| among action differences */
     double max_done_gap;     /* largest |V'-1 -+ theta| among done differences */
+    long hidden_replays;     /* hidden roundings adopted from the path under test (inside the bound) */
+    long hidden_mismatches;  /* hidden values of the path that no point within the bound rounds to */
+    double max_hidden_excess;/* largest distance of such a value from the allowed interval, in bounds */
 } oracle_stats;
 
 /* ------------------------------------------------------------------ */
@@ -159,6 +183,75 @@ void oracle_dense(const float *W, const float *b, int n_out, int n_in,
     }
 }
 
+/* The float32 accumulation bound of a K-term dot product plus bias whose
+ * terms' magnitudes sum to S (see "Rounding replay" above). */
+static double accum_bound(int K, double S) { return (double)(K + 4) * ldexp(S, -23); }
+
+/* oracle_dense followed by the operand rounding of the next layer's input
+ * (relu and quant as oracle_dense / q_operand).  gpu (may be NULL): the path
+ * under test's rounded outputs for the same layer; where they differ from the
+ * oracle's, they are adopted as described under "Rounding replay". */
+static void dense_round_replay(const float *W, const float *b, int n_out, int n_in, const double *in,
+                               double *out, int relu, int quant, const float *gpu, oracle_stats *st)
+{
+    for (int j = 0; j < n_out; ++j) {
+        double acc = 0.0, mag = fabs((double)b[j]);
+        for (int i = 0; i < n_in; ++i) {
+            double p = q_operand((double)W[(long)j * n_in + i], quant) * in[i];
+            acc += p;
+            mag += fabs(p);
+        }
+        acc += (double)b[j];
+        double own = q_operand((relu && acc < 0.0) ? 0.0 : acc, quant);
+        out[j] = own;
+        if (!gpu || (double)gpu[j] == own) continue;
+        double g = (double)gpu[j], d = accum_bound(n_in, mag);
+        double zl = acc - d, zh = acc + d;
+        if (relu) { zl = zl < 0.0 ? 0.0 : zl; zh = zh < 0.0 ? 0.0 : zh; }
+        double lo = q_operand(zl, quant), hi = q_operand(zh, quant);
+        if (g >= lo && g <= hi) {
+            st->hidden_replays++;
+        } else {
+            double ex = (g < lo ? lo - g : g - hi) / (d > 0.0 ? d : 1.0);
+            st->hidden_mismatches++;
+            if (ex > st->max_hidden_excess || !(ex == ex)) st->max_hidden_excess = ex;
+        }
+        out[j] = g;
+    }
+}
+
+/* The operand rounding of a state input x[0..n) into xq, given the path's
+ * rounded input gpu (may be NULL): a different value is adopted as a replay
+ * when it is the rounding of a point within band * max(|x_j|, 1) of x_j, and
+ * as a mismatch otherwise. */
+static void input_round_replay(const double *x, int n, int quant, const float *gpu, double band, double *xq,
+                               oracle_stats *st)
+{
+    for (int j = 0; j < n; ++j) {
+        double own = q_operand(x[j], quant);
+        xq[j] = own;
+        if (!gpu || (double)gpu[j] == own) continue;
+        double g = (double)gpu[j], d = band * fmax(fabs(x[j]), 1.0);
+        double lo = q_operand(x[j] - d, quant), hi = q_operand(x[j] + d, quant);
+        if (g >= lo && g <= hi) {
+            st->hidden_replays++;
+        } else {
+            double ex = (g < lo ? lo - g : g - hi) / (d > 0.0 ? d : 1.0);
+            st->hidden_mismatches++;
+            if (ex > st->max_hidden_excess || !(ex == ex)) st->max_hidden_excess = ex;
+        }
+        xq[j] = g;
+    }
+}
+
+/* dense_round_replay for the pins: one layer's rounded outputs `out`, given
+ * the path's rounded outputs `gpu` (may be NULL); counts in *st */
+void oracle_dense_round_replay(const float *W, const float *b, int n_out, int n_in, const double *in,
+                               double *out, int relu, int quant, const float *gpu, oracle_stats *st)
+{
+    dense_round_replay(W, b, n_out, n_in, in, out, relu, quant, gpu, st);
+}
+
 static void q_vector(const double *in, double *out, int n, int quant)
 {
     for (int i = 0; i < n; ++i) out[i] = q_operand(in[i], quant);
@@ -212,51 +305,101 @@ long oracle_weight_count(const oracle_cfg *c)
     return lo.q_b[1] + lo.q_out[1];
 }
 
-/* [P1] Phase A step 3: state[54] -> h1[128] ReLU -> h2[64] ReLU -> logits[45] */
-void oracle_actor(const float *w, const oracle_cfg *c, const double *x, double *logits)
+/* [P1] Phase A step 3: state[54] -> h1[128] ReLU -> h2[64] ReLU -> logits[45].
+ * gpu_h (may be NULL): the path's rounded h1 | h2, replayed (mode Q).
+ * used_h (may be NULL) receives the h1 | h2 the logits were computed from.
+ * xq (may be NULL): the already rounded state input. */
+static void actor_replay(const float *w, const oracle_cfg *c, const double *x, double *logits,
+                         const float *gpu_h, oracle_stats *st, float *used_h, const double *xq)
 {
+    long at = 0;
     layout lo;
     double in[ORACLE_MAX_W], out[ORACLE_MAX_W];
     make_layout(c, &lo);
-    q_vector(x, in, lo.a_in[0], c->quant);
+    if (xq) memcpy(in, xq, sizeof(double) * (size_t)lo.a_in[0]);
+    else q_vector(x, in, lo.a_in[0], c->quant);
     for (int l = 0; l < 3; ++l) {
-        int last = (l == 2);
-        oracle_dense(w + lo.a_w[l], w + lo.a_b[l], lo.a_out[l], lo.a_in[l], in,
-                     last ? logits : out, !last, c->quant);
-        if (!last) q_vector(out, in, lo.a_out[l], c->quant);
+        if (l == 2) {
+            oracle_dense(w + lo.a_w[l], w + lo.a_b[l], lo.a_out[l], lo.a_in[l], in, logits, 0, c->quant);
+        } else {
+            if (gpu_h && c->quant) {
+                dense_round_replay(w + lo.a_w[l], w + lo.a_b[l], lo.a_out[l], lo.a_in[l], in, out, 1, c->quant,
+                                   gpu_h + at, st);
+                memcpy(in, out, sizeof(double) * (size_t)lo.a_out[l]);
+            } else {
+                oracle_dense(w + lo.a_w[l], w + lo.a_b[l], lo.a_out[l], lo.a_in[l], in, out, 1, c->quant);
+                q_vector(out, in, lo.a_out[l], c->quant);
+            }
+            if (used_h) for (int j = 0; j < lo.a_out[l]; ++j) used_h[at + j] = (float)in[j];
+            at += lo.a_out[l];
+        }
     }
 }
 
-/* [P1] Phase A step 5: state[54] -> 512 -> 384 -> 256 -> 128 -> 64 (ReLU) -> 1 */
-double oracle_critic(const float *w, const oracle_cfg *c, const double *x)
+void oracle_actor(const float *w, const oracle_cfg *c, const double *x, double *logits)
+{
+    actor_replay(w, c, x, logits, NULL, NULL, NULL, NULL);
+}
+
+/* [P1] Phase A step 5: state[54] -> 512 -> 384 -> 256 -> 128 -> 64 (ReLU) -> 1.
+ * gpu_h (may be NULL): the path's rounded hidden layers, concatenated, replayed (mode Q).
+ * used_h (may be NULL) receives the hidden layers the value was computed from.
+ * xq (may be NULL): the already rounded state input. */
+static double critic_replay(const float *w, const oracle_cfg *c, const double *x, const float *gpu_h,
+                            oracle_stats *st, float *used_h, const double *xq)
 {
     layout lo;
     double in[ORACLE_MAX_W], out[ORACLE_MAX_W];
     make_layout(c, &lo);
-    q_vector(x, in, lo.c_in[0], c->quant);
+    if (xq) memcpy(in, xq, sizeof(double) * (size_t)lo.c_in[0]);
+    else q_vector(x, in, lo.c_in[0], c->quant);
+    long at = 0;
     for (int l = 0; l < lo.n_critic; ++l) {
         int last = (l == lo.n_critic - 1);
-        oracle_dense(w + lo.c_w[l], w + lo.c_b[l], lo.c_out[l], lo.c_in[l], in, out,
-                     !last, c->quant);
-        if (last) return out[0];
-        q_vector(out, in, lo.c_out[l], c->quant);
+        if (last) {
+            oracle_dense(w + lo.c_w[l], w + lo.c_b[l], lo.c_out[l], lo.c_in[l], in, out, 0, c->quant);
+            return out[0];
+        }
+        if (gpu_h && c->quant) {
+            dense_round_replay(w + lo.c_w[l], w + lo.c_b[l], lo.c_out[l], lo.c_in[l], in, out, 1, c->quant,
+                               gpu_h + at, st);
+            memcpy(in, out, sizeof(double) * (size_t)lo.c_out[l]);
+        } else {
+            oracle_dense(w + lo.c_w[l], w + lo.c_b[l], lo.c_out[l], lo.c_in[l], in, out, 1, c->quant);
+            q_vector(out, in, lo.c_out[l], c->quant);
+        }
+        if (used_h) for (int j = 0; j < lo.c_out[l]; ++j) used_h[at + j] = (float)in[j];
+        at += lo.c_out[l];
     }
     return 0.0;
+}
+
+double oracle_critic(const float *w, const oracle_cfg *c, const double *x)
+{
+    return critic_replay(w, c, x, NULL, NULL, NULL, NULL);
 }
 
 /* [P1] Phase A step 9 / [P2] "Curiosity Forward Model": forward-dynamics
  * prediction from [state ; one-hot(action)] -> cur_h ReLU -> next state.
  * cw points at the curiosity block [C1 (cur_h x (sd + n_actions)), c1,
  * C2 (sd x cur_h), c2]. */
-static void curiosity_block(const float *cw, const oracle_cfg *c, const double *x, int a, double *pred)
+static void curiosity_block(const float *cw, const oracle_cfg *c, const double *x, int a, double *pred,
+                            const float *gpu_z, oracle_stats *st, float *used_z, const double *xq)
 {
     double in[ORACLE_MAX_W], hid[ORACLE_MAX_W];
     const int sd = c->n_market + 3, nin = sd + c->n_actions, h = c->cur_h;
     const float *C1 = cw, *c1 = C1 + (long)h * nin, *C2 = c1 + h, *c2 = C2 + (long)sd * h;
-    q_vector(x, in, sd, c->quant);
+    if (xq) memcpy(in, xq, sizeof(double) * (size_t)sd);
+    else q_vector(x, in, sd, c->quant);
     for (int i = 0; i < c->n_actions; ++i) in[sd + i] = (i == a) ? 1.0 : 0.0;
-    oracle_dense(C1, c1, h, nin, in, hid, 1, c->quant);
-    q_vector(hid, in, h, c->quant);
+    if (gpu_z && c->quant) {
+        dense_round_replay(C1, c1, h, nin, in, hid, 1, c->quant, gpu_z, st);
+        memcpy(in, hid, sizeof(double) * (size_t)h);
+    } else {
+        oracle_dense(C1, c1, h, nin, in, hid, 1, c->quant);
+        q_vector(hid, in, h, c->quant);
+    }
+    if (used_z) for (int j = 0; j < h; ++j) used_z[j] = (float)in[j];
     oracle_dense(C2, c2, sd, h, in, pred, 0, c->quant);
 }
 
@@ -264,7 +407,18 @@ void oracle_curiosity(const float *w, const oracle_cfg *c, const double *x, int 
 {
     layout lo;
     make_layout(c, &lo);
-    curiosity_block(w + lo.q_w[0], c, x, a, pred);
+    curiosity_block(w + lo.q_w[0], c, x, a, pred, NULL, NULL, NULL, NULL);
+}
+
+/* Columns of one row of the path's rounded operands (see oracle_episode):
+ * state input (ORACLE_IN_COLS, the first n_market + 3 used) | actor h1 |
+ * actor h2 | critic hidden layers | curiosity hidden. */
+#define ORACLE_IN_COLS 64
+long oracle_hidden_width(const oracle_cfg *c)
+{
+    long wd = ORACLE_IN_COLS + c->actor_h1 + c->actor_h2 + c->cur_h;
+    for (int l = 0; l < c->critic_nh; ++l) wd += c->critic_h[l];
+    return wd;
 }
 
 /* [P1] Phase A step 4: stable softmax, CDF summed in index order, inverse-CDF
@@ -369,11 +523,13 @@ static void env_reset(env_state *s) { s->V = 1.0; s->e = 0.0; s->k = 0; s->nwin 
 /* Portfolio, triple barrier, diversity, curiosity and reward for action a at
  * bar b, from state x (= [F[b], V, e, spread]).  Fills xn with the pre-reset
  * next state [F[b+1], V', e', spread].  gpu_done (or -1): the done decision of
- * the path under test, adopted as in oracle_episode.  Sets *done; the state's
+ * the path under test, adopted as in oracle_episode; gpu_z (or NULL): its
+ * rounded curiosity hidden layer, replayed; used_z (or NULL) receives the
+ * curiosity hidden layer used; xq (or NULL): the rounded state input.  Sets *done; the state's
  * V, e, k and window advance, and are reset when *done. */
 static double env_step(const float *cw, const oracle_cfg *c, const float *features, long b, const double *x,
                        int a, int gpu_done, double done_band, env_state *es, oracle_stats *st, double *xn,
-                       int *done_out)
+                       int *done_out, const float *gpu_z, float *used_z, const double *xq)
 {
     const int nm = c->n_market, sd = nm + 3;
     double pred[ORACLE_MAX_W];
@@ -415,7 +571,7 @@ static double env_step(const float *cw, const oracle_cfg *c, const float *featur
     /* step 9: curiosity against the pre-reset next state */
     for (int j = 0; j < nm; ++j) xn[j] = (double)features[(b + 1) * nm + j];
     xn[nm] = V2; xn[nm + 1] = e2; xn[nm + 2] = c->spread;
-    curiosity_block(cw, c, x, a, pred);
+    curiosity_block(cw, c, x, a, pred, gpu_z, st, used_z, xq);
     double mse = 0.0;
     for (int j = 0; j < sd; ++j) mse += (pred[j] - xn[j]) * (pred[j] - xn[j]);
     mse /= (double)sd;
@@ -446,16 +602,28 @@ static double env_step(const float *cw, const oracle_cfg *c, const float *featur
  *   < done_band), the oracle adopts it and counts a replay.  A difference
  *   outside the band is counted as a mismatch and also adopted, so that the
  *   rest of the episode can still be compared.
+ * gpu_h ((L + 1) rows of oracle_hidden_width(c) floats, or NULL): the path
+ *   under test's rounded operands, row t for step t (state input | actor h1 |
+ *   h2 | critic hidden layers | curiosity hidden) and row L for the bootstrap
+ *   critic (its state input and critic columns only); under mode Q they are
+ *   replayed as described under "Rounding replay", the state input within
+ *   state_band.
+ * o_h ((L + 1) rows in gpu_h's layout, or NULL) receives the hidden
+ *   activations the oracle used (after any replay).
  * Outputs (each of length L, or L*state_dim for states) may be NULL.
  * Returns 0, or -1 on an invalid argument.
  */
 int oracle_episode(const float *w, const oracle_cfg *c, const float *features, long n_bars,
                    int start, uint32_t seed, int L, double gamma, double lambda,
                    const int32_t *gpu_a, const int32_t *gpu_d, double act_band, double done_band,
+                   const float *gpu_h, double state_band, float *o_h,
                    float *o_states, int32_t *o_a, float *o_logp, float *o_v, float *o_r,
                    int32_t *o_d, float *o_adv, float *o_ret, double *o_vboot, oracle_stats *st)
 {
     const int nm = c->n_market, sd = nm + 3, na = c->n_actions;
+    const long hw = oracle_hidden_width(c), h_act = ORACLE_IN_COLS, h_crit = h_act + c->actor_h1 + c->actor_h2,
+               h_cur = hw - c->cur_h;
+    double xq[ORACLE_MAX_W];
     if (L <= 0 || start < 0 || (long)start + L > n_bars - 1 || na > ORACLE_MAX_W ||
         c->div_window > ORACLE_MAX_WIN || c->div_window <= 0)
         return -1;
@@ -475,8 +643,19 @@ int oracle_episode(const float *w, const oracle_cfg *c, const float *features, l
         for (int j = 0; j < nm; ++j) x[j] = (double)features[b * nm + j];
         x[nm] = es.V; x[nm + 1] = es.e; x[nm + 2] = c->spread;
 
+        const float *gh = (gpu_h && c->quant) ? gpu_h + (long)t * hw : NULL;
+        float *oh = o_h ? o_h + (long)t * hw : NULL;
+        const double *xqp = NULL;
+        if (gh) {
+            input_round_replay(x, sd, c->quant, gh, state_band, xq, st);
+            xqp = xq;
+        } else if (oh) {
+            q_vector(x, xq, sd, c->quant);
+        }
+        if (oh) for (int j = 0; j < sd; ++j) oh[j] = (float)xq[j];
+
         /* steps 3-4: actor, softmax, CDF draw */
-        oracle_actor(w, c, x, logits);
+        actor_replay(w, c, x, logits, gh ? gh + h_act : NULL, st, oh ? oh + h_act : NULL, xqp);
         double u = oracle_lcg_uniform(&s);
         double logp;
         int a = oracle_sample(logits, na, u, &logp, cdf);
@@ -495,12 +674,12 @@ int oracle_episode(const float *w, const oracle_cfg *c, const float *features, l
         }
 
         /* step 5: critic */
-        double val = oracle_critic(w, c, x);
+        double val = critic_replay(w, c, x, gh ? gh + h_crit : NULL, st, oh ? oh + h_crit : NULL, xqp);
 
         /* steps 6-10 and 12 */
         int done;
         double rew = env_step(w + lo.q_w[0], c, features, b, x, a, gpu_d ? gpu_d[t] : -1, done_band, &es, st,
-                              xn, &done);
+                              xn, &done, gh ? gh + h_cur : NULL, oh ? oh + h_cur : NULL, xqp);
 
         /* step 11: store */
         if (o_states) for (int j = 0; j < sd; ++j) o_states[(long)t * sd + j] = (float)x[j];
@@ -513,7 +692,17 @@ int oracle_episode(const float *w, const oracle_cfg *c, const float *features, l
     }
 
     /* bootstrap: critic of the final pre-reset next state */
-    double vboot = oracle_critic(w, c, xn);
+    const float *gb = (gpu_h && c->quant) ? gpu_h + (long)L * hw : NULL;
+    float *ob = o_h ? o_h + (long)L * hw : NULL;
+    const double *xbp = NULL;
+    if (gb) {
+        input_round_replay(xn, sd, c->quant, gb, state_band, xq, st);
+        xbp = xq;
+    } else if (ob) {
+        q_vector(xn, xq, sd, c->quant);
+    }
+    if (ob) for (int j = 0; j < sd; ++j) ob[j] = (float)xq[j];
+    double vboot = critic_replay(w, c, xn, gb ? gb + h_crit : NULL, st, ob ? ob + h_crit : NULL, xbp);
     if (o_vboot) *o_vboot = vboot;
 
     double *adv = malloc(sizeof(double) * (size_t)L), *ret = malloc(sizeof(double) * (size_t)L);
@@ -529,22 +718,29 @@ int oracle_episode(const float *w, const oracle_cfg *c, const float *features, l
 /*
  * Runs episodes idx[0..n_sel-1] of a batch.  Per-episode outputs are written
  * at row i of the [n_sel, L(, state_dim)] output arrays.  gpu_a / gpu_d, when
- * given, are the path-under-test's full [N, L] arrays.
+ * given, are the path-under-test's full [N, L] arrays; gpu_h (or NULL) holds
+ * its hidden activations of episodes 0..n_h-1, (L + 1) rows each (see
+ * oracle_episode), replayed for those episodes; o_h (or NULL) receives the
+ * oracle's, (L + 1) rows per selected episode.
  */
 int oracle_rollout(const float *w, const oracle_cfg *c, const float *features, long n_bars,
                    const int32_t *starts, const uint32_t *seeds, const int32_t *idx, int n_sel,
                    int L, double gamma, double lambda,
                    const int32_t *gpu_a, const int32_t *gpu_d, double act_band, double done_band,
+                   const float *gpu_h, int n_h, double state_band, float *o_h,
                    float *o_states, int32_t *o_a, float *o_logp, float *o_v, float *o_r,
                    int32_t *o_d, float *o_adv, float *o_ret, double *o_vboot, oracle_stats *st)
 {
     const int sd = c->n_market + 3;
+    const long hw = oracle_hidden_width(c);
     for (int i = 0; i < n_sel; ++i) {
         long n = idx[i];
         long row = (long)i * L;
         int rc = oracle_episode(w, c, features, n_bars, starts[n], seeds[n], L, gamma, lambda,
                                 gpu_a ? gpu_a + n * L : NULL, gpu_d ? gpu_d + n * L : NULL,
                                 act_band, done_band,
+                                (gpu_h && n < n_h) ? gpu_h + n * (long)(L + 1) * hw : NULL, state_band,
+                                o_h ? o_h + (long)i * (L + 1) * hw : NULL,
                                 o_states ? o_states + row * sd : NULL,
                                 o_a ? o_a + row : NULL, o_logp ? o_logp + row : NULL,
                                 o_v ? o_v + row : NULL, o_r ? o_r + row : NULL,

@@ -41,6 +41,7 @@ class OracleStats(C.Structure):
         ("action_replays", C.c_long), ("done_replays", C.c_long),
         ("action_mismatches", C.c_long), ("done_mismatches", C.c_long),
         ("max_action_gap", C.c_double), ("max_done_gap", C.c_double),
+        ("hidden_replays", C.c_long), ("hidden_mismatches", C.c_long), ("max_hidden_excess", C.c_double),
     ]
 
     def as_dict(self) -> Dict[str, float]:
@@ -101,8 +102,13 @@ def lib():
         L.oracle_episode.restype = C.c_int
         L.oracle_rollout.restype = C.c_int
         L.oracle_rollout.argtypes = [p, C.POINTER(OracleCfg), p, C.c_long, p, p, p, C.c_int, C.c_int,
-                                     C.c_double, C.c_double, p, p, C.c_double, C.c_double,
-                                     p, p, p, p, p, p, p, p, p, C.POINTER(OracleStats)]
+                                     C.c_double, C.c_double, p, p, C.c_double, C.c_double, p, C.c_int,
+                                     C.c_double, p, p, p, p, p, p, p, p, p, p, C.POINTER(OracleStats)]
+        L.oracle_dense_round_replay.restype = None
+        L.oracle_dense_round_replay.argtypes = [p, p, C.c_int, C.c_int, p, p, C.c_int, C.c_int, p,
+                                                C.POINTER(OracleStats)]
+        L.oracle_hidden_width.restype = C.c_long
+        L.oracle_hidden_width.argtypes = [C.POINTER(OracleCfg)]
         _lib = L
     return _lib
 
@@ -130,6 +136,28 @@ def make_cfg(w, quant: Optional[str] = None) -> OracleCfg:
 
 
 # ---------------------------------------------------------------- small calls
+
+def dense_round_replay(W: np.ndarray, b: np.ndarray, x: np.ndarray, relu: bool, quant: int,
+                       gpu: Optional[np.ndarray] = None):
+    """One layer's rounded outputs under mode Q, replaying the path's rounded
+    outputs ``gpu`` where allowed; returns (outputs, stats dict)."""
+    W = np.ascontiguousarray(W, np.float32)
+    b = np.ascontiguousarray(b, np.float32)
+    x = np.ascontiguousarray(x, np.float64)
+    g = None if gpu is None else np.ascontiguousarray(gpu, np.float32)
+    out = np.zeros(W.shape[0], np.float64)
+    st = OracleStats()
+    lib().oracle_dense_round_replay(_ptr(W), _ptr(b), W.shape[0], W.shape[1], _ptr(x), _ptr(out), int(relu),
+                                    quant, _ptr(g), C.byref(st))
+    return out, st.as_dict()
+
+
+def hidden_width(w) -> int:
+    """Floats per row of a path's rounded operands (state input, 64 columns of
+    which the first 54 are used | actor h1 | h2 | critic hidden layers |
+    curiosity hidden)."""
+    return int(lib().oracle_hidden_width(C.byref(make_cfg(w))))
+
 
 def lcg_step(s: int) -> int:
     return lib().oracle_lcg_step(s)
@@ -218,9 +246,20 @@ def gae(r, v, d, v_boot: float, gamma: float, lam: float):
 def rollout(w, inputs, idx: Sequence[int], quant: Optional[str] = None, horizon: Optional[int] = None,
             gpu_actions: Optional[np.ndarray] = None, gpu_dones: Optional[np.ndarray] = None,
             act_band: float = 1e-5, done_band: float = 1e-6, threads: int = 1,
-            gamma: Optional[float] = None, lam: Optional[float] = None):
+            gamma: Optional[float] = None, lam: Optional[float] = None,
+            gpu_hidden: Optional[np.ndarray] = None, return_hidden: bool = False, state_band: float = 2e-6):
     """Oracle outputs for episodes ``idx`` of a batch.
 
+    ``gpu_hidden`` (optional, float32 ``[n_h, L + 1, hidden_width(w)]``): the
+    path under test's rounded operands of episodes ``0..n_h-1`` (row t per
+    step, row L the bootstrap critic: state input, actor h1, h2, critic
+    hidden layers, curiosity hidden), replayed under mode Q where they differ
+    from the oracle's own rounding within the float32 accumulation bound (the
+    state input within ``state_band`` relative to max(|x|, 1)); counted in
+    ``stats``: ``hidden_replays``, and ``hidden_mismatches`` for any other
+    difference.  ``return_hidden``:
+    also return the hidden activations the oracle used, as ``hidden``
+    ([len(idx), L + 1, hidden_width(w)]).
     Returns a dict of arrays with a leading axis ``len(idx)`` plus ``stats``.
     ``threads > 1`` runs disjoint episode subsets on Python threads (the C
     call releases the GIL); the arithmetic is unchanged.
@@ -239,10 +278,16 @@ def rollout(w, inputs, idx: Sequence[int], quant: Optional[str] = None, horizon:
         "adv": np.zeros((n, L), np.float32), "ret": np.zeros((n, L), np.float32),
         "vboot": np.zeros(n, np.float64),
     }
+    if return_hidden:
+        out["hidden"] = np.zeros((n, L + 1, hidden_width(w)), np.float32)
     feats = np.ascontiguousarray(inputs.features, np.float32)
     starts = np.ascontiguousarray(inputs.starts, np.int32)
     seeds = np.ascontiguousarray(inputs.seeds, np.uint32)
     weights = np.ascontiguousarray(inputs.weights, np.float32)
+    gh = None if gpu_hidden is None else np.ascontiguousarray(gpu_hidden, np.float32)
+    n_h = 0 if gh is None else gh.shape[0]
+    if gh is not None and gh.shape[1:] != (L + 1, hidden_width(w)):
+        raise ValueError(f"gpu_hidden has shape {gh.shape}, want [n, {L + 1}, {hidden_width(w)}]")
     ga = None if gpu_actions is None else np.ascontiguousarray(gpu_actions, np.int32)
     gd = None if gpu_dones is None else np.ascontiguousarray(gpu_dones, np.int32)
     L_ = lib()
@@ -252,7 +297,8 @@ def rollout(w, inputs, idx: Sequence[int], quant: Optional[str] = None, horizon:
         sub = idx[lo:hi]
         rc = L_.oracle_rollout(
             _ptr(weights), C.byref(cfg), _ptr(feats), feats.shape[0], _ptr(starts), _ptr(seeds),
-            _ptr(sub), sub.size, L, g, lm, _ptr(ga), _ptr(gd), act_band, done_band,
+            _ptr(sub), sub.size, L, g, lm, _ptr(ga), _ptr(gd), act_band, done_band, _ptr(gh), n_h, state_band,
+            _ptr(out["hidden"][lo:hi]) if return_hidden else None,
             _ptr(out["states"][lo:hi]), _ptr(out["actions"][lo:hi]), _ptr(out["logp"][lo:hi]),
             _ptr(out["values"][lo:hi]), _ptr(out["rewards"][lo:hi]), _ptr(out["dones"][lo:hi]),
             _ptr(out["adv"][lo:hi]), _ptr(out["ret"][lo:hi]), _ptr(out["vboot"][lo:hi]), C.byref(st))

@@ -26,7 +26,7 @@ DTYPE = {"fp32": 0, "tf32": 1, "bf16": 2}
 
 EXPORTS = ["rollout_create", "rollout_set_weights", "rollout_run", "rollout_status", "rollout_destroy",
            "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static", "rollout_run_host",
-           "rollout_set_weights_device", "rollout_test_stall"]
+           "rollout_set_weights_device", "rollout_test_stall", "rollout_test_activations"]
 
 
 class RolloutDims(C.Structure):
@@ -108,6 +108,8 @@ def lib(path: Optional[str] = None):
     L.rollout_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
     L.rollout_test_stall.restype = C.c_int
     L.rollout_test_stall.argtypes = [vp, C.c_int]
+    L.rollout_test_activations.restype = C.c_int
+    L.rollout_test_activations.argtypes = [vp, vp, C.c_int]
     L.rollout_last_error.restype = C.c_char_p
     L.rollout_last_error.argtypes = []
     L.dqn_weight_count.restype = C.c_longlong
@@ -306,6 +308,14 @@ class Rollout:
         """Test hook: later runs launch the value kernel's stalling test build."""
         _check(lib().rollout_test_stall(self._h, int(on)))
 
+    def test_activations(self, dump=None, n_episodes: int = 0) -> None:
+        """Test hook: later runs also write the rounded hidden activations of
+        episodes 0..n_episodes-1 into the device tensor ``dump``
+        ([n_episodes, L + 1, activation_width] float32); None turns it off."""
+        ptr = None if dump is None else dump.data_ptr()
+        self._dump = dump                        # keeps the array alive while runs may use it
+        _check(lib().rollout_test_activations(self._h, ptr, int(n_episodes) if dump is not None else 0))
+
     def status(self) -> int:
         return lib().rollout_status(self._h)
 
@@ -405,9 +415,21 @@ class PpoTrainer:
             pass
 
 
+DUMP_IN_COLS = 64
+
+
+def activation_width(critic_h) -> int:
+    """Floats per row of rollout_test_activations' array: state input (64
+    columns, the first 54 used) | actor h1 | h2 | critic hidden layers |
+    curiosity hidden."""
+    return DUMP_IN_COLS + wl.ACTOR_H[0] + wl.ACTOR_H[1] + int(sum(critic_h)) + wl.CUR_H
+
+
 def collect(w: wl.Workload, inputs: "wl.Inputs", N: Optional[int] = None, L: Optional[int] = None,
-            device="cuda", handle: Optional[Rollout] = None) -> Dict[str, "torch.Tensor"]:
-    """One-call convenience: uploads inputs, runs one collection, returns device outputs."""
+            device="cuda", handle: Optional[Rollout] = None, dump_episodes: int = 0) -> Dict[str, "torch.Tensor"]:
+    """One-call convenience: uploads inputs, runs one collection, returns device outputs.
+    dump_episodes > 0 (tf32 / bf16 only) also returns, under "hidden", the rounded
+    hidden activations of episodes 0..dump_episodes-1 (rollout_test_activations)."""
     import torch
     N = w.n_episodes if N is None else N
     L = w.horizon if L is None else L
@@ -416,8 +438,16 @@ def collect(w: wl.Workload, inputs: "wl.Inputs", N: Optional[int] = None, L: Opt
     starts = torch.from_numpy(inputs.starts[:N]).to(device)
     seeds = torch.from_numpy(inputs.seeds[:N].view("int32")).to(device)
     out = make_outputs(N, L, device)
+    dump = None
+    if dump_episodes > 0:
+        k = min(dump_episodes, N)
+        dump = torch.full((k, L + 1, activation_width(w.critic_h)), float("nan"), dtype=torch.float32, device=device)
+        h.test_activations(dump, k)
     h.run(feats, starts, seeds, N, L, w.gamma, w.lam, out)
     st = h.status()
+    if dump is not None:
+        h.test_activations(None)
+        out["hidden"] = dump
     if st != ROLLOUT_OK:
         raise RolloutError(st, "device-side status")
     if handle is None:

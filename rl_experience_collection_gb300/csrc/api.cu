@@ -73,6 +73,9 @@ struct rollout_handle {
     bool timing = false, timed_run = false;
     // rollout_test_stall: runs launch the value kernel's stalling test build
     bool test_stall = false;
+    // rollout_test_activations: runs launch the kernels' dump builds
+    float *dump = nullptr;
+    int dump_episodes = 0;
     cudaEvent_t ev[kTimedKernels + 1] = {};
     // rollout_run_host: device copies of the inputs and outputs (one allocation,
     // grown on demand), the copy streams and their events
@@ -607,6 +610,20 @@ int enqueue_run(rollout_handle *h, const RunBuffers &b, int N, int L, float gamm
     ValueArgs va{b.features, b.starts, N, L, d.n_bars, b.actions, b.dones, b.values,
                  b.adv, b.rewards, b.ret, h->d_status, env};
     GaeArgs ga{b.rewards, b.values, b.dones, b.adv, b.ret, N, L, gamma, lambda};
+    if (h->dump && d.dtype != ROLLOUT_FP32) {
+        ActDump ad;
+        ad.p = h->dump;
+        ad.n_ep = h->dump_episodes;
+        int col = kDumpIn + kActorH1 + kActorH2;
+        for (int l = 0; l < kCriticLayers - 1; ++l) {
+            ad.crit_off[l] = col;
+            col += d.critic_h[l];
+        }
+        ad.cur_off = col;
+        ad.width = col + d.cur_h;
+        p1.dump = ad;
+        va.dump = ad;
+    }
 
     auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
     auto point = [&](int p) { return points ? cudaEventRecord(points[p], s) : cudaSuccess; };
@@ -870,6 +887,18 @@ int rollout_test_stall(rollout_handle *h, int on)
     if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
     if (h->dims.dtype == ROLLOUT_FP32) return fail(ROLLOUT_ERR_INVALID, "the fp32 path has no bounded waits to stall");
     h->test_stall = on != 0;
+    return ROLLOUT_OK;
+}
+
+int rollout_test_activations(rollout_handle *h, float *dump, int n_episodes)
+{
+    g_err[0] = 0;
+    if (!h) return fail(ROLLOUT_ERR_INVALID, "null handle");
+    if (h->dims.dtype == ROLLOUT_FP32) return fail(ROLLOUT_ERR_INVALID, "the fp32 path rounds no activations");
+    if (dump && (n_episodes <= 0 || ((uintptr_t)dump & 15u)))
+        return fail(ROLLOUT_ERR_INVALID, "the dump needs n_episodes > 0 and a 16-byte aligned array");
+    h->dump = dump;
+    h->dump_episodes = dump ? n_episodes : 0;
     return ROLLOUT_OK;
 }
 

@@ -49,6 +49,29 @@ constexpr int kActorH2 = 64;
 constexpr int kCurH = 64;
 constexpr int kCriticLayers = 6;   // 5 hidden + scalar head
 
+// Test hook (rollout_test_activations): the rounded operands that the
+// tensor-core kernels feed to their layers, for the first n_ep episodes.
+// Row n*(L+1)+t holds step t of episode n, row n*(L+1)+L the bootstrap critic
+// of episode n; a row is `width` floats: state input (kDumpIn columns, the
+// first kState used) | actor h1 (from act_off) | actor h2 | critic hidden
+// layers (crit_off[l] is layer l's first column) | curiosity hidden (from
+// cur_off).  p == nullptr: nothing is written (the normal builds of the
+// kernels never write it).
+constexpr int kDumpIn = 64;
+struct ActDump {
+    float *p = nullptr;
+    int n_ep = 0;
+    int width = 0;
+    int act_off = kDumpIn;
+    int crit_off[5] = {};
+    int cur_off = 0;
+    // row of step t of episode n (t == L: its bootstrap row), or nullptr
+    __device__ __forceinline__ float *row(long long n, int t, int L) const
+    {
+        return (p && n >= 0 && n < n_ep) ? p + ((long long)n * (L + 1) + t) * width : nullptr;
+    }
+};
+
 // device status word values (first error wins)
 constexpr int kStatusOk = 0;
 
@@ -65,6 +88,7 @@ struct Phase1Args {
     float *v_post;             // [N, L]: V' after the trade (out_adv)
     int *status;
     EnvConst env;
+    ActDump dump;              // test hook, see ActDump
 };
 
 struct ValueArgs {
@@ -79,6 +103,7 @@ struct ValueArgs {
     float *boot;               // out_ret: [n*L + L-1] receives the bootstrap value
     int *status;
     EnvConst env;
+    ActDump dump;              // test hook, see ActDump
 };
 
 // the stored state rows (states.cu), written between the rollout and the value phase

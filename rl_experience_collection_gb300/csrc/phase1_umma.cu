@@ -60,10 +60,24 @@ static_assert(P1Geo<true>::FR_OFF % 1024 == 0 && P1Geo<true>::FR_GROUP % 128 == 
                   P1Geo<true>::FR_GROUP >= 4 * kFPad * 4 && P1Geo<true>::SMEM <= 232448,
               "row ring: 128-byte aligned gather destinations, fits in shared memory");
 
+// the operand values of a packed bf16 unit (8 values) or tf32 unit (4) at dst
+__device__ __forceinline__ void dump_unit_bf16(float *dst, uint4 p)
+{
+    const float2 a = unpack_bf16x2(p.x), b = unpack_bf16x2(p.y), c = unpack_bf16x2(p.z), d = unpack_bf16x2(p.w);
+    reinterpret_cast<float4 *>(dst)[0] = make_float4(a.x, a.y, b.x, b.y);
+    reinterpret_cast<float4 *>(dst)[1] = make_float4(c.x, c.y, d.x, d.y);
+}
+__device__ __forceinline__ void dump_unit_tf32(float *dst, uint4 p)
+{
+    *reinterpret_cast<float4 *>(dst) =
+        make_float4(__uint_as_float(p.x), __uint_as_float(p.y), __uint_as_float(p.z), __uint_as_float(p.w));
+}
+
 // write values v[0..n) (n multiple of 8 for bf16, 4 for tf32) as row `r` of a
-// K-major swizzled operand starting at column c0 (c0 a multiple of 8 / 4)
-template <bool BF16, int N>
-__device__ __forceinline__ void put_row(uint8_t *op, int r, int c0, const float (&v)[N])
+// K-major swizzled operand starting at column c0 (c0 a multiple of 8 / 4);
+// D: also the rounded values to dst[0..n) when dst is not null (test hook)
+template <bool BF16, int N, bool D = false>
+__device__ __forceinline__ void put_row(uint8_t *op, int r, int c0, const float (&v)[N], float *dst = nullptr)
 {
     constexpr int KC = P1Geo<BF16>::KC;
     if constexpr (BF16) {
@@ -77,6 +91,9 @@ __device__ __forceinline__ void put_row(uint8_t *op, int r, int c0, const float 
             p.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
             uint8_t *tile = op + (c / KC) * (128 * 128);
             *reinterpret_cast<uint4 *>(tile + sw128_offset(r, (c % KC) / 8)) = p;
+            if constexpr (D) {
+                if (dst) dump_unit_bf16(dst + 8 * q, p);
+            }
         }
     } else {
 #pragma unroll
@@ -89,6 +106,9 @@ __device__ __forceinline__ void put_row(uint8_t *op, int r, int c0, const float 
             p.w = to_tf32(v[4 * q + 3]);
             uint8_t *tile = op + (c / KC) * (128 * 128);
             *reinterpret_cast<uint4 *>(tile + sw128_offset(r, (c % KC) / 4)) = p;
+            if constexpr (D) {
+                if (dst) dump_unit_tf32(dst + 4 * q, p);
+            }
         }
     }
 }
@@ -109,8 +129,10 @@ __device__ __forceinline__ void issue_layer(uint32_t d, uint32_t a_base, uint32_
 }
 
 // relu(D[col0 .. col0+32*G) + bias) of this thread's lane, into operand `op`
-template <bool BF16, int G>
-__device__ __forceinline__ void epi_hidden(uint32_t taddr, const float *bias, uint8_t *op, int r)
+// (D: and to dst[0 .. 32*G) when dst is not null)
+template <bool BF16, int G, bool D = false>
+__device__ __forceinline__ void epi_hidden(uint32_t taddr, const float *bias, uint8_t *op, int r,
+                                           float *dst = nullptr)
 {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -119,11 +141,12 @@ __device__ __forceinline__ void epi_hidden(uint32_t taddr, const float *bias, ui
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i] + bias[32 * g + i], 0.f);
-        put_row<BF16, 32>(op, r, 32 * g, v);
+        put_row<BF16, 32, D>(op, r, 32 * g, v, dst ? dst + 32 * g : nullptr);
     }
 }
 
-template <bool BF16>
+// kDump: the test build that also writes the rounded hidden activations (ActDump)
+template <bool BF16, bool kDump>
 __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a, UmmaWeights w,
                                                                     const __grid_constant__ CUtensorMap fmap)
 {
@@ -283,7 +306,9 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
         ok = ok && mbar_wait(&bar_mma, ph, abort);
         ph ^= 1;
         tc_fence_after();
-        epi_hidden<BF16, kActorH1 / 32>(lane_addr + 0, bias, H1, tid);
+        float *drow = nullptr;
+        if constexpr (kDump) drow = live ? a.dump.row(n, t, L) : nullptr;
+        epi_hidden<BF16, kActorH1 / 32, kDump>(lane_addr + 0, bias, H1, tid, drow ? drow + a.dump.act_off : nullptr);
 
         fence_async_smem();
         tc_fence_before();
@@ -296,7 +321,8 @@ __global__ void __launch_bounds__(kP1Threads, 1) phase1_umma_kernel(Phase1Args a
         ok = ok && mbar_wait(&bar_mma, ph, abort);
         ph ^= 1;
         tc_fence_after();
-        epi_hidden<BF16, kActorH2 / 32>(lane_addr + 128, bias + kActorH1, H2, tid);
+        epi_hidden<BF16, kActorH2 / 32, kDump>(lane_addr + 128, bias + kActorH1, H2, tid,
+                                                drow ? drow + a.dump.act_off + kActorH1 : nullptr);
 
         fence_async_smem();
         tc_fence_before();
@@ -456,9 +482,10 @@ __device__ __forceinline__ void tmem_ld_x<4>(uint32_t taddr, float *v)
     for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(x[i]);
 }
 
-// relu(v[0..N)) as bf16, row r, columns c0.. of a K-major swizzled operand (c0 % 8 == 0, N % 8 == 0)
-template <int N>
-__device__ __forceinline__ void put_row_relu(uint8_t *op, int r, int c0, const float (&v)[N])
+// relu(v[0..N)) as bf16, row r, columns c0.. of a K-major swizzled operand (c0 % 8 == 0, N % 8 == 0);
+// D: also the rounded values to dst[0..N) when dst is not null (test hook)
+template <int N, bool D = false>
+__device__ __forceinline__ void put_row_relu(uint8_t *op, int r, int c0, const float (&v)[N], float *dst = nullptr)
 {
     constexpr int KC = P1Geo<true>::KC;
 #pragma unroll
@@ -471,6 +498,9 @@ __device__ __forceinline__ void put_row_relu(uint8_t *op, int r, int c0, const f
         p.w = pack_bf16x2_relu(v[8 * q + 6], v[8 * q + 7]);
         uint8_t *tile = op + (c / KC) * (128 * 128);
         *reinterpret_cast<uint4 *>(tile + sw128_offset(r, (c % KC) / 8)) = p;
+        if constexpr (D) {
+            if (dst) dump_unit_bf16(dst + 8 * q, p);
+        }
     }
 }
 
@@ -485,6 +515,8 @@ __device__ __forceinline__ float bf16_round(float x)
     return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// kDump: the test build that also writes the rounded hidden activations (ActDump)
+template <bool kDump>
 __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a, UmmaWeights w,
                                                                   const __grid_constant__ CUtensorMap fmap)
 {
@@ -720,7 +752,9 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
                     v[4 * k + 2] = hi.x;
                     v[4 * k + 3] = hi.y;
                 }
-                put_row_relu<32>(H1, ei, 32 * part, v);
+                float *drow = nullptr;
+                if constexpr (kDump) drow = live ? a.dump.row(n, t, L) : nullptr;
+                put_row_relu<32, kDump>(H1, ei, 32 * part, v, drow ? drow + a.dump.act_off + 32 * part : nullptr);
             }
             fence_async_smem();
             tc_fence_before();
@@ -740,7 +774,10 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] += bias[16 * part + j];
-                put_row_relu<16>(H2, ei, 16 * part, v);
+                float *drow = nullptr;
+                if constexpr (kDump) drow = live ? a.dump.row(n, t, L) : nullptr;
+                put_row_relu<16, kDump>(H2, ei, 16 * part, v,
+                                        drow ? drow + a.dump.act_off + kActorH1 + 16 * part : nullptr);
             }
             fence_async_smem();
             tc_fence_before();
@@ -851,19 +888,35 @@ __global__ void __launch_bounds__(kQThreads, 1) phase1_bf16_kernel(Phase1Args a,
     if (warp == 0) tmem_dealloc(tmem, kP1TmemCols);
 }
 
-template <bool BF16>
+template <bool BF16, bool kDump>
 cudaError_t launch_p1(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
 {
     using G = P1Geo<BF16>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(phase1_umma_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(phase1_umma_kernel<BF16, kDump>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int blocks = (a.N + kP1Threads - 1) / kP1Threads;
+    phase1_umma_kernel<BF16, kDump><<<blocks, kP1Threads, G::SMEM, s>>>(a, w, fmap);
+    return cudaGetLastError();
+}
+
+template <bool kDump>
+cudaError_t launch_bf16(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
+{
+    using G = P1Geo<true>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(phase1_bf16_kernel<kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              G::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const int blocks = (a.N + kP1Threads - 1) / kP1Threads;
-    phase1_umma_kernel<BF16><<<blocks, kP1Threads, G::SMEM, s>>>(a, w, fmap);
+    phase1_bf16_kernel<kDump><<<blocks, kQThreads, G::SMEM, s>>>(a, w, fmap);
     return cudaGetLastError();
 }
 
@@ -871,17 +924,9 @@ cudaError_t launch_p1(const Phase1Args &a, const UmmaWeights &w, const CUtensorM
 
 cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
 {
-    if (!w.bf16) return launch_p1<false>(a, w, fmap, s);
-    using G = P1Geo<true>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(phase1_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    const int blocks = (a.N + kP1Threads - 1) / kP1Threads;
-    phase1_bf16_kernel<<<blocks, kQThreads, G::SMEM, s>>>(a, w, fmap);
-    return cudaGetLastError();
+    const bool dump = a.dump.p != nullptr;
+    if (!w.bf16) return dump ? launch_p1<false, true>(a, w, fmap, s) : launch_p1<false, false>(a, w, fmap, s);
+    return dump ? launch_bf16<true>(a, w, fmap, s) : launch_bf16<false>(a, w, fmap, s);
 }
 
 namespace {

@@ -247,6 +247,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// the two bf16 values of a pack_bf16x2 word, as floats
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t p)
+{
+    return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+}
+
 // max(x, 0) of both values rounded to bf16 and packed (the rounding commutes
 // with the clamp, so this equals rounding relu(x))
 __device__ __forceinline__ uint32_t pack_bf16x2_relu(float lo, float hi)

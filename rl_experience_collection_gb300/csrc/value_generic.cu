@@ -201,10 +201,29 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar)
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// the test hook's row of a tile row (ActDump), or nullptr
+__device__ __forceinline__ float *dump_row_g(const ValueArgs &a, const RowInfoG &ri)
+{
+    if (ri.kind != 0 && ri.kind != 1) return nullptr;
+    const long long n = ri.row / a.L;
+    return a.dump.row(n, ri.kind == 0 ? (int)(ri.row - n * a.L) : a.L, a.L);
+}
+
+// the operand values v (as the next layer reads them) to dst[0..16), columns
+// below n_valid only
+template <bool BF16>
+__device__ __forceinline__ void dump16(float *dst, const float (&v)[16], int c0, int n_valid)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (c0 + i < n_valid) dst[i] = round_op(v[i], BF16);
+}
+
 // kStall: a test build in which the producer of CTA 0 issues no copy, so that
 // CTA's MMA issuer waits on a stage that never fills and the bounded-wait exit
-// runs (rollout_test_stall)
-template <bool BF16, bool kStall>
+// runs (rollout_test_stall).  kDump: a test build that also writes every
+// row's rounded hidden activations (rollout_test_activations).
+template <bool BF16, bool kStall, bool kDump>
 __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a, UmmaWeights w, uint8_t *scratch,
                                                                     long long scratch_per_cta)
 {
@@ -349,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
         for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
             const RowInfoG ri = decode_g(a, tile * 128 + r);
             const bool has = ri.kind == 0 || ri.kind == 1;
+            float *drow = nullptr;                              // test hook: this row's activation dump
+            if constexpr (kDump) drow = dump_row_g(a, ri);
             // ---- state row: X buffer (operand)
             {
                 float xv[16];
@@ -365,6 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                     xv[j] = x;
                 }
                 put16g<BF16>(bufs[kBufX], r, 16 * q, xv);
+                if constexpr (kDump) {
+                    if (drow) dump16<BF16>(drow + 16 * q, xv, 16 * q, kState);
+                }
             }
             fence_async_global();
             warp_arrive(&B.act);
@@ -389,6 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
 #pragma unroll
                             for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i] + __ldg(bias + cg + i), 0.f);
                             put16g<BF16>(bufs[J.out_buf], r, cg, v);
+                            if constexpr (kDump) {
+                                if (drow) dump16<BF16>(drow + a.dump.crit_off[J.layer - kJobCrit1] + cg, v, cg, Ly.n_out);
+                            }
                         } else if (J.epi == kEpiCur1) {
                             const int act = (ri.act >= 0 && ri.act < kActions) ? ri.act : 0;
                             const float *oh = vec + w.onehot_off + act * kCurH;
@@ -396,6 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                             for (int i = 0; i < 16; ++i)
                                 v[i] = fmaxf((v[i] + __ldg(oh + cg + i)) + __ldg(bias + cg + i), 0.f);
                             put16g<BF16>(bufs[J.out_buf], r, cg, v);
+                            if constexpr (kDump) {
+                                if (drow && ri.kind == 0) dump16<BF16>(drow + a.dump.cur_off + cg, v, cg, Ly.n_out);
+                            }
                         } else if (J.epi == kEpiCur2) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
@@ -414,6 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                             for (int i = 0; i < 16; ++i) {
                                 const float hv = round_op(fmaxf(v[i] + __ldg(bias + cg + i), 0.f), BF16);
                                 dot = fmaf(hv, __ldg(vec + w.head_w_off + cg + i), dot);
+                                if constexpr (kDump) {
+                                    if (drow && cg + i < Ly.n_out) drow[a.dump.crit_off[4] + cg + i] = hv;
+                                }
                             }
                         }
                     }
@@ -459,16 +492,20 @@ cudaError_t launch_g(const ValueArgs &a, const UmmaWeights &w, uint8_t *scratch,
 {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(value_generic_kernel<BF16, false>,
+        cudaError_t e = cudaFuncSetAttribute(value_generic_kernel<BF16, false, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(value_generic_kernel<BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmem);
+            e = cudaFuncSetAttribute(value_generic_kernel<BF16, true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(value_generic_kernel<BF16, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    if (stall) value_generic_kernel<BF16, true><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
-    else value_generic_kernel<BF16, false><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
+    if (stall) value_generic_kernel<BF16, true, false><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
+    else if (a.dump.p) value_generic_kernel<BF16, false, true><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
+    else value_generic_kernel<BF16, false, false><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
     return cudaGetLastError();
 }
 

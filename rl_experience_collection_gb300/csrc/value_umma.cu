@@ -310,8 +310,11 @@ __device__ __forceinline__ void target_cols(const ValueArgs &a, const RowInfo &r
     }
 }
 
-// 16 f32 values -> 2 bf16 units of row r, columns [16q, 16q+16) of operand tile `tile`
-__device__ __forceinline__ void put16(uint8_t *tile, int r, int q, const float (&v)[16])
+// 16 f32 values -> 2 bf16 units of row r, columns [16q, 16q+16) of operand tile
+// `tile`; D: also the rounded values of columns below n_valid to dst (test hook)
+template <bool D = false>
+__device__ __forceinline__ void put16(uint8_t *tile, int r, int q, const float (&v)[16], float *dst = nullptr,
+                                      int n_valid = 0)
 {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -321,6 +324,18 @@ __device__ __forceinline__ void put16(uint8_t *tile, int r, int q, const float (
         p.z = pack_bf16x2(v[8 * h + 4], v[8 * h + 5]);
         p.w = pack_bf16x2(v[8 * h + 6], v[8 * h + 7]);
         *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 2 * q + h)) = p;
+        if constexpr (D) {
+            if (dst) {
+                const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = unpack_bf16x2(w4[k]);
+                    const int c = 16 * q + 8 * h + 2 * k;
+                    if (c < n_valid) dst[8 * h + 2 * k] = f.x;
+                    if (c + 1 < n_valid) dst[8 * h + 2 * k + 1] = f.y;
+                }
+            }
+        }
     }
 }
 
@@ -339,8 +354,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(x[i]);
 }
 
-// 16 f32 values -> relu -> 2 bf16 units, as put16
-__device__ __forceinline__ void put16_relu(uint8_t *tile, int r, int q, const float (&v)[16])
+// 16 f32 values -> relu -> 2 bf16 units, as put16; D: also the rounded
+// values to dst[0..16) when dst is not null (test hook)
+template <bool D = false>
+__device__ __forceinline__ void put16_relu(uint8_t *tile, int r, int q, const float (&v)[16], float *dst = nullptr)
 {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -350,11 +367,30 @@ __device__ __forceinline__ void put16_relu(uint8_t *tile, int r, int q, const fl
         p.z = pack_bf16x2_relu(v[8 * h + 4], v[8 * h + 5]);
         p.w = pack_bf16x2_relu(v[8 * h + 6], v[8 * h + 7]);
         *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 2 * q + h)) = p;
+        if constexpr (D) {
+            if (dst) {
+                const float2 a = unpack_bf16x2(p.x), b = unpack_bf16x2(p.y), c = unpack_bf16x2(p.z),
+                             d = unpack_bf16x2(p.w);
+                reinterpret_cast<float4 *>(dst + 8 * h)[0] = make_float4(a.x, a.y, b.x, b.y);
+                reinterpret_cast<float4 *>(dst + 8 * h)[1] = make_float4(c.x, c.y, d.x, d.y);
+            }
+        }
     }
 }
 
-// relu(D[cols] + bias) rounded to bf16 into row r / quarter q of operand tile `tile`
-__device__ __forceinline__ void drain16(uint32_t taddr, const float *bias, uint8_t *tile, int r, int q)
+// the test hook's row of a tile row (ActDump), or nullptr
+__device__ __forceinline__ float *dump_row(const ValueArgs &a, const RowInfo &ri)
+{
+    if (ri.kind == 0) return a.dump.row(ri.n, (int)(ri.row - (long long)ri.n * a.L), a.L);
+    if (ri.kind == 1) return a.dump.row(ri.n, a.L, a.L);
+    return nullptr;
+}
+
+// relu(D[cols] + bias) rounded to bf16 into row r / quarter q of operand tile
+// `tile` (D: and to dst[0..16) when dst is not null)
+template <bool D = false>
+__device__ __forceinline__ void drain16(uint32_t taddr, const float *bias, uint8_t *tile, int r, int q,
+                                        float *dst = nullptr)
 {
     float v[16];
     tmem_ld16(taddr, v);
@@ -367,7 +403,7 @@ __device__ __forceinline__ void drain16(uint32_t taddr, const float *bias, uint8
         v[4 * k + 2] += b.z;
         v[4 * k + 3] += b.w;
     }
-    put16_relu(tile, r, q, v);
+    put16_relu<D>(tile, r, q, v, dst);
 }
 
 __device__ __forceinline__ void row_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory"); }
@@ -424,8 +460,9 @@ struct MmaCtx {
 
 // kStall: a test build in which the first producer of CTA 0 issues no copy, so
 // that CTA's MMA issuer waits on a weight stage that never fills and the
-// bounded-wait exit runs (rollout_test_stall)
-template <bool kStall>
+// bounded-wait exit runs (rollout_test_stall).  kDump: a test build that also
+// writes every row's rounded hidden activations (rollout_test_activations).
+template <bool kStall, bool kDump>
 __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs a, UmmaWeights w)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -654,7 +691,12 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             ph_feat ^= 1u;
             float xv[16];
             state_cols(a, ri, seg, feat, q, xv);
-            put16(slots + kXSlot * kSlot, r, q, xv);
+            float *dx = nullptr;
+            if constexpr (kDump) {
+                dx = dump_row(a, ri);
+                if (dx) dx += 16 * q;
+            }
+            put16<kDump>(slots + kXSlot * kSlot, r, q, xv, dx, kState);
             publish(&B.act_x);
         };
 
@@ -674,7 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 v[4 * k + 2] = (v[4 * k + 2] + o.z) + b.z;
                 v[4 * k + 3] = (v[4 * k + 3] + o.w) + b.w;
             }
-            put16_relu(slots + kZSlot * kSlot, r, q, v);
+            float *dz = nullptr;
+            if constexpr (kDump) {
+                dz = dump_row(a, ri);
+                if (dz && ri.kind == 0) dz += a.dump.cur_off + 16 * q;
+                else dz = nullptr;
+            }
+            put16_relu<kDump>(slots + kZSlot * kSlot, r, q, v, dz);
             publish(&B.act_z);
         };
 
@@ -693,9 +741,13 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             const RowInfo ri = nri;
             const long long next = tile + gridDim.x;
             const bool has_next = next < n_tiles;
+            float *drow = nullptr;                              // test hook: this row's activation dump
+            if constexpr (kDump) drow = dump_row(a, ri);
+            // column c of critic hidden layer l in the dump row, or nullptr
+            auto dcol = [&](int l, int c) -> float * { return drow ? drow + a.dump.crit_off[l] + c : nullptr; };
             // ---- h1 chunk 0 first: the tensor pipe waits for it
             wait_acc(&B.acc_d1, ph_d1);
-            drain16(lane_addr + kColD1, bias + kB1 + 16 * q, slots, r, q);
+            drain16<kDump>(lane_addr + kColD1, bias + kB1 + 16 * q, slots, r, q, dcol(0, 16 * q));
             publish(&B.act_h1[0]);
             // ---- curiosity layer 2: squared error against the pre-reset next state
             wait_acc(&B.acc_cur, ph_cur);
@@ -718,14 +770,16 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             // ---- h1 chunks 1..7 (the tensor pipe accumulates layer 2 meanwhile): the
             // first half of each layer-1 chunk goes to slot 0, the second to slot 1
             // once layer 2 has read the chunk before it there
-            drain16(lane_addr + kColD1 + 64, bias + kB1 + 64 + 16 * q, slots + kSlot, r, q);
+            drain16<kDump>(lane_addr + kColD1 + 64, bias + kB1 + 64 + 16 * q, slots + kSlot, r, q, dcol(0, 64 + 16 * q));
             publish(&B.act_h1[1]);
             for (int c = 1; c < 4; ++c) {
                 wait_acc(&B.acc_d1, ph_d1);
-                drain16(lane_addr + kColD1, bias + kB1 + 128 * c + 16 * q, slots, r, q);
+                drain16<kDump>(lane_addr + kColD1, bias + kB1 + 128 * c + 16 * q, slots, r, q,
+                               dcol(0, 128 * c + 16 * q));
                 publish(&B.act_h1[0]);
                 wait_acc(&B.acc_h1free, ph_free);
-                drain16(lane_addr + kColD1 + 64, bias + kB1 + 128 * c + 64 + 16 * q, slots + kSlot, r, q);
+                drain16<kDump>(lane_addr + kColD1 + 64, bias + kB1 + 128 * c + 64 + 16 * q, slots + kSlot, r, q,
+                               dcol(0, 128 * c + 64 + 16 * q));
                 publish(&B.act_h1[1]);
             }
             // the next tile's row metadata: loads issued where the rows wait for
@@ -735,21 +789,24 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
             wait_acc(&B.acc_main, ph_main);
             for (int kk = 0; kk < 6; ++kk) {
                 const int k = kk < 2 ? 4 + kk : kk - 2;
-                drain16(lane_addr + kColD2 + 64 * k, bias + kB2 + 64 * k + 16 * q, slots + k * kSlot, r, q);
+                drain16<kDump>(lane_addr + kColD2 + 64 * k, bias + kB2 + 64 * k + 16 * q, slots + k * kSlot, r, q,
+                               dcol(1, 64 * k + 16 * q));
                 publish(&B.act_h2[k]);
             }
             // ---- layer 3 -> h3 (layer 3 has read slots 4-5: stage the next tile's features there)
             wait_acc(&B.acc_main, ph_main);
             if (has_next && tid == 0) mbar_arrive(&B.feat_free);
             for (int k = 0; k < 4; ++k) {
-                drain16(lane_addr + kColD3 + 64 * k, bias + kB3 + 64 * k + 16 * q, slots + k * kSlot, r, q);
+                drain16<kDump>(lane_addr + kColD3 + 64 * k, bias + kB3 + 64 * k + 16 * q, slots + k * kSlot, r, q,
+                               dcol(2, 64 * k + 16 * q));
                 publish(&B.act_h3[k]);
             }
             if (has_next) nri = resolve(a, nf);                // the next tile's metadata has arrived
             // ---- layer 4 -> h4
             wait_acc(&B.acc_main, ph_main);
             for (int k = 0; k < 2; ++k) {
-                drain16(lane_addr + kColD4 + 64 * k, bias + kB4 + 64 * k + 16 * q, slots + k * kSlot, r, q);
+                drain16<kDump>(lane_addr + kColD4 + 64 * k, bias + kB4 + 64 * k + 16 * q, slots + k * kSlot, r, q,
+                               dcol(3, 64 * k + 16 * q));
                 publish(&B.act_h4[k]);
             }
             // ---- next tile's state row (slot 2 and TMEM [0,128) are free now): the
@@ -765,6 +822,9 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 for (int j = 0; j < 16; ++j) {
                     const float h = bf16_round(fmaxf(v[j] + bias[kB5 + 16 * q + j], 0.f));
                     dot = fmaf(h, bias[kHW + 16 * q + j], dot);
+                    if constexpr (kDump) {
+                        if (drow) drow[a.dump.crit_off[4] + 16 * q + j] = h;
+                    }
                 }
                 part_v[q * 128 + r] = dot;
             }
@@ -806,10 +866,14 @@ cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStre
         if (w.unit_bytes[u] > (uint32_t)kStage || (w.unit_bytes[u] & 15u) || (w.unit_off[u] & 15)) return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(value_umma_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmem);
+        cudaError_t e = cudaFuncSetAttribute(value_umma_bf16_kernel<false, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(value_umma_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            e = cudaFuncSetAttribute(value_umma_bf16_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(value_umma_bf16_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -819,8 +883,9 @@ cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStre
     const long long total = (long long)a.N * a.L + a.N;
     const long long tiles = (total + 127) / 128;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    if (stall) value_umma_bf16_kernel<true><<<grid, kThreads, kSmem, s>>>(a, w);
-    else value_umma_bf16_kernel<false><<<grid, kThreads, kSmem, s>>>(a, w);
+    if (stall) value_umma_bf16_kernel<true, false><<<grid, kThreads, kSmem, s>>>(a, w);
+    else if (a.dump.p) value_umma_bf16_kernel<false, true><<<grid, kThreads, kSmem, s>>>(a, w);
+    else value_umma_bf16_kernel<false, false><<<grid, kThreads, kSmem, s>>>(a, w);
     return cudaGetLastError();
 }
 

@@ -11,8 +11,6 @@ import pytest
 
 from rl_experience_collection_gb300 import workloads as wl
 
-from . import parity
-
 pytestmark = pytest.mark.gpu
 
 
@@ -46,12 +44,9 @@ def test_static_scratch_entry_matches_rollout_run(name, N, L):
         h.run_static(feats, starts, seeds, N, L, w.gamma, w.lam, out)
         assert h.status() == binding.ROLLOUT_OK, binding.last_error()
         got = {k: v.cpu().numpy() for k, v in out.items()}
-        for k in ("actions", "dones"):
+        # every tile's arithmetic is independent of the CTA and grid that run it,
+        # so the two entry points agree bit for bit; a tolerance could hide two
+        # CTAs overlapping in the shared array
+        for k in binding.OUTPUTS:
             np.testing.assert_array_equal(got[k], ref[k], err_msg=f"call {call}: {k}")
-        np.testing.assert_array_equal(got["states"], ref["states"])
-        rtol, atol = parity.RTOL[w.dtype], parity.ATOL[w.dtype]
-        for k in ("logp", "values"):
-            assert parity.rel_err(got[k], ref[k]).max() <= rtol, (call, k)
-        for k in ("rewards", "adv", "ret"):
-            assert np.abs(got[k].astype(np.float64) - ref[k]).max() <= atol, (call, k)
     h.close()
