@@ -236,6 +236,59 @@ def measure_dqn(dev, flush, steps, warmup):
     return w, statistics.mean(ms), [statistics.mean(p[i] for p in phase) for i in range(3)]
 
 
+OTHER_WORKLOADS = ("scaleout_tf32", "ceiling_bf16")
+
+
+def measure_workload(name: str, dev, flush, steps: int, warmup: int):
+    """One more workload timed like the main line (inputs resident, warm-up,
+    L2 flushed before every step, CUDA events on the launching stream) with its
+    value kernel's roofline against the tensor peak of its operand type."""
+    import torch
+    from rl_experience_collection_gb300 import binding
+    w = wl.WORKLOADS[name]
+    N, L = w.n_episodes, w.horizon
+    inputs = wl.generate(w)
+    h = binding.Rollout.for_workload(w, inputs.weights)
+    feats = torch.from_numpy(inputs.features).to(dev)
+    starts = torch.from_numpy(inputs.starts).to(dev)
+    seeds = torch.from_numpy(inputs.seeds.view(np.int32)).to(dev)
+    out = binding.make_outputs(N, L, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        h.run(feats, starts, seeds, N, L, w.gamma, w.lam, out, stream)
+    torch.cuda.synchronize()
+    h.set_timing(True)
+    ms, phase = [], []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(steps):
+        flush.fill_(float(i))
+        e0.record(stream)
+        h.run(feats, starts, seeds, N, L, w.gamma, w.lam, out, stream)
+        e1.record(stream)
+        phase.append(h.phase_ms())
+        ms.append(e0.elapsed_time(e1))
+    if h.status() != binding.ROLLOUT_OK:
+        raise SystemExit(f"{name}: device status")
+    h.close()
+    del out
+    torch.cuda.empty_cache()
+    pk = peaks()
+    tpk, tpk_name = tensor_peak(w.dtype, pk)
+    flop_step, flop_value = path_flops(w, N, L)
+    step_ms = statistics.mean(ms)
+    pm = {k: statistics.mean(p[i] for p in phase) for i, k in enumerate(("rollout", "states", "value", "gae"))}
+    achieved = flop_value / (pm["value"] / 1000.0) / 1e12
+    return {"workload": f"{name}: {N} x {L}, {w.dtype}, critic {'/'.join(map(str, w.critic_h))}",
+            "tuples_per_s": N * L / (step_ms / 1000.0), "ms_per_step": step_ms, "steps": steps, "warmup": warmup,
+            "phase_ms": pm,
+            "roofline": {"kernel": "value (critic + curiosity, tcgen05; activations in per-CTA L2 scratch)",
+                         "bound": "tensor", "achieved": achieved, "peak": tpk, "unit": "TFLOP/s",
+                         "frac": achieved / tpk, "peak_kind": f"{tpk_name}, burst, {pk['src']}",
+                         "algorithmic_flop_per_launch": flop_value, "traffic": None},
+            "tensor_pipe_frac_step": flop_step / (step_ms / 1000.0) / 1e12 / tpk,
+            "gpu_launches": launches_per_run(w.dtype) * steps, "l2": "flushed between steps"}
+
+
 def launches_per_run(dtype):
     """Kernels one rollout_run launches: feature padding (bf16 only), rollout,
     state rows, value, GAE."""
@@ -426,11 +479,36 @@ def max_over_ranks(x: float, dist, device):
     return float(t.item())
 
 
-def run_oracle_sample(w: wl.Workload, inputs, n_eps: int, first: int = 0):
+def host_cpu():
+    """The host's logical CPU count and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "model": model or platform.machine()}
+
+
+def run_oracle_sample(w: wl.Workload, inputs, n_eps: int, first: int = 0, threads: int = 1):
+    """Times the oracle (as it stands) on episodes first .. first+n_eps-1, episode-
+    parallel over `threads` host threads (the C calls release the GIL)."""
     from oracle import oracle as orc
-    idx = list(range(first, first + n_eps))
+    idx = [(first + i) % w.n_episodes for i in range(n_eps)]
     t0 = time.perf_counter()
-    orc.rollout(w, inputs, idx, quant=w.dtype, threads=1)
+    orc.rollout(w, inputs, idx, quant=w.dtype, threads=threads)
     return time.perf_counter() - t0, n_eps * w.horizon
 
 
@@ -438,12 +516,14 @@ def reference_arm(args, w: wl.Workload, rank: int):
     if rank != 0:
         return
     inputs = wl.generate(w)
-    n_eps = max(1, int(args.ref_episodes))
+    cpu = host_cpu()
+    threads = max(1, cpu["nproc"] or 1)
+    n_eps = max(1, int(args.ref_episodes)) * threads
     for i in range(args.warmup):
-        run_oracle_sample(w, inputs, n_eps, first=i * n_eps % w.n_episodes)
+        run_oracle_sample(w, inputs, n_eps, first=i * n_eps, threads=threads)
     times, tuples = [], 0
     for i in range(args.steps):
-        dt, n = run_oracle_sample(w, inputs, n_eps, first=(args.warmup + i) * n_eps % w.n_episodes)
+        dt, n = run_oracle_sample(w, inputs, n_eps, first=(args.warmup + i) * n_eps, threads=threads)
         times.append(dt)
         tuples += n
     v = tuples / sum(times)
@@ -453,8 +533,10 @@ def reference_arm(args, w: wl.Workload, rank: int):
             "data": "synthetic",
             "config": {"workload": w.name, "episodes": w.n_episodes, "horizon": w.horizon, "n_bars": w.n_bars,
                        "mlp_dtype": w.dtype, "sample_episodes_per_step": n_eps},
-            "cpu_baseline": {"value": v, "unit": "tuples/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{n_eps} episodes x {w.horizon} steps per step"},
+            "cpu_baseline": {"value": v, "unit": "tuples/s", "cores": threads, "kind": "oracle",
+                             "nproc": cpu["nproc"], "cpu_model": cpu["model"],
+                             "sample": f"{n_eps} episodes x {w.horizon} steps per step, episode-parallel "
+                                       f"over {threads} threads"},
             "e2e": {"value": v, "unit": "tuples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -466,8 +548,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS))
-    ap.add_argument("--ref-episodes", type=int, default=2, help="oracle episodes per reference step")
-    ap.add_argument("--cpu-episodes", type=int, default=12, help="oracle episodes for cpu_baseline")
+    ap.add_argument("--ref-episodes", type=int, default=1, help="oracle episodes per host thread per reference step")
+    ap.add_argument("--cpu-episodes", type=int, default=256, help="oracle episodes for cpu_baseline (all host cores)")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the measurements of the tf32 and widened-critic workloads")
     ap.add_argument("--episodes", type=int, default=None,
                     help="override the workload's episode count (a smaller case for profiling)")
     ap.add_argument("--horizon", type=int, default=None, help="override the workload's horizon")
@@ -583,6 +667,12 @@ def main():
             "phase_ms": {"rollout": rollout_ms, "states": states_ms, "value": value_ms, "gae": gae_ms},
             "roofline": roofline, "clocks": clk.summary(), "gpu_launches": launches_per_run(w.dtype) * args.steps}
 
+    # ---------------- the tf32 and widened-critic workloads (rank 0 alone)
+    if not args.no_others and rank == 0 and args.workload == DEFAULT_WORKLOAD and not (args.episodes or args.horizon):
+        line["workloads"] = {}
+        for name in OTHER_WORKLOADS:
+            line["workloads"][name] = measure_workload(name, dev, flush, args.steps, args.warmup)
+
     # ---------------- the PPO update on the collected tuples (rank 0 alone, float32)
     if not args.no_ppo and rank == 0:
         ms, flop = measure_ppo(w, inputs.weights, out, N, L, args.ppo_steps, 10, dev)
@@ -662,10 +752,16 @@ def main():
 
     # ---------------- CPU oracle baseline (rank 0, N=1 only)
     if rank == 0 and world == 1 and not args.no_cpu:
-        dt, n = run_oracle_sample(w, inputs, args.cpu_episodes)
-        line["cpu_baseline"] = {"value": n / dt, "unit": "tuples/s", "cores": 1, "kind": "oracle",
+        cpu = host_cpu()
+        threads = max(1, cpu["nproc"] or 1)
+        dt, n = run_oracle_sample(w, inputs, args.cpu_episodes, threads=threads)
+        dt1, n1 = run_oracle_sample(w, inputs, 4, first=args.cpu_episodes)
+        line["cpu_baseline"] = {"value": n / dt, "unit": "tuples/s", "cores": threads, "kind": "oracle",
+                                "nproc": cpu["nproc"], "cpu_model": cpu["model"],
+                                "single_thread_value": n1 / dt1,
                                 "sample": f"first {args.cpu_episodes} episodes x {L} steps of {w.name}, "
-                                          f"{w.dtype} operand rounding, single thread, {dt:.1f} s"}
+                                          f"{w.dtype} operand rounding, episode-parallel over {threads} "
+                                          f"threads, {dt:.1f} s (single thread: 4 episodes, {dt1:.1f} s)"}
     h.close()
     if rank == 0:
         print(json.dumps(line), flush=True)

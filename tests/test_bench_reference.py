@@ -21,7 +21,8 @@ def _check(line, n_gpus):
     assert line["steps"] == 2 and line["warmup"] >= 3 and line["data"] == "synthetic"
     assert line["config"]["workload"] == "tiny_fp32"
     cb = line["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] == os.cpu_count() and cb["value"] == line["value"] and cb["sample"]
+    assert cb["nproc"] == os.cpu_count() and cb["cpu_model"]
     assert line["e2e"] == {"value": line["value"], "unit": "tuples/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
 
