@@ -230,6 +230,21 @@ ROLLOUT_API int rollout_test_stall(rollout_handle *h, int on);
 ROLLOUT_API int rollout_test_activations(rollout_handle *h, float *dump, int n_episodes);
 
 /*
+ * rollout_test_alloc -- a test hook for allocation failures, not for
+ * production use.  (An addition of this library; the pages name no such
+ * hook.)  Every device allocation that a rollout handle makes (in
+ * rollout_create, rollout_set_weights and rollout_run_host's staging) is
+ * counted.  After rollout_test_alloc(k, ...) with k > 0, the k-th such
+ * allocation fails as if the device were out of memory; the call that
+ * needed it then returns ROLLOUT_ERR_NOMEM after freeing whatever it had
+ * allocated.  k <= 0 turns the hook off.  Every call restarts the count.
+ * live (may be NULL) receives the number of the library's device allocations
+ * currently held.  Process-wide; not thread-safe with respect to concurrent
+ * creates.  Returns ROLLOUT_OK.
+ */
+ROLLOUT_API int rollout_test_alloc(long long fail_at, long long *live);
+
+/*
  * rollout_run_static -- rollout_run for callers that cannot allocate device
  * memory.  (An addition of this library; the paper has no counterpart.)
  *

@@ -26,7 +26,8 @@ DTYPE = {"fp32": 0, "tf32": 1, "bf16": 2}
 
 EXPORTS = ["rollout_create", "rollout_set_weights", "rollout_run", "rollout_status", "rollout_destroy",
            "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static", "rollout_run_host",
-           "rollout_set_weights_device", "rollout_test_stall", "rollout_test_activations"]
+           "rollout_set_weights_device", "rollout_test_stall", "rollout_test_activations",
+           "rollout_test_alloc"]
 
 
 class RolloutDims(C.Structure):
@@ -110,6 +111,8 @@ def lib(path: Optional[str] = None):
     L.rollout_test_stall.argtypes = [vp, C.c_int]
     L.rollout_test_activations.restype = C.c_int
     L.rollout_test_activations.argtypes = [vp, vp, C.c_int]
+    L.rollout_test_alloc.restype = C.c_int
+    L.rollout_test_alloc.argtypes = [C.c_longlong, C.POINTER(C.c_longlong)]
     L.rollout_last_error.restype = C.c_char_p
     L.rollout_last_error.argtypes = []
     L.dqn_weight_count.restype = C.c_longlong
@@ -165,6 +168,14 @@ def lib(path: Optional[str] = None):
     L.ppo_destroy.argtypes = [vp]
     _lib = L
     return L
+
+
+def test_alloc(fail_at: int = 0) -> int:
+    """Test hook: the fail_at-th device allocation of rollout handles from now on
+    fails as out of memory (0: none).  Returns the live allocations."""
+    live = C.c_longlong()
+    _check(lib().rollout_test_alloc(int(fail_at), C.byref(live)))
+    return live.value
 
 
 def last_error() -> str:

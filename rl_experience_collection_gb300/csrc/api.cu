@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -214,9 +215,9 @@ int upload_simt(rollout_handle *h, const float *w)
     const size_t *offs_T = sh.offs_T, *offs_b = sh.offs_b, *q_T = sh.q_T, *q_b = sh.q_b;
     cudaError_t e;
     if (!h->d_actor_packed) {
-        if ((e = cudaMalloc(&h->d_actor_packed, sizeof(float) * ap.size())) != cudaSuccess)
+        if ((e = dev_alloc((void **)&h->d_actor_packed, sizeof(float) * ap.size())) != cudaSuccess)
             return cuda_fail(e, "cudaMalloc(actor)");
-        if ((e = cudaMalloc(&h->d_simt, sizeof(float) * sp.size())) != cudaSuccess)
+        if ((e = dev_alloc((void **)&h->d_simt, sizeof(float) * sp.size())) != cudaSuccess)
             return cuda_fail(e, "cudaMalloc(critic)");
     }
     if ((e = cudaMemcpy(h->d_actor_packed, ap.data(), sizeof(float) * ap.size(), cudaMemcpyHostToDevice)) !=
@@ -260,7 +261,7 @@ int upload_div_table(rollout_handle *h)
                 }
             }
     cudaError_t e;
-    if (!h->d_div_low && (e = cudaMalloc(&h->d_div_low, bits.size() * 4)) != cudaSuccess)
+    if (!h->d_div_low && (e = dev_alloc((void **)&h->d_div_low, bits.size() * 4)) != cudaSuccess)
         return cuda_fail(e, "cudaMalloc(div table)");
     if ((e = cudaMemcpy(h->d_div_low, bits.data(), bits.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
         return cuda_fail(e, "cudaMemcpy(div table)");
@@ -293,7 +294,7 @@ int upload_weights(rollout_handle *h, const float *w)
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
         h->scratch_per_cta = value_generic_scratch_per_cta(h->umma);
         h->scratch_ctas = sms;
-        if ((e = cudaMalloc(&h->d_scratch, (size_t)h->scratch_per_cta * sms)) != cudaSuccess)
+        if ((e = dev_alloc((void **)&h->d_scratch, (size_t)h->scratch_per_cta * sms)) != cudaSuccess)
             return cuda_fail(e, "cudaMalloc(value scratch)");
     }
     return ROLLOUT_OK;
@@ -391,7 +392,7 @@ int build_repack(rollout_handle *h)
         }
     }
     cudaError_t e;
-    if ((e = cudaMalloc(&h->d_maps, maps.size() * 4)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(weight map)");
+    if ((e = dev_alloc((void **)&h->d_maps, maps.size() * 4)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(weight map)");
     if ((e = cudaMemcpy(h->d_maps, maps.data(), maps.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
         return cuda_fail(e, "cudaMemcpy(weight map)");
     h->n_repack = (int)reg[0].size();
@@ -428,7 +429,7 @@ int make_feature_map(rollout_handle *h)
 {
     const size_t bytes = (size_t)h->dims.n_bars * kFPad * sizeof(float);
     cudaError_t e;
-    if ((e = cudaMalloc(&h->d_fpad, bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(padded features)");
+    if ((e = dev_alloc((void **)&h->d_fpad, bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(padded features)");
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
     e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
@@ -449,23 +450,23 @@ int make_feature_map(rollout_handle *h)
 void free_handle(rollout_handle *h)
 {
     if (!h) return;
-    cudaFree(h->d_fpad);
-    cudaFree(h->d_actor_packed);
-    cudaFree(h->d_simt);
-    cudaFree(h->d_umma);
-    cudaFree(h->d_scratch);
-    cudaFree(h->d_div_low);
-    cudaFree(h->d_status);
+    dev_free(h->d_fpad);
+    dev_free(h->d_actor_packed);
+    dev_free(h->d_simt);
+    dev_free(h->d_umma);
+    dev_free(h->d_scratch);
+    dev_free(h->d_div_low);
+    dev_free(h->d_status);
     for (cudaEvent_t e : h->ev)
         if (e) cudaEventDestroy(e);
-    cudaFree(h->d_stage);
+    dev_free(h->d_stage);
     for (cudaStream_t st : h->copy_stream)
         if (st) cudaStreamDestroy(st);
     for (cudaEvent_t e : h->point_ev)
         if (e) cudaEventDestroy(e);
     for (cudaEvent_t e : h->copy_done)
         if (e) cudaEventDestroy(e);
-    cudaFree(h->d_maps);
+    dev_free(h->d_maps);
     delete h;
 }
 
@@ -487,6 +488,29 @@ void clear_error() { g_err[0] = 0; }
 
 int validate_dims(const rollout_dims *d) { return check_dims(d); }
 
+static std::atomic<long long> g_alloc_fail_at{0};   // 0: no injected failure
+static std::atomic<long long> g_alloc_seen{0};      // allocations requested since the hook was set
+static std::atomic<long long> g_alloc_live{0};      // allocations not yet freed
+
+cudaError_t dev_alloc(void **p, size_t bytes)
+{
+    const long long k = g_alloc_fail_at.load();
+    if (k > 0 && ++g_alloc_seen == k) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e == cudaSuccess) ++g_alloc_live;
+    return e;
+}
+
+void dev_free(void *p)
+{
+    if (!p) return;
+    cudaFree(p);
+    --g_alloc_live;
+}
+
 }  // namespace rl
 
 extern "C" {
@@ -504,7 +528,7 @@ int rollout_create(const float *weights, const rollout_dims *dims, rollout_handl
     h->dims = *dims;
     cudaError_t e = cudaGetDevice(&h->device);
     if (e != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaGetDevice"); }
-    if ((e = cudaMalloc(&h->d_status, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMalloc(status)"); }
+    if ((e = dev_alloc((void **)&h->d_status, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMalloc(status)"); }
     if ((e = cudaMemset(h->d_status, 0, sizeof(int))) != cudaSuccess) { free_handle(h); return cuda_fail(e, "cudaMemset"); }
     if ((rc = upload_div_table(h)) || (rc = upload_weights(h, weights)) || (rc = build_repack(h)) ||
         (dims->dtype == ROLLOUT_BF16 && (rc = make_feature_map(h)))) {
@@ -725,10 +749,10 @@ int stage_buffers(rollout_handle *h, int N, int L, RunBuffers *b)
     cudaError_t e;
     if (total > h->stage_bytes) {
         // the previous run's copies may still read the old allocation: cudaFree waits for the device
-        cudaFree(h->d_stage);
+        dev_free(h->d_stage);
         h->d_stage = nullptr;
         h->stage_bytes = 0;
-        if ((e = cudaMalloc(&h->d_stage, total)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(staging)");
+        if ((e = dev_alloc((void **)&h->d_stage, total)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(staging)");
         h->stage_bytes = total;
     }
     uint8_t *p[11];
@@ -899,6 +923,15 @@ int rollout_test_activations(rollout_handle *h, float *dump, int n_episodes)
         return fail(ROLLOUT_ERR_INVALID, "the dump needs n_episodes > 0 and a 16-byte aligned array");
     h->dump = dump;
     h->dump_episodes = dump ? n_episodes : 0;
+    return ROLLOUT_OK;
+}
+
+int rollout_test_alloc(long long fail_at, long long *live)
+{
+    g_err[0] = 0;
+    rl::g_alloc_seen = 0;
+    rl::g_alloc_fail_at = fail_at > 0 ? fail_at : 0;
+    if (live) *live = rl::g_alloc_live.load();
     return ROLLOUT_OK;
 }
 

@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, D
                 tmem_ld_wait();
                 const float *oh = w.cur_onehot + act * 64 + c0;
 #pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = fmaxf(v[k] + cb1[c0 + k] + __ldg(oh + k), 0.f);
+                for (int k = 0; k < 32; ++k) v[k] = relu(v[k] + cb1[c0 + k] + __ldg(oh + k));
                 put32(Z, r, c0, v);
             }
             fence_async_smem();

@@ -72,6 +72,10 @@ struct ActDump {
     }
 };
 
+// ReLU as max(x, 0) through the comparison x < 0: a NaN input stays NaN (as
+// with cvt.rn.relu), where fmaxf(x, 0) would turn it into 0
+__device__ __forceinline__ float relu(float x) { return x < 0.f ? 0.f : x; }
+
 // device status word values (first error wins)
 constexpr int kStatusOk = 0;
 
@@ -144,6 +148,13 @@ cudaError_t launch_states(const StatesArgs &a, cudaStream_t s);
 
 // --- GAE (gae.cu) ---
 cudaError_t launch_gae(const GaeArgs &a, cudaStream_t s);
+
+// --- device allocations of rollout handles (api.cu) ---
+// Every device allocation a rollout handle makes goes through dev_alloc /
+// dev_free, which count the live ones and let a test make the k-th
+// allocation fail as if the device were out of memory (rollout_test_alloc).
+cudaError_t dev_alloc(void **p, size_t bytes);
+void dev_free(void *p);
 
 // --- shared host helpers (api.cu) ---
 int set_error(int code, const char *fmt, ...);   // records the message rollout_last_error returns; returns code

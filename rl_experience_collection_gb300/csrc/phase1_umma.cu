@@ -140,7 +140,7 @@ __device__ __forceinline__ void epi_hidden(uint32_t taddr, const float *bias, ui
         tmem_ld32(taddr + 32 * g, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i] + bias[32 * g + i], 0.f);
+        for (int i = 0; i < 32; ++i) v[i] = relu(v[i] + bias[32 * g + i]);
         put_row<BF16, 32, D>(op, r, 32 * g, v, dst ? dst + 32 * g : nullptr);
     }
 }

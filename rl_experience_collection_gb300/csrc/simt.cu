@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kP1Threads) phase1_simt_kernel(Phase1Args a, c
                 acc_row32(acc, W + kA1 + i * kActorH1 + jc * 32, xs[i * kP1Threads + tid]);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                h1[(jc * 32 + j) * kP1Threads + tid] = fmaxf(acc[j] + W[kB1 + jc * 32 + j], 0.f);
+                h1[(jc * 32 + j) * kP1Threads + tid] = relu(acc[j] + W[kB1 + jc * 32 + j]);
         }
         // actor layer 2: 128 -> 64, ReLU
         for (int jc = 0; jc < kActorH2 / 32; ++jc) {
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kP1Threads) phase1_simt_kernel(Phase1Args a, c
                 acc_row32(acc, W + kA2 + i * kActorH2 + jc * 32, h1[i * kP1Threads + tid]);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                h2[(jc * 32 + j) * kP1Threads + tid] = fmaxf(acc[j] + W[kB2 + jc * 32 + j], 0.f);
+                h2[(jc * 32 + j) * kP1Threads + tid] = relu(acc[j] + W[kB2 + jc * 32 + j]);
         }
         // actor layer 3: 64 -> 45 logits
         float lg[48];
@@ -145,10 +145,10 @@ __global__ void __launch_bounds__(kP1Threads) phase1_simt_kernel(Phase1Args a, c
 
 constexpr int kVThreads = 256;
 
-// out[r][j] = (relu)(b[j] + sum_k in[r][k] * W^T[k][j]) for the block's ROWS rows.
+// out[r][j] = (relu_ ? relu : identity)(b[j] + sum_k in[r][k] * W^T[k][j]) for the block's ROWS rows.
 template <int ROWS>
 __device__ void dense_rows(const float *__restrict__ WT, const float *__restrict__ bias, int K, int N,
-                           const float *in, int ldi, float *out, int ldo, bool relu,
+                           const float *in, int ldi, float *out, int ldo, bool relu_,
                            const int *onehot = nullptr)
 {
     constexpr int RPT = ROWS / 4;
@@ -174,7 +174,7 @@ __device__ void dense_rows(const float *__restrict__ WT, const float *__restrict
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 float v = acc[r] + bj;
-                out[(ty * RPT + r) * ldo + j] = relu ? fmaxf(v, 0.f) : v;
+                out[(ty * RPT + r) * ldo + j] = relu_ ? rl::relu(v) : v;
             }
         }
     }

@@ -225,11 +225,11 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *hw, const 
     // later uploads of the same shapes reuse the allocation, so device pointers
     // into it (the weight-refresh maps) stay valid
     if (*d_buf && w->buf_bytes != total) {
-        cudaFree(*d_buf);
+        dev_free(*d_buf);
         *d_buf = nullptr;
     }
     if (!*d_buf) {
-        if ((e = cudaMalloc(d_buf, total)) != cudaSuccess) {
+        if ((e = dev_alloc(d_buf, total)) != cudaSuccess) {
             snprintf(err, err_len, "cudaMalloc(tensor-core weights): %s", cudaGetErrorString(e));
             return e == cudaErrorMemoryAllocation ? ROLLOUT_ERR_NOMEM : ROLLOUT_ERR_CUDA;
         }

@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                         tmem_ld16g(lane_addr + 256 * h + cl, v);
                         if (J.epi == kEpiHidden) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i] + __ldg(bias + cg + i), 0.f);
+                            for (int i = 0; i < 16; ++i) v[i] = relu(v[i] + __ldg(bias + cg + i));
                             put16g<BF16>(bufs[J.out_buf], r, cg, v);
                             if constexpr (kDump) {
                                 if (drow) dump16<BF16>(drow + a.dump.crit_off[J.layer - kJobCrit1] + cg, v, cg, Ly.n_out);
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                             const float *oh = vec + w.onehot_off + act * kCurH;
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
-                                v[i] = fmaxf((v[i] + __ldg(oh + cg + i)) + __ldg(bias + cg + i), 0.f);
+                                v[i] = relu((v[i] + __ldg(oh + cg + i)) + __ldg(bias + cg + i));
                             put16g<BF16>(bufs[J.out_buf], r, cg, v);
                             if constexpr (kDump) {
                                 if (drow && ri.kind == 0) dump16<BF16>(drow + a.dump.cur_off + cg, v, cg, Ly.n_out);
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                         } else {   // head: relu, operand rounding, dot with the head weights
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
-                                const float hv = round_op(fmaxf(v[i] + __ldg(bias + cg + i), 0.f), BF16);
+                                const float hv = round_op(relu(v[i] + __ldg(bias + cg + i)), BF16);
                                 dot = fmaf(hv, __ldg(vec + w.head_w_off + cg + i), dot);
                                 if constexpr (kDump) {
                                     if (drow && cg + i < Ly.n_out) drow[a.dump.crit_off[4] + cg + i] = hv;

@@ -820,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 float dot = 0.f;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float h = bf16_round(fmaxf(v[j] + bias[kB5 + 16 * q + j], 0.f));
+                    const float h = bf16_round(relu(v[j] + bias[kB5 + 16 * q + j]));
                     dot = fmaf(h, bias[kHW + 16 * q + j], dot);
                     if constexpr (kDump) {
                         if (drow) drow[a.dump.crit_off[4] + 16 * q + j] = h;
