@@ -95,6 +95,20 @@ ROLLOUT_API int ppo_gradient(ppo_trainer *t, const float *states, const int32_t 
                              const float *adv, const float *ret, long long T, const int32_t *indices, int batch,
                              const ppo_hparams *hp, float *grad, float *stats, void *stream);
 
+/*
+ * ppo_test_activations -- a test hook (not for production use): copies the
+ * hidden activations of the last mini-batch forward pass (that of the last
+ * ppo_gradient call, or of the last step of ppo_update) to `act` (device or
+ * host), after the work enqueued on `stream`: row r of the batch is
+ * [actor hidden layers | critic hidden layers] (actor_h1 + actor_h2 + the
+ * critic's hidden widths floats, after the ReLU).  Lets a check see which side
+ * of the ReLU kink the float32 tensor-core products put each pre-activation.
+ * (An addition of this library: page "Fused CUDA Training Kernel --
+ * Implementation Plan", "Chunk 2: Backward Pass Kernel", defines the masks it
+ * exposes.)  Returns ROLLOUT_OK, _INVALID (no forward pass yet) or _CUDA.
+ */
+ROLLOUT_API int ppo_test_activations(ppo_trainer *t, float *act, void *stream);
+
 /* ppo_get_weights -- copy the packed float32 weights (device or host
  * destination, n_weights floats) after the work enqueued on `stream`. */
 ROLLOUT_API int ppo_get_weights(ppo_trainer *t, float *weights, void *stream);

@@ -87,18 +87,48 @@ long ppo_trained_count(const ppo_shape *s)
     return layout(s, &a, &c);
 }
 
+/* Replay of the path's ReLU decisions.  The path under test computes each
+ * hidden pre-activation z in float32 from products whose relative error is at
+ * most 2^-15 (its operands' split), so where the exact z lies within
+ * (2^-15 + (K + 4) 2^-23) sum|terms| of 0 it may take the other side of the
+ * kink: a floating-point decision, like an action drawn within rounding of a
+ * CDF boundary.  There the oracle adopts the path's activation (a replay);
+ * a different side farther from the kink is a mismatch (adopted as well). */
+typedef struct {
+    long replays, mismatches;
+} ppo_replay;
+
 /* forward pass keeping every layer's output: act[l] is layer l's output
- * (after the ReLU for hidden layers), act_in = the input */
-static void forward(const double *p, const net *n, const double *x, double act[][PPO_MAX_W])
+ * (after the ReLU for hidden layers), act_in = the input.  gact (or NULL):
+ * the path's hidden activations of this row and net, layer after layer,
+ * replayed as above. */
+static void forward(const double *p, const net *n, const double *x, double act[][PPO_MAX_W], const float *gact,
+                    ppo_replay *rp)
 {
     const double *in = x;
+    long at = 0;
     for (int l = 0; l < n->n_layers; ++l) {
         const int last = l == n->n_layers - 1;
         for (int j = 0; j < n->out[l]; ++j) {
-            double acc = p[n->b[l] + j];
-            for (int i = 0; i < n->in[l]; ++i) acc += p[n->w[l] + (long)j * n->in[l] + i] * in[i];
-            act[l][j] = (!last && acc <= 0.0) ? 0.0 : acc;
+            double acc = p[n->b[l] + j], mag = fabs(p[n->b[l] + j]);
+            for (int i = 0; i < n->in[l]; ++i) {
+                const double t = p[n->w[l] + (long)j * n->in[l] + i] * in[i];
+                acc += t;
+                mag += fabs(t);
+            }
+            double y = (!last && acc <= 0.0) ? 0.0 : acc;
+            if (gact && !last) {
+                const double g = (double)gact[at + j];
+                if ((g > 0.0) != (acc > 0.0)) {
+                    const double bound = (ldexp(1.0, -15) + (double)(n->in[l] + 4) * ldexp(1.0, -23)) * mag;
+                    if (fabs(acc) <= bound) rp->replays++;
+                    else rp->mismatches++;
+                    y = g > 0.0 ? g : 0.0;
+                }
+            }
+            act[l][j] = y;
         }
+        if (!last) at += n->out[l];
         in = act[l];
     }
 }
@@ -173,10 +203,28 @@ void ppo_kink_margin(const double *p, const ppo_shape *s, const float *states, c
  * [1] value loss (before c_v), [2] fraction of rows whose clipped term is the
  * smaller, [3] mean ratio.
  */
+void ppo_loss_grad_replay(const double *p, const ppo_shape *s, const ppo_hp *hp, const float *states,
+                          const int32_t *actions, const float *logp_old, const float *adv, const float *ret,
+                          const int32_t *rows, int B, double *g, double *stats, const float *gpu_act, long gpu_ld,
+                          long *replays, long *mismatches);
+
 void ppo_loss_grad(const double *p, const ppo_shape *s, const ppo_hp *hp, const float *states,
                    const int32_t *actions, const float *logp_old, const float *adv, const float *ret,
                    const int32_t *rows, int B, double *g, double *stats)
 {
+    ppo_loss_grad_replay(p, s, hp, states, actions, logp_old, adv, ret, rows, B, g, stats, NULL, 0, NULL, NULL);
+}
+
+/* ppo_loss_grad, given the path's hidden activations of the mini-batch
+ * (gpu_act row r at gpu_act + r * gpu_ld: [actor hidden layers | critic
+ * hidden layers]), replaying its ReLU decisions (see ppo_replay); the counts
+ * go to *replays and *mismatches. */
+void ppo_loss_grad_replay(const double *p, const ppo_shape *s, const ppo_hp *hp, const float *states,
+                          const int32_t *actions, const float *logp_old, const float *adv, const float *ret,
+                          const int32_t *rows, int B, double *g, double *stats, const float *gpu_act, long gpu_ld,
+                          long *replays, long *mismatches)
+{
+    ppo_replay rp = {0, 0};
     net an, cn;
     const long np = layout(s, &an, &cn);
     const int sd = s->n_market + 3, na = s->n_actions;
@@ -189,8 +237,9 @@ void ppo_loss_grad(const double *p, const ppo_shape *s, const ppo_hp *hp, const 
         for (int i = 0; i < sd; ++i) x[i] = (double)states[row * sd + i];
         const int a = actions[row];
         const double A = (double)adv[row], R = (double)ret[row];
+        const float *ga = gpu_act ? gpu_act + (long)r * gpu_ld : NULL;
         /* actor: log-softmax of the taken action */
-        forward(p, &an, x, act);
+        forward(p, &an, x, act, ga, &rp);
         const double *lg = act[an.n_layers - 1];
         double m = lg[0];
         for (int j = 1; j < na; ++j) m = lg[j] > m ? lg[j] : m;
@@ -209,12 +258,14 @@ void ppo_loss_grad(const double *p, const ppo_shape *s, const ppo_hp *hp, const 
         for (int j = 0; j < na; ++j) dl[j] = glp * ((j == a ? 1.0 : 0.0) - exp(lg[j] - m) / z);
         backward(p, &an, x, act, dl, g);
         /* critic */
-        forward(p, &cn, x, act);
+        forward(p, &cn, x, act, ga ? ga + s->actor_h1 + s->actor_h2 : NULL, &rp);
         const double v = act[cn.n_layers - 1][0];
         l_v += (v - R) * (v - R);
         const double dv = 2.0 * hp->value_coef * (v - R) / (double)B;
         backward(p, &cn, x, act, &dv, g);
     }
+    if (replays) *replays = rp.replays;
+    if (mismatches) *mismatches = rp.mismatches;
     if (stats) {
         stats[0] = l_clip / B;
         stats[1] = l_v / B;

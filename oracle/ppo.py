@@ -77,6 +77,9 @@ def lib():
                                  vp, vp, C.POINTER(C.c_long), vp]
         L.ppo_kink_margin.restype = None
         L.ppo_kink_margin.argtypes = [vp, C.POINTER(Shape), vp, vp, C.c_int, vp]
+        L.ppo_loss_grad_replay.restype = None
+        L.ppo_loss_grad_replay.argtypes = [vp, C.POINTER(Shape), C.POINTER(HP), vp, vp, vp, vp, vp, vp, C.c_int, vp,
+                                           vp, vp, C.c_long, C.POINTER(C.c_long), C.POINTER(C.c_long)]
         _lib = L
     return _lib
 
@@ -127,6 +130,25 @@ def loss_grad(params: np.ndarray, shape: Shape, hp: Hyper, b: Batch, rows: np.nd
     lib().ppo_loss_grad(_p(p), C.byref(shape), C.byref(h), _p(b.states), _p(b.actions), _p(b.logp), _p(b.adv),
                         _p(b.ret), _p(rows), len(rows), _p(g), _p(st))
     return st, g
+
+
+def loss_grad_replay(params: np.ndarray, shape: Shape, hp: Hyper, b: Batch, rows: np.ndarray, gpu_act: np.ndarray):
+    """loss_grad, adopting the path's side of the ReLU kink where its float32
+    evaluation may differ from the exact one.  gpu_act: [len(rows), actor hidden |
+    critic hidden] float32, the path's hidden activations.  Returns (stats,
+    gradient, replays, mismatches)."""
+    p = np.ascontiguousarray(params, dtype=np.float64)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    ga = np.ascontiguousarray(gpu_act, dtype=np.float32)
+    assert ga.shape[0] == len(rows)
+    g = np.zeros(trained_count(shape), dtype=np.float64)
+    st = np.zeros(4, dtype=np.float64)
+    h = hp.c()
+    rep, mis = C.c_long(0), C.c_long(0)
+    lib().ppo_loss_grad_replay(_p(p), C.byref(shape), C.byref(h), _p(b.states), _p(b.actions), _p(b.logp), _p(b.adv),
+                               _p(b.ret), _p(rows), len(rows), _p(g), _p(st), _p(ga), ga.shape[1], C.byref(rep),
+                               C.byref(mis))
+    return st, g, rep.value, mis.value
 
 
 def kink_margin(params: np.ndarray, shape: Shape, b: Batch, rows: np.ndarray) -> np.ndarray:

@@ -42,7 +42,7 @@ class RolloutDims(C.Structure):
 
 
 PPO_EXPORTS = ["ppo_create", "ppo_update", "ppo_gradient", "ppo_get_weights", "ppo_reset_optimizer", "ppo_status",
-               "ppo_device_weights",
+               "ppo_device_weights", "ppo_test_activations",
                "ppo_destroy"]
 
 
@@ -160,6 +160,8 @@ def lib(path: Optional[str] = None):
     L.ppo_gradient.argtypes = [vp, vp, vp, vp, vp, vp, C.c_longlong, vp, C.c_int, C.POINTER(PpoHparams), vp, vp, vp]
     L.ppo_get_weights.restype = C.c_int
     L.ppo_get_weights.argtypes = [vp, vp, vp]
+    L.ppo_test_activations.restype = C.c_int
+    L.ppo_test_activations.argtypes = [vp, vp, vp]
     L.ppo_reset_optimizer.restype = C.c_int
     L.ppo_reset_optimizer.argtypes = [vp, vp]
     L.ppo_status.restype = C.c_int
@@ -360,6 +362,7 @@ class PpoTrainer:
         _check(lib().ppo_create(self._w.ctypes.data_as(C.c_void_p), C.byref(dims), C.byref(h)))
         self._h = h
         self.n_weights = self._w.size
+        self.critic_h = tuple(dims.critic_h[i] for i in range(dims.critic_nh))
 
     @classmethod
     def for_workload(cls, w: wl.Workload, weights):
@@ -400,6 +403,17 @@ class PpoTrainer:
         if not (out.is_cuda and out.is_contiguous()) or out.numel() != self.n_weights or out.dtype.itemsize != 4:
             raise ValueError("out must be a contiguous float32 CUDA tensor of n_weights elements")
         _check(lib().ppo_get_weights(self._h, C.c_void_p(out.data_ptr()), C.c_void_p(_stream_handle(stream))))
+
+    def activations(self, batch: int, stream=None):
+        """Test hook: the last forward pass's hidden activations, [batch, actor
+        hidden | critic hidden] float32 (numpy, after a synchronise)."""
+        import numpy as np
+        import torch
+        width = wl.ACTOR_H[0] + wl.ACTOR_H[1] + int(sum(self.critic_h))
+        out = torch.empty((batch, width), dtype=torch.float32, device="cuda")
+        _check(lib().ppo_test_activations(self._h, C.c_void_p(out.data_ptr()), C.c_void_p(_stream_handle(stream))))
+        torch.cuda.synchronize()
+        return out.cpu().numpy()
 
     def device_weights(self) -> int:
         """ppo_device_weights: the address of the trainer's own device weights (updated

@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             if log:
                 sys.stderr.write(log)
     tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart", "-lcublas"]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stderr}")

@@ -10,16 +10,21 @@
 //
 // Parameters, gradients and moments are float32, in the packed weight layout
 // (actor, then critic; the curiosity part is carried along untrained).  Each
-// dense layer's forward, weight-gradient and input-gradient products are
-// float32 GEMMs (cuBLAS, row-major [out, in] weights seen as column-major);
-// the gather, bias, ReLU, loss heads, bias gradients, the norm and Adam are the
-// kernels below.  Every reduction runs in a fixed order (per column, per
-// block, then over the blocks), so a step's result does not depend on timing.
-// One optimizer step is captured as a CUDA graph (about 55 launches) and
-// replayed for every step of a call: the step's mini-batch slice, statistics
-// slot and Adam step count are read from device counters that a last 1-thread
-// kernel advances, so that the same graph serves every step.
-#include <cublas_v2.h>
+// dense layer's forward, weight-gradient and input-gradient products run on
+// the tensor cores (ppo_gemm.cu: tcgen05 MMAs on a bf16 high/low split of the
+// float32 operands, float32-grade products), with the bias and ReLU fused into
+// the forward product, the bias gradient into the weight-gradient product (a
+// row of ones appended to the layer input) and the ReLU derivative into the
+// input-gradient product.  Each product also writes the transposed copy that
+// the next product reads as its K-contiguous operand; the weights' transposes
+// are refreshed after every Adam step.  The gather, the loss heads, the norm
+// and Adam are the kernels below.  Every reduction runs in a fixed order (the
+// tensor core's per tile, per block, then over the blocks), so a step's result
+// does not depend on timing.  One optimizer step is captured as a CUDA graph
+// (34 launches) and replayed for every step of a call: the step's mini-batch
+// slice, statistics slot and Adam step count are read from device counters
+// that a last 1-thread kernel advances, so that the same graph serves every
+// step.
 #include <math.h>
 #include <string.h>
 
@@ -27,6 +32,7 @@
 
 #include "../../include/ppo.h"
 #include "internal.cuh"
+#include "ppo_gemm.cuh"
 
 using namespace rl;
 
@@ -39,7 +45,6 @@ constexpr int kNormBlocks = 304;   // fixed, so that the norm's summation order 
 constexpr int kNormThreads = 256;
 
 constexpr int kGraphMinSteps = 4;              // calls with fewer steps launch directly
-constexpr size_t kBlasWorkspace = 32u << 20;   // cuBLAS workspace, fixed so that capture allocates nothing
 
 struct Net {
     int n = 0;
@@ -74,16 +79,19 @@ struct ppo_trainer {
     float *d_x = nullptr;              // [cap, 54]
     int32_t *d_a = nullptr;
     float *d_lpo = nullptr, *d_adv = nullptr, *d_ret = nullptr;
+    float *d_xt = nullptr;             // [kState + 1, cap]: x^T and a row of ones
     float *d_act[2][kMaxLayers] = {};  // layer outputs [cap, out]
+    float *d_actt[2][kMaxLayers] = {}; // their transposes [out + 1, cap], the last row ones
     float *d_da = nullptr, *d_db = nullptr;   // backpropagated gradients [cap, kMaxWidth]
+    float *d_dat = nullptr, *d_dbt = nullptr; // their transposes [kMaxWidth, cap]
+    float *d_wt = nullptr;             // transposed weights: layer l's [in, out] at its offset
     float *d_rows = nullptr;           // per-row statistics [4][cap]
     double *d_part = nullptr;          // [kNormBlocks] partial sums of g^2
     int *d_status = nullptr;
     int *d_k = nullptr;                // step index within the current call
     long long *d_t = nullptr;          // Adam step count
-    cublasHandle_t blas = nullptr;
-    void *d_ws = nullptr;              // cuBLAS workspace
     cudaStream_t last_stream = nullptr;
+    int last_batch = 0;                // rows of the last forward pass (ppo_test_activations)
     cudaStream_t cap_stream = nullptr; // where one step is captured
     cudaGraphExec_t exec = nullptr;
     GraphKey key;
@@ -97,18 +105,14 @@ int cuda_err(cudaError_t e, const char *what)
                      cudaGetErrorString(e));
 }
 
-int blas_err(cublasStatus_t st, const char *what)
-{
-    return set_error(st == CUBLAS_STATUS_ALLOC_FAILED ? ROLLOUT_ERR_NOMEM : ROLLOUT_ERR_CUDA, "%s: cuBLAS status %d",
-                     what, (int)st);
-}
 
 // ------------------------------------------------------------------ kernels
 
 // one block per mini-batch row: copy the tuple the index names
 __global__ void gather_kernel(const float *states, const int32_t *actions, const float *logp_old,
                               const float *adv, const float *ret, long long T, const int32_t *idx_base,
-                              const int *step_k, float *x, int32_t *a, float *lpo, float *A, float *R, int *status)
+                              const int *step_k, float *x, float *xt, int ldt, int32_t *a, float *lpo, float *A,
+                              float *R, int *status)
 {
     const int r = blockIdx.x;
     long long i = idx_base[(size_t)*step_k * gridDim.x + r];
@@ -116,7 +120,11 @@ __global__ void gather_kernel(const float *states, const int32_t *actions, const
         if (threadIdx.x == 0) atomicCAS(status, 0, ROLLOUT_ERR_RANGE);
         i = 0;
     }
-    for (int c = threadIdx.x; c < kState; c += blockDim.x) x[(size_t)r * kState + c] = states[i * kState + c];
+    for (int c = threadIdx.x; c < kState; c += blockDim.x) {
+        const float v = states[i * kState + c];
+        x[(size_t)r * kState + c] = v;
+        xt[(size_t)c * ldt + r] = v;
+    }
     if (threadIdx.x == 0) {
         int act = actions[i];
         if (act < 0 || act >= kActions) {
@@ -130,20 +138,10 @@ __global__ void gather_kernel(const float *states, const int32_t *actions, const
     }
 }
 
-// Y[r, j] += b[j], then ReLU for hidden layers
-__global__ void bias_act_kernel(float *Y, const float *b, int rows, int n, int relu)
-{
-    const size_t total = (size_t)rows * n;
-    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
-        const float y = Y[e] + b[e % n];
-        Y[e] = (relu && y <= 0.f) ? 0.f : y;
-    }
-}
-
 // one warp per row: log-softmax of the taken action, ratio, clipped surrogate,
 // and the gradient of the loss with respect to the logits
 __global__ void actor_head_kernel(const float *logits, const int32_t *a, const float *lpo, const float *A, int B,
-                                  float clip_eps, float *dl, float *rows)
+                                  float clip_eps, float *dl, float *dlt, int ldt, float *rows)
 {
     const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (w >= B) return;
@@ -164,8 +162,14 @@ __global__ void actor_head_kernel(const float *logits, const int32_t *a, const f
     const bool unclipped = s1 <= s2;
     const float glp = unclipped ? -adv * rho / (float)B : 0.f;
     float *d = dl + (size_t)w * kActions;
-    d[lane] = glp * ((lane == act ? 1.f : 0.f) - e0 / z);
-    if (lane + 32 < kActions) d[lane + 32] = glp * ((lane + 32 == act ? 1.f : 0.f) - e1 / z);
+    const float g0 = glp * ((lane == act ? 1.f : 0.f) - e0 / z);
+    d[lane] = g0;
+    dlt[(size_t)lane * ldt + w] = g0;
+    if (lane + 32 < kActions) {
+        const float g1 = glp * ((lane + 32 == act ? 1.f : 0.f) - e1 / z);
+        d[lane + 32] = g1;
+        dlt[(size_t)(lane + 32) * ldt + w] = g1;
+    }
     if (lane == 0) {
         rows[0 * B + w] = -(unclipped ? s1 : s2);
         rows[2 * B + w] = unclipped ? 0.f : 1.f;
@@ -174,41 +178,16 @@ __global__ void actor_head_kernel(const float *logits, const int32_t *a, const f
 }
 
 // critic head: squared error and its gradient with respect to v
-__global__ void critic_head_kernel(const float *v, const float *R, int B, float value_coef, float *dv, float *rows)
+__global__ void critic_head_kernel(const float *v, const float *R, int B, float value_coef, float *dv, float *dvt,
+                                   float *rows)
 {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= B) return;
     const float d = v[r] - R[r];
     rows[1 * B + r] = d * d;
-    dv[r] = 2.f * value_coef * d / (float)B;
-}
-
-// db[j] = sum over rows of dY[r, j] (double): a block takes 32 columns; row
-// group y (of 8) sums rows y, y+8, ... in order, then the groups are added in
-// order, so the result does not depend on scheduling
-constexpr int kBgCols = 32, kBgGroups = 8;
-__global__ void __launch_bounds__(kBgCols * kBgGroups) bias_grad_kernel(const float *dY, int rows, int n, float *db)
-{
-    __shared__ double part[kBgGroups][kBgCols];
-    const int c = threadIdx.x % kBgCols, y = threadIdx.x / kBgCols;
-    const int j = blockIdx.x * kBgCols + c;
-    double s = 0.0;
-    if (j < n)
-        for (int r = y; r < rows; r += kBgGroups) s += (double)dY[(size_t)r * n + j];
-    part[y][c] = s;
-    __syncthreads();
-    if (y == 0 && j < n) {
-        double t = 0.0;
-        for (int k = 0; k < kBgGroups; ++k) t += part[k][c];
-        db[j] = (float)t;
-    }
-}
-
-// ReLU' of the layer whose output is H: dX = 0 where H = 0
-__global__ void relu_back_kernel(float *dX, const float *H, size_t total)
-{
-    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x)
-        if (!(H[e] > 0.f)) dX[e] = 0.f;
+    const float g = 2.f * value_coef * d / (float)B;
+    dv[r] = g;
+    dvt[r] = g;                                  // [1, B]: the same values
 }
 
 __device__ __forceinline__ double block_sum(double v, double *sh)
@@ -281,6 +260,35 @@ __global__ void stats_kernel(const float *rows, int B, float *stats, const int *
     }
 }
 
+// WT[l] = W[l]^T for every dense layer (layer l's [in, out] transpose at the
+// offset of its [out, in] weights)
+struct LayerTable {
+    int n;
+    long long off[2 * kMaxLayers];
+    int in[2 * kMaxLayers], out[2 * kMaxLayers];
+};
+
+__global__ void transpose_weights_kernel(const float *w, float *wt, LayerTable lt)
+{
+    for (int l = 0; l < lt.n; ++l) {
+        const long long n = (long long)lt.in[l] * lt.out[l];
+        const float *src = w + lt.off[l];
+        float *dst = wt + lt.off[l];
+        for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n;
+             e += (long long)gridDim.x * blockDim.x) {
+            const long long o = e / lt.in[l], j = e - o * lt.in[l];
+            dst[j * lt.out[l] + o] = src[e];
+        }
+    }
+}
+
+// row `row` of a [rows, ld] buffer set to 1 (the ones row of a transposed input)
+__global__ void ones_row_kernel(float *buf, int row, int ld)
+{
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < ld; c += gridDim.x * blockDim.x)
+        buf[(size_t)row * ld + c] = 1.f;
+}
+
 // the end of a step: the next step's slice and Adam count
 __global__ void advance_kernel(int *step_k, long long *step_t)
 {
@@ -290,15 +298,19 @@ __global__ void advance_kernel(int *step_k, long long *step_t)
 
 // ------------------------------------------------------------------ host side
 
-int grid_for(size_t total, int threads)
-{
-    const size_t b = (total + threads - 1) / threads;
-    return (int)(b < 4096 ? b : 4096);
-}
-
 void free_batch(ppo_trainer *t)
 {
     cudaFree(t->d_x);
+    cudaFree(t->d_xt);
+    t->d_xt = nullptr;
+    for (auto &net : t->d_actt)
+        for (float *&p : net) {
+            cudaFree(p);
+            p = nullptr;
+        }
+    cudaFree(t->d_dat);
+    cudaFree(t->d_dbt);
+    t->d_dat = t->d_dbt = nullptr;
     cudaFree(t->d_a);
     cudaFree(t->d_lpo);
     cudaFree(t->d_adv);
@@ -332,12 +344,26 @@ int ensure_batch(ppo_trainer *t, int B)
     ALLOC(t->d_lpo, (size_t)B * 4);
     ALLOC(t->d_adv, (size_t)B * 4);
     ALLOC(t->d_ret, (size_t)B * 4);
+    ALLOC(t->d_xt, (size_t)(kState + 1) * B * 4);
     for (int k = 0; k < 2; ++k)
-        for (int l = 0; l < t->net[k].n; ++l) ALLOC(t->d_act[k][l], (size_t)B * t->net[k].out[l] * 4);
+        for (int l = 0; l < t->net[k].n; ++l) {
+            ALLOC(t->d_act[k][l], (size_t)B * t->net[k].out[l] * 4);
+            ALLOC(t->d_actt[k][l], (size_t)(t->net[k].out[l] + 1) * B * 4);
+        }
     ALLOC(t->d_da, (size_t)B * kMaxWidth * 4);
     ALLOC(t->d_db, (size_t)B * kMaxWidth * 4);
+    ALLOC(t->d_dat, (size_t)B * kMaxWidth * 4);
+    ALLOC(t->d_dbt, (size_t)B * kMaxWidth * 4);
     ALLOC(t->d_rows, (size_t)4 * B * 4);
 #undef ALLOC
+    // the ones rows of the transposed layer inputs (their bias-gradient column)
+    ones_row_kernel<<<1, 256>>>(t->d_xt, kState, B);
+    for (int k = 0; k < 2; ++k)
+        for (int l = 0; l < t->net[k].n; ++l) ones_row_kernel<<<1, 256>>>(t->d_actt[k][l], t->net[k].out[l], B);
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+        free_batch(t);
+        return cuda_err(e, "mini-batch set-up");
+    }
     t->cap = B;
     return ROLLOUT_OK;
 }
@@ -354,70 +380,111 @@ void free_trainer(ppo_trainer *t)
     cudaFree(t->d_status);
     cudaFree(t->d_k);
     cudaFree(t->d_t);
+    cudaFree(t->d_wt);
     if (t->exec) cudaGraphExecDestroy(t->exec);
-    if (t->blas) cublasDestroy(t->blas);
-    cudaFree(t->d_ws);
     if (t->cap_stream) cudaStreamDestroy(t->cap_stream);
     delete t;
 }
 
-const float kOne = 1.f, kZero = 0.f;
-
-// Y[B, out] = X[B, in] W^T (row-major; W is [out, in])
-cublasStatus_t gemm_fwd(cublasHandle_t h, const float *W, const float *X, float *Y, int B, int in, int out)
+int gemm(const GemmArgs &g, cudaStream_t s, const char *what)
 {
-    return cublasSgemm(h, CUBLAS_OP_T, CUBLAS_OP_N, out, B, in, &kOne, W, in, X, in, &kZero, Y, out);
+    cudaError_t e = launch_gemm_split(g, s);
+    return e == cudaSuccess ? ROLLOUT_OK : cuda_err(e, what);
 }
 
-// dW[out, in] = dY[B, out]^T X[B, in]
-cublasStatus_t gemm_dw(cublasHandle_t h, const float *X, const float *dY, float *dW, int B, int in, int out)
-{
-    return cublasSgemm(h, CUBLAS_OP_N, CUBLAS_OP_T, in, out, B, &kOne, X, in, dY, out, &kZero, dW, in);
-}
-
-// dX[B, in] = dY[B, out] W[out, in]
-cublasStatus_t gemm_dx(cublasHandle_t h, const float *W, const float *dY, float *dX, int B, int in, int out)
-{
-    return cublasSgemm(h, CUBLAS_OP_N, CUBLAS_OP_N, in, B, out, &kOne, W, in, dY, out, &kZero, dX, in);
-}
-
-// forward of net k over the mini-batch (outputs in d_act[k][*])
+// forward of net k over the mini-batch: layer l's output in d_act[k][l] and
+// (hidden layers) its transpose in d_actt[k][l]
 int forward(ppo_trainer *t, int k, int B, cudaStream_t s)
 {
     const Net &n = t->net[k];
     const float *in = t->d_x;
     for (int l = 0; l < n.n; ++l) {
-        cublasStatus_t st = gemm_fwd(t->blas, t->d_w + n.w[l], in, t->d_act[k][l], B, n.in[l], n.out[l]);
-        if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "forward GEMM");
-        const size_t total = (size_t)B * n.out[l];
-        bias_act_kernel<<<grid_for(total, 256), 256, 0, s>>>(t->d_act[k][l], t->d_w + n.b[l], B, n.out[l],
-                                                             l < n.n - 1);
+        GemmArgs g;
+        g.A = in;
+        g.lda = n.in[l];
+        g.B = t->d_w + n.w[l];                           // [out, in]
+        g.ldb = n.in[l];
+        g.M = B;
+        g.N = n.out[l];
+        g.K = n.in[l];
+        g.epi = kGemmFwd;
+        g.bias = t->d_w + n.b[l];
+        g.relu = l < n.n - 1;
+        g.Y = t->d_act[k][l];
+        g.ldy = n.out[l];
+        g.YT = l < n.n - 1 ? t->d_actt[k][l] : nullptr;
+        g.ldt = t->cap;
+        g.status = t->d_status;
+        int rc = gemm(g, s, "forward product");
+        if (rc) return rc;
         in = t->d_act[k][l];
     }
     return ROLLOUT_OK;
 }
 
-// backward of net k from the gradient at its output (in d_da), into d_g
+// backward of net k from the gradient at its output (d_da, its transpose in
+// d_dat), into d_g: per layer the weight and bias gradient dY^T [X | 1] and,
+// below the first layer, the input gradient dY W masked by ReLU'
 int backward(ppo_trainer *t, int k, int B, cudaStream_t s)
 {
     const Net &n = t->net[k];
-    float *dy = t->d_da, *dx = t->d_db;
+    float *dy = t->d_da, *dyt = t->d_dat, *dx = t->d_db, *dxt = t->d_dbt;
     for (int l = n.n - 1; l >= 0; --l) {
-        const float *in = l == 0 ? t->d_x : t->d_act[k][l - 1];
-        cublasStatus_t st = gemm_dw(t->blas, in, dy, t->d_g + n.w[l], B, n.in[l], n.out[l]);
-        if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "weight-gradient GEMM");
-        bias_grad_kernel<<<(n.out[l] + kBgCols - 1) / kBgCols, kBgCols * kBgGroups, 0, s>>>(dy, B, n.out[l],
-                                                                                          t->d_g + n.b[l]);
+        GemmArgs g;
+        g.A = dyt;                                       // [out, B]
+        g.lda = t->cap;
+        g.B = l == 0 ? t->d_xt : t->d_actt[k][l - 1];    // [in + 1, B], the last row ones
+        g.ldb = t->cap;
+        g.M = n.out[l];
+        g.N = n.in[l] + 1;
+        g.K = B;
+        g.epi = kGemmDw;
+        g.Y = t->d_g + n.w[l];
+        g.ldy = n.in[l];
+        g.nw = n.in[l];
+        g.db = t->d_g + n.b[l];
+        g.status = t->d_status;
+        int rc = gemm(g, s, "weight-gradient product");
+        if (rc) return rc;
         if (l == 0) break;
-        st = gemm_dx(t->blas, t->d_w + n.w[l], dy, dx, B, n.in[l], n.out[l]);
-        if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "input-gradient GEMM");
-        const size_t total = (size_t)B * n.in[l];
-        relu_back_kernel<<<grid_for(total, 256), 256, 0, s>>>(dx, t->d_act[k][l - 1], total);
+        GemmArgs x;
+        x.A = dy;                                        // [B, out]
+        x.lda = n.out[l];
+        x.B = t->d_wt + n.w[l];                          // W^T [in, out]
+        x.ldb = n.out[l];
+        x.M = B;
+        x.N = n.in[l];
+        x.K = n.out[l];
+        x.epi = kGemmDx;
+        x.H = t->d_act[k][l - 1];
+        x.ldh = n.in[l];
+        x.Y = dx;
+        x.ldy = n.in[l];
+        x.YT = dxt;
+        x.ldt = t->cap;
+        x.status = t->d_status;
+        if ((rc = gemm(x, s, "input-gradient product"))) return rc;
         float *tmp = dy;
         dy = dx;
         dx = tmp;
+        tmp = dyt;
+        dyt = dxt;
+        dxt = tmp;
     }
     return ROLLOUT_OK;
+}
+
+LayerTable layer_table(const ppo_trainer *t)
+{
+    LayerTable lt{};
+    for (int k = 0; k < 2; ++k)
+        for (int l = 0; l < t->net[k].n; ++l) {
+            lt.off[lt.n] = (long long)t->net[k].w[l];
+            lt.in[lt.n] = t->net[k].in[l];
+            lt.out[lt.n] = t->net[k].out[l];
+            ++lt.n;
+        }
+    return lt;
 }
 
 int check_update_args(ppo_trainer *t, const float *states, const int32_t *actions, const float *logp_old,
@@ -450,17 +517,18 @@ int loss_gradient(ppo_trainer *t, const float *states, const int32_t *actions, c
                   cudaStream_t s)
 {
     int rc;
-    gather_kernel<<<B, 64, 0, s>>>(states, actions, logp_old, adv, ret, T, rows, t->d_k, t->d_x, t->d_a, t->d_lpo,
-                                   t->d_adv, t->d_ret, t->d_status);
+    t->last_batch = B;
+    gather_kernel<<<B, 64, 0, s>>>(states, actions, logp_old, adv, ret, T, rows, t->d_k, t->d_x, t->d_xt, t->cap,
+                                   t->d_a, t->d_lpo, t->d_adv, t->d_ret, t->d_status);
     // actor: log-probs, surrogate, its gradient
     if ((rc = forward(t, 0, B, s))) return rc;
     actor_head_kernel<<<(B * 32 + 255) / 256, 256, 0, s>>>(t->d_act[0][2], t->d_a, t->d_lpo, t->d_adv, B,
-                                                           hp->clip_eps, t->d_da, t->d_rows);
+                                                           hp->clip_eps, t->d_da, t->d_dat, t->cap, t->d_rows);
     if ((rc = backward(t, 0, B, s))) return rc;
     // critic: squared error, its gradient
     if ((rc = forward(t, 1, B, s))) return rc;
     critic_head_kernel<<<(B + 255) / 256, 256, 0, s>>>(t->d_act[1][kCriticLayers - 1], t->d_ret, B, hp->value_coef,
-                                                       t->d_da, t->d_rows);
+                                                       t->d_da, t->d_dat, t->d_rows);
     return backward(t, 1, B, s);
 }
 
@@ -469,13 +537,12 @@ int step(ppo_trainer *t, const float *states, const int32_t *actions, const floa
          const float *ret, long long T, const int32_t *indices, int B, const ppo_hparams *hp, float *stats,
          cudaStream_t s)
 {
-    cublasStatus_t st = cublasSetStream(t->blas, s);
-    if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "cublasSetStream");
     int rc = loss_gradient(t, states, actions, logp_old, adv, ret, T, indices, B, hp, s);
     if (rc) return rc;
     norm_partial_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_g, t->n_trained, t->d_part);
     adam_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_w, t->d_g, t->d_m, t->d_v, t->n_trained, t->d_part, *hp,
                                                      t->d_t, t->d_k, stats);
+    transpose_weights_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_w, t->d_wt, layer_table(t));
     if (stats) stats_kernel<<<1, 256, 0, s>>>(t->d_rows, B, stats, t->d_k);
     advance_kernel<<<1, 1, 0, s>>>(t->d_k, t->d_t);
     cudaError_t e = cudaGetLastError();
@@ -559,7 +626,7 @@ int ppo_create(const float *weights, const rollout_dims *dims, ppo_trainer **out
         (e = cudaMalloc(&t->d_status, sizeof(int))) != cudaSuccess ||
         (e = cudaMalloc(&t->d_k, sizeof(int))) != cudaSuccess ||
         (e = cudaMalloc(&t->d_t, sizeof(long long))) != cudaSuccess ||
-        (e = cudaMalloc(&t->d_ws, kBlasWorkspace)) != cudaSuccess) {
+        (e = cudaMalloc(&t->d_wt, t->n_trained * 4)) != cudaSuccess) {
         free_trainer(t);
         return cuda_err(e, "cudaMalloc(trainer)");
     }
@@ -576,13 +643,10 @@ int ppo_create(const float *weights, const rollout_dims *dims, ppo_trainer **out
         free_trainer(t);
         return cuda_err(e, "trainer upload");
     }
-    cublasStatus_t st = cublasCreate(&t->blas);
-    if (st != CUBLAS_STATUS_SUCCESS) { free_trainer(t); return blas_err(st, "cublasCreate"); }
-    // float32 GEMMs: no TF32 or other reduced-precision math
-    if ((st = cublasSetMathMode(t->blas, CUBLAS_PEDANTIC_MATH)) != CUBLAS_STATUS_SUCCESS ||
-        (st = cublasSetWorkspace(t->blas, t->d_ws, kBlasWorkspace)) != CUBLAS_STATUS_SUCCESS) {
+    transpose_weights_kernel<<<kNormBlocks, kNormThreads>>>(t->d_w, t->d_wt, layer_table(t));
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
         free_trainer(t);
-        return blas_err(st, "cuBLAS setup");
+        return cuda_err(e, "transposed weights");
     }
     *out = t;
     return ROLLOUT_OK;
@@ -629,8 +693,6 @@ int ppo_gradient(ppo_trainer *t, const float *states, const int32_t *actions, co
     if (rc) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     t->last_stream = s;
-    cublasStatus_t st = cublasSetStream(t->blas, s);
-    if (st != CUBLAS_STATUS_SUCCESS) return blas_err(st, "cublasSetStream");
     cudaError_t e = cudaMemsetAsync(t->d_k, 0, sizeof(int), s);
     if (e != cudaSuccess) return cuda_err(e, "cudaMemsetAsync(step index)");
     if ((rc = loss_gradient(t, states, actions, logp_old, adv, ret, T, indices, batch, hp, s))) return rc;
@@ -638,6 +700,27 @@ int ppo_gradient(ppo_trainer *t, const float *states, const int32_t *actions, co
     e = cudaMemcpyAsync(grad, t->d_g, t->n_trained * 4, cudaMemcpyDefault, s);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? ROLLOUT_OK : cuda_err(e, "PPO gradient");
+}
+
+int ppo_test_activations(ppo_trainer *t, float *act, void *stream)
+{
+    clear_error();
+    if (!t || !act) return set_error(ROLLOUT_ERR_INVALID, "null argument");
+    const int B = t->last_batch;
+    if (B <= 0) return set_error(ROLLOUT_ERR_INVALID, "no forward pass yet");
+    int width = 0;
+    for (int k = 0; k < 2; ++k)
+        for (int l = 0; l < t->net[k].n - 1; ++l) width += t->net[k].out[l];
+    int col = 0;
+    for (int k = 0; k < 2; ++k)
+        for (int l = 0; l < t->net[k].n - 1; ++l) {
+            const int o = t->net[k].out[l];
+            cudaError_t e = cudaMemcpy2DAsync(act + col, (size_t)width * 4, t->d_act[k][l], (size_t)o * 4,
+                                              (size_t)o * 4, (size_t)B, cudaMemcpyDefault, (cudaStream_t)stream);
+            if (e != cudaSuccess) return cuda_err(e, "cudaMemcpy2DAsync(activations)");
+            col += o;
+        }
+    return ROLLOUT_OK;
 }
 
 int ppo_get_weights(ppo_trainer *t, float *weights, void *stream)

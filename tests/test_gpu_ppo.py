@@ -49,9 +49,6 @@ def _layer_bounds(critic_h):
     return np.cumsum([0] + sizes)
 
 
-KINK_MARGIN = 1e-5   # ~10x the float32 error of these dot products, relative to sum |w x|
-
-
 def _teacher_forced(w, inp, g, idx, n_steps, B, hp_kw):
     """Runs the GPU trainer one step at a time and checks each step in two parts.
     (1) The gradient: ppo_gradient at the GPU's current weights against the oracle's
@@ -59,12 +56,11 @@ def _teacher_forced(w, inp, g, idx, n_steps, B, hp_kw):
     statistics.  (2) The optimizer: the oracle's clip + Adam fed the GPU's own gradient
     (its moments follow the same gradients) against the GPU's step, element by element.
     Comparing free-running trajectories instead would amplify float32-level gradient
-    differences: Adam normalises each element, and a ReLU mask that flips between
-    float32 and double shifts a row's contribution to every earlier layer.  For the same
-    reason each step's mini-batch takes, from the seeded order idx, the first B rows
-    whose hidden pre-activations all lie farther from the ReLU kink than float32 error
-    at the current weights (at the kink both sides are right, like an action drawn
-    within rounding of a CDF boundary)."""
+    differences: Adam normalises each element.  Each step takes the next B rows of the
+    seeded order idx, unfiltered; where a hidden pre-activation lies within the float32
+    products' error of the ReLU kink, the oracle adopts the side the GPU took (a replay,
+    like an action drawn within rounding of a CDF boundary) and any other difference
+    fails the step."""
     import torch
     from rl_experience_collection_gb300 import binding
     from oracle import ppo
@@ -79,25 +75,25 @@ def _teacher_forced(w, inp, g, idx, n_steps, B, hp_kw):
     v = np.zeros(N_TRAINED)
     w_prev = inp.weights.astype(np.float32)
     grad_dev = torch.zeros(N_TRAINED, dtype=torch.float32, device="cuda")
-    used = np.zeros(len(idx), dtype=bool)
+    replays = 0
     for k in range(n_steps):
-        margin = ppo.kink_margin(w_prev[:N_TRAINED].astype(np.float64), shape, b, idx)
-        pick = np.flatnonzero((margin >= KINK_MARGIN) & ~used)[:B]
-        assert len(pick) == B, "not enough rows away from the ReLU kink"
-        used[pick] = True
-        rows = np.ascontiguousarray(idx[pick])
+        rows = np.ascontiguousarray(idx[k * B:(k + 1) * B])
+        assert len(rows) == B
         rows_dev = torch.from_numpy(rows).cuda()
         st_g = torch.zeros(4, dtype=torch.float32, device="cuda")
         tr.gradient(states, actions, logp, adv, ret, rows_dev, B, grad_dev, st_g, hp_g)
+        act = tr.activations(B)
         st_dev = torch.zeros((1, 5), dtype=torch.float32, device="cuda")
         tr.update(states, actions, logp, adv, ret, rows_dev, 1, B, hp_g, st_dev)
         w_gpu = tr.weights()
         g_gpu = grad_dev.cpu().numpy().astype(np.float64)
         st_gpu = st_dev.cpu().numpy()[0]
         np.testing.assert_array_equal(st_g.cpu().numpy(), st_gpu[:4])
-        # (1) gradient and statistics at the same weights
+        # (1) gradient and statistics at the same weights, the GPU's ReLU sides replayed
         p = w_prev[:N_TRAINED].astype(np.float64)
-        st_o, g_o = ppo.loss_grad(p, shape, hp_o, b, rows)
+        st_o, g_o, rep, mis = ppo.loss_grad_replay(p, shape, hp_o, b, rows, act)
+        assert mis == 0, (k, mis, "ReLU sides differ beyond the products' float32 error")
+        replays += rep
         for lo, hi in zip(bounds[:-1], bounds[1:]):
             ref = np.linalg.norm(g_o[lo:hi])
             assert np.linalg.norm(g_gpu[lo:hi] - g_o[lo:hi]) <= 1e-3 * ref + 1e-9, (k, lo, hi)
@@ -119,6 +115,7 @@ def _teacher_forced(w, inp, g, idx, n_steps, B, hp_kw):
         w_prev = w_gpu
     assert tr.status() == binding.ROLLOUT_OK
     tr.close()
+    print("ReLU replays", replays)
 
 
 def test_update_matches_oracle_small_batches(tuples):

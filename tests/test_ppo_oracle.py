@@ -190,3 +190,70 @@ def test_trainer_update_runs_steps_in_order(setup):
     np.testing.assert_array_equal(tr.w[:n], p.astype(np.float32))
     np.testing.assert_array_equal(tr.w[n:], inp.weights[n:])    # curiosity untouched
     assert tr.t.value == 2
+
+
+# ------------------------------------------------------------------ ReLU-decision replay
+
+def _hidden(p, w, b, rows):
+    """The hidden activations of actor and critic, computed here in float64 with
+    numpy from the packed layout: [rows, actor hidden | critic hidden]."""
+    views = wl.weight_views(np.concatenate([p, np.zeros(wl.n_params(w.critic_h) - p.size)]).astype(np.float64),
+                            w.critic_h)
+    out = []
+    for r in rows:
+        x = b.states[r].astype(np.float64)
+        parts = []
+        for names in (["actor0", "actor1"], [f"critic{i}" for i in range(len(w.critic_h))]):
+            h = x
+            for nm in names:
+                h = np.maximum(views[nm + ".w"] @ h + views[nm + ".b"], 0.0)
+                parts.append(h)
+        out.append(np.concatenate(parts))
+    return np.array(out, dtype=np.float32)
+
+
+def test_relu_replay_on_own_activations_changes_nothing(setup):
+    w, inp = setup
+    shape = ppo.shape_of(w.critic_h)
+    n = ppo.trained_count(shape)
+    b, _ = _batch(w, inp, 8, seed=21)
+    rows = np.arange(8, dtype=np.int32)
+    hp = ppo.Hyper()
+    p = inp.weights[:n].astype(np.float64)
+    st0, g0 = ppo.loss_grad(p, shape, hp, b, rows)
+    act = _hidden(p, w, b, rows)
+    assert act.shape == (8, 128 + 64 + sum(w.critic_h))
+    st1, g1, rep, mis = ppo.loss_grad_replay(p, shape, hp, b, rows, act)
+    assert rep == 0 and mis == 0
+    # only the float32 rounding of the adopted activation values separates them
+    np.testing.assert_allclose(g1, g0, rtol=0, atol=1e-6 * np.abs(g0).max())
+    np.testing.assert_allclose(st1, st0, rtol=1e-6)
+
+
+def test_relu_replay_adopts_a_kink_decision_and_flags_a_far_one(setup):
+    w, inp = setup
+    shape = ppo.shape_of(w.critic_h)
+    n = ppo.trained_count(shape)
+    b, _ = _batch(w, inp, 4, seed=22)
+    rows = np.arange(4, dtype=np.int32)
+    hp = ppo.Hyper()
+    p = inp.weights[:n].astype(np.float64)
+    # put the pre-activation of critic unit 5 (first layer) exactly at the kink on row 0
+    views = wl.weight_views(inp.weights.copy(), w.critic_h)
+    c0 = sum(o * i + o for _, (o, i) in wl.layer_shapes(w.critic_h)[:3])      # offset of the critic's first matrix
+    W0 = views["critic0.w"].astype(np.float64)
+    x0 = b.states[0].astype(np.float64)
+    p[c0 + W0.size + 5] = -float(W0[5] @ x0)                                    # its bias
+    act = _hidden(p, w, b, rows)
+    col = 128 + 64 + 5
+    # the path put it on the positive side, by float32 error: a replay
+    act_pos = act.copy()
+    act_pos[0, col] = np.float32(1e-7)
+    _, g_rep, rep, mis = ppo.loss_grad_replay(p, shape, hp, b, rows, act_pos)
+    assert mis == 0 and rep >= 1
+    # the same activation on the other side, far from the kink: a mismatch
+    r1 = 1 if act[1, col] > 0.1 else 2
+    act_far = act.copy()
+    act_far[r1, col] = 0.0 if act[r1, col] > 0 else 0.5
+    _, _, rep2, mis2 = ppo.loss_grad_replay(p, shape, hp, b, rows, act_far)
+    assert mis2 >= 1
