@@ -82,8 +82,12 @@ struct ppo_trainer {
     float *d_xt = nullptr;             // [kState + 1, cap]: x^T and a row of ones
     float *d_act[2][kMaxLayers] = {};  // layer outputs [cap, out]
     float *d_actt[2][kMaxLayers] = {}; // their transposes [out + 1, cap], the last row ones
-    float *d_da = nullptr, *d_db = nullptr;   // backpropagated gradients [cap, kMaxWidth]
-    float *d_dat = nullptr, *d_dbt = nullptr; // their transposes [kMaxWidth, cap]
+    float *d_dy[2][2] = {};            // per net, backpropagated gradients (ping-pong) [cap, kMaxWidth]
+    float *d_dyt[2][2] = {};           // their transposes [kMaxWidth, cap]
+    float *d_ws = nullptr;             // split-K partial tiles of the products of one stage
+    unsigned int *d_cnt = nullptr;     // their per-tile arrival counters (zero between launches)
+    long long ws_floats = 0;
+    int n_cnt = 0;
     float *d_wt = nullptr;             // transposed weights: layer l's [in, out] at its offset
     float *d_rows = nullptr;           // per-row statistics [4][cap]
     double *d_part = nullptr;          // [kNormBlocks] partial sums of g^2
@@ -221,13 +225,17 @@ __global__ void __launch_bounds__(kNormThreads) adam_kernel(float *p, const floa
                                                              const int *step_k, float *stats)
 {
     __shared__ float sh_scale, sh_bc1, sh_bc2;
+    __shared__ double sh[kNormThreads];
+    // every block adds the partials in the same fixed order (a strided
+    // per-thread sum, then the tree of block_sum), so all see the same norm
+    double ps = 0.0;
+    for (int b = threadIdx.x; b < kNormBlocks; b += kNormThreads) ps += part[b];
+    const double ss = block_sum(ps, sh);
     if (threadIdx.x == 0) {
         const double t = (double)(*step_t + 1);
         sh_bc1 = (float)(1.0 - pow((double)hp.beta1, t));
         sh_bc2 = (float)(1.0 - pow((double)hp.beta2, t));
         float *norm_out = stats ? stats + (size_t)*step_k * 5 + 4 : nullptr;
-        double ss = 0.0;
-        for (int b = 0; b < kNormBlocks; ++b) ss += part[b];
         const double norm = sqrt(ss);
         double scale = 1.0;
         if (hp.max_grad_norm > 0.f) scale = fmin(1.0, (double)hp.max_grad_norm / (norm + 1e-6));
@@ -308,9 +316,16 @@ void free_batch(ppo_trainer *t)
             cudaFree(p);
             p = nullptr;
         }
-    cudaFree(t->d_dat);
-    cudaFree(t->d_dbt);
-    t->d_dat = t->d_dbt = nullptr;
+    for (int k = 0; k < 2; ++k)
+        for (int i = 0; i < 2; ++i) {
+            cudaFree(t->d_dy[k][i]);
+            cudaFree(t->d_dyt[k][i]);
+            t->d_dy[k][i] = t->d_dyt[k][i] = nullptr;
+        }
+    cudaFree(t->d_ws);
+    cudaFree(t->d_cnt);
+    t->d_ws = nullptr;
+    t->d_cnt = nullptr;
     cudaFree(t->d_a);
     cudaFree(t->d_lpo);
     cudaFree(t->d_adv);
@@ -320,14 +335,14 @@ void free_batch(ppo_trainer *t)
             cudaFree(p);
             p = nullptr;
         }
-    cudaFree(t->d_da);
-    cudaFree(t->d_db);
     cudaFree(t->d_rows);
     t->d_x = nullptr;
     t->d_a = nullptr;
-    t->d_lpo = t->d_adv = t->d_ret = t->d_da = t->d_db = t->d_rows = nullptr;
+    t->d_lpo = t->d_adv = t->d_ret = t->d_rows = nullptr;
     t->cap = 0;
 }
+
+void plan_workspace(ppo_trainer *t, int B);
 
 int ensure_batch(ppo_trainer *t, int B)
 {
@@ -350,12 +365,21 @@ int ensure_batch(ppo_trainer *t, int B)
             ALLOC(t->d_act[k][l], (size_t)B * t->net[k].out[l] * 4);
             ALLOC(t->d_actt[k][l], (size_t)(t->net[k].out[l] + 1) * B * 4);
         }
-    ALLOC(t->d_da, (size_t)B * kMaxWidth * 4);
-    ALLOC(t->d_db, (size_t)B * kMaxWidth * 4);
-    ALLOC(t->d_dat, (size_t)B * kMaxWidth * 4);
-    ALLOC(t->d_dbt, (size_t)B * kMaxWidth * 4);
+    for (int k = 0; k < 2; ++k)
+        for (int i = 0; i < 2; ++i) {
+            ALLOC(t->d_dy[k][i], (size_t)B * kMaxWidth * 4);
+            ALLOC(t->d_dyt[k][i], (size_t)B * kMaxWidth * 4);
+        }
     ALLOC(t->d_rows, (size_t)4 * B * 4);
+    t->cap = B;
+    plan_workspace(t, B);
+    ALLOC(t->d_ws, (size_t)(t->ws_floats > 0 ? t->ws_floats : 4) * 4);
+    ALLOC(t->d_cnt, (size_t)(t->n_cnt > 0 ? t->n_cnt : 1) * 4);
 #undef ALLOC
+    if ((e = cudaMemset(t->d_cnt, 0, (size_t)(t->n_cnt > 0 ? t->n_cnt : 1) * 4)) != cudaSuccess) {
+        free_batch(t);
+        return cuda_err(e, "cudaMemset(counters)");
+    }
     // the ones rows of the transposed layer inputs (their bias-gradient column)
     ones_row_kernel<<<1, 256>>>(t->d_xt, kState, B);
     for (int k = 0; k < 2; ++k)
@@ -364,7 +388,6 @@ int ensure_batch(ppo_trainer *t, int B)
         free_batch(t);
         return cuda_err(e, "mini-batch set-up");
     }
-    t->cap = B;
     return ROLLOUT_OK;
 }
 
@@ -386,92 +409,144 @@ void free_trainer(ppo_trainer *t)
     delete t;
 }
 
-int gemm(const GemmArgs &g, cudaStream_t s, const char *what)
-{
-    cudaError_t e = launch_gemm_split(g, s);
-    return e == cudaSuccess ? ROLLOUT_OK : cuda_err(e, what);
-}
+constexpr int kMaxSplit = 4;        // CTAs a product's K may be split over
+constexpr int kStages = 2 * kMaxLayers;
 
-// forward of net k over the mini-batch: layer l's output in d_act[k][l] and
-// (hidden layers) its transpose in d_actt[k][l]
-int forward(ppo_trainer *t, int k, int B, cudaStream_t s)
+// the forward product of net k's layer l over B rows
+GemmArgs fwd_args(ppo_trainer *t, int k, int l, int B)
 {
     const Net &n = t->net[k];
-    const float *in = t->d_x;
-    for (int l = 0; l < n.n; ++l) {
-        GemmArgs g;
-        g.A = in;
-        g.lda = n.in[l];
-        g.B = t->d_w + n.w[l];                           // [out, in]
-        g.ldb = n.in[l];
-        g.M = B;
-        g.N = n.out[l];
-        g.K = n.in[l];
-        g.epi = kGemmFwd;
-        g.bias = t->d_w + n.b[l];
-        g.relu = l < n.n - 1;
-        g.Y = t->d_act[k][l];
-        g.ldy = n.out[l];
-        g.YT = l < n.n - 1 ? t->d_actt[k][l] : nullptr;
-        g.ldt = t->cap;
-        g.status = t->d_status;
-        int rc = gemm(g, s, "forward product");
-        if (rc) return rc;
-        in = t->d_act[k][l];
-    }
-    return ROLLOUT_OK;
+    GemmArgs g;
+    g.A = l == 0 ? t->d_x : t->d_act[k][l - 1];
+    g.lda = n.in[l];
+    g.B = t->d_w + n.w[l];                           // [out, in]
+    g.ldb = n.in[l];
+    g.M = B;
+    g.N = n.out[l];
+    g.K = n.in[l];
+    g.epi = kGemmFwd;
+    g.bias = t->d_w + n.b[l];
+    g.relu = l < n.n - 1;
+    g.Y = t->d_act[k][l];
+    g.ldy = n.out[l];
+    g.YT = l < n.n - 1 ? t->d_actt[k][l] : nullptr;
+    g.ldt = t->cap;
+    g.status = t->d_status;
+    return g;
 }
 
-// backward of net k from the gradient at its output (d_da, its transpose in
-// d_dat), into d_g: per layer the weight and bias gradient dY^T [X | 1] and,
-// below the first layer, the input gradient dY W masked by ReLU'
-int backward(ppo_trainer *t, int k, int B, cudaStream_t s)
+// the weight- and bias-gradient product dY^T [X | 1] of net k's layer l; dY^T
+// is d_dyt[k][p]
+GemmArgs dw_args(ppo_trainer *t, int k, int l, int p, int B)
 {
     const Net &n = t->net[k];
-    float *dy = t->d_da, *dyt = t->d_dat, *dx = t->d_db, *dxt = t->d_dbt;
-    for (int l = n.n - 1; l >= 0; --l) {
-        GemmArgs g;
-        g.A = dyt;                                       // [out, B]
-        g.lda = t->cap;
-        g.B = l == 0 ? t->d_xt : t->d_actt[k][l - 1];    // [in + 1, B], the last row ones
-        g.ldb = t->cap;
-        g.M = n.out[l];
-        g.N = n.in[l] + 1;
-        g.K = B;
-        g.epi = kGemmDw;
-        g.Y = t->d_g + n.w[l];
-        g.ldy = n.in[l];
-        g.nw = n.in[l];
-        g.db = t->d_g + n.b[l];
-        g.status = t->d_status;
-        int rc = gemm(g, s, "weight-gradient product");
-        if (rc) return rc;
-        if (l == 0) break;
-        GemmArgs x;
-        x.A = dy;                                        // [B, out]
-        x.lda = n.out[l];
-        x.B = t->d_wt + n.w[l];                          // W^T [in, out]
-        x.ldb = n.out[l];
-        x.M = B;
-        x.N = n.in[l];
-        x.K = n.out[l];
-        x.epi = kGemmDx;
-        x.H = t->d_act[k][l - 1];
-        x.ldh = n.in[l];
-        x.Y = dx;
-        x.ldy = n.in[l];
-        x.YT = dxt;
-        x.ldt = t->cap;
-        x.status = t->d_status;
-        if ((rc = gemm(x, s, "input-gradient product"))) return rc;
-        float *tmp = dy;
-        dy = dx;
-        dx = tmp;
-        tmp = dyt;
-        dyt = dxt;
-        dxt = tmp;
+    GemmArgs g;
+    g.A = t->d_dyt[k][p];                            // [out, B]
+    g.lda = t->cap;
+    g.B = l == 0 ? t->d_xt : t->d_actt[k][l - 1];    // [in + 1, B], the last row ones
+    g.ldb = t->cap;
+    g.M = n.out[l];
+    g.N = n.in[l] + 1;
+    g.K = B;
+    g.epi = kGemmDw;
+    g.Y = t->d_g + n.w[l];
+    g.ldy = n.in[l];
+    g.nw = n.in[l];
+    g.db = t->d_g + n.b[l];
+    g.status = t->d_status;
+    return g;
+}
+
+// the input-gradient product dY W masked by ReLU' of net k's layer l (l > 0):
+// dY = d_dy[k][p], the result into d_dy[k][1 - p] and its transpose
+GemmArgs dx_args(ppo_trainer *t, int k, int l, int p, int B)
+{
+    const Net &n = t->net[k];
+    GemmArgs x;
+    x.A = t->d_dy[k][p];                             // [B, out]
+    x.lda = n.out[l];
+    x.B = t->d_wt + n.w[l];                          // W^T [in, out]
+    x.ldb = n.out[l];
+    x.M = B;
+    x.N = n.in[l];
+    x.K = n.out[l];
+    x.epi = kGemmDx;
+    x.H = t->d_act[k][l - 1];
+    x.ldh = n.in[l];
+    x.Y = t->d_dy[k][1 - p];
+    x.ldy = n.in[l];
+    x.YT = t->d_dyt[k][1 - p];
+    x.ldt = t->cap;
+    x.status = t->d_status;
+    return x;
+}
+
+// the products of stage j of a step, all independent of one another:
+// j < kMaxLayers: the forward products of depth j of both nets; after that the
+// backward products of depth j - kMaxLayers from the top of each net (its
+// weight gradient and, below the first layer, its input gradient)
+int stage_products(ppo_trainer *t, int j, int B, GemmArgs *g)
+{
+    int n = 0;
+    for (int k = 0; k < 2; ++k) {
+        const int L = t->net[k].n;
+        if (j < kMaxLayers) {
+            if (j < L) g[n++] = fwd_args(t, k, j, B);
+        } else {
+            const int d = j - kMaxLayers, l = L - 1 - d;
+            if (l < 0) continue;
+            g[n++] = dw_args(t, k, l, d & 1, B);
+            if (l > 0) g[n++] = dx_args(t, k, l, d & 1, B);
+        }
     }
-    return ROLLOUT_OK;
+    return n;
+}
+
+// split-K plans of a stage's products and their workspace regions (ws / cnt
+// may be null when only the sizes are wanted)
+void plan_stage(GemmArgs *g, int n, float *ws, unsigned int *cnt, long long *ws_floats, int *n_cnt)
+{
+    long long wo = 0;
+    int co = 0;
+    for (int i = 0; i < n; ++i) {
+        long long wf;
+        int c;
+        gemm_plan(g[i], kMaxSplit, &wf, &c);
+        g[i].ws = ws ? ws + wo : nullptr;
+        g[i].cnt = cnt ? cnt + co : nullptr;
+        wo += wf;
+        co += c;
+    }
+    *ws_floats = wo;
+    *n_cnt = co;
+}
+
+void plan_workspace(ppo_trainer *t, int B)
+{
+    t->ws_floats = 0;
+    t->n_cnt = 0;
+    for (int j = 0; j < kStages; ++j) {
+        GemmArgs g[kGemmGroup];
+        const int n = stage_products(t, j, B, g);
+        if (n == 0) continue;
+        long long wf;
+        int c;
+        plan_stage(g, n, nullptr, nullptr, &wf, &c);
+        if (wf > t->ws_floats) t->ws_floats = wf;
+        if (c > t->n_cnt) t->n_cnt = c;
+    }
+}
+
+int run_stage(ppo_trainer *t, int j, int B, cudaStream_t s)
+{
+    GemmArgs g[kGemmGroup];
+    const int n = stage_products(t, j, B, g);
+    if (n == 0) return ROLLOUT_OK;
+    long long wf;
+    int c;
+    plan_stage(g, n, t->d_ws, t->d_cnt, &wf, &c);
+    cudaError_t e = launch_gemm_group(g, n, s);
+    return e == cudaSuccess ? ROLLOUT_OK : cuda_err(e, "tensor-core product");
 }
 
 LayerTable layer_table(const ppo_trainer *t)
@@ -520,16 +595,20 @@ int loss_gradient(ppo_trainer *t, const float *states, const int32_t *actions, c
     t->last_batch = B;
     gather_kernel<<<B, 64, 0, s>>>(states, actions, logp_old, adv, ret, T, rows, t->d_k, t->d_x, t->d_xt, t->cap,
                                    t->d_a, t->d_lpo, t->d_adv, t->d_ret, t->d_status);
-    // actor: log-probs, surrogate, its gradient
-    if ((rc = forward(t, 0, B, s))) return rc;
+    // forward products of both nets, depth by depth
+    for (int j = 0; j < kMaxLayers; ++j)
+        if ((rc = run_stage(t, j, B, s))) return rc;
+    // the two loss heads: the actor's surrogate and the critic's squared error,
+    // each with its gradient at the net's output (and that gradient's transpose)
     actor_head_kernel<<<(B * 32 + 255) / 256, 256, 0, s>>>(t->d_act[0][2], t->d_a, t->d_lpo, t->d_adv, B,
-                                                           hp->clip_eps, t->d_da, t->d_dat, t->cap, t->d_rows);
-    if ((rc = backward(t, 0, B, s))) return rc;
-    // critic: squared error, its gradient
-    if ((rc = forward(t, 1, B, s))) return rc;
+                                                           hp->clip_eps, t->d_dy[0][0], t->d_dyt[0][0], t->cap,
+                                                           t->d_rows);
     critic_head_kernel<<<(B + 255) / 256, 256, 0, s>>>(t->d_act[1][kCriticLayers - 1], t->d_ret, B, hp->value_coef,
-                                                       t->d_da, t->d_dat, t->d_rows);
-    return backward(t, 1, B, s);
+                                                       t->d_dy[1][0], t->d_dyt[1][0], t->d_rows);
+    // backward products of both nets, depth by depth from the top
+    for (int j = kMaxLayers; j < kStages; ++j)
+        if ((rc = run_stage(t, j, B, s))) return rc;
+    return ROLLOUT_OK;
 }
 
 // one optimizer step (the counters pick the mini-batch, the statistics slot and t)

@@ -16,16 +16,23 @@
 // product, far inside the update's parity tolerances, so the float32 oracle
 // stays the reference.
 //
-// One CTA computes a 128 x 128 tile of C: its 128 threads load the tile's
-// K-chunks of A and B (64 elements each, zero outside the matrices), split
-// them into swizzled bf16 operand tiles in shared memory (two stages, so that
-// loading chunk c + 1 overlaps the MMAs of chunk c), one thread issues the
-// MMAs, and after the last chunk each thread takes one row of the accumulator
-// from tensor memory through the epilogue:
+// One CTA (16 warps) computes a 128 x 128 tile of C: its threads load the
+// tile's K-chunks of A and B (64 elements each, zero outside the matrices),
+// split them into swizzled bf16 operand tiles in shared memory (two stages, so
+// that loading chunk c + 1 overlaps the MMAs of chunk c), one thread issues
+// the MMAs, and after the last chunk the accumulator goes from tensor memory
+// (each warp reads its lane quadrant's share of the columns) through shared
+// memory, so that every global write is coalesced, into the epilogue:
 //   forward:         Y = C + bias (ReLU for hidden layers), and Y^T
 //   weight gradient: C[:, :nw] into dW, column nw into db (the B operand's
 //                    row nw is all ones: the column sums of dY)
 //   input gradient:  Y = C where H > 0, else 0 (ReLU'), and Y^T
+// A product whose K spans many chunks is split along K: each of its ksplit
+// CTAs per tile writes its partial tile to a workspace, and the CTA that
+// arrives last at the tile's counter (atomic ticket, reset by that CTA) adds
+// the partials in split order and runs the epilogue, so the sum's order is
+// fixed.  Several independent products share one launch (blockIdx.x runs over
+// the tiles and splits of all of them).
 // Every wait is bounded; a CTA that gives up sets ROLLOUT_ERR_TIMEOUT.
 #include "env.cuh"
 #include "ppo_gemm.cuh"
@@ -37,11 +44,15 @@ namespace {
 
 using namespace umma;
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;            // tile rows, columns, K elements per chunk
+constexpr int kBM = kGemmTile, kBN = kGemmTile, kBK = kGemmChunk;   // tile rows, columns, K elements per chunk
 constexpr int kTile = 128 * 128;                           // bytes of one 128-row bf16 operand tile
 constexpr int kStageBytes = 4 * kTile;                     // A hi, A lo, B hi, B lo
 constexpr int kGemmSmem = 2 * kStageBytes + 1024;          // two stages + alignment slack
-constexpr int kGemmThreads = 128;
+constexpr int kWarps = 16;
+constexpr int kGemmThreads = 32 * kWarps;
+constexpr int kRuns = (kBM * kBK / 4) / kGemmThreads;      // runs of four elements per thread and operand
+constexpr int kMaxSplitG = 4;                              // most K-splits of one product
+constexpr int kLd = kBN + 1;                               // row stride of the staged tile (floats)
 
 // the bf16 pair (hi, lo) of x
 __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo)
@@ -51,23 +62,48 @@ __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo)
     lo = x - hi;                                             // exact in float32
 }
 
-// loads K-chunk c of rows [r0, r0 + 128) of X [rows, K] (row stride ld) into
-// the swizzled hi / lo tiles; thread t takes 16 runs of four elements
-__device__ __forceinline__ void load_split(const float *X, int ld, int rows, int K, int r0, int c, uint8_t *hi_tile,
-                                           uint8_t *lo_tile)
+// K-chunk c of rows [r0, r0 + 128) of X [rows, K] (row stride ld), held in
+// registers: thread t takes kRuns runs of four elements (zero outside X), as
+// one 16-byte load where the run is whole and aligned (vec: ld a multiple of
+// 4 and X 16-byte aligned).  All loads are issued before any is used, so a
+// chunk costs one round trip to L2.
+struct Runs {
+    float v[kRuns][4];
+};
+
+__device__ __forceinline__ void load_runs(const float *X, int ld, int rows, int K, int r0, int c, bool vec, Runs &R)
 {
     const int tid = threadIdx.x;
-#pragma unroll 4
-    for (int s = 0; s < (kBM * kBK / 4) / kGemmThreads; ++s) {
+#pragma unroll
+    for (int s = 0; s < kRuns; ++s) {
         const int j = tid + kGemmThreads * s;                   // run of four elements
         const int r = j >> 4, q = j & 15;                        // row, run within the row
         const int row = r0 + r, col = c * kBK + 4 * q;
-        float v[4];
+        const float *src = X + (long long)row * ld + col;
+        if (vec && row < rows && col + 3 < K) {
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(src));
+            R.v[s][0] = f.x;
+            R.v[s][1] = f.y;
+            R.v[s][2] = f.z;
+            R.v[s][3] = f.w;
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = (row < rows && col + i < K) ? __ldg(X + (long long)row * ld + col + i) : 0.f;
+            for (int i = 0; i < 4; ++i) R.v[s][i] = (row < rows && col + i < K) ? __ldg(src + i) : 0.f;
+        }
+    }
+}
+
+// the runs split into the swizzled hi / lo operand tiles
+__device__ __forceinline__ void store_split(const Runs &R, uint8_t *hi_tile, uint8_t *lo_tile)
+{
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int s = 0; s < kRuns; ++s) {
+        const int j = tid + kGemmThreads * s;
+        const int r = j >> 4, q = j & 15;
         float h[4], l[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) split_bf16(v[i], h[i], l[i]);
+        for (int i = 0; i < 4; ++i) split_bf16(R.v[s][i], h[i], l[i]);
         const uint2 ph = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
         const uint2 pl = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
         const uint32_t off = sw128_offset(r, q >> 1) + 8 * (q & 1);   // 16-byte unit q/2 of row r, half q%2
@@ -76,15 +112,95 @@ __device__ __forceinline__ void load_split(const float *X, int ld, int rows, int
     }
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_split_kernel(GemmArgs g)
+struct GemmGroup {
+    GemmArgs g[kGemmGroup];
+    int n;
+    int first[kGemmGroup + 1];   // first block of each product
+};
+
+// The epilogue of the staged tile (rows [0, nrows), columns [0, ncols) of
+// `stage`), one instantiation per kind of product.  Warp w takes rows w,
+// w + 16, ...; lane l columns l, l + 32, ... of each (consecutive lanes:
+// consecutive addresses); bounds are predicates on the accesses.
+template <int EPI>
+__device__ __forceinline__ void epilogue(const GemmArgs &g, float *stage, int m0, int n0, int nrows, int ncols)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int jb = (ncols + 31) >> 5;                        // column blocks in use (CTA-uniform)
+    for (int j = 0; j < jb; ++j) {
+        const int cc = lane + 32 * j;
+        const bool cin = cc < ncols;
+        const int n = n0 + cc;
+        float bj = 0.f;
+        if (EPI == kGemmFwd) bj = cin ? __ldg(g.bias + n) : 0.f;
+        for (int r0 = warp; r0 < nrows; r0 += 4 * kWarps) {
+            float y[4], h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = r0 + kWarps * i;
+                const bool in = cin && rr < nrows;
+                y[i] = in ? stage[rr * kLd + cc] : 0.f;
+                h[i] = 1.f;
+                if (EPI == kGemmDx) h[i] = in ? __ldg(g.H + (long long)(m0 + rr) * g.ldh + n) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = r0 + kWarps * i;
+                const bool in = cin && rr < nrows;
+                float v = y[i];
+                if (EPI == kGemmFwd) {
+                    v += bj;
+                    if (g.relu) v = relu(v);
+                }
+                if (EPI == kGemmDx) v = h[i] > 0.f ? v : 0.f;
+                const long long m = m0 + rr;
+                if (EPI == kGemmDw) {
+                    if (in && n < g.nw) g.Y[m * g.ldy + n] = v;
+                    if (in && n == g.nw) g.db[m] = v;
+                } else if (in) {
+                    g.Y[m * g.ldy + n] = v;
+                    stage[rr * kLd + cc] = v;                      // for the transposed pass
+                }
+            }
+        }
+    }
+    if (EPI != kGemmDw && g.YT) {
+        __syncthreads();
+        // transposed pass: warp w takes columns w, w + 16, ..., lane l rows l, l + 32, ...
+        for (int c0 = warp; c0 < ncols; c0 += kWarps) {
+            float *dst = g.YT + (long long)(n0 + c0) * g.ldt + m0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int rr = lane + 32 * j;
+                if (rr < nrows) dst[rr] = stage[rr * kLd + c0];
+            }
+        }
+    }
+}
+
+// one CTA of product g (block `local` of its blocks); g is a member of the
+// kernel's parameter block selected with a constant index, so that its fields
+// are parameter-space reads that no global store can alias
+__device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *sm)
+{
     __shared__ __align__(8) uint64_t bar_done[2], bar_final;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
+    __shared__ unsigned int ticket_sh;
+    // the staged accumulator, named through the dynamic shared-memory array so
+    // that the compiler knows it cannot alias the global outputs
+    extern __shared__ uint8_t smem_raw[];
+    float *stage = reinterpret_cast<float *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the tile and split this block computes
+    const int z = local % g.ksplit, tile = local / g.ksplit;
+    const int mt = (g.M + kBM - 1) / kBM;
+    const int m0 = (tile % mt) * kBM, n0 = (tile / mt) * kBN;
+    const int chunks = (g.K + kBK - 1) / kBK;
+    const int c_begin = g.ksplit > 1 ? z * g.chunks_per_split : 0;
+    const int c_end = g.ksplit > 1 ? min(chunks, c_begin + g.chunks_per_split) : chunks;
+    const bool vec_a = (g.lda & 3) == 0 && ((uintptr_t)g.A & 15) == 0;
+    const bool vec_b = (g.ldb & 3) == 0 && ((uintptr_t)g.B & 15) == 0;
     if (tid == 0) {
         abort_sh = 0;
         mbar_init(&bar_done[0], 1);
@@ -101,17 +217,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_split_kernel(GemmArgs g)
     tc_fence_after();
     const uint32_t tmem = tmem_sh;
     volatile int *abort = &abort_sh;
-    const int chunks = (g.K + kBK - 1) / kBK;
     constexpr uint32_t id = idesc(true, kBM, kBN);
     bool ok = true;
-    for (int c = 0; c < chunks; ++c) {
-        const int s = c & 1;
+    for (int c = c_begin; c < c_end; ++c) {
+        const int i = c - c_begin, s = i & 1;
         uint8_t *st = sm + s * kStageBytes;
-        // the MMAs of chunk c - 2 read this stage: wait until they are done
-        if (c >= 2) ok = __syncthreads_and(ok && mbar_wait(&bar_done[s], (uint32_t)(((c - 2) >> 1) & 1), abort));
+        // the MMAs of chunk i - 2 read this stage: wait until they are done
+        if (i >= 2) ok = __syncthreads_and(ok && mbar_wait(&bar_done[s], (uint32_t)(((i - 2) >> 1) & 1), abort));
         if (!ok) break;
-        load_split(g.A, g.lda, g.M, g.K, m0, c, st, st + kTile);
-        load_split(g.B, g.ldb, g.N, g.K, n0, c, st + 2 * kTile, st + 3 * kTile);
+        {
+            Runs ra, rb;
+            load_runs(g.A, g.lda, g.M, g.K, m0, c, vec_a, ra);
+            load_runs(g.B, g.ldb, g.N, g.K, n0, c, vec_b, rb);
+            store_split(ra, st, st + kTile);
+            store_split(rb, st + 2 * kTile, st + 3 * kTile);
+        }
         fence_async_smem();                       // generic-proxy stores -> visible to the tensor core
         tc_fence_before();
         __syncthreads();
@@ -120,7 +240,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_split_kernel(GemmArgs g)
             const uint32_t a_hi = smem_u32(st), a_lo = a_hi + kTile, b_hi = a_hi + 2 * kTile, b_lo = a_hi + 3 * kTile;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint32_t acc = (c > 0 || k > 0) ? 1u : 0u;
+                const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
                 mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_hi + 32 * k), id, acc);
                 mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_lo + 32 * k), id, 1u);
                 mma<true>(tmem, desc_sw128(a_lo + 32 * k), desc_sw128(b_hi + 32 * k), id, 1u);
@@ -136,57 +256,141 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_split_kernel(GemmArgs g)
         ok = __syncthreads_and(ok && fin);
     }
     tc_fence_after();
-    if (ok && chunks > 0) {
-        const int r = tid, m = m0 + r;
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-        for (int cb = 0; cb < kBN; cb += 32) {
-            if (n0 + cb >= g.N) break;                             // CTA-uniform
-            float v[32];
-            tmem_ld32(lane_addr + cb, v);
-            tmem_ld_wait();
-            if (m >= g.M) continue;
+    // tensor memory -> stage[r][c] (the operand stages are free now): warp w
+    // reads lane quadrant w % 4, columns [32 (w / 4), +32); row stride kLd so
+    // that rows and columns are both read without bank conflicts
+    const int ncols = min(kBN, g.N - n0), nrows = min(kBM, g.M - m0);
+    const bool has = c_end > c_begin;            // a split past the last chunk holds zeros
+    if (ok) {
+        const int q = warp & 3, cb = 32 * (warp >> 2);
+        const int r = 32 * q + lane;
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + cb, v);
+        tmem_ld_wait();
+        if (cb < ncols) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int n = n0 + cb + i;
-                if (n >= g.N) continue;
-                float y = v[i];
-                if (g.epi == kGemmFwd) {
-                    y += __ldg(g.bias + n);
-                    if (g.relu) y = relu(y);
-                } else if (g.epi == kGemmDx) {
-                    y = __ldg(g.H + (long long)m * g.ldh + n) > 0.f ? y : 0.f;
-                }
-                if (g.epi == kGemmDw) {
-                    if (n < g.nw) g.Y[(long long)m * g.ldy + n] = y;
-                    else g.db[m] = y;
-                } else {
-                    g.Y[(long long)m * g.ldy + n] = y;
-                    if (g.YT) g.YT[(long long)n * g.ldt + m] = y;
+            for (int j = 0; j < 32; ++j) stage[r * kLd + cb + j] = has ? v[j] : 0.f;
+        }
+    }
+    __syncthreads();
+    bool fin_here = ok && g.ksplit == 1;          // this CTA runs the epilogue
+    if (ok && g.ksplit > 1) {
+        // this split's partial tile (warp w: rows w, w + 16, ...; coalesced), then
+        // the tile's arrival ticket
+        float *part = g.ws + ((long long)tile * g.ksplit + z) * (kBM * kBN);
+        const int jb = (ncols + 31) >> 5;
+        for (int rr = warp; rr < kBM; rr += kWarps)
+            for (int j = 0; j < jb; ++j) {
+                const int cc = lane + 32 * j;
+                if (cc < ncols) part[rr * kBN + cc] = stage[rr * kLd + cc];
+            }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) ticket_sh = atomicAdd(g.cnt + tile, 1u);
+        __syncthreads();
+        if (ticket_sh == (unsigned int)(g.ksplit - 1)) {
+            // the last split of this tile: the partials added in split order
+            __threadfence();
+            const float *base = g.ws + (long long)tile * g.ksplit * (kBM * kBN);
+            for (int j = 0; j < jb; ++j) {
+                const int cc = lane + 32 * j;
+                for (int r0 = warp; r0 < nrows; r0 += 4 * kWarps) {
+                    float acc[4], p[kMaxSplitG - 1][4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = r0 + kWarps * i;
+                        const bool in = cc < ncols && rr < nrows;
+                        acc[i] = in ? __ldcg(base + rr * kBN + cc) : 0.f;
+#pragma unroll
+                        for (int zz = 1; zz < kMaxSplitG; ++zz)
+                            p[zz - 1][i] = (in && zz < g.ksplit)
+                                               ? __ldcg(base + (long long)zz * (kBM * kBN) + rr * kBN + cc)
+                                               : 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                        for (int zz = 1; zz < kMaxSplitG; ++zz)
+                            if (zz < g.ksplit) acc[i] += p[zz - 1][i];
+                        const int rr = r0 + kWarps * i;
+                        if (cc < ncols && rr < nrows) stage[rr * kLd + cc] = acc[i];
+                    }
                 }
             }
+            if (tid == 0) g.cnt[tile] = 0u;                        // ready for the next launch
+            __syncthreads();
+            fin_here = true;
         }
-    } else if (!ok && tid == 0) {
-        set_status(g.status, ROLLOUT_ERR_TIMEOUT);
     }
+    if (fin_here) {
+        if (g.epi == kGemmFwd) epilogue<kGemmFwd>(g, stage, m0, n0, nrows, ncols);
+        else if (g.epi == kGemmDw) epilogue<kGemmDw>(g, stage, m0, n0, nrows, ncols);
+        else epilogue<kGemmDx>(g, stage, m0, n0, nrows, ncols);
+    }
+    if (!ok && tid == 0) set_status(g.status, ROLLOUT_ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, kBN);
 }
 
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_group_kernel(const __grid_constant__ GemmGroup grp)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // which product this block belongs to; each case names its member with a
+    // constant index (a dynamic index into the parameter block would make
+    // every field access a generic memory load, reloaded after each store)
+    int gi = 0;
+    while (gi + 1 < grp.n && (int)blockIdx.x >= grp.first[gi + 1]) ++gi;
+    const int local = (int)blockIdx.x - grp.first[gi];
+    switch (gi) {
+    case 0: gemm_cta(grp.g[0], local, sm); break;
+    case 1: gemm_cta(grp.g[1], local, sm); break;
+    case 2: gemm_cta(grp.g[2], local, sm); break;
+    default: gemm_cta(grp.g[3], local, sm); break;
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_gemm_split(const GemmArgs &g, cudaStream_t s)
+void gemm_plan(GemmArgs &g, int max_split, long long *ws_floats, int *counters)
+{
+    const int chunks = (g.K + kBK - 1) / kBK;
+    const int tiles = ((g.M + kBM - 1) / kBM) * ((g.N + kBN - 1) / kBN);
+    int ks = (chunks + 1) / 2;                   // two chunks per split
+    if (ks > max_split) ks = max_split;
+    if (ks > kMaxSplitG) ks = kMaxSplitG;
+    if (ks < 1) ks = 1;
+    g.ksplit = ks;
+    g.chunks_per_split = (chunks + ks - 1) / ks;
+    *ws_floats = ks > 1 ? (long long)tiles * ks * kBM * kBN : 0;
+    *counters = ks > 1 ? tiles : 0;
+}
+
+cudaError_t launch_gemm_group(const GemmArgs *g, int n, cudaStream_t s)
 {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    if (g.M <= 0 || g.N <= 0 || g.K <= 0) return cudaErrorInvalidValue;
-    const dim3 grid((g.M + kBM - 1) / kBM, (g.N + kBN - 1) / kBN);
-    gemm_split_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(g);
+    if (n < 1 || n > kGemmGroup) return cudaErrorInvalidValue;
+    GemmGroup grp{};
+    grp.n = n;
+    int blocks = 0;
+    for (int i = 0; i < n; ++i) {
+        const GemmArgs &a = g[i];
+        if (a.M <= 0 || a.N <= 0 || a.K <= 0 || a.ksplit < 1 || a.ksplit > kMaxSplitG ||
+            (a.ksplit > 1 && (!a.ws || !a.cnt)))
+            return cudaErrorInvalidValue;
+        grp.g[i] = a;
+        grp.first[i] = blocks;
+        blocks += ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN) * a.ksplit;
+    }
+    grp.first[n] = blocks;
+    gemm_group_kernel<<<blocks, kGemmThreads, kGemmSmem, s>>>(grp);
     return cudaGetLastError();
 }
 

@@ -1,6 +1,9 @@
 // ppo_gemm.cuh -- the PPO update's tensor-core GEMM (ppo_gemm.cu):
 // C[M, N] = A[M, K] B[N, K]^T, float32 in and out, both operands row-major with
 // K contiguous, each product taken from a bf16 high/low split of its operands.
+// Up to kGemmGroup independent products run in one launch; a product may be
+// split along K over several CTAs, whose partial tiles the last CTA of each
+// tile adds in split order (so the result does not depend on scheduling).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -8,6 +11,9 @@
 namespace rl {
 
 enum { kGemmFwd = 0, kGemmDw = 1, kGemmDx = 2 };
+constexpr int kGemmGroup = 4;
+constexpr int kGemmTile = 128;            // C tile: 128 x 128
+constexpr int kGemmChunk = 64;            // K elements per chunk
 
 struct GemmArgs {
     const float *A = nullptr;   // [M, K], row stride lda (floats)
@@ -29,9 +35,21 @@ struct GemmArgs {
     // kGemmDw: columns n < nw go to Y (dW), column nw to db[m]
     int nw = 0;
     float *db = nullptr;
+    // split along K: ksplit CTAs per tile, each taking `chunks_per_split`
+    // K-chunks; partial tiles in ws (tiles x ksplit x 128 x 128 floats), one
+    // arrival counter per tile in cnt (zero between launches)
+    int ksplit = 1, chunks_per_split = 0;
+    float *ws = nullptr;
+    unsigned int *cnt = nullptr;
     int *status = nullptr;      // ROLLOUT_ERR_TIMEOUT if a bounded wait gives up
 };
 
-cudaError_t launch_gemm_split(const GemmArgs &g, cudaStream_t s);
+// fills ksplit / chunks_per_split for a product (at most max_split CTAs per
+// tile) and returns the workspace floats and counters it needs
+void gemm_plan(GemmArgs &g, int max_split, long long *ws_floats, int *counters);
+
+// launches n (<= kGemmGroup) planned products at once; their ws / cnt regions
+// must not overlap
+cudaError_t launch_gemm_group(const GemmArgs *g, int n, cudaStream_t s);
 
 }  // namespace rl
