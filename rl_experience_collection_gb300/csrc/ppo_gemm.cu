@@ -120,8 +120,9 @@ struct GemmGroup {
 
 // The epilogue of the staged tile (rows [0, nrows), columns [0, ncols) of
 // `stage`), one instantiation per kind of product.  Warp w takes rows w,
-// w + 16, ...; lane l columns l, l + 32, ... of each (consecutive lanes:
-// consecutive addresses); bounds are predicates on the accesses.
+// w + 16, ... (eight at a time); lane l columns l, l + 32, ... of each
+// (consecutive lanes: consecutive addresses); bounds are predicates on the
+// accesses.
 template <int EPI>
 __device__ __forceinline__ void epilogue(const GemmArgs &g, float *stage, int m0, int n0, int nrows, int ncols)
 {
@@ -133,10 +134,10 @@ __device__ __forceinline__ void epilogue(const GemmArgs &g, float *stage, int m0
         const int n = n0 + cc;
         float bj = 0.f;
         if (EPI == kGemmFwd) bj = cin ? __ldg(g.bias + n) : 0.f;
-        for (int r0 = warp; r0 < nrows; r0 += 4 * kWarps) {
-            float y[4], h[4];
+        for (int r0 = warp; r0 < nrows; r0 += 8 * kWarps) {
+            float y[8], h[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const int rr = r0 + kWarps * i;
                 const bool in = cin && rr < nrows;
                 y[i] = in ? stage[rr * kLd + cc] : 0.f;
@@ -144,7 +145,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs &g, float *stage, int m0
                 if (EPI == kGemmDx) h[i] = in ? __ldg(g.H + (long long)(m0 + rr) * g.ldh + n) : 0.f;
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const int rr = r0 + kWarps * i;
                 const bool in = cin && rr < nrows;
                 float v = y[i];
@@ -219,18 +220,24 @@ __device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *
     volatile int *abort = &abort_sh;
     constexpr uint32_t id = idesc(true, kBM, kBN);
     bool ok = true;
+    // software pipeline: the loads of chunk c + 1 are in flight while chunk c
+    // is split into its stage and its MMAs are issued
+    Runs ra, rb;
+    if (c_begin < c_end) {
+        load_runs(g.A, g.lda, g.M, g.K, m0, c_begin, vec_a, ra);
+        load_runs(g.B, g.ldb, g.N, g.K, n0, c_begin, vec_b, rb);
+    }
     for (int c = c_begin; c < c_end; ++c) {
         const int i = c - c_begin, s = i & 1;
         uint8_t *st = sm + s * kStageBytes;
         // the MMAs of chunk i - 2 read this stage: wait until they are done
         if (i >= 2) ok = __syncthreads_and(ok && mbar_wait(&bar_done[s], (uint32_t)(((i - 2) >> 1) & 1), abort));
         if (!ok) break;
-        {
-            Runs ra, rb;
-            load_runs(g.A, g.lda, g.M, g.K, m0, c, vec_a, ra);
-            load_runs(g.B, g.ldb, g.N, g.K, n0, c, vec_b, rb);
-            store_split(ra, st, st + kTile);
-            store_split(rb, st + 2 * kTile, st + 3 * kTile);
+        store_split(ra, st, st + kTile);
+        store_split(rb, st + 2 * kTile, st + 3 * kTile);
+        if (c + 1 < c_end) {
+            load_runs(g.A, g.lda, g.M, g.K, m0, c + 1, vec_a, ra);
+            load_runs(g.B, g.ldb, g.N, g.K, n0, c + 1, vec_b, rb);
         }
         fence_async_smem();                       // generic-proxy stores -> visible to the tensor core
         tc_fence_before();
@@ -294,10 +301,10 @@ __device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *
             const float *base = g.ws + (long long)tile * g.ksplit * (kBM * kBN);
             for (int j = 0; j < jb; ++j) {
                 const int cc = lane + 32 * j;
-                for (int r0 = warp; r0 < nrows; r0 += 4 * kWarps) {
-                    float acc[4], p[kMaxSplitG - 1][4];
+                for (int r0 = warp; r0 < nrows; r0 += 8 * kWarps) {
+                    float acc[8], p[kMaxSplitG - 1][8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         const int rr = r0 + kWarps * i;
                         const bool in = cc < ncols && rr < nrows;
                         acc[i] = in ? __ldcg(base + rr * kBN + cc) : 0.f;
@@ -308,7 +315,7 @@ __device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *
                                                : 0.f;
                     }
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 8; ++i) {
 #pragma unroll
                         for (int zz = 1; zz < kMaxSplitG; ++zz)
                             if (zz < g.ksplit) acc[i] += p[zz - 1][i];
