@@ -199,6 +199,34 @@ ROLLOUT_API int rollout_phase_ms(rollout_handle *h, float *ms);
 ROLLOUT_API int rollout_test_stall(rollout_handle *h, int on);
 
 /*
+ * rollout_forward -- the three networks on given states, for checking them in
+ * isolation (test and debugging use, not the collection path).  Page "PPO
+ * CUDA Pipeline Design -- Zero-Roundtrip Experience Collection", section
+ * "Kernel Phases", Phase A steps 3 (actor: state -> logits), 5 (critic: state
+ * -> value) and 9 (curiosity forward model: [state ; one-hot(action)] ->
+ * predicted next state); section "Weight Layout".
+ *
+ * All arrays are DEVICE pointers owned by the caller, on the handle's device:
+ *   states   [M, n_market+3] f32 (any values)
+ *   actions  [M] i32 in [0, n_actions): the curiosity model's one-hot input
+ *   logits   [M, n_actions] f32, values [M] f32, cur_pred [M, n_market+3] f32
+ *            (outputs, fully overwritten)
+ * The products run on the tensor cores in the handle's operand format, as
+ * the collector's networks compute them: every weight and every layer input
+ * rounded once to bf16 (ROLLOUT_BF16) or tf32 (ROLLOUT_TF32), float32
+ * accumulation, float32 bias and ReLU; ROLLOUT_FP32 handles take float32-grade
+ * products (each operand split into three bf16 parts, the six largest
+ * products of parts taken: relative error below 2^-22 per product).  The handle
+ * keeps a device copy of the float32 weights for this (refreshed by
+ * rollout_set_weights and rollout_set_weights_device) and its own buffers,
+ * grown on demand.  Stream-ordered and asynchronous.  An action out of range
+ * gives a zero one-hot and records ROLLOUT_ERR_RANGE in the status word
+ * (rollout_status).  Returns ROLLOUT_OK, _INVALID, _NOMEM or _CUDA.
+ */
+ROLLOUT_API int rollout_forward(rollout_handle *h, const float *states, const int32_t *actions, int M,
+                                float *logits, float *values, float *cur_pred, void *stream);
+
+/*
  * rollout_test_activations -- a test hook for checking the tensor-core paths
  * layer by layer, not for production use.  (An addition of this library: the
  * page "PPO CUDA Pipeline Design -- Zero-Roundtrip Experience Collection",

@@ -27,7 +27,7 @@ DTYPE = {"fp32": 0, "tf32": 1, "bf16": 2}
 EXPORTS = ["rollout_create", "rollout_set_weights", "rollout_run", "rollout_status", "rollout_destroy",
            "rollout_last_error", "rollout_set_timing", "rollout_phase_ms", "rollout_run_static", "rollout_run_host",
            "rollout_set_weights_device", "rollout_test_stall", "rollout_test_activations",
-           "rollout_test_alloc"]
+           "rollout_test_alloc", "rollout_forward"]
 
 
 class RolloutDims(C.Structure):
@@ -111,6 +111,8 @@ def lib(path: Optional[str] = None):
     L.rollout_test_stall.argtypes = [vp, C.c_int]
     L.rollout_test_activations.restype = C.c_int
     L.rollout_test_activations.argtypes = [vp, vp, C.c_int]
+    L.rollout_forward.restype = C.c_int
+    L.rollout_forward.argtypes = [vp, vp, vp, C.c_int, vp, vp, vp, vp]
     L.rollout_test_alloc.restype = C.c_int
     L.rollout_test_alloc.argtypes = [C.c_longlong, C.POINTER(C.c_longlong)]
     L.rollout_last_error.restype = C.c_char_p
@@ -320,6 +322,22 @@ class Rollout:
     def test_stall(self, on: bool = True) -> None:
         """Test hook: later runs launch the value kernel's stalling test build."""
         _check(lib().rollout_test_stall(self._h, int(on)))
+
+    def forward(self, states, actions, stream=None):
+        """rollout_forward: (logits [M, 45], values [M], cur_pred [M, 54]) of the
+        device tensors states [M, 54] float32 and actions [M] int32."""
+        import torch
+        M = int(states.shape[0])
+        dev = states.device
+        logits = torch.empty((M, wl.N_ACTIONS), dtype=torch.float32, device=dev)
+        values = torch.empty(M, dtype=torch.float32, device=dev)
+        cur = torch.empty((M, wl.STATE_DIM), dtype=torch.float32, device=dev)
+        st = states.contiguous()
+        ac = actions.contiguous()
+        _check(lib().rollout_forward(self._h, C.c_void_p(st.data_ptr()), C.c_void_p(ac.data_ptr()), M,
+                                     C.c_void_p(logits.data_ptr()), C.c_void_p(values.data_ptr()),
+                                     C.c_void_p(cur.data_ptr()), C.c_void_p(_stream_handle(stream))))
+        return logits, values, cur
 
     def test_activations(self, dump=None, n_episodes: int = 0) -> None:
         """Test hook: later runs also write the rounded hidden activations of

@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "internal.cuh"
+#include "ppo_gemm.cuh"
 #include "umma_path.cuh"
 
 using namespace rl;
@@ -77,6 +78,11 @@ struct rollout_handle {
     // rollout_test_activations: runs launch the kernels' dump builds
     float *dump = nullptr;
     int dump_episodes = 0;
+    // rollout_forward: the packed float32 weights and the forward pass's
+    // buffers (grown on demand)
+    float *d_wf32 = nullptr;
+    uint8_t *d_fwd = nullptr;
+    size_t fwd_bytes = 0;
     cudaEvent_t ev[kTimedKernels + 1] = {};
     // rollout_run_host: device copies of the inputs and outputs (one allocation,
     // grown on demand), the copy streams and their events
@@ -285,6 +291,11 @@ int upload_weights(rollout_handle *h, const float *w)
     const HostLayout lo = host_layout(h->dims);
     for (size_t i = 0; i < lo.total; ++i)
         if (!isfinite(w[i])) return fail(ROLLOUT_ERR_INVALID, "weight %zu is not finite", i);
+    cudaError_t ew;
+    if (!h->d_wf32 && (ew = dev_alloc((void **)&h->d_wf32, lo.total * 4)) != cudaSuccess)
+        return cuda_fail(ew, "cudaMalloc(float32 weights)");
+    if ((ew = cudaMemcpy(h->d_wf32, w, lo.total * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
+        return cuda_fail(ew, "cudaMemcpy(float32 weights)");
     if (h->dims.dtype == ROLLOUT_FP32) return upload_simt(h, w);
     int rc = umma_upload(&h->umma, &h->d_umma, h->dims.dtype == ROLLOUT_BF16, w, umma_layout(lo), g_err, sizeof(g_err));
     if (rc) return rc;
@@ -467,6 +478,8 @@ void free_handle(rollout_handle *h)
     for (cudaEvent_t e : h->copy_done)
         if (e) cudaEventDestroy(e);
     dev_free(h->d_maps);
+    dev_free(h->d_wf32);
+    dev_free(h->d_fwd);
     delete h;
 }
 
@@ -552,6 +565,8 @@ int rollout_set_weights_device(rollout_handle *h, const float *weights, void *st
     if (!h || !weights) return fail(ROLLOUT_ERR_INVALID, "null argument");
     if (((uintptr_t)weights & 3u) != 0) return fail(ROLLOUT_ERR_INVALID, "weights must be 4-byte aligned");
     cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t ec = cudaMemcpyAsync(h->d_wf32, weights, host_layout(h->dims).total * 4, cudaMemcpyDeviceToDevice, st);
+    if (ec != cudaSuccess) return cuda_fail(ec, "cudaMemcpyAsync(float32 weights)");
     for (int r = 0; r < h->n_repack; ++r) {
         const auto &g = h->repack[r];
         const long long blocks = (g.n + 255) / 256;
@@ -876,6 +891,148 @@ int rollout_run_host(rollout_handle *h, const float *features, const int32_t *ep
         if ((e = cudaEventRecord(h->copy_done[k], h->copy_stream[k])) != cudaSuccess ||
             (e = cudaStreamWaitEvent(s, h->copy_done[k], 0)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord / cudaStreamWaitEvent");
+    return ROLLOUT_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// the curiosity model's input [state ; one-hot(action)], row stride ldc
+__global__ void forward_prep_kernel(const float *states, const int32_t *actions, int M, float *ci, int ldc,
+                                    int *status)
+{
+    const long long total = (long long)M * ldc;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long m = e / ldc;
+        const int c = (int)(e - m * ldc);
+        float v = 0.f;
+        if (c < kState) {
+            v = states[m * kState + c];
+        } else if (c < kState + kActions) {
+            const int a = actions[m];
+            if (a < 0 || a >= kActions) {
+                if (c == kState) atomicCAS(status, 0, ROLLOUT_ERR_RANGE);
+            } else {
+                v = (c - kState == a) ? 1.f : 0.f;
+            }
+        }
+        ci[e] = v;
+    }
+}
+
+constexpr int kFwdCi = 100;   // row stride of the curiosity input (99 used)
+
+}  // namespace
+
+extern "C" {
+
+int rollout_forward(rollout_handle *h, const float *states, const int32_t *actions, int M, float *logits,
+                    float *values, float *cur_pred, void *stream)
+{
+    g_err[0] = 0;
+    if (!h || !states || !actions || !logits || !values || !cur_pred) return fail(ROLLOUT_ERR_INVALID, "null argument");
+    if (M <= 0 || M > (1 << 24)) return fail(ROLLOUT_ERR_INVALID, "M must be in [1, 2^24]");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != h->device) return fail(ROLLOUT_ERR_INVALID, "current device %d is not the handle's device %d", dev, h->device);
+    const rollout_dims &d = h->dims;
+    const HostLayout lo = host_layout(d);
+    const int ops = d.dtype == ROLLOUT_BF16 ? kGemmBf16 : d.dtype == ROLLOUT_TF32 ? kGemmTf32 : kGemmSplit3;
+    cudaStream_t st = (cudaStream_t)stream;
+    h->last_stream = st;
+    // buffers: curiosity input, every hidden layer, split-K workspace and counters
+    int csum = 0;
+    for (int l = 0; l < kCriticLayers - 1; ++l) csum += lo.c_out[l];
+    const size_t act_floats = (size_t)M * (kFwdCi + kActorH1 + kActorH2 + csum + kCurH);
+    float *buf_probe = nullptr;
+    float *ci = buf_probe, *ah[2], *ch[kCriticLayers - 1], *qz;
+    auto layout_bufs = [&](float *base) {
+        float *p = base;
+        ci = p; p += (size_t)M * kFwdCi;
+        ah[0] = p; p += (size_t)M * kActorH1;
+        ah[1] = p; p += (size_t)M * kActorH2;
+        for (int l = 0; l < kCriticLayers - 1; ++l) { ch[l] = p; p += (size_t)M * lo.c_out[l]; }
+        qz = p;
+    };
+    // the products of depth j of the three networks
+    auto stage = [&](int j, GemmArgs *g) -> int {
+        int n = 0;
+        auto prod = [&](const float *A, int lda, size_t w, size_t b, int in, int out, bool relu, float *Y) {
+            GemmArgs x;
+            x.A = A; x.lda = lda;
+            x.B = h->d_wf32 + w; x.ldb = in;
+            x.M = M; x.N = out; x.K = in;
+            x.epi = kGemmFwd; x.operands = ops;
+            x.bias = h->d_wf32 + b; x.relu = relu ? 1 : 0;
+            x.Y = Y; x.ldy = out;
+            x.status = h->d_status;
+            g[n++] = x;
+        };
+        if (j < 3) prod(j == 0 ? states : ah[j - 1], j == 0 ? kState : lo.a_in[j], lo.a_w[j], lo.a_b[j], lo.a_in[j],
+                        lo.a_out[j], j < 2, j < 2 ? ah[j] : logits);
+        prod(j == 0 ? states : ch[j - 1], j == 0 ? kState : lo.c_in[j], lo.c_w[j], lo.c_b[j], lo.c_in[j], lo.c_out[j],
+             j < kCriticLayers - 1, j < kCriticLayers - 1 ? ch[j] : values);
+        if (j < 2) prod(j == 0 ? ci : qz, j == 0 ? kFwdCi : kCurH, lo.q_w[j], lo.q_b[j], lo.q_in[j], lo.q_out[j],
+                        j == 0, j == 0 ? qz : cur_pred);
+        return n;
+    };
+    // workspace: the largest over the stages
+    layout_bufs(nullptr);
+    long long ws_max = 0;
+    int cnt_max = 0;
+    for (int j = 0; j < kCriticLayers; ++j) {
+        GemmArgs g[kGemmGroup];
+        const int n = stage(j, g);
+        long long wsum = 0;
+        int csm = 0;
+        for (int i = 0; i < n; ++i) {
+            long long wf;
+            int c;
+            gemm_plan(g[i], 4, &wf, &c);
+            wsum += wf;
+            csm += c;
+        }
+        ws_max = wsum > ws_max ? wsum : ws_max;
+        cnt_max = csm > cnt_max ? csm : cnt_max;
+    }
+    const size_t need = act_floats * 4 + (size_t)ws_max * 4 + (size_t)(cnt_max + 1) * 4 + 256;
+    if (need > h->fwd_bytes) {
+        dev_free(h->d_fwd);                      // cudaFree waits for work that may still use it
+        h->d_fwd = nullptr;
+        h->fwd_bytes = 0;
+        if ((e = dev_alloc((void **)&h->d_fwd, need)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(forward buffers)");
+        h->fwd_bytes = need;
+    }
+    float *base = reinterpret_cast<float *>(h->d_fwd);
+    layout_bufs(base);
+    float *ws = base + act_floats;
+    unsigned int *cnt = reinterpret_cast<unsigned int *>(ws + ws_max);
+    if ((e = cudaMemsetAsync(cnt, 0, (size_t)(cnt_max + 1) * 4, st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(h->d_status, 0, sizeof(int), st)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync");
+    const long long tot = (long long)M * kFwdCi;
+    forward_prep_kernel<<<(int)((tot + 255) / 256 < 4096 ? (tot + 255) / 256 : 4096), 256, 0, st>>>(
+        states, actions, M, ci, kFwdCi, h->d_status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "forward input launch");
+    for (int j = 0; j < kCriticLayers; ++j) {
+        GemmArgs g[kGemmGroup];
+        const int n = stage(j, g);
+        long long wo = 0;
+        int co = 0;
+        for (int i = 0; i < n; ++i) {
+            long long wf;
+            int c;
+            gemm_plan(g[i], 4, &wf, &c);
+            g[i].ws = ws + wo;
+            g[i].cnt = cnt + co;
+            wo += wf;
+            co += c;
+        }
+        if ((e = launch_gemm_group(g, n, st)) != cudaSuccess) return cuda_fail(e, "forward product launch");
+    }
     return ROLLOUT_OK;
 }
 

@@ -27,6 +27,12 @@
 //   weight gradient: C[:, :nw] into dW, column nw into db (the B operand's
 //                    row nw is all ones: the column sums of dY)
 //   input gradient:  Y = C where H > 0, else 0 (ReLU'), and Y^T
+// Where float32 products are needed to float32 rounding (a forward pass of
+// float32 networks), each operand is split three ways, hi + mid + lo, and the
+// six products of parts above 2^-23 relative are taken.
+// For a forward pass in the collector's own operand format the operands are
+// instead rounded once to bf16 (one kind::f16 MMA per K-step) or to tf32 (one
+// kind::tf32 MMA per K-step over two 32-element tiles).
 // A product whose K spans many chunks is split along K: each of its ksplit
 // CTAs per tile writes its partial tile to a workspace, and the CTA that
 // arrives last at the tile's counter (atomic ticket, reset by that CTA) adds
@@ -46,7 +52,7 @@ using namespace umma;
 
 constexpr int kBM = kGemmTile, kBN = kGemmTile, kBK = kGemmChunk;   // tile rows, columns, K elements per chunk
 constexpr int kTile = 128 * 128;                           // bytes of one 128-row bf16 operand tile
-constexpr int kStageBytes = 4 * kTile;                     // A hi, A lo, B hi, B lo
+constexpr int kStageBytes = 6 * kTile;                     // A hi, A lo, B hi, B lo (, A mid, B mid)
 constexpr int kGemmSmem = 2 * kStageBytes + 1024;          // two stages + alignment slack
 constexpr int kWarps = 16;
 constexpr int kGemmThreads = 32 * kWarps;
@@ -109,6 +115,50 @@ __device__ __forceinline__ void store_split(const Runs &R, uint8_t *hi_tile, uin
         const uint32_t off = sw128_offset(r, q >> 1) + 8 * (q & 1);   // 16-byte unit q/2 of row r, half q%2
         *reinterpret_cast<uint2 *>(hi_tile + off) = ph;
         *reinterpret_cast<uint2 *>(lo_tile + off) = pl;
+    }
+}
+
+// the runs rounded to one operand format into two swizzled tiles: bf16
+// (K elements 0..63 of the chunk in `t0`; `t1` unused) or tf32 (elements 0..31
+// in `t0`, 32..63 in `t1`, four bytes each)
+template <int OPS>
+__device__ __forceinline__ void store_round(const Runs &R, uint8_t *t0, uint8_t *t1)
+{
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int s = 0; s < kRuns; ++s) {
+        const int j = tid + kGemmThreads * s;
+        const int r = j >> 4, q = j & 15;
+        if constexpr (OPS == kGemmBf16) {
+            const uint2 p = make_uint2(pack_bf16x2(R.v[s][0], R.v[s][1]), pack_bf16x2(R.v[s][2], R.v[s][3]));
+            *reinterpret_cast<uint2 *>(t0 + sw128_offset(r, q >> 1) + 8 * (q & 1)) = p;
+        } else {
+            const uint4 p = make_uint4(to_tf32(R.v[s][0]), to_tf32(R.v[s][1]), to_tf32(R.v[s][2]), to_tf32(R.v[s][3]));
+            *reinterpret_cast<uint4 *>((q < 8 ? t0 : t1) + sw128_offset(r, q & 7)) = p;
+        }
+    }
+}
+
+// the runs split three ways (x = hi + mid + lo, |x - hi - mid - lo| <= 2^-27 |x|)
+// into the swizzled hi / mid / lo tiles
+__device__ __forceinline__ void store_split3(const Runs &R, uint8_t *hi_tile, uint8_t *mid_tile, uint8_t *lo_tile)
+{
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int s = 0; s < kRuns; ++s) {
+        const int j = tid + kGemmThreads * s;
+        const int r = j >> 4, q = j & 15;
+        float h[4], m[4], l[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float r1;
+            split_bf16(R.v[s][i], h[i], r1);
+            split_bf16(r1, m[i], l[i]);
+        }
+        const uint32_t off = sw128_offset(r, q >> 1) + 8 * (q & 1);
+        *reinterpret_cast<uint2 *>(hi_tile + off) = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+        *reinterpret_cast<uint2 *>(mid_tile + off) = make_uint2(pack_bf16x2(m[0], m[1]), pack_bf16x2(m[2], m[3]));
+        *reinterpret_cast<uint2 *>(lo_tile + off) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
     }
 }
 
@@ -233,8 +283,19 @@ __device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *
         // the MMAs of chunk i - 2 read this stage: wait until they are done
         if (i >= 2) ok = __syncthreads_and(ok && mbar_wait(&bar_done[s], (uint32_t)(((i - 2) >> 1) & 1), abort));
         if (!ok) break;
-        store_split(ra, st, st + kTile);
-        store_split(rb, st + 2 * kTile, st + 3 * kTile);
+        if (g.operands == kGemmSplit) {
+            store_split(ra, st, st + kTile);
+            store_split(rb, st + 2 * kTile, st + 3 * kTile);
+        } else if (g.operands == kGemmSplit3) {
+            store_split3(ra, st, st + 4 * kTile, st + kTile);
+            store_split3(rb, st + 2 * kTile, st + 5 * kTile, st + 3 * kTile);
+        } else if (g.operands == kGemmBf16) {
+            store_round<kGemmBf16>(ra, st, st + kTile);
+            store_round<kGemmBf16>(rb, st + 2 * kTile, st + 3 * kTile);
+        } else {
+            store_round<kGemmTf32>(ra, st, st + kTile);
+            store_round<kGemmTf32>(rb, st + 2 * kTile, st + 3 * kTile);
+        }
         if (c + 1 < c_end) {
             load_runs(g.A, g.lda, g.M, g.K, m0, c + 1, vec_a, ra);
             load_runs(g.B, g.ldb, g.N, g.K, n0, c + 1, vec_b, rb);
@@ -245,12 +306,39 @@ __device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *
         tc_fence_after();
         if (tid == 0) {
             const uint32_t a_hi = smem_u32(st), a_lo = a_hi + kTile, b_hi = a_hi + 2 * kTile, b_lo = a_hi + 3 * kTile;
+            if (g.operands == kGemmSplit) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
-                mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_hi + 32 * k), id, acc);
-                mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_lo + 32 * k), id, 1u);
-                mma<true>(tmem, desc_sw128(a_lo + 32 * k), desc_sw128(b_hi + 32 * k), id, 1u);
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
+                    mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_hi + 32 * k), id, acc);
+                    mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_lo + 32 * k), id, 1u);
+                    mma<true>(tmem, desc_sw128(a_lo + 32 * k), desc_sw128(b_hi + 32 * k), id, 1u);
+                }
+            } else if (g.operands == kGemmSplit3) {
+                const uint32_t a_mi = a_hi + 4 * kTile, b_mi = a_hi + 5 * kTile;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
+                    // every product of parts down to 2^-16 relative: the dropped ones are below 2^-23
+                    mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_hi + 32 * k), id, acc);
+                    mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_mi + 32 * k), id, 1u);
+                    mma<true>(tmem, desc_sw128(a_mi + 32 * k), desc_sw128(b_hi + 32 * k), id, 1u);
+                    mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_lo + 32 * k), id, 1u);
+                    mma<true>(tmem, desc_sw128(a_lo + 32 * k), desc_sw128(b_hi + 32 * k), id, 1u);
+                    mma<true>(tmem, desc_sw128(a_mi + 32 * k), desc_sw128(b_mi + 32 * k), id, 1u);
+                }
+            } else if (g.operands == kGemmBf16) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma<true>(tmem, desc_sw128(a_hi + 32 * k), desc_sw128(b_hi + 32 * k), id, (i > 0 || k > 0) ? 1u : 0u);
+            } else {
+                constexpr uint32_t idt = idesc(false, kBM, kBN);
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma<false>(tmem, desc_sw128((t ? a_lo : a_hi) + 32 * k), desc_sw128((t ? b_lo : b_hi) + 32 * k),
+                                   idt, (i > 0 || t > 0 || k > 0) ? 1u : 0u);
             }
             mma_commit(&bar_done[s]);
         }

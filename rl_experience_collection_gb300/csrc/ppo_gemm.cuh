@@ -1,6 +1,8 @@
 // ppo_gemm.cuh -- the PPO update's tensor-core GEMM (ppo_gemm.cu):
 // C[M, N] = A[M, K] B[N, K]^T, float32 in and out, both operands row-major with
-// K contiguous, each product taken from a bf16 high/low split of its operands.
+// K contiguous, each product taken from a bf16 high/low split of its operands
+// (or, for a forward pass in the collector's operand format, from operands
+// rounded once to bf16 or tf32).
 // Up to kGemmGroup independent products run in one launch; a product may be
 // split along K over several CTAs, whose partial tiles the last CTA of each
 // tile adds in split order (so the result does not depend on scheduling).
@@ -11,6 +13,11 @@
 namespace rl {
 
 enum { kGemmFwd = 0, kGemmDw = 1, kGemmDx = 2 };
+// how the float32 operands enter the tensor cores
+enum { kGemmSplit = 0,   // bf16 high + low parts, three MMAs per product (relative error < 1.2e-5)
+       kGemmBf16 = 1,    // each operand rounded to bf16 (nearest even), one kind::f16 MMA
+       kGemmTf32 = 2,    // each operand rounded to tf32 (nearest, ties away), one kind::tf32 MMA
+       kGemmSplit3 = 3 };// bf16 high + middle + low parts, six MMAs per product (relative error < 2^-22)
 constexpr int kGemmGroup = 4;
 constexpr int kGemmTile = 128;            // C tile: 128 x 128
 constexpr int kGemmChunk = 64;            // K elements per chunk
@@ -22,6 +29,7 @@ struct GemmArgs {
     int ldb = 0;
     int M = 0, N = 0, K = 0;
     int epi = kGemmFwd;
+    int operands = kGemmSplit;
     // kGemmFwd: Y = C + bias[n] (ReLU when relu), YT = Y^T (optional)
     const float *bias = nullptr;
     int relu = 0;
