@@ -512,6 +512,14 @@ def run_oracle_sample(w: wl.Workload, inputs, n_eps: int, first: int = 0, thread
     return time.perf_counter() - t0, n_eps * w.horizon
 
 
+def workload_config(w: wl.Workload, n_episodes: int, horizon: int, world: int) -> dict:
+    """The `config` object of both arms' JSON lines (the same dict for the same
+    workload, so the two lines compare)."""
+    return {"workload": w.name, "episodes": n_episodes, "horizon": horizon, "n_bars": w.n_bars,
+            "critic": list(w.critic_h), "l2": "flushed between steps (512 MB write)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def reference_arm(args, w: wl.Workload, rank: int):
     if rank != 0:
         return
@@ -531,8 +539,7 @@ def reference_arm(args, w: wl.Workload, rank: int):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sum(times) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": w.name, "episodes": w.n_episodes, "horizon": w.horizon, "n_bars": w.n_bars,
-                       "mlp_dtype": w.dtype, "sample_episodes_per_step": n_eps},
+            "config": workload_config(w, w.n_episodes, w.horizon, args.gpus),
             "cpu_baseline": {"value": v, "unit": "tuples/s", "cores": threads, "kind": "oracle",
                              "nproc": cpu["nproc"], "cpu_model": cpu["model"],
                              "sample": f"{n_eps} episodes x {w.horizon} steps per step, episode-parallel "
@@ -660,9 +667,7 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "tuples/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.name, "episodes": N, "horizon": L, "n_bars": w.n_bars,
-                       "critic": list(w.critic_h), "l2": "flushed between steps (512 MB write)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": workload_config(w, N, L, world),
             "tensor_pipe_frac_step": (flop_step / (ms / 1000.0) / 1e12 / tpk) if tpk else None,
             "phase_ms": {"rollout": rollout_ms, "states": states_ms, "value": value_ms, "gae": gae_ms},
             "roofline": roofline, "clocks": clk.summary(), "gpu_launches": launches_per_run(w.dtype) * args.steps}

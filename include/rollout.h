@@ -94,10 +94,9 @@ typedef struct rollout_handle rollout_handle;
  *   it on return.
  * out: receives the handle on success (unchanged on failure).
  * Allocates device memory on the current device; all later calls must use
- * that device.  The kernels' shared-memory limits are raised once per
- * process, on the device of the first launch, so a process uses one device
- * (one process per GPU; handles on a second device fail with
- * ROLLOUT_ERR_CUDA).  Synchronous.  Returns ROLLOUT_OK, _INVALID,
+ * that device.  The kernels' shared-memory limits are raised once on each
+ * device that launches them, so handles on several devices of one process
+ * work side by side.  Synchronous.  Returns ROLLOUT_OK, _INVALID,
  * _UNSUPPORTED, _NOMEM or _CUDA.
  */
 ROLLOUT_API int rollout_create(const float *weights, const rollout_dims *dims, rollout_handle **out);

@@ -21,6 +21,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/rollout.h"
 
 namespace rl {
@@ -148,6 +150,23 @@ cudaError_t launch_states(const StatesArgs &a, cudaStream_t s);
 
 // --- GAE (gae.cu) ---
 cudaError_t launch_gae(const GaeArgs &a, cudaStream_t s);
+
+// Runs set_up() (a kernel's attribute calls) once per device, on the current
+// device, and remembers which devices are done; devices past 63 run it on
+// every call.  Returns its status.
+template <class F>
+inline cudaError_t once_per_device(std::atomic<unsigned long long> &done, F &&set_up)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return set_up();
+    const unsigned long long bit = 1ull << dev;
+    if (done.load() & bit) return cudaSuccess;
+    e = set_up();
+    if (e == cudaSuccess) done.fetch_or(bit);
+    return e;
+}
 
 // --- device allocations of rollout handles (api.cu) ---
 // Every device allocation a rollout handle makes goes through dev_alloc /

@@ -892,12 +892,15 @@ template <bool BF16, bool kDump>
 cudaError_t launch_p1(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
 {
     using G = P1Geo<BF16>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(phase1_umma_kernel<BF16, kDump>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    static std::atomic<unsigned long long> attr{0};   // devices whose attributes are set
+    {
+        const cudaError_t e_attr = once_per_device(attr, [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(phase1_umma_kernel<BF16, kDump>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+            if (e != cudaSuccess) return e;
+            return cudaSuccess;
+        });
+        if (e_attr != cudaSuccess) return e_attr;
     }
     const int blocks = (a.N + kP1Threads - 1) / kP1Threads;
     phase1_umma_kernel<BF16, kDump><<<blocks, kP1Threads, G::SMEM, s>>>(a, w, fmap);
@@ -908,12 +911,15 @@ template <bool kDump>
 cudaError_t launch_bf16(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s)
 {
     using G = P1Geo<true>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(phase1_bf16_kernel<kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             G::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    static std::atomic<unsigned long long> attr{0};   // devices whose attributes are set
+    {
+        const cudaError_t e_attr = once_per_device(attr, [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(phase1_bf16_kernel<kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 G::SMEM);
+            if (e != cudaSuccess) return e;
+            return cudaSuccess;
+        });
+        if (e_attr != cudaSuccess) return e_attr;
     }
     const int blocks = (a.N + kP1Threads - 1) / kP1Threads;
     phase1_bf16_kernel<kDump><<<blocks, kQThreads, G::SMEM, s>>>(a, w, fmap);

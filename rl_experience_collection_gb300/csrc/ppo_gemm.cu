@@ -465,11 +465,14 @@ void gemm_plan(GemmArgs &g, int max_split, long long *ws_floats, int *counters)
 
 cudaError_t launch_gemm_group(const GemmArgs *g, int n, cudaStream_t s)
 {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    static std::atomic<unsigned long long> attr{0};   // devices whose attributes are set
+    {
+        const cudaError_t e_attr = once_per_device(attr, [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(gemm_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+            if (e != cudaSuccess) return e;
+            return cudaSuccess;
+        });
+        if (e_attr != cudaSuccess) return e_attr;
     }
     if (n < 1 || n > kGemmGroup) return cudaErrorInvalidValue;
     GemmGroup grp{};

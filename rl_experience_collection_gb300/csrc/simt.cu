@@ -317,12 +317,15 @@ __global__ void __launch_bounds__(kVThreads) value_simt_kernel(ValueArgs a, Simt
 cudaError_t launch_phase1_simt(const Phase1Args &a, const float *actor_packed, cudaStream_t s)
 {
     const size_t smem = sizeof(float) * (kActorPacked + (kState + kActorH1 + kActorH2) * kP1Threads);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(phase1_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    static std::atomic<unsigned long long> attr{0};   // devices whose attributes are set
+    {
+        const cudaError_t e_attr = once_per_device(attr, [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(phase1_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            return cudaSuccess;
+        });
+        if (e_attr != cudaSuccess) return e_attr;
     }
     const int blocks = (a.N + kP1Threads - 1) / kP1Threads;
     phase1_simt_kernel<<<blocks, kP1Threads, smem, s>>>(a, actor_packed);
@@ -333,12 +336,15 @@ template <int ROWS, int LD>
 static cudaError_t launch_value_t(const ValueArgs &a, const SimtWeights &w, cudaStream_t s)
 {
     const size_t smem = sizeof(float) * (2 * ROWS * LD + ROWS * (56 + 64 + 56));
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(value_simt_kernel<ROWS, LD>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    static std::atomic<unsigned long long> attr{0};   // devices whose attributes are set
+    {
+        const cudaError_t e_attr = once_per_device(attr, [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(value_simt_kernel<ROWS, LD>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            return cudaSuccess;
+        });
+        if (e_attr != cudaSuccess) return e_attr;
     }
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);

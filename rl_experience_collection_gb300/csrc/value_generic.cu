@@ -490,18 +490,21 @@ template <bool BF16>
 cudaError_t launch_g(const ValueArgs &a, const UmmaWeights &w, uint8_t *scratch, long long per_cta, int grid,
                      cudaStream_t s, bool stall)
 {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(value_generic_kernel<BF16, false, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(value_generic_kernel<BF16, true, false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(value_generic_kernel<BF16, false, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    static std::atomic<unsigned long long> attr{0};   // devices whose attributes are set
+    {
+        const cudaError_t e_attr = once_per_device(attr, [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(value_generic_kernel<BF16, false, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(value_generic_kernel<BF16, true, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(value_generic_kernel<BF16, false, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            if (e != cudaSuccess) return e;
+            return cudaSuccess;
+        });
+        if (e_attr != cudaSuccess) return e_attr;
     }
     if (stall) value_generic_kernel<BF16, true, false><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);
     else if (a.dump.p) value_generic_kernel<BF16, false, true><<<grid, kThreads, kSmem, s>>>(a, w, scratch, per_cta);

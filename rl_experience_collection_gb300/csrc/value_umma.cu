@@ -864,18 +864,21 @@ cudaError_t launch_value_umma(const ValueArgs &a, const UmmaWeights &w, cudaStre
     if ((reinterpret_cast<uintptr_t>(a.F) & 15u) != 0) return cudaErrorInvalidValue;   // feature copies
     for (int u = 0; u < w.n_units; ++u)
         if (w.unit_bytes[u] > (uint32_t)kStage || (w.unit_bytes[u] & 15u) || (w.unit_off[u] & 15)) return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(value_umma_bf16_kernel<false, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(value_umma_bf16_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(value_umma_bf16_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    static std::atomic<unsigned long long> attr{0};   // devices whose attributes are set
+    {
+        const cudaError_t e_attr = once_per_device(attr, [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(value_umma_bf16_kernel<false, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(value_umma_bf16_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(value_umma_bf16_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmem);
+            if (e != cudaSuccess) return e;
+            return cudaSuccess;
+        });
+        if (e_attr != cudaSuccess) return e_attr;
     }
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);

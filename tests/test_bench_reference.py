@@ -19,6 +19,12 @@ def _check(line, n_gpus):
     assert line["impl"] == "reference" and line["n_gpus"] == n_gpus
     assert line["value"] > 0 and line["unit"] == "tuples/s" and line["higher_is_better"] is True
     assert line["steps"] == 2 and line["warmup"] >= 3 and line["data"] == "synthetic"
+    # the same config object as the GPU arm's line for this workload
+    sys.path.insert(0, ROOT)
+    import bench
+    from rl_experience_collection_gb300 import workloads as wl
+    w = wl.WORKLOADS["tiny_fp32"]
+    assert line["config"] == bench.workload_config(w, w.n_episodes, w.horizon, n_gpus)
     assert line["config"]["workload"] == "tiny_fp32"
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == os.cpu_count() and cb["value"] == line["value"] and cb["sample"]
