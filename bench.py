@@ -726,7 +726,7 @@ def main():
             "target_roofline": {"bound": "tensor", "achieved": t_fl / (t_ms / 1000.0) / 1e12, "peak": peak_b,
                                 "unit": "TFLOP/s", "frac": t_fl / (t_ms / 1000.0) / 1e12 / peak_b,
                                 "algorithmic_flop_per_launch": t_fl},
-            "gpu_launches_per_run": 3, "l2": "flushed between runs"}
+            "gpu_launches_per_run": 4, "l2": "flushed between runs"}
         out = binding.make_outputs(N, L, dev)
 
     # ---------------- end to end through the C ABI with host buffers (rollout_run_host:

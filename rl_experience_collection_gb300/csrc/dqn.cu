@@ -24,12 +24,15 @@
 // Between the phases out_td holds V entering each step and a handle-owned
 // array V' after the trade.
 //
-// Warp roles (both kernels): warps 0-7 are row warps (warp w serves TMEM lanes
-// and rows 32 (w % 4) .. + 31 and the column half w / 4 of each layer), warps
-// 8-10 stream the weights, warp 8 + s filling ring stage s (the bulk copies of
-// one warp complete one after another, those of different warps overlap), and
-// warp 11 allocates TMEM and one lane issues the MMAs.  Every wait is bounded; a wait that gives up sets a flag
-// that ends every role's loop, and the status word records the timeout.
+// Warp roles of the rollout kernel: warps 0-7 are row warps (warp w serves
+// TMEM lanes and rows 32 (w % 4) .. + 31 and the column half w / 4 of each
+// layer), warps 8-10 stream the weights, warp 8 + s filling ring stage s (the
+// bulk copies of one warp complete one after another, those of different
+// warps overlap), and warp 11 allocates TMEM and one lane issues the MMAs.
+// The target pass has 16 row warps (column quarters) and overlaps each
+// layer's epilogue with the next layer's MMAs (see its comment).  Every wait
+// is bounded; a wait that gives up sets a flag that ends every role's loop,
+// and the status word records the timeout.
 #include <math.h>
 #include <string.h>
 
@@ -87,6 +90,7 @@ struct RolloutArgs {
 
 struct TargetArgs {
     const float *F;
+    const float *Fpad;   // F with rows padded to kFPad floats (16-byte aligned)
     const int32_t *starts;
     int N, L, n_bars;
     float gamma;
@@ -410,27 +414,231 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_rollout_kernel(RolloutArgs a,
 
 // ---------------------------------------------------------------------------
 // target pass: curiosity and the target network over every transition
+//
+// Persistent CTAs over tiles of 128 transitions.  Warp roles: 16 row warps
+// (warp w serves TMEM lanes / rows 32 (w % 4) .. + 31 and the column quarter
+// w / 4 of every 64-column chunk), three producer warps (warp kTProd0 + s fills
+// ring stage s), one MMA warp (TMEM allocation; one lane issues), and four
+// builder warps that write the next tile's operand rows X and X' while the
+// row warps drain the current one.
+//
+// TMEM holds two 256-column regions.  The j-th tile of a CTA puts target
+// layers 1 and 3 and the head into region s = j & 1 and layer 2 into the
+// other one, so every layer starts on its first K-chunk while the rows still
+// drain the rest of the previous layer, and the next tile's layer 1 runs
+// while this tile's layer 3 drains.  The curiosity model takes the 64 columns that a drained
+// chunk leaves free: layer 1 at [0, 64) of region s once H1's chunk 0 is out,
+// layer 2 at [0, 64) of the other region once H2's chunk 0 is out.  The head
+// (N = 48) accumulates into [0, 48) of region s, which H3's chunk 0 frees.
+//
+// Per tile the MMA lane takes its weight units in this order (the producers
+// stream them in the same order): W2 chunk 0, C1, W2 chunks 1-3, W3 chunk 0,
+// C2, W3 chunks 1-3, the head, the next tile's W1 (none after the last tile);
+// the CTA's first tile is preceded by its W1.
+constexpr int kTRowWarps = 16;
+constexpr int kTBuilders = 4;                     // X / X' builder warps, 32 rows each
+constexpr int kTProd0 = kTRowWarps, kTMma = kTProd0 + kStages, kTBuild0 = kTMma + 1;
+constexpr int kTThreads = (kTBuild0 + kTBuilders) * 32;
+constexpr int kTUnitsPerTile = 12;
 
 struct TBars {
     uint64_t full[kStages], empty[kStages];
-    uint64_t x_ready;     // rows -> MMA: X and X' of the tile are written (8 warp arrivals)
-    uint64_t z_ready;     // rows -> MMA: the curiosity hidden layer Z is written
-    uint64_t h_ready;     // rows -> MMA: a hidden layer of the target net is in H (3 a tile)
-    uint64_t acc_c;       // MMA -> rows: curiosity layer 1, then 2 (2 a tile)
-    uint64_t acc_q;       // MMA -> rows: target layers 1..3 and the head (4 a tile)
-    uint64_t mse_ready;   // column half 1 -> half 0: its share of the curiosity error (4 warp arrivals)
+    uint64_t x;             // builders -> MMA: X and X' of a tile are written
+    uint64_t h1[4], h2[4], h3[4];   // rows -> MMA: K-chunk c of a hidden layer is in Hb
+    uint64_t z;             // rows -> MMA: the curiosity hidden layer Z is written
+    uint64_t cz;            // rows -> MMA: curiosity layer 2's columns are read
+    uint64_t hd_free;       // quarter-0 row warps -> MMA: the head's columns are read
+    uint64_t q1, c1, q2, c2, q3, hd;   // MMA -> rows: that group of MMAs is complete
+    uint64_t mse[4];        // quarters 1-3 -> quarter 0 of the same lanes: partial sums written
     uint64_t fin;
 };
 
-constexpr int kTSmem = 1024 + 3 * kChunk + 4 * kChunk + kStages * kStage + (kBiasFloats + 128 + 128) * 4 + 1024;
-static_assert(kTSmem <= 232448 - 2048, "target pass shared memory");
-constexpr uint32_t kTmemQ = 0, kTmemC1 = 256, kTmemC2 = 320;
+constexpr int kOneHotLd = 72;                        // bf16 per one-hot row (64 + 8: rows start on different banks)
+constexpr int kTFloats = kBiasFloats + 128 + 3 * 128 + 2 * 128 + 2 * 128 + 128;
+constexpr int kTSmem = 1024 + 3 * kChunk + 4 * kChunk + kStages * kStage + kTFloats * 4 + kActions * kOneHotLd * 2 + 1024;
+static_assert(kTSmem <= 232448, "target pass shared memory");
+static_assert(sizeof(TBars) <= 1024, "target pass barriers");
+
+// unit g of a CTA (12 a tile, the last tile's 11 ending with its head): its
+// byte offset and size in the weight image (see the order above)
+__device__ __forceinline__ void target_unit(const DqnImage &w, long long g, long long &off, uint32_t &bytes)
+{
+    int u;            // 0 W1, 1-4 W2, 5-8 W3, 9 head, 10 C1, 11 C2
+    if (g == 0) {
+        u = 0;
+    } else {
+        const long long k = g - 1, j = k / kTUnitsPerTile;
+        int pos = (int)(k - j * kTUnitsPerTile);
+        // positions 0..11 -> units 1, 10, 2, 3, 4, 5, 11, 6, 7, 8, 9, 0 (a nibble each)
+        u = (int)((0x0987'6B54'32A1ull >> (4 * pos)) & 15u);
+    }
+    if (u >= 10) {
+        off = w.unit_off[kNetUnits] + (u - 10) * kCurTile;
+        bytes = kCurTile;
+    } else {
+        off = w.unit_off[kNetUnits + 1 + u];
+        bytes = w.unit_bytes[kNetUnits + 1 + u];
+    }
+}
+
+// one transition's inputs to the target pass, loaded a tile ahead: every
+// address depends on the row index only, so the loads are issued together
+struct TMeta {
+    long long i;     // flat transition index
+    int valid;       // i < N L and the episode's start is in range
+    int act, done, start, t, aprev, dprev;
+    float r0, qs, vin, vp;
+};
+
+__device__ __forceinline__ void load_meta(const TargetArgs &a, long long tile, int r, TMeta &m)
+{
+    const long long R = (long long)a.N * a.L;
+    m.i = tile * 128 + r;
+    const long long ic = m.i < R ? m.i : R - 1;
+    const long long n = ic <= 0x7fffffffLL ? (long long)((uint32_t)ic / (uint32_t)a.L) : ic / a.L;
+    m.t = (int)(ic - n * a.L);
+    const long long ip = m.t > 0 ? ic - 1 : ic;
+    m.start = __ldg(a.starts + n);
+    m.act = a.actions[ic];
+    m.done = a.dones[ic];
+    m.r0 = a.rewards[ic];
+    m.qs = a.q[ic];
+    m.vin = a.td[ic];
+    m.vp = a.v_post[ic];
+    m.aprev = a.actions[ip];
+    m.dprev = a.dones[ip];
+}
+
+// validity and the derived fields, once the loads have landed
+__device__ __forceinline__ void resolve_meta(const TargetArgs &a, TMeta &m)
+{
+    const long long R = (long long)a.N * a.L;
+    m.valid = m.i < R && start_ok(m.start, a.L, a.n_bars);
+    // the one-hot row read stays in bounds whatever the rollout left here
+    // (its rows after a give-up are unwritten)
+    if (!m.valid || (unsigned)m.act >= (unsigned)kActions) m.act = 0;
+}
+
+// the market columns of [16 q, 16 q + 16) of a padded feature row (zero past
+// column 50 or when !valid), in 16-byte loads; state16_tail then fills V, e,
+// spread into columns 51-53
+__device__ __forceinline__ void feat16(const float *Fprow, int q, bool valid, float (&v)[16])
+{
+    const float4 *src = reinterpret_cast<const float4 *>(Fprow) + 4 * q;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid && 16 * q + 4 * k < kMarket) f = __ldg(src + k);
+        v[4 * k + 0] = f.x;
+        v[4 * k + 1] = f.y;
+        v[4 * k + 2] = f.z;
+        v[4 * k + 3] = f.w;
+    }
+    if (q == 3) v[kMarket - 48] = 0.f;   // column 51 of the padded row is not a market column
+}
+
+__device__ __forceinline__ void state16_tail(float V, float e, float spread, int q, bool valid, float (&v)[16])
+{
+    if (q == 3 && valid) {
+        v[kMarket - 48] = V;
+        v[kMarket + 1 - 48] = e;
+        v[kMarket + 2 - 48] = spread;
+    }
+}
+
+// one whole operand row: [F[b, 0..50], V, e, spread, 0 x 10] rounded to bf16
+// into row r of a 64-column 128-byte-swizzled tile (zeros when !valid); Fprow
+// is the padded feature row (13 16-byte loads, in flight together)
+__device__ __forceinline__ void state_row(uint8_t *tile, int r, const float *Fprow, bool valid, float V, float e,
+                                          float spread)
+{
+    const float4 *src = reinterpret_cast<const float4 *>(Fprow);
+    float4 f[13];
+#pragma unroll
+    for (int k = 0; k < 13; ++k) f[k] = valid ? __ldg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 6; ++u) {
+        uint4 p;
+        p.x = pack_bf16x2(f[2 * u].x, f[2 * u].y);
+        p.y = pack_bf16x2(f[2 * u].z, f[2 * u].w);
+        p.z = pack_bf16x2(f[2 * u + 1].x, f[2 * u + 1].y);
+        p.w = pack_bf16x2(f[2 * u + 1].z, f[2 * u + 1].w);
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(r, u)) = p;
+    }
+    uint4 p;
+    p.x = pack_bf16x2(f[12].x, f[12].y);
+    p.y = pack_bf16x2(f[12].z, valid ? V : 0.f);
+    p.z = valid ? pack_bf16x2(e, spread) : 0u;
+    p.w = 0u;
+    *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 6)) = p;
+    *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 7)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// 16 values rounded to bf16 into a 128-byte-swizzled operand chunk, at the
+// byte offsets of the row's two 16-byte units (sw128_offset)
+__device__ __forceinline__ void put16(uint8_t *chunk, uint32_t off0, uint32_t off1, const float (&v)[16])
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint4 p;
+        p.x = pack_bf16x2(v[8 * h + 0], v[8 * h + 1]);
+        p.y = pack_bf16x2(v[8 * h + 2], v[8 * h + 3]);
+        p.z = pack_bf16x2(v[8 * h + 4], v[8 * h + 5]);
+        p.w = pack_bf16x2(v[8 * h + 6], v[8 * h + 7]);
+        *reinterpret_cast<uint4 *>(chunk + (h ? off1 : off0)) = p;
+    }
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t x[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
+          "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15])
+        : "r"(taddr)
+        : "memory");
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(x[i]);
+}
+
+// 16 accumulator columns + bias (16-byte aligned), LeakyReLU, bf16 into the
+// operand chunk; max(y, 0.01 y) is LeakyReLU(0.01) exactly, signed zeros included
+__device__ __forceinline__ void drain16_leaky(uint32_t taddr, const float *bias, uint8_t *chunk, uint32_t off0,
+                                              uint32_t off1)
+{
+    float v[16];
+    tmem_ld16(taddr, v);
+    const float4 *b4 = reinterpret_cast<const float4 *>(bias);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 b = b4[k];
+        v[4 * k + 0] += b.x;
+        v[4 * k + 1] += b.y;
+        v[4 * k + 2] += b.z;
+        v[4 * k + 3] += b.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = fmaxf(v[k], 0.01f * v[k]);
+    put16(chunk, off0, off1, v);
+}
+
+// one arrival per warp after every lane's shared-memory writes and TMEM reads
+__device__ __forceinline__ void publish(uint64_t *bar)
+{
+    fence_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 
 // kStall: a test build in which the first producer of CTA 0 issues no copy, so
 // that CTA's MMA issuer waits on a weight stage that never fills and the
 // bounded-wait exit runs (dqn_test_stall)
 template <bool kStall>
-__global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, DqnImage w)
+__global__ void __launch_bounds__(kTThreads, 1) dqn_target_kernel(TargetArgs a, DqnImage w)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -439,8 +647,12 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, D
     uint8_t *ring = Hb + 4 * kChunk;
     float *bias = reinterpret_cast<float *>(ring + kStages * kStage);
     float *cb1 = bias + kBiasFloats, *cb2 = cb1 + 64;
-    float *mse_part = cb2 + 64;
-    TBars *bars = reinterpret_cast<TBars *>(mse_part + 128);
+    float *mse_part = cb2 + 64;                        // [3][128]: curiosity partial sums of quarters 1-3
+    float *hsum = mse_part + 3 * 128;                  // [2][128]: advantage partial sums of quarters 1, 2
+    float *hmax = hsum + 2 * 128;                      // [2][128]: advantage partial maxima of quarters 1, 2
+    float *hval = hmax + 2 * 128;                      // [128]: V (quarter 2)
+    uint16_t *onehot = reinterpret_cast<uint16_t *>(hval + 128);   // [45][kOneHotLd] bf16 C1[:, 54 + a]
+    TBars *bars = reinterpret_cast<TBars *>(onehot + kActions * kOneHotLd);
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
@@ -450,22 +662,35 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, D
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
-        mbar_init(&bars->x_ready, kRowWarps);
-        mbar_init(&bars->z_ready, kRowWarps);
-        mbar_init(&bars->h_ready, kRowWarps);
-        mbar_init(&bars->acc_c, 1);
-        mbar_init(&bars->acc_q, 1);
-        mbar_init(&bars->mse_ready, kRowWarps / 2);
+        mbar_init(&bars->x, kTBuilders);
+        for (int c = 0; c < 4; ++c) {
+            mbar_init(&bars->h1[c], kTRowWarps);
+            mbar_init(&bars->h2[c], kTRowWarps);
+            mbar_init(&bars->h3[c], kTRowWarps);
+            mbar_init(&bars->mse[c], 3);
+        }
+        mbar_init(&bars->z, kTRowWarps);
+        mbar_init(&bars->cz, kTRowWarps);
+        mbar_init(&bars->hd_free, 12);
+        mbar_init(&bars->q1, 1);
+        mbar_init(&bars->c1, 1);
+        mbar_init(&bars->q2, 1);
+        mbar_init(&bars->c2, 1);
+        mbar_init(&bars->q3, 1);
+        mbar_init(&bars->hd, 1);
         mbar_init(&bars->fin, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
-    for (int i = tid; i < kBiasFloats; i += kThreads) bias[i] = w.target_bias[i];
-    for (int i = tid; i < 64; i += kThreads) {
+    for (int i = tid; i < kBiasFloats; i += kTThreads) bias[i] = w.target_bias[i];
+    for (int i = tid; i < 64; i += kTThreads) {
         cb1[i] = w.cur_b1[i];
         cb2[i] = w.cur_b2[i];
     }
-    if (warp == kMmaWarp) {
+    // the one-hot columns are bf16 values already: their upper halves are exact
+    for (int i = tid; i < kActions * 64; i += kTThreads)
+        onehot[(i >> 6) * kOneHotLd + (i & 63)] = (uint16_t)(__float_as_uint(w.cur_onehot[i]) >> 16);
+    if (warp == kTMma) {
         tmem_alloc(&tmem_base_s, 512);
         tmem_relinquish();
     }
@@ -476,215 +701,371 @@ __global__ void __launch_bounds__(kThreads, 1) dqn_target_kernel(TargetArgs a, D
     const long long R = (long long)a.N * a.L;
     const long long n_tiles = (R + 127) / 128;
 
-    if (warp < kRowWarps) {
+    if (warp < kTRowWarps) {
         // ------------------------------------------------------------ rows
-        const int quad = warp & 3, hf = warp >> 2, r = quad * 32 + lane;
-        const int c0 = state_c0(hf);
-        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
-        uint32_t pc = 0, pq = 0, it = 0;
+        const int quad = warp & 3, q = warp >> 2, r = quad * 32 + lane;
+        const uint32_t lane_t = tmem + ((uint32_t)(quad * 32) << 16) + 16 * q;
+        const uint32_t off0 = sw128_offset(r, 2 * q), off1 = sw128_offset(r, 2 * q + 1);
+        uint32_t it = 0;
         bool ok = true;
-        for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
-            const long long i = tile * 128 + r;
-            bool valid = i < R;
-            int act = 0, done = 0;
-            float r0 = 0.f, qs = 0.f, vin = 0.f, vp = 0.f, e_in = 0.f;
-            long long b = 0;
-            if (valid) {
-                const long long n = i / a.L;
-                const int t = (int)(i - n * a.L);
-                const int start = __ldg(a.starts + n);
-                valid = start_ok(start, a.L, a.n_bars);
-                if (valid) {
-                    b = (long long)start + t;
-                    act = a.actions[i];
-                    // the one-hot row read below stays in bounds whatever the
-                    // rollout left here (its rows after a give-up are unwritten)
-                    if ((unsigned)act >= (unsigned)kActions) act = 0;
-                    done = a.dones[i];
-                    r0 = a.rewards[i];
-                    qs = a.q[i];
-                    vin = a.td[i];
-                    vp = a.v_post[i];
-                    e_in = (t == 0 || a.dones[i - 1]) ? 0.f : exposure_of(a.actions[i - 1]);
-                }
-            }
-            float xn[32];
-            {
-                float v[32];
-                state_cols(a.F + b * kMarket, vin, e_in, a.env.spread, hf, valid, v);
-                put32(X, r, c0, v);
-                state_cols(a.F + (b + 1) * kMarket, vp, exposure_of(act), a.env.spread, hf, valid, xn);
-                put32(Xn, r, c0, xn);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->x_ready);
-            // curiosity layer 1: Z = ReLU(X C1^T + c1 + C1[:, 54 + a])
-            if (!warp_wait(&bars->acc_c, pc & 1, &abort_flag)) break;
-            ++pc;
+        auto wait = [&](uint64_t *bar) {
+            ok = ok && warp_wait(bar, it & 1, &abort_flag);
             tc_fence_after();
-            {
-                float v[32];
-                tmem_ld32(taddr + kTmemC1 + c0, v);
-                tmem_ld_wait();
-                const float *oh = w.cur_onehot + act * 64 + c0;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = relu(v[k] + cb1[c0 + k] + __ldg(oh + k));
-                put32(Z, r, c0, v);
+        };
+        TMeta cur;
+        for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
+            const uint32_t rs = (it & 1) * 256, ro = 256 - rs;
+            load_meta(a, tile, r, cur);                    // first used by curiosity layer 1
+            // layer 1 of the target net (region s) -> H1, chunk by chunk
+            wait(&bars->q1);
+            if (!ok) break;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                drain16_leaky(lane_t + rs + 64 * c, bias + 64 * c + 16 * q, Hb + c * kChunk, off0, off1);
+                publish(&bars->h1[c]);
             }
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->z_ready);
-            // target layer 1, then curiosity layer 2, then target layers 2, 3
-            float cur = 0.f;
-            for (int l = 0; l < 3 && ok; ++l) {
-                if (!warp_wait(&bars->acc_q, pq & 1, &abort_flag)) { ok = false; break; }
-                ++pq;
-                tc_fence_after();
+            // x' (this quarter's columns, float32) for the curiosity error, in
+            // flight until curiosity layer 2; issued before the builders' loads
+            // of the next tile begin (they wait for curiosity layer 1)
+            resolve_meta(a, cur);
+            float xn[16];
+            {
+                const long long b = cur.valid ? (long long)cur.start + cur.t : 0;
+                feat16(a.Fpad + (b + 1) * kFPad, q, cur.valid, xn);
+                state16_tail(cur.vp, exposure_of(cur.act), a.env.spread, q, cur.valid, xn);
+            }
+            // curiosity layer 1 ([0, 64) of region s): Z = ReLU(X C1^T + c1 + C1[:, 54 + a])
+            wait(&bars->c1);
+            if (!ok) break;
+            {
+                float v[16];
+                tmem_ld16(lane_t + rs, v);
+                const uint4 *oh = reinterpret_cast<const uint4 *>(onehot + cur.act * kOneHotLd + 16 * q);
+                const float4 *b4 = reinterpret_cast<const float4 *>(cb1 + 16 * q);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int cc = hf * 128 + 32 * j;
-                    drain32_leaky(taddr + kTmemQ, cc, bias + l * kH, Hb, r, cc);
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 o = oh[h];
+                    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 of = unpack_bf16x2(ow[k]);
+                        const int j = 8 * h + 2 * k;
+                        const float4 b = b4[j >> 2];
+                        const float b0 = (j & 3) ? b.z : b.x, b1 = (j & 3) ? b.w : b.y;
+                        v[j] = relu(v[j] + b0 + of.x);
+                        v[j + 1] = relu(v[j + 1] + b1 + of.y);
+                    }
                 }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->h_ready);
-                if (l == 0) {
-                    // curiosity layer 2: squared error against x' over the 54 state columns
-                    if (!warp_wait(&bars->acc_c, pc & 1, &abort_flag)) { ok = false; break; }
-                    ++pc;
-                    tc_fence_after();
-                    float v[32];
-                    tmem_ld32(taddr + kTmemC2 + c0, v);
-                    tmem_ld_wait();
-                    float part = 0.f;
+                put16(Z, off0, off1, v);
+            }
+            publish(&bars->z);
+            // layer 2 (the other region) -> H2
+            wait(&bars->q2);
+            if (!ok) break;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                drain16_leaky(lane_t + ro + 64 * c, bias + kH + 64 * c + 16 * q, Hb + c * kChunk, off0, off1);
+                publish(&bars->h2[c]);
+            }
+            // curiosity layer 2 ([0, 64) of the other region): squared error
+            // against x' over the 54 state columns
+            wait(&bars->c2);
+            if (!ok) break;
+            float part = 0.f;
+            {
+                float v[16];
+                tmem_ld16(lane_t + ro, v);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        if (c0 + k < kState) {
-                            const float dlt = (v[k] + cb2[c0 + k]) - xn[k];
-                            part += dlt * dlt;
-                        }
-                    tc_fence_before();
-                    if (hf == 1) {
-                        mse_part[r] = part;
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bars->mse_ready);
-                    } else {
-                        if (!warp_wait(&bars->mse_ready, it & 1, &abort_flag)) { ok = false; break; }
-                        cur = a.env.cur_coef * ((mse_part[r] + part) / (float)kState);
+                for (int k = 0; k < 16; ++k)
+                    if (16 * q + k < kState) {
+                        const float dlt = (v[k] + cb2[16 * q + k]) - xn[k];
+                        part += dlt * dlt;
+                    }
+            }
+            publish(&bars->cz);
+            if (q != 0) mse_part[(q - 1) * 128 + r] = part;
+            if (q == 3) {                                   // no head columns: its share is complete
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->mse[quad]);
+            }
+            if (a.next_states && cur.i < R) {
+                float *dst = a.next_states + cur.i * kState + 16 * q;
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    if (16 * q + k < kState) dst[k] = cur.valid ? xn[k] : 0.f;
+            }
+            // layer 3 (region s) -> H3
+            wait(&bars->q3);
+            if (!ok) break;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                drain16_leaky(lane_t + rs + 64 * c, bias + 2 * kH + 64 * c + 16 * q, Hb + c * kChunk, off0,
+                              off1);
+                publish(&bars->h3[c]);
+            }
+            // the head ([0, 48) of region s); every warp waits for it, since the
+            // next tile's H1 overwrites the H3 it reads
+            wait(&bars->hd);
+            if (!ok) break;
+            if (q < 3) {
+                // advantage columns 16 q .. 16 q + 15 (V at column 45): this
+                // quarter's sum (in column order) and maximum of A_j = D_j + b_j.
+                // Q_j = V + (A_j - mean A) is nondecreasing in A_j under float
+                // rounding, so max_j Q_j = V + (max_j A_j - mean A) exactly.
+                // The TMEM load is warp-wide (.sync.aligned): every lane issues it,
+                // rows past the end included; only stores are per row.
+                float d[16], sA = 0.f, mA = -INFINITY, V = 0.f;
+                tmem_ld16(lane_t + rs, d);
+                publish(&bars->hd_free);
+                const float *bh = bias + 3 * kH + 16 * q;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int j = 16 * q + k;
+                    const float A = d[k] + bh[k];
+                    if (j < kActions) {
+                        sA += A;
+                        mA = fmaxf(mA, A);
+                    } else if (j == kActions) {
+                        V = A;
+                    }
+                }
+                if (q > 0) {
+                    hsum[(q - 1) * 128 + r] = sA;
+                    hmax[(q - 1) * 128 + r] = mA;
+                    if (q == 2) hval[r] = V;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->mse[quad]);
+                } else {
+                    ok = warp_wait(&bars->mse[quad], it & 1, &abort_flag);
+                    if (!ok) break;
+                    const float sumA = (sA + hsum[r]) + hsum[128 + r];
+                    const float maxA = fmaxf(fmaxf(mA, hmax[r]), hmax[128 + r]);
+                    const float Vh = hval[r];
+                    const float meanA = sumA / (float)kActions;
+                    const float qmax = Vh + (maxA - meanA);
+                    const float mse = part + mse_part[r] + mse_part[128 + r] + mse_part[256 + r];
+                    const float cur_bonus = a.env.cur_coef * (mse / (float)kState);
+                    if (cur.valid) {
+                        const float rew = cur.r0 + cur_bonus;
+                        a.rewards[cur.i] = rew;
+                        a.td[cur.i] = fabsf(rew + a.gamma * qmax * (1.f - (float)cur.done) - cur.qs);
+                    } else if (cur.i < R) {
+                        a.rewards[cur.i] = 0.f;
+                        a.td[cur.i] = 0.f;
                     }
                 }
             }
-            if (!ok || !warp_wait(&bars->acc_q, pq & 1, &abort_flag)) break;
-            ++pq;
-            tc_fence_after();
-            if (hf == 0) {
-                // the TMEM loads are warp-wide (.sync.aligned): every lane of the
-                // warp issues them, rows past the end included; only stores are per row
-                float d0[32], d1[32];
-                tmem_ld32(taddr + kTmemQ, d0);
-                tmem_ld32(taddr + kTmemQ + 32, d1);
-                tmem_ld_wait();
-                const float *bh = bias + 3 * kH;
-                float sumA = 0.f;
-#pragma unroll
-                for (int j = 0; j < kActions; ++j) sumA += (j < 32 ? d0[j] : d1[j - 32]) + bh[j];
-                const float V = d1[kActions - 32] + bh[kActions];
-                const float meanA = sumA / (float)kActions;
-                float qmax = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < kActions; ++j) qmax = fmaxf(qmax, V + (((j < 32 ? d0[j] : d1[j - 32]) + bh[j]) - meanA));
-                if (valid) {
-                    const float rew = r0 + cur;
-                    a.rewards[i] = rew;
-                    a.td[i] = fabsf(rew + a.gamma * qmax * (1.f - (float)done) - qs);
-                } else if (i < R) {
-                    a.rewards[i] = 0.f;
-                    a.td[i] = 0.f;
-                }
-            }
-            if (a.next_states && i < R) {
-                float *dst = a.next_states + i * kState + c0;
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (c0 + k < kState) dst[k] = valid ? xn[k] : 0.f;
-            }
-            tc_fence_before();
         }
-    } else if (warp < kMmaWarp) {
-        const int st = warp - kProdWarp0;
+    } else if (warp < kTMma) {
+        // ------------------------------------------------------------ weight stream, stage st
+        const int st = warp - kTProd0;
         if (lane == 0) {
-            const long long my_tiles = n_tiles > blockIdx.x ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-            const long long total = (kStall && blockIdx.x == 0 && st == 0) ? 0 : my_tiles * kTargetUnits;
+            const long long n_my = n_tiles > blockIdx.x ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+            const long long total = (kStall && blockIdx.x == 0 && st == 0) ? 0 : kTUnitsPerTile * n_my;
             long long last = -1;
             for (long long u = st; u < total; u += kStages) {
-                const int i = kNetUnits + (int)(u % kTargetUnits);
+                long long off;
+                uint32_t bytes;
+                target_unit(w, u, off, bytes);
                 if (u >= kStages && !mbar_wait(&bars->empty[st], (uint32_t)((u / kStages - 1) & 1), &abort_flag))
                     break;
-                mbar_arrive_expect_tx(&bars->full[st], w.unit_bytes[i]);
-                bulk_g2s(ring + st * kStage, w.base + w.unit_off[i], w.unit_bytes[i], &bars->full[st]);
+                mbar_arrive_expect_tx(&bars->full[st], bytes);
+                bulk_g2s(ring + st * kStage, w.base + off, bytes, &bars->full[st]);
                 last = u;
             }
+            // its last copy completes before the CTA may exit
             if (last >= 0) mbar_wait_drain(&bars->full[st], (uint32_t)((last / kStages) & 1));
         }
+    } else if (warp >= kTBuild0) {
+        // ------------------------------------------------------------ X and X' builders
+        // Build a tile's operand rows while the row warps drain the previous
+        // tile, builder w taking rows 32 w .. 32 w + 31: X = the state rows; X'
+        // = the pre-reset next states, whose market columns are those of the
+        // next row of X (the same rounding of the same bar) wherever that row is
+        // the same episode's next step and this warp's own, and otherwise come
+        // from the feature matrix.  X and X' of the previous tile are free once
+        // its layer 1 and curiosity layer 1 are complete.
+        const int r = 32 * (warp - kTBuild0) + lane;
+        uint32_t it = 0;
+        bool ok = true;
+        for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
+            if (it > 0) {
+                ok = warp_wait(&bars->q1, (it - 1) & 1, &abort_flag);
+                ok = ok && warp_wait(&bars->c1, (it - 1) & 1, &abort_flag);
+                if (!ok) break;
+            }
+            TMeta m;
+            load_meta(a, tile, r, m);
+            resolve_meta(a, m);
+            const long long b = m.valid ? (long long)m.start + m.t : 0;
+            const float e_in = (m.t == 0 || m.dprev) ? 0.f : exposure_of(m.aprev);
+            // the warp's 32 rows are consecutive bars of one episode: their
+            // padded feature rows are one contiguous run, read in whole lines
+            const long long b0 = __shfl_sync(0xffffffffu, b, 0);
+            if (__all_sync(0xffffffffu, m.valid && b == b0 + lane)) {
+                const float4 *run = reinterpret_cast<const float4 *>(a.Fpad + b0 * kFPad);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {                  // two batches of loads in flight (registers)
+                    const int j0 = h ? 7 : 0, j1 = h ? 13 : 7;
+                    float4 f[7];
+#pragma unroll
+                    for (int j = 0; j < 7; ++j)
+                        if (j0 + j < j1) f[j] = __ldg(run + 32 * (j0 + j) + lane);
+#pragma unroll
+                    for (int jj = 0; jj < 7; ++jj) {
+                        const int j = j0 + jj;
+                        if (j >= j1) break;
+                        const float4 v = f[jj];
+                        const int idx = 32 * j + lane, rr = idx / 13, c4 = idx - 13 * rr;   // columns 4 c4 .. + 3
+                        const float Vr = __shfl_sync(0xffffffffu, m.vin, rr);
+                        uint2 p;
+                        p.x = pack_bf16x2(v.x, v.y);
+                        p.y = pack_bf16x2(v.z, c4 == 12 ? Vr : v.w);                   // column 51 is V
+                        *reinterpret_cast<uint2 *>(X + sw128_offset(32 * (warp - kTBuild0) + rr, c4 >> 1) +
+                                                   8 * (c4 & 1)) = p;
+                    }
+                }
+                // columns 52..63 of the lane's own row: e, spread, zeros
+                *reinterpret_cast<uint2 *>(X + sw128_offset(r, 6) + 8) = make_uint2(pack_bf16x2(e_in, a.env.spread), 0u);
+                *reinterpret_cast<uint4 *>(X + sw128_offset(r, 7)) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                state_row(X, r, a.Fpad + b * kFPad, m.valid, m.vin, e_in, a.env.spread);
+            }
+            __syncwarp();                                  // the warp's rows of X are written
+            if (m.valid && lane < 31 && m.t < a.L - 1) {
+#pragma unroll
+                for (int u = 0; u < 6; ++u)
+                    *reinterpret_cast<uint4 *>(Xn + sw128_offset(r, u)) =
+                        *reinterpret_cast<const uint4 *>(X + sw128_offset(r + 1, u));
+                const uint4 w6 = *reinterpret_cast<const uint4 *>(X + sw128_offset(r + 1, 6));
+                uint4 p;
+                p.x = w6.x;                                                           // columns 48, 49
+                p.y = (w6.y & 0xFFFFu) | (pack_bf16x2(0.f, m.vp) & 0xFFFF0000u);       // 50, V'
+                p.z = pack_bf16x2(exposure_of(m.act), a.env.spread);                  // e', spread
+                p.w = 0u;
+                *reinterpret_cast<uint4 *>(Xn + sw128_offset(r, 6)) = p;
+                *reinterpret_cast<uint4 *>(Xn + sw128_offset(r, 7)) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                state_row(Xn, r, a.Fpad + (b + 1) * kFPad, m.valid, m.vp, exposure_of(m.act), a.env.spread);
+            }
+            publish(&bars->x);
+        }
     } else {
+        // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
             const uint32_t id256 = idesc(true, 128, kH), id48 = idesc(true, 128, kHeadN), id64 = idesc(true, 128, 64);
-            long long u = 0;
-            uint32_t it = 0, hp = 0;
+            const uint32_t sX = smem_u32(X), sXn = smem_u32(Xn), sZ = smem_u32(Z), sH = smem_u32(Hb);
+            const uint32_t sRing = smem_u32(ring);
+            long long g = 0;      // weight units taken
+            uint32_t it = 0;
             bool ok = true;
-            auto take = [&](long long unit, int &st) -> bool {
-                st = (int)(unit % kStages);
-                if (!mbar_wait(&bars->full[st], (uint32_t)((unit / kStages) & 1), &abort_flag)) return false;
+            auto take = [&]() -> uint32_t {
+                const int st = (int)(g % kStages);
+                ok = ok && mbar_wait(&bars->full[st], (uint32_t)((g / kStages) & 1), &abort_flag);
                 tc_fence_after();
-                return true;
+                return sRing + st * kStage;
+            };
+            auto release = [&]() {
+                mma_commit(&bars->empty[g % kStages]);
+                ++g;
+            };
+            auto wait = [&](uint64_t *bar, uint32_t parity) {
+                ok = ok && mbar_wait(bar, parity, &abort_flag);
+                tc_fence_after();
+            };
+            // D[col] (+)= A(one 64-column K-chunk at a) B(b)^T
+            auto chunk = [&](uint32_t col, uint32_t a_s, uint32_t b_s, uint32_t id, bool accumulate) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma<true>(tmem + col, desc_sw128(a_s + 32 * k), desc_sw128(b_s + 32 * k), id,
+                              (accumulate || k > 0) ? 1u : 0u);
             };
             for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
-                if (!mbar_wait(&bars->x_ready, it & 1, &abort_flag)) break;
-                tc_fence_after();
-                int s_cur, st;
-                // curiosity layer 1 (its unit's second tile, C2, waits for Z)
-                if (!take(u, s_cur)) break;
-                ++u;
-                mma_layer(tmem + kTmemC1, X, ring + s_cur * kStage, 0, 1, id64, false);
-                mma_commit(&bars->acc_c);
-                // target layer 1 on X'
-                if (!take(u, st)) break;
-                ++u;
-                mma_layer(tmem + kTmemQ, Xn, ring + st * kStage, 0, 1, id256, false);
-                mma_commit(&bars->empty[st]);
-                mma_commit(&bars->acc_q);
-                // curiosity layer 2
-                if (!mbar_wait(&bars->z_ready, it & 1, &abort_flag)) break;
-                tc_fence_after();
-                mma_layer(tmem + kTmemC2, Z, ring + s_cur * kStage + kCurTile, 0, 1, id64, false);
-                mma_commit(&bars->empty[s_cur]);
-                mma_commit(&bars->acc_c);
-                // target layers 2, 3 (4 units each) and the head
-                for (int layer = 1; layer < 4 && ok; ++layer) {
-                    if (!mbar_wait(&bars->h_ready, hp & 1, &abort_flag)) { ok = false; break; }
-                    ++hp;
-                    tc_fence_after();
-                    const int n_units = layer == 3 ? 1 : 4;
-                    for (int cu = 0; cu < n_units; ++cu) {
-                        if (!take(u, st)) { ok = false; break; }
-                        ++u;
-                        if (layer == 3) mma_layer(tmem + kTmemQ, Hb, ring + st * kStage, kHeadTile, 4, id48, false);
-                        else mma_layer(tmem + kTmemQ, Hb + cu * kChunk, ring + st * kStage, 0, 1, id256, cu > 0);
-                        mma_commit(&bars->empty[st]);
-                    }
-                    if (ok) mma_commit(&bars->acc_q);
+                const uint32_t rs = (it & 1) * 256, ro = 256 - rs, par = it & 1;
+                const bool has_next = tile + gridDim.x < n_tiles;
+                uint32_t u;
+                if (it == 0) {
+                    u = take();
+                    wait(&bars->x, 0);
+                    if (!ok) break;
+                    chunk(rs, sXn, u, id256, false);
+                    release();
+                    mma_commit(&bars->q1);
+                }
+                // layer 2 into the other region; the previous tile's head was there
+                u = take();
+                wait(&bars->h1[0], par);
+                if (it > 0) wait(&bars->hd_free, par ^ 1u);
+                if (!ok) break;
+                chunk(ro, sH, u, id256, false);
+                release();
+                // curiosity layer 1 into [0, 64) of region s, which H1's chunk 0 has left
+                u = take();
+                if (!ok) break;
+                chunk(rs, sX, u, id64, false);
+                release();
+                mma_commit(&bars->c1);
+                for (int c = 1; c < 4 && ok; ++c) {
+                    u = take();
+                    wait(&bars->h1[c], par);
+                    if (!ok) break;
+                    chunk(ro, sH + c * kChunk, u, id256, true);
+                    release();
+                }
+                if (!ok) break;
+                mma_commit(&bars->q2);
+                // layer 3 into region s (H1 and curiosity layer 1 are out of it)
+                u = take();
+                wait(&bars->h2[0], par);
+                if (!ok) break;
+                chunk(rs, sH, u, id256, false);
+                release();
+                // curiosity layer 2 into [0, 64) of the other region, which H2's chunk 0 has left
+                u = take();
+                wait(&bars->z, par);
+                if (!ok) break;
+                chunk(ro, sZ, u, id64, false);
+                release();
+                mma_commit(&bars->c2);
+                for (int c = 1; c < 4 && ok; ++c) {
+                    u = take();
+                    wait(&bars->h2[c], par);
+                    if (!ok) break;
+                    chunk(rs, sH + c * kChunk, u, id256, true);
+                    release();
+                }
+                if (!ok) break;
+                mma_commit(&bars->q3);
+                // the head into [0, 48) of region s, K-chunk by K-chunk as H3 comes out
+                u = take();
+                for (int c = 0; c < 4 && ok; ++c) {
+                    wait(&bars->h3[c], par);
+                    if (!ok) break;
+                    chunk(rs, sH + c * kChunk, u + c * kHeadTile, id48, c > 0);
+                }
+                if (!ok) break;
+                release();
+                mma_commit(&bars->hd);
+                // the next tile's layer 1 into the other region, once H2 and
+                // curiosity layer 2 are out of it and the builders have written X'
+                if (has_next) {
+                    u = take();
+                    wait(&bars->cz, par);
+                    wait(&bars->x, par ^ 1u);
+                    if (!ok) break;
+                    chunk(ro, sXn, u, id256, false);
+                    release();
+                    mma_commit(&bars->q1);
                 }
             }
+            // every MMA issued has completed before TMEM is freed
             mma_commit(&bars->fin);
             mbar_wait_drain(&bars->fin, 0);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kTMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -707,6 +1088,7 @@ struct dqn_handle {
     int *d_status = nullptr;
     float *d_vpost = nullptr;
     size_t vpost_cap = 0;
+    float *d_fpad = nullptr;   // the features with rows padded to kFPad floats, refilled every run
     cudaStream_t last_stream = nullptr;
     bool timing = false, timed_run = false;
     cudaEvent_t ev[4] = {};
@@ -919,6 +1301,7 @@ void free_handle(dqn_handle *h)
     cudaFree(h->d_div);
     cudaFree(h->d_status);
     cudaFree(h->d_vpost);
+    cudaFree(h->d_fpad);
     for (cudaEvent_t e : h->ev)
         if (e) cudaEventDestroy(e);
     delete h;
@@ -947,6 +1330,7 @@ int dqn_create(const float *weights, const rollout_dims *dims, dqn_handle **out)
         (e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device)) != cudaSuccess ||
         (e = cudaMalloc(&h->d_status, sizeof(int))) != cudaSuccess ||
         (e = cudaMemset(h->d_status, 0, sizeof(int))) != cudaSuccess ||
+        (e = cudaMalloc(&h->d_fpad, (size_t)dims->n_bars * kFPad * sizeof(float))) != cudaSuccess ||
         (e = cudaFuncSetAttribute(dqn_rollout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem)) !=
             cudaSuccess ||
         (e = cudaFuncSetAttribute(dqn_target_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem)) !=
@@ -1003,19 +1387,21 @@ int dqn_run(dqn_handle *h, const float *features, const int32_t *starts, const u
     const RolloutArgs ra{features, starts, seeds, N, L, d.n_bars, epsilon, actions, dones, rewards, td, h->d_vpost, q,
                          h->d_status, env};
     auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
+    if ((e = launch_pad_features(features, h->d_fpad, d.n_bars, s)) != cudaSuccess)
+        return cuda_fail(e, "feature padding launch");
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     dqn_rollout_kernel<<<(N + 127) / 128, kThreads, kRSmem, s>>>(ra, h->img);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "DQN rollout launch");
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    const StatesArgs sa{features, starts, N, L, d.n_bars, actions, dones, td, d.spread, states};
+    const StatesArgs sa{features, starts, N, L, d.n_bars, actions, dones, td, d.spread, states, h->d_fpad};
     if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    const TargetArgs ta{features, starts, N, L, d.n_bars, gamma, actions, dones, rewards, td, h->d_vpost, q,
-                        next_states, h->d_status, env};
+    const TargetArgs ta{features, h->d_fpad, starts, N, L, d.n_bars, gamma, actions, dones, rewards, td, h->d_vpost,
+                        q, next_states, h->d_status, env};
     const long long tiles = (long long)((NL + 127) / 128);
     const int grid = (int)(tiles < h->sms ? tiles : h->sms);
-    if (h->test_stall) dqn_target_kernel<true><<<grid, kThreads, kTSmem, s>>>(ta, h->img);
-    else dqn_target_kernel<false><<<grid, kThreads, kTSmem, s>>>(ta, h->img);
+    if (h->test_stall) dqn_target_kernel<true><<<grid, kTThreads, kTSmem, s>>>(ta, h->img);
+    else dqn_target_kernel<false><<<grid, kTThreads, kTSmem, s>>>(ta, h->img);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "DQN target launch");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     h->timed_run = h->timing;

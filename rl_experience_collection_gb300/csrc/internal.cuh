@@ -125,6 +125,11 @@ struct StatesArgs {
     const float *Fpad = nullptr;   // optional copy of F with rows padded to kFPad floats (16-byte aligned rows)
 };
 
+// the feature matrix with rows padded to kFPad floats (16-byte aligned rows;
+// column 51 holds the bar's simple return expm1(F[b, 0])), for 16-byte loads
+// and tensor maps (phase1_umma.cu)
+cudaError_t launch_pad_features(const float *F, float *fpad, int n_bars, cudaStream_t s);
+
 struct GaeArgs {
     const float *rewards, *values;
     const int32_t *dones;

@@ -76,7 +76,6 @@ int umma_upload(UmmaWeights *w, void **d_buf, bool bf16, const float *host_w, co
 // fmap: 2-D tensor map over the padded feature copy [n_bars][kFPad] (f32,
 // box 52 x 1), used by the bf16 kernel; fpad is filled by launch_pad_features
 cudaError_t launch_phase1_umma(const Phase1Args &a, const UmmaWeights &w, const CUtensorMap &fmap, cudaStream_t s);
-cudaError_t launch_pad_features(const float *F, float *fpad, int n_bars, cudaStream_t s);
 // bf16 operands with the 512/384/256/128/64 critic: activations resident in shared memory
 // stall: launch the test build whose first weight producer in CTA 0 issues
 // nothing (that CTA's bounded wait expires and the run reports a timeout)

@@ -64,6 +64,9 @@ def _compare(w, inp, W, g, idx, L, eps):
         np.testing.assert_array_equal(g[k][..., 52:], ref[k][..., 52:], err_msg=k)
         np.testing.assert_allclose(g[k][..., 51], ref[k][..., 51], rtol=2e-6, atol=0, err_msg=k)
     r64 = {k: ref[k].astype(np.float64) for k in ("rewards", "q", "td")}
+    print(f"max |d rewards| {np.abs(g['rewards'] - r64['rewards']).max():.3e}  "
+          f"max rel d q {(np.abs(g['q'] - r64['q']) / np.maximum(np.abs(r64['q']), 1.0)).max():.3e}  "
+          f"max |d td| {np.abs(g['td'] - r64['td']).max():.3e}")
     assert np.abs(g["rewards"] - r64["rewards"]).max() <= 5e-2
     assert (np.abs(g["q"] - r64["q"]) / np.maximum(np.abs(r64["q"]), 1.0)).max() <= 2e-2
     tol = 5e-2 + 2e-2 * (2 * np.abs(r64["q"]) + np.abs(r64["td"]) + 1.0)
@@ -72,10 +75,14 @@ def _compare(w, inp, W, g, idx, L, eps):
     return st
 
 
-@pytest.mark.parametrize("N,L,eps,next_states", [(300, 40, 0.1, True), (129, 25, 0.6, False), (1, 7, 0.0, True)])
+@pytest.mark.parametrize("N,L,eps,next_states", [(300, 40, 0.1, True), (129, 25, 0.6, False), (1, 7, 0.0, True),
+                                                  (641, 100, 0.1, True)])
 def test_dqn_matches_oracle(N, L, eps, next_states):
     """Several CTAs with a ragged last one; exploration-heavy without the optional
-    next states; a single episode acting greedily."""
+    next states; a single episode acting greedily; 501 target-pass tiles, so that
+    every CTA of the target pass takes several (both TMEM region assignments,
+    the next tile's layer 1 issued inside the current one) and the last tile is
+    ragged."""
     from rl_experience_collection_gb300 import binding
     w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
     inp = wl.generate(w, n_episodes=N, horizon=L)
