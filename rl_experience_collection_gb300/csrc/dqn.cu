@@ -5,7 +5,9 @@
 // "Data Flow" (steps 1-15) and "Kernel Components" 1 (dueling Q network), 7
 // (TD error), 8 (LCG); the environment is the PPO collector's (env.cuh).
 //
-// Three stream-ordered phases, as in the PPO collector:
+// A padded copy of the features (rows of kFPad floats, the bar's simple
+// return in column 51) is refilled first; then three stream-ordered phases,
+// as in the PPO collector:
 //   rollout (dqn_rollout_kernel): a CTA owns 128 episodes and steps them
 //     together.  Per step the online network's four layers run as M = 128
 //     MMAs: L1 X[128 x 64] W1^T -> 256, L2 H W2^T -> 256, L3 H [Wv1; Wa1]^T ->
@@ -24,15 +26,13 @@
 // Between the phases out_td holds V entering each step and a handle-owned
 // array V' after the trade.
 //
-// Warp roles of the rollout kernel: warps 0-7 are row warps (warp w serves
-// TMEM lanes and rows 32 (w % 4) .. + 31 and the column half w / 4 of each
-// layer), warps 8-10 stream the weights, warp 8 + s filling ring stage s (the
-// bulk copies of one warp complete one after another, those of different
-// warps overlap), and warp 11 allocates TMEM and one lane issues the MMAs.
-// The target pass has 16 row warps (column quarters) and overlaps each
-// layer's epilogue with the next layer's MMAs (see its comment).  Every wait
-// is bounded; a wait that gives up sets a flag that ends every role's loop,
-// and the status word records the timeout.
+// Both kernels have 16 row warps (warp w serves TMEM lanes and rows
+// 32 (w % 4) .. + 31 and the column quarter w / 4 of every 64-column chunk),
+// three producer warps streaming the weights (one per ring stage), one MMA
+// warp, and overlap each layer's epilogue with the next layer's MMAs through
+// two alternating TMEM regions and per-K-chunk handoffs (see each kernel's
+// comment).  Every wait is bounded; a wait that gives up sets a flag that
+// ends every role's loop, and the status word records the timeout.
 #include <math.h>
 #include <string.h>
 
@@ -51,9 +51,7 @@ namespace {
 using namespace umma;
 
 constexpr int kH = 256, kHeadN = 48;
-constexpr int kRowWarps = 8;
 constexpr int kStages = 3;
-constexpr int kProdWarp0 = 8, kMmaWarp = kProdWarp0 + kStages, kThreads = (kMmaWarp + 1) * 32;
 constexpr int kChunk = 128 * 128;                   // one K-chunk (64 bf16 columns) of 128 rows
 constexpr int kStage = 32 * 1024;
 constexpr int kNetUnits = 10;                       // W1, W2 x4, W3 x4, head
@@ -75,6 +73,7 @@ struct DqnImage {
 
 struct RolloutArgs {
     const float *F;
+    const float *Fpad;   // F with rows padded to kFPad floats; column 51 holds the bar's simple return
     const int32_t *starts;
     const uint32_t *seeds;
     int N, L, n_bars;
@@ -104,64 +103,6 @@ struct TargetArgs {
     EnvConst env;
 };
 
-__device__ __forceinline__ float leaky(float x) { return x > 0.f ? x : 0.01f * x; }
-
-// 32 consecutive columns [c0, c0 + 32) of row r (c0 a multiple of 32), rounded
-// to bf16, into a chunked, 128-byte-swizzled operand buffer
-__device__ __forceinline__ void put32(uint8_t *buf, int r, int c0, const float (&v)[32])
-{
-    uint8_t *chunk = buf + (c0 >> 6) * kChunk;
-    const int u0 = (c0 & 63) >> 3;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 p;
-        p.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-        p.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-        p.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-        p.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-        *reinterpret_cast<uint4 *>(chunk + sw128_offset(r, u0 + q)) = p;
-    }
-}
-
-// the warp's 32 rows, columns [c0, c0 + 32) of the accumulator at TMEM column
-// `col`, + bias, LeakyReLU, into the operand buffer
-__device__ __forceinline__ void drain32_leaky(uint32_t taddr, int col, const float *bias, uint8_t *buf, int r,
-                                              int c0)
-{
-    float v[32];
-    tmem_ld32(taddr + col, v);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = leaky(v[i] + bias[c0 + i]);
-    put32(buf, r, c0, v);
-}
-
-// columns of a state row [F[b, 0..50], V, e, spread, 0 x 10] (or of x'), Frow
-// the feature row F[b]: column half 1 holds columns 0..31, half 0 32..63
-__device__ __forceinline__ void state_cols(const float *Frow, float V, float e, float spread, int hf, bool valid,
-                                           float (&v)[32])
-{
-    if (hf == 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = valid ? __ldg(Frow + i) : 0.f;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int c = 32 + i;
-            float x = 0.f;
-            if (valid) {
-                if (c < kMarket) x = __ldg(Frow + c);
-                else if (c == kMarket) x = V;
-                else if (c == kMarket + 1) x = e;
-                else if (c == kMarket + 2) x = spread;
-            }
-            v[i] = x;
-        }
-    }
-}
-
-__device__ __forceinline__ int state_c0(int hf) { return hf == 1 ? 0 : 32; }
-
 // a row warp's wait: every lane waits, and the warp goes on only if all of them
 // saw the phase, so that the warp-wide TMEM loads after it are never reached by
 // part of a warp (a lane can give up at the moment another sees the phase)
@@ -176,240 +117,6 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity)
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
         if (global_ns() - t0 > 1000000000ull) return;
-}
-
-// one layer's MMAs: A = nk K-chunks at `a` (chunk stride kChunk), B = the
-// stage's tiles (chunk stride b_stride), N columns into TMEM column d
-__device__ __forceinline__ void mma_layer(uint32_t d, const uint8_t *a, const uint8_t *b, int b_stride, int nk,
-                                          uint32_t id, bool accumulate_first)
-{
-    for (int c = 0; c < nk; ++c)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            mma<true>(d, desc_sw128(smem_u32(a + c * kChunk + 32 * k)), desc_sw128(smem_u32(b + c * b_stride + 32 * k)),
-                      id, (accumulate_first || c > 0 || k > 0) ? 1u : 0u);
-}
-
-// ---------------------------------------------------------------------------
-// rollout: the online network inside the serial step loop
-
-struct RBars {
-    uint64_t full[kStages], empty[kStages];
-    uint64_t x_ready;     // rows -> MMA: the step's state rows are in X (8 warp arrivals)
-    uint64_t h_ready;     // rows -> MMA: a hidden layer is in H (8 warp arrivals, 3 a step)
-    uint64_t acc;         // MMA -> rows: a layer's accumulator is complete (4 a step)
-    uint64_t fin;         // MMA: everything issued has completed (exit)
-};
-
-constexpr int kRSmem = 1024 + kChunk + 4 * kChunk + kStages * kStage + kBiasFloats * 4 + 1024;
-static_assert(kRSmem <= 232448, "rollout shared memory");
-
-__global__ void __launch_bounds__(kThreads, 1) dqn_rollout_kernel(RolloutArgs a, DqnImage w)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *X = base;                          // 1 K-chunk
-    uint8_t *Hb = X + kChunk;                   // 4 K-chunks
-    uint8_t *ring = Hb + 4 * kChunk;
-    float *bias = reinterpret_cast<float *>(ring + kStages * kStage);
-    RBars *bars = reinterpret_cast<RBars *>(bias + kBiasFloats);
-    __shared__ uint32_t tmem_base_s;
-    __shared__ volatile int abort_flag;
-    __shared__ uint32_t div_s[kDivWords];
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1);
-        }
-        mbar_init(&bars->x_ready, kRowWarps);
-        mbar_init(&bars->h_ready, kRowWarps);
-        mbar_init(&bars->acc, 1);
-        mbar_init(&bars->fin, 1);
-        abort_flag = 0;
-        fence_mbar_init();
-    }
-    for (int i = tid; i < kBiasFloats; i += kThreads) bias[i] = w.online_bias[i];
-    for (int i = tid; i < kDivWords; i += kThreads) div_s[i] = a.env.div_low[i];
-    if (warp == kMmaWarp) {
-        tmem_alloc(&tmem_base_s, 256);
-        tmem_relinquish();            // this CTA allocates once; later CTAs on the SM may allocate
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_base_s;
-    EnvConst env = a.env;
-    env.div_low = div_s;
-    const int L = a.L;
-
-    if (warp < kRowWarps) {
-        // ------------------------------------------------------------ rows
-        const int quad = warp & 3, hf = warp >> 2, r = quad * 32 + lane;
-        const int n = blockIdx.x * 128 + r;
-        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
-        int start = 0;
-        bool valid = n < a.N;
-        if (valid) {
-            start = a.starts[n];
-            if (!start_ok(start, L, a.n_bars)) {
-                valid = false;
-                if (hf == 0) set_status(a.status, ROLLOUT_ERR_RANGE);
-            }
-        }
-        EpState s;
-        ep_reset(s);
-        s.rng = n < a.N ? a.seeds[n] : 0u;
-        uint32_t acc_phase = 0;
-        for (int t = 0; t < L; ++t) {
-            const long long b = (long long)start + t;
-            const float *Frow = a.F + b * kMarket;
-            {
-                float v[32];
-                state_cols(Frow, s.V, s.e, env.spread, hf, valid, v);
-                put32(X, r, state_c0(hf), v);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->x_ready);
-            // three hidden layers: accumulator -> bias, LeakyReLU, bf16 -> H
-            bool ok = true;
-            for (int l = 0; l < 3 && ok; ++l) {
-                if (!warp_wait(&bars->acc, acc_phase & 1, &abort_flag)) { ok = false; break; }
-                ++acc_phase;
-                tc_fence_after();
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int c0 = hf * 128 + 32 * j;
-                    drain32_leaky(taddr, c0, bias + l * kH, Hb, r, c0);
-                }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->h_ready);
-            }
-            if (!ok || !warp_wait(&bars->acc, acc_phase & 1, &abort_flag)) break;
-            ++acc_phase;
-            tc_fence_after();
-            if (hf == 0) {
-                // head: A = cols 0..44, V = col 45; Q = V + (A - mean A)
-                float d0[32], d1[32];
-                tmem_ld32(taddr + 0, d0);
-                tmem_ld32(taddr + 32, d1);
-                tmem_ld_wait();
-                const float *bh = bias + 3 * kH;
-                float qv[kActions];
-                float sumA = 0.f;
-#pragma unroll
-                for (int j = 0; j < kActions; ++j) {
-                    qv[j] = (j < 32 ? d0[j] : d1[j - 32]) + bh[j];
-                    sumA += qv[j];
-                }
-                const float V = d1[kActions - 32] + bh[kActions];
-                const float meanA = sumA / (float)kActions;
-                int best = 0;
-                float qbest = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < kActions; ++j) {
-                    qv[j] = V + (qv[j] - meanA);
-                    if (qv[j] > qbest) { qbest = qv[j]; best = j; }
-                }
-                // epsilon-greedy: u1 decides, the second state gives the random action
-                const float u1 = lcg_uniform(s.rng);
-                s.rng = s.rng * 1664525u + 1013904223u;
-                const int a_rand = (int)(((uint64_t)(s.rng >> 8) * (uint64_t)kActions) >> 24);
-                const int act = (u1 < a.epsilon) ? a_rand : best;
-                float q_sel = qv[0];
-#pragma unroll
-                for (int j = 1; j < kActions; ++j)
-                    if (j == act) q_sel = qv[j];
-                const long long i = (long long)n * L + t;
-                if (valid) {
-                    const float v_in = s.V;
-                    float pnl, v_post;
-                    int label, done;
-                    env_trade(s, act, expm1f(__ldg(a.F + (b + 1) * kMarket)), env, pnl, v_post, label, done);
-                    const float rew = env_window_reward(s, act, pnl, label, done, env);
-                    a.actions[i] = act;
-                    a.dones[i] = done;
-                    a.rewards[i] = rew;
-                    a.v_in[i] = v_in;
-                    a.v_post[i] = v_post;
-                    a.q[i] = q_sel;
-                } else if (n < a.N) {
-                    a.actions[i] = 0;
-                    a.dones[i] = 0;
-                    a.rewards[i] = 0.f;
-                    a.v_in[i] = 0.f;
-                    a.v_post[i] = 0.f;
-                    a.q[i] = 0.f;
-                }
-            }
-            tc_fence_before();
-        }
-    } else if (warp < kMmaWarp) {
-        // ------------------------------------------------------------ weight stream, stage st
-        const int st = warp - kProdWarp0;
-        if (lane == 0) {
-            const long long total = (long long)kNetUnits * L;
-            long long last = -1;
-            for (long long u = st; u < total; u += kStages) {
-                const int i = (int)(u % kNetUnits);
-                if (u >= kStages && !mbar_wait(&bars->empty[st], (uint32_t)((u / kStages - 1) & 1), &abort_flag))
-                    break;
-                mbar_arrive_expect_tx(&bars->full[st], w.unit_bytes[i]);
-                bulk_g2s(ring + st * kStage, w.base + w.unit_off[i], w.unit_bytes[i], &bars->full[st]);
-                last = u;
-            }
-            // its last copy completes before the CTA may exit
-            if (last >= 0) mbar_wait_drain(&bars->full[st], (uint32_t)((last / kStages) & 1));
-        }
-    } else {
-        // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            const uint32_t id256 = idesc(true, 128, kH), id48 = idesc(true, 128, kHeadN);
-            long long u = 0;
-            uint32_t h_phase = 0;
-            bool ok = true;
-            for (int t = 0; t < L && ok; ++t) {
-                if (!mbar_wait(&bars->x_ready, (uint32_t)(t & 1), &abort_flag)) break;
-                tc_fence_after();
-                for (int layer = 0; layer < 4 && ok; ++layer) {
-                    if (layer > 0) {
-                        if (!mbar_wait(&bars->h_ready, h_phase & 1, &abort_flag)) { ok = false; break; }
-                        ++h_phase;
-                        tc_fence_after();
-                    }
-                    const int n_units = (layer == 0 || layer == 3) ? 1 : 4;
-                    for (int cu = 0; cu < n_units; ++cu, ++u) {
-                        const int st = (int)(u % kStages);
-                        if (!mbar_wait(&bars->full[st], (uint32_t)((u / kStages) & 1), &abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint8_t *bsrc = ring + st * kStage;
-                        if (layer == 0) mma_layer(tmem, X, bsrc, 0, 1, id256, false);
-                        else if (layer == 3) mma_layer(tmem, Hb, bsrc, kHeadTile, 4, id48, false);
-                        else mma_layer(tmem, Hb + cu * kChunk, bsrc, 0, 1, id256, cu > 0);
-                        mma_commit(&bars->empty[st]);
-                    }
-                    if (ok) mma_commit(&bars->acc);
-                }
-            }
-            // every MMA issued has completed before TMEM is freed
-            mma_commit(&bars->fin);
-            mbar_wait_drain(&bars->fin, 0);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 256);
-    }
-    if (tid == 0 && abort_flag) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------
@@ -1072,6 +779,451 @@ __global__ void __launch_bounds__(kTThreads, 1) dqn_target_kernel(TargetArgs a, 
     if (tid == 0 && abort_flag) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
 }
 
+// two K-chunks (16 accumulator columns each, at taddr0 and taddr1) loaded
+// together, then each + bias, LeakyReLU, bf16 into its operand chunk and
+// published on its barrier: one TMEM round trip for two chunks
+__device__ __forceinline__ void drain_pair_leaky(uint32_t taddr0, uint32_t taddr1, const float *bias0,
+                                                 const float *bias1, uint8_t *chunk0, uint8_t *chunk1, uint32_t off0,
+                                                 uint32_t off1, uint64_t *bar0, uint64_t *bar1)
+{
+    uint32_t x[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
+          "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15])
+        : "r"(taddr0)
+        : "memory");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]),
+          "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
+        : "r"(taddr1)
+        : "memory");
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float4 *b4 = reinterpret_cast<const float4 *>(h ? bias1 : bias0);
+        float v[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 b = b4[k];
+            v[4 * k + 0] = __uint_as_float(x[16 * h + 4 * k + 0]) + b.x;
+            v[4 * k + 1] = __uint_as_float(x[16 * h + 4 * k + 1]) + b.y;
+            v[4 * k + 2] = __uint_as_float(x[16 * h + 4 * k + 2]) + b.z;
+            v[4 * k + 3] = __uint_as_float(x[16 * h + 4 * k + 3]) + b.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = fmaxf(v[k], 0.01f * v[k]);
+        put16(h ? chunk1 : chunk0, off0, off1, v);
+        publish(h ? bar1 : bar0);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// rollout: the online network inside the serial step loop
+//
+// A CTA steps 128 episodes (one per TMEM lane / operand row) through all L
+// bars.  Warp roles: 16 row warps (warp w serves TMEM lanes / rows
+// 32 (w % 4) .. + 31 and the column quarter w / 4 of every 64-column chunk),
+// three producer warps (warp kRProd0 + s fills ring stage s), one MMA warp.
+// TMEM holds two 256-column regions; step t puts layers 1 and 3 and the head
+// into region s = t & 1 and layer 2 into the other one, so each layer starts
+// on its first K-chunk while the rows still drain the rest of the previous
+// one.  The head accumulates into [0, 48) of region s (freed by H3's chunk 0).
+// The market columns of the next step's state rows are known a step ahead
+// (the bar advances by one whatever the action): warps of quarters 1-3 write
+// columns 0-47 of X as soon as layer 1 has read it.  The head's 48 columns
+// are read by the quarter 0-2 warps, 16 each: they exchange their advantage
+// sums through shared memory, each forms Q for its columns and its first
+// maximum, and the quarter-0 warps, which hold the episodes' environment
+// state, combine them, pick the action, step the environment and write
+// columns 48-55 (F[.., 48..50], V, e, spread).  Per step the MMA lane takes its weight units in this order
+// (the producers stream them in the same order): W2 chunks 0-3, W3 chunks
+// 0-3, the head, the next step's W1 (none after the last step); the first
+// step is preceded by its W1.
+constexpr int kRRowWarps = 16;
+constexpr int kRProd0 = kRRowWarps, kRMma = kRProd0 + kStages, kRThreads = (kRMma + 1) * 32;
+constexpr int kRUnitsPerStep = 10;
+
+struct RBars {
+    uint64_t full[kStages], empty[kStages];
+    uint64_t x;             // rows -> MMA: X of a step is written (16 warp arrivals)
+    uint64_t h1[4], h2[4], h3[4];   // rows -> MMA: K-chunk c of a hidden layer is in Hb
+    uint64_t hd_free;       // quarter 0-2 row warps -> MMA: the head's columns are read
+    uint64_t q1, q2, q3, hd;        // MMA -> rows: that layer's MMAs are complete
+    uint64_t hx1[4], hx2[4];        // head exchange among the quarter 0-2 warps of the same lanes
+    uint64_t fin;
+};
+
+constexpr int kRXFloats = 9 * 128;   // head exchange: sums [3][128], V [128], best [2][128], max [2][128], Q(a_rand) [128]
+constexpr int kRSmem =
+    1024 + kChunk + 4 * kChunk + kStages * kStage + kBiasFloats * 4 + kDivWords * 4 + kRXFloats * 4 + 1024;
+static_assert(kRSmem <= 232448, "rollout shared memory");
+static_assert(sizeof(RBars) <= 1024, "rollout barriers");
+
+// unit g of the rollout's weight stream (10 a step): its index in the image
+__device__ __forceinline__ int rollout_unit(long long g)
+{
+    if (g == 0) return 0;                                  // the first step's W1
+    const int pos = (int)((g - 1) % kRUnitsPerStep);       // W2 0-3, W3 0-3, head, next W1
+    return pos < 9 ? 1 + pos : 0;
+}
+
+__global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a, DqnImage w)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *X = base;                          // 1 K-chunk
+    uint8_t *Hb = X + kChunk;                   // 4 K-chunks
+    uint8_t *ring = Hb + 4 * kChunk;
+    float *bias = reinterpret_cast<float *>(ring + kStages * kStage);
+    uint32_t *div_s = reinterpret_cast<uint32_t *>(bias + kBiasFloats);
+    float *hsum = reinterpret_cast<float *>(div_s + kDivWords);      // [3][128] advantage sums of quarters 0-2
+    float *hval = hsum + 3 * 128;                                     // [128] V (quarter 2)
+    int *hbest = reinterpret_cast<int *>(hval + 128);                 // [2][128] first argmax of quarters 1, 2
+    float *hqmax = reinterpret_cast<float *>(hbest + 2 * 128);        // [2][128] their maxima
+    float *hqrand = hqmax + 2 * 128;                                  // [128] Q of the random action (quarters 1, 2)
+    RBars *bars = reinterpret_cast<RBars *>(hqrand + 128);
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        mbar_init(&bars->x, kRRowWarps);
+        for (int c = 0; c < 4; ++c) {
+            mbar_init(&bars->h1[c], kRRowWarps);
+            mbar_init(&bars->h2[c], kRRowWarps);
+            mbar_init(&bars->h3[c], kRRowWarps);
+        }
+        mbar_init(&bars->hd_free, 12);
+        for (int k = 0; k < 4; ++k) {
+            mbar_init(&bars->hx1[k], 3);
+            mbar_init(&bars->hx2[k], 2);
+        }
+        mbar_init(&bars->q1, 1);
+        mbar_init(&bars->q2, 1);
+        mbar_init(&bars->q3, 1);
+        mbar_init(&bars->hd, 1);
+        mbar_init(&bars->fin, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int i = tid; i < kBiasFloats; i += kRThreads) bias[i] = w.online_bias[i];
+    for (int i = tid; i < kDivWords; i += kRThreads) div_s[i] = a.env.div_low[i];
+    if (warp == kRMma) {
+        tmem_alloc(&tmem_base_s, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    EnvConst env = a.env;
+    env.div_low = div_s;
+    const int L = a.L;
+
+    if (warp < kRRowWarps) {
+        // ------------------------------------------------------------ rows
+        const int quad = warp & 3, q = warp >> 2, r = quad * 32 + lane;
+        const int n = blockIdx.x * 128 + r;
+        const uint32_t lane_t = tmem + ((uint32_t)(quad * 32) << 16) + 16 * q;
+        const uint32_t off0 = sw128_offset(r, 2 * q), off1 = sw128_offset(r, 2 * q + 1);
+        // the columns this warp writes into X: quarters 1-3 columns 16 (q - 1) ..
+        // + 15 (units 2 (q - 1), 2 (q - 1) + 1); quarter 0 unit 6 (and unit 7, zero)
+        const uint32_t xo0 = sw128_offset(r, q > 0 ? 2 * (q - 1) : 6), xo1 = sw128_offset(r, q > 0 ? 2 * q - 1 : 7);
+        int start = 0;
+        bool valid = n < a.N;
+        if (valid) {
+            start = a.starts[n];
+            if (!start_ok(start, L, a.n_bars)) {
+                valid = false;
+                if (q == 0) set_status(a.status, ROLLOUT_ERR_RANGE);
+            }
+        }
+        EpState s;
+        ep_reset(s);
+        s.rng = n < a.N ? a.seeds[n] : 0u;
+        // X columns of bar b: quarters 1-3 their 16 market columns; quarter 0
+        // F[b, 48..50] and the bar's simple return (column 51 of the padded row)
+        auto fetch = [&](long long b, float (&f)[16]) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.Fpad + b * kFPad);
+            if (q > 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 v = valid ? __ldg(src + 4 * (q - 1) + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    f[4 * k + 0] = v.x;
+                    f[4 * k + 1] = v.y;
+                    f[4 * k + 2] = v.z;
+                    f[4 * k + 3] = v.w;
+                }
+            } else {
+                const float4 v = valid ? __ldg(src + 12) : make_float4(0.f, 0.f, 0.f, 0.f);
+                f[0] = v.x;
+                f[1] = v.y;
+                f[2] = v.z;
+                f[3] = v.w;
+            }
+        };
+        // quarter 0's unit 6: F[.., 48..50], V, e, spread, 0, 0 (zero when !valid)
+        auto put_tail = [&](const float (&f)[16]) {
+            uint4 p;
+            p.x = pack_bf16x2(f[0], f[1]);
+            p.y = pack_bf16x2(f[2], valid ? s.V : 0.f);
+            p.z = valid ? pack_bf16x2(s.e, env.spread) : 0u;
+            p.w = 0u;
+            *reinterpret_cast<uint4 *>(X + xo0) = p;
+        };
+        float f[16];
+        // X of step 0
+        fetch(valid ? start : 0, f);
+        if (q > 0) {
+            put16(X, xo0, xo1, f);
+        } else {
+            put_tail(f);
+            *reinterpret_cast<uint4 *>(X + xo1) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        publish(&bars->x);
+        bool ok = true;
+        for (int t = 0; t < L && ok; ++t) {
+            const uint32_t par = t & 1, rs = par * 256, ro = 256 - rs;
+            const long long b = (long long)start + t;
+            fetch(valid ? b + 1 : 0, f);                   // the next bar: X of step t + 1, its return
+            auto wait = [&](uint64_t *bar) {
+                ok = ok && warp_wait(bar, par, &abort_flag);
+                tc_fence_after();
+            };
+            // layer 1 (region s) -> H1
+            wait(&bars->q1);
+            if (!ok) break;
+#pragma unroll 1
+            for (int c = 0; c < 4; c += 2)
+                drain_pair_leaky(lane_t + rs + 64 * c, lane_t + rs + 64 * c + 64, bias + 64 * c + 16 * q,
+                                 bias + 64 * c + 64 + 16 * q, Hb + c * kChunk, Hb + (c + 1) * kChunk, off0, off1,
+                                 &bars->h1[c], &bars->h1[c + 1]);
+            // layer 1 has read X: quarters 1-3 write the next step's market columns
+            if (q > 0) {
+                put16(X, xo0, xo1, f);
+                publish(&bars->x);
+            }
+            // layer 2 (the other region) -> H2
+            wait(&bars->q2);
+            if (!ok) break;
+#pragma unroll 1
+            for (int c = 0; c < 4; c += 2)
+                drain_pair_leaky(lane_t + ro + 64 * c, lane_t + ro + 64 * c + 64, bias + kH + 64 * c + 16 * q,
+                                 bias + kH + 64 * c + 64 + 16 * q, Hb + c * kChunk, Hb + (c + 1) * kChunk, off0, off1,
+                                 &bars->h2[c], &bars->h2[c + 1]);
+            // layer 3 (region s) -> H3
+            wait(&bars->q3);
+            if (!ok) break;
+#pragma unroll 1
+            for (int c = 0; c < 4; c += 2)
+                drain_pair_leaky(lane_t + rs + 64 * c, lane_t + rs + 64 * c + 64, bias + 2 * kH + 64 * c + 16 * q,
+                                 bias + 2 * kH + 64 * c + 64 + 16 * q, Hb + c * kChunk, Hb + (c + 1) * kChunk, off0, off1,
+                                 &bars->h3[c], &bars->h3[c + 1]);
+            if (q == 3) continue;
+            // ---- quarters 0-2: the head ([0, 48) of region s): A = columns
+            // 0..44, V = column 45; Q_j = V + (A_j - mean A).  The TMEM load is
+            // warp-wide (.sync.aligned): every lane issues it, invalid rows included.
+            wait(&bars->hd);
+            if (!ok) break;
+            const float *bh = bias + 3 * kH + 16 * q;
+            float d[16];
+            tmem_ld16(lane_t + rs, d);
+            publish(&bars->hd_free);
+            float sA = 0.f, Vq = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int j = 16 * q + k;
+                d[k] += bh[k];                                 // A_j
+                if (j < kActions) sA += d[k];
+                else if (j == kActions) Vq = d[k];
+            }
+            hsum[q * 128 + r] = sA;
+            if (q == 2) hval[r] = Vq;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->hx1[quad]);
+            ok = warp_wait(&bars->hx1[quad], par, &abort_flag);
+            if (!ok) break;
+            const float meanA = ((hsum[r] + hsum[128 + r]) + hsum[256 + r]) / (float)kActions;
+            const float V = hval[r];
+            // epsilon-greedy (every quarter advances an identical copy of the
+            // episode's LCG): u1 decides, the second state gives the random action
+            const float u1 = lcg_uniform(s.rng);
+            s.rng = s.rng * 1664525u + 1013904223u;
+            const int a_rand = (int)(((uint64_t)(s.rng >> 8) * (uint64_t)kActions) >> 24);
+            int best = 16 * q;
+            float qbest = -INFINITY, q_rand = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int j = 16 * q + k;
+                if (j < kActions) {
+                    const float Qj = V + (d[k] - meanA);
+                    if (Qj > qbest) {
+                        qbest = Qj;
+                        best = j;
+                    }
+                    if (j == a_rand) q_rand = Qj;
+                }
+            }
+            if (q > 0) {
+                hbest[(q - 1) * 128 + r] = best;
+                hqmax[(q - 1) * 128 + r] = qbest;
+                if (a_rand >= 16 * q && a_rand < 16 * q + 16) hqrand[r] = q_rand;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->hx2[quad]);
+                continue;
+            }
+            ok = warp_wait(&bars->hx2[quad], par, &abort_flag);
+            if (!ok) break;
+            // the first maximum over all 45 columns: a later quarter wins only if strictly greater
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                if (hqmax[k * 128 + r] > qbest) {
+                    qbest = hqmax[k * 128 + r];
+                    best = hbest[k * 128 + r];
+                }
+            if (a_rand >= 16) q_rand = hqrand[r];
+            const bool explore = u1 < a.epsilon;
+            const int act = explore ? a_rand : best;
+            const float q_sel = explore ? q_rand : qbest;
+            const long long i = (long long)n * L + t;
+            float v_in = 0.f, v_post = 0.f, rew = 0.f;
+            int done = 0;
+            if (valid) {
+                v_in = s.V;
+                float pnl;
+                int label;
+                env_trade(s, act, f[3], env, pnl, v_post, label, done);
+                rew = env_window_reward(s, act, pnl, label, done, env);
+            }
+            // the next step's columns 48..55 (V and e after the trade), then the stores
+            put_tail(f);
+            publish(&bars->x);
+            if (n < a.N) {
+                a.actions[i] = valid ? act : 0;
+                a.dones[i] = done;
+                a.rewards[i] = rew;
+                a.v_in[i] = v_in;
+                a.v_post[i] = v_post;
+                a.q[i] = valid ? q_sel : 0.f;
+            }
+        }
+    } else if (warp < kRMma) {
+        // ------------------------------------------------------------ weight stream, stage st
+        const int st = warp - kRProd0;
+        if (lane == 0) {
+            const long long total = (long long)kRUnitsPerStep * L;
+            long long last = -1;
+            for (long long u = st; u < total; u += kStages) {
+                const int i = rollout_unit(u);
+                if (u >= kStages && !mbar_wait(&bars->empty[st], (uint32_t)((u / kStages - 1) & 1), &abort_flag))
+                    break;
+                mbar_arrive_expect_tx(&bars->full[st], w.unit_bytes[i]);
+                bulk_g2s(ring + st * kStage, w.base + w.unit_off[i], w.unit_bytes[i], &bars->full[st]);
+                last = u;
+            }
+            // its last copy completes before the CTA may exit
+            if (last >= 0) mbar_wait_drain(&bars->full[st], (uint32_t)((last / kStages) & 1));
+        }
+    } else {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t id256 = idesc(true, 128, kH), id48 = idesc(true, 128, kHeadN);
+            const uint32_t sX = smem_u32(X), sH = smem_u32(Hb), sRing = smem_u32(ring);
+            long long g = 0;
+            bool ok = true;
+            auto take = [&]() -> uint32_t {
+                const int st = (int)(g % kStages);
+                ok = ok && mbar_wait(&bars->full[st], (uint32_t)((g / kStages) & 1), &abort_flag);
+                tc_fence_after();
+                return sRing + st * kStage;
+            };
+            auto release = [&]() {
+                mma_commit(&bars->empty[g % kStages]);
+                ++g;
+            };
+            auto wait = [&](uint64_t *bar, uint32_t parity) {
+                ok = ok && mbar_wait(bar, parity, &abort_flag);
+                tc_fence_after();
+            };
+            auto chunk = [&](uint32_t col, uint32_t a_s, uint32_t b_s, uint32_t id, bool accumulate) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma<true>(tmem + col, desc_sw128(a_s + 32 * k), desc_sw128(b_s + 32 * k), id,
+                              (accumulate || k > 0) ? 1u : 0u);
+            };
+            uint32_t u;
+            u = take();
+            wait(&bars->x, 0);
+            if (ok) {
+                chunk(0, sX, u, id256, false);
+                release();
+                mma_commit(&bars->q1);
+            }
+            for (int t = 0; t < L && ok; ++t) {
+                const uint32_t par = t & 1, rs = par * 256, ro = 256 - rs;
+                // layer 2 into the other region (the previous step's head was there)
+                for (int c = 0; c < 4 && ok; ++c) {
+                    u = take();
+                    wait(&bars->h1[c], par);
+                    if (c == 0 && t > 0) wait(&bars->hd_free, par ^ 1u);
+                    if (!ok) break;
+                    chunk(ro, sH + c * kChunk, u, id256, c > 0);
+                    release();
+                }
+                if (!ok) break;
+                mma_commit(&bars->q2);
+                // layer 3 into region s
+                for (int c = 0; c < 4 && ok; ++c) {
+                    u = take();
+                    wait(&bars->h2[c], par);
+                    if (!ok) break;
+                    chunk(rs, sH + c * kChunk, u, id256, c > 0);
+                    release();
+                }
+                if (!ok) break;
+                mma_commit(&bars->q3);
+                // the head into [0, 48) of region s, K-chunk by K-chunk
+                u = take();
+                for (int c = 0; c < 4 && ok; ++c) {
+                    wait(&bars->h3[c], par);
+                    if (!ok) break;
+                    chunk(rs, sH + c * kChunk, u + c * kHeadTile, id48, c > 0);
+                }
+                if (!ok) break;
+                release();
+                mma_commit(&bars->hd);
+                // the next step's layer 1 into the other region (H2 is out of it)
+                if (t + 1 < L) {
+                    u = take();
+                    wait(&bars->x, par ^ 1u);
+                    if (!ok) break;
+                    chunk(ro, sX, u, id256, false);
+                    release();
+                    mma_commit(&bars->q1);
+                }
+            }
+            // every MMA issued has completed before TMEM is freed
+            mma_commit(&bars->fin);
+            mbar_wait_drain(&bars->fin, 0);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kRMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (tid == 0 && abort_flag) set_status(a.status, ROLLOUT_ERR_TIMEOUT);
+}
+
 }  // namespace
 }  // namespace rl
 
@@ -1384,13 +1536,13 @@ int dqn_run(dqn_handle *h, const float *features, const int32_t *starts, const u
     if ((e = cudaMemsetAsync(h->d_status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     const EnvConst env{d.barrier, d.max_hold, d.pt_scale, d.sl_scale, d.div_window, d.div_thresh, d.div_penalty,
                        d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div};
-    const RolloutArgs ra{features, starts, seeds, N, L, d.n_bars, epsilon, actions, dones, rewards, td, h->d_vpost, q,
-                         h->d_status, env};
+    const RolloutArgs ra{features, h->d_fpad, starts, seeds, N, L, d.n_bars, epsilon, actions, dones, rewards, td,
+                         h->d_vpost, q, h->d_status, env};
     auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
     if ((e = launch_pad_features(features, h->d_fpad, d.n_bars, s)) != cudaSuccess)
         return cuda_fail(e, "feature padding launch");
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    dqn_rollout_kernel<<<(N + 127) / 128, kThreads, kRSmem, s>>>(ra, h->img);
+    dqn_rollout_kernel<<<(N + 127) / 128, kRThreads, kRSmem, s>>>(ra, h->img);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "DQN rollout launch");
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     const StatesArgs sa{features, starts, N, L, d.n_bars, actions, dones, td, d.spread, states, h->d_fpad};
