@@ -37,7 +37,14 @@ constexpr int kAStage = kChunk;
 constexpr int kBStage = 256 * 128;
 constexpr int kStageBytes = kAStage + kBStage;
 constexpr int kStages = 4;
-constexpr int kSmem = kStages * kStageBytes + 2 * 4 * 128 * 4 + 1024;
+// shared-memory copy of the epilogue constants: every job's bias (each padded
+// to a multiple of 64 columns), the head weights and the curiosity one-hot
+// columns (rows padded to kOhLd floats, so the rows of different actions start
+// on different banks); sized for the widened critic, the larger of the two
+// shapes the library accepts
+constexpr int kOhLd = kCurH + 4;
+constexpr int kVecCap = (1024 + 768 + 512 + 256 + 128 + 64 + 64) + 128 + kActions * kOhLd;
+constexpr int kSmem = kStages * kStageBytes + 2 * 4 * 128 * 4 + kVecCap * 4 + 1024;
 static_assert(kSmem <= 232448, "generic value kernel shared memory");
 
 enum { kBufX = 0, kBufZ = 1, kBufP = 2, kBufQ = 3 };
@@ -231,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *ring = sm;
     float *part = reinterpret_cast<float *>(ring + kStages * kStageBytes);   // [2][4][128]
+    float *vc = part + 2 * 4 * 128;                                            // [kVecCap] epilogue constants
     __shared__ __align__(8) GBars B;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -259,6 +267,19 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
+    // epilogue constants into shared memory (offsets: jobs in execution order,
+    // then the head weights, then the one-hot rows)
+    int vc_n = 0;
+    for (int jj = 0; jj < 7; ++jj) {
+        const UmmaLayer &Ly = w.job[kJobs[jj].layer];
+        const int n = (Ly.n_out + 63) & ~63;
+        for (int i = tid; i < n; i += kThreads) vc[vc_n + i] = i < Ly.n_out ? w.vec[Ly.bias_off + i] : 0.f;
+        vc_n += n;
+    }
+    const int vc_head = vc_n, vc_oh = vc_head + w.job[kJobCrit5].n_out;
+    for (int i = tid; i < w.job[kJobCrit5].n_out; i += kThreads) vc[vc_head + i] = w.vec[w.head_w_off + i];
+    for (int i = tid; i < kActions * kCurH; i += kThreads)
+        vc[vc_oh + (i / kCurH) * kOhLd + i % kCurH] = w.vec[w.onehot_off + i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -393,10 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
             fence_async_global();
             warp_arrive(&B.act);
             float se = 0.f, dot = 0.f;
+            int vc_off = 0;                           // this job's bias in vc (64-column padded)
             for (int jj = 0; jj < 7; ++jj) {
                 const Job J = kJobs[jj];
                 const UmmaLayer &Ly = w.job[J.layer];
-                const float *bias = vec + Ly.bias_off;
+                const float *bias = vc + vc_off;
+                vc_off += (Ly.n_out + 63) & ~63;
                 int col0 = 0;
                 for (int nb = 0; nb < Ly.n_blocks; ++nb, ++pass) {
                     const int h = pass & 1, rows = Ly.nb_rows[nb];
@@ -409,19 +432,36 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                         const int cg = col0 + cl;                // column within the layer
                         float v[16];
                         tmem_ld16g(lane_addr + 256 * h + cl, v);
+                        float bv[16];
+                        {
+                            const float4 *b4 = reinterpret_cast<const float4 *>(bias + cg);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float4 b = b4[k];
+                                bv[4 * k + 0] = b.x;
+                                bv[4 * k + 1] = b.y;
+                                bv[4 * k + 2] = b.z;
+                                bv[4 * k + 3] = b.w;
+                            }
+                        }
                         if (J.epi == kEpiHidden) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] = relu(v[i] + __ldg(bias + cg + i));
+                            for (int i = 0; i < 16; ++i) v[i] = relu(v[i] + bv[i]);
                             put16g<BF16>(bufs[J.out_buf], r, cg, v);
                             if constexpr (kDump) {
                                 if (drow) dump16<BF16>(drow + a.dump.crit_off[J.layer - kJobCrit1] + cg, v, cg, Ly.n_out);
                             }
                         } else if (J.epi == kEpiCur1) {
                             const int act = (ri.act >= 0 && ri.act < kActions) ? ri.act : 0;
-                            const float *oh = vec + w.onehot_off + act * kCurH;
+                            const float4 *oh4 = reinterpret_cast<const float4 *>(vc + vc_oh + act * kOhLd + cg);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v[i] = relu((v[i] + __ldg(oh + cg + i)) + __ldg(bias + cg + i));
+                            for (int k = 0; k < 4; ++k) {
+                                const float4 o = oh4[k];
+                                v[4 * k + 0] = relu((v[4 * k + 0] + o.x) + bv[4 * k + 0]);
+                                v[4 * k + 1] = relu((v[4 * k + 1] + o.y) + bv[4 * k + 1]);
+                                v[4 * k + 2] = relu((v[4 * k + 2] + o.z) + bv[4 * k + 2]);
+                                v[4 * k + 3] = relu((v[4 * k + 3] + o.w) + bv[4 * k + 3]);
+                            }
                             put16g<BF16>(bufs[J.out_buf], r, cg, v);
                             if constexpr (kDump) {
                                 if (drow && ri.kind == 0) dump16<BF16>(drow + a.dump.cur_off + cg, v, cg, Ly.n_out);
@@ -435,15 +475,15 @@ __global__ void __launch_bounds__(kThreads, 1) value_generic_kernel(ValueArgs a,
                                     if (c < kMarket) tgt = ri.kind == 0 ? __ldg(a.F + (ri.bar + 1) * kMarket + c) : 0.f;
                                     else if (c == kMarket) tgt = ri.vpost;
                                     else if (c == kMarket + 1) tgt = ri.epost;
-                                    const float d = (v[i] + __ldg(bias + c)) - tgt;
+                                    const float d = (v[i] + bv[i]) - tgt;
                                     se = fmaf(d, d, se);
                                 }
                             }
                         } else {   // head: relu, operand rounding, dot with the head weights
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
-                                const float hv = round_op(relu(v[i] + __ldg(bias + cg + i)), BF16);
-                                dot = fmaf(hv, __ldg(vec + w.head_w_off + cg + i), dot);
+                                const float hv = round_op(relu(v[i] + bv[i]), BF16);
+                                dot = fmaf(hv, vc[vc_head + cg + i], dot);
                                 if constexpr (kDump) {
                                     if (drow && cg + i < Ly.n_out) drow[a.dump.crit_off[4] + cg + i] = hv;
                                 }
