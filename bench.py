@@ -50,13 +50,15 @@ def path_flops(w: wl.Workload, N: int, L: int):
     return N * L * ACTOR_FLOP + value, value
 
 
-# DRAM bytes (read + write) of one value-kernel launch, from a two-counter ncu
-# capture at the bench's full size (profiles/ncu_dram_value_umma_reset_heavy_bf16.md).
-# A figure only holds for the source it was measured on: the sha256 below covers
-# the kernel and the files it is built from; any change makes the traffic null.
+# DRAM bytes (read + write) of one value-kernel launch at the bench's full size,
+# scaled from two-counter ncu captures of two small cases of the same workload
+# (profiles/ncu_dram_value_umma_reset_heavy_bf16.md: reads fitted as fixed + per
+# row, writes at the algorithmic 8 B per row).  A figure only holds for the
+# source it was measured on: the sha256 below covers the kernel and the files it
+# is built from; any change makes the traffic null.
 VALUE_DRAM_CAPTURE = {"workload": "reset_heavy_bf16", "episodes": 16384, "horizon": 1000,
-                      "bytes": 549.19e6,
-                      "sources_sha256": "f224d5799f9f839dd5a09aa7ba37c47e7371f6371a7a12c098cc036482321bb2"}
+                      "bytes": 528.25e6,
+                      "sources_sha256": "925981c9d481c990e771c43edac7af9380d12ffe1db65a45b6831e21dc6cf52b"}
 VALUE_KERNEL_SOURCES = ["value_umma.cu", "umma.cuh", "umma_path.cuh", "env.cuh", "internal.cuh", "umma_pack.cu"]
 
 
