@@ -28,7 +28,8 @@
 //   19    allocates TMEM; one lane issues the MMAs and commits
 //
 // Per tile the MMA lane runs (TMEM columns in brackets):
-//   CUR1 [0,64) = X C1^T ; D1_0 [384,512) = X W1[rows 0..127]^T
+//   CUR1 [320,384) = X C1^T and D1_0 [384,512) = X W1[rows 0..127]^T, one
+//   N=192 MMA (the previous tile's layer 3 has left [256,512))
 //   CUR2 [256,320) = Z C2^T                        (after the rows wrote Z)
 //   for i < 8:  D2 [0,384) += h1_i W2[:, chunk i]^T  (after rows wrote h1_i;
 //                 for i = 0 the columns [256,384) also wait for CUR2's drain)
@@ -90,7 +91,7 @@ constexpr int kB1 = 0, kB2 = 512, kB3 = 896, kB4 = 1152, kB5 = 1280, kHW = 1344,
               kC2B = 1476;
 
 // TMEM columns
-constexpr uint32_t kColCur1 = 0, kColCur2 = 256, kColD1 = 384, kColD2 = 0, kColD3 = 256, kColD4 = 0, kColD5 = 128;
+constexpr uint32_t kColCur1 = 320, kColCur2 = 256, kColD1 = 384, kColD2 = 0, kColD3 = 256, kColD4 = 0, kColD5 = 128;
 
 struct Bars {
     uint64_t full[kStages], empty[kStages];
@@ -601,12 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1) value_umma_bf16_kernel(ValueArgs 
                 if (++stage == kStages) { stage = 0; ring_ph ^= 1u; }
             };
             for (long long tile = blockIdx.x; tile < n_tiles && m.ok; tile += gridDim.x) {
-                // ---- unit 0: CUR1, D1_0, D1_1, CUR2
+                // ---- unit 0: CUR1 and D1_0 as one N=192 MMA (C1's 64 rows and W1's
+                // first 128 are contiguous in the unit, CUR1's columns [320,384)
+                // adjoin D1's), then CUR2
                 m.wait(&B.act_x, ph_x);
                 uint32_t u = take();
-                m.mma_chunk(kColCur1, m.slot(kXSlot), u, 64, false);
+                m.mma_chunk(kColCur1, m.slot(kXSlot), u, 192, false);
                 mma_commit(&B.acc_cur);
-                m.mma_chunk(kColD1, m.slot(kXSlot), u + 8192, 128, false);
                 mma_commit(&B.acc_d1);
                 m.wait(&B.act_z, ph_z);
                 m.mma_chunk(kColCur2, m.slot(kZSlot), u + 24576, 64, false);
