@@ -76,13 +76,14 @@ def _compare(w, inp, W, g, idx, L, eps):
 
 
 @pytest.mark.parametrize("N,L,eps,next_states", [(300, 40, 0.1, True), (129, 25, 0.6, False), (1, 7, 0.0, True),
-                                                  (641, 100, 0.1, True)])
+                                                  (641, 100, 0.1, True), (130, 1, 0.3, True)])
 def test_dqn_matches_oracle(N, L, eps, next_states):
     """Several CTAs with a ragged last one; exploration-heavy without the optional
     next states; a single episode acting greedily; 501 target-pass tiles, so that
     every CTA of the target pass takes several (both TMEM region assignments,
     the next tile's layer 1 issued inside the current one) and the last tile is
-    ragged."""
+    ragged; a one-step horizon, where every row is its episode's last step (the
+    next state's features come from the feature matrix, never from the next row)."""
     from rl_experience_collection_gb300 import binding
     w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
     inp = wl.generate(w, n_episodes=N, horizon=L)
