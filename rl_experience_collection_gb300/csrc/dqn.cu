@@ -835,11 +835,11 @@ __device__ __forceinline__ void drain_pair_leaky(uint32_t taddr0, uint32_t taddr
 // The market columns of the next step's state rows are known a step ahead
 // (the bar advances by one whatever the action): warps of quarters 1-3 write
 // columns 0-47 of X as soon as layer 1 has read it.  The head's 48 columns
-// are read by the quarter 0-2 warps, 16 each: they exchange their advantage
-// sums through shared memory, each forms Q for its columns and its first
-// maximum, and the quarter-0 warps, which hold the episodes' environment
-// state, combine them, pick the action, step the environment and write
-// columns 48-55 (F[.., 48..50], V, e, spread).  Per step the MMA lane takes its weight units in this order
+// are read by the quarter 0-2 warps, 16 each: each forms its advantage sum and
+// first maximum, quarters 1 and 2 pass theirs through shared memory, and the
+// quarter-0 warps, which hold the episodes' environment state, combine them,
+// pick the action, step the environment and write columns 48-55 (F[.., 48..50],
+// V, e, spread).  Per step the MMA lane takes its weight units in this order
 // (the producers stream them in the same order): W2 chunks 0-3, W3 chunks
 // 0-3, the head, the next step's W1 (none after the last step); the first
 // step is preceded by its W1.
@@ -853,11 +853,11 @@ struct RBars {
     uint64_t h1[4], h2[4], h3[4];   // rows -> MMA: K-chunk c of a hidden layer is in Hb
     uint64_t hd_free;       // quarter 0-2 row warps -> MMA: the head's columns are read
     uint64_t q1, q2, q3, hd;        // MMA -> rows: that layer's MMAs are complete
-    uint64_t hx1[4], hx2[4];        // head exchange among the quarter 0-2 warps of the same lanes
+    uint64_t hx2[4];                // quarters 1, 2 -> quarter 0 of the same lanes: head partials written
     uint64_t fin;
 };
 
-constexpr int kRXFloats = 9 * 128;   // head exchange: sums [3][128], V [128], best [2][128], max [2][128], Q(a_rand) [128]
+constexpr int kRXFloats = 8 * 128;   // head exchange: sums [2][128], V [128], best [2][128], max [2][128], A(a_rand) [128]
 constexpr int kRSmem =
     1024 + kChunk + 4 * kChunk + kStages * kStage + kBiasFloats * 4 + kDivWords * 4 + kRXFloats * 4 + 1024;
 static_assert(kRSmem <= 232448, "rollout shared memory");
@@ -880,11 +880,11 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
     uint8_t *ring = Hb + 4 * kChunk;
     float *bias = reinterpret_cast<float *>(ring + kStages * kStage);
     uint32_t *div_s = reinterpret_cast<uint32_t *>(bias + kBiasFloats);
-    float *hsum = reinterpret_cast<float *>(div_s + kDivWords);      // [3][128] advantage sums of quarters 0-2
-    float *hval = hsum + 3 * 128;                                     // [128] V (quarter 2)
-    int *hbest = reinterpret_cast<int *>(hval + 128);                 // [2][128] first argmax of quarters 1, 2
-    float *hqmax = reinterpret_cast<float *>(hbest + 2 * 128);        // [2][128] their maxima
-    float *hqrand = hqmax + 2 * 128;                                  // [128] Q of the random action (quarters 1, 2)
+    float *hsum = reinterpret_cast<float *>(div_s + kDivWords);      // [2][128] advantage sums of quarters 1, 2
+    float *hval = hsum + 2 * 128;                                     // [128] V (quarter 2)
+    int *hbest = reinterpret_cast<int *>(hval + 128);                 // [2][128] first maximum's column, quarters 1, 2
+    float *hqmax = reinterpret_cast<float *>(hbest + 2 * 128);        // [2][128] their maxima of A
+    float *hqrand = hqmax + 2 * 128;                                  // [128] A of the random action (quarters 1, 2)
     RBars *bars = reinterpret_cast<RBars *>(hqrand + 128);
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
@@ -902,10 +902,7 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
             mbar_init(&bars->h3[c], kRRowWarps);
         }
         mbar_init(&bars->hd_free, 12);
-        for (int k = 0; k < 4; ++k) {
-            mbar_init(&bars->hx1[k], 3);
-            mbar_init(&bars->hx2[k], 2);
-        }
+        for (int k = 0; k < 4; ++k) mbar_init(&bars->hx2[k], 2);
         mbar_init(&bars->q1, 1);
         mbar_init(&bars->q2, 1);
         mbar_init(&bars->q3, 1);
@@ -1037,59 +1034,56 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
             float d[16];
             tmem_ld16(lane_t + rs, d);
             publish(&bars->hd_free);
-            float sA = 0.f, Vq = 0.f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int j = 16 * q + k;
-                d[k] += bh[k];                                 // A_j
-                if (j < kActions) sA += d[k];
-                else if (j == kActions) Vq = d[k];
-            }
-            hsum[q * 128 + r] = sA;
-            if (q == 2) hval[r] = Vq;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->hx1[quad]);
-            ok = warp_wait(&bars->hx1[quad], par, &abort_flag);
-            if (!ok) break;
-            const float meanA = ((hsum[r] + hsum[128 + r]) + hsum[256 + r]) / (float)kActions;
-            const float V = hval[r];
             // epsilon-greedy (every quarter advances an identical copy of the
             // episode's LCG): u1 decides, the second state gives the random action
             const float u1 = lcg_uniform(s.rng);
             s.rng = s.rng * 1664525u + 1013904223u;
             const int a_rand = (int)(((uint64_t)(s.rng >> 8) * (uint64_t)kActions) >> 24);
-            int best = 16 * q;
-            float qbest = -INFINITY, q_rand = 0.f;
+            // this quarter's advantage sum (column order), first maximum and its
+            // column, V (quarter 2) and A of the random action.  Q_j = V + (A_j -
+            // mean A) is nondecreasing in A_j under float rounding, so the greedy
+            // action is the first maximum of A and max Q = V + (max A - mean A).
+            float sA = 0.f, mA = -INFINITY, Vq = 0.f, Ar = 0.f;
+            int bA = 16 * q;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int j = 16 * q + k;
+                const float A = d[k] + bh[k];
                 if (j < kActions) {
-                    const float Qj = V + (d[k] - meanA);
-                    if (Qj > qbest) {
-                        qbest = Qj;
-                        best = j;
+                    sA += A;
+                    if (A > mA) {
+                        mA = A;
+                        bA = j;
                     }
-                    if (j == a_rand) q_rand = Qj;
+                    if (j == a_rand) Ar = A;
+                } else if (j == kActions) {
+                    Vq = A;
                 }
             }
             if (q > 0) {
-                hbest[(q - 1) * 128 + r] = best;
-                hqmax[(q - 1) * 128 + r] = qbest;
-                if (a_rand >= 16 * q && a_rand < 16 * q + 16) hqrand[r] = q_rand;
+                hsum[(q - 1) * 128 + r] = sA;
+                hqmax[(q - 1) * 128 + r] = mA;
+                hbest[(q - 1) * 128 + r] = bA;
+                if (q == 2) hval[r] = Vq;
+                if (a_rand >= 16 * q && a_rand < 16 * q + 16) hqrand[r] = Ar;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->hx2[quad]);
                 continue;
             }
             ok = warp_wait(&bars->hx2[quad], par, &abort_flag);
             if (!ok) break;
+            const float meanA = ((sA + hsum[r]) + hsum[128 + r]) / (float)kActions;
+            const float V = hval[r];
             // the first maximum over all 45 columns: a later quarter wins only if strictly greater
+            int best = bA;
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                if (hqmax[k * 128 + r] > qbest) {
-                    qbest = hqmax[k * 128 + r];
+                if (hqmax[k * 128 + r] > mA) {
+                    mA = hqmax[k * 128 + r];
                     best = hbest[k * 128 + r];
                 }
-            if (a_rand >= 16) q_rand = hqrand[r];
+            if (a_rand >= 16) Ar = hqrand[r];
+            const float qbest = V + (mA - meanA), q_rand = V + (Ar - meanA);
             const bool explore = u1 < a.epsilon;
             const int act = explore ? a_rand : best;
             const float q_sel = explore ? q_rand : qbest;
