@@ -173,6 +173,59 @@ struct GemmGroup {
 // w + 16, ... (eight at a time); lane l columns l, l + 32, ... of each
 // (consecutive lanes: consecutive addresses); bounds are predicates on the
 // accesses.
+// The same with 16-byte accesses: lane l takes columns 4 l .. 4 l + 3 of a
+// row (a warp one whole 128-column row per instruction), and in the transposed
+// pass rows 4 l .. 4 l + 3 of a column.  Used when the row strides and base
+// addresses allow it and the tile is whole in the directions it stores.
+template <int EPI>
+__device__ __forceinline__ void epilogue_vec(const GemmArgs &g, float *stage, int m0, int n0, int nrows, int ncols)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cc = 4 * lane, n = n0 + cc;
+    const bool cin = cc < ncols;                             // ncols is a multiple of 4
+    float4 bj = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (EPI == kGemmFwd && cin) bj = __ldg(reinterpret_cast<const float4 *>(g.bias + n));
+    for (int rr = warp; rr < nrows; rr += kWarps) {
+        const long long m = m0 + rr;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = cin ? stage[rr * kLd + cc + i] : 0.f;
+        if (EPI == kGemmFwd) {
+            v[0] += bj.x;
+            v[1] += bj.y;
+            v[2] += bj.z;
+            v[3] += bj.w;
+            if (g.relu) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[i] = relu(v[i]);
+            }
+        }
+        if (EPI == kGemmDx && cin) {
+            const float4 h = __ldg(reinterpret_cast<const float4 *>(g.H + m * g.ldh + n));
+            v[0] = h.x > 0.f ? v[0] : 0.f;
+            v[1] = h.y > 0.f ? v[1] : 0.f;
+            v[2] = h.z > 0.f ? v[2] : 0.f;
+            v[3] = h.w > 0.f ? v[3] : 0.f;
+        }
+        if (cin) {
+            *reinterpret_cast<float4 *>(g.Y + m * g.ldy + n) = make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) stage[rr * kLd + cc + i] = v[i];   // for the transposed pass
+        }
+    }
+    if (g.YT) {
+        __syncthreads();
+        const int r4 = 4 * lane;                             // nrows is a multiple of 4
+        for (int c0 = warp; c0 < ncols; c0 += kWarps) {
+            if (r4 < nrows) {
+                float *dst = g.YT + (long long)(n0 + c0) * g.ldt + m0 + r4;
+                *reinterpret_cast<float4 *>(dst) = make_float4(stage[r4 * kLd + c0], stage[(r4 + 1) * kLd + c0],
+                                                               stage[(r4 + 2) * kLd + c0], stage[(r4 + 3) * kLd + c0]);
+            }
+        }
+    }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue(const GemmArgs &g, float *stage, int m0, int n0, int nrows, int ncols)
 {
@@ -418,7 +471,17 @@ __device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *
         }
     }
     if (fin_here) {
-        if (g.epi == kGemmFwd) epilogue<kGemmFwd>(g, stage, m0, n0, nrows, ncols);
+        // 16-byte accesses where every row start is 16-byte aligned and the tile's
+        // extents are multiples of 4 (the weight-gradient product keeps the
+        // scalar form: its last column is the bias gradient)
+        const bool vec = g.epi != kGemmDw && (ncols & 3) == 0 && (nrows & 3) == 0 && (g.ldy & 3) == 0 &&
+                         ((uintptr_t)g.Y & 15) == 0 &&
+                         (g.epi != kGemmFwd || ((uintptr_t)g.bias & 15) == 0) &&
+                         (g.epi != kGemmDx || ((g.ldh & 3) == 0 && ((uintptr_t)g.H & 15) == 0)) &&
+                         (!g.YT || ((g.ldt & 3) == 0 && ((uintptr_t)g.YT & 15) == 0));
+        if (vec && g.epi == kGemmFwd) epilogue_vec<kGemmFwd>(g, stage, m0, n0, nrows, ncols);
+        else if (vec) epilogue_vec<kGemmDx>(g, stage, m0, n0, nrows, ncols);
+        else if (g.epi == kGemmFwd) epilogue<kGemmFwd>(g, stage, m0, n0, nrows, ncols);
         else if (g.epi == kGemmDw) epilogue<kGemmDw>(g, stage, m0, n0, nrows, ncols);
         else epilogue<kGemmDx>(g, stage, m0, n0, nrows, ncols);
     }
