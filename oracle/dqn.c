@@ -29,6 +29,14 @@
  * (floor(u2 * n_actions), exact in integers); the greedy action is the first
  * index of the largest Q; the target network sees the pre-reset next state
  * (the curiosity target); the stored Q is the online Q of the action taken.
+ * Episode recycling ("Future Phase 3 Optimization": when an episode ends,
+ * start a new one from a new random bar instead of idling), an option: after
+ * a done at step t < L - 1 the LCG is stepped once more and step t + 1 starts
+ * at bar ((s >> 8) * R) >> 24, R = n_bars - L + t + 1 (every bar that leaves
+ * room for the remaining steps and their next bars), with the portfolio reset
+ * as on every done; the finished transition's next state stays the
+ * pre-reset state at the bar after its own.  Without the option the episode
+ * goes on at the next bar, as in the PPO collector.
  *
  * Weights: one float32 buffer [online net | target net | curiosity block],
  * each net W1 [256 x 54], b1, W2 [256 x 256], b2, Wv1 [128 x 256], bv1,
@@ -128,12 +136,13 @@ static int first_argmax(const double *q, int n)
  * near-equal values); any other difference is a mismatch (also adopted, so
  * that the rest of the episode can be compared).  Dones as in oracle_episode.
  * Outputs (length L, or L * state_dim) may be NULL: states, actions, rewards,
- * dones, q (online Q of the action taken), td, next_states (pre-reset).
+ * dones, q (online Q of the action taken), td, next_states (pre-reset), bars
+ * (the bar each step's state was read from).  recycle: the option above.
  */
 int dqn_episode(const float *w, const oracle_cfg *c, const float *features, long n_bars, int start,
-                uint32_t seed, int L, double gamma, double epsilon, const int32_t *gpu_a, const int32_t *gpu_d,
-                double q_band, double done_band, float *o_states, int32_t *o_a, float *o_r, int32_t *o_d,
-                float *o_q, float *o_td, float *o_next, oracle_stats *st)
+                uint32_t seed, int L, double gamma, double epsilon, int recycle, const int32_t *gpu_a,
+                const int32_t *gpu_d, double q_band, double done_band, float *o_states, int32_t *o_a, float *o_r,
+                int32_t *o_d, float *o_q, float *o_td, float *o_next, int32_t *o_bars, oracle_stats *st)
 {
     const int nm = c->n_market, sd = nm + 3, na = c->n_actions;
     if (L <= 0 || start < 0 || (long)start + L > n_bars - 1 || na > ORACLE_MAX_W ||
@@ -145,9 +154,10 @@ int dqn_episode(const float *w, const oracle_cfg *c, const float *features, long
     env_state es;
     env_reset(&es);
     uint32_t s = seed;
+    long bar = start;
 
     for (int t = 0; t < L; ++t) {
-        long b = (long)start + t;
+        const long b = bar;
         for (int j = 0; j < nm; ++j) x[j] = (double)features[b * nm + j];
         x[nm] = es.V; x[nm + 1] = es.e; x[nm + 2] = c->spread;
 
@@ -192,6 +202,17 @@ int dqn_episode(const float *w, const oracle_cfg *c, const float *features, long
         if (o_d) o_d[t] = done;
         if (o_q) o_q[t] = (float)q_sel;
         if (o_td) o_td[t] = (float)td;
+        if (o_bars) o_bars[t] = (int32_t)b;
+
+        /* the next step's bar: the next one, or after a done with recycling a
+           fresh bar from the episode's LCG */
+        if (recycle && done && t < L - 1) {
+            s = oracle_lcg_step(s);
+            const uint64_t range = (uint64_t)(n_bars - L + t + 1);
+            bar = (long)((((uint64_t)(s >> 8)) * range) >> 24);
+        } else {
+            bar = b + 1;
+        }
     }
     return 0;
 }
@@ -199,17 +220,19 @@ int dqn_episode(const float *w, const oracle_cfg *c, const float *features, long
 /* episodes idx[0..n_sel-1]; per-episode outputs at row i; gpu_a / gpu_d are [N, L] */
 int dqn_rollout(const float *w, const oracle_cfg *c, const float *features, long n_bars, const int32_t *starts,
                 const uint32_t *seeds, const int32_t *idx, int n_sel, int L, double gamma, double epsilon,
-                const int32_t *gpu_a, const int32_t *gpu_d, double q_band, double done_band, float *o_states,
-                int32_t *o_a, float *o_r, int32_t *o_d, float *o_q, float *o_td, float *o_next, oracle_stats *st)
+                int recycle, const int32_t *gpu_a, const int32_t *gpu_d, double q_band, double done_band,
+                float *o_states, int32_t *o_a, float *o_r, int32_t *o_d, float *o_q, float *o_td, float *o_next,
+                int32_t *o_bars, oracle_stats *st)
 {
     const int sd = c->n_market + 3;
     for (int i = 0; i < n_sel; ++i) {
         long n = idx[i], row = (long)i * L;
-        int rc = dqn_episode(w, c, features, n_bars, starts[n], seeds[n], L, gamma, epsilon,
+        int rc = dqn_episode(w, c, features, n_bars, starts[n], seeds[n], L, gamma, epsilon, recycle,
                              gpu_a ? gpu_a + n * L : NULL, gpu_d ? gpu_d + n * L : NULL, q_band, done_band,
                              o_states ? o_states + row * sd : NULL, o_a ? o_a + row : NULL,
                              o_r ? o_r + row : NULL, o_d ? o_d + row : NULL, o_q ? o_q + row : NULL,
-                             o_td ? o_td + row : NULL, o_next ? o_next + row * sd : NULL, st);
+                             o_td ? o_td + row : NULL, o_next ? o_next + row * sd : NULL,
+                             o_bars ? o_bars + row : NULL, st);
         if (rc) return rc;
     }
     return 0;

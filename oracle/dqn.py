@@ -52,7 +52,8 @@ def lib():
         L.dqn_q.argtypes = [p, cfg, p, p]
         L.dqn_rollout.restype = C.c_int
         L.dqn_rollout.argtypes = [p, cfg, p, C.c_long, p, p, p, C.c_int, C.c_int, C.c_double, C.c_double,
-                                  p, p, C.c_double, C.c_double, p, p, p, p, p, p, p, C.POINTER(orc.OracleStats)]
+                                  C.c_int, p, p, C.c_double, C.c_double, p, p, p, p, p, p, p, p,
+                                  C.POINTER(orc.OracleStats)]
         _lib = L
     return _lib
 
@@ -82,9 +83,10 @@ def q_values(net: np.ndarray, cfg, x: np.ndarray) -> np.ndarray:
 
 def rollout(w, inputs, weights: np.ndarray, idx: Sequence[int], epsilon: float, quant: Optional[str] = None,
             horizon: Optional[int] = None, gamma: Optional[float] = None, gpu_actions=None, gpu_dones=None,
-            q_band: float = 0.0, done_band: float = 1e-6, threads: int = 1):
-    """Oracle outputs (states, next_states, actions, rewards, dones, q, td; leading
-    axis len(idx)) of the DQN collector for episodes idx, plus ``stats``."""
+            q_band: float = 0.0, done_band: float = 1e-6, threads: int = 1, recycle: bool = False):
+    """Oracle outputs (states, next_states, actions, rewards, dones, q, td, bars;
+    leading axis len(idx)) of the DQN collector for episodes idx, plus ``stats``.
+    recycle: after a done, the next step starts at a fresh bar from the LCG."""
     L = w.horizon if horizon is None else horizon
     g = w.gamma if gamma is None else gamma
     cfg = orc.make_cfg(w, quant)
@@ -93,7 +95,7 @@ def rollout(w, inputs, weights: np.ndarray, idx: Sequence[int], epsilon: float, 
     out = {"states": np.zeros((n, L, sd), np.float32), "next_states": np.zeros((n, L, sd), np.float32),
            "actions": np.zeros((n, L), np.int32), "rewards": np.zeros((n, L), np.float32),
            "dones": np.zeros((n, L), np.int32), "q": np.zeros((n, L), np.float32),
-           "td": np.zeros((n, L), np.float32)}
+           "td": np.zeros((n, L), np.float32), "bars": np.zeros((n, L), np.int32)}
     feats = np.ascontiguousarray(inputs.features, np.float32)
     starts = np.ascontiguousarray(inputs.starts, np.int32)
     seeds = np.ascontiguousarray(inputs.seeds, np.uint32)
@@ -106,10 +108,11 @@ def rollout(w, inputs, weights: np.ndarray, idx: Sequence[int], epsilon: float, 
         st = orc.OracleStats()
         sub = idx[lo:hi]
         rc = L_.dqn_rollout(_ptr(wts), C.byref(cfg), _ptr(feats), feats.shape[0], _ptr(starts), _ptr(seeds),
-                            _ptr(sub), sub.size, L, g, float(np.float32(epsilon)), _ptr(ga), _ptr(gd), q_band,
-                            done_band, _ptr(out["states"][lo:hi]), _ptr(out["actions"][lo:hi]),
+                            _ptr(sub), sub.size, L, g, float(np.float32(epsilon)), int(recycle), _ptr(ga),
+                            _ptr(gd), q_band, done_band, _ptr(out["states"][lo:hi]), _ptr(out["actions"][lo:hi]),
                             _ptr(out["rewards"][lo:hi]), _ptr(out["dones"][lo:hi]), _ptr(out["q"][lo:hi]),
-                            _ptr(out["td"][lo:hi]), _ptr(out["next_states"][lo:hi]), C.byref(st))
+                            _ptr(out["td"][lo:hi]), _ptr(out["next_states"][lo:hi]), _ptr(out["bars"][lo:hi]),
+                            C.byref(st))
         if rc != 0:
             raise ValueError(f"dqn_rollout rejected its arguments (rc={rc})")
         return st

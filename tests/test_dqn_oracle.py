@@ -187,3 +187,69 @@ def test_biases_and_stream_heads_closed_form(quant):
         assert abs(V - V0) <= 1e-12 * max(1.0, abs(V0))
         np.testing.assert_allclose(A, A0, rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(dqn.q_values(net, cfg, x), V0 + (A0 - A0.mean()), rtol=1e-12, atol=1e-12)
+
+
+def test_recycling_bars_follow_the_lcg():
+    """Episode recycling with a done on every step (a one-bar time barrier) and
+    epsilon = 1: each step draws u1, then the random action from the second LCG
+    state, then (before the last step) the next bar ((s3 >> 8) * R) >> 24 with
+    R = n_bars - L + t + 1 from the third; every state row reads its own bar and
+    every next state the bar after it."""
+    import dataclasses
+    w = dataclasses.replace(wl.DQN_WORKLOADS["dqn_tiny_bf16"], max_hold=1)
+    L = 40
+    inp = wl.generate(w, n_episodes=3, horizon=L)
+    W = wl.dqn_weights(5, 0.05)
+    nb = inp.features.shape[0]
+    out = dqn.rollout(w, inp, W, np.arange(3), 1.0, horizon=L, recycle=True)
+    assert (out["dones"] == 1).all()
+    for n in range(3):
+        s = int(inp.seeds[n])
+        bar = int(inp.starts[n])
+        for t in range(L):
+            assert out["bars"][n, t] == bar, (n, t)
+            np.testing.assert_array_equal(out["states"][n, t, :51], inp.features[bar])
+            np.testing.assert_array_equal(out["next_states"][n, t, :51], inp.features[bar + 1])
+            s = _lcg(s)
+            s = _lcg(s)
+            assert out["actions"][n, t] == ((s >> 8) * 45) >> 24, (n, t)
+            if t < L - 1:
+                s = _lcg(s)
+                R = nb - L + t + 1
+                bar = ((s >> 8) * R) >> 24
+                assert 0 <= bar and bar + (L - 1 - t) <= nb - 1
+        # the portfolio restarts with every step: V = 1, e = 0
+        assert (out["states"][n, :, 51] == 1.0).all() and (out["states"][n, :, 52] == 0.0).all()
+
+
+def test_recycling_off_is_the_default_and_on_keeps_the_rules():
+    """Without the option the bars are start + t and nothing else changes; with it,
+    a step after a done starts at a bar in [0, n_bars - L + t], every other step
+    at the next bar, and the states read those bars."""
+    w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
+    L = 120
+    inp = wl.generate(w, n_episodes=6, horizon=L)
+    W = wl.dqn_weights(6, 0.05)
+    a = dqn.rollout(w, inp, W, np.arange(6), 0.3, horizon=L)
+    b = dqn.rollout(w, inp, W, np.arange(6), 0.3, horizon=L, recycle=False)
+    for k in ("states", "next_states", "actions", "rewards", "dones", "q", "td", "bars"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    np.testing.assert_array_equal(a["bars"], inp.starts[:6, None] + np.arange(L)[None, :])
+    r = dqn.rollout(w, inp, W, np.arange(6), 0.3, horizon=L, recycle=True)
+    nb = inp.features.shape[0]
+    jumps = 0
+    for n in range(6):
+        for t in range(L - 1):
+            if r["dones"][n, t]:
+                assert 0 <= r["bars"][n, t + 1] <= nb - L + t
+                jumps += r["bars"][n, t + 1] != r["bars"][n, t] + 1
+            else:
+                assert r["bars"][n, t + 1] == r["bars"][n, t] + 1
+        np.testing.assert_array_equal(r["states"][n, :, :51], inp.features[r["bars"][n]])
+        np.testing.assert_array_equal(r["next_states"][n, :, :51], inp.features[r["bars"][n] + 1])
+    assert r["dones"].sum() > 0 and jumps > 0
+    # up to the first done the two runs agree
+    for n in range(6):
+        d = np.flatnonzero(r["dones"][n])
+        t0 = int(d[0]) + 1 if d.size else L
+        np.testing.assert_array_equal(r["actions"][n, :t0], a["actions"][n, :t0])
