@@ -208,7 +208,8 @@ DQN_CUR_FLOP = 2 * (54 * 64 + 64 * 54)                                    # curi
 
 def measure_dqn(dev, flush, steps, warmup):
     """The DQN collector on the reset-heavy environment at full size (16384 x 1000,
-    bf16): CUDA events around each run (L2 flushed before it) and per-kernel times."""
+    bf16): CUDA events around each run (L2 flushed before it) and per-kernel times,
+    without and with episode recycling: {False: (ms, phases), True: (ms, phases)}."""
     import torch
     from rl_experience_collection_gb300 import binding
     w = wl.DQN_WORKLOADS["dqn_reset_heavy_bf16"]
@@ -219,23 +220,28 @@ def measure_dqn(dev, flush, steps, warmup):
     stream = torch.cuda.current_stream(dev)
     args = (torch.from_numpy(inp.features).to(dev), torch.from_numpy(inp.starts).to(dev),
             torch.from_numpy(inp.seeds.view(np.int32)).to(dev), N, L, w.gamma, wl.DQN_EPSILON, out, stream)
-    for _ in range(warmup):
-        h.run(*args)
-    torch.cuda.synchronize()
-    h.set_timing(True)
-    ms, phase = [], []
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i in range(steps):
-        flush.fill_(float(i))
-        e0.record(stream)
-        h.run(*args)
-        e1.record(stream)
-        phase.append(h.phase_ms())
-        ms.append(e0.elapsed_time(e1))
-    if h.status() != binding.ROLLOUT_OK:
-        raise SystemExit("DQN status")
+    res = {}
+    for recycle in (False, True):
+        h.set_recycle(recycle)
+        h.set_timing(False)
+        for _ in range(warmup):
+            h.run(*args)
+        torch.cuda.synchronize()
+        h.set_timing(True)
+        ms, phase = [], []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(steps):
+            flush.fill_(float(i))
+            e0.record(stream)
+            h.run(*args)
+            e1.record(stream)
+            phase.append(h.phase_ms())
+            ms.append(e0.elapsed_time(e1))
+        if h.status() != binding.ROLLOUT_OK:
+            raise SystemExit("DQN status")
+        res[recycle] = (statistics.mean(ms), [statistics.mean(p[i] for p in phase) for i in range(3)])
     h.close()
-    return w, statistics.mean(ms), [statistics.mean(p[i] for p in phase) for i in range(3)]
+    return w, res
 
 
 OTHER_WORKLOADS = ("scaleout_tf32", "ceiling_bf16")
@@ -714,7 +720,9 @@ def main():
         del out
         out = None
         torch.cuda.empty_cache()
-        dw, d_ms, (r_ms, s_ms, t_ms) = measure_dqn(dev, flush, args.steps, args.warmup)
+        dw, dres = measure_dqn(dev, flush, args.steps, args.warmup)
+        d_ms, (r_ms, s_ms, t_ms) = dres[False]
+        dr_ms, dr_phase = dres[True]
         T = dw.n_episodes * dw.horizon
         r_fl, t_fl = T * DQN_NET_FLOP, T * (DQN_NET_FLOP + DQN_CUR_FLOP)
         peak_b = pk["bf16"]
@@ -728,7 +736,9 @@ def main():
             "target_roofline": {"bound": "tensor", "achieved": t_fl / (t_ms / 1000.0) / 1e12, "peak": peak_b,
                                 "unit": "TFLOP/s", "frac": t_fl / (t_ms / 1000.0) / 1e12 / peak_b,
                                 "algorithmic_flop_per_launch": t_fl},
-            "gpu_launches_per_run": 4, "l2": "flushed between runs"}
+            "gpu_launches_per_run": 4, "l2": "flushed between runs",
+            "recycle": {"tuples_per_s": T / (dr_ms / 1000.0), "ms_per_run": dr_ms,
+                        "phase_ms": dict(zip(("rollout", "states", "target"), dr_phase))}}
         out = binding.make_outputs(N, L, dev)
 
     # ---------------- end to end through the C ABI with host buffers (rollout_run_host:

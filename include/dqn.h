@@ -83,6 +83,22 @@ ROLLOUT_API int dqn_run(dqn_handle *h, const float *features, const int32_t *sta
                         int L, float gamma, float epsilon, float *states, int32_t *actions, float *rewards,
                         int32_t *dones, float *q, float *td, float *next_states, void *stream);
 
+/*
+ * dqn_set_recycle -- episode recycling ("GPU Pipeline Phase 2b", section
+ * "Future Phase 3 Optimization": an episode that ends starts again from a new
+ * random bar instead of idling).  When on != 0, in every later dqn_run a done
+ * at step t < L - 1 steps the episode's LCG state s once more and step t + 1
+ * starts at bar ((s >> 8) * R) >> 24 with R = n_bars - L + t + 1 (every bar
+ * that leaves room for the remaining steps and their next bars), with the
+ * portfolio reset as on every done; the done transition's next state (in
+ * next_states and behind td) stays the pre-reset state at the bar after its
+ * own.  on == 0 (the default) continues the episode at the next bar.  The
+ * handle then keeps an array of N * L int32 (the bar of every step), grown on
+ * the first run of a larger size (ROLLOUT_ERR_NOMEM when that fails).  Returns
+ * ROLLOUT_OK or ROLLOUT_ERR_INVALID (null handle).
+ */
+ROLLOUT_API int dqn_set_recycle(dqn_handle *h, int on);
+
 /* dqn_set_timing -- on: later runs record CUDA events around their rollout,
  * state-row and target-pass kernels (for measurement).  dqn_phase_ms --
  * synchronises and writes the last timed run's three kernel times (ms).

@@ -62,7 +62,7 @@ PER_EXPORTS = ["per_create", "per_insert", "per_sample", "per_update_priorities"
 
 
 DQN_EXPORTS = ["dqn_weight_count", "dqn_create", "dqn_set_weights", "dqn_run", "dqn_status", "dqn_destroy",
-               "dqn_set_timing", "dqn_phase_ms", "dqn_test_stall"]
+               "dqn_set_timing", "dqn_phase_ms", "dqn_test_stall", "dqn_set_recycle"]
 DQN_OUTPUTS = ("states", "actions", "rewards", "dones", "q", "td", "next_states")
 
 
@@ -133,6 +133,8 @@ def lib(path: Optional[str] = None):
     L.dqn_phase_ms.argtypes = [vp, C.POINTER(C.c_float)]
     L.dqn_test_stall.restype = C.c_int
     L.dqn_test_stall.argtypes = [vp, C.c_int]
+    L.dqn_set_recycle.restype = C.c_int
+    L.dqn_set_recycle.argtypes = [vp, C.c_int]
     L.dqn_destroy.restype = None
     L.dqn_destroy.argtypes = [vp]
     L.per_create.restype = C.c_int
@@ -623,6 +625,10 @@ class DqnCollector:
         ms = (C.c_float * 3)()
         _check(lib().dqn_phase_ms(self._h, ms))
         return [float(x) for x in ms]
+
+    def set_recycle(self, on: bool = True) -> None:
+        """Episode recycling: after a done, the next step starts at a fresh bar from the episode's LCG."""
+        _check(lib().dqn_set_recycle(self._h, int(on)))
 
     def test_stall(self, on: bool = True) -> None:
         """Test hook: later runs launch the target pass's stalling test build."""

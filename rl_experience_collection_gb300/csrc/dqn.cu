@@ -85,6 +85,7 @@ struct RolloutArgs {
     float *q;            // online Q of the action taken
     int *status;
     EnvConst env;
+    int32_t *bars;       // recycling build: the bar of every step (read by the state rows and the target pass)
 };
 
 struct TargetArgs {
@@ -101,6 +102,7 @@ struct TargetArgs {
     float *next_states;  // [N, L, 54] or null
     int *status;
     EnvConst env;
+    const int32_t *bars; // the bar of every step (episode recycling), or null: start + t
 };
 
 // a row warp's wait: every lane waits, and the warp goes on only if all of them
@@ -194,9 +196,11 @@ struct TMeta {
     long long i;     // flat transition index
     int valid;       // i < N L and the episode's start is in range
     int act, done, start, t, aprev, dprev;
+    int bar;         // the bar of the step (0 when !valid)
     float r0, qs, vin, vp;
 };
 
+template <bool kRecycle>
 __device__ __forceinline__ void load_meta(const TargetArgs &a, long long tile, int r, TMeta &m)
 {
     const long long R = (long long)a.N * a.L;
@@ -214,9 +218,11 @@ __device__ __forceinline__ void load_meta(const TargetArgs &a, long long tile, i
     m.vp = a.v_post[ic];
     m.aprev = a.actions[ip];
     m.dprev = a.dones[ip];
+    if (kRecycle) m.bar = a.bars[ic];
 }
 
 // validity and the derived fields, once the loads have landed
+template <bool kRecycle>
 __device__ __forceinline__ void resolve_meta(const TargetArgs &a, TMeta &m)
 {
     const long long R = (long long)a.N * a.L;
@@ -224,6 +230,10 @@ __device__ __forceinline__ void resolve_meta(const TargetArgs &a, TMeta &m)
     // the one-hot row read stays in bounds whatever the rollout left here
     // (its rows after a give-up are unwritten)
     if (!m.valid || (unsigned)m.act >= (unsigned)kActions) m.act = 0;
+    // a stored bar (episode recycling) is read where the rollout wrote it; the
+    // feature reads stay in bounds whatever a rollout that gave up left behind
+    if (!kRecycle) m.bar = m.start + m.t;
+    if (!m.valid || (unsigned)m.bar > (unsigned)(a.n_bars - 2)) m.bar = 0;
 }
 
 // the market columns of [16 q, 16 q + 16) of a padded feature row (zero past
@@ -343,8 +353,10 @@ __device__ __forceinline__ void publish(uint64_t *bar)
 
 // kStall: a test build in which the first producer of CTA 0 issues no copy, so
 // that CTA's MMA issuer waits on a weight stage that never fills and the
-// bounded-wait exit runs (dqn_test_stall)
-template <bool kStall>
+// bounded-wait exit runs (dqn_test_stall).  kRecycle: every step's bar is the
+// one the rollout stored (episode recycling), and a done step's next state is
+// never the next row's.
+template <bool kStall, bool kRecycle>
 __global__ void __launch_bounds__(kTThreads, 1) dqn_target_kernel(TargetArgs a, DqnImage w)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -422,7 +434,7 @@ __global__ void __launch_bounds__(kTThreads, 1) dqn_target_kernel(TargetArgs a, 
         TMeta cur;
         for (long long tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
             const uint32_t rs = (it & 1) * 256, ro = 256 - rs;
-            load_meta(a, tile, r, cur);                    // first used by curiosity layer 1
+            load_meta<kRecycle>(a, tile, r, cur);                    // first used by curiosity layer 1
             // layer 1 of the target net (region s) -> H1, chunk by chunk
             wait(&bars->q1);
             if (!ok) break;
@@ -434,10 +446,10 @@ __global__ void __launch_bounds__(kTThreads, 1) dqn_target_kernel(TargetArgs a, 
             // x' (this quarter's columns, float32) for the curiosity error, in
             // flight until curiosity layer 2; issued before the builders' loads
             // of the next tile begin (they wait for curiosity layer 1)
-            resolve_meta(a, cur);
+            resolve_meta<kRecycle>(a, cur);
             float xn[16];
             {
-                const long long b = cur.valid ? (long long)cur.start + cur.t : 0;
+                const long long b = cur.bar;
                 feat16(a.Fpad + (b + 1) * kFPad, q, cur.valid, xn);
                 state16_tail(cur.vp, exposure_of(cur.act), a.env.spread, q, cur.valid, xn);
             }
@@ -602,9 +614,9 @@ __global__ void __launch_bounds__(kTThreads, 1) dqn_target_kernel(TargetArgs a, 
                 if (!ok) break;
             }
             TMeta m;
-            load_meta(a, tile, r, m);
-            resolve_meta(a, m);
-            const long long b = m.valid ? (long long)m.start + m.t : 0;
+            load_meta<kRecycle>(a, tile, r, m);
+            resolve_meta<kRecycle>(a, m);
+            const long long b = m.bar;
             const float e_in = (m.t == 0 || m.dprev) ? 0.f : exposure_of(m.aprev);
             // the warp's 32 rows are consecutive bars of one episode: their
             // padded feature rows are one contiguous run, read in whole lines
@@ -639,7 +651,8 @@ __global__ void __launch_bounds__(kTThreads, 1) dqn_target_kernel(TargetArgs a, 
                 state_row(X, r, a.Fpad + b * kFPad, m.valid, m.vin, e_in, a.env.spread);
             }
             __syncwarp();                                  // the warp's rows of X are written
-            if (m.valid && lane < 31 && m.t < a.L - 1) {
+            // (with recycling a done step's next row starts a new episode elsewhere)
+            if (m.valid && lane < 31 && m.t < a.L - 1 && !(kRecycle && m.done)) {
 #pragma unroll
                 for (int u = 0; u < 6; ++u)
                     *reinterpret_cast<uint4 *>(Xn + sw128_offset(r, u)) =
@@ -854,10 +867,13 @@ struct RBars {
     uint64_t hd_free;       // quarter 0-2 row warps -> MMA: the head's columns are read
     uint64_t q1, q2, q3, hd;        // MMA -> rows: that layer's MMAs are complete
     uint64_t hx2[4];                // quarters 1, 2 -> quarter 0 of the same lanes: head partials written
+    uint64_t ve;                    // recycling build: quarter 0 -> the others: the next step's bar and LCG state
     uint64_t fin;
 };
 
-constexpr int kRXFloats = 8 * 128;   // head exchange: sums [2][128], V [128], best [2][128], max [2][128], A(a_rand) [128]
+// head exchange: sums [2][128], V [128], best [2][128], max [2][128], A(a_rand) [128];
+// recycling: the next step's bar [128] and LCG state [128]
+constexpr int kRXFloats = 10 * 128;
 constexpr int kRSmem =
     1024 + kChunk + 4 * kChunk + kStages * kStage + kBiasFloats * 4 + kDivWords * 4 + kRXFloats * 4 + 1024;
 static_assert(kRSmem <= 232448, "rollout shared memory");
@@ -871,6 +887,10 @@ __device__ __forceinline__ int rollout_unit(long long g)
     return pos < 9 ? 1 + pos : 0;
 }
 
+// kRecycle: episode recycling (after a done, the next step starts at a fresh bar
+// drawn from the episode's LCG); the quarter-0 warps, which step the
+// environment, pass each row's next bar and LCG state to the other warps
+template <bool kRecycle>
 __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a, DqnImage w)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -885,7 +905,9 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
     int *hbest = reinterpret_cast<int *>(hval + 128);                 // [2][128] first maximum's column, quarters 1, 2
     float *hqmax = reinterpret_cast<float *>(hbest + 2 * 128);        // [2][128] their maxima of A
     float *hqrand = hqmax + 2 * 128;                                  // [128] A of the random action (quarters 1, 2)
-    RBars *bars = reinterpret_cast<RBars *>(hqrand + 128);
+    int *bar_s = reinterpret_cast<int *>(hqrand + 128);               // [128] recycling: the row's next bar
+    uint32_t *rng_s = reinterpret_cast<uint32_t *>(bar_s + 128);      // [128] recycling: the row's LCG state
+    RBars *bars = reinterpret_cast<RBars *>(rng_s + 128);
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
@@ -903,6 +925,7 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
         }
         mbar_init(&bars->hd_free, 12);
         for (int k = 0; k < 4; ++k) mbar_init(&bars->hx2[k], 2);
+        mbar_init(&bars->ve, 4);
         mbar_init(&bars->q1, 1);
         mbar_init(&bars->q2, 1);
         mbar_init(&bars->q3, 1);
@@ -946,6 +969,7 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
         EpState s;
         ep_reset(s);
         s.rng = n < a.N ? a.seeds[n] : 0u;
+        long long bar = valid ? start : 0;            // the bar of the current step
         // X columns of bar b: quarters 1-3 their 16 market columns; quarter 0
         // F[b, 48..50] and the bar's simple return (column 51 of the padded row)
         auto fetch = [&](long long b, float (&f)[16]) {
@@ -989,15 +1013,27 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
         bool ok = true;
         for (int t = 0; t < L && ok; ++t) {
             const uint32_t par = t & 1, rs = par * 256, ro = 256 - rs;
-            const long long b = (long long)start + t;
-            fetch(valid ? b + 1 : 0, f);                   // the next bar: X of step t + 1, its return
             auto wait = [&](uint64_t *bar) {
                 ok = ok && warp_wait(bar, par, &abort_flag);
                 tc_fence_after();
             };
+            if (!kRecycle || q == 0) {
+                if (!kRecycle) bar = valid ? (long long)start + t : 0;
+                fetch(valid ? bar + 1 : 0, f);             // the next bar: X of step t + 1, its return
+            }
             // layer 1 (region s) -> H1
             wait(&bars->q1);
             if (!ok) break;
+            if (kRecycle && q > 0) {
+                // this step's bar and LCG state as the quarter-0 warp left them
+                if (t > 0) {
+                    ok = warp_wait(&bars->ve, par ^ 1u, &abort_flag);
+                    if (!ok) break;
+                    bar = bar_s[r];
+                    s.rng = rng_s[r];
+                }
+                fetch(valid ? bar + 1 : 0, f);
+            }
 #pragma unroll 1
             for (int c = 0; c < 4; c += 2)
                 drain_pair_leaky(lane_t + rs + 64 * c, lane_t + rs + 64 * c + 64, bias + 64 * c + 16 * q,
@@ -1098,7 +1134,41 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
                 rew = env_window_reward(s, act, pnl, label, done, env);
             }
             // the next step's columns 48..55 (V and e after the trade), then the stores
-            put_tail(f);
+            if (kRecycle) {
+                // after a done, the next step starts at a fresh bar: one more LCG
+                // state, over every bar that leaves room for the remaining steps
+                long long nb = bar + 1;
+                if (valid && done && t < L - 1) {
+                    s.rng = s.rng * 1664525u + 1013904223u;
+                    const uint64_t range = (uint64_t)(a.n_bars - L + t + 1);
+                    nb = (long long)(((uint64_t)(s.rng >> 8) * range) >> 24);
+                }
+                if (n < a.N) a.bars[i] = valid ? (int32_t)bar : 0;
+                if (nb != bar + 1) {
+                    // this row's next state: the market columns of the new bar (the
+                    // other quarters wrote the previous bar's), V = 1, e = 0
+                    const float4 *src = reinterpret_cast<const float4 *>(a.Fpad + nb * kFPad);
+#pragma unroll
+                    for (int u = 0; u < 6; ++u) {
+                        const float4 f0 = __ldg(src + 2 * u), f1 = __ldg(src + 2 * u + 1);
+                        *reinterpret_cast<uint4 *>(X + sw128_offset(r, u)) =
+                            make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f0.z, f0.w), pack_bf16x2(f1.x, f1.y),
+                                       pack_bf16x2(f1.z, f1.w));
+                    }
+                    const float4 f12 = __ldg(src + 12);
+                    float g[16] = {f12.x, f12.y, f12.z};
+                    put_tail(g);
+                } else {
+                    put_tail(f);
+                }
+                bar_s[r] = (int)nb;
+                rng_s[r] = s.rng;
+                bar = nb;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->ve);
+            } else {
+                put_tail(f);
+            }
             publish(&bars->x);
             if (n < a.N) {
                 a.actions[i] = valid ? act : 0;
@@ -1239,6 +1309,9 @@ struct dqn_handle {
     bool timing = false, timed_run = false;
     cudaEvent_t ev[4] = {};
     bool test_stall = false;   // dqn_test_stall: launch the target pass's stalling test build
+    bool recycle = false;      // dqn_set_recycle: episode recycling
+    int32_t *d_bars = nullptr; // recycling: the bar of every step [N L]
+    size_t bars_cap = 0;
 };
 
 namespace rl {
@@ -1447,6 +1520,7 @@ void free_handle(dqn_handle *h)
     cudaFree(h->d_div);
     cudaFree(h->d_status);
     cudaFree(h->d_vpost);
+    cudaFree(h->d_bars);
     cudaFree(h->d_fpad);
     for (cudaEvent_t e : h->ev)
         if (e) cudaEventDestroy(e);
@@ -1477,12 +1551,18 @@ int dqn_create(const float *weights, const rollout_dims *dims, dqn_handle **out)
         (e = cudaMalloc(&h->d_status, sizeof(int))) != cudaSuccess ||
         (e = cudaMemset(h->d_status, 0, sizeof(int))) != cudaSuccess ||
         (e = cudaMalloc(&h->d_fpad, (size_t)dims->n_bars * kFPad * sizeof(float))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(dqn_rollout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem)) !=
+        (e = cudaFuncSetAttribute(dqn_rollout_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem)) !=
             cudaSuccess ||
-        (e = cudaFuncSetAttribute(dqn_target_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem)) !=
+        (e = cudaFuncSetAttribute(dqn_rollout_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem)) !=
             cudaSuccess ||
-        (e = cudaFuncSetAttribute(dqn_target_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem)) !=
-            cudaSuccess) {
+        (e = cudaFuncSetAttribute(dqn_target_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kTSmem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(dqn_target_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kTSmem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(dqn_target_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kTSmem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(dqn_target_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kTSmem)) != cudaSuccess) {
         free_handle(h);
         return cuda_fail(e, "DQN handle setup");
     }
@@ -1524,6 +1604,15 @@ int dqn_run(dqn_handle *h, const float *features, const int32_t *starts, const u
         if ((e = cudaMalloc(&h->d_vpost, NL * sizeof(float))) != cudaSuccess) return cuda_fail(e, "cudaMalloc(scratch)");
         h->vpost_cap = NL;
     }
+    if (h->recycle && NL > h->bars_cap) {
+        if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        cudaFree(h->d_bars);
+        h->d_bars = nullptr;
+        h->bars_cap = 0;
+        if ((e = cudaMalloc(&h->d_bars, NL * sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc(bars)");
+        h->bars_cap = NL;
+    }
+    int32_t *bars = h->recycle ? h->d_bars : nullptr;
     cudaStream_t s = (cudaStream_t)stream;
     h->last_stream = s;
     const rollout_dims &d = h->dims;
@@ -1531,23 +1620,29 @@ int dqn_run(dqn_handle *h, const float *features, const int32_t *starts, const u
     const EnvConst env{d.barrier, d.max_hold, d.pt_scale, d.sl_scale, d.div_window, d.div_thresh, d.div_penalty,
                        d.cur_coef, d.risk_coef, d.tx_base, d.spread, h->d_div};
     const RolloutArgs ra{features, h->d_fpad, starts, seeds, N, L, d.n_bars, epsilon, actions, dones, rewards, td,
-                         h->d_vpost, q, h->d_status, env};
+                         h->d_vpost, q, h->d_status, env, bars};
     auto mark = [&](int i) { return h->timing ? cudaEventRecord(h->ev[i], s) : cudaSuccess; };
     if ((e = launch_pad_features(features, h->d_fpad, d.n_bars, s)) != cudaSuccess)
         return cuda_fail(e, "feature padding launch");
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    dqn_rollout_kernel<<<(N + 127) / 128, kRThreads, kRSmem, s>>>(ra, h->img);
+    if (h->recycle) dqn_rollout_kernel<true><<<(N + 127) / 128, kRThreads, kRSmem, s>>>(ra, h->img);
+    else dqn_rollout_kernel<false><<<(N + 127) / 128, kRThreads, kRSmem, s>>>(ra, h->img);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "DQN rollout launch");
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    const StatesArgs sa{features, starts, N, L, d.n_bars, actions, dones, td, d.spread, states, h->d_fpad};
+    const StatesArgs sa{features, starts, N, L, d.n_bars, actions, dones, td, d.spread, states, h->d_fpad, bars};
     if ((e = launch_states(sa, s)) != cudaSuccess) return cuda_fail(e, "state-row launch");
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     const TargetArgs ta{features, h->d_fpad, starts, N, L, d.n_bars, gamma, actions, dones, rewards, td, h->d_vpost,
-                        q, next_states, h->d_status, env};
+                        q, next_states, h->d_status, env, bars};
     const long long tiles = (long long)((NL + 127) / 128);
     const int grid = (int)(tiles < h->sms ? tiles : h->sms);
-    if (h->test_stall) dqn_target_kernel<true><<<grid, kTThreads, kTSmem, s>>>(ta, h->img);
-    else dqn_target_kernel<false><<<grid, kTThreads, kTSmem, s>>>(ta, h->img);
+    if (h->test_stall) {
+        if (h->recycle) dqn_target_kernel<true, true><<<grid, kTThreads, kTSmem, s>>>(ta, h->img);
+        else dqn_target_kernel<true, false><<<grid, kTThreads, kTSmem, s>>>(ta, h->img);
+    } else {
+        if (h->recycle) dqn_target_kernel<false, true><<<grid, kTThreads, kTSmem, s>>>(ta, h->img);
+        else dqn_target_kernel<false, false><<<grid, kTThreads, kTSmem, s>>>(ta, h->img);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "DQN target launch");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     h->timed_run = h->timing;
@@ -1564,6 +1659,14 @@ int dqn_set_timing(dqn_handle *h, int on)
             if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
         }
     h->timing = on != 0;
+    return ROLLOUT_OK;
+}
+
+int dqn_set_recycle(dqn_handle *h, int on)
+{
+    clear_error();
+    if (!h) return set_error(ROLLOUT_ERR_INVALID, "null handle");
+    h->recycle = on != 0;
     return ROLLOUT_OK;
 }
 

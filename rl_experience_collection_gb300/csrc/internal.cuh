@@ -123,6 +123,7 @@ struct StatesArgs {
     float spread;
     float *states;             // [N, L, 54] written
     const float *Fpad = nullptr;   // optional copy of F with rows padded to kFPad floats (16-byte aligned rows)
+    const int32_t *bars = nullptr; // optional bar of every step (episode recycling); else start + t
 };
 
 // the feature matrix with rows padded to kFPad floats (16-byte aligned rows;

@@ -57,7 +57,13 @@ __global__ void __launch_bounds__(kWarps * 32) states_kernel(StatesArgs a)
             const int dprev = t > 0 ? a.dones[row - 1] : 1;
             const int aprev = t > 0 ? a.actions[row - 1] : 0;
             if (start_ok(start, a.L, a.n_bars)) {
-                fb = ((long long)start + t) * RS;
+                long long b = (long long)start + t;
+                // a stored bar (episode recycling), read where the rollout wrote it
+                if (a.bars) {
+                    b = a.bars[row];
+                    if (b < 0 || b > a.n_bars - 2) b = 0;
+                }
+                fb = b * RS;
                 v = vin;
                 e = dprev ? 0.f : exposure_of(aprev);
             }

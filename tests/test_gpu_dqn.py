@@ -34,10 +34,12 @@ def _built():
     dqn.build()
 
 
-def _run(w, inp, W, N, L, eps, next_states=True, starts=None):
+def _run(w, inp, W, N, L, eps, next_states=True, starts=None, recycle=False):
     import torch
     from rl_experience_collection_gb300 import binding
     h = binding.DqnCollector.for_workload(w, W, n_bars=inp.features.shape[0])
+    if recycle:
+        h.set_recycle(True)
     out = binding.make_dqn_outputs(N, L, next_states=next_states)
     st = inp.starts[:N] if starts is None else starts
     h.run(torch.from_numpy(inp.features).cuda(), torch.from_numpy(np.ascontiguousarray(st)).cuda(),
@@ -47,11 +49,13 @@ def _run(w, inp, W, N, L, eps, next_states=True, starts=None):
     return status, {k: v.cpu().numpy() for k, v in out.items()}
 
 
-def _compare(w, inp, W, g, idx, L, eps):
+def _compare(w, inp, W, g, idx, L, eps, recycle=False, ref_out=None):
     from oracle import dqn
     sel = np.asarray(idx)
     ref = dqn.rollout(w, inp, W, sel, eps, horizon=L, gpu_actions=g["actions"], gpu_dones=g["dones"],
-                      q_band=Q_BAND, done_band=DONE_BAND, threads=16)
+                      q_band=Q_BAND, done_band=DONE_BAND, threads=16, recycle=recycle)
+    if ref_out is not None:
+        ref_out.update(ref)
     st = ref["stats"]
     assert st["action_mismatches"] == 0 and st["done_mismatches"] == 0, st
     g = {k: v[sel] for k, v in g.items()}
@@ -94,6 +98,60 @@ def test_dqn_matches_oracle(N, L, eps, next_states):
     assert st["action_replays"] <= max(2, N * L // 2000)
     if L > w.max_hold:                       # the time barrier alone ends every episode by then
         assert g["dones"].sum() > 0
+
+
+@pytest.mark.parametrize("N,L,eps", [(300, 60, 0.1), (129, 200, 0.3), (1, 40, 0.0)])
+def test_dqn_recycling_matches_oracle(N, L, eps):
+    """Episode recycling: after a done the next step starts at a bar drawn from
+    the episode's LCG.  The states' market columns are compared exactly, so every
+    recycled bar is checked; the next states of done steps stay the pre-reset
+    state at the bar after their own.  Several rollout CTAs with a ragged last
+    one; 202 target-pass tiles (several per CTA, rows of one warp spanning
+    recycled bars); a single greedy episode."""
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
+    inp = wl.generate(w, n_episodes=N, horizon=L)
+    W = wl.dqn_weights(N + 3, 0.05)
+    status, g = _run(w, inp, W, N, L, eps, recycle=True)
+    assert status == binding.ROLLOUT_OK
+    ref = {}
+    st = _compare(w, inp, W, g, np.arange(N), L, eps, recycle=True, ref_out=ref)
+    assert st["action_replays"] <= max(2, N * L // 2000)
+    nb = inp.features.shape[0]
+    bars = ref["bars"]
+    plain = inp.starts[:N, None].astype(np.int64) + np.arange(L)[None, :]
+    assert (bars >= 0).all() and (bars + (L - np.arange(L))[None, :] <= nb - 1).all()
+    if N > 1:
+        assert (bars != plain).any()          # some episodes did recycle
+        # a recycled step's state holds a fresh portfolio
+        d = g["dones"][:, :-1].astype(bool)
+        np.testing.assert_array_equal(g["states"][:, 1:, 51][d], 1.0)
+        np.testing.assert_array_equal(g["states"][:, 1:, 52][d], 0.0)
+
+
+def test_recycling_off_again_restores_the_plain_run():
+    """set_recycle(False) after a recycling run gives the default outputs again."""
+    import torch
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
+    N, L = 140, 50
+    inp = wl.generate(w, n_episodes=N, horizon=L)
+    W = wl.dqn_weights(11, 0.05)
+    _, g0 = _run(w, inp, W, N, L, 0.2)
+    h = binding.DqnCollector.for_workload(w, W, n_bars=inp.features.shape[0])
+    args = (torch.from_numpy(inp.features).cuda(), torch.from_numpy(inp.starts[:N]).cuda(),
+            torch.from_numpy(inp.seeds[:N].view(np.int32)).cuda(), N, L, w.gamma, 0.2)
+    outs = []
+    for on in (True, False):
+        h.set_recycle(on)
+        out = binding.make_dqn_outputs(N, L)
+        h.run(*args, out)
+        assert h.status() == binding.ROLLOUT_OK
+        outs.append({k: v.cpu().numpy() for k, v in out.items()})
+    h.close()
+    assert not np.array_equal(outs[0]["states"], g0["states"])
+    for k in g0:
+        np.testing.assert_array_equal(outs[1][k], g0[k], err_msg=k)
 
 
 def test_out_of_range_start_and_determinism():
