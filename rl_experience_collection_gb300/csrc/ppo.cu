@@ -32,6 +32,7 @@
 
 #include "../../include/ppo.h"
 #include "internal.cuh"
+#include "pdl.cuh"
 #include "ppo_gemm.cuh"
 
 using namespace rl;
@@ -147,6 +148,7 @@ __global__ void gather_kernel(const float *states, const int32_t *actions, const
 __global__ void actor_head_kernel(const float *logits, const int32_t *a, const float *lpo, const float *A, int B,
                                   float clip_eps, float *dl, float *dlt, int ldt, float *rows)
 {
+    pdl_wait();
     const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (w >= B) return;
     const float *l = logits + (size_t)w * kActions;
@@ -185,6 +187,7 @@ __global__ void actor_head_kernel(const float *logits, const int32_t *a, const f
 __global__ void critic_head_kernel(const float *v, const float *R, int B, float value_coef, float *dv, float *dvt,
                                    float *rows)
 {
+    pdl_wait();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= B) return;
     const float d = v[r] - R[r];
@@ -210,6 +213,7 @@ __device__ __forceinline__ double block_sum(double v, double *sh)
 // partial sums of g^2 over a fixed partition (kNormBlocks blocks)
 __global__ void __launch_bounds__(kNormThreads) norm_partial_kernel(const float *g, size_t n, double *part)
 {
+    pdl_wait();
     __shared__ double sh[kNormThreads];
     double s = 0.0;
     for (size_t i = blockIdx.x * (size_t)kNormThreads + threadIdx.x; i < n; i += (size_t)kNormBlocks * kNormThreads)
@@ -224,6 +228,7 @@ __global__ void __launch_bounds__(kNormThreads) adam_kernel(float *p, const floa
                                                              const double *part, ppo_hparams hp, const long long *step_t,
                                                              const int *step_k, float *stats)
 {
+    pdl_wait();
     __shared__ float sh_scale, sh_bc1, sh_bc2;
     __shared__ double sh[kNormThreads];
     // every block adds the partials in the same fixed order (a strided
@@ -258,6 +263,7 @@ __global__ void __launch_bounds__(kNormThreads) adam_kernel(float *p, const floa
 // means of the four per-row statistics, in row order, into slot step_k of stats
 __global__ void stats_kernel(const float *rows, int B, float *stats, const int *step_k)
 {
+    pdl_wait();
     __shared__ double sh[256];
     float *out = stats + (size_t)*step_k * 5;
     for (int k = 0; k < 4; ++k) {
@@ -278,6 +284,7 @@ struct LayerTable {
 
 __global__ void transpose_weights_kernel(const float *w, float *wt, LayerTable lt)
 {
+    pdl_wait();
     for (int l = 0; l < lt.n; ++l) {
         const long long n = (long long)lt.in[l] * lt.out[l];
         const float *src = w + lt.off[l];
@@ -300,6 +307,7 @@ __global__ void ones_row_kernel(float *buf, int row, int ld)
 // the end of a step: the next step's slice and Adam count
 __global__ void advance_kernel(int *step_k, long long *step_t)
 {
+    pdl_wait();
     *step_k += 1;
     *step_t += 1;
 }
@@ -600,11 +608,15 @@ int loss_gradient(ppo_trainer *t, const float *states, const int32_t *actions, c
         if ((rc = run_stage(t, j, B, s))) return rc;
     // the two loss heads: the actor's surrogate and the critic's squared error,
     // each with its gradient at the net's output (and that gradient's transpose)
-    actor_head_kernel<<<(B * 32 + 255) / 256, 256, 0, s>>>(t->d_act[0][2], t->d_a, t->d_lpo, t->d_adv, B,
-                                                           hp->clip_eps, t->d_dy[0][0], t->d_dyt[0][0], t->cap,
-                                                           t->d_rows);
-    critic_head_kernel<<<(B + 255) / 256, 256, 0, s>>>(t->d_act[1][kCriticLayers - 1], t->d_ret, B, hp->value_coef,
-                                                       t->d_dy[1][0], t->d_dyt[1][0], t->d_rows);
+    cudaError_t e = launch_dependent(actor_head_kernel, dim3((B * 32 + 255) / 256), dim3(256), 0, s,
+                                     (const float *)t->d_act[0][2], (const int32_t *)t->d_a, (const float *)t->d_lpo,
+                                     (const float *)t->d_adv, B, hp->clip_eps, t->d_dy[0][0], t->d_dyt[0][0], t->cap,
+                                     t->d_rows);
+    if (e == cudaSuccess)
+        e = launch_dependent(critic_head_kernel, dim3((B + 255) / 256), dim3(256), 0, s,
+                             (const float *)t->d_act[1][kCriticLayers - 1], (const float *)t->d_ret, B,
+                             hp->value_coef, t->d_dy[1][0], t->d_dyt[1][0], t->d_rows);
+    if (e != cudaSuccess) return cuda_err(e, "PPO loss-head launch");
     // backward products of both nets, depth by depth from the top
     for (int j = kMaxLayers; j < kStages; ++j)
         if ((rc = run_stage(t, j, B, s))) return rc;
@@ -618,13 +630,18 @@ int step(ppo_trainer *t, const float *states, const int32_t *actions, const floa
 {
     int rc = loss_gradient(t, states, actions, logp_old, adv, ret, T, indices, B, hp, s);
     if (rc) return rc;
-    norm_partial_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_g, t->n_trained, t->d_part);
-    adam_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_w, t->d_g, t->d_m, t->d_v, t->n_trained, t->d_part, *hp,
-                                                     t->d_t, t->d_k, stats);
-    transpose_weights_kernel<<<kNormBlocks, kNormThreads, 0, s>>>(t->d_w, t->d_wt, layer_table(t));
-    if (stats) stats_kernel<<<1, 256, 0, s>>>(t->d_rows, B, stats, t->d_k);
-    advance_kernel<<<1, 1, 0, s>>>(t->d_k, t->d_t);
-    cudaError_t e = cudaGetLastError();
+    const dim3 nb(kNormBlocks), nt(kNormThreads);
+    cudaError_t e = launch_dependent(norm_partial_kernel, nb, nt, 0, s, (const float *)t->d_g, t->n_trained, t->d_part);
+    if (e == cudaSuccess)
+        e = launch_dependent(adam_kernel, nb, nt, 0, s, t->d_w, (const float *)t->d_g, t->d_m, t->d_v, t->n_trained,
+                             (const double *)t->d_part, *hp, (const long long *)t->d_t, (const int *)t->d_k, stats);
+    if (e == cudaSuccess)
+        e = launch_dependent(transpose_weights_kernel, nb, nt, 0, s, (const float *)t->d_w, t->d_wt, layer_table(t));
+    if (e == cudaSuccess && stats)
+        e = launch_dependent(stats_kernel, dim3(1), dim3(256), 0, s, (const float *)t->d_rows, B, stats,
+                             (const int *)t->d_k);
+    if (e == cudaSuccess) e = launch_dependent(advance_kernel, dim3(1), dim3(1), 0, s, t->d_k, t->d_t);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? ROLLOUT_OK : cuda_err(e, "PPO step launch");
 }
 

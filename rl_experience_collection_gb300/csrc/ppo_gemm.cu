@@ -41,6 +41,7 @@
 // the tiles and splits of all of them).
 // Every wait is bounded; a CTA that gives up sets ROLLOUT_ERR_TIMEOUT.
 #include "env.cuh"
+#include "pdl.cuh"
 #include "ppo_gemm.cuh"
 #include "umma.cuh"
 
@@ -319,6 +320,9 @@ __device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the set-up above overlaps the kernel ahead on the stream; its outputs are
+    // read from here on
+    pdl_wait();
     const uint32_t tmem = tmem_sh;
     volatile int *abort = &abort_sh;
     constexpr uint32_t id = idesc(true, kBM, kBN);
@@ -485,6 +489,9 @@ __device__ __forceinline__ void gemm_cta(const GemmArgs &g, int local, uint8_t *
         else if (g.epi == kGemmDw) epilogue<kGemmDw>(g, stage, m0, n0, nrows, ncols);
         else epilogue<kGemmDx>(g, stage, m0, n0, nrows, ncols);
     }
+    // the next kernel may be scheduled while this one tears down (it still waits
+    // for this grid's completion before reading what it wrote)
+    pdl_trigger();
     if (!ok && tid == 0) set_status(g.status, ROLLOUT_ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
@@ -551,8 +558,8 @@ cudaError_t launch_gemm_group(const GemmArgs *g, int n, cudaStream_t s)
         blocks += ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN) * a.ksplit;
     }
     grp.first[n] = blocks;
-    gemm_group_kernel<<<blocks, kGemmThreads, kGemmSmem, s>>>(grp);
-    return cudaGetLastError();
+    const cudaError_t e = launch_dependent(gemm_group_kernel, dim3(blocks), dim3(kGemmThreads), kGemmSmem, s, grp);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace rl
