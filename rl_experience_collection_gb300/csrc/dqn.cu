@@ -1017,22 +1017,23 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
                 ok = ok && warp_wait(bar, par, &abort_flag);
                 tc_fence_after();
             };
-            if (!kRecycle || q == 0) {
-                if (!kRecycle) bar = valid ? (long long)start + t : 0;
-                fetch(valid ? bar + 1 : 0, f);             // the next bar: X of step t + 1, its return
-            }
+            // the next bar: X of step t + 1, its return.  With recycling the other
+            // quarters learn this step's bar from the quarter-0 warp only after
+            // layer 1; they fetch for the bar after the previous one meanwhile and
+            // fetch again where the episode was recycled.
+            const long long guess = (kRecycle && q > 0 && t > 0) ? bar + 1 : bar;
+            if (!kRecycle) bar = valid ? (long long)start + t : 0;
+            fetch(valid ? (kRecycle ? guess : bar) + 1 : 0, f);
             // layer 1 (region s) -> H1
             wait(&bars->q1);
             if (!ok) break;
-            if (kRecycle && q > 0) {
+            if (kRecycle && q > 0 && t > 0) {
                 // this step's bar and LCG state as the quarter-0 warp left them
-                if (t > 0) {
-                    ok = warp_wait(&bars->ve, par ^ 1u, &abort_flag);
-                    if (!ok) break;
-                    bar = bar_s[r];
-                    s.rng = rng_s[r];
-                }
-                fetch(valid ? bar + 1 : 0, f);
+                ok = warp_wait(&bars->ve, par ^ 1u, &abort_flag);
+                if (!ok) break;
+                bar = bar_s[r];
+                s.rng = rng_s[r];
+                if (bar != guess) fetch(valid ? bar + 1 : 0, f);
             }
 #pragma unroll 1
             for (int c = 0; c < 4; c += 2)
