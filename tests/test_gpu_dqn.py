@@ -225,3 +225,37 @@ def test_full_size_sampled_episodes():
     sub = wl.Inputs(inp.features, inp.starts[idx], inp.seeds[idx], inp.weights)
     st = _compare(w, sub, W, {k: v for k, v in g.items()}, np.arange(idx.size), L, wl.DQN_EPSILON)
     assert st["action_replays"] <= 4
+
+
+def test_full_size_recycling_sampled_episodes():
+    """Episode recycling in the benchmark's launch (16384 episodes x 1000 steps):
+    eight episodes spread over the CTAs against the oracle with the same option
+    (every recycled bar checked through the states' market columns, which are
+    compared exactly), and properties of every transition: a fresh portfolio
+    after every done, and the episodes do move to new bars."""
+    import torch
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_reset_heavy_bf16"]
+    N, L = w.n_episodes, w.horizon
+    inp = wl.generate(w)
+    W = wl.dqn_weights(w.seed, 0.05)
+    h = binding.DqnCollector.for_workload(w, W)
+    h.set_recycle(True)
+    out = binding.make_dqn_outputs(N, L, next_states=False)
+    h.run(torch.from_numpy(inp.features).cuda(), torch.from_numpy(inp.starts).cuda(),
+          torch.from_numpy(inp.seeds.view(np.int32)).cuda(), N, L, w.gamma, wl.DQN_EPSILON, out)
+    assert h.status() == binding.ROLLOUT_OK
+    h.close()
+    a = out["actions"]
+    assert int(a.min()) >= 0 and int(a.max()) < wl.N_ACTIONS
+    assert bool((out["td"] >= 0).all()) and bool(torch.isfinite(out["q"]).all())
+    d = out["dones"][:, :-1].bool()
+    assert bool((out["states"][:, 1:, 51][d] == 1.0).all()) and bool((out["states"][:, 1:, 52][d] == 0.0).all())
+    idx = np.array([0, 127, 128, 5000, 8191, 12345, 16255, 16383])
+    g = {k: v[idx].cpu().numpy() for k, v in out.items()}
+    sub = wl.Inputs(inp.features, inp.starts[idx], inp.seeds[idx], inp.weights)
+    ref = {}
+    st = _compare(w, sub, W, g, np.arange(idx.size), L, wl.DQN_EPSILON, recycle=True, ref_out=ref)
+    assert st["action_replays"] <= 4
+    plain = inp.starts[idx][:, None].astype(np.int64) + np.arange(L)[None, :]
+    assert (ref["bars"] != plain).any()
