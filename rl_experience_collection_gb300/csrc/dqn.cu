@@ -24,7 +24,10 @@
 //     state x', and the target network on x'; the epilogues add the curiosity
 //     bonus to the reward and form the TD error.
 // Between the phases out_td holds V entering each step and a handle-owned
-// array V' after the trade.
+// array V' after the trade.  Episode recycling (dqn_set_recycle) runs second
+// builds of the rollout and the target pass: after a done the rollout moves the
+// episode to a bar drawn from its LCG and stores every step's bar, which the
+// state rows and the target pass read instead of start + t.
 //
 // Both kernels have 16 row warps (warp w serves TMEM lanes and rows
 // 32 (w % 4) .. + 31 and the column quarter w / 4 of every 64-column chunk),
