@@ -865,7 +865,8 @@ constexpr int kRUnitsPerStep = 10;
 
 struct RBars {
     uint64_t full[kStages], empty[kStages];
-    uint64_t x;             // rows -> MMA: X of a step is written (16 warp arrivals)
+    uint64_t xm, xt;        // rows -> MMA: X of a step is written, market columns 0..47 (the
+                            // quarter 1-3 warps) and columns 48..63 (the quarter-0 warps)
     uint64_t h1[4], h2[4], h3[4];   // rows -> MMA: K-chunk c of a hidden layer is in Hb
     uint64_t hd_free;       // quarter 0-2 row warps -> MMA: the head's columns are read
     uint64_t q1, q2, q3, hd;        // MMA -> rows: that layer's MMAs are complete
@@ -882,12 +883,13 @@ constexpr int kRSmem =
 static_assert(kRSmem <= 232448, "rollout shared memory");
 static_assert(sizeof(RBars) <= 1024, "rollout barriers");
 
-// unit g of the rollout's weight stream (10 a step): its index in the image
+// unit g of the rollout's weight stream (10 a step, and one more W1 after the
+// last step's W3, unused): its index in the image
 __device__ __forceinline__ int rollout_unit(long long g)
 {
     if (g == 0) return 0;                                  // the first step's W1
-    const int pos = (int)((g - 1) % kRUnitsPerStep);       // W2 0-3, W3 0-3, head, next W1
-    return pos < 9 ? 1 + pos : 0;
+    const int pos = (int)((g - 1) % kRUnitsPerStep);       // W2 0-3, W3 0-3, next W1, head
+    return pos < 8 ? 1 + pos : (pos == 8 ? 0 : 9);
 }
 
 // kRecycle: episode recycling (after a done, the next step starts at a fresh bar
@@ -920,7 +922,8 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
-        mbar_init(&bars->x, kRRowWarps);
+        mbar_init(&bars->xm, kRRowWarps - 4);
+        mbar_init(&bars->xt, 4);
         for (int c = 0; c < 4; ++c) {
             mbar_init(&bars->h1[c], kRRowWarps);
             mbar_init(&bars->h2[c], kRRowWarps);
@@ -1012,7 +1015,7 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
             put_tail(f);
             *reinterpret_cast<uint4 *>(X + xo1) = make_uint4(0u, 0u, 0u, 0u);
         }
-        publish(&bars->x);
+        publish(q > 0 ? &bars->xm : &bars->xt);
         bool ok = true;
         for (int t = 0; t < L && ok; ++t) {
             const uint32_t par = t & 1, rs = par * 256, ro = 256 - rs;
@@ -1046,7 +1049,7 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
             // layer 1 has read X: quarters 1-3 write the next step's market columns
             if (q > 0) {
                 put16(X, xo0, xo1, f);
-                publish(&bars->x);
+                publish(&bars->xm);
             }
             // layer 2 (the other region) -> H2
             wait(&bars->q2);
@@ -1173,7 +1176,7 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
             } else {
                 put_tail(f);
             }
-            publish(&bars->x);
+            publish(&bars->xt);
             if (n < a.N) {
                 a.actions[i] = valid ? act : 0;
                 a.dones[i] = done;
@@ -1187,7 +1190,7 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
         // ------------------------------------------------------------ weight stream, stage st
         const int st = warp - kRProd0;
         if (lane == 0) {
-            const long long total = (long long)kRUnitsPerStep * L;
+            const long long total = (long long)kRUnitsPerStep * L + 1;
             long long last = -1;
             for (long long u = st; u < total; u += kStages) {
                 const int i = rollout_unit(u);
@@ -1207,14 +1210,19 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
             const uint32_t sX = smem_u32(X), sH = smem_u32(Hb), sRing = smem_u32(ring);
             long long g = 0;
             bool ok = true;
-            auto take = [&]() -> uint32_t {
-                const int st = (int)(g % kStages);
-                ok = ok && mbar_wait(&bars->full[st], (uint32_t)((g / kStages) & 1), &abort_flag);
+            // units are taken in stream order; each is released (its stage reusable
+            // once the MMAs issued so far complete) when its MMAs are issued, the
+            // next step's W1 only after the head
+            auto take_at = [&](long long gg) -> uint32_t {
+                const int st = (int)(gg % kStages);
+                ok = ok && mbar_wait(&bars->full[st], (uint32_t)((gg / kStages) & 1), &abort_flag);
                 tc_fence_after();
                 return sRing + st * kStage;
             };
+            auto release_at = [&](long long gg) { mma_commit(&bars->empty[gg % kStages]); };
+            auto take = [&]() -> uint32_t { return take_at(g); };
             auto release = [&]() {
-                mma_commit(&bars->empty[g % kStages]);
+                release_at(g);
                 ++g;
             };
             auto wait = [&](uint64_t *bar, uint32_t parity) {
@@ -1229,7 +1237,8 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
             };
             uint32_t u;
             u = take();
-            wait(&bars->x, 0);
+            wait(&bars->xm, 0);
+            wait(&bars->xt, 0);
             if (ok) {
                 chunk(0, sX, u, id256, false);
                 release();
@@ -1258,25 +1267,44 @@ __global__ void __launch_bounds__(kRThreads, 1) dqn_rollout_kernel(RolloutArgs a
                 }
                 if (!ok) break;
                 mma_commit(&bars->q3);
+                // the next step's layer 1 into the other region (H2 is out of it): its
+                // market columns (K16 steps 0-2) are in X already, written while
+                // this step's layer 1 was drained, so they go in now and only the
+                // portfolio columns wait for the environment step.  With recycling
+                // a row's market columns change after the environment step: all of
+                // layer 1 waits.
+                const bool more = t + 1 < L;
+                const long long g_w1 = g++;
+                const uint32_t uw = take_at(g_w1);
+                if (!ok) break;
+                if (!kRecycle && more) {
+                    wait(&bars->xm, par ^ 1u);
+                    if (!ok) break;
+#pragma unroll
+                    for (int k = 0; k < 3; ++k)
+                        mma<true>(tmem + ro, desc_sw128(sX + 32 * k), desc_sw128(uw + 32 * k), id256,
+                                  k > 0 ? 1u : 0u);
+                }
                 // the head into [0, 48) of region s, K-chunk by K-chunk
-                u = take();
+                const long long g_hd = g++;
+                u = take_at(g_hd);
                 for (int c = 0; c < 4 && ok; ++c) {
                     wait(&bars->h3[c], par);
                     if (!ok) break;
                     chunk(rs, sH + c * kChunk, u + c * kHeadTile, id48, c > 0);
                 }
                 if (!ok) break;
-                release();
+                release_at(g_hd);
                 mma_commit(&bars->hd);
-                // the next step's layer 1 into the other region (H2 is out of it)
-                if (t + 1 < L) {
-                    u = take();
-                    wait(&bars->x, par ^ 1u);
+                if (more) {
+                    wait(&bars->xt, par ^ 1u);
+                    if (kRecycle) wait(&bars->xm, par ^ 1u);
                     if (!ok) break;
-                    chunk(ro, sX, u, id256, false);
-                    release();
+                    if (kRecycle) chunk(ro, sX, uw, id256, false);
+                    else mma<true>(tmem + ro, desc_sw128(sX + 96), desc_sw128(uw + 96), id256, 1u);
                     mma_commit(&bars->q1);
                 }
+                release_at(g_w1);
             }
             // every MMA issued has completed before TMEM is freed
             mma_commit(&bars->fin);
