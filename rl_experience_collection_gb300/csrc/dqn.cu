@@ -855,10 +855,13 @@ __device__ __forceinline__ void drain_pair_leaky(uint32_t taddr0, uint32_t taddr
 // first maximum, quarters 1 and 2 pass theirs through shared memory, and the
 // quarter-0 warps, which hold the episodes' environment state, combine them,
 // pick the action, step the environment and write columns 48-55 (F[.., 48..50],
-// V, e, spread).  Per step the MMA lane takes its weight units in this order
-// (the producers stream them in the same order): W2 chunks 0-3, W3 chunks
-// 0-3, the head, the next step's W1 (none after the last step); the first
-// step is preceded by its W1.
+// V, e, spread).  The next step's layer 1 is issued in two parts: its three
+// K16 steps over the market columns before this step's head, its last one
+// (columns 48-63) once the quarter-0 warps have written them.  Per step the
+// MMA lane takes its weight units in this order (the producers stream them in
+// the same order): W2 chunks 0-3, W3 chunks 0-3, the next step's W1 (streamed
+// but unused after the last step), the head; the first step is preceded by
+// its W1.
 constexpr int kRRowWarps = 16;
 constexpr int kRProd0 = kRRowWarps, kRMma = kRProd0 + kStages, kRThreads = (kRMma + 1) * 32;
 constexpr int kRUnitsPerStep = 10;
