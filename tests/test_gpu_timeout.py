@@ -86,11 +86,13 @@ def test_stall_hook_rejects_the_fp32_path():
     h.close()
 
 
-def test_stalled_dqn_target_pass_times_out_and_collector_recovers():
+@pytest.mark.parametrize("recycle", [False, True])
+def test_stalled_dqn_target_pass_times_out_and_collector_recovers(recycle):
     """The DQN collector's target pass with CTA 0's first weight stage never
     filled: ROLLOUT_ERR_TIMEOUT after the bounded wait (read once: dqn_status
     clears the word), the rollout's outputs complete, the other CTAs' rewards
-    and TD errors untouched, and the next run bit-identical."""
+    and TD errors untouched, and the next run bit-identical; also with episode
+    recycling (the target pass's recycling builds)."""
     import torch
     from rl_experience_collection_gb300 import binding
     w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
@@ -99,6 +101,7 @@ def test_stalled_dqn_target_pass_times_out_and_collector_recovers():
     dev = (torch.from_numpy(inp.features).cuda(), torch.from_numpy(inp.starts[:N]).cuda(),
            torch.from_numpy(inp.seeds[:N].view(np.int32)).cuda())
     h = binding.DqnCollector.for_workload(w, wl.dqn_weights(3, 0.05), n_bars=inp.features.shape[0])
+    h.set_recycle(recycle)
 
     def run():
         out = binding.make_dqn_outputs(N, L)
