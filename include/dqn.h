@@ -75,9 +75,12 @@ ROLLOUT_API int dqn_set_weights(dqn_handle *h, const float *weights);
  * 0 <= epsilon <= 1.  Validates everything checkable on the host first
  * (ROLLOUT_ERR_INVALID).  An out-of-range start zeroes that episode's outputs
  * and records ROLLOUT_ERR_RANGE; a device-side wait that times out records
- * ROLLOUT_ERR_TIMEOUT (read with dqn_status).  The handle grows a scratch
- * array of N * L floats on the first call of a larger size (ROLLOUT_ERR_NOMEM
- * when that fails).  Returns ROLLOUT_OK, _INVALID, _NOMEM or _CUDA.
+ * ROLLOUT_ERR_TIMEOUT (read with dqn_status).  Step t of episode n reads bar
+ * starts[n] + t, or with episode recycling on (dqn_set_recycle) the bar the
+ * episode has moved to; states holds that bar's features.  The handle grows a
+ * scratch array of N * L floats on the first call of a larger size
+ * (ROLLOUT_ERR_NOMEM when that fails).  Returns ROLLOUT_OK, _INVALID, _NOMEM
+ * or _CUDA.
  */
 ROLLOUT_API int dqn_run(dqn_handle *h, const float *features, const int32_t *starts, const uint32_t *seeds, int N,
                         int L, float gamma, float epsilon, float *states, int32_t *actions, float *rewards,
