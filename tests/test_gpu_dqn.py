@@ -259,3 +259,26 @@ def test_full_size_recycling_sampled_episodes():
     assert st["action_replays"] <= 4
     plain = inp.starts[idx][:, None].astype(np.int64) + np.arange(L)[None, :]
     assert (ref["bars"] != plain).any()
+
+
+def test_recycling_at_the_smallest_feature_matrix():
+    """Episode recycling with a done on every step (a one-bar time barrier) on the
+    smallest feature matrix the horizon allows (n_bars = L + 1, every start 0): each
+    draw's range reaches the matrix's end (the last step reads its final row), and
+    the collector agrees with the oracle with the same option."""
+    import dataclasses
+    from rl_experience_collection_gb300 import binding
+    w = dataclasses.replace(wl.DQN_WORKLOADS["dqn_tiny_bf16"], max_hold=1)
+    N, L = 200, 30
+    full = wl.generate(w, n_episodes=N, horizon=L)
+    inp = wl.Inputs(np.ascontiguousarray(full.features[:L + 1]), np.zeros(N, np.int32), full.seeds[:N],
+                    full.weights)
+    W = wl.dqn_weights(17, 0.05)
+    status, g = _run(w, inp, W, N, L, 0.3, recycle=True)
+    assert status == binding.ROLLOUT_OK
+    assert (g["dones"] == 1).all()
+    ref = {}
+    _compare(w, inp, W, g, np.arange(N), L, 0.3, recycle=True, ref_out=ref)
+    bars = ref["bars"]
+    assert (bars + (L - np.arange(L))[None, :] <= L).all()      # every next bar inside the matrix
+    assert (bars[:, 1:] == np.arange(1, L)[None, :]).any()       # some draws reach the top of the range
