@@ -126,6 +126,23 @@ def test_sampler_chi_squared_through_kernel(dtype):
 
 # ------------------------------------------------------------------ edge cases and errors
 
+@pytest.mark.parametrize("name", ["reset_heavy_bf16", "scaleout_tf32", "tiny_fp32"])
+def test_episodes_at_the_end_of_the_feature_matrix(name):
+    """Episodes starting at the last valid bar (their last step's next bar is the
+    feature matrix's last row), mixed with episodes at bar 0: the rollout's row
+    gathers, the value phase's staged feature runs and the state rows all reach
+    the end of the matrix, and every episode matches the oracle."""
+    w = wl.WORKLOADS[name]
+    N, L = 130, 40
+    inp = wl.generate(w, n_episodes=N, horizon=L)
+    nb = inp.features.shape[0]
+    inp.starts[:] = nb - L - 1
+    inp.starts[::3] = 0
+    gpu = parity.gpu_run(w, inp, N, L, dump_episodes=_dump(w, N))
+    parity.compare(w, inp, gpu, np.arange(N), L)
+    parity.invariants(w, inp, gpu, L)
+
+
 def test_out_of_range_start_sets_status_and_zeroes_episode():
     import torch
     from rl_experience_collection_gb300 import binding
