@@ -282,3 +282,22 @@ def test_recycling_at_the_smallest_feature_matrix():
     bars = ref["bars"]
     assert (bars + (L - np.arange(L))[None, :] <= L).all()      # every next bar inside the matrix
     assert (bars[:, 1:] == np.arange(1, L)[None, :]).any()       # some draws reach the top of the range
+
+
+def test_episodes_at_the_end_of_the_feature_matrix():
+    """Episodes starting at the last valid bar (their last step's next bar, the
+    next state behind the TD target, is the feature matrix's last row), mixed with
+    episodes at bar 0, against the oracle: the rollout's feature fetches, the state
+    rows and the target pass's builders all reach the end of the matrix."""
+    from rl_experience_collection_gb300 import binding
+    w = wl.DQN_WORKLOADS["dqn_tiny_bf16"]
+    N, L = 300, 40
+    inp = wl.generate(w, n_episodes=N, horizon=L)
+    nb = inp.features.shape[0]
+    starts = np.full(N, nb - L - 1, np.int32)
+    starts[::3] = 0
+    sub = wl.Inputs(inp.features, starts, inp.seeds[:N], inp.weights)
+    W = wl.dqn_weights(23, 0.05)
+    status, g = _run(w, sub, W, N, L, 0.2)
+    assert status == binding.ROLLOUT_OK
+    _compare(w, sub, W, g, np.arange(N), L, 0.2)
