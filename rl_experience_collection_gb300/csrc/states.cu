@@ -9,8 +9,9 @@
 //
 // Runs after the rollout kernel and before the value phase, while out_values
 // still holds V_t, the portfolio value entering each step.  e_t is 0 at t = 0
-// and after a reset, else the exposure of a_{t-1}.  Every row of an episode
-// whose start bar is out of range is zero.
+// and after a reset, else the exposure of a_{t-1}.  bar_t is start + t, or the
+// bar the rollout stored for the step (the DQN collector's episode recycling).
+// Every row of an episode whose start bar is out of range is zero.
 //
 // Each warp owns chunks of 32 consecutive rows (6912 bytes, 54 whole 128-byte
 // lines of out_states): its lanes resolve one row's metadata each into shared
